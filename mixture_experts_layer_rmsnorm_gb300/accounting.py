@@ -1,0 +1,74 @@
+"""Byte and FLOP accounting of the fused MoE layer (host-side arithmetic only).
+
+Traffic model: an operation that reads and writes a tensor of m elements of
+s bytes moves 2*m*s bytes; fusing n such elementwise passes into one moves
+2*m*s instead of n*2*m*s ("4 · La fusion de noyaux", §4.1, fusion arithmetic).
+A GEMM of M x N x K costs 2*M*N*K floating-point operations (the same page's
+quiz on two 4096^3 GEMMs: 1.37e11 FLOP each), and a bf16 matrix of M x N
+elements occupies 2*M*N bytes (§4.2 "GEMM + épilogue": 33.5 MB for 4096^2).
+
+Per-call figures of the layer (T tokens, H hidden, I expert intermediate, E
+experts, k = top_k, n_touched = distinct experts that received a token):
+  weight bytes      n_touched * (2I*H + H*I) * 2     (W13 and W2 of touched experts)
+  router bytes      E*H*4 + H*2                      (fp32 router, bf16 norm gain)
+  token bytes       T*H*2 in + T*H*2 out
+  FLOP              2*(T*k)*(2I)*H + 2*(T*k)*H*I + 2*T*E*H   (= 6*T*k*H*I + router)
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BF16 = 2
+FP32 = 4
+
+
+def elementwise_bytes(n_ops: int, m: int, s: int, fused: bool) -> int:
+    """Bytes moved by n elementwise passes over m elements of s bytes."""
+    return 2 * m * s if fused else n_ops * 2 * m * s
+
+
+def gemm_flops(M: int, N: int, K: int) -> int:
+    return 2 * M * N * K
+
+
+def matrix_bytes(M: int, N: int, elem: int = BF16) -> int:
+    return M * N * elem
+
+
+def n_touched(topk_ids: np.ndarray, E: int) -> int:
+    return int(np.unique(np.asarray(topk_ids).reshape(-1)).size) if np.asarray(topk_ids).size else 0
+
+
+def expert_weight_bytes(H: int, I: int) -> dict:
+    """Bytes of one expert's weights: gate/up (W13) and down (W2)."""
+    return {"w13": 2 * I * H * BF16, "w2": H * I * BF16}
+
+
+def layer_bytes(T: int, H: int, I: int, E: int, k: int, touched: int) -> dict:
+    ew = expert_weight_bytes(H, I)
+    d = {
+        "weights_w13": touched * ew["w13"],
+        "weights_w2": touched * ew["w2"],
+        "router": E * H * FP32 + H * BF16,
+        "tokens": 2 * T * H * BF16,
+    }
+    d["weights"] = d["weights_w13"] + d["weights_w2"]
+    d["total"] = d["weights"] + d["router"] + d["tokens"]
+    return d
+
+
+def layer_flops(T: int, H: int, I: int, E: int, k: int) -> dict:
+    g1 = gemm_flops(T * k, 2 * I, H)
+    g2 = gemm_flops(T * k, H, I)
+    r = gemm_flops(T, E, H)
+    return {"gemm1": g1, "gemm2": g2, "router": r, "total": g1 + g2 + r}
+
+
+def gemm1_kernel_bytes(T: int, H: int, I: int, k: int, touched: int) -> int:
+    """Algorithmic bytes of the gate/up expert GEMM: touched W13, the T*k
+    gathered token rows read once, the T*k activation rows written once."""
+    return touched * 2 * I * H * BF16 + T * k * H * BF16 + T * k * I * BF16
+
+
+def gemm2_kernel_bytes(T: int, H: int, I: int, k: int, touched: int) -> int:
+    return touched * H * I * BF16 + T * k * I * BF16 + T * k * H * BF16

@@ -1,0 +1,65 @@
+"""Planted mistakes in copies of the CPU oracle must each fail at least one pin.
+
+Each mutation is a plausible slip (a dropped term, a wrong sign or index, a
+transposed operand, a wrong order) applied as a text edit to a copy of
+moe_oracle.c, compiled into a temporary library on the CPU.  The real oracle
+is never modified.
+"""
+import os
+
+import pytest
+
+import oracle
+import pins
+
+MUTATIONS = {
+    "eps_dropped": ("sqrt(ss / (double)H + eps)", "sqrt(ss / (double)H)"),
+    "mean_not_divided": ("sqrt(ss / (double)H + eps)", "sqrt(ss + eps)"),
+    "gain_dropped": ("double v = bf16_to_f64(x[j]) * rstd * bf16_to_f64(g[j]);",
+                     "double v = bf16_to_f64(x[j]) * rstd;"),
+    "gate_up_swapped": ("const uint16_t* wg = W13e + i * H;\n    const uint16_t* wu = W13e + (I + i) * H;",
+                        "const uint16_t* wg = W13e + (I + i) * H;\n    const uint16_t* wu = W13e + i * H;"),
+    "silu_sign": ("gate / (1.0 + exp(-gate))", "gate / (1.0 + exp(gate))"),
+    "w2_transposed": ("acc += a[i] * bf16_to_f64(wd[i]);", "acc += a[i] * bf16_to_f64(W2e[i * H + n]);"),
+    "bias_dropped": ("logits[e] = acc + (bias ? (double)bias[e] : 0.0);", "logits[e] = acc;"),
+    "tie_to_higher_f32": ("if (!taken[e] && (best < 0 || l[e] > l[best])) best = e;\n      taken[best] = 1;\n"
+                          "      ids[t * k + j] = (int32_t)best;\n    }\n  }\n  free(taken);\n}\n\nvoid oracle_topk_f64",
+                          "if (!taken[e] && (best < 0 || l[e] >= l[best])) best = e;\n      taken[best] = 1;\n"
+                          "      ids[t * k + j] = (int32_t)best;\n    }\n  }\n  free(taken);\n}\n\nvoid oracle_topk_f64"),
+    "renorm_ignored": ("    if (renorm)\n      for (int j = 0; j < k; ++j) w[t * k + j] /= s;", ""),
+    "softmax_not_shifted_sum": ("for (int64_t e = 0; e < E; ++e) z += exp(l[e] - m);",
+                                "for (int64_t e = 0; e < E; ++e) z += exp(l[e]);"),
+    "combine_unweighted": ("acc += w[s * k + j] * c.o[(s * k + j) * H + n];", "acc += c.o[(s * k + j) * H + n];"),
+    "butterfly_reversed": ("for (int off = 16; off >= 1; off >>= 1) {", "for (int off = 1; off <= 16; off <<= 1) {"),
+    "chunks_blocked": ("for (int64_t c = L; c * 8 < H; c += 32)",
+                       "for (int64_t c = L * ((H / 8 + 31) / 32); c < (L + 1) * ((H / 8 + 31) / 32) && c * 8 < H; c += 1)"),
+    "no_fma_in_router": ("acc = fmaf(a[j], b[j], acc);", "acc = acc + a[j] * b[j];"),
+    "align_unstable": ("  for (int64_t i = 0; i < N; ++i) {\n    int32_t e = ids[i];",
+                       "  for (int64_t i = N - 1; i >= 0; --i) {\n    int32_t e = ids[i];"),
+    "align_unpadded": ("int64_t padded = (counts[e] + pad - 1) / pad * pad;", "int64_t padded = counts[e];"),
+    "h_not_rounded_to_bf16": ("if (h) h[j] = f64_to_bf16(v);", "if (h) h[j] = f32_to_bf16((float)v);"),
+    "act_round_dropped": ("a[i] = round_act ? bf16_to_f64(f64_to_bf16(v)) : v;", "a[i] = v;"),
+}
+
+
+def _build_variant(tmp_path, name, old, new):
+    src = open(oracle._SRC).read()
+    assert old in src, f"mutation {name}: pattern not found"
+    mutated = src.replace(old, new, 1)
+    cpath = os.path.join(tmp_path, f"oracle_{name}.c")
+    with open(cpath, "w") as f:
+        f.write(mutated)
+    return oracle.Oracle(oracle.build_lib(force=True, src=cpath, out=os.path.join(tmp_path, f"lib_{name}.so")))
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name, tmp_path):
+    old, new = MUTATIONS[name]
+    o = _build_variant(str(tmp_path), name, old, new)
+    failed = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"planted mistake {name!r} passed every pin"
