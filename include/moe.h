@@ -1,0 +1,169 @@
+/*
+ * moe.h -- C ABI of the fused MoE layer forward on one GB300 (sm_103a).
+ *
+ * One call runs the whole layer on the GPU:
+ *   RMSNorm -> router GEMV + top-k softmax -> expert align (histogram,
+ *   prefix sum, padded permutation) -> gather -> gate/up grouped GEMM with a
+ *   SwiGLU epilogue -> down grouped GEMM -> top-k weighted combine.
+ *
+ * Definitions the calls implement:
+ *   RMSNorm      h_j = bf16( x_j / sqrt(mean_i x_i^2 + eps) * g_j ), fp32
+ *                accumulation -- "4 · La fusion de noyaux", §4.2
+ *                "Réduction + élémentaire"; eps inside the square root and
+ *                the cast back to the input type as in "CuTeDSL chez
+ *                Perplexity", section "Norme QK".
+ *   Router       fp32 logits l_e = sum_j h_j Wr[e,j] (+ b_e); the top_k
+ *                largest (ties to the lower expert index), weights =
+ *                softmax over all E taken at the selected experts, divided
+ *                by their sum when renormalize != 0.
+ *   Dispatch     per-expert counts, a unique slot per routed token in its
+ *                expert's list, lists copied into padded per-expert buffers
+ *                -- "CuTeDSL chez Perplexity", MoE dispatch/combine, "Local".
+ *   Experts      SwiGLU(x) = (SiLU(x W_gate) (.) (x W_up)) W_down with gate
+ *                and up in one concatenated weight -- "4 · La fusion de
+ *                noyaux", §4.2 "GEMM + GEMM"; SiLU(gate)*up is applied to
+ *                the accumulators before the only store ("GEMM + épilogue").
+ *   Combine      y_t = bf16( sum_j w_tj * o_tj ) -- "CuTeDSL chez
+ *                Perplexity", MoE dispatch/combine, "Local".
+ *
+ * Conventions for every call:
+ *   - bf16 tensors are passed as raw bfloat16 bits (moe_bf16).
+ *   - All tensor pointers are DEVICE pointers of the current CUDA device,
+ *     row-major and contiguous, 16-byte aligned; the workspace is 256-byte
+ *     aligned.  The caller owns every buffer; the library allocates no
+ *     device memory on any call.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default
+ *     stream).  Outputs are valid once the stream has reached the end of
+ *     the call.  Inputs are never modified.
+ *   - Argument and shape errors are reported synchronously, before anything
+ *     is enqueued.  A failed launch returns MOE_ERR_CUDA.  Errors found on
+ *     the device (a routing index out of range, a bounded wait that ran out)
+ *     are written to an error word at the start of the workspace and are
+ *     returned by moe_device_status().
+ *   - The library keeps no state between calls except per-device kernel
+ *     attributes set once; it is reentrant as long as concurrent calls use
+ *     different workspaces.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* raw bfloat16 bits */
+typedef uint16_t moe_bf16;
+/* a cudaStream_t */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, bad alignment, bad shape value */
+  MOE_ERR_UNSUPPORTED = 2, /* a shape outside the supported set (see moe_shape) */
+  MOE_ERR_WORKSPACE = 3,   /* workspace smaller than moe_workspace_size() */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  MOE_ERR_TIMEOUT = 5,     /* a device-side bounded wait ran out (reported by moe_device_status) */
+  MOE_ERR_DEVICE = 6       /* the device found bad data, e.g. an expert index >= E */
+} moe_status;
+
+/* Layer shape and routing options.
+ *   T            tokens (>= 0; moe_forward with T = 0 returns MOE_OK at once and
+ *                touches no pointer)
+ *   H            hidden size, a multiple of 128, <= 16384
+ *   I            expert intermediate size, a multiple of 128, <= 16384
+ *   E            experts, 1..1024
+ *   top_k        experts per token, 1..min(E, 32)
+ *   renormalize  nonzero: the top_k weights are divided by their sum
+ *   eps          RMSNorm epsilon (>= 0, finite)                              */
+typedef struct {
+  int32_t T, H, I, E, top_k;
+  int32_t renormalize;
+  float eps;
+} moe_shape;
+
+/* Bytes of device workspace moe_forward() needs for this shape.  Host only:
+ * makes no CUDA call.  Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for
+ * a bad shape. */
+MOE_API moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes);
+
+/* The layer forward.
+ *   x          [T, H]        bf16 token activations
+ *   g_norm     [H]           bf16 RMSNorm gain
+ *   w_router   [E, H]        fp32 router weight
+ *   router_bias[E]           fp32 logit bias, or NULL for none
+ *   w13        [E, 2I, H]    bf16; rows [0, I) of expert e are W_gate
+ *                            (transposed, K-major), rows [I, 2I) are W_up
+ *   w2         [E, H, I]     bf16; W_down of expert e (transposed, K-major)
+ *   y          [T, H]        bf16 output (must not alias the inputs)
+ *   workspace  device scratch of at least moe_workspace_size() bytes; its
+ *              contents on entry do not matter; it holds the intermediate
+ *              tensors (see moe_workspace_views) after the call.
+ * Ownership: all buffers belong to the caller.  Errors: as above. */
+MOE_API moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                       const float* w_router, const float* router_bias, const moe_bf16* w13,
+                       const moe_bf16* w2, moe_bf16* y, void* workspace, size_t workspace_bytes,
+                       moe_stream_t stream);
+
+/* Routing front end only (RMSNorm, router, top-k, align with `pad_rows`
+ * rows of padding granularity), with the results copied out:
+ *   topk_ids       [T, top_k] int32   selected experts, best first
+ *   topk_w         [T, top_k] fp32    their weights
+ *   expert_offsets [E + 1]    int32   start row of each expert's padded list;
+ *                                     expert_offsets[E] = total rows P
+ *   sorted_ids     [sorted_capacity] int32: rows [0, P) hold the flat index
+ *                  t*top_k + j routed there (increasing within an expert),
+ *                  padding rows hold T*top_k; entries in [P, T*top_k + E*(pad_rows-1))
+ *                  are unspecified, entries beyond that are not written.
+ * sorted_capacity must be >= T*top_k + E*(pad_rows - 1).  pad_rows: 1..256.
+ * The workspace must be sized by moe_workspace_size() for the same shape. */
+MOE_API moe_status moe_route_debug(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                           const float* w_router, const float* router_bias, int32_t pad_rows,
+                           int32_t* topk_ids, float* topk_w, int32_t* expert_offsets,
+                           int32_t* sorted_ids, int64_t sorted_capacity, void* workspace,
+                           size_t workspace_bytes, moe_stream_t stream);
+
+/* Device pointers to the intermediate tensors inside a workspace, valid for
+ * the shape it was sized for (layout only; makes no CUDA call). */
+typedef struct {
+  void* error_word;   /* int32[4]: code, kernel id, detail, detail */
+  void* h;            /* [T, H] bf16 RMSNorm output */
+  void* logits;       /* [T, E] fp32 router logits (bias included) */
+  void* topk_ids;     /* [T, top_k] int32 */
+  void* topk_w;       /* [T, top_k] fp32 */
+  void* counts;       /* [E] int32 tokens per expert */
+  void* offsets;      /* [E + 1] int32 padded row offsets (16-row padding) */
+  void* sorted_ids;   /* [P_max] int32 */
+  void* slot_of;      /* [T * top_k] int32 row of each routed token */
+  void* xg;           /* [P_max, H] bf16 gathered, padded expert inputs */
+  void* act;          /* [P_max, I] bf16 SwiGLU activations */
+  void* out_rows;     /* [P_max, H] bf16 per-row expert outputs */
+  int64_t P_max;      /* T*top_k + E*15: the most padded rows any routing can need */
+} moe_views;
+
+MOE_API moe_status moe_workspace_views(const moe_shape* shape, void* workspace, size_t workspace_bytes,
+                               moe_views* views);
+
+/* Waits for `stream`, then reads the workspace's error word: MOE_OK, or the
+ * device-side error of the last call that used this workspace
+ * (MOE_ERR_TIMEOUT / MOE_ERR_DEVICE).  detail (may be NULL) receives the
+ * four raw int32 words. */
+MOE_API moe_status moe_device_status(const void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                             int32_t* detail);
+
+/* Static text for a status code. */
+MOE_API const char* moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,186 @@
+"""Python binding of the C ABI in include/moe.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and forwards
+plain integers / device pointers; all of the layer's work runs in the CUDA
+kernels of libmoe_gb300.so.  There is no fallback: if the library cannot be
+built or loaded, :func:`load` raises.
+
+:class:`MoeLayer` is a convenience holder for torch tensors (weights and a
+workspace on the GPU) that marshals their pointers into :func:`moe_forward`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, \
+    MOE_ERR_DEVICE = range(7)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoeShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("eps", ctypes.c_float)]
+
+
+class MoeViews(ctypes.Structure):
+    _fields_ = [("error_word", ctypes.c_void_p), ("h", ctypes.c_void_p), ("logits", ctypes.c_void_p),
+                ("topk_ids", ctypes.c_void_p), ("topk_w", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("sorted_ids", ctypes.c_void_p), ("slot_of", ctypes.c_void_p),
+                ("xg", ctypes.c_void_p), ("act", ctypes.c_void_p), ("out_rows", ctypes.c_void_p),
+                ("P_max", ctypes.c_int64)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {moe_status_string(status)} (status {status})")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build: bool = True):
+    """Load libmoe_gb300.so (compiling it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build else _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"CUDA library {path} is missing; run __graft_entry__.build()")
+            lib = ctypes.CDLL(path)
+            p, sz, i32, i64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int64
+            sp = ctypes.POINTER(MoeShape)
+            lib.moe_workspace_size.argtypes = [sp, ctypes.POINTER(sz)]
+            lib.moe_forward.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p]
+            lib.moe_route_debug.argtypes = [sp, p, p, p, p, i32, p, p, p, p, i64, p, sz, p]
+            lib.moe_workspace_views.argtypes = [sp, p, sz, ctypes.POINTER(MoeViews)]
+            lib.moe_device_status.argtypes = [p, sz, p, ctypes.POINTER(ctypes.c_int32)]
+            lib.moe_status_string.argtypes = [ctypes.c_int]
+            lib.moe_status_string.restype = ctypes.c_char_p
+            for f in ("moe_workspace_size", "moe_forward", "moe_route_debug", "moe_workspace_views",
+                      "moe_device_status"):
+                getattr(lib, f).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def shape(T, H, I, E, top_k, renormalize=True, eps=1e-6) -> MoeShape:
+    return MoeShape(int(T), int(H), int(I), int(E), int(top_k), int(bool(renormalize)), float(eps))
+
+
+def moe_status_string(status: int) -> str:
+    return load().moe_status_string(int(status)).decode()
+
+
+def moe_workspace_size(s: MoeShape) -> tuple[int, int]:
+    n = ctypes.c_size_t(0)
+    st = load().moe_workspace_size(ctypes.byref(s), ctypes.byref(n))
+    return st, n.value
+
+
+def moe_forward(s: MoeShape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes,
+                stream) -> int:
+    return load().moe_forward(ctypes.byref(s), x, g_norm, w_router, router_bias, w13, w2, y, workspace,
+                              workspace_bytes, stream)
+
+
+def moe_route_debug(s: MoeShape, x, g_norm, w_router, router_bias, pad_rows, topk_ids, topk_w, expert_offsets,
+                    sorted_ids, sorted_capacity, workspace, workspace_bytes, stream) -> int:
+    return load().moe_route_debug(ctypes.byref(s), x, g_norm, w_router, router_bias, pad_rows, topk_ids, topk_w,
+                                  expert_offsets, sorted_ids, sorted_capacity, workspace, workspace_bytes, stream)
+
+
+def moe_workspace_views(s: MoeShape, workspace, workspace_bytes) -> tuple[int, MoeViews]:
+    v = MoeViews()
+    st = load().moe_workspace_views(ctypes.byref(s), workspace, workspace_bytes, ctypes.byref(v))
+    return st, v
+
+
+def moe_device_status(workspace, workspace_bytes, stream) -> tuple[int, list]:
+    d = (ctypes.c_int32 * 4)()
+    st = load().moe_device_status(workspace, workspace_bytes, stream, d)
+    return st, list(d)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+class MoeLayer:
+    """One MoE layer's weights on the GPU plus a workspace sized for up to
+    ``max_tokens`` tokens.  Inputs and outputs are torch tensors on the same
+    device; bf16 tensors may be torch.bfloat16 or raw int16 bit patterns."""
+
+    def __init__(self, g_norm, w_router, w13, w2, top_k, renormalize=True, eps=1e-6, router_bias=None,
+                 max_tokens=1):
+        import torch
+        self.g_norm, self.w_router, self.w13, self.w2, self.bias = g_norm, w_router, w13, w2, router_bias
+        self.E, two_i, self.H = w13.shape
+        self.I = two_i // 2
+        self.top_k, self.renormalize, self.eps = int(top_k), bool(renormalize), float(eps)
+        self.device = w13.device
+        self.max_tokens = 0
+        self.workspace = None
+        self.ensure_capacity(max_tokens)
+        self._torch = torch
+
+    def shape(self, T) -> MoeShape:
+        return shape(T, self.H, self.I, self.E, self.top_k, self.renormalize, self.eps)
+
+    def ensure_capacity(self, T):
+        import torch
+        if T <= self.max_tokens and self.workspace is not None:
+            return
+        st, n = moe_workspace_size(self.shape(max(T, 1)))
+        if st != MOE_OK:
+            raise MoeError(st, "moe_workspace_size")
+        self.workspace = torch.empty(n, dtype=torch.uint8, device=self.device)
+        self.max_tokens = max(T, 1)
+
+    def workspace_bytes(self, T) -> int:
+        st, n = moe_workspace_size(self.shape(T))
+        if st != MOE_OK:
+            raise MoeError(st, "moe_workspace_size")
+        return n
+
+    def forward(self, x, y=None, stream=None):
+        import torch
+        T = x.shape[0]
+        self.ensure_capacity(T)
+        if y is None:
+            y = torch.empty((T, self.H), dtype=x.dtype, device=x.device)
+        s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
+        st = moe_forward(self.shape(T), _ptr(x), _ptr(self.g_norm), _ptr(self.w_router), _ptr(self.bias),
+                         _ptr(self.w13), _ptr(self.w2), _ptr(y), _ptr(self.workspace), self.workspace_bytes(T), s)
+        if st != MOE_OK:
+            raise MoeError(st, "moe_forward")
+        return y
+
+    def views(self, T):
+        st, v = moe_workspace_views(self.shape(T), _ptr(self.workspace), self.workspace_bytes(T))
+        if st != MOE_OK:
+            raise MoeError(st, "moe_workspace_views")
+        return v
+
+    def view_tensor(self, T, name, dtype, shape_):
+        """A torch view of one intermediate tensor inside the workspace."""
+        import torch
+        v = self.views(T)
+        off = getattr(v, name) - self.workspace.data_ptr()
+        n = 1
+        for d in shape_:
+            n *= d
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return self.workspace[off:off + nbytes].view(dtype).view(*shape_)
+
+    def device_status(self, T, stream=None):
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        return moe_device_status(_ptr(self.workspace), self.workspace_bytes(T), s)

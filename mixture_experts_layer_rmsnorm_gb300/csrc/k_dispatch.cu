@@ -1,0 +1,253 @@
+// k_dispatch.cu -- K2 expert align, K3 gather into padded per-expert rows,
+// K6 top-k weighted combine.
+//
+// Dispatch and combine follow "CuTeDSL chez Perplexity", MoE dispatch /
+// combine, "Local": count the tokens routed to each expert, give each routed
+// token a unique index in its expert's list, copy the tokens into optionally
+// padded per-expert buffers for the MoE GEMM, and after the GEMMs accumulate
+// each token's expert outputs in registers with its routing weights.
+//
+// The pages hand out list slots with atomic counters, which makes the order
+// inside a list depend on timing.  Here slots follow the flat routing index
+// t*k + j in increasing order, found with warp match/popc ranks and a
+// per-warp prefix in shared memory, so the permutation is the same on every
+// run.
+#include <cuda_bf16.h>
+
+#include "moe_kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr int kAlignThreads = 1024;
+constexpr int kAlignWarps = kAlignThreads / 32;
+
+// Block-wide exclusive scan of one int per thread (1024 threads).  `tmp` is
+// kAlignWarps ints of shared memory.  Returns the exclusive prefix; *total
+// receives the block total.
+__device__ int block_exclusive_scan(int v, int* tmp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(kFull, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) tmp[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = tmp[lane];
+    int winc = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFull, winc, off);
+      if (lane >= off) winc += o;
+    }
+    tmp[lane] = winc - w;  // exclusive prefix of warp totals
+    if (lane == 31) tmp[kAlignWarps] = winc;
+  }
+  __syncthreads();
+  const int r = tmp[warp] + inc - v;
+  *total = tmp[kAlignWarps];
+  __syncthreads();
+  return r;
+}
+
+// One CTA of 1024 threads.  Dynamic shared memory: cnt[E], cursor[E],
+// wbase[32][E] (ints).
+__global__ void __launch_bounds__(kAlignThreads)
+    align_kernel(const int32_t* __restrict__ ids, int N, int E, int pad, int bn1, int tiles1, int bn2, int tiles2,
+                 int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
+                 int32_t* __restrict__ slot_of, int32_t* __restrict__ unit_off1, int32_t* __restrict__ unit_off2,
+                 int32_t* __restrict__ err) {
+  extern __shared__ int sm[];
+  int* cnt = sm;                 // [E]
+  int* cursor = sm + E;          // [E]
+  int* wbase = sm + 2 * E;       // [32][E]
+  __shared__ int scan_tmp[kAlignWarps + 1];
+  __shared__ int bad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  if (tid == 0) bad = 0;
+  for (int e = tid; e < E; e += kAlignThreads) cnt[e] = 0;
+  __syncthreads();
+  for (int i = tid; i < N; i += kAlignThreads) {
+    const int e = ids[i];
+    if (e < 0 || e >= E)
+      bad = 1;
+    else
+      atomicAdd(&cnt[e], 1);
+  }
+  __syncthreads();
+  if (bad) {
+    if (tid == 0) {
+      err[1] = kKernAlign;
+      err[0] = kErrDevice;
+    }
+    // leave an empty, consistent routing behind: no rows, no units
+    for (int e = tid; e <= E; e += kAlignThreads) {
+      offsets[e] = 0;
+      if (unit_off1) unit_off1[e] = 0;
+      if (unit_off2) unit_off2[e] = 0;
+      if (e < E) counts[e] = 0;
+    }
+    return;
+  }
+
+  // padded sizes, offsets and work-unit prefix sums (E <= 1024: one pass)
+  {
+    const int e = tid;
+    const int c = (e < E) ? cnt[e] : 0;
+    const int p = (c + pad - 1) / pad * pad;
+    const int u1 = (bn1 > 0) ? (p + bn1 - 1) / bn1 * tiles1 : 0;
+    const int u2 = (bn2 > 0) ? (p + bn2 - 1) / bn2 * tiles2 : 0;
+    int tot_p, tot_u1, tot_u2;
+    const int off = block_exclusive_scan(p, scan_tmp, &tot_p);
+    const int o1 = block_exclusive_scan(u1, scan_tmp, &tot_u1);
+    const int o2 = block_exclusive_scan(u2, scan_tmp, &tot_u2);
+    if (e < E) {
+      counts[e] = c;
+      offsets[e] = off;
+      cursor[e] = off;
+      if (unit_off1) unit_off1[e] = o1;
+      if (unit_off2) unit_off2[e] = o2;
+      // padding rows of this expert's list
+      for (int q = off + c; q < off + p; ++q) sorted_ids[q] = N;
+    }
+    if (tid == 0) {
+      offsets[E] = tot_p;
+      if (unit_off1) unit_off1[E] = tot_u1;
+      if (unit_off2) unit_off2[E] = tot_u2;
+    }
+  }
+  __syncthreads();
+
+  // stable ranks, 1024 routing entries per round
+  for (int base = 0; base < N; base += kAlignThreads) {
+    const int i = base + tid;
+    const bool valid = i < N;
+    const int e = valid ? ids[i] : -1;
+    const unsigned same = __match_any_sync(kFull, e);
+    const int rank = __popc(same & ((1u << lane) - 1u));
+    for (int q = tid; q < kAlignWarps * E; q += kAlignThreads) wbase[q] = 0;
+    __syncthreads();
+    if (valid && rank == 0) wbase[warp * E + e] = __popc(same);
+    __syncthreads();
+    for (int ex = tid; ex < E; ex += kAlignThreads) {
+      int run = cursor[ex];
+      for (int w = 0; w < kAlignWarps; ++w) {
+        const int c = wbase[w * E + ex];
+        wbase[w * E + ex] = run;
+        run += c;
+      }
+      cursor[ex] = run;
+    }
+    __syncthreads();
+    if (valid) {
+      const int pos = wbase[warp * E + e] + rank;
+      sorted_ids[pos] = i;
+      slot_of[i] = pos;
+    }
+    __syncthreads();
+  }
+}
+
+// One warp per padded row; 8 rows per block of 256 threads.
+__global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ h, const int32_t* __restrict__ sorted_ids,
+                                                     const int32_t* __restrict__ offsets, int E, int N, int k, int H,
+                                                     int64_t P_max, uint16_t* __restrict__ xg) {
+  const int64_t p = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (p >= P_max || p >= offsets[E]) return;
+  const int src = sorted_ids[p];
+  const int nch = H >> 3;
+  uint4* dst = reinterpret_cast<uint4*>(xg + p * H);
+  if (src >= N || src < 0) {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int c = lane; c < nch; c += 32) dst[c] = z;
+  } else {
+    const uint4* s = reinterpret_cast<const uint4*>(h + static_cast<int64_t>(src / k) * H);
+    for (int c = lane; c < nch; c += 32) dst[c] = __ldg(s + c);
+  }
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t hh = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return l | (hh << 16);
+}
+
+// One block per token; each thread owns 8 consecutive outputs (128-bit loads
+// and stores) and accumulates over the k routed rows in order j = 0..k-1.
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ rows, const int32_t* __restrict__ slot_of,
+                                                      const float* __restrict__ w, int T, int H, int k,
+                                                      uint16_t* __restrict__ y) {
+  const int t = blockIdx.x;
+  const int nch = H >> 3;
+  for (int c = threadIdx.x; c < nch; c += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const int slot = slot_of[static_cast<int64_t>(t) * k + j];
+      const float wj = w[static_cast<int64_t>(t) * k + j];
+      float f[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(slot) * H) + c), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+    }
+    uint4 o;
+    o.x = pack2_bf16(acc[0], acc[1]);
+    o.y = pack2_bf16(acc[2], acc[3]);
+    o.z = pack2_bf16(acc[4], acc[5]);
+    o.w = pack2_bf16(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(y + static_cast<int64_t>(t) * H)[c] = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_align(const int32_t* topk_ids, int N, int E, int pad, int bn1, int tiles1, int bn2, int tiles2,
+                         int32_t* counts, int32_t* offsets, int32_t* sorted_ids, int32_t* slot_of,
+                         int32_t* unit_off1, int32_t* unit_off2, int32_t* err, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(2 + kAlignWarps) * E * sizeof(int);
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  align_kernel<<<1, kAlignThreads, smem, stream>>>(topk_ids, N, E, pad, bn1, tiles1, bn2, tiles2, counts, offsets,
+                                                   sorted_ids, slot_of, unit_off1, unit_off2, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets, int E, int N, int k,
+                          int H, int64_t P_max, uint16_t* xg, cudaStream_t stream) {
+  const int64_t blocks = (P_max + 7) / 8;
+  if (blocks == 0) return cudaSuccess;
+  gather_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(h, sorted_ids, offsets, E, N, k, H, P_max, xg);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const uint16_t* out_rows, const int32_t* slot_of, const float* topk_w, int T, int H, int k,
+                           uint16_t* y, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const int threads = (H / 8 >= 256) ? 256 : ((H / 8 + 31) / 32 * 32);
+  combine_kernel<<<T, threads, 0, stream>>>(out_rows, slot_of, topk_w, T, H, k, y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

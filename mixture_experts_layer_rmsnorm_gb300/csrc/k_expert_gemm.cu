@@ -1,0 +1,323 @@
+// k_expert_gemm.cu -- K4 gate/up grouped GEMM with the SwiGLU epilogue and K5
+// down grouped GEMM, on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// Mapping.  For every expert e the layer computes C[n_e, F] = X_e[n_e, K] W_e^T
+// with X_e the e-th list of gathered token rows and W_e [F, K] the expert's
+// weight.  The MMA's M dimension is fixed at 128 rows, while an expert often
+// holds only a handful of tokens in decode.  So the weights take the M side:
+// each work unit computes C^T tile = W_e[128 rows, K] * X_e[n tok, K]^T, the
+// transposition trick of the fused-MoE article ("Swap-AB para la utilización
+// de WGMMA", Fig. 1), re-done for tcgen05 (M = 128, N = tokens in
+// multiples of 16 up to 256).  The same mapping serves prefill: a unit then
+// covers 128 weight rows x up to 128 / 256 tokens.
+//
+// Gate/up: W13[e] holds W_gate^T in rows [0, I) and W_up^T in rows [I, 2I) (the
+// concatenated (d x 2 d_ff) weight of "4 · La fusion de noyaux", §4.2
+// "GEMM + GEMM").  A unit loads the gate rows [i0, i0+128) and the matching up
+// rows [I+i0, I+i0+128) and issues two MMAs per K step into two TMEM column
+// ranges, so TMEM lane l holds gate and up of feature i0+l for every token:
+// the epilogue applies SiLU(gate) * up to the accumulators before the only
+// store ("GEMM + épilogue", §4.2).
+//
+// Roles in a CTA of 192 threads (persistent, one CTA per SM):
+//   warp 0 lane 0   TMA producer: weight tiles [128 x 64] and token tiles
+//                   [16 x 64] per box, 128-byte swizzle, into a STAGES-deep ring
+//   warp 1          owns the TMEM allocation; lane 0 issues tcgen05.mma and
+//                   tcgen05.commit (frees a ring slot / hands an accumulator
+//                   buffer to the epilogue)
+//   warps 2..5      epilogue: tcgen05.ld of their TMEM lane quarter, SwiGLU or
+//                   plain bf16 convert, global stores
+// Two accumulator buffers in TMEM let the epilogue of one unit overlap the
+// MMAs of the next.  Every wait is bounded; a wait that runs out sets the
+// workspace error word and the kernel winds down.
+#include <cuda_bf16.h>
+
+#include "moe_kernels.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace ptx;
+
+constexpr int kGemmThreads = 192;
+constexpr int kABytes = kWeightBoxRows * kBlockK * 2;  // 16 KB weight tile per stage
+constexpr int kTokRowBytes = kBlockK * 2;              // 128 B per token row per stage
+
+template <bool SWIGLU, int BN, int STAGES>
+struct GemmCfg {
+  static constexpr int NA = SWIGLU ? 2 : 1;
+  static constexpr int kBBytes = BN * kTokRowBytes;
+  static constexpr int kStageBytes = NA * kABytes + kBBytes;
+  static constexpr int kAccCols = SWIGLU ? 2 * BN : BN;  // fp32 TMEM columns per accumulator buffer
+  static constexpr int kTmemNeed = 2 * kAccCols;
+  static constexpr uint32_t kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
+                                        : kTmemNeed <= 256 ? 256 : 512;
+  static constexpr int kBarBytes = 256;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes;
+  static_assert(BN % kTokBoxRows == 0 && BN >= 16 && BN <= 256, "token tile");
+  static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+  static_assert(kTmemNeed <= 512, "TMEM has 512 columns");
+  static_assert((2 * STAGES + 5) * 8 + 8 <= kBarBytes, "barrier area");
+};
+
+struct Unit {
+  int e, tile, tok0, n;
+};
+
+// Work unit u -> expert (binary search in the unit prefix sums), token chunk
+// and weight tile (tile index fastest, so CTAs running side by side share a
+// token chunk and walk the expert's weight tiles).
+__device__ __forceinline__ Unit decode_unit(int u, const int32_t* __restrict__ unit_off,
+                                            const int32_t* __restrict__ offsets, int E, int tiles, int bn) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(unit_off + mid) <= u)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  Unit r;
+  r.e = lo;
+  const int local = u - __ldg(unit_off + lo);
+  const int chunk = local / tiles;
+  r.tile = local - chunk * tiles;
+  r.tok0 = __ldg(offsets + lo) + chunk * bn;
+  r.n = min(bn, __ldg(offsets + lo + 1) - r.tok0);
+  return r;
+}
+
+__device__ __forceinline__ void raise_timeout(int32_t* err, volatile int* abort_flag, int kern) {
+  *abort_flag = 1;
+  if (atomicCAS(err, 0, kErrTimeout) == 0) atomicExch(err + 1, kern);
+}
+
+__device__ __forceinline__ uint16_t f2bf(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+template <bool SWIGLU, int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                       const ExpertGemmArgs args) {
+  using C = GemmCfg<SWIGLU, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kern = SWIGLU ? kKernGemm1 : kKernGemm2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total_units = __ldg(args.unit_off + args.E);
+  const int kblocks = args.K / kBlockK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      prefetch_tensormap(&tm_w);
+      prefetch_tensormap(&tm_x);
+      const uint64_t pol_w = policy_evict_first();  // weight tiles: streamed, each read by few CTAs
+      const uint64_t pol_x = policy_evict_last();   // token tiles: re-read by every weight tile
+      int stage = 0;
+      uint32_t phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
+        const int wrow = un.e * args.w_rows_per_expert + un.tile * kWeightBoxRows;
+        const uint32_t bytes = C::NA * kABytes + un.n * kTokRowBytes;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitTimeoutNs, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * C::kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d(sa, &tm_w, &full[stage], kb * kBlockK, wrow, pol_w);
+          if (SWIGLU) tma_load_2d(sa + kABytes, &tm_w, &full[stage], kb * kBlockK, wrow + args.up_offset, pol_w);
+          uint8_t* sb = sa + C::NA * kABytes;
+          for (int r = 0; r < un.n; r += kTokBoxRows)
+            tma_load_2d(sb + r * kTokRowBytes, &tm_x, &full[stage], kb * kBlockK, un.tok0 + r, pol_x);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) raise_timeout(args.err, abort_flag, kern);
+      // every load this thread issued must have landed before the CTA exits
+      for (int s = 0; s < STAGES; ++s) {
+        if (issued <= s) break;
+        const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+        int dummy = 0;
+        mbar_wait(&full[s], par, kWaitTimeoutNs, &dummy);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, kWaitTimeoutNs, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(un.n));
+        const uint32_t d_gate = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, kWaitTimeoutNs, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
+          const uint32_t sb = sa + C::NA * kABytes;
+#pragma unroll
+          for (int k = 0; k < kBlockK / 16; ++k) {
+            const uint64_t bdesc = sdesc_kmajor_sw128(sb + k * 32);
+            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+            mma_bf16_ss(d_gate, sdesc_kmajor_sw128(sa + k * 32), bdesc, idesc, accum);
+            if (SWIGLU) mma_bf16_ss(d_gate + BN, sdesc_kmajor_sw128(sa + kABytes + k * 32), bdesc, idesc, accum);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) raise_timeout(args.err, abort_flag, kern);
+      // all MMAs this thread issued have finished before TMEM is released
+      mma_commit(done);
+      int dummy = 0;
+      mbar_wait(done, 0, kWaitTimeoutNs, &dummy);
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+      const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
+      // warp-uniform outcome: tcgen05.ld below must be executed by all 32 lanes
+      const bool got = mbar_wait(&tfull[acc], acc_phase, kWaitTimeoutNs, abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, got)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int feat = un.tile * kWeightBoxRows + q * 32 + lane;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * C::kAccCols);
+      uint16_t* out = args.out + static_cast<int64_t>(un.tok0) * args.n_out + feat;
+      for (int c0 = 0; c0 < un.n; c0 += 16) {
+        uint32_t ra[16], rb[16];
+        tmem_ld_32x32b_x16(t_row + c0, ra);
+        if (SWIGLU) tmem_ld_32x32b_x16(t_row + BN + c0, rb);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float v = __uint_as_float(ra[j]);
+          if (SWIGLU) {
+            const float up = __uint_as_float(rb[j]);
+            v = v / (1.0f + __expf(-v)) * up;
+          }
+          out[static_cast<int64_t>(c0 + j) * args.n_out] = f2bf(v);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok && lane == 0) raise_timeout(args.err, abort_flag, kern);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <bool SWIGLU, int BN, int STAGES>
+cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, int num_sms,
+                               cudaStream_t stream) {
+  using C = GemmCfg<SWIGLU, BN, STAGES>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(expert_gemm_kernel<SWIGLU, BN, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  expert_gemm_kernel<SWIGLU, BN, STAGES><<<num_sms, kGemmThreads, C::kSmemBytes, stream>>>(tw, tx, a);
+  return cudaGetLastError();
+}
+
+constexpr int kGateUpBnDecode = 64, kGateUpStagesDecode = 5;
+constexpr int kGateUpBnPrefill = 128, kGateUpStagesPrefill = 4;
+constexpr int kDownBnDecode = 64, kDownStagesDecode = 8;
+constexpr int kDownBnPrefill = 256, kDownStagesPrefill = 4;
+
+}  // namespace
+
+int gemm_gate_up_bn(GemmPlan plan) { return plan == GemmPlan::kDecode ? kGateUpBnDecode : kGateUpBnPrefill; }
+int gemm_down_bn(GemmPlan plan) { return plan == GemmPlan::kDecode ? kDownBnDecode : kDownBnPrefill; }
+
+cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
+                                GemmPlan plan, int num_sms, cudaStream_t stream) {
+  if (plan == GemmPlan::kDecode)
+    return launch_expert_gemm<true, kGateUpBnDecode, kGateUpStagesDecode>(tm_w13, tm_x, a, num_sms, stream);
+  return launch_expert_gemm<true, kGateUpBnPrefill, kGateUpStagesPrefill>(tm_w13, tm_x, a, num_sms, stream);
+}
+
+cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const ExpertGemmArgs& a,
+                             GemmPlan plan, int num_sms, cudaStream_t stream) {
+  if (plan == GemmPlan::kDecode)
+    return launch_expert_gemm<false, kDownBnDecode, kDownStagesDecode>(tm_w2, tm_act, a, num_sms, stream);
+  return launch_expert_gemm<false, kDownBnPrefill, kDownStagesPrefill>(tm_w2, tm_act, a, num_sms, stream);
+}
+
+}  // namespace moe

@@ -1,0 +1,253 @@
+// k_route.cu -- K1: fused RMSNorm + router logits; K1b: top-k + softmax weights.
+//
+// RMSNorm ("4 · La fusion de noyaux", §4.2 "Réduction + élémentaire"; "CuTeDSL
+// chez Perplexity", "Norme QK"): one warp per token row, 128-bit loads of 8
+// bf16 per lane, fp32 sum of squares reduced by an xor butterfly of warp
+// shuffles, h = bf16((x * rstd) * g) with rstd = 1/sqrt(mean + eps).
+//
+// Router: l_e = sum_j h_j Wr[e,j] (+ b_e) in fp32.  Every dot product (and
+// the sum of squares) is taken in one fixed order so that the routing
+// decision is reproducible bit for bit:
+//   chunk c = elements [8c, 8c+8) belongs to lane c mod 32; a lane runs over
+//   its chunks in increasing c, one fused multiply-add per element in
+//   increasing index, from +0; the 32 lane sums are combined by
+//   v += shfl_xor(v, off) for off = 16, 8, 4, 2, 1.
+// All roundings are explicit (__fmaf_rn, __fadd_rn, __fmul_rn, __fdiv_rn,
+// __fsqrt_rn), so the compiler cannot contract or reorder them.
+#include <cuda_bf16.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "moe_kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteWarps = 8;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return l | (h << 16);
+}
+
+__device__ __forceinline__ float warp_butterfly_sum(float v) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, off));
+  return v;
+}
+
+// grid = (ceil(T / TT), ceil(E / experts_per_cta)), block = 256, dyn smem = TT*H*2.
+// Each warp computes TE experts x TT tokens at a time.
+template <int TT, int TE>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+    norm_router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g,
+                       const float* __restrict__ w_router, const float* __restrict__ bias, int T, int H, int E,
+                       float eps, int experts_per_cta, uint16_t* __restrict__ h_out, float* __restrict__ logits,
+                       int32_t* __restrict__ err) {
+  extern __shared__ uint4 h_s[];  // [TT][H/8]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nch = H >> 3;
+  const int t0 = blockIdx.x * TT;
+  const int e0 = blockIdx.y * experts_per_cta;
+
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 4) err[threadIdx.x] = 0;
+
+  // ---- RMSNorm: one warp per token
+  for (int tt = warp; tt < TT; tt += kRouteWarps) {
+    const int t = t0 + tt;
+    if (t >= T) break;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
+    float ss = 0.0f;
+    for (int c = lane; c < nch; c += 32) {
+      float f[8];
+      unpack8(__ldg(xr + c), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = __fmaf_rn(f[i], f[i], ss);
+    }
+    ss = warp_butterfly_sum(ss);
+    const float ms = __fdiv_rn(ss, static_cast<float>(H));
+    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+    const uint4* gr = reinterpret_cast<const uint4*>(g);
+    uint4* hrow = reinterpret_cast<uint4*>(h_out + static_cast<size_t>(t) * H);
+    for (int c = lane; c < nch; c += 32) {
+      float f[8], gg[8];
+      unpack8(__ldg(xr + c), f);
+      unpack8(__ldg(gr + c), gg);
+      uint4 o;
+      o.x = pack2_bf16(__fmul_rn(__fmul_rn(f[0], rstd), gg[0]), __fmul_rn(__fmul_rn(f[1], rstd), gg[1]));
+      o.y = pack2_bf16(__fmul_rn(__fmul_rn(f[2], rstd), gg[2]), __fmul_rn(__fmul_rn(f[3], rstd), gg[3]));
+      o.z = pack2_bf16(__fmul_rn(__fmul_rn(f[4], rstd), gg[4]), __fmul_rn(__fmul_rn(f[5], rstd), gg[5]));
+      o.w = pack2_bf16(__fmul_rn(__fmul_rn(f[6], rstd), gg[6]), __fmul_rn(__fmul_rn(f[7], rstd), gg[7]));
+      h_s[tt * nch + c] = o;
+      if (blockIdx.y == 0) hrow[c] = o;
+    }
+  }
+  __syncthreads();
+
+  // ---- logits: warp w takes expert groups e0 + (w + 8 r) * TE .. + TE
+  const int e_end = min(E, e0 + experts_per_cta);
+  const int ntok = min(TT, T - t0);
+  for (int eg = e0 + warp * TE; eg < e_end; eg += kRouteWarps * TE) {
+    float acc[TT][TE];
+#pragma unroll
+    for (int a = 0; a < TT; ++a)
+#pragma unroll
+      for (int b = 0; b < TE; ++b) acc[a][b] = 0.0f;
+    const float4* wrow[TE];
+#pragma unroll
+    for (int b = 0; b < TE; ++b) {
+      const int e = min(eg + b, E - 1);  // clamp: a tail expert's duplicate is computed but not stored
+      wrow[b] = reinterpret_cast<const float4*>(w_router + static_cast<size_t>(e) * H);
+    }
+    for (int c = lane; c < nch; c += 32) {
+      float w[TE][8];
+#pragma unroll
+      for (int b = 0; b < TE; ++b) {
+        const float4 p = __ldg(wrow[b] + 2 * c), q = __ldg(wrow[b] + 2 * c + 1);
+        w[b][0] = p.x; w[b][1] = p.y; w[b][2] = p.z; w[b][3] = p.w;
+        w[b][4] = q.x; w[b][5] = q.y; w[b][6] = q.z; w[b][7] = q.w;
+      }
+#pragma unroll
+      for (int a = 0; a < TT; ++a) {
+        float hv[8];
+        unpack8(h_s[a * nch + c], hv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int b = 0; b < TE; ++b) acc[a][b] = __fmaf_rn(hv[i], w[b][i], acc[a][b]);
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < TT; ++a)
+#pragma unroll
+      for (int b = 0; b < TE; ++b) {
+        float v = warp_butterfly_sum(acc[a][b]);
+        const int e = eg + b;
+        if (lane == 0 && a < ntok && e < e_end) {
+          if (bias) v = __fadd_rn(v, bias[e]);
+          logits[static_cast<size_t>(t0 + a) * E + e] = v;
+        }
+      }
+  }
+}
+
+// one warp per token; block = 256 (8 tokens).  E <= 1024, k <= 32.
+__global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                           int renorm, int32_t* __restrict__ topk_ids,
+                                                           float* __restrict__ topk_w) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* l = logits + static_cast<size_t>(t) * E;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? l[e] : -FLT_MAX;
+  }
+  uint32_t taken = 0;
+  float my_v = 0.0f;  // lane j keeps the j-th selection
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
+        bv = v[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      const float ov = __shfl_xor_sync(kFull, bv, off);
+      const int oe = __shfl_xor_sync(kFull, be, off);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) {
+      my_v = bv;
+      my_e = be;
+    }
+  }
+  const float m = __shfl_sync(kFull, my_v, 0);  // the largest logit
+  float denom;
+  if (renorm) {
+    float s = (lane < k) ? expf(my_v - m) : 0.0f;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+    denom = s;
+  } else {
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (lane + 32 * i < E) s += expf(v[i] - m);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
+    denom = s;
+  }
+  if (lane < k) {
+    topk_ids[static_cast<size_t>(t) * k + lane] = my_e;
+    topk_w[static_cast<size_t>(t) * k + lane] = expf(my_v - m) / denom;
+  }
+}
+
+template <int TT, int TE>
+cudaError_t launch_nr(const uint16_t* x, const uint16_t* g, const float* wr, const float* bias, int T, int H, int E,
+                      float eps, uint16_t* h, float* logits, int32_t* err, int num_sms, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(TT) * H * 2;
+  static int configured_device = -1;  // attribute is per device; re-set when the device changes
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(norm_router_kernel<TT, TE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         200 * 1024);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int tiles = (T + TT - 1) / TT;
+  const int group = kRouteWarps * TE;
+  // few token tiles: one expert group per CTA to spread the router weights over
+  // many SMs; many token tiles: all experts per CTA so Wr is read once per tile
+  int epc = group;
+  if (static_cast<long long>(tiles) * ((E + group - 1) / group) > 4LL * num_sms) epc = (E + group - 1) / group * group;
+  dim3 grid(tiles, (E + epc - 1) / epc);
+  norm_router_kernel<TT, TE><<<grid, kRouteWarps * 32, smem, stream>>>(x, g, wr, bias, T, H, E, eps, epc, h,
+                                                                        logits, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_norm_router(const uint16_t* x, const uint16_t* g, const float* w_router, const float* bias,
+                               int T, int H, int E, float eps, uint16_t* h, float* logits, int32_t* err,
+                               int num_sms, cudaStream_t stream) {
+  if (T <= 3) return launch_nr<1, 1>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
+  if (T <= 64 || H > 8192)
+    return launch_nr<4, 2>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
+  return launch_nr<8, 4>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
+}
+
+cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int renorm, int32_t* topk_ids,
+                                float* topk_w, cudaStream_t stream) {
+  topk_softmax_kernel<<<(T + 7) / 8, 256, 0, stream>>>(logits, T, E, k, renorm, topk_ids, topk_w);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

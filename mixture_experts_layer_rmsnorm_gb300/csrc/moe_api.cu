@@ -1,0 +1,311 @@
+// moe_api.cu -- the C ABI declared in include/moe.h: argument checks, the
+// workspace layout, TMA tensor maps, the decode / prefill plan and the launch
+// sequence K1 -> K1b -> K2 -> K3 -> K4 -> K5 -> K6 on the caller's stream.
+//
+// Plan ("CuTeDSL chez Perplexity", "Pré-remplir et décoder la
+// spécialisation": kernels are split into prefill and decode variants by
+// token count, hidden size and dtype).  The expected tokens per expert
+// T*top_k/E decides: <= 64 takes the decode tiles (64 tokens per unit, deep
+// weight pipelines), above it the prefill tiles (128 / 256 tokens per unit).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "moe_kernels.cuh"
+
+namespace {
+
+using moe::GemmPlan;
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxDebugPad = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Layout {
+  size_t err, h, logits, ids, w, counts, offsets, unit1, unit2, sorted, slot, xg, act, out, total;
+  int64_t P_max;       // padded rows with 16-row padding
+  int64_t sorted_cap;  // sorted_ids entries (room for debug padding up to 256)
+};
+
+Layout make_layout(const moe_shape& s) {
+  Layout L{};
+  const int64_t T = s.T, H = s.H, I = s.I, E = s.E, k = s.top_k;
+  L.P_max = T * k + E * (moe::kPadRows - 1);
+  L.sorted_cap = T * k + E * (kMaxDebugPad - 1);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t r = off;
+    off = align_up(off + bytes, kAlign);
+    return r;
+  };
+  L.err = take(64);
+  L.h = take(static_cast<size_t>(T * H * 2));
+  L.logits = take(static_cast<size_t>(T * E * 4));
+  L.ids = take(static_cast<size_t>(T * k * 4));
+  L.w = take(static_cast<size_t>(T * k * 4));
+  L.counts = take(static_cast<size_t>(E * 4));
+  L.offsets = take(static_cast<size_t>((E + 1) * 4));
+  L.unit1 = take(static_cast<size_t>((E + 1) * 4));
+  L.unit2 = take(static_cast<size_t>((E + 1) * 4));
+  L.sorted = take(static_cast<size_t>(L.sorted_cap * 4));
+  L.slot = take(static_cast<size_t>(T * k * 4));
+  L.xg = take(static_cast<size_t>(L.P_max * H * 2));
+  L.act = take(static_cast<size_t>(L.P_max * I * 2));
+  L.out = take(static_cast<size_t>(L.P_max * H * 2));
+  L.total = off;
+  return L;
+}
+
+moe_status check_shape(const moe_shape* s) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (s->T < 0 || s->H <= 0 || s->I <= 0 || s->E <= 0 || s->top_k <= 0 || s->top_k > s->E)
+    return MOE_ERR_INVALID_ARG;
+  if (!(s->eps >= 0.0f) || !std::isfinite(s->eps)) return MOE_ERR_INVALID_ARG;
+  if (s->H % 128 != 0 || s->I % 128 != 0 || s->H > 16384 || s->I > 16384 || s->E > 1024 || s->top_k > 32)
+    return MOE_ERR_UNSUPPORTED;
+  // 32-bit row indices inside the kernels
+  const int64_t rows = static_cast<int64_t>(s->T) * s->top_k + static_cast<int64_t>(s->E) * (kMaxDebugPad - 1);
+  if (rows >= (int64_t(1) << 30)) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(s->E) * 2 * s->I >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 row-major [rows, inner] tensor, boxes of 64 x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(moe::kBlockK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms_of_current_device() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+moe_status check_inputs(const moe_shape* s, const void* x, const void* g, const float* wr, const float* bias,
+                        void* ws, size_t ws_bytes) {
+  if (!x || !g || !wr || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(g, 16) || !aligned(wr, 16) || (bias && !aligned(bias, 4)) || !aligned(ws, kAlign))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < make_layout(*s).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+// K1 + K1b + K2 with the given padding; unit tables only when bn1/bn2 > 0.
+moe_status run_front(const moe_shape& s, const Layout& L, const moe_bf16* x, const moe_bf16* g, const float* wr,
+                     const float* bias, int pad, int bn1, int bn2, void* ws, cudaStream_t st, int num_sms) {
+  int32_t* err = at<int32_t>(ws, L.err);
+  if (moe::launch_norm_router(x, g, wr, bias, s.T, s.H, s.E, s.eps, at<uint16_t>(ws, L.h), at<float>(ws, L.logits),
+                              err, num_sms, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (moe::launch_topk_softmax(at<float>(ws, L.logits), s.T, s.E, s.top_k, s.renormalize, at<int32_t>(ws, L.ids),
+                               at<float>(ws, L.w), st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (moe::launch_align(at<int32_t>(ws, L.ids), s.T * s.top_k, s.E, pad, bn1, s.I / moe::kWeightBoxRows, bn2,
+                        s.H / moe::kWeightBoxRows, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+                        at<int32_t>(ws, L.sorted), at<int32_t>(ws, L.slot), bn1 > 0 ? at<int32_t>(ws, L.unit1) : nullptr,
+                        bn2 > 0 ? at<int32_t>(ws, L.unit2) : nullptr, err, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes) {
+  const moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(*shape).total;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_views(const moe_shape* shape, void* workspace, size_t workspace_bytes, moe_views* v) {
+  const moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!workspace || !v) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*shape);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  v->error_word = at<void>(workspace, L.err);
+  v->h = at<void>(workspace, L.h);
+  v->logits = at<void>(workspace, L.logits);
+  v->topk_ids = at<void>(workspace, L.ids);
+  v->topk_w = at<void>(workspace, L.w);
+  v->counts = at<void>(workspace, L.counts);
+  v->offsets = at<void>(workspace, L.offsets);
+  v->sorted_ids = at<void>(workspace, L.sorted);
+  v->slot_of = at<void>(workspace, L.slot);
+  v->xg = at<void>(workspace, L.xg);
+  v->act = at<void>(workspace, L.act);
+  v->out_rows = at<void>(workspace, L.out);
+  v->P_max = L.P_max;
+  return MOE_OK;
+}
+
+moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
+                       const float* router_bias, const moe_bf16* w13, const moe_bf16* w2, moe_bf16* y,
+                       void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  const moe_shape& s = *shape;
+  if (s.T == 0) return MOE_OK;  // nothing to compute; no pointer is touched
+  st = check_inputs(shape, x, g_norm, w_router, router_bias, workspace, workspace_bytes);
+  if (st != MOE_OK) return st;
+  if (!w13 || !w2 || !y || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int num_sms = num_sms_of_current_device();
+  if (num_sms <= 0) return MOE_ERR_CUDA;
+  const Layout L = make_layout(s);
+  const GemmPlan plan = (static_cast<int64_t>(s.T) * s.top_k <= 64LL * s.E) ? GemmPlan::kDecode : GemmPlan::kPrefill;
+  const int bn1 = moe::gemm_gate_up_bn(plan), bn2 = moe::gemm_down_bn(plan);
+
+  CUtensorMap tm_w13, tm_xg, tm_w2, tm_act;
+  if (!make_map(&tm_w13, w13, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, moe::kWeightBoxRows) ||
+      !make_map(&tm_xg, at<void>(workspace, L.xg), s.H, L.P_max, moe::kTokBoxRows) ||
+      !make_map(&tm_w2, w2, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows) ||
+      !make_map(&tm_act, at<void>(workspace, L.act), s.I, L.P_max, moe::kTokBoxRows))
+    return MOE_ERR_CUDA;
+
+  st = run_front(s, L, x, g_norm, w_router, router_bias, moe::kPadRows, bn1, bn2, workspace, cs, num_sms);
+  if (st != MOE_OK) return st;
+  const int N = s.T * s.top_k;
+  int32_t* err = at<int32_t>(workspace, L.err);
+  if (moe::launch_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
+                         at<int32_t>(workspace, L.offsets), s.E, N, s.top_k, s.H, L.P_max,
+                         at<uint16_t>(workspace, L.xg), cs) != cudaSuccess)
+    return MOE_ERR_CUDA;
+
+  moe::ExpertGemmArgs a1{};
+  a1.offsets = at<int32_t>(workspace, L.offsets);
+  a1.unit_off = at<int32_t>(workspace, L.unit1);
+  a1.E = s.E;
+  a1.K = s.H;
+  a1.tiles_per_expert = s.I / moe::kWeightBoxRows;
+  a1.w_rows_per_expert = 2 * s.I;
+  a1.up_offset = s.I;
+  a1.n_out = s.I;
+  a1.out = at<uint16_t>(workspace, L.act);
+  a1.err = err;
+  if (moe::launch_gemm_gate_up(tm_w13, tm_xg, a1, plan, num_sms, cs) != cudaSuccess) return MOE_ERR_CUDA;
+
+  moe::ExpertGemmArgs a2{};
+  a2.offsets = at<int32_t>(workspace, L.offsets);
+  a2.unit_off = at<int32_t>(workspace, L.unit2);
+  a2.E = s.E;
+  a2.K = s.I;
+  a2.tiles_per_expert = s.H / moe::kWeightBoxRows;
+  a2.w_rows_per_expert = s.H;
+  a2.up_offset = 0;
+  a2.n_out = s.H;
+  a2.out = at<uint16_t>(workspace, L.out);
+  a2.err = err;
+  if (moe::launch_gemm_down(tm_w2, tm_act, a2, plan, num_sms, cs) != cudaSuccess) return MOE_ERR_CUDA;
+
+  if (moe::launch_combine(at<uint16_t>(workspace, L.out), at<int32_t>(workspace, L.slot), at<float>(workspace, L.w),
+                          s.T, s.H, s.top_k, y, cs) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_route_debug(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
+                           const float* router_bias, int32_t pad_rows, int32_t* topk_ids, float* topk_w,
+                           int32_t* expert_offsets, int32_t* sorted_ids, int64_t sorted_capacity, void* workspace,
+                           size_t workspace_bytes, moe_stream_t stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  st = check_inputs(shape, x, g_norm, w_router, router_bias, workspace, workspace_bytes);
+  if (st != MOE_OK) return st;
+  if (pad_rows < 1 || pad_rows > kMaxDebugPad) return MOE_ERR_INVALID_ARG;
+  if (!topk_ids || !topk_w || !expert_offsets || !sorted_ids) return MOE_ERR_INVALID_ARG;
+  const moe_shape& s = *shape;
+  const int64_t need = static_cast<int64_t>(s.T) * s.top_k + static_cast<int64_t>(s.E) * (pad_rows - 1);
+  if (sorted_capacity < need) return MOE_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const Layout L = make_layout(s);
+  if (s.T == 0) {
+    // an empty routing: every list is empty
+    if (cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (s.E + 1), cs) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  const int num_sms = num_sms_of_current_device();
+  if (num_sms <= 0) return MOE_ERR_CUDA;
+  st = run_front(s, L, x, g_norm, w_router, router_bias, pad_rows, 0, 0, workspace, cs, num_sms);
+  if (st != MOE_OK) return st;
+  const size_t tk = static_cast<size_t>(s.T) * s.top_k;
+  if (cudaMemcpyAsync(topk_ids, at<void>(workspace, L.ids), tk * 4, cudaMemcpyDeviceToDevice, cs) != cudaSuccess ||
+      cudaMemcpyAsync(topk_w, at<void>(workspace, L.w), tk * 4, cudaMemcpyDeviceToDevice, cs) != cudaSuccess ||
+      cudaMemcpyAsync(expert_offsets, at<void>(workspace, L.offsets), (s.E + 1) * 4, cudaMemcpyDeviceToDevice, cs) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(sorted_ids, at<void>(workspace, L.sorted), static_cast<size_t>(need) * 4,
+                      cudaMemcpyDeviceToDevice, cs) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_device_status(const void* workspace, size_t workspace_bytes, moe_stream_t stream, int32_t* detail) {
+  if (!workspace || workspace_bytes < 64) return MOE_ERR_INVALID_ARG;
+  int32_t w[4] = {0, 0, 0, 0};
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(w, workspace, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (detail) std::memcpy(detail, w, sizeof(w));
+  if (w[0] == moe::kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (w[0] == moe::kErrDevice) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, misaligned pointer or bad shape value)";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape (H, I multiples of 128 up to 16384; E <= 1024; top_k <= 32)";
+    case MOE_ERR_WORKSPACE: return "workspace smaller than moe_workspace_size()";
+    case MOE_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case MOE_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+    case MOE_ERR_DEVICE: return "the device found invalid data (expert index out of range)";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

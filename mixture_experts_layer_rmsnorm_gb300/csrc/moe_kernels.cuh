@@ -1,0 +1,74 @@
+// moe_kernels.cuh -- launchers of the layer's kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace moe {
+
+// error word codes (match moe_status) and kernel ids written with them
+enum : int32_t { kErrTimeout = 5, kErrDevice = 6 };
+enum : int32_t { kKernNormRouter = 1, kKernTopk = 2, kKernAlign = 3, kKernGather = 4, kKernGemm1 = 5,
+                 kKernGemm2 = 6, kKernCombine = 7 };
+
+// rows of padding granularity of each expert's list in the expert GEMMs
+constexpr int kPadRows = 16;
+// bounded device waits give up after this long
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+// K1: RMSNorm of every token + fp32 router logits (canonical summation order).
+// Writes h[T,H] bf16 and logits[T,E] fp32; clears the error word.
+cudaError_t launch_norm_router(const uint16_t* x, const uint16_t* g, const float* w_router, const float* bias,
+                               int T, int H, int E, float eps, uint16_t* h, float* logits, int32_t* err,
+                               int num_sms, cudaStream_t stream);
+
+// K1b: top-k + softmax weights per token from the logits.
+cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int renorm, int32_t* topk_ids,
+                                float* topk_w, cudaStream_t stream);
+
+// K2: deterministic align: counts, padded offsets, sorted_ids, slot_of and the
+// prefix sums of work units of the two expert GEMMs (units per expert =
+// ceil(P_e / bn) * tiles; bn = 0 skips that table).
+cudaError_t launch_align(const int32_t* topk_ids, int N, int E, int pad, int bn1, int tiles1, int bn2, int tiles2,
+                         int32_t* counts, int32_t* offsets, int32_t* sorted_ids, int32_t* slot_of,
+                         int32_t* unit_off1, int32_t* unit_off2, int32_t* err, cudaStream_t stream);
+
+// K3: xg[p,:] = h[sorted_ids[p] / k, :] for real rows, zeros for padding rows.
+cudaError_t launch_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets, int E, int N,
+                          int k, int H, int64_t P_max, uint16_t* xg, cudaStream_t stream);
+
+// K4 / K5: grouped expert GEMMs on tcgen05.  Weights are the MMA's A operand
+// (128 weight rows per tile), the tokens of one expert its B operand.
+struct ExpertGemmArgs {
+  const int32_t* offsets;   // [E+1] padded row offsets
+  const int32_t* unit_off;  // [E+1] prefix sums of work units
+  int E;
+  int K;                    // reduction length
+  int tiles_per_expert;     // output features / 128
+  int w_rows_per_expert;    // 2I (gate/up) or H (down)
+  int up_offset;            // I for gate/up, unused for down
+  int n_out;                // output row length (I or H)
+  uint16_t* out;            // [P_max, n_out] bf16
+  int32_t* err;
+};
+
+enum class GemmPlan { kDecode, kPrefill };
+
+// Encodes nothing itself: the tensor maps are built by the caller.
+cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
+                                GemmPlan plan, int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const ExpertGemmArgs& a,
+                             GemmPlan plan, int num_sms, cudaStream_t stream);
+// token rows per unit (B-operand width) and rows per TMA box of the token tile
+int gemm_gate_up_bn(GemmPlan plan);
+int gemm_down_bn(GemmPlan plan);
+constexpr int kTokBoxRows = 16;
+constexpr int kWeightBoxRows = 128;
+constexpr int kBlockK = 64;
+
+// K6: y[t,:] = bf16(sum_j topk_w[t,j] * out_rows[slot_of[t*k+j], :]).
+cudaError_t launch_combine(const uint16_t* out_rows, const int32_t* slot_of, const float* topk_w, int T, int H,
+                           int k, uint16_t* y, cudaStream_t stream);
+
+}  // namespace moe

@@ -74,20 +74,35 @@ typedef struct {
   int kind; /* 0 = bf16, 1 = f32, 2 = raw uint64 */
 } gen_job;
 
+static void store_value(gen_job* j, uint64_t i, double z) {
+  float f = (float)(j->mean + j->std * z);
+  if (j->kind == 0)
+    ((uint16_t*)j->out)[i] = float_to_bf16_bits(f);
+  else
+    ((float*)j->out)[i] = f;
+}
+
 static void* gen_worker(void* arg) {
   gen_job* j = (gen_job*)arg;
-  for (uint64_t i = j->lo; i < j->hi; ++i) {
-    if (j->kind == 2) {
-      ((uint64_t*)j->out)[i] = mix64(j->base + (i + 1) * 0x9E3779B97F4A7C15ULL);
-      continue;
-    }
-    double v = j->mean + j->std * normal_at(j->base, i);
-    float f = (float)v;
-    if (j->kind == 0)
-      ((uint16_t*)j->out)[i] = float_to_bf16_bits(f);
-    else
-      ((float*)j->out)[i] = f;
+  uint64_t i = j->lo;
+  if (j->kind == 2) {
+    for (; i < j->hi; ++i) ((uint64_t*)j->out)[i] = mix64(j->base + (i + 1) * 0x9E3779B97F4A7C15ULL);
+    return NULL;
   }
+  if (i < j->hi && (i & 1)) { /* odd start: second half of a pair */
+    store_value(j, i, normal_at(j->base, i));
+    ++i;
+  }
+  for (; i + 1 < j->hi; i += 2) { /* whole pairs: one log/sqrt for both values */
+    uint64_t p = i >> 1;
+    double u1 = uniform01(j->base, 2 * p);
+    double u2 = uniform01(j->base, 2 * p + 1);
+    double rad = sqrt(-2.0 * log(u1));
+    double th = 2.0 * GEN_PI * u2;
+    store_value(j, i, rad * cos(th));
+    store_value(j, i + 1, rad * sin(th));
+  }
+  if (i < j->hi) store_value(j, i, normal_at(j->base, i));
   return NULL;
 }
 

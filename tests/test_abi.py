@@ -1,0 +1,104 @@
+"""The C-ABI library loads on a host without a GPU, exports every entry point
+include/moe.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_layer_rmsnorm_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_entry_points():
+    txt = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", txt)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = binding.load()
+    names = declared_entry_points()
+    assert {"moe_forward", "moe_workspace_size", "moe_route_debug", "moe_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/moe.h but not exported"
+
+
+def test_status_strings():
+    for code in range(7):
+        assert binding.moe_status_string(code)
+    assert "unknown" in binding.moe_status_string(99)
+
+
+def test_workspace_size_and_shape_checks():
+    st, n = binding.moe_workspace_size(binding.shape(4096, 4096, 4096, 64, 8))
+    assert st == binding.MOE_OK and n > 3 * 33728 * 4096 * 2
+    bad = [
+        (binding.shape(4, 100, 256, 8, 2), binding.MOE_ERR_UNSUPPORTED),   # H not a multiple of 128
+        (binding.shape(4, 128, 200, 8, 2), binding.MOE_ERR_UNSUPPORTED),   # I not a multiple of 128
+        (binding.shape(4, 128, 256, 8, 9), binding.MOE_ERR_INVALID_ARG),   # top_k > E
+        (binding.shape(4, 128, 256, 2048, 2), binding.MOE_ERR_UNSUPPORTED),  # E > 1024
+        (binding.shape(4, 128, 256, 64, 33), binding.MOE_ERR_UNSUPPORTED),  # top_k > 32
+        (binding.shape(-1, 128, 256, 8, 2), binding.MOE_ERR_INVALID_ARG),
+        (binding.shape(4, 128, 256, 8, 2, eps=-1.0), binding.MOE_ERR_INVALID_ARG),
+        (binding.shape(4, 128, 256, 8, 2, eps=float("nan")), binding.MOE_ERR_INVALID_ARG),
+    ]
+    for s, want in bad:
+        st, _ = binding.moe_workspace_size(s)
+        assert st == want, (s.H, s.I, s.E, s.top_k, st)
+
+
+def test_forward_rejects_bad_arguments_without_a_gpu():
+    # fake, aligned, never-dereferenced addresses: every case fails validation first
+    s = binding.shape(4, 128, 256, 8, 2)
+    _, need = binding.moe_workspace_size(s)
+    A = 1 << 20
+    args = dict(x=A, g=A, wr=A, b=None, w13=A, w2=A, y=A, ws=A, nbytes=need)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return binding.moe_forward(s, a["x"], a["g"], a["wr"], a["b"], a["w13"], a["w2"], a["y"], a["ws"],
+                                   a["nbytes"], None)
+
+    assert call(nbytes=need - 1) == binding.MOE_ERR_WORKSPACE
+    assert call(x=None) == binding.MOE_ERR_INVALID_ARG
+    assert call(w13=None) == binding.MOE_ERR_INVALID_ARG
+    assert call(y=None) == binding.MOE_ERR_INVALID_ARG
+    assert call(x=A + 2) == binding.MOE_ERR_INVALID_ARG       # not 16-byte aligned
+    assert call(ws=A + 16) == binding.MOE_ERR_INVALID_ARG     # workspace not 256-byte aligned
+    assert binding.moe_forward(binding.shape(4, 100, 256, 8, 2), A, A, A, None, A, A, A, A, need, None) == \
+        binding.MOE_ERR_UNSUPPORTED
+    # T = 0 is a no-op that touches no pointer
+    assert binding.moe_forward(binding.shape(0, 128, 256, 8, 2), None, None, None, None, None, None, None, None, 0,
+                               None) == binding.MOE_OK
+
+
+def test_route_debug_rejects_bad_arguments_without_a_gpu():
+    s = binding.shape(4, 128, 256, 8, 2)
+    _, need = binding.moe_workspace_size(s)
+    A = 1 << 20
+    cap = 4 * 2 + 8 * 15
+    assert binding.moe_route_debug(s, A, A, A, None, 0, A, A, A, A, cap, A, need, None) == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_route_debug(s, A, A, A, None, 257, A, A, A, A, 10**6, A, need, None) == \
+        binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_route_debug(s, A, A, A, None, 16, A, A, A, A, cap - 1, A, need, None) == \
+        binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_route_debug(s, A, A, A, None, 16, None, A, A, A, cap, A, need, None) == \
+        binding.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_views_layout():
+    T, H, I, E, k = 100, 256, 384, 16, 4
+    s = binding.shape(T, H, I, E, k)
+    _, need = binding.moe_workspace_size(s)
+    base = 1 << 30
+    st, v = binding.moe_workspace_views(s, base, need)
+    assert st == binding.MOE_OK
+    assert v.P_max == T * k + E * 15
+    ptrs = [v.error_word, v.h, v.logits, v.topk_ids, v.topk_w, v.counts, v.offsets, v.sorted_ids, v.slot_of, v.xg,
+            v.act, v.out_rows]
+    assert ptrs == sorted(ptrs) and all(p % 256 == 0 for p in ptrs)
+    assert v.out_rows + v.P_max * H * 2 <= base + need
+    assert v.act + v.P_max * I * 2 <= v.out_rows
+    st, _ = binding.moe_workspace_views(s, base, need - 1)
+    assert st == binding.MOE_ERR_WORKSPACE

@@ -1,0 +1,113 @@
+"""GPU parity on small workloads the oracle computes completely.
+
+Each case runs the whole layer through the C ABI and compares it with the CPU
+oracle on the same seeded inputs: h, router logits, expert ids and the align
+outputs bit for bit; routing weights within fp32 rounding; the per-row expert
+intermediates and the layer output within the tolerance of the fp64 oracle.
+The shapes span several weight tiles, several token chunks per expert, ragged
+tails, both launch plans (decode tiles and prefill tiles) and the degenerate
+cases (T = 0, T = 1, E = 1, k = E, unnormalised weights, a router bias).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as gu
+import oracle
+from mixture_experts_layer_rmsnorm_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # name, T, H, I, E, k, renorm, zipf, seed
+    ("tiny", 4, 128, 256, 8, 2, True, None, 0),
+    ("T1", 1, 256, 256, 16, 4, True, None, 3),
+    ("ragged_decode", 37, 256, 384, 16, 4, True, None, 1),
+    ("deep_k", 64, 1024, 512, 8, 2, True, None, 2),
+    ("prefill_chunks", 1024, 256, 256, 4, 2, True, None, 4),
+    ("prefill_ragged_norenorm", 300, 384, 128, 6, 3, False, None, 5),
+    ("skewed_bias", 96, 256, 256, 32, 6, True, 1.2, 7),
+    ("single_expert", 20, 128, 128, 1, 1, True, None, 6),
+    ("k_equals_E", 9, 128, 256, 4, 4, True, None, 8),
+]
+
+
+@pytest.fixture(scope="module")
+def o():
+    return oracle.default()
+
+
+def _layer_inputs(T, H, I, E, k, renorm, zipf, seed):
+    cfg = inputs.LayerConfig(T=T, H=H, I=I, E=E, top_k=k, renormalize=renorm, seed=seed, zipf_bias=zipf)
+    return inputs.make_layer_inputs(cfg)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_layer_parity(case, o):
+    _, T, H, I, E, k, renorm, zipf, seed = case
+    li = _layer_inputs(T, H, I, E, k, renorm, zipf, seed)
+    dl = gu.DeviceLayer(li)
+    g = dl.run(li.x)
+    ids = gu.check_routing(o, li, li.x, g)
+    # expert intermediates of a few real rows: SwiGLU activations and expert outputs
+    real = np.nonzero(g["sorted"] < T * k)[0]
+    rows = real[np.linspace(0, real.size - 1, min(6, real.size)).astype(np.int64)]
+    act, out = dl.act_rows(T, rows)
+    for r_i, p in enumerate(rows):
+        flat = int(g["sorted"][p])
+        t, j = divmod(flat, k)
+        e = int(ids[t, j])
+        a_ref, o_ref = o.expert_f64(g["h"][t], li.w13[e], li.w2[e], round_act=True)
+        ea = np.linalg.norm(gu.widen(act[r_i]) - a_ref) / np.linalg.norm(a_ref)
+        eo = np.linalg.norm(gu.widen(out[r_i]) - o_ref) / np.linalg.norm(o_ref)
+        assert ea < 1e-2, f"SwiGLU activation row {p}: rel err {ea:.3e}"
+        assert eo < 1e-2, f"expert output row {p}: rel err {eo:.3e}"
+    gu.check_output(o, li, li.x, g["y"])
+
+
+def test_zero_tokens_is_a_noop():
+    li = _layer_inputs(4, 128, 128, 4, 2, True, None, 0)
+    dl = gu.DeviceLayer(li)
+    L = dl.layer
+    x = torch.empty((0, 128), dtype=torch.int16, device="cuda")
+    y = torch.empty((0, 128), dtype=torch.int16, device="cuda")
+    st = binding.moe_forward(L.shape(0), x.data_ptr(), L.g_norm.data_ptr(), L.w_router.data_ptr(), None,
+                             L.w13.data_ptr(), L.w2.data_ptr(), y.data_ptr(), L.workspace.data_ptr(),
+                             L.workspace.numel(), torch.cuda.current_stream().cuda_stream)
+    assert st == binding.MOE_OK
+
+
+def test_repeat_calls_are_identical(o):
+    # same inputs, same bits: the permutation and the accumulation order are fixed
+    li = _layer_inputs(50, 256, 256, 8, 2, True, None, 11)
+    dl = gu.DeviceLayer(li)
+    a = dl.run(li.x)
+    b = dl.run(li.x)
+    for key in ("y", "h", "logits", "ids", "w", "offsets", "sorted", "slot"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_route_debug_entry_point(o):
+    li = _layer_inputs(33, 256, 256, 16, 4, True, None, 12)
+    dl = gu.DeviceLayer(li)
+    L = dl.layer
+    T, E, k = 33, 16, 4
+    for pad in (1, 16, 128):
+        cap = T * k + E * (pad - 1)
+        ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+        srt = torch.full((cap,), -7, dtype=torch.int32, device="cuda")
+        xd = gu.dev_bf16(li.x)
+        st = binding.moe_route_debug(L.shape(T), xd.data_ptr(), L.g_norm.data_ptr(), L.w_router.data_ptr(), None,
+                                     pad, ids.data_ptr(), w.data_ptr(), offs.data_ptr(), srt.data_ptr(), cap,
+                                     L.workspace.data_ptr(), L.workspace.numel(),
+                                     torch.cuda.current_stream().cuda_stream)
+        assert st == binding.MOE_OK
+        torch.cuda.synchronize()
+        _, l32, _ = o.route_f32(li.x, li.g, li.cfg.eps, li.w_router, None)
+        ids_ref = o.topk(l32, k)
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+        counts, offsets, sorted_ids, _ = o.align(ids_ref, E, pad)
+        assert np.array_equal(offs.cpu().numpy(), offsets)
+        assert np.array_equal(srt.cpu().numpy()[:offsets[-1]], sorted_ids)
