@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused MoE layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One JSON line on stdout (rank 0).  Workloads (synthetic, seeded, the shapes
+and distributions of the layer's configurations):
+  decode       (default) H = I = 4096, E = 64, top_k = 8; one step = one layer
+               call at each of T = 1, 8, 32, 64 tokens (the thin-M sweep)
+  prefill      same layer, T = 4096
+  finegrained  H = 7168, I = 2048, E = 256, top_k = 8; T = 16, 128, 1024
+  skewed       H = 4096, I = 1408, E = 128, top_k = 6, T = 512, Zipf(1.2) router bias
+  tiny         T = 4, H = 128, I = 256, E = 8, top_k = 2
+The L2 cache is flushed (a 256 MB write) before every layer call; the flush
+is outside the timed intervals, which are CUDA events on the launch stream
+around each call (and around each of its kernels).
+
+--impl reference times the CPU oracle (the reference of this build) on the
+host cores on a bounded sample of the same workload.
+
+N > 1 (torchrun): every rank runs an independent replica of the workload on
+its own GPU; the only cross-rank traffic is the host-side barrier and the max
+of the timings.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused-MoE layer µs & tokens/s; % HBM roofline (decode), % bf16 TC peak (prefill)"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+WORKLOADS = {
+    "decode": dict(H=4096, I=4096, E=64, k=8, Ts=[1, 8, 32, 64], seed=0, zipf=None,
+                   label="decode sweep T in {1,8,32,64}, H=I=4096, E=64, top_k=8, bf16"),
+    "prefill": dict(H=4096, I=4096, E=64, k=8, Ts=[4096], seed=0, zipf=None,
+                    label="prefill T=4096, H=I=4096, E=64, top_k=8, bf16"),
+    "finegrained": dict(H=7168, I=2048, E=256, k=8, Ts=[16, 128, 1024], seed=0, zipf=None,
+                        label="fine-grained T in {16,128,1024}, H=7168, I=2048, E=256, top_k=8, bf16"),
+    "skewed": dict(H=4096, I=1408, E=128, k=6, Ts=[512], seed=7, zipf=1.2,
+                   label="skewed routing T=512, H=4096, I=1408, E=128, top_k=6, Zipf(1.2) bias, bf16"),
+    "tiny": dict(H=128, I=256, E=8, k=2, Ts=[4], seed=0, zipf=None,
+                 label="tiny T=4, H=128, I=256, E=8, top_k=2, bf16"),
+}
+KERNEL_SOURCES = {  # files whose content the ncu traffic figure of a kernel depends on
+    "gemm_gate_up_swiglu": ["k_expert_gemm.cu", "tc_ptx.cuh", "moe_kernels.cuh", "moe_api.cu"],
+    "gemm_down": ["k_expert_gemm.cu", "tc_ptx.cuh", "moe_kernels.cuh", "moe_api.cu"],
+}
+
+
+# ----------------------------------------------------------------- host logic
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha(name: str) -> str:
+    h = hashlib.sha256()
+    for fn in KERNEL_SOURCES.get(name, []):
+        with open(os.path.join(ROOT, "mixture_experts_layer_rmsnorm_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic_per_launch(name: str, workload: str):
+    """DRAM bytes per launch of `name` from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(name)
+    if not e or e.get("source_sha") != kernel_source_sha(name):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def roofline(bound, algorithmic, seconds, peak, traffic):
+    """achieved = algorithmic bytes (or FLOPs) per launch / average launch time."""
+    if bound == "hbm":
+        achieved = algorithmic / seconds / 1e9
+        unit = "GB/s"
+    else:
+        achieved = algorithmic / seconds / 1e12
+        unit = "TFLOP/s"
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": traffic}
+
+
+def parse_clock_samples(lines):
+    """nvidia-smi CSV rows (noheader, nounits) -> clocks summary for the JSON line."""
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[5:9]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        return parse_clock_samples(self.lines)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a host scalar over ranks (gloo); identity on one rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- workloads
+
+def make_host_inputs(wl):
+    from mixture_experts_layer_rmsnorm_gb300 import inputs
+    cfg0 = inputs.LayerConfig(T=wl["Ts"][0], H=wl["H"], I=wl["I"], E=wl["E"], top_k=wl["k"], seed=wl["seed"],
+                              zipf_bias=wl["zipf"])
+    g, wr, bias, w13, w2 = inputs.make_weights(cfg0)
+    xs = {}
+    for T in wl["Ts"]:
+        cfg = inputs.LayerConfig(T=T, H=wl["H"], I=wl["I"], E=wl["E"], top_k=wl["k"], seed=wl["seed"],
+                                 zipf_bias=wl["zipf"])
+        xs[T] = inputs.make_tokens(cfg)
+    return dict(g=g, wr=wr, bias=bias, w13=w13, w2=w2, xs=xs)
+
+
+def cpu_oracle_rate(wl, host, n_tokens, steps=1):
+    """Tokens/s of the CPU oracle (as it stands) over `steps` runs of a bounded
+    sample of n_tokens tokens spread over the workload's batches."""
+    import numpy as np
+    import oracle
+    Ts = wl["Ts"]
+    per = max(1, n_tokens // len(Ts))
+    total_tok, total_s = 0, 0.0
+    for _ in range(steps):
+        for T in Ts:
+            sample = np.unique(np.linspace(0, T - 1, min(T, per)).astype(np.int64))
+            t0 = time.perf_counter()
+            oracle.moe_forward(host["xs"][T], host["g"], host["wr"], host["bias"], host["w13"], host["w2"], wl["k"],
+                               True, 1e-6, sample=sample)
+            total_s += time.perf_counter() - t0
+            total_tok += sample.size
+    return total_tok / total_s, total_tok, total_s, oracle.threads()
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args, wl, world, rank, local):
+    import numpy as np
+    import torch
+    from mixture_experts_layer_rmsnorm_gb300 import accounting, binding
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    t_setup = time.time()
+    host = make_host_inputs(wl)
+
+    def d16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+    layer = binding.MoeLayer(d16(host["g"]), torch.from_numpy(host["wr"]).to(dev), d16(host["w13"]),
+                             d16(host["w2"]), wl["k"], True, 1e-6,
+                             router_bias=None if host["bias"] is None else torch.from_numpy(host["bias"]).to(dev),
+                             max_tokens=max(wl["Ts"]))
+    Ts = wl["Ts"]
+    H = wl["H"]
+    xs = {T: d16(host["xs"][T]) for T in Ts}
+    ys = {T: torch.empty((T, H), dtype=torch.int16, device=dev) for T in Ts}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nk = binding.MOE_NUM_KERNELS
+
+    def new_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+        for e in evs:
+            e.record(stream)  # creates the CUDA event behind the torch object
+        return evs
+
+    ev_sets = {T: [new_events() for _ in range(args.steps)] for T in Ts}
+    setup_s = time.time() - t_setup
+
+    def one_step(step_idx=None):
+        for T in Ts:
+            flush.fill_(step_idx & 0xFF if step_idx is not None else 1)
+            if step_idx is None:
+                layer.forward(xs[T], ys[T])
+            else:
+                evs = ev_sets[T][step_idx]
+                layer.forward(xs[T], ys[T], events=[e.cuda_event for e in evs])
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    for T in Ts:
+        st, det = layer.device_status(T)
+        if st != binding.MOE_OK:
+            raise binding.MoeError(st, f"device status after warm-up (T={T}, detail {det})")
+
+    # routing facts (touched experts) of each batch, from the last warm-up call
+    touched = {}
+    for T in Ts:
+        layer.forward(xs[T], ys[T])
+        ids = layer.view_tensor(T, "topk_ids", torch.int32, (T, wl["k"])).cpu().numpy()
+        touched[T] = accounting.n_touched(ids, wl["E"])
+    torch.cuda.synchronize()
+
+    gpu_index = local
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if cvd:
+        try:
+            gpu_index = int(cvd.split(",")[local])
+        except (ValueError, IndexError):
+            gpu_index = local
+    sampler = ClockSampler(gpu_index)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    for s in range(args.steps):
+        one_step(s)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    clocks = sampler.stop()
+
+    # per-call and per-kernel device times
+    per_T = {}
+    kern_ms = {n: 0.0 for n in binding.KERNEL_NAMES}
+    kern_launch_ms = {T: {n: [] for n in binding.KERNEL_NAMES} for T in Ts}
+    total_ms = 0.0
+    for T in Ts:
+        calls = []
+        for evs in ev_sets[T]:
+            calls.append(evs[0].elapsed_time(evs[nk]))
+            for i, n in enumerate(binding.KERNEL_NAMES):
+                dt = evs[i].elapsed_time(evs[i + 1])
+                kern_ms[n] += dt
+                kern_launch_ms[T][n].append(dt)
+        total_ms += sum(calls)
+        lb = accounting.layer_bytes(T, H, wl["I"], wl["E"], wl["k"], touched[T])
+        us = statistics.median(calls) * 1e3
+        per_T[str(T)] = {"us_median": round(us, 2), "us_mean": round(sum(calls) / len(calls) * 1e3, 2),
+                         "tokens_per_s": round(T / (us * 1e-6), 1), "experts_touched": touched[T],
+                         "weight_GB": round(lb["weights"] / 1e9, 4),
+                         "weight_GBps": round(lb["weights"] / (us * 1e-6) / 1e9, 1),
+                         "hbm_frac_of_8TBps": round(lb["weights"] / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4)}
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = sum(Ts)
+    ms_max = reduce_max(ms_per_step, world)
+    value = world * tokens_per_step / (ms_max * 1e-3)
+
+    # dominant kernel and its roofline
+    peaks, peak_kind = load_peaks()
+    dom = max(kern_ms, key=kern_ms.get)
+    launches = args.steps * len(Ts)
+    avg_s = kern_ms[dom] / launches * 1e-3
+    prefill_like = all(T * wl["k"] > 64 * wl["E"] for T in Ts)
+    if dom in ("gemm_gate_up_swiglu", "gemm_down") and prefill_like:
+        fl = accounting.layer_flops
+        per = [fl(T, H, wl["I"], wl["E"], wl["k"])["gemm1" if dom == "gemm_gate_up_swiglu" else "gemm2"]
+               for T in Ts]
+        roof = roofline("tensor", sum(per) / len(per), avg_s, peaks["bf16_tflops"], None)
+        roof["peak_source"] = f"bf16_tflops ({peak_kind})"
+    else:
+        if dom == "gemm_gate_up_swiglu":
+            per = [accounting.gemm1_kernel_bytes(T, H, wl["I"], wl["k"], touched[T]) for T in Ts]
+        elif dom == "gemm_down":
+            per = [accounting.gemm2_kernel_bytes(T, H, wl["I"], wl["k"], touched[T]) for T in Ts]
+        else:
+            per = [accounting.layer_bytes(T, H, wl["I"], wl["E"], wl["k"], touched[T])["total"] for T in Ts]
+        traffic = ncu_traffic_per_launch(dom, args.workload)
+        roof = roofline("hbm", sum(per) / len(per), avg_s, peaks["hbm_gbs"], traffic)
+        roof["peak_source"] = f"hbm_gbs ({peak_kind}, copy bandwidth)"
+    roof["kernel"] = dom
+    roof["algorithmic_per_launch"] = sum(per) / len(per)
+    roof["avg_launch_us"] = round(avg_s * 1e6, 2)
+
+    # end to end through the public API with host buffers: H2D of x, forward, D2H of y
+    pinned_x = {T: torch.from_numpy(host["xs"][T].view(np.int16)).pin_memory() for T in Ts}
+    pinned_y = {T: torch.empty((T, H), dtype=torch.int16).pin_memory() for T in Ts}
+    e2e_ms = 0.0
+    for s in range(args.steps):
+        for T in Ts:
+            flush.fill_(s & 0xFF)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            xs[T].copy_(pinned_x[T], non_blocking=True)
+            layer.forward(xs[T], ys[T])
+            pinned_y[T].copy_(ys[T], non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            e2e_ms += a.elapsed_time(b)
+    e2e_ms_step = reduce_max(e2e_ms / args.steps, world)
+    e2e = {"value": round(world * tokens_per_step / (e2e_ms_step * 1e-3), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": sum(T * H * 2 for T in Ts), "d2h_bytes_per_step": sum(T * H * 2 for T in Ts),
+           "ms_per_step": round(e2e_ms_step, 4)}
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator; random-init weights)",
+        "config": {"workload": wl["label"], "tokens_per_step": tokens_per_step,
+                   "layer_calls_per_step": len(Ts),
+                   "l2": "flushed (256 MB write) before every layer call; flush outside the timed CUDA-event "
+                         "intervals",
+                   "parallelism": f"replicas x{world} (no cross-GPU data path)", "per_T": per_T,
+                   "kernel_ms_per_step": {n: round(v / args.steps, 4) for n, v in kern_ms.items()},
+                   "wall_s_timed_region": round(t_wall, 3), "setup_s": round(setup_s, 1)},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": launches * nk,
+        "clocks": clocks,
+    }
+    return out, host
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample-tokens", type=int, default=24)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("bench: at least 3 warm-up steps are required; using 3", file=sys.stderr)
+        args.warmup = 3
+    wl = WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+
+    if args.impl == "reference":
+        if rank == 0:
+            host = make_host_inputs(wl)
+            cpu_oracle_rate(wl, host, max(len(wl["Ts"]), args.cpu_sample_tokens // 6), steps=1)  # warm-up (one pass)
+            rate, ntok, secs, cores = cpu_oracle_rate(wl, host, max(len(wl["Ts"]), args.cpu_sample_tokens // 6),
+                                                      steps=args.steps)
+            out = {"impl": "reference", "metric": METRIC, "value": round(rate, 3), "unit": "tokens/s", "n_gpus": world,
+                   "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 1),
+                   "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                   "data": "synthetic (seeded generator; random-init weights)",
+                   "config": {"workload": wl["label"], "reference": "CPU oracle (fp64 C, threaded)"},
+                   "cpu_baseline": {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                    "sample": f"{ntok} tokens over {args.steps} steps, spread over the batches T={wl['Ts']}"},
+                   "e2e": {"value": round(rate, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}}
+            print(json.dumps(out), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    out, host = run_ours(args, wl, world, rank, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, ntok, secs, cores = cpu_oracle_rate(wl, host, args.cpu_sample_tokens)
+        out["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                               "sample": f"{ntok} tokens spread over the batches T={wl['Ts']} ({secs:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

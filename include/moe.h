@@ -113,6 +113,23 @@ MOE_API moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const 
                        const moe_bf16* w2, moe_bf16* y, void* workspace, size_t workspace_bytes,
                        moe_stream_t stream);
 
+/* Number of kernels one moe_forward call launches, in order:
+ *   1 RMSNorm + router logits, 2 top-k + softmax, 3 expert align, 4 gather,
+ *   5 gate/up grouped GEMM + SwiGLU, 6 down grouped GEMM, 7 weighted combine. */
+#define MOE_NUM_KERNELS 7
+
+/* moe_forward, plus CUDA events recorded on `stream` around the kernels:
+ * events[0] before kernel 1 and events[i] right after kernel i (i = 1..7),
+ * so cudaEventElapsedTime(events[i-1], events[i]) is kernel i's time on the
+ * stream.  `events` holds n_events >= MOE_NUM_KERNELS + 1 cudaEvent_t
+ * handles created by the caller (cudaEventCreate); the library records them
+ * and does not create, wait on or destroy them.  Everything else is as for
+ * moe_forward; with T = 0 no event is recorded. */
+MOE_API moe_status moe_forward_events(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                                      const float* w_router, const float* router_bias, const moe_bf16* w13,
+                                      const moe_bf16* w2, moe_bf16* y, void* workspace, size_t workspace_bytes,
+                                      moe_stream_t stream, void* const* events, int32_t n_events);
+
 /* Routing front end only (RMSNorm, router, top-k, align with `pad_rows`
  * rows of padding granularity), with the results copied out:
  *   topk_ids       [T, top_k] int32   selected experts, best first

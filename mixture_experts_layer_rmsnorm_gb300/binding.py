@@ -59,13 +59,14 @@ def load(build: bool = True):
             sp = ctypes.POINTER(MoeShape)
             lib.moe_workspace_size.argtypes = [sp, ctypes.POINTER(sz)]
             lib.moe_forward.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p]
+            lib.moe_forward_events.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_route_debug.argtypes = [sp, p, p, p, p, i32, p, p, p, p, i64, p, sz, p]
             lib.moe_workspace_views.argtypes = [sp, p, sz, ctypes.POINTER(MoeViews)]
             lib.moe_device_status.argtypes = [p, sz, p, ctypes.POINTER(ctypes.c_int32)]
             lib.moe_status_string.argtypes = [ctypes.c_int]
             lib.moe_status_string.restype = ctypes.c_char_p
-            for f in ("moe_workspace_size", "moe_forward", "moe_route_debug", "moe_workspace_views",
-                      "moe_device_status"):
+            for f in ("moe_workspace_size", "moe_forward", "moe_forward_events", "moe_route_debug",
+                      "moe_workspace_views", "moe_device_status"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -89,6 +90,18 @@ def moe_forward(s: MoeShape, x, g_norm, w_router, router_bias, w13, w2, y, works
                 stream) -> int:
     return load().moe_forward(ctypes.byref(s), x, g_norm, w_router, router_bias, w13, w2, y, workspace,
                               workspace_bytes, stream)
+
+
+MOE_NUM_KERNELS = 7
+KERNEL_NAMES = ("norm_router", "topk_softmax", "align", "gather", "gemm_gate_up_swiglu", "gemm_down", "combine")
+
+
+def moe_forward_events(s: MoeShape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes,
+                       stream, events) -> int:
+    """events: a sequence of MOE_NUM_KERNELS + 1 raw cudaEvent_t handles (ints)."""
+    arr = (ctypes.c_void_p * len(events))(*events)
+    return load().moe_forward_events(ctypes.byref(s), x, g_norm, w_router, router_bias, w13, w2, y, workspace,
+                                     workspace_bytes, stream, arr, len(events))
 
 
 def moe_route_debug(s: MoeShape, x, g_norm, w_router, router_bias, pad_rows, topk_ids, topk_w, expert_offsets,
@@ -150,15 +163,21 @@ class MoeLayer:
             raise MoeError(st, "moe_workspace_size")
         return n
 
-    def forward(self, x, y=None, stream=None):
+    def forward(self, x, y=None, stream=None, events=None):
+        """y = layer(x).  events: optional MOE_NUM_KERNELS + 1 cudaEvent_t handles
+        recorded around the kernels (moe_forward_events)."""
         import torch
         T = x.shape[0]
         self.ensure_capacity(T)
         if y is None:
             y = torch.empty((T, self.H), dtype=x.dtype, device=x.device)
         s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
-        st = moe_forward(self.shape(T), _ptr(x), _ptr(self.g_norm), _ptr(self.w_router), _ptr(self.bias),
-                         _ptr(self.w13), _ptr(self.w2), _ptr(y), _ptr(self.workspace), self.workspace_bytes(T), s)
+        args = (self.shape(T), _ptr(x), _ptr(self.g_norm), _ptr(self.w_router), _ptr(self.bias), _ptr(self.w13),
+                _ptr(self.w2), _ptr(y), _ptr(self.workspace), self.workspace_bytes(T), s)
+        if events is None:
+            st = moe_forward(*args)
+        else:
+            st = moe_forward_events(*args, events)
         if st != MOE_OK:
             raise MoeError(st, "moe_forward")
         return y

@@ -184,9 +184,15 @@ moe_status moe_workspace_views(const moe_shape* shape, void* workspace, size_t w
   return MOE_OK;
 }
 
-moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
-                       const float* router_bias, const moe_bf16* w13, const moe_bf16* w2, moe_bf16* y,
-                       void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward pass; when `events` is given, events[0] is recorded before the
+// first kernel and events[i] after the i-th of the seven kernels.
+moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
+                        const float* router_bias, const moe_bf16* w13, const moe_bf16* w2, moe_bf16* y,
+                        void* workspace, size_t workspace_bytes, moe_stream_t stream, void* const* events) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   const moe_shape& s = *shape;
@@ -200,6 +206,9 @@ moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16
   const Layout L = make_layout(s);
   const GemmPlan plan = (static_cast<int64_t>(s.T) * s.top_k <= 64LL * s.E) ? GemmPlan::kDecode : GemmPlan::kPrefill;
   const int bn1 = moe::gemm_gate_up_bn(plan), bn2 = moe::gemm_down_bn(plan);
+  auto mark = [&](int i) {
+    return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), cs) == cudaSuccess;
+  };
 
   CUtensorMap tm_w13, tm_xg, tm_w2, tm_act;
   if (!make_map(&tm_w13, w13, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, moe::kWeightBoxRows) ||
@@ -208,13 +217,26 @@ moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16
       !make_map(&tm_act, at<void>(workspace, L.act), s.I, L.P_max, moe::kTokBoxRows))
     return MOE_ERR_CUDA;
 
-  st = run_front(s, L, x, g_norm, w_router, router_bias, moe::kPadRows, bn1, bn2, workspace, cs, num_sms);
-  if (st != MOE_OK) return st;
-  const int N = s.T * s.top_k;
   int32_t* err = at<int32_t>(workspace, L.err);
+  if (!mark(0)) return MOE_ERR_CUDA;
+  if (moe::launch_norm_router(x, g_norm, w_router, router_bias, s.T, s.H, s.E, s.eps, at<uint16_t>(workspace, L.h),
+                              at<float>(workspace, L.logits), err, num_sms, cs) != cudaSuccess || !mark(1))
+    return MOE_ERR_CUDA;
+  if (moe::launch_topk_softmax(at<float>(workspace, L.logits), s.T, s.E, s.top_k, s.renormalize,
+                               at<int32_t>(workspace, L.ids), at<float>(workspace, L.w), cs) != cudaSuccess ||
+      !mark(2))
+    return MOE_ERR_CUDA;
+  const int N = s.T * s.top_k;
+  if (moe::launch_align(at<int32_t>(workspace, L.ids), N, s.E, moe::kPadRows, bn1, s.I / moe::kWeightBoxRows, bn2,
+                        s.H / moe::kWeightBoxRows, at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.offsets),
+                        at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.slot),
+                        at<int32_t>(workspace, L.unit1), at<int32_t>(workspace, L.unit2), err, cs) != cudaSuccess ||
+      !mark(3))
+    return MOE_ERR_CUDA;
   if (moe::launch_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
                          at<int32_t>(workspace, L.offsets), s.E, N, s.top_k, s.H, L.P_max,
-                         at<uint16_t>(workspace, L.xg), cs) != cudaSuccess)
+                         at<uint16_t>(workspace, L.xg), cs) != cudaSuccess ||
+      !mark(4))
     return MOE_ERR_CUDA;
 
   moe::ExpertGemmArgs a1{};
@@ -228,7 +250,7 @@ moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16
   a1.n_out = s.I;
   a1.out = at<uint16_t>(workspace, L.act);
   a1.err = err;
-  if (moe::launch_gemm_gate_up(tm_w13, tm_xg, a1, plan, num_sms, cs) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_gemm_gate_up(tm_w13, tm_xg, a1, plan, num_sms, cs) != cudaSuccess || !mark(5)) return MOE_ERR_CUDA;
 
   moe::ExpertGemmArgs a2{};
   a2.offsets = at<int32_t>(workspace, L.offsets);
@@ -241,12 +263,35 @@ moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16
   a2.n_out = s.H;
   a2.out = at<uint16_t>(workspace, L.out);
   a2.err = err;
-  if (moe::launch_gemm_down(tm_w2, tm_act, a2, plan, num_sms, cs) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::launch_gemm_down(tm_w2, tm_act, a2, plan, num_sms, cs) != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
 
   if (moe::launch_combine(at<uint16_t>(workspace, L.out), at<int32_t>(workspace, L.slot), at<float>(workspace, L.w),
-                          s.T, s.H, s.top_k, y, cs) != cudaSuccess)
+                          s.T, s.H, s.top_k, y, cs) != cudaSuccess ||
+      !mark(7))
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
+                       const float* router_bias, const moe_bf16* w13, const moe_bf16* w2, moe_bf16* y,
+                       void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  return forward_impl(shape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes, stream,
+                      nullptr);
+}
+
+moe_status moe_forward_events(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                              const float* w_router, const float* router_bias, const moe_bf16* w13, const moe_bf16* w2,
+                              moe_bf16* y, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                              void* const* events, int32_t n_events) {
+  if (!events || n_events < MOE_NUM_KERNELS + 1) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i <= MOE_NUM_KERNELS; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return forward_impl(shape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes, stream,
+                      events);
 }
 
 moe_status moe_route_debug(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
