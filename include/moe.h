@@ -148,6 +148,35 @@ MOE_API moe_status moe_route_debug(const moe_shape* shape, const moe_bf16* x, co
                            int32_t* sorted_ids, int64_t sorted_capacity, void* workspace,
                            size_t workspace_bytes, moe_stream_t stream);
 
+/* Bytes of the fixed device scratch array used by moe_forward_static_scratch. */
+#define MOE_STATIC_SCRATCH_BYTES (64ull << 20)
+
+/* moe_forward without a caller-provided workspace and without allocating.
+ * The pages have no counterpart of this call; it exists for callers that
+ * cannot allocate device memory: hosts that give all device memory to their
+ * own pool or run under a fixed budget, callers without a device allocator
+ * (plain C, plug-ins), and latency-critical loops that avoid cudaMalloc /
+ * cudaFree because those can block and synchronise the device.
+ * The scratch is a file-scope __device__ array of MOE_STATIC_SCRATCH_BYTES
+ * (64 MiB) inside the library; every GPU that loads the library holds it
+ * until the process exits.  The caller still passes inputs and output, as
+ * for moe_forward.
+ *   - Shapes whose moe_workspace_size() exceeds MOE_STATIC_SCRATCH_BYTES are
+ *     rejected with MOE_ERR_WORKSPACE before anything is enqueued (e.g. the
+ *     decode layer H = I = 4096, E = 64, top_k = 8 fits for T <= 211).
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address once (cudaGetSymbolAddress) and keeps it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents; each call rewrites everything it reads, so nothing
+ *     has to be cleared between calls.  Calls whose work overlaps on the GPU
+ *     (other streams, other host threads) race on the array: serialise them.
+ *   - The intermediate tensors are not exposed (no moe_workspace_views).
+ *   - No cudaMalloc, cudaFree or allocating library routine is called. */
+MOE_API moe_status moe_forward_static_scratch(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                                              const float* w_router, const float* router_bias, const moe_bf16* w13,
+                                              const moe_bf16* w2, moe_bf16* y, moe_stream_t stream);
+
 /* Device pointers to the intermediate tensors inside a workspace, valid for
  * the shape it was sized for (layout only; makes no CUDA call). */
 typedef struct {

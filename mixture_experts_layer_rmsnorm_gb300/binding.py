@@ -61,12 +61,13 @@ def load(build: bool = True):
             lib.moe_forward.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p]
             lib.moe_forward_events.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_route_debug.argtypes = [sp, p, p, p, p, i32, p, p, p, p, i64, p, sz, p]
+            lib.moe_forward_static_scratch.argtypes = [sp, p, p, p, p, p, p, p, p]
             lib.moe_workspace_views.argtypes = [sp, p, sz, ctypes.POINTER(MoeViews)]
             lib.moe_device_status.argtypes = [p, sz, p, ctypes.POINTER(ctypes.c_int32)]
             lib.moe_status_string.argtypes = [ctypes.c_int]
             lib.moe_status_string.restype = ctypes.c_char_p
             for f in ("moe_workspace_size", "moe_forward", "moe_forward_events", "moe_route_debug",
-                      "moe_workspace_views", "moe_device_status"):
+                      "moe_workspace_views", "moe_device_status", "moe_forward_static_scratch"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -102,6 +103,15 @@ def moe_forward_events(s: MoeShape, x, g_norm, w_router, router_bias, w13, w2, y
     arr = (ctypes.c_void_p * len(events))(*events)
     return load().moe_forward_events(ctypes.byref(s), x, g_norm, w_router, router_bias, w13, w2, y, workspace,
                                      workspace_bytes, stream, arr, len(events))
+
+
+MOE_STATIC_SCRATCH_BYTES = 64 << 20
+
+
+def moe_forward_static_scratch(s: MoeShape, x, g_norm, w_router, router_bias, w13, w2, y, stream) -> int:
+    """moe_forward with the library's fixed device scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    return load().moe_forward_static_scratch(ctypes.byref(s), x, g_norm, w_router, router_bias, w13, w2, y, stream)
 
 
 def moe_route_debug(s: MoeShape, x, g_norm, w_router, router_bias, pad_rows, topk_ids, topk_w, expert_offsets,

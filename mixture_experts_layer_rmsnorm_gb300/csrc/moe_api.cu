@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "../../include/moe.h"
+#include "moe_forward_impl.h"
 #include "moe_kernels.cuh"
 
 namespace {
@@ -186,7 +187,7 @@ moe_status moe_workspace_views(const moe_shape* shape, void* workspace, size_t w
 
 }  // extern "C"
 
-namespace {
+namespace moe {
 
 // The forward pass; when `events` is given, events[0] is recorded before the
 // first kernel and events[i] after the i-th of the seven kernels.
@@ -272,15 +273,15 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   return MOE_OK;
 }
 
-}  // namespace
+}  // namespace moe
 
 extern "C" {
 
 moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
                        const float* router_bias, const moe_bf16* w13, const moe_bf16* w2, moe_bf16* y,
                        void* workspace, size_t workspace_bytes, moe_stream_t stream) {
-  return forward_impl(shape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes, stream,
-                      nullptr);
+  return moe::forward_impl(shape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes, stream,
+                           nullptr);
 }
 
 moe_status moe_forward_events(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
@@ -290,8 +291,8 @@ moe_status moe_forward_events(const moe_shape* shape, const moe_bf16* x, const m
   if (!events || n_events < MOE_NUM_KERNELS + 1) return MOE_ERR_INVALID_ARG;
   for (int i = 0; i <= MOE_NUM_KERNELS; ++i)
     if (!events[i]) return MOE_ERR_INVALID_ARG;
-  return forward_impl(shape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes, stream,
-                      events);
+  return moe::forward_impl(shape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes, stream,
+                           events);
 }
 
 moe_status moe_route_debug(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
