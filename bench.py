@@ -52,6 +52,13 @@ WORKLOADS = {
                    label="skewed routing T=512, H=4096, I=1408, E=128, top_k=6, Zipf(1.2) bias, bf16"),
     "tiny": dict(H=128, I=256, E=8, k=2, Ts=[4], seed=0, zipf=None,
                  label="tiny T=4, H=128, I=256, E=8, top_k=2, bf16"),
+    # small cases of the same per-unit shapes, for ncu captures (inputs > L2, < 2 GB on the device)
+    "decode_ncu": dict(H=4096, I=4096, E=16, k=8, Ts=[64], seed=0, zipf=None,
+                       label="ncu case: T=64, H=I=4096, E=16, top_k=8 (decode tiles, 32 tokens/expert)"),
+    "router_ncu": dict(H=4096, I=256, E=64, k=8, Ts=[1, 64], seed=0, zipf=None,
+                       label="ncu case: router of the decode layer (H=4096, E=64) with small experts (I=256)"),
+    "prefill_ncu": dict(H=4096, I=4096, E=8, k=8, Ts=[512], seed=0, zipf=None,
+                        label="ncu case: T=512, H=I=4096, E=8, top_k=8 (prefill tiles, 512 tokens/expert)"),
 }
 KERNEL_SOURCES = {  # files whose content the ncu traffic figure of a kernel depends on
     "gemm_gate_up_swiglu": ["k_expert_gemm.cu", "tc_ptx.cuh", "moe_kernels.cuh", "moe_api.cu"],
@@ -205,23 +212,24 @@ def make_host_inputs(wl):
     return dict(g=g, wr=wr, bias=bias, w13=w13, w2=w2, xs=xs)
 
 
-def cpu_oracle_rate(wl, host, n_tokens, steps=1):
-    """Tokens/s of the CPU oracle (as it stands) over `steps` runs of a bounded
-    sample of n_tokens tokens spread over the workload's batches."""
+def cpu_oracle_rate(wl, host, per_batch_cap, reps=1, min_seconds=0.0, max_reps=50):
+    """Tokens/s of the CPU oracle (as it stands, all host cores) on a bounded
+    sample: from each of the workload's batches, up to per_batch_cap tokens
+    spread over the batch; repeated `reps` times, or more until min_seconds of
+    CPU work have been timed (at most max_reps)."""
     import numpy as np
     import oracle
-    Ts = wl["Ts"]
-    per = max(1, n_tokens // len(Ts))
-    total_tok, total_s = 0, 0.0
-    for _ in range(steps):
-        for T in Ts:
-            sample = np.unique(np.linspace(0, T - 1, min(T, per)).astype(np.int64))
+    total_tok, total_s, r = 0, 0.0, 0
+    while r < reps or (total_s < min_seconds and r < max_reps):
+        for T in wl["Ts"]:
+            sample = np.unique(np.linspace(0, T - 1, min(T, per_batch_cap)).astype(np.int64))
             t0 = time.perf_counter()
             oracle.moe_forward(host["xs"][T], host["g"], host["wr"], host["bias"], host["w13"], host["w2"], wl["k"],
                                True, 1e-6, sample=sample)
             total_s += time.perf_counter() - t0
             total_tok += sample.size
-    return total_tok / total_s, total_tok, total_s, oracle.threads()
+        r += 1
+    return total_tok / total_s, total_tok, total_s, oracle.threads(), r
 
 
 # ----------------------------------------------------------------- our arm
@@ -247,7 +255,15 @@ def run_ours(args, wl, world, rank, local):
     H = wl["H"]
     xs = {T: d16(host["xs"][T]) for T in Ts}
     ys = {T: torch.empty((T, H), dtype=torch.int16, device=dev) for T in Ts}
+    # L2 flush: write 256 MB (2x L2), then read another 256 MB so that the
+    # write's dirty lines are written back here rather than inside the timed call
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(64 << 20, dtype=torch.int32, device=dev)
+
+    def flush_l2(v):
+        flush.fill_(v & 0xFF)
+        flush_rd.sum()
+
     stream = torch.cuda.current_stream(dev)
     nk = binding.MOE_NUM_KERNELS
 
@@ -257,17 +273,23 @@ def run_ours(args, wl, world, rank, local):
             e.record(stream)  # creates the CUDA event behind the torch object
         return evs
 
-    ev_sets = {T: [new_events() for _ in range(args.steps)] for T in Ts}
+    call_ev = {T: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)] for T in Ts}
+    kern_ev = {T: [new_events() for _ in range(args.steps)] for T in Ts}
     setup_s = time.time() - t_setup
 
-    def one_step(step_idx=None):
+    def one_step(step_idx=None, per_kernel=False):
         for T in Ts:
-            flush.fill_(step_idx & 0xFF if step_idx is not None else 1)
+            flush_l2(step_idx or 0)
             if step_idx is None:
                 layer.forward(xs[T], ys[T])
+            elif per_kernel:
+                layer.forward(xs[T], ys[T], events=[e.cuda_event for e in kern_ev[T][step_idx]])
             else:
-                evs = ev_sets[T][step_idx]
-                layer.forward(xs[T], ys[T], events=[e.cuda_event for e in evs])
+                a, b = call_ev[T][step_idx]
+                a.record(stream)
+                layer.forward(xs[T], ys[T])
+                b.record(stream)
 
     for _ in range(args.warmup):
         one_step()
@@ -302,21 +324,24 @@ def run_ours(args, wl, world, rank, local):
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
     barrier(world)
+    # second pass, same work: CUDA events recorded by the library around each kernel
+    for s in range(args.steps):
+        one_step(s, per_kernel=True)
+    torch.cuda.synchronize()
     clocks = sampler.stop()
 
-    # per-call and per-kernel device times
+    # per-call device times (plain calls) and per-kernel times (second pass)
     per_T = {}
     kern_ms = {n: 0.0 for n in binding.KERNEL_NAMES}
-    kern_launch_ms = {T: {n: [] for n in binding.KERNEL_NAMES} for T in Ts}
     total_ms = 0.0
     for T in Ts:
-        calls = []
-        for evs in ev_sets[T]:
-            calls.append(evs[0].elapsed_time(evs[nk]))
+        calls = [a.elapsed_time(b) for a, b in call_ev[T]]
+        kt = {n: [] for n in binding.KERNEL_NAMES}
+        for evs in kern_ev[T]:
             for i, n in enumerate(binding.KERNEL_NAMES):
                 dt = evs[i].elapsed_time(evs[i + 1])
                 kern_ms[n] += dt
-                kern_launch_ms[T][n].append(dt)
+                kt[n].append(dt)
         total_ms += sum(calls)
         lb = accounting.layer_bytes(T, H, wl["I"], wl["E"], wl["k"], touched[T])
         us = statistics.median(calls) * 1e3
@@ -324,7 +349,8 @@ def run_ours(args, wl, world, rank, local):
                          "tokens_per_s": round(T / (us * 1e-6), 1), "experts_touched": touched[T],
                          "weight_GB": round(lb["weights"] / 1e9, 4),
                          "weight_GBps": round(lb["weights"] / (us * 1e-6) / 1e9, 1),
-                         "hbm_frac_of_8TBps": round(lb["weights"] / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4)}
+                         "hbm_frac_of_8TBps": round(lb["weights"] / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
+                         "kernel_us_median": {n: round(statistics.median(v) * 1e3, 2) for n, v in kt.items()}}
     ms_per_step = total_ms / args.steps
     tokens_per_step = sum(Ts)
     ms_max = reduce_max(ms_per_step, world)
@@ -362,7 +388,7 @@ def run_ours(args, wl, world, rank, local):
     e2e_ms = 0.0
     for s in range(args.steps):
         for T in Ts:
-            flush.fill_(s & 0xFF)
+            flush_l2(s)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -383,14 +409,18 @@ def run_ours(args, wl, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator; random-init weights)",
         "config": {"workload": wl["label"], "tokens_per_step": tokens_per_step,
                    "layer_calls_per_step": len(Ts),
-                   "l2": "flushed (256 MB write) before every layer call; flush outside the timed CUDA-event "
-                         "intervals",
+                   "l2": "flushed before every layer call (256 MB write, then a 256 MB read of another buffer so "
+                         "no dirty lines remain); flush outside the timed CUDA-event intervals",
+                   "timing": "CUDA events on the launch stream around each plain moe_forward call; kernel times from "
+                             "a second pass of the same calls through moe_forward_events",
                    "parallelism": f"replicas x{world} (no cross-GPU data path)", "per_T": per_T,
                    "kernel_ms_per_step": {n: round(v / args.steps, 4) for n, v in kern_ms.items()},
                    "wall_s_timed_region": round(t_wall, 3), "setup_s": round(setup_s, 1)},
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": launches * nk,
+        # kernels of the timed pass (top-k runs inside the align kernel for small T and E); the per-kernel pass
+        # launches as many again
+        "gpu_launches": sum(args.steps * binding.kernels_per_call(T, wl["E"]) for T in Ts),
         "clocks": clocks,
     }
     return out, host
@@ -403,7 +433,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-sample-tokens", type=int, default=24)
+    ap.add_argument("--ref-tokens-per-batch", type=int, default=32,
+                    help="CPU oracle sample: at most this many tokens of each batch per step")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum timed CPU-oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -418,16 +450,18 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             host = make_host_inputs(wl)
-            cpu_oracle_rate(wl, host, max(len(wl["Ts"]), args.cpu_sample_tokens // 6), steps=1)  # warm-up (one pass)
-            rate, ntok, secs, cores = cpu_oracle_rate(wl, host, max(len(wl["Ts"]), args.cpu_sample_tokens // 6),
-                                                      steps=args.steps)
+            cap = args.ref_tokens_per_batch
+            cpu_oracle_rate(wl, host, cap, reps=args.warmup)  # warm-up steps, untimed
+            rate, ntok, secs, cores, _ = cpu_oracle_rate(wl, host, cap, reps=args.steps)
             out = {"impl": "reference", "metric": METRIC, "value": round(rate, 3), "unit": "tokens/s", "n_gpus": world,
                    "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 1),
                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                    "data": "synthetic (seeded generator; random-init weights)",
-                   "config": {"workload": wl["label"], "reference": "CPU oracle (fp64 C, threaded)"},
+                   "config": {"workload": wl["label"], "reference": "CPU oracle (fp64 C, all host cores)",
+                              "step": f"up to {cap} tokens of each batch T={wl['Ts']}"},
                    "cpu_baseline": {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                    "sample": f"{ntok} tokens over {args.steps} steps, spread over the batches T={wl['Ts']}"},
+                                    "sample": f"{ntok} tokens over {args.steps} steps (up to {cap} per batch of "
+                                              f"T={wl['Ts']}), {secs:.1f} s"},
                    "e2e": {"value": round(rate, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}}
             print(json.dumps(out), flush=True)
@@ -438,9 +472,11 @@ def main():
 
     out, host = run_ours(args, wl, world, rank, local)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, ntok, secs, cores = cpu_oracle_rate(wl, host, args.cpu_sample_tokens)
+        cap = args.ref_tokens_per_batch
+        rate, ntok, secs, cores, reps = cpu_oracle_rate(wl, host, cap, reps=1, min_seconds=args.cpu_seconds)
         out["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                               "sample": f"{ntok} tokens spread over the batches T={wl['Ts']} ({secs:.1f} s)"}
+                               "sample": f"{ntok} tokens: {reps} passes over up to {cap} tokens of each batch "
+                                         f"T={wl['Ts']} ({secs:.1f} s)"}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -113,15 +113,20 @@ MOE_API moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const 
                        const moe_bf16* w2, moe_bf16* y, void* workspace, size_t workspace_bytes,
                        moe_stream_t stream);
 
-/* Number of kernels one moe_forward call launches, in order:
+/* The kernels of one moe_forward call, in order:
  *   1 RMSNorm + router logits, 2 top-k + softmax, 3 expert align, 4 gather,
- *   5 gate/up grouped GEMM + SwiGLU, 6 down grouped GEMM, 7 weighted combine. */
+ *   5 gate/up grouped GEMM + SwiGLU, 6 down grouped GEMM, 7 weighted combine.
+ * For T <= MOE_FUSED_TOPK_MAX_T and E <= MOE_FUSED_TOPK_MAX_E, step 2 runs
+ * inside the align kernel (one launch fewer: MOE_NUM_KERNELS - 1 per call). */
 #define MOE_NUM_KERNELS 7
+#define MOE_FUSED_TOPK_MAX_T 256
+#define MOE_FUSED_TOPK_MAX_E 256
 
 /* moe_forward, plus CUDA events recorded on `stream` around the kernels:
  * events[0] before kernel 1 and events[i] right after kernel i (i = 1..7),
  * so cudaEventElapsedTime(events[i-1], events[i]) is kernel i's time on the
- * stream.  `events` holds n_events >= MOE_NUM_KERNELS + 1 cudaEvent_t
+ * stream (with top-k fused into the align kernel, events[2] follows events[1]
+ * at once and the align interval includes the top-k).  `events` holds n_events >= MOE_NUM_KERNELS + 1 cudaEvent_t
  * handles created by the caller (cudaEventCreate); the library records them
  * and does not create, wait on or destroy them.  Everything else is as for
  * moe_forward; with T = 0 no event is recorded. */

@@ -94,6 +94,13 @@ def moe_forward(s: MoeShape, x, g_norm, w_router, router_bias, w13, w2, y, works
 
 
 MOE_NUM_KERNELS = 7
+MOE_FUSED_TOPK_MAX_T = 256  # top-k runs inside the align kernel up to this many tokens ...
+MOE_FUSED_TOPK_MAX_E = 256  # ... and experts
+
+
+def kernels_per_call(T: int, E: int) -> int:
+    fused = T <= MOE_FUSED_TOPK_MAX_T and E <= MOE_FUSED_TOPK_MAX_E
+    return MOE_NUM_KERNELS - 1 if fused else MOE_NUM_KERNELS
 KERNEL_NAMES = ("norm_router", "topk_softmax", "align", "gather", "gemm_gate_up_swiglu", "gemm_down", "combine")
 
 

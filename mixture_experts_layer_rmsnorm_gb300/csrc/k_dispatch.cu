@@ -15,6 +15,8 @@
 #include <cuda_bf16.h>
 
 #include "moe_kernels.cuh"
+#include "pdl.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -55,9 +57,15 @@ __device__ int block_exclusive_scan(int v, int* tmp, int* total) {
 }
 
 // One CTA of 1024 threads.  Dynamic shared memory: cnt[E], cursor[E],
-// wbase[32][E] (ints).
+// wbase[32][E] (ints).  With FUSED_TOPK the CTA first selects the top-k
+// experts of all T tokens from the logits (one warp per token; used for small
+// T, where a separate launch costs more than the work), then aligns.
+// The routing ids are read with L2-coherent loads: in the fused form this
+// kernel wrote them itself.
+template <int FUSED_VPL>  // 0: ids given; else top-k first, with FUSED_VPL logits per lane
 __global__ void __launch_bounds__(kAlignThreads)
-    align_kernel(const int32_t* __restrict__ ids, int N, int E, int pad, int bn1, int tiles1, int bn2, int tiles2,
+    align_kernel(const float* __restrict__ logits, int T, int k, int renorm, float* __restrict__ topk_w,
+                 int32_t* ids, int N, int E, int pad, int bn1, int tiles1, int bn2, int tiles2,
                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
                  int32_t* __restrict__ slot_of, int32_t* __restrict__ unit_off1, int32_t* __restrict__ unit_off2,
                  int32_t* __restrict__ err) {
@@ -68,12 +76,20 @@ __global__ void __launch_bounds__(kAlignThreads)
   __shared__ int scan_tmp[kAlignWarps + 1];
   __shared__ int bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_launch_dependents();
+  pdl_wait();
+  if constexpr (FUSED_VPL > 0) {
+    for (int t = warp; t < T; t += kAlignWarps)
+      topk_softmax_warp<FUSED_VPL>(logits + static_cast<size_t>(t) * E, E, k, renorm,
+                                   ids + static_cast<size_t>(t) * k, topk_w + static_cast<size_t>(t) * k);
+    __syncthreads();
+  }
 
   if (tid == 0) bad = 0;
   for (int e = tid; e < E; e += kAlignThreads) cnt[e] = 0;
   __syncthreads();
   for (int i = tid; i < N; i += kAlignThreads) {
-    const int e = ids[i];
+    const int e = __ldcg(ids + i);
     if (e < 0 || e >= E)
       bad = 1;
     else
@@ -127,7 +143,7 @@ __global__ void __launch_bounds__(kAlignThreads)
   for (int base = 0; base < N; base += kAlignThreads) {
     const int i = base + tid;
     const bool valid = i < N;
-    const int e = valid ? ids[i] : -1;
+    const int e = valid ? __ldcg(ids + i) : -1;
     const unsigned same = __match_any_sync(kFull, e);
     const int rank = __popc(same & ((1u << lane) - 1u));
     for (int q = tid; q < kAlignWarps * E; q += kAlignThreads) wbase[q] = 0;
@@ -157,6 +173,8 @@ __global__ void __launch_bounds__(kAlignThreads)
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ h, const int32_t* __restrict__ sorted_ids,
                                                      const int32_t* __restrict__ offsets, int E, int N, int k, int H,
                                                      int64_t P_max, uint16_t* __restrict__ xg) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t p = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (p >= P_max || p >= offsets[E]) return;
@@ -168,6 +186,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
     for (int c = lane; c < nch; c += 32) dst[c] = z;
   } else {
     const uint4* s = reinterpret_cast<const uint4*>(h + static_cast<int64_t>(src / k) * H);
+#pragma unroll 4
     for (int c = lane; c < nch; c += 32) dst[c] = __ldg(s + c);
   }
 }
@@ -192,19 +211,35 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ rows, const int32_t* __restrict__ slot_of,
                                                       const float* __restrict__ w, int T, int H, int k,
                                                       uint16_t* __restrict__ y) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int t = blockIdx.x;
   const int nch = H >> 3;
   for (int c = threadIdx.x; c < nch; c += blockDim.x) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      const int slot = slot_of[static_cast<int64_t>(t) * k + j];
-      const float wj = w[static_cast<int64_t>(t) * k + j];
-      float f[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(slot) * H) + c), f);
+    // up to 8 routed rows' loads in flight, then accumulated in j order
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint4 v[8];
+      float wj[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+      for (int d = 0; d < 8; ++d) {
+        if (j0 + d < k) {
+          const int slot = slot_of[static_cast<int64_t>(t) * k + j0 + d];
+          wj[d] = w[static_cast<int64_t>(t) * k + j0 + d];
+          v[d] = __ldg(reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(slot) * H) + c);
+        }
+      }
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        if (j0 + d < k) {
+          float f[8];
+          unpack8(v[d], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[d], f[i], acc[i]);
+        }
+      }
     }
     uint4 o;
     o.x = pack2_bf16(acc[0], acc[1]);
@@ -217,37 +252,59 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 
 }  // namespace
 
-cudaError_t launch_align(const int32_t* topk_ids, int N, int E, int pad, int bn1, int tiles1, int bn2, int tiles2,
-                         int32_t* counts, int32_t* offsets, int32_t* sorted_ids, int32_t* slot_of,
-                         int32_t* unit_off1, int32_t* unit_off2, int32_t* err, cudaStream_t stream) {
+template <int VPL>
+cudaError_t launch_align_t(const float* logits, int T, int k, int renorm, int32_t* topk_ids, float* topk_w, int N,
+                           int E, int pad, int bn1, int tiles1, int bn2, int tiles2, int32_t* counts, int32_t* offsets,
+                           int32_t* sorted_ids, int32_t* slot_of, int32_t* unit_off1, int32_t* unit_off2,
+                           int32_t* err, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(2 + kAlignWarps) * E * sizeof(int);
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    const cudaError_t e =
+        cudaFuncSetAttribute(align_kernel<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  align_kernel<<<1, kAlignThreads, smem, stream>>>(topk_ids, N, E, pad, bn1, tiles1, bn2, tiles2, counts, offsets,
-                                                   sorted_ids, slot_of, unit_off1, unit_off2, err);
-  return cudaGetLastError();
+  return launch_pdl(align_kernel<VPL>, dim3(1), dim3(kAlignThreads), smem, stream, logits, T, k, renorm, topk_w,
+                    topk_ids, N, E, pad, bn1, tiles1, bn2, tiles2, counts, offsets, sorted_ids, slot_of, unit_off1,
+                    unit_off2, err);
 }
+
+
+bool align_fuses_topk(int T, int E) { return T <= kFusedTopkMaxT && E <= kFusedTopkMaxE; }
+
+cudaError_t launch_align(const float* logits, int T, int k, int renorm, int32_t* topk_ids, float* topk_w, int N,
+                         int E, int pad, int bn1, int tiles1, int bn2, int tiles2, int32_t* counts, int32_t* offsets,
+                         int32_t* sorted_ids, int32_t* slot_of, int32_t* unit_off1, int32_t* unit_off2, int32_t* err,
+                         cudaStream_t stream) {
+#define MOE_ALIGN_ARGS logits, T, k, renorm, topk_ids, topk_w, N, E, pad, bn1, tiles1, bn2, tiles2, counts, offsets, \
+                       sorted_ids, slot_of, unit_off1, unit_off2, err, stream
+  if (!align_fuses_topk(T, E)) return launch_align_t<0>(MOE_ALIGN_ARGS);
+  switch (topk_vpl(E)) {
+    case 1: return launch_align_t<1>(MOE_ALIGN_ARGS);
+    case 2: return launch_align_t<2>(MOE_ALIGN_ARGS);
+    case 4: return launch_align_t<4>(MOE_ALIGN_ARGS);
+    default: return launch_align_t<8>(MOE_ALIGN_ARGS);
+  }
+#undef MOE_ALIGN_ARGS
+}
+
 
 cudaError_t launch_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets, int E, int N, int k,
                           int H, int64_t P_max, uint16_t* xg, cudaStream_t stream) {
   const int64_t blocks = (P_max + 7) / 8;
   if (blocks == 0) return cudaSuccess;
-  gather_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(h, sorted_ids, offsets, E, N, k, H, P_max, xg);
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, h, sorted_ids, offsets, E,
+                    N, k, H, P_max, xg);
 }
 
 cudaError_t launch_combine(const uint16_t* out_rows, const int32_t* slot_of, const float* topk_w, int T, int H, int k,
                            uint16_t* y, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int threads = (H / 8 >= 256) ? 256 : ((H / 8 + 31) / 32 * 32);
-  combine_kernel<<<T, threads, 0, stream>>>(out_rows, slot_of, topk_w, T, H, k, y);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(T), dim3(threads), 0, stream, out_rows, slot_of, topk_w, T, H, k, y);
 }
 
 }  // namespace moe

@@ -13,15 +13,17 @@
 //
 // Gate/up: W13[e] holds W_gate^T in rows [0, I) and W_up^T in rows [I, 2I) (the
 // concatenated (d x 2 d_ff) weight of "4 · La fusion de noyaux", §4.2
-// "GEMM + GEMM").  A unit loads the gate rows [i0, i0+128) and the matching up
-// rows [I+i0, I+i0+128) and issues two MMAs per K step into two TMEM column
-// ranges, so TMEM lane l holds gate and up of feature i0+l for every token:
-// the epilogue applies SiLU(gate) * up to the accumulators before the only
-// store ("GEMM + épilogue", §4.2).
+// "GEMM + GEMM").  A unit stacks the gate rows [i0, i0+64) on the matching up
+// rows [I+i0, I+i0+64) into one 128-row A tile, so one MMA per K step leaves
+// gate(i0+l) in TMEM lane l and up(i0+l) in lane 64+l.  The epilogue warp
+// reading lanes 64..127 hands its up values through shared memory to the warp
+// reading lanes 0..63, which applies SiLU(gate) * up to the accumulators
+// before the only store ("GEMM + épilogue", §4.2).
 //
 // Roles in a CTA of 192 threads (persistent, one CTA per SM):
-//   warp 0 lane 0   TMA producer: weight tiles [128 x 64] and token tiles
-//                   [16 x 64] per box, 128-byte swizzle, into a STAGES-deep ring
+//   warp 0 lane 0   TMA producer: weight tiles [128 x 64] (gate/up: two boxes
+//                   of 64 rows) and token tiles of TOKBOX rows per box, 128-byte
+//                   swizzle, into a STAGES-deep ring
 //   warp 1          owns the TMEM allocation; lane 0 issues tcgen05.mma and
 //                   tcgen05.commit (frees a ring slot / hands an accumulator
 //                   buffer to the epilogue)
@@ -33,6 +35,7 @@
 #include <cuda_bf16.h>
 
 #include "moe_kernels.cuh"
+#include "pdl.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -44,21 +47,25 @@ constexpr int kGemmThreads = 192;
 constexpr int kABytes = kWeightBoxRows * kBlockK * 2;  // 16 KB weight tile per stage
 constexpr int kTokRowBytes = kBlockK * 2;              // 128 B per token row per stage
 
-template <bool SWIGLU, int BN, int STAGES>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX>
 struct GemmCfg {
-  static constexpr int NA = SWIGLU ? 2 : 1;
   static constexpr int kBBytes = BN * kTokRowBytes;
-  static constexpr int kStageBytes = NA * kABytes + kBBytes;
-  static constexpr int kAccCols = SWIGLU ? 2 * BN : BN;  // fp32 TMEM columns per accumulator buffer
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kAccCols = BN;  // fp32 TMEM columns per accumulator buffer
   static constexpr int kTmemNeed = 2 * kAccCols;
   static constexpr uint32_t kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                         : kTmemNeed <= 256 ? 256 : 512;
-  static constexpr int kBarBytes = 256;
-  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes;
-  static_assert(BN % kTokBoxRows == 0 && BN >= 16 && BN <= 256, "token tile");
+  // gate/up hand-off: 2 warp pairs x 2 slots x [16 columns][32 lanes] fp32
+  static constexpr int kXchgFloats = 16 * 32;
+  static constexpr int kXchgBytes = SWIGLU ? 2 * 2 * kXchgFloats * 4 : 0;
+  static constexpr int kBarBytes = 512;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kXchgBytes + kBarBytes;
+  static constexpr int kFeatPerTile = SWIGLU ? 64 : 128;  // output features per unit
+  static_assert(BN % TOKBOX == 0 && TOKBOX % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
   static_assert(kTmemNeed <= 512, "TMEM has 512 columns");
-  static_assert((2 * STAGES + 5) * 8 + 8 <= kBarBytes, "barrier area");
+  static_assert((2 * STAGES + 5 + 8) * 8 + 8 <= kBarBytes, "barrier area");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
 struct Unit {
@@ -95,19 +102,22 @@ __device__ __forceinline__ void raise_timeout(int32_t* err, volatile int* abort_
 
 __device__ __forceinline__ uint16_t f2bf(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
-template <bool SWIGLU, int BN, int STAGES>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const ExpertGemmArgs args) {
-  using C = GemmCfg<SWIGLU, BN, STAGES>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
+  float* xchg = reinterpret_cast<float*>(smem + STAGES * C::kStageBytes);  // [pair][slot][16][32] (gate/up)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes + C::kXchgBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* xfull = done + 1;   // [pair][slot]: up values written
+  uint64_t* xempty = xfull + 4; // [pair][slot]: up values consumed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xempty + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -123,6 +133,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tempty[b], 4);
     }
     mbar_init(done, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&xfull[i], 1);
+      mbar_init(&xempty[i], 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -135,6 +149,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // everything above touched only on-chip state; from here on the routing
+  // tables and token rows of the previous kernels are read
+  pdl_launch_dependents();
+  pdl_wait();
   const int total_units = __ldg(args.unit_off + args.E);
   const int kblocks = args.K / kBlockK;
 
@@ -143,16 +161,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // ---------------- TMA producer
       prefetch_tensormap(&tm_w);
       prefetch_tensormap(&tm_x);
-      const uint64_t pol_w = policy_evict_first();  // weight tiles: streamed, each read by few CTAs
-      const uint64_t pol_x = policy_evict_last();   // token tiles: re-read by every weight tile
+      // A weight tile is read by every token chunk of its expert: streamed once
+      // (evict first) when the expert's tokens fit one chunk, kept (evict last)
+      // when more chunks will read it.  Token tiles are re-read by every
+      // weight tile of their expert.
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_keep = policy_evict_last();
+      const uint64_t pol_x = pol_keep;
       int stage = 0;
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
         const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
-        const int wrow = un.e * args.w_rows_per_expert + un.tile * kWeightBoxRows;
-        const uint32_t bytes = C::NA * kABytes + un.n * kTokRowBytes;
+        const int wrow = un.e * args.w_rows_per_expert + un.tile * C::kFeatPerTile;
+        const int tok_rows = (un.n + TOKBOX - 1) / TOKBOX * TOKBOX;  // whole boxes; rows past n are unused
+        const bool reused = __ldg(args.offsets + un.e + 1) - __ldg(args.offsets + un.e) > BN;
+        const uint64_t pol_w = reused ? pol_keep : pol_stream;
+        const uint32_t bytes = kABytes + tok_rows * kTokRowBytes;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitTimeoutNs, abort_flag)) {
             ok = false;
@@ -160,10 +186,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           uint8_t* sa = smem + stage * C::kStageBytes;
           mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(sa, &tm_w, &full[stage], kb * kBlockK, wrow, pol_w);
-          if (SWIGLU) tma_load_2d(sa + kABytes, &tm_w, &full[stage], kb * kBlockK, wrow + args.up_offset, pol_w);
-          uint8_t* sb = sa + C::NA * kABytes;
-          for (int r = 0; r < un.n; r += kTokBoxRows)
+          if (SWIGLU) {  // gate rows on top of the matching up rows
+            tma_load_2d(sa, &tm_w, &full[stage], kb * kBlockK, wrow, pol_w);
+            tma_load_2d(sa + kABytes / 2, &tm_w, &full[stage], kb * kBlockK, wrow + args.up_offset, pol_w);
+          } else {
+            tma_load_2d(sa, &tm_w, &full[stage], kb * kBlockK, wrow, pol_w);
+          }
+          uint8_t* sb = sa + kABytes;
+          for (int r = 0; r < tok_rows; r += TOKBOX)
             tma_load_2d(sb + r * kTokRowBytes, &tm_x, &full[stage], kb * kBlockK, un.tok0 + r, pol_x);
           ++issued;
           if (++stage == STAGES) {
@@ -197,7 +227,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(un.n));
-        const uint32_t d_gate = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
+        const uint32_t d_acc = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&full[stage], phase, kWaitTimeoutNs, abort_flag)) {
             ok = false;
@@ -205,13 +235,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
-          const uint32_t sb = sa + C::NA * kABytes;
+          const uint32_t sb = sa + kABytes;
 #pragma unroll
           for (int k = 0; k < kBlockK / 16; ++k) {
-            const uint64_t bdesc = sdesc_kmajor_sw128(sb + k * 32);
             const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-            mma_bf16_ss(d_gate, sdesc_kmajor_sw128(sa + k * 32), bdesc, idesc, accum);
-            if (SWIGLU) mma_bf16_ss(d_gate + BN, sdesc_kmajor_sw128(sa + kABytes + k * 32), bdesc, idesc, accum);
+            mma_bf16_ss(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc, accum);
           }
           mma_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -235,8 +263,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t xit = 0;  // gate/up hand-off counter (slot = xit & 1)
     bool ok = true;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    // gate/up: quarters 0,1 hold gate of features +0..31 / +32..63, quarters
+    // 2,3 the matching up values; pair p = q & 1 joins quarter p and p + 2
+    const int pair = q & 1;
+    const bool gate_warp = q < 2;
+    float* xb = xchg + pair * 2 * C::kXchgFloats;
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
       const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
       // warp-uniform outcome: tcgen05.ld below must be executed by all 32 lanes
       const bool got = mbar_wait(&tfull[acc], acc_phase, kWaitTimeoutNs, abort_flag);
@@ -245,23 +279,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
-      const int feat = un.tile * kWeightBoxRows + q * 32 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * C::kAccCols);
-      uint16_t* out = args.out + static_cast<int64_t>(un.tok0) * args.n_out + feat;
-      for (int c0 = 0; c0 < un.n; c0 += 16) {
-        uint32_t ra[16], rb[16];
-        tmem_ld_32x32b_x16(t_row + c0, ra);
-        if (SWIGLU) tmem_ld_32x32b_x16(t_row + BN + c0, rb);
-        tmem_ld_wait();
+      if (!SWIGLU) {
+        const int feat = un.tile * C::kFeatPerTile + q * 32 + lane;
+        uint16_t* out = args.out + static_cast<int64_t>(un.tok0) * args.n_out + feat;
+        for (int c0 = 0; c0 < un.n; c0 += 16) {
+          uint32_t ra[16];
+          tmem_ld_32x32b_x16(t_row + c0, ra);
+          tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          float v = __uint_as_float(ra[j]);
-          if (SWIGLU) {
-            const float up = __uint_as_float(rb[j]);
-            v = v / (1.0f + __expf(-v)) * up;
-          }
-          out[static_cast<int64_t>(c0 + j) * args.n_out] = f2bf(v);
+          for (int j = 0; j < 16; ++j) out[static_cast<int64_t>(c0 + j) * args.n_out] = f2bf(__uint_as_float(ra[j]));
         }
+      } else {
+        const int feat = un.tile * C::kFeatPerTile + pair * 32 + lane;
+        uint16_t* out = args.out + static_cast<int64_t>(un.tok0) * args.n_out + feat;
+        for (int c0 = 0; c0 < un.n && ok; c0 += 16, ++xit) {
+          const int slot = xit & 1;
+          const uint32_t par = (xit >> 1) & 1u;
+          float* xs = xb + slot * C::kXchgFloats;
+          uint32_t ra[16];
+          tmem_ld_32x32b_x16(t_row + c0, ra);
+          tmem_ld_wait();
+          if (!gate_warp) {
+            // hand the up values of these 16 tokens to the gate warp
+            const bool free_slot = mbar_wait(&xempty[pair * 2 + slot], par ^ 1u, kWaitTimeoutNs, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, free_slot)) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xs[j * 32 + lane] = __uint_as_float(ra[j]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xfull[pair * 2 + slot]);
+          } else {
+            const bool have = mbar_wait(&xfull[pair * 2 + slot], par, kWaitTimeoutNs, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, have)) {
+              ok = false;
+              break;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float g = __uint_as_float(ra[j]);
+              const float up = xs[j * 32 + lane];
+              const float a = __fdividef(g, 1.0f + __expf(-g)) * up;  // SiLU(gate) * up
+              out[static_cast<int64_t>(c0 + j) * args.n_out] = f2bf(a);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xempty[pair * 2 + slot]);
+          }
+        }
+        if (!ok) break;
       }
       tc_fence_before();
       __syncwarp();
@@ -279,45 +346,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-template <bool SWIGLU, int BN, int STAGES>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX>
 cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, int num_sms,
                                cudaStream_t stream) {
-  using C = GemmCfg<SWIGLU, BN, STAGES>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX>;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(expert_gemm_kernel<SWIGLU, BN, STAGES>,
+    cudaError_t e = cudaFuncSetAttribute(expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  expert_gemm_kernel<SWIGLU, BN, STAGES><<<num_sms, kGemmThreads, C::kSmemBytes, stream>>>(tw, tx, a);
-  return cudaGetLastError();
+  return launch_pdl(expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX>, dim3(num_sms), dim3(kGemmThreads),
+                    C::kSmemBytes,
+                    stream, tw, tx, a);
 }
 
-constexpr int kGateUpBnDecode = 64, kGateUpStagesDecode = 5;
-constexpr int kGateUpBnPrefill = 128, kGateUpStagesPrefill = 4;
-constexpr int kDownBnDecode = 64, kDownStagesDecode = 8;
-constexpr int kDownBnPrefill = 256, kDownStagesPrefill = 4;
+// Three tile plans by the expected tokens per expert (T*top_k/E):
+//   small (<= 16): 32-token units, deep weight pipelines (decode);
+//   mid   (<= 64): 64-token units, so most experts still fit one chunk;
+//   large (> 64) : 128 / 256-token units and 64-row token boxes (prefill).
+constexpr int kGateUpBn[3] = {32, 64, 256}, kGateUpStages[3] = {10, 8, 4};  // stages of 20 / 24 / 48 KB
+constexpr int kDownBn[3] = {32, 64, 256}, kDownStages[3] = {10, 8, 4};      // stages of 20 / 24 / 48 KB
+// token rows per TMA box: small units hold few tokens (16-row boxes waste
+// nothing); large units hold 128-256 (64-row boxes: 4x fewer TMA requests)
+constexpr int kTokBox[3] = {16, 16, 64};
 
 }  // namespace
 
-int gemm_gate_up_bn(GemmPlan plan) { return plan == GemmPlan::kDecode ? kGateUpBnDecode : kGateUpBnPrefill; }
-int gemm_down_bn(GemmPlan plan) { return plan == GemmPlan::kDecode ? kDownBnDecode : kDownBnPrefill; }
+int gemm_gate_up_bn(GemmPlan plan) { return kGateUpBn[static_cast<int>(plan)]; }
+int gemm_down_bn(GemmPlan plan) { return kDownBn[static_cast<int>(plan)]; }
+int gemm_tok_box_rows(GemmPlan plan) { return kTokBox[static_cast<int>(plan)]; }
 
 cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
                                 GemmPlan plan, int num_sms, cudaStream_t stream) {
-  if (plan == GemmPlan::kDecode)
-    return launch_expert_gemm<true, kGateUpBnDecode, kGateUpStagesDecode>(tm_w13, tm_x, a, num_sms, stream);
-  return launch_expert_gemm<true, kGateUpBnPrefill, kGateUpStagesPrefill>(tm_w13, tm_x, a, num_sms, stream);
+  switch (plan) {
+    case GemmPlan::kSmall:
+      return launch_expert_gemm<true, kGateUpBn[0], kGateUpStages[0], kTokBox[0]>(tm_w13, tm_x, a, num_sms, stream);
+    case GemmPlan::kMid:
+      return launch_expert_gemm<true, kGateUpBn[1], kGateUpStages[1], kTokBox[1]>(tm_w13, tm_x, a, num_sms, stream);
+    default:
+      return launch_expert_gemm<true, kGateUpBn[2], kGateUpStages[2], kTokBox[2]>(tm_w13, tm_x, a, num_sms, stream);
+  }
 }
 
 cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const ExpertGemmArgs& a,
                              GemmPlan plan, int num_sms, cudaStream_t stream) {
-  if (plan == GemmPlan::kDecode)
-    return launch_expert_gemm<false, kDownBnDecode, kDownStagesDecode>(tm_w2, tm_act, a, num_sms, stream);
-  return launch_expert_gemm<false, kDownBnPrefill, kDownStagesPrefill>(tm_w2, tm_act, a, num_sms, stream);
+  switch (plan) {
+    case GemmPlan::kSmall:
+      return launch_expert_gemm<false, kDownBn[0], kDownStages[0], kTokBox[0]>(tm_w2, tm_act, a, num_sms, stream);
+    case GemmPlan::kMid:
+      return launch_expert_gemm<false, kDownBn[1], kDownStages[1], kTokBox[1]>(tm_w2, tm_act, a, num_sms, stream);
+    default:
+      return launch_expert_gemm<false, kDownBn[2], kDownStages[2], kTokBox[2]>(tm_w2, tm_act, a, num_sms, stream);
+  }
 }
 
 }  // namespace moe

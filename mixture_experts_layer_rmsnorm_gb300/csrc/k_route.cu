@@ -20,6 +20,8 @@
 #include <climits>
 
 #include "moe_kernels.cuh"
+#include "pdl.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -51,7 +53,7 @@ __device__ __forceinline__ float warp_butterfly_sum(float v) {
 // grid = (ceil(T / TT), ceil(E / experts_per_cta)), block = 256, dyn smem = TT*H*2.
 // Each warp computes TE experts x TT tokens at a time.
 template <int TT, int TE>
-__global__ void __launch_bounds__(kRouteWarps * 32)
+__global__ void __launch_bounds__(kRouteWarps * 32, 1)
     norm_router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g,
                        const float* __restrict__ w_router, const float* __restrict__ bias, int T, int H, int E,
                        float eps, int experts_per_cta, uint16_t* __restrict__ h_out, float* __restrict__ logits,
@@ -62,6 +64,21 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   const int t0 = blockIdx.x * TT;
   const int e0 = blockIdx.y * experts_per_cta;
 
+  pdl_launch_dependents();
+  // The router rows this CTA will need and the norm gain do not depend on the
+  // previous kernel: start pulling them into L2 now, so that their DRAM
+  // latency overlaps the RMSNorm below.
+  {
+    const int e_hi = min(E, e0 + experts_per_cta);
+    const char* wb = reinterpret_cast<const char*>(w_router + static_cast<size_t>(e0) * H);
+    const size_t wbytes = static_cast<size_t>(max(e_hi - e0, 0)) * H * 4;
+    for (size_t off = static_cast<size_t>(threadIdx.x) * 128; off < wbytes; off += 128 * blockDim.x)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(wb + off));
+    const char* gb = reinterpret_cast<const char*>(g);
+    for (int off = threadIdx.x * 128; off < H * 2; off += 128 * blockDim.x)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(gb + off));
+  }
+  pdl_wait();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 4) err[threadIdx.x] = 0;
 
   // ---- RMSNorm: one warp per token
@@ -70,7 +87,21 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     if (t >= T) break;
     const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
     float ss = 0.0f;
-    for (int c = lane; c < nch; c += 32) {
+    int c = lane;
+    // 8 chunks' loads in flight, then their FMAs in chunk order
+    for (; c + 32 * 7 < nch; c += 32 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int d = 0; d < 8; ++d) v[d] = __ldg(xr + c + 32 * d);
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        float f[8];
+        unpack8(v[d], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = __fmaf_rn(f[i], f[i], ss);
+      }
+    }
+    for (; c < nch; c += 32) {
       float f[8];
       unpack8(__ldg(xr + c), f);
 #pragma unroll
@@ -81,6 +112,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
     const uint4* gr = reinterpret_cast<const uint4*>(g);
     uint4* hrow = reinterpret_cast<uint4*>(h_out + static_cast<size_t>(t) * H);
+#pragma unroll 4
     for (int c = lane; c < nch; c += 32) {
       float f[8], gg[8];
       unpack8(__ldg(xr + c), f);
@@ -111,7 +143,36 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
       const int e = min(eg + b, E - 1);  // clamp: a tail expert's duplicate is computed but not stored
       wrow[b] = reinterpret_cast<const float4*>(w_router + static_cast<size_t>(e) * H);
     }
-    for (int c = lane; c < nch; c += 32) {
+    // DEPTH chunks of router weights in flight per lane, consumed in chunk
+    // order, so every accumulator keeps the canonical sequence
+    constexpr int DEPTH = (TE >= 4) ? 2 : (TE == 2 ? 4 : 8);
+    int c = lane;
+    for (; c + 32 * (DEPTH - 1) < nch; c += 32 * DEPTH) {
+      float4 wv[DEPTH][TE][2];
+#pragma unroll
+      for (int d = 0; d < DEPTH; ++d)
+#pragma unroll
+        for (int b = 0; b < TE; ++b) {
+          wv[d][b][0] = __ldg(wrow[b] + 2 * (c + 32 * d));
+          wv[d][b][1] = __ldg(wrow[b] + 2 * (c + 32 * d) + 1);
+        }
+#pragma unroll
+      for (int d = 0; d < DEPTH; ++d) {
+#pragma unroll
+        for (int a = 0; a < TT; ++a) {
+          float hv[8];
+          unpack8(h_s[a * nch + c + 32 * d], hv);
+#pragma unroll
+          for (int b = 0; b < TE; ++b) {
+            const float w[8] = {wv[d][b][0].x, wv[d][b][0].y, wv[d][b][0].z, wv[d][b][0].w,
+                                wv[d][b][1].x, wv[d][b][1].y, wv[d][b][1].z, wv[d][b][1].w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[a][b] = __fmaf_rn(hv[i], w[i], acc[a][b]);
+          }
+        }
+      }
+    }
+    for (; c < nch; c += 32) {
       float w[TE][8];
 #pragma unroll
       for (int b = 0; b < TE; ++b) {
@@ -143,69 +204,17 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   }
 }
 
-// one warp per token; block = 256 (8 tokens).  E <= 1024, k <= 32.
+// one warp per token; block = 256 (8 tokens).  E <= 32 * VPL, k <= 32.
+template <int VPL>
 __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                            int renorm, int32_t* __restrict__ topk_ids,
                                                            float* __restrict__ topk_w) {
-  const int lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  pdl_wait();
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
-  const float* l = logits + static_cast<size_t>(t) * E;
-  float v[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = (e < E) ? l[e] : -FLT_MAX;
-  }
-  uint32_t taken = 0;
-  float my_v = 0.0f;  // lane j keeps the j-th selection
-  int my_e = 0;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = INT_MAX;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
-        bv = v[i];
-        be = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, bv, off);
-      const int oe = __shfl_xor_sync(kFull, be, off);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == j) {
-      my_v = bv;
-      my_e = be;
-    }
-  }
-  const float m = __shfl_sync(kFull, my_v, 0);  // the largest logit
-  float denom;
-  if (renorm) {
-    float s = (lane < k) ? expf(my_v - m) : 0.0f;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
-    denom = s;
-  } else {
-    float s = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (lane + 32 * i < E) s += expf(v[i] - m);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(kFull, s, off);
-    denom = s;
-  }
-  if (lane < k) {
-    topk_ids[static_cast<size_t>(t) * k + lane] = my_e;
-    topk_w[static_cast<size_t>(t) * k + lane] = expf(my_v - m) / denom;
-  }
+  topk_softmax_warp<VPL>(logits + static_cast<size_t>(t) * E, E, k, renorm, topk_ids + static_cast<size_t>(t) * k,
+                         topk_w + static_cast<size_t>(t) * k);
 }
 
 template <int TT, int TE>
@@ -223,14 +232,13 @@ cudaError_t launch_nr(const uint16_t* x, const uint16_t* g, const float* wr, con
   }
   const int tiles = (T + TT - 1) / TT;
   const int group = kRouteWarps * TE;
-  // few token tiles: one expert group per CTA to spread the router weights over
-  // many SMs; many token tiles: all experts per CTA so Wr is read once per tile
+  // one expert group per CTA spreads the work (and the router weights) over
+  // many SMs; only with very many token tiles does a CTA take all experts
   int epc = group;
-  if (static_cast<long long>(tiles) * ((E + group - 1) / group) > 4LL * num_sms) epc = (E + group - 1) / group * group;
+  if (static_cast<long long>(tiles) * ((E + group - 1) / group) > 16LL * num_sms) epc = (E + group - 1) / group * group;
   dim3 grid(tiles, (E + epc - 1) / epc);
-  norm_router_kernel<TT, TE><<<grid, kRouteWarps * 32, smem, stream>>>(x, g, wr, bias, T, H, E, eps, epc, h,
-                                                                        logits, err);
-  return cudaGetLastError();
+  return launch_pdl(norm_router_kernel<TT, TE>, grid, dim3(kRouteWarps * 32), smem, stream, x, g, wr, bias, T, H, E,
+                    eps, epc, h, logits, err);
 }
 
 }  // namespace
@@ -246,8 +254,18 @@ cudaError_t launch_norm_router(const uint16_t* x, const uint16_t* g, const float
 
 cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int renorm, int32_t* topk_ids,
                                 float* topk_w, cudaStream_t stream) {
-  topk_softmax_kernel<<<(T + 7) / 8, 256, 0, stream>>>(logits, T, E, k, renorm, topk_ids, topk_w);
-  return cudaGetLastError();
+  const dim3 grid((T + 7) / 8), block(256);
+  switch (topk_vpl(E)) {
+    case 1: return launch_pdl(topk_softmax_kernel<1>, grid, block, 0, stream, logits, T, E, k, renorm, topk_ids, topk_w);
+    case 2: return launch_pdl(topk_softmax_kernel<2>, grid, block, 0, stream, logits, T, E, k, renorm, topk_ids, topk_w);
+    case 4: return launch_pdl(topk_softmax_kernel<4>, grid, block, 0, stream, logits, T, E, k, renorm, topk_ids, topk_w);
+    case 8: return launch_pdl(topk_softmax_kernel<8>, grid, block, 0, stream, logits, T, E, k, renorm, topk_ids, topk_w);
+    case 16:
+      return launch_pdl(topk_softmax_kernel<16>, grid, block, 0, stream, logits, T, E, k, renorm, topk_ids, topk_w);
+    default:
+      return launch_pdl(topk_softmax_kernel<32>, grid, block, 0, stream, logits, T, E, k, renorm, topk_ids, topk_w);
+  }
 }
+
 
 }  // namespace moe

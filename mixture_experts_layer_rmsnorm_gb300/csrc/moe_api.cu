@@ -5,8 +5,9 @@
 // Plan ("CuTeDSL chez Perplexity", "Pré-remplir et décoder la
 // spécialisation": kernels are split into prefill and decode variants by
 // token count, hidden size and dtype).  The expected tokens per expert
-// T*top_k/E decides: <= 64 takes the decode tiles (64 tokens per unit, deep
-// weight pipelines), above it the prefill tiles (128 / 256 tokens per unit).
+// T*top_k/E picks the expert-GEMM tiles: <= 16 small (32 tokens per unit,
+// deepest weight pipelines), <= 64 mid (64 tokens per unit), above that the
+// prefill tiles (128 / 256 tokens per unit).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -140,11 +141,13 @@ moe_status run_front(const moe_shape& s, const Layout& L, const moe_bf16* x, con
   if (moe::launch_norm_router(x, g, wr, bias, s.T, s.H, s.E, s.eps, at<uint16_t>(ws, L.h), at<float>(ws, L.logits),
                               err, num_sms, st) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (moe::launch_topk_softmax(at<float>(ws, L.logits), s.T, s.E, s.top_k, s.renormalize, at<int32_t>(ws, L.ids),
-                               at<float>(ws, L.w), st) != cudaSuccess)
+  const bool fused = moe::align_fuses_topk(s.T, s.E);
+  if (!fused && moe::launch_topk_softmax(at<float>(ws, L.logits), s.T, s.E, s.top_k, s.renormalize,
+                                         at<int32_t>(ws, L.ids), at<float>(ws, L.w), st) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (moe::launch_align(at<int32_t>(ws, L.ids), s.T * s.top_k, s.E, pad, bn1, s.I / moe::kWeightBoxRows, bn2,
-                        s.H / moe::kWeightBoxRows, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+  if (moe::launch_align(at<float>(ws, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(ws, L.ids),
+                        at<float>(ws, L.w), s.T * s.top_k, s.E, pad, bn1, s.I / moe::kGateUpTileFeat, bn2,
+                        s.H / moe::kDownTileFeat, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                         at<int32_t>(ws, L.sorted), at<int32_t>(ws, L.slot), bn1 > 0 ? at<int32_t>(ws, L.unit1) : nullptr,
                         bn2 > 0 ? at<int32_t>(ws, L.unit2) : nullptr, err, st) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -205,17 +208,17 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   const int num_sms = num_sms_of_current_device();
   if (num_sms <= 0) return MOE_ERR_CUDA;
   const Layout L = make_layout(s);
-  const GemmPlan plan = (static_cast<int64_t>(s.T) * s.top_k <= 64LL * s.E) ? GemmPlan::kDecode : GemmPlan::kPrefill;
+  const GemmPlan plan = moe::choose_plan(s.T, s.top_k, s.E);
   const int bn1 = moe::gemm_gate_up_bn(plan), bn2 = moe::gemm_down_bn(plan);
   auto mark = [&](int i) {
     return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), cs) == cudaSuccess;
   };
 
   CUtensorMap tm_w13, tm_xg, tm_w2, tm_act;
-  if (!make_map(&tm_w13, w13, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, moe::kWeightBoxRows) ||
-      !make_map(&tm_xg, at<void>(workspace, L.xg), s.H, L.P_max, moe::kTokBoxRows) ||
+  if (!make_map(&tm_w13, w13, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, moe::kWeightBoxRows / 2) ||
+      !make_map(&tm_xg, at<void>(workspace, L.xg), s.H, L.P_max, moe::gemm_tok_box_rows(plan)) ||
       !make_map(&tm_w2, w2, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows) ||
-      !make_map(&tm_act, at<void>(workspace, L.act), s.I, L.P_max, moe::kTokBoxRows))
+      !make_map(&tm_act, at<void>(workspace, L.act), s.I, L.P_max, moe::gemm_tok_box_rows(plan)))
     return MOE_ERR_CUDA;
 
   int32_t* err = at<int32_t>(workspace, L.err);
@@ -223,15 +226,18 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   if (moe::launch_norm_router(x, g_norm, w_router, router_bias, s.T, s.H, s.E, s.eps, at<uint16_t>(workspace, L.h),
                               at<float>(workspace, L.logits), err, num_sms, cs) != cudaSuccess || !mark(1))
     return MOE_ERR_CUDA;
-  if (moe::launch_topk_softmax(at<float>(workspace, L.logits), s.T, s.E, s.top_k, s.renormalize,
-                               at<int32_t>(workspace, L.ids), at<float>(workspace, L.w), cs) != cudaSuccess ||
-      !mark(2))
+  // top-k runs in its own kernel for large T, inside the align kernel for small T
+  const bool fused = moe::align_fuses_topk(s.T, s.E);
+  if (!fused && moe::launch_topk_softmax(at<float>(workspace, L.logits), s.T, s.E, s.top_k, s.renormalize,
+                                         at<int32_t>(workspace, L.ids), at<float>(workspace, L.w), cs) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (!mark(2)) return MOE_ERR_CUDA;
   const int N = s.T * s.top_k;
-  if (moe::launch_align(at<int32_t>(workspace, L.ids), N, s.E, moe::kPadRows, bn1, s.I / moe::kWeightBoxRows, bn2,
-                        s.H / moe::kWeightBoxRows, at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.offsets),
-                        at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.slot),
-                        at<int32_t>(workspace, L.unit1), at<int32_t>(workspace, L.unit2), err, cs) != cudaSuccess ||
+  if (moe::launch_align(at<float>(workspace, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(workspace, L.ids), at<float>(workspace, L.w), N, s.E, moe::kPadRows, bn1,
+                        s.I / moe::kGateUpTileFeat, bn2, s.H / moe::kDownTileFeat, at<int32_t>(workspace, L.counts),
+                        at<int32_t>(workspace, L.offsets), at<int32_t>(workspace, L.sorted),
+                        at<int32_t>(workspace, L.slot), at<int32_t>(workspace, L.unit1), at<int32_t>(workspace, L.unit2),
+                        err, cs) != cudaSuccess ||
       !mark(3))
     return MOE_ERR_CUDA;
   if (moe::launch_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
@@ -245,7 +251,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a1.unit_off = at<int32_t>(workspace, L.unit1);
   a1.E = s.E;
   a1.K = s.H;
-  a1.tiles_per_expert = s.I / moe::kWeightBoxRows;
+  a1.tiles_per_expert = s.I / moe::kGateUpTileFeat;
   a1.w_rows_per_expert = 2 * s.I;
   a1.up_offset = s.I;
   a1.n_out = s.I;
@@ -258,7 +264,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a2.unit_off = at<int32_t>(workspace, L.unit2);
   a2.E = s.E;
   a2.K = s.I;
-  a2.tiles_per_expert = s.H / moe::kWeightBoxRows;
+  a2.tiles_per_expert = s.H / moe::kDownTileFeat;
   a2.w_rows_per_expert = s.H;
   a2.up_offset = 0;
   a2.n_out = s.H;

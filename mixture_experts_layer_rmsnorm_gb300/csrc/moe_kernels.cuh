@@ -29,10 +29,16 @@ cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int re
 
 // K2: deterministic align: counts, padded offsets, sorted_ids, slot_of and the
 // prefix sums of work units of the two expert GEMMs (units per expert =
-// ceil(P_e / bn) * tiles; bn = 0 skips that table).
-cudaError_t launch_align(const int32_t* topk_ids, int N, int E, int pad, int bn1, int tiles1, int bn2, int tiles2,
-                         int32_t* counts, int32_t* offsets, int32_t* sorted_ids, int32_t* slot_of,
-                         int32_t* unit_off1, int32_t* unit_off2, int32_t* err, cudaStream_t stream);
+// ceil(P_e / bn) * tiles; bn = 0 skips that table).  When
+// align_fuses_topk(T, E), the same single CTA first runs K1b for all T tokens
+// (topk_ids / topk_w from the logits) and K1b must not be launched.
+cudaError_t launch_align(const float* logits, int T, int k, int renorm, int32_t* topk_ids, float* topk_w, int N,
+                         int E, int pad, int bn1, int tiles1, int bn2, int tiles2, int32_t* counts, int32_t* offsets,
+                         int32_t* sorted_ids, int32_t* slot_of, int32_t* unit_off1, int32_t* unit_off2, int32_t* err,
+                         cudaStream_t stream);
+constexpr int kFusedTopkMaxT = 256;
+constexpr int kFusedTopkMaxE = 256;
+bool align_fuses_topk(int T, int E);
 
 // K3: xg[p,:] = h[sorted_ids[p] / k, :] for real rows, zeros for padding rows.
 cudaError_t launch_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets, int E, int N,
@@ -53,7 +59,14 @@ struct ExpertGemmArgs {
   int32_t* err;
 };
 
-enum class GemmPlan { kDecode, kPrefill };
+// tile plan of the expert GEMMs, by the expected tokens per expert
+enum class GemmPlan { kSmall = 0, kMid = 1, kLarge = 2 };
+inline GemmPlan choose_plan(int64_t T, int64_t top_k, int64_t E) {
+  const int64_t tk = T * top_k;
+  if (tk <= 16 * E) return GemmPlan::kSmall;
+  if (tk <= 64 * E) return GemmPlan::kMid;
+  return GemmPlan::kLarge;
+}
 
 // Encodes nothing itself: the tensor maps are built by the caller.
 cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
@@ -63,9 +76,31 @@ cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act
 // token rows per unit (B-operand width) and rows per TMA box of the token tile
 int gemm_gate_up_bn(GemmPlan plan);
 int gemm_down_bn(GemmPlan plan);
-constexpr int kTokBoxRows = 16;
-constexpr int kWeightBoxRows = 128;
+int gemm_tok_box_rows(GemmPlan plan);
+constexpr int kWeightBoxRows = 128;  // A-operand rows of one unit (one MMA's M)
+constexpr int kGateUpTileFeat = 64;  // gate/up unit: 64 gate rows stacked on the matching 64 up rows
+constexpr int kDownTileFeat = 128;   // down unit: 128 rows of W2
 constexpr int kBlockK = 64;
+
+// Launch with programmatic dependent launch allowed: the kernel may be
+// scheduled while the previous kernel in the stream is finishing; it must
+// execute griddepcontrol.wait (pdl_wait) before touching global memory that
+// earlier stream work reads or writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // K6: y[t,:] = bf16(sum_j topk_w[t,j] * out_rows[slot_of[t*k+j], :]).
 cudaError_t launch_combine(const uint16_t* out_rows, const int32_t* slot_of, const float* topk_w, int T, int H,

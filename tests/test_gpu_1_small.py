@@ -27,6 +27,7 @@ CASES = [
     ("prefill_chunks", 1024, 256, 256, 4, 2, True, None, 4),
     ("prefill_ragged_norenorm", 300, 384, 128, 6, 3, False, None, 5),
     ("skewed_bias", 96, 256, 256, 32, 6, True, 1.2, 7),
+    ("mid_multichunk", 200, 256, 256, 8, 2, True, None, 9),
     ("single_expert", 20, 128, 128, 1, 1, True, None, 6),
     ("k_equals_E", 9, 128, 256, 4, 4, True, None, 8),
 ]
