@@ -116,8 +116,10 @@ MOE_API moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const 
 /* The kernels of one moe_forward call, in order:
  *   1 RMSNorm + router logits, 2 top-k + softmax, 3 expert align, 4 gather,
  *   5 gate/up grouped GEMM + SwiGLU, 6 down grouped GEMM, 7 weighted combine.
- * For T <= MOE_FUSED_TOPK_MAX_T and E <= MOE_FUSED_TOPK_MAX_E, step 2 runs
- * inside the align kernel (one launch fewer: MOE_NUM_KERNELS - 1 per call). */
+ * For T <= MOE_FUSED_TOPK_MAX_T and E <= MOE_FUSED_TOPK_MAX_E, steps 2 and 3
+ * run as one single-CTA kernel (6 launches per call); otherwise step 2 is one
+ * multi-CTA kernel (top-k with per-block expert counts) and step 3 two (scan,
+ * scatter), 8 launches per call. */
 #define MOE_NUM_KERNELS 7
 #define MOE_FUSED_TOPK_MAX_T 256
 #define MOE_FUSED_TOPK_MAX_E 256
@@ -126,7 +128,8 @@ MOE_API moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const 
  * events[0] before kernel 1 and events[i] right after kernel i (i = 1..7),
  * so cudaEventElapsedTime(events[i-1], events[i]) is kernel i's time on the
  * stream (with top-k fused into the align kernel, events[2] follows events[1]
- * at once and the align interval includes the top-k).  `events` holds n_events >= MOE_NUM_KERNELS + 1 cudaEvent_t
+ * at once and the align interval includes the top-k; otherwise events[2] ends
+ * the top-k/count kernel and events[3] the scan and scatter kernels).  `events` holds n_events >= MOE_NUM_KERNELS + 1 cudaEvent_t
  * handles created by the caller (cudaEventCreate); the library records them
  * and does not create, wait on or destroy them.  Everything else is as for
  * moe_forward; with T = 0 no event is recorded. */
@@ -168,7 +171,7 @@ MOE_API moe_status moe_route_debug(const moe_shape* shape, const moe_bf16* x, co
  * for moe_forward.
  *   - Shapes whose moe_workspace_size() exceeds MOE_STATIC_SCRATCH_BYTES are
  *     rejected with MOE_ERR_WORKSPACE before anything is enqueued (e.g. the
- *     decode layer H = I = 4096, E = 64, top_k = 8 fits for T <= 211).
+ *     decode layer H = I = 4096, E = 64, top_k = 8 fits for T <= 170).
  *   - The first call on a device (with that device current) looks up the
  *     array's device address once (cudaGetSymbolAddress) and keeps it; make
  *     that first call before any stream capture.

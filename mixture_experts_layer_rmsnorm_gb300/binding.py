@@ -99,8 +99,9 @@ MOE_FUSED_TOPK_MAX_E = 256  # ... and experts
 
 
 def kernels_per_call(T: int, E: int) -> int:
+    """Kernel launches of one moe_forward call (T > 0)."""
     fused = T <= MOE_FUSED_TOPK_MAX_T and E <= MOE_FUSED_TOPK_MAX_E
-    return MOE_NUM_KERNELS - 1 if fused else MOE_NUM_KERNELS
+    return 6 if fused else 8
 KERNEL_NAMES = ("norm_router", "topk_softmax", "align", "gather", "gemm_gate_up_swiglu", "gemm_down", "combine")
 
 

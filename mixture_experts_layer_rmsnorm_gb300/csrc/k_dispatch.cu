@@ -14,6 +14,7 @@
 // run.
 #include <cuda_bf16.h>
 
+#include "block_scan.cuh"
 #include "moe_kernels.cuh"
 #include "pdl.cuh"
 #include "topk.cuh"
@@ -24,37 +25,6 @@ namespace {
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
-
-// Block-wide exclusive scan of one int per thread (1024 threads).  `tmp` is
-// kAlignWarps ints of shared memory.  Returns the exclusive prefix; *total
-// receives the block total.
-__device__ int block_exclusive_scan(int v, int* tmp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(kFull, inc, off);
-    if (lane >= off) inc += o;
-  }
-  if (lane == 31) tmp[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int w = tmp[lane];
-    int winc = w;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(kFull, winc, off);
-      if (lane >= off) winc += o;
-    }
-    tmp[lane] = winc - w;  // exclusive prefix of warp totals
-    if (lane == 31) tmp[kAlignWarps] = winc;
-  }
-  __syncthreads();
-  const int r = tmp[warp] + inc - v;
-  *total = tmp[kAlignWarps];
-  __syncthreads();
-  return r;
-}
 
 // One CTA of 1024 threads.  Dynamic shared memory: cnt[E], cursor[E],
 // wbase[32][E] (ints).  With FUSED_TOPK the CTA first selects the top-k
@@ -68,7 +38,7 @@ __global__ void __launch_bounds__(kAlignThreads)
                  int32_t* ids, int N, int E, int pad, int bn1, int tiles1, int bn2, int tiles2,
                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
                  int32_t* __restrict__ slot_of, int32_t* __restrict__ unit_off1, int32_t* __restrict__ unit_off2,
-                 int32_t* __restrict__ err) {
+                 int32_t* __restrict__ err, int32_t* __restrict__ flags, int n_flags) {
   extern __shared__ int sm[];
   int* cnt = sm;                 // [E]
   int* cursor = sm + E;          // [E]
@@ -78,6 +48,7 @@ __global__ void __launch_bounds__(kAlignThreads)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_launch_dependents();
   pdl_wait();
+  for (int i = tid; i < n_flags; i += kAlignThreads) flags[i] = 0;
   if constexpr (FUSED_VPL > 0) {
     for (int t = warp; t < T; t += kAlignWarps)
       topk_softmax_warp<FUSED_VPL>(logits + static_cast<size_t>(t) * E, E, k, renorm,
@@ -101,13 +72,15 @@ __global__ void __launch_bounds__(kAlignThreads)
       err[1] = kKernAlign;
       err[0] = kErrDevice;
     }
-    // leave an empty, consistent routing behind: no rows, no units
+    // leave an empty, consistent routing behind: no rows, no units, and every
+    // routed token pointing at row 0 (so the combine stays in bounds)
     for (int e = tid; e <= E; e += kAlignThreads) {
       offsets[e] = 0;
       if (unit_off1) unit_off1[e] = 0;
       if (unit_off2) unit_off2[e] = 0;
       if (e < E) counts[e] = 0;
     }
+    for (int i = tid; i < N; i += kAlignThreads) slot_of[i] = 0;
     return;
   }
 
@@ -119,9 +92,9 @@ __global__ void __launch_bounds__(kAlignThreads)
     const int u1 = (bn1 > 0) ? (p + bn1 - 1) / bn1 * tiles1 : 0;
     const int u2 = (bn2 > 0) ? (p + bn2 - 1) / bn2 * tiles2 : 0;
     int tot_p, tot_u1, tot_u2;
-    const int off = block_exclusive_scan(p, scan_tmp, &tot_p);
-    const int o1 = block_exclusive_scan(u1, scan_tmp, &tot_u1);
-    const int o2 = block_exclusive_scan(u2, scan_tmp, &tot_u2);
+    const int off = block_exclusive_scan_1024(p, scan_tmp, &tot_p);
+    const int o1 = block_exclusive_scan_1024(u1, scan_tmp, &tot_u1);
+    const int o2 = block_exclusive_scan_1024(u2, scan_tmp, &tot_u2);
     if (e < E) {
       counts[e] = c;
       offsets[e] = off;
@@ -256,7 +229,7 @@ template <int VPL>
 cudaError_t launch_align_t(const float* logits, int T, int k, int renorm, int32_t* topk_ids, float* topk_w, int N,
                            int E, int pad, int bn1, int tiles1, int bn2, int tiles2, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_ids, int32_t* slot_of, int32_t* unit_off1, int32_t* unit_off2,
-                           int32_t* err, cudaStream_t stream) {
+                           int32_t* err, int32_t* flags, int n_flags, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(2 + kAlignWarps) * E * sizeof(int);
   static int configured_device = -1;
   int dev = 0;
@@ -269,7 +242,7 @@ cudaError_t launch_align_t(const float* logits, int T, int k, int renorm, int32_
   }
   return launch_pdl(align_kernel<VPL>, dim3(1), dim3(kAlignThreads), smem, stream, logits, T, k, renorm, topk_w,
                     topk_ids, N, E, pad, bn1, tiles1, bn2, tiles2, counts, offsets, sorted_ids, slot_of, unit_off1,
-                    unit_off2, err);
+                    unit_off2, err, flags, n_flags);
 }
 
 
@@ -278,9 +251,9 @@ bool align_fuses_topk(int T, int E) { return T <= kFusedTopkMaxT && E <= kFusedT
 cudaError_t launch_align(const float* logits, int T, int k, int renorm, int32_t* topk_ids, float* topk_w, int N,
                          int E, int pad, int bn1, int tiles1, int bn2, int tiles2, int32_t* counts, int32_t* offsets,
                          int32_t* sorted_ids, int32_t* slot_of, int32_t* unit_off1, int32_t* unit_off2, int32_t* err,
-                         cudaStream_t stream) {
+                         int32_t* flags, int n_flags, cudaStream_t stream) {
 #define MOE_ALIGN_ARGS logits, T, k, renorm, topk_ids, topk_w, N, E, pad, bn1, tiles1, bn2, tiles2, counts, offsets, \
-                       sorted_ids, slot_of, unit_off1, unit_off2, err, stream
+                       sorted_ids, slot_of, unit_off1, unit_off2, err, flags, n_flags, stream
   if (!align_fuses_topk(T, E)) return launch_align_t<0>(MOE_ALIGN_ARGS);
   switch (topk_vpl(E)) {
     case 1: return launch_align_t<1>(MOE_ALIGN_ARGS);

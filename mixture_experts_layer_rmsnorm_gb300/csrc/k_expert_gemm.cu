@@ -9,7 +9,7 @@
 // transposition trick of the fused-MoE article ("Swap-AB para la utilización
 // de WGMMA", Fig. 1), re-done for tcgen05 (M = 128, N = tokens in
 // multiples of 16 up to 256).  The same mapping serves prefill: a unit then
-// covers 128 weight rows x up to 128 / 256 tokens.
+// covers 128 weight rows x up to 256 tokens.
 //
 // Gate/up: W13[e] holds W_gate^T in rows [0, I) and W_up^T in rows [I, 2I) (the
 // concatenated (d x 2 d_ff) weight of "4 · La fusion de noyaux", §4.2
@@ -20,6 +20,19 @@
 // reading lanes 0..63, which applies SiLU(gate) * up to the accumulators
 // before the only store ("GEMM + épilogue", §4.2).
 //
+// Work split.  Units are dealt round-robin to the persistent CTAs, except in
+// the decode tile plan (each weight tile read once, so no L2 reuse to keep),
+// which splits stream-K: the U units x KB K-blocks form one list of
+// iterations; CTA c (of G persistent CTAs) takes the contiguous range
+// [c*W/G, (c+1)*W/G), W = U*KB, so every CTA streams the same number of
+// weight bytes whatever the routing.  A range can start or end inside a
+// unit: the CTA that holds a unit's first K-blocks finishes that unit, as
+// the last work of its range; every later CTA that holds a part of the unit
+// does that part first, writes the fp32 partial sums of its TMEM accumulator
+// to a per-CTA slot in global memory and raises one flag per TMEM lane
+// quarter.  The finishing CTA adds the partials of the following CTAs
+// before its epilogue, so it never waits on work that has not started.
+//
 // Roles in a CTA of 192 threads (persistent, one CTA per SM):
 //   warp 0 lane 0   TMA producer: weight tiles [128 x 64] (gate/up: two boxes
 //                   of 64 rows) and token tiles of TOKBOX rows per box, 128-byte
@@ -27,11 +40,11 @@
 //   warp 1          owns the TMEM allocation; lane 0 issues tcgen05.mma and
 //                   tcgen05.commit (frees a ring slot / hands an accumulator
 //                   buffer to the epilogue)
-//   warps 2..5      epilogue: tcgen05.ld of their TMEM lane quarter, SwiGLU or
-//                   plain bf16 convert, global stores
-// Two accumulator buffers in TMEM let the epilogue of one unit overlap the
-// MMAs of the next.  Every wait is bounded; a wait that runs out sets the
-// workspace error word and the kernel winds down.
+//   warps 2..5      epilogue: tcgen05.ld of their TMEM lane quarter, partial
+//                   sums, SwiGLU or plain bf16 convert, global stores
+// Two accumulator buffers in TMEM let the epilogue of one range segment
+// overlap the MMAs of the next.  Every wait is bounded; a wait that runs out
+// sets the workspace error word and the kernel winds down.
 #include <cuda_bf16.h>
 
 #include "moe_kernels.cuh"
@@ -60,7 +73,7 @@ struct GemmCfg {
   static constexpr int kXchgBytes = SWIGLU ? 2 * 2 * kXchgFloats * 4 : 0;
   static constexpr int kBarBytes = 512;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kXchgBytes + kBarBytes;
-  static constexpr int kFeatPerTile = SWIGLU ? 64 : 128;  // output features per unit
+  static constexpr int kFeatPerTile = SWIGLU ? kGateUpTileFeat : kDownTileFeat;  // output features per unit
   static_assert(BN % TOKBOX == 0 && TOKBOX % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
   static_assert(kTmemNeed <= 512, "TMEM has 512 columns");
@@ -95,12 +108,79 @@ __device__ __forceinline__ Unit decode_unit(int u, const int32_t* __restrict__ u
   return r;
 }
 
+// The CTA's work, walked as segments: K-blocks [kb0, kb1) of unit u.
+// Stream-K: a contiguous range of (unit, K-block) iterations.  Otherwise
+// whole units u = cta, cta + ctas, ... (CTAs running side by side then work
+// on neighbouring units, which share weight and token tiles in L2).
+struct Range {
+  int64_t it, end, W;
+  int kblocks, units, step;
+  bool stream_k;
+  __device__ Range(int n_units, int kb, int cta, int ctas, bool sk)
+      : kblocks(kb), units(n_units), step(ctas), stream_k(sk) {
+    W = static_cast<int64_t>(n_units) * kb;
+    if (sk) {
+      it = W * cta / ctas;
+      end = W * (cta + 1) / ctas;
+    } else {
+      it = cta;
+      end = n_units;
+    }
+  }
+  __device__ bool next(int& u, int& kb0, int& kb1) {
+    if (it >= end) return false;
+    if (!stream_k) {
+      u = static_cast<int>(it);
+      kb0 = 0;
+      kb1 = kblocks;
+      it += step;
+      return true;
+    }
+    u = static_cast<int>(it / kblocks);
+    kb0 = static_cast<int>(it - static_cast<int64_t>(u) * kblocks);
+    const int64_t stop = kb0 + (end - it);
+    kb1 = stop < kblocks ? static_cast<int>(stop) : kblocks;
+    it += kb1 - kb0;
+    return true;
+  }
+};
+
+__device__ __forceinline__ int64_t range_start(int64_t W, int cta, int ctas) { return W * cta / ctas; }
+
 __device__ __forceinline__ void raise_timeout(int32_t* err, volatile int* abort_flag, int kern) {
   *abort_flag = 1;
   if (atomicCAS(err, 0, kErrTimeout) == 0) atomicExch(err + 1, kern);
 }
 
 __device__ __forceinline__ uint16_t f2bf(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release(int32_t* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait of one warp for a partial-sum flag; warp-uniform result.
+__device__ __forceinline__ bool wait_flag(const int32_t* flag, const volatile int* abort_flag) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire(flag) == 0) {
+      if (*abort_flag || globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        ok = false;
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  if (ok) (void)ld_acquire(flag);  // every lane acquires before reading the partials
+  return ok;
+}
 
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -115,8 +195,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
-  uint64_t* xfull = done + 1;   // [pair][slot]: up values written
-  uint64_t* xempty = xfull + 4; // [pair][slot]: up values consumed
+  uint64_t* xfull = done + 1;    // [pair][slot]: up values written
+  uint64_t* xempty = xfull + 4;  // [pair][slot]: up values consumed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xempty + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -155,6 +235,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   pdl_wait();
   const int total_units = __ldg(args.unit_off + args.E);
   const int kblocks = args.K / kBlockK;
+  const int ctas = gridDim.x;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -172,14 +253,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      Range rg(total_units, kblocks, blockIdx.x, ctas, args.stream_k != 0);
+      int u, kb0, kb1;
+      while (ok && rg.next(u, kb0, kb1)) {
         const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
         const int wrow = un.e * args.w_rows_per_expert + un.tile * C::kFeatPerTile;
         const int tok_rows = (un.n + TOKBOX - 1) / TOKBOX * TOKBOX;  // whole boxes; rows past n are unused
         const bool reused = __ldg(args.offsets + un.e + 1) - __ldg(args.offsets + un.e) > BN;
         const uint64_t pol_w = reused ? pol_keep : pol_stream;
         const uint32_t bytes = kABytes + tok_rows * kTokRowBytes;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitTimeoutNs, abort_flag)) {
             ok = false;
             break;
@@ -219,7 +302,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      Range rg(total_units, kblocks, blockIdx.x, ctas, args.stream_k != 0);
+      int u, kb0, kb1;
+      while (ok && rg.next(u, kb0, kb1)) {
         const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, kWaitTimeoutNs, abort_flag)) {
           ok = false;
@@ -228,7 +313,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(un.n));
         const uint32_t d_acc = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, kWaitTimeoutNs, abort_flag)) {
             ok = false;
             break;
@@ -238,7 +323,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sb = sa + kABytes;
 #pragma unroll
           for (int k = 0; k < kBlockK / 16; ++k) {
-            const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+            const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;  // each segment starts a fresh sum
             mma_bf16_ss(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc, accum);
           }
           mma_commit(&empty[stage]);
@@ -261,6 +346,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4
     const int q = warp & 3;
+    const int row = q * 32 + lane;  // this thread's TMEM lane = A-tile row
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t xit = 0;  // gate/up hand-off counter (slot = xit & 1)
@@ -270,7 +356,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int pair = q & 1;
     const bool gate_warp = q < 2;
     float* xb = xchg + pair * 2 * C::kXchgFloats;
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+    // this CTA's partial-sum slot: [BN columns][128 rows] fp32
+    float* my_slot = args.partials + static_cast<int64_t>(blockIdx.x) * BN * 128;
+    Range rg(total_units, kblocks, blockIdx.x, ctas, args.stream_k != 0);
+    int u, kb0, kb1;
+    while (ok && rg.next(u, kb0, kb1)) {
       const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
       // warp-uniform outcome: tcgen05.ld below must be executed by all 32 lanes
       const bool got = mbar_wait(&tfull[acc], acc_phase, kWaitTimeoutNs, abort_flag);
@@ -280,56 +370,90 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * C::kAccCols);
-      if (!SWIGLU) {
-        const int feat = un.tile * C::kFeatPerTile + q * 32 + lane;
-        uint16_t* out = args.out + static_cast<int64_t>(un.tok0) * args.n_out + feat;
+
+      if (kb0 > 0) {
+        // a later part of a unit started by an earlier CTA: hand over the partial sums
         for (int c0 = 0; c0 < un.n; c0 += 16) {
           uint32_t ra[16];
           tmem_ld_32x32b_x16(t_row + c0, ra);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) out[static_cast<int64_t>(c0 + j) * args.n_out] = f2bf(__uint_as_float(ra[j]));
+          for (int j = 0; j < 16; ++j) __stcg(my_slot + (c0 + j) * 128 + row, __uint_as_float(ra[j]));
         }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release(args.flags + blockIdx.x * 4 + q, 1);
       } else {
-        const int feat = un.tile * C::kFeatPerTile + pair * 32 + lane;
-        uint16_t* out = args.out + static_cast<int64_t>(un.tok0) * args.n_out + feat;
+        // this CTA finishes the unit: the CTAs after it whose (non-empty)
+        // ranges start inside the unit hold its later K-blocks and have
+        // written their partial sums as their first work
+        const int64_t unit_end = static_cast<int64_t>(u + 1) * kblocks;
+        int c_last = blockIdx.x;  // producers are the CTAs in (blockIdx.x, c_last] with non-empty ranges
+        if (kb1 < kblocks)
+          while (c_last + 1 < ctas && range_start(rg.W, c_last + 1, ctas) < unit_end) ++c_last;
+        const int feat_base = un.tile * C::kFeatPerTile;
         for (int c0 = 0; c0 < un.n && ok; c0 += 16, ++xit) {
-          const int slot = xit & 1;
-          const uint32_t par = (xit >> 1) & 1u;
-          float* xs = xb + slot * C::kXchgFloats;
           uint32_t ra[16];
           tmem_ld_32x32b_x16(t_row + c0, ra);
           tmem_ld_wait();
-          if (!gate_warp) {
-            // hand the up values of these 16 tokens to the gate warp
-            const bool free_slot = mbar_wait(&xempty[pair * 2 + slot], par ^ 1u, kWaitTimeoutNs, abort_flag);
-            if (!__all_sync(0xFFFFFFFFu, free_slot)) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(ra[j]);
+          for (int c = blockIdx.x + 1; c <= c_last; ++c) {
+            if (range_start(rg.W, c, ctas) == range_start(rg.W, c + 1, ctas)) continue;  // empty range
+            if (c0 == 0 && !wait_flag(args.flags + c * 4 + q, abort_flag)) {
               ok = false;
               break;
             }
+            const float* slot = args.partials + static_cast<int64_t>(c) * BN * 128;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) xs[j * 32 + lane] = __uint_as_float(ra[j]);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&xfull[pair * 2 + slot]);
+            for (int j = 0; j < 16; ++j) v[j] += __ldcg(slot + (c0 + j) * 128 + row);
+          }
+          if (!ok) break;
+          if (!SWIGLU) {
+            uint16_t* out = args.out + static_cast<int64_t>(un.tok0 + c0) * args.n_out + feat_base + row;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) out[static_cast<int64_t>(j) * args.n_out] = f2bf(v[j]);
           } else {
-            const bool have = mbar_wait(&xfull[pair * 2 + slot], par, kWaitTimeoutNs, abort_flag);
-            if (!__all_sync(0xFFFFFFFFu, have)) {
-              ok = false;
-              break;
-            }
+            const int slot_i = xit & 1;
+            const uint32_t par = (xit >> 1) & 1u;
+            float* xs = xb + slot_i * C::kXchgFloats;
+            if (!gate_warp) {
+              // hand the up values of these 16 tokens to the gate warp
+              const bool free_slot = mbar_wait(&xempty[pair * 2 + slot_i], par ^ 1u, kWaitTimeoutNs, abort_flag);
+              if (!__all_sync(0xFFFFFFFFu, free_slot)) {
+                ok = false;
+                break;
+              }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float g = __uint_as_float(ra[j]);
-              const float up = xs[j * 32 + lane];
-              const float a = __fdividef(g, 1.0f + __expf(-g)) * up;  // SiLU(gate) * up
-              out[static_cast<int64_t>(c0 + j) * args.n_out] = f2bf(a);
+              for (int j = 0; j < 16; ++j) xs[j * 32 + lane] = v[j];
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&xfull[pair * 2 + slot_i]);
+            } else {
+              const bool have = mbar_wait(&xfull[pair * 2 + slot_i], par, kWaitTimeoutNs, abort_flag);
+              if (!__all_sync(0xFFFFFFFFu, have)) {
+                ok = false;
+                break;
+              }
+              uint16_t* out =
+                  args.out + static_cast<int64_t>(un.tok0 + c0) * args.n_out + feat_base + pair * 32 + lane;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float g = v[j];
+                const float up = xs[j * 32 + lane];
+                const float a = __fdividef(g, 1.0f + __expf(-g)) * up;  // SiLU(gate) * up
+                out[static_cast<int64_t>(j) * args.n_out] = f2bf(a);
+              }
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&xempty[pair * 2 + slot_i]);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&xempty[pair * 2 + slot]);
           }
         }
-        if (!ok) break;
+        // the partial-sum flags read here are cleared for the next launch
+        if (ok && lane == 0)
+          for (int c = blockIdx.x + 1; c <= c_last; ++c) args.flags[c * 4 + q] = 0;
       }
+      if (!ok) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -359,19 +483,19 @@ cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, con
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  return launch_pdl(expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX>, dim3(num_sms), dim3(kGemmThreads),
-                    C::kSmemBytes,
-                    stream, tw, tx, a);
+  const int grid = num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas;
+  return launch_pdl(expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX>, dim3(grid), dim3(kGemmThreads),
+                    C::kSmemBytes, stream, tw, tx, a);
 }
 
 // Three tile plans by the expected tokens per expert (T*top_k/E):
 //   small (<= 16): 32-token units, deep weight pipelines (decode);
 //   mid   (<= 64): 64-token units, so most experts still fit one chunk;
-//   large (> 64) : 128 / 256-token units and 64-row token boxes (prefill).
+//   large (> 64) : 256-token units and 64-row token boxes (prefill).
 constexpr int kGateUpBn[3] = {32, 64, 256}, kGateUpStages[3] = {10, 8, 4};  // stages of 20 / 24 / 48 KB
 constexpr int kDownBn[3] = {32, 64, 256}, kDownStages[3] = {10, 8, 4};      // stages of 20 / 24 / 48 KB
 // token rows per TMA box: small units hold few tokens (16-row boxes waste
-// nothing); large units hold 128-256 (64-row boxes: 4x fewer TMA requests)
+// nothing); large units hold up to 256 (64-row boxes: 4x fewer TMA requests)
 constexpr int kTokBox[3] = {16, 16, 64};
 
 }  // namespace

@@ -1,4 +1,4 @@
-// k_route.cu -- K1: fused RMSNorm + router logits; K1b: top-k + softmax weights.
+// k_route.cu -- K1: fused RMSNorm + router logits (top-k runs in the align kernels).
 //
 // RMSNorm ("4 · La fusion de noyaux", §4.2 "Réduction + élémentaire"; "CuTeDSL
 // chez Perplexity", "Norme QK"): one warp per token row, 128-bit loads of 8
@@ -21,7 +21,6 @@
 
 #include "moe_kernels.cuh"
 #include "pdl.cuh"
-#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -53,7 +52,7 @@ __device__ __forceinline__ float warp_butterfly_sum(float v) {
 // grid = (ceil(T / TT), ceil(E / experts_per_cta)), block = 256, dyn smem = TT*H*2.
 // Each warp computes TE experts x TT tokens at a time.
 template <int TT, int TE>
-__global__ void __launch_bounds__(kRouteWarps * 32, 1)
+__global__ void __launch_bounds__(kRouteWarps * 32, (TT >= 8) ? 2 : 1)
     norm_router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g,
                        const float* __restrict__ w_router, const float* __restrict__ bias, int T, int H, int E,
                        float eps, int experts_per_cta, uint16_t* __restrict__ h_out, float* __restrict__ logits,
@@ -204,19 +203,6 @@ __global__ void __launch_bounds__(kRouteWarps * 32, 1)
   }
 }
 
-// one warp per token; block = 256 (8 tokens).  E <= 32 * VPL, k <= 32.
-template <int VPL>
-__global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                           int renorm, int32_t* __restrict__ topk_ids,
-                                                           float* __restrict__ topk_w) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= T) return;
-  topk_softmax_warp<VPL>(logits + static_cast<size_t>(t) * E, E, k, renorm, topk_ids + static_cast<size_t>(t) * k,
-                         topk_w + static_cast<size_t>(t) * k);
-}
-
 template <int TT, int TE>
 cudaError_t launch_nr(const uint16_t* x, const uint16_t* g, const float* wr, const float* bias, int T, int H, int E,
                       float eps, uint16_t* h, float* logits, int32_t* err, int num_sms, cudaStream_t stream) {
@@ -232,10 +218,11 @@ cudaError_t launch_nr(const uint16_t* x, const uint16_t* g, const float* wr, con
   }
   const int tiles = (T + TT - 1) / TT;
   const int group = kRouteWarps * TE;
-  // one expert group per CTA spreads the work (and the router weights) over
-  // many SMs; only with very many token tiles does a CTA take all experts
+  // fewer token tiles than SMs: one expert group per CTA spreads the work
+  // (and the router weights) over the SMs; otherwise a CTA takes all experts
+  // so that its tokens are normalised once
   int epc = group;
-  if (static_cast<long long>(tiles) * ((E + group - 1) / group) > 16LL * num_sms) epc = (E + group - 1) / group * group;
+  if (tiles >= num_sms) epc = (E + group - 1) / group * group;
   dim3 grid(tiles, (E + epc - 1) / epc);
   return launch_pdl(norm_router_kernel<TT, TE>, grid, dim3(kRouteWarps * 32), smem, stream, x, g, wr, bias, T, H, E,
                     eps, epc, h, logits, err);
@@ -251,21 +238,5 @@ cudaError_t launch_norm_router(const uint16_t* x, const uint16_t* g, const float
     return launch_nr<4, 2>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
   return launch_nr<8, 4>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
 }
-
-cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int renorm, int32_t* topk_ids,
-                                float* topk_w, cudaStream_t stream) {
-  const dim3 grid((T + 7) / 8), block(256);
-  switch (topk_vpl(E)) {
-    case 1: return launch_pdl(topk_softmax_kernel<1>, grid, block, 0, stream, logits, T, E, k, renorm, topk_ids, topk_w);
-    case 2: return launch_pdl(topk_softmax_kernel<2>, grid, block, 0, stream, logits, T, E, k, renorm, topk_ids, topk_w);
-    case 4: return launch_pdl(topk_softmax_kernel<4>, grid, block, 0, stream, logits, T, E, k, renorm, topk_ids, topk_w);
-    case 8: return launch_pdl(topk_softmax_kernel<8>, grid, block, 0, stream, logits, T, E, k, renorm, topk_ids, topk_w);
-    case 16:
-      return launch_pdl(topk_softmax_kernel<16>, grid, block, 0, stream, logits, T, E, k, renorm, topk_ids, topk_w);
-    default:
-      return launch_pdl(topk_softmax_kernel<32>, grid, block, 0, stream, logits, T, E, k, renorm, topk_ids, topk_w);
-  }
-}
-
 
 }  // namespace moe

@@ -30,7 +30,8 @@ constexpr int kMaxDebugPad = 256;
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-  size_t err, h, logits, ids, w, counts, offsets, unit1, unit2, sorted, slot, xg, act, out, total;
+  size_t err, h, logits, ids, w, counts, offsets, unit1, unit2, sorted, slot, flags, blk_counts, blk_base, partials, xg,
+      act, out, total;
   int64_t P_max;       // padded rows with 16-row padding
   int64_t sorted_cap;  // sorted_ids entries (room for debug padding up to 256)
 };
@@ -57,6 +58,12 @@ Layout make_layout(const moe_shape& s) {
   L.unit2 = take(static_cast<size_t>((E + 1) * 4));
   L.sorted = take(static_cast<size_t>(L.sorted_cap * 4));
   L.slot = take(static_cast<size_t>(T * k * 4));
+  // stream-K flags and partial sums of the expert GEMMs (slot = BN x 128 fp32 per CTA)
+  L.flags = take(static_cast<size_t>(moe::kMaxGemmCtas) * 4 * 4);
+  // per-block counts / bases of the multi-CTA align
+  L.blk_counts = take(static_cast<size_t>((T + moe::kAlignTokPerBlk - 1) / moe::kAlignTokPerBlk) * E * 4);
+  L.blk_base = take(static_cast<size_t>((T + moe::kAlignTokPerBlk - 1) / moe::kAlignTokPerBlk) * E * 4);
+  L.partials = take(static_cast<size_t>(moe::kMaxGemmCtas) * moe::gemm_gate_up_bn(moe::choose_plan(T, k, E)) * 128 * 4);
   L.xg = take(static_cast<size_t>(L.P_max * H * 2));
   L.act = take(static_cast<size_t>(L.P_max * I * 2));
   L.out = take(static_cast<size_t>(L.P_max * H * 2));
@@ -141,15 +148,24 @@ moe_status run_front(const moe_shape& s, const Layout& L, const moe_bf16* x, con
   if (moe::launch_norm_router(x, g, wr, bias, s.T, s.H, s.E, s.eps, at<uint16_t>(ws, L.h), at<float>(ws, L.logits),
                               err, num_sms, st) != cudaSuccess)
     return MOE_ERR_CUDA;
-  const bool fused = moe::align_fuses_topk(s.T, s.E);
-  if (!fused && moe::launch_topk_softmax(at<float>(ws, L.logits), s.T, s.E, s.top_k, s.renormalize,
-                                         at<int32_t>(ws, L.ids), at<float>(ws, L.w), st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (moe::launch_align(at<float>(ws, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(ws, L.ids),
-                        at<float>(ws, L.w), s.T * s.top_k, s.E, pad, bn1, s.I / moe::kGateUpTileFeat, bn2,
-                        s.H / moe::kDownTileFeat, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
-                        at<int32_t>(ws, L.sorted), at<int32_t>(ws, L.slot), bn1 > 0 ? at<int32_t>(ws, L.unit1) : nullptr,
-                        bn2 > 0 ? at<int32_t>(ws, L.unit2) : nullptr, err, st) != cudaSuccess)
+  cudaError_t ce;
+  if (moe::align_fuses_topk(s.T, s.E))
+    ce = moe::launch_align(at<float>(ws, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(ws, L.ids),
+                           at<float>(ws, L.w), s.T * s.top_k, s.E, pad, bn1, s.I / moe::kGateUpTileFeat, bn2,
+                           s.H / moe::kDownTileFeat, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+                           at<int32_t>(ws, L.sorted), at<int32_t>(ws, L.slot),
+                           bn1 > 0 ? at<int32_t>(ws, L.unit1) : nullptr, bn2 > 0 ? at<int32_t>(ws, L.unit2) : nullptr,
+                           err, at<int32_t>(ws, L.flags), moe::kMaxGemmCtas * 4, st);
+  else
+    ce = moe::launch_align_multi(at<float>(ws, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(ws, L.ids),
+                                 at<float>(ws, L.w), s.E, pad, bn1, s.I / moe::kGateUpTileFeat, bn2,
+                                 s.H / moe::kDownTileFeat, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+                                 at<int32_t>(ws, L.sorted), at<int32_t>(ws, L.slot),
+                                 bn1 > 0 ? at<int32_t>(ws, L.unit1) : nullptr,
+                                 bn2 > 0 ? at<int32_t>(ws, L.unit2) : nullptr, at<int32_t>(ws, L.blk_counts),
+                                 at<int32_t>(ws, L.blk_base), err, at<int32_t>(ws, L.flags), moe::kMaxGemmCtas * 4, st,
+                                 nullptr);
+  if (ce != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -226,20 +242,31 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   if (moe::launch_norm_router(x, g_norm, w_router, router_bias, s.T, s.H, s.E, s.eps, at<uint16_t>(workspace, L.h),
                               at<float>(workspace, L.logits), err, num_sms, cs) != cudaSuccess || !mark(1))
     return MOE_ERR_CUDA;
-  // top-k runs in its own kernel for large T, inside the align kernel for small T
-  const bool fused = moe::align_fuses_topk(s.T, s.E);
-  if (!fused && moe::launch_topk_softmax(at<float>(workspace, L.logits), s.T, s.E, s.top_k, s.renormalize,
-                                         at<int32_t>(workspace, L.ids), at<float>(workspace, L.w), cs) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (!mark(2)) return MOE_ERR_CUDA;
+  // small T and E: top-k and align in one single-CTA kernel (events[2] then
+  // follows events[1] at once); otherwise three multi-CTA kernels: top-k with
+  // per-block counts (ends at events[2]), scan and scatter (end at events[3])
   const int N = s.T * s.top_k;
-  if (moe::launch_align(at<float>(workspace, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(workspace, L.ids), at<float>(workspace, L.w), N, s.E, moe::kPadRows, bn1,
-                        s.I / moe::kGateUpTileFeat, bn2, s.H / moe::kDownTileFeat, at<int32_t>(workspace, L.counts),
-                        at<int32_t>(workspace, L.offsets), at<int32_t>(workspace, L.sorted),
-                        at<int32_t>(workspace, L.slot), at<int32_t>(workspace, L.unit1), at<int32_t>(workspace, L.unit2),
-                        err, cs) != cudaSuccess ||
-      !mark(3))
-    return MOE_ERR_CUDA;
+  cudaError_t ce;
+  if (moe::align_fuses_topk(s.T, s.E)) {
+    if (!mark(2)) return MOE_ERR_CUDA;
+    ce = moe::launch_align(at<float>(workspace, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(workspace, L.ids),
+                           at<float>(workspace, L.w), N, s.E, moe::kPadRows, bn1, s.I / moe::kGateUpTileFeat, bn2,
+                           s.H / moe::kDownTileFeat, at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.offsets),
+                           at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.slot),
+                           at<int32_t>(workspace, L.unit1), at<int32_t>(workspace, L.unit2), err,
+                           at<int32_t>(workspace, L.flags), moe::kMaxGemmCtas * 4, cs);
+  } else {
+    ce = moe::launch_align_multi(at<float>(workspace, L.logits), s.T, s.top_k, s.renormalize,
+                                 at<int32_t>(workspace, L.ids), at<float>(workspace, L.w), s.E, moe::kPadRows, bn1,
+                                 s.I / moe::kGateUpTileFeat, bn2, s.H / moe::kDownTileFeat,
+                                 at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.offsets),
+                                 at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.slot),
+                                 at<int32_t>(workspace, L.unit1), at<int32_t>(workspace, L.unit2),
+                                 at<int32_t>(workspace, L.blk_counts), at<int32_t>(workspace, L.blk_base), err,
+                                 at<int32_t>(workspace, L.flags), moe::kMaxGemmCtas * 4, cs,
+                                 events ? events[2] : nullptr);
+  }
+  if (ce != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
   if (moe::launch_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
                          at<int32_t>(workspace, L.offsets), s.E, N, s.top_k, s.H, L.P_max,
                          at<uint16_t>(workspace, L.xg), cs) != cudaSuccess ||
@@ -257,6 +284,9 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a1.n_out = s.I;
   a1.out = at<uint16_t>(workspace, L.act);
   a1.err = err;
+  a1.partials = at<float>(workspace, L.partials);
+  a1.flags = at<int32_t>(workspace, L.flags);
+  a1.stream_k = plan == GemmPlan::kSmall;
   if (moe::launch_gemm_gate_up(tm_w13, tm_xg, a1, plan, num_sms, cs) != cudaSuccess || !mark(5)) return MOE_ERR_CUDA;
 
   moe::ExpertGemmArgs a2{};
@@ -270,6 +300,9 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a2.n_out = s.H;
   a2.out = at<uint16_t>(workspace, L.out);
   a2.err = err;
+  a2.partials = at<float>(workspace, L.partials);
+  a2.flags = at<int32_t>(workspace, L.flags);
+  a2.stream_k = plan == GemmPlan::kSmall;
   if (moe::launch_gemm_down(tm_w2, tm_act, a2, plan, num_sms, cs) != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
 
   if (moe::launch_combine(at<uint16_t>(workspace, L.out), at<int32_t>(workspace, L.slot), at<float>(workspace, L.w),

@@ -23,22 +23,31 @@ cudaError_t launch_norm_router(const uint16_t* x, const uint16_t* g, const float
                                int T, int H, int E, float eps, uint16_t* h, float* logits, int32_t* err,
                                int num_sms, cudaStream_t stream);
 
-// K1b: top-k + softmax weights per token from the logits.
-cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int renorm, int32_t* topk_ids,
-                                float* topk_w, cudaStream_t stream);
-
 // K2: deterministic align: counts, padded offsets, sorted_ids, slot_of and the
 // prefix sums of work units of the two expert GEMMs (units per expert =
 // ceil(P_e / bn) * tiles; bn = 0 skips that table).  When
 // align_fuses_topk(T, E), the same single CTA first runs K1b for all T tokens
 // (topk_ids / topk_w from the logits) and K1b must not be launched.
+// It also clears n_flags ints at `flags` (the expert GEMMs' stream-K flags).
 cudaError_t launch_align(const float* logits, int T, int k, int renorm, int32_t* topk_ids, float* topk_w, int N,
                          int E, int pad, int bn1, int tiles1, int bn2, int tiles2, int32_t* counts, int32_t* offsets,
                          int32_t* sorted_ids, int32_t* slot_of, int32_t* unit_off1, int32_t* unit_off2, int32_t* err,
-                         cudaStream_t stream);
+                         int32_t* flags, int n_flags, cudaStream_t stream);
 constexpr int kFusedTopkMaxT = 256;
 constexpr int kFusedTopkMaxE = 256;
 bool align_fuses_topk(int T, int E);
+
+// K1b + K2 for the other shapes, over many CTAs (three launches: count with
+// top-k, scan, scatter).  blk_counts / blk_base: align_multi_blocks(T) * E
+// ints of scratch each.  count_done_event (a cudaEvent_t, or null) is recorded
+// after the first of the three kernels.
+constexpr int kAlignTokPerBlk = 64;
+int align_multi_blocks(int T);
+cudaError_t launch_align_multi(const float* logits, int T, int k, int renorm, int32_t* topk_ids, float* topk_w, int E,
+                               int pad, int bn1, int tiles1, int bn2, int tiles2, int32_t* counts, int32_t* offsets,
+                               int32_t* sorted_ids, int32_t* slot_of, int32_t* unit_off1, int32_t* unit_off2,
+                               int32_t* blk_counts, int32_t* blk_base, int32_t* err, int32_t* flags, int n_flags,
+                               cudaStream_t stream, void* count_done_event);
 
 // K3: xg[p,:] = h[sorted_ids[p] / k, :] for real rows, zeros for padding rows.
 cudaError_t launch_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets, int E, int N,
@@ -57,7 +66,12 @@ struct ExpertGemmArgs {
   int n_out;                // output row length (I or H)
   uint16_t* out;            // [P_max, n_out] bf16
   int32_t* err;
+  float* partials;          // stream-K partial sums: [kMaxGemmCtas][BN][128] fp32
+  int32_t* flags;           // [kMaxGemmCtas * 4], zero on entry; left zero on exit
+  int stream_k;             // 1: equal K-block ranges per CTA; 0: whole units round-robin
 };
+// persistent GEMM grid: min(SM count, kMaxGemmCtas) CTAs
+constexpr int kMaxGemmCtas = 256;
 
 // tile plan of the expert GEMMs, by the expected tokens per expert
 enum class GemmPlan { kSmall = 0, kMid = 1, kLarge = 2 };
