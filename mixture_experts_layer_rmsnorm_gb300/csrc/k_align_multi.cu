@@ -5,11 +5,11 @@
 // into three launches so that it scales with T ("CuTeDSL chez Perplexity",
 // MoE dispatch/combine: the prefill dispatch assigns indices with local
 // counters first and then combines them across blocks in global memory):
-//   count   one CTA per 64 tokens: top-k + softmax of its tokens, then the
+//   count   one CTA per 32 tokens: top-k + softmax of its tokens, then the
 //           CTA's count per expert -> blk_counts[b][e]
 //   scan    one CTA: totals, padded offsets, work-unit prefix sums, and each
 //           CTA's base row per expert blk_base[b][e] (a prefix over b)
-//   scatter one CTA per 64 tokens again: stable ranks of its entries (warp
+//   scatter one CTA per 32 tokens again: stable ranks of its entries (warp
 //           match / popc + per-warp prefix), written to sorted_ids / slot_of
 // Every step is deterministic.
 #include "block_scan.cuh"

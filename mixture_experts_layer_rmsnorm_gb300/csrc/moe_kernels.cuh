@@ -41,7 +41,7 @@ bool align_fuses_topk(int T, int E);
 // top-k, scan, scatter).  blk_counts / blk_base: align_multi_blocks(T) * E
 // ints of scratch each.  count_done_event (a cudaEvent_t, or null) is recorded
 // after the first of the three kernels.
-constexpr int kAlignTokPerBlk = 64;
+constexpr int kAlignTokPerBlk = 32;
 int align_multi_blocks(int T);
 cudaError_t launch_align_multi(const float* logits, int T, int k, int renorm, int32_t* topk_ids, float* topk_w, int E,
                                int pad, int bn1, int tiles1, int bn2, int tiles2, int32_t* counts, int32_t* offsets,
