@@ -171,7 +171,7 @@ MOE_API moe_status moe_route_debug(const moe_shape* shape, const moe_bf16* x, co
  * for moe_forward.
  *   - Shapes whose moe_workspace_size() exceeds MOE_STATIC_SCRATCH_BYTES are
  *     rejected with MOE_ERR_WORKSPACE before anything is enqueued (e.g. the
- *     decode layer H = I = 4096, E = 64, top_k = 8 fits for T <= 170).
+ *     decode layer H = I = 4096, E = 64, top_k = 8 fits for T <= 129).
  *   - The first call on a device (with that device current) looks up the
  *     array's device address once (cudaGetSymbolAddress) and keeps it; make
  *     that first call before any stream capture.

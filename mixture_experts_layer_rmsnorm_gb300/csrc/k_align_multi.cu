@@ -35,8 +35,8 @@ __global__ void __launch_bounds__(kThreads)
   const int b = blockIdx.x;
   const int t0 = b * kAlignTokPerBlk;
   const int t1 = min(T, t0 + kAlignTokPerBlk);
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   if (b == 0)
     for (int i = tid; i < n_flags; i += kThreads) flags[i] = 0;
   if (tid == 0) bad = 0;
@@ -69,8 +69,8 @@ __global__ void __launch_bounds__(1024)
                       int32_t* __restrict__ unit_off1, int32_t* __restrict__ unit_off2,
                       int32_t* __restrict__ blk_base, int32_t* __restrict__ sorted_ids) {
   __shared__ int scan_tmp[33];
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int e = threadIdx.x;
   int c = 0;
   if (e < E)
@@ -112,8 +112,8 @@ __global__ void __launch_bounds__(kThreads)
   const int b = blockIdx.x;
   const int i0 = b * kAlignTokPerBlk * k;
   const int i1 = min(T, (b + 1) * kAlignTokPerBlk) * k;
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   for (int e = tid; e < E; e += kThreads) cursor[e] = blk_base[static_cast<size_t>(b) * E + e];
   __syncthreads();
   for (int base = i0; base < i1; base += kThreads) {

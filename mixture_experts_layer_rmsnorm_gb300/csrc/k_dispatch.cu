@@ -46,8 +46,8 @@ __global__ void __launch_bounds__(kAlignThreads)
   __shared__ int scan_tmp[kAlignWarps + 1];
   __shared__ int bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   for (int i = tid; i < n_flags; i += kAlignThreads) flags[i] = 0;
   if constexpr (FUSED_VPL > 0) {
     for (int t = warp; t < T; t += kAlignWarps)
@@ -146,8 +146,8 @@ __global__ void __launch_bounds__(kAlignThreads)
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ h, const int32_t* __restrict__ sorted_ids,
                                                      const int32_t* __restrict__ offsets, int E, int N, int k, int H,
                                                      int64_t P_max, uint16_t* __restrict__ xg) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int64_t p = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (p >= P_max || p >= offsets[E]) return;
@@ -184,8 +184,8 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ rows, const int32_t* __restrict__ slot_of,
                                                       const float* __restrict__ w, int T, int H, int k,
                                                       uint16_t* __restrict__ y) {
-  pdl_launch_dependents();
   pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   const int nch = H >> 3;
   for (int c = threadIdx.x; c < nch; c += blockDim.x) {

@@ -229,10 +229,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // everything above touched only on-chip state; from here on the routing
-  // tables and token rows of the previous kernels are read
-  pdl_launch_dependents();
-  pdl_wait();
+  // The routing tables come from a kernel at least two launches back, which
+  // has completed (see pdl.cuh); only the token / activation rows written by
+  // the immediately preceding kernel need the producer's pdl_wait below.
   const int total_units = __ldg(args.unit_off + args.E);
   const int kblocks = args.K / kBlockK;
   const int ctas = gridDim.x;
@@ -253,6 +252,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
+      // Until the previous kernel has completed, only weight tiles are loaded:
+      // the first ring-full of stages gets its weights at once and its token
+      // rows after pdl_wait.
+      bool deps_ready = false;
+      int n_pend = 0;
+      int pend_stage[STAGES], pend_kb[STAGES], pend_tok0[STAGES], pend_rows[STAGES];
+      auto load_tokens = [&](int st, int kb, int tok0, int rows) {
+        uint8_t* sb = smem + st * C::kStageBytes + kABytes;
+        for (int r = 0; r < rows; r += TOKBOX)
+          tma_load_2d(sb + r * kTokRowBytes, &tm_x, &full[st], kb * kBlockK, tok0 + r, pol_x);
+      };
+      auto resolve_deps = [&]() {
+        pdl_wait();
+        pdl_launch_dependents();
+        deps_ready = true;
+        for (int i = 0; i < n_pend; ++i) load_tokens(pend_stage[i], pend_kb[i], pend_tok0[i], pend_rows[i]);
+        n_pend = 0;
+      };
       Range rg(total_units, kblocks, blockIdx.x, ctas, args.stream_k != 0);
       int u, kb0, kb1;
       while (ok && rg.next(u, kb0, kb1)) {
@@ -275,9 +292,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
             tma_load_2d(sa, &tm_w, &full[stage], kb * kBlockK, wrow, pol_w);
           }
-          uint8_t* sb = sa + kABytes;
-          for (int r = 0; r < tok_rows; r += TOKBOX)
-            tma_load_2d(sb + r * kTokRowBytes, &tm_x, &full[stage], kb * kBlockK, un.tok0 + r, pol_x);
+          if (deps_ready) {
+            load_tokens(stage, kb, un.tok0, tok_rows);
+          } else {
+            pend_stage[n_pend] = stage;
+            pend_kb[n_pend] = kb;
+            pend_tok0[n_pend] = un.tok0;
+            pend_rows[n_pend] = tok_rows;
+            if (++n_pend == STAGES) resolve_deps();
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -285,6 +308,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
+      if (!deps_ready) resolve_deps();  // fewer iterations than stages (or none)
       if (!ok) raise_timeout(args.err, abort_flag, kern);
       // every load this thread issued must have landed before the CTA exits
       for (int s = 0; s < STAGES; ++s) {

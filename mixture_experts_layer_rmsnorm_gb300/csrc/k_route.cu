@@ -63,7 +63,6 @@ __global__ void __launch_bounds__(kRouteWarps * 32, (TT >= 8) ? 2 : 1)
   const int t0 = blockIdx.x * TT;
   const int e0 = blockIdx.y * experts_per_cta;
 
-  pdl_launch_dependents();
   // The router rows this CTA will need and the norm gain do not depend on the
   // previous kernel: start pulling them into L2 now, so that their DRAM
   // latency overlaps the RMSNorm below.
@@ -78,6 +77,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32, (TT >= 8) ? 2 : 1)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(gb + off));
   }
   pdl_wait();
+  pdl_launch_dependents();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 4) err[threadIdx.x] = 0;
 
   // ---- RMSNorm: one warp per token

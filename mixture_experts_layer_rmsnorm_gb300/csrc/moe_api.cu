@@ -36,6 +36,14 @@ struct Layout {
   int64_t sorted_cap;  // sorted_ids entries (room for debug padding up to 256)
 };
 
+// stream-K flags: [2 GEMMs][kMaxGemmCtas][4 lane quarters]
+constexpr int kGemmFlagInts = 2 * moe::kMaxGemmCtas * 4;
+
+// stream-K partial sums of one GEMM: per CTA a [BN][128] fp32 slot
+size_t partial_slots_bytes(const moe_shape& s) {
+  return static_cast<size_t>(moe::kMaxGemmCtas) * moe::gemm_gate_up_bn(moe::choose_plan(s.T, s.top_k, s.E)) * 128 * 4;
+}
+
 Layout make_layout(const moe_shape& s) {
   Layout L{};
   const int64_t T = s.T, H = s.H, I = s.I, E = s.E, k = s.top_k;
@@ -59,11 +67,11 @@ Layout make_layout(const moe_shape& s) {
   L.sorted = take(static_cast<size_t>(L.sorted_cap * 4));
   L.slot = take(static_cast<size_t>(T * k * 4));
   // stream-K flags and partial sums of the expert GEMMs (slot = BN x 128 fp32 per CTA)
-  L.flags = take(static_cast<size_t>(moe::kMaxGemmCtas) * 4 * 4);
+  L.flags = take(static_cast<size_t>(kGemmFlagInts) * 4);
   // per-block counts / bases of the multi-CTA align
   L.blk_counts = take(static_cast<size_t>((T + moe::kAlignTokPerBlk - 1) / moe::kAlignTokPerBlk) * E * 4);
   L.blk_base = take(static_cast<size_t>((T + moe::kAlignTokPerBlk - 1) / moe::kAlignTokPerBlk) * E * 4);
-  L.partials = take(static_cast<size_t>(moe::kMaxGemmCtas) * moe::gemm_gate_up_bn(moe::choose_plan(T, k, E)) * 128 * 4);
+  L.partials = take(2 * partial_slots_bytes(s));
   L.xg = take(static_cast<size_t>(L.P_max * H * 2));
   L.act = take(static_cast<size_t>(L.P_max * I * 2));
   L.out = take(static_cast<size_t>(L.P_max * H * 2));
@@ -155,7 +163,7 @@ moe_status run_front(const moe_shape& s, const Layout& L, const moe_bf16* x, con
                            s.H / moe::kDownTileFeat, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                            at<int32_t>(ws, L.sorted), at<int32_t>(ws, L.slot),
                            bn1 > 0 ? at<int32_t>(ws, L.unit1) : nullptr, bn2 > 0 ? at<int32_t>(ws, L.unit2) : nullptr,
-                           err, at<int32_t>(ws, L.flags), moe::kMaxGemmCtas * 4, st);
+                           err, at<int32_t>(ws, L.flags), kGemmFlagInts, st);
   else
     ce = moe::launch_align_multi(at<float>(ws, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(ws, L.ids),
                                  at<float>(ws, L.w), s.E, pad, bn1, s.I / moe::kGateUpTileFeat, bn2,
@@ -163,7 +171,7 @@ moe_status run_front(const moe_shape& s, const Layout& L, const moe_bf16* x, con
                                  at<int32_t>(ws, L.sorted), at<int32_t>(ws, L.slot),
                                  bn1 > 0 ? at<int32_t>(ws, L.unit1) : nullptr,
                                  bn2 > 0 ? at<int32_t>(ws, L.unit2) : nullptr, at<int32_t>(ws, L.blk_counts),
-                                 at<int32_t>(ws, L.blk_base), err, at<int32_t>(ws, L.flags), moe::kMaxGemmCtas * 4, st,
+                                 at<int32_t>(ws, L.blk_base), err, at<int32_t>(ws, L.flags), kGemmFlagInts, st,
                                  nullptr);
   if (ce != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -254,7 +262,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
                            s.H / moe::kDownTileFeat, at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.offsets),
                            at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.slot),
                            at<int32_t>(workspace, L.unit1), at<int32_t>(workspace, L.unit2), err,
-                           at<int32_t>(workspace, L.flags), moe::kMaxGemmCtas * 4, cs);
+                           at<int32_t>(workspace, L.flags), kGemmFlagInts, cs);
   } else {
     ce = moe::launch_align_multi(at<float>(workspace, L.logits), s.T, s.top_k, s.renormalize,
                                  at<int32_t>(workspace, L.ids), at<float>(workspace, L.w), s.E, moe::kPadRows, bn1,
@@ -263,7 +271,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
                                  at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.slot),
                                  at<int32_t>(workspace, L.unit1), at<int32_t>(workspace, L.unit2),
                                  at<int32_t>(workspace, L.blk_counts), at<int32_t>(workspace, L.blk_base), err,
-                                 at<int32_t>(workspace, L.flags), moe::kMaxGemmCtas * 4, cs,
+                                 at<int32_t>(workspace, L.flags), kGemmFlagInts, cs,
                                  events ? events[2] : nullptr);
   }
   if (ce != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
@@ -300,8 +308,8 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a2.n_out = s.H;
   a2.out = at<uint16_t>(workspace, L.out);
   a2.err = err;
-  a2.partials = at<float>(workspace, L.partials);
-  a2.flags = at<int32_t>(workspace, L.flags);
+  a2.partials = at<float>(workspace, L.partials + partial_slots_bytes(s));  // own slots and flags: the
+  a2.flags = at<int32_t>(workspace, L.flags) + moe::kMaxGemmCtas * 4;        // two GEMMs may overlap
   a2.stream_k = plan == GemmPlan::kSmall;
   if (moe::launch_gemm_down(tm_w2, tm_act, a2, plan, num_sms, cs) != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
 

@@ -1,4 +1,10 @@
 // pdl.cuh -- device side of programmatic dependent launch.
+//
+// Convention of this library: a kernel executes pdl_wait() before
+// pdl_launch_dependents().  So when a kernel starts, its predecessor may still
+// be running, but the kernel before that one has completed: a kernel may read
+// its grandparent's outputs (e.g. the routing tables) before its own
+// pdl_wait(), and must wait before reading its parent's outputs.
 #pragma once
 
 namespace moe {

@@ -22,6 +22,8 @@ CASES = [
     # name, T, H, I, E, k, renorm, zipf, seed
     ("tiny", 4, 128, 256, 8, 2, True, None, 0),
     ("T1", 1, 256, 256, 16, 4, True, None, 3),
+    ("T2_wide_rows", 2, 5120, 256, 12, 3, True, None, 13),
+    ("T3_bias", 3, 384, 256, 20, 5, True, 1.2, 14),
     ("ragged_decode", 37, 256, 384, 16, 4, True, None, 1),
     ("deep_k", 64, 1024, 512, 8, 2, True, None, 2),
     ("prefill_chunks", 1024, 256, 256, 4, 2, True, None, 4),
