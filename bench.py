@@ -260,7 +260,7 @@ def run_ours(args, wl, world, rank, local):
     # L2 flush: write 256 MB (2x L2), then read another 256 MB so that the
     # write's dirty lines are written back here rather than inside the timed call
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    flush_rd = torch.ones(64 << 20, dtype=torch.int32, device=dev)
+    flush_rd = torch.ones(64 << 20, dtype=torch.float32, device=dev)
 
     def flush_l2(v):
         flush.fill_(v & 0xFF)
