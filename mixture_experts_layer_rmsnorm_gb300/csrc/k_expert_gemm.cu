@@ -60,9 +60,10 @@ constexpr int kGemmThreads = 192;
 constexpr int kABytes = kWeightBoxRows * kBlockK * 2;  // 16 KB weight tile per stage
 constexpr int kTokRowBytes = kBlockK * 2;              // 128 B per token row per stage
 
-template <bool SWIGLU, int BN, int STAGES, int TOKBOX>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR>
 struct GemmCfg {
-  static constexpr int kBBytes = BN * kTokRowBytes;
+  // a CTA pair splits the unit's tokens: each CTA holds half of the B tile
+  static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * kTokRowBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kAccCols = BN;  // fp32 TMEM columns per accumulator buffer
   static constexpr int kTmemNeed = 2 * kAccCols;
@@ -75,6 +76,7 @@ struct GemmCfg {
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kXchgBytes + kBarBytes;
   static constexpr int kFeatPerTile = SWIGLU ? kGateUpTileFeat : kDownTileFeat;  // output features per unit
   static_assert(BN % TOKBOX == 0 && TOKBOX % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
+  static_assert(!PAIR || (BN / 2) % TOKBOX == 0, "token boxes of a CTA pair");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
   static_assert(kTmemNeed <= 512, "TMEM has 512 columns");
   static_assert((2 * STAGES + 5 + 8) * 8 + 8 <= kBarBytes, "barrier area");
@@ -182,11 +184,11 @@ __device__ __forceinline__ bool wait_flag(const int32_t* flag, const volatile in
   return ok;
 }
 
-template <bool SWIGLU, int BN, int STAGES, int TOKBOX>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const ExpertGemmArgs args) {
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* xchg = reinterpret_cast<float*>(smem + STAGES * C::kStageBytes);  // [pair][slot][16][32] (gate/up)
@@ -202,6 +204,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kern = SWIGLU ? kKernGemm1 : kKernGemm2;
+  // CTA pair (cluster of 2): rank 0 issues the MMAs for both; the pair takes
+  // work as one worker
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int worker = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int workers = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -210,7 +218,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], PAIR ? 8 : 4);  // the epilogue warps (of both CTAs of a pair)
     }
     mbar_init(done, 1);
     for (int i = 0; i < 4; ++i) {
@@ -221,11 +229,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(tmem_slot, C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();  // the peer's barriers are initialised before any remote signal
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -234,7 +250,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // the immediately preceding kernel need the producer's pdl_wait below.
   const int total_units = __ldg(args.unit_off + args.E);
   const int kblocks = args.K / kBlockK;
-  const int ctas = gridDim.x;
+  const int ctas = workers;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -258,10 +274,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool deps_ready = false;
       int n_pend = 0;
       int pend_stage[STAGES], pend_kb[STAGES], pend_tok0[STAGES], pend_rows[STAGES];
+      // a CTA pair signals every load on the even CTA's full barrier
+      const uint32_t full_cl = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;
+      auto load_2d = [&](void* dst, const CUtensorMap* map, int st, int c0, int c1, uint64_t pol) {
+        if (PAIR)
+          tma_load_2d_pair(dst, map, full_cl + 8u * st, c0, c1, pol);
+        else
+          tma_load_2d(dst, map, &full[st], c0, c1, pol);
+      };
       auto load_tokens = [&](int st, int kb, int tok0, int rows) {
         uint8_t* sb = smem + st * C::kStageBytes + kABytes;
-        for (int r = 0; r < rows; r += TOKBOX)
-          tma_load_2d(sb + r * kTokRowBytes, &tm_x, &full[st], kb * kBlockK, tok0 + r, pol_x);
+        for (int r = 0; r < rows; r += TOKBOX) load_2d(sb + r * kTokRowBytes, &tm_x, st, kb * kBlockK, tok0 + r, pol_x);
       };
       auto resolve_deps = [&]() {
         pdl_wait();
@@ -270,34 +293,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int i = 0; i < n_pend; ++i) load_tokens(pend_stage[i], pend_kb[i], pend_tok0[i], pend_rows[i]);
         n_pend = 0;
       };
-      Range rg(total_units, kblocks, blockIdx.x, ctas, args.stream_k != 0);
+      Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
       int u, kb0, kb1;
       while (ok && rg.next(u, kb0, kb1)) {
         const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
-        const int wrow = un.e * args.w_rows_per_expert + un.tile * C::kFeatPerTile;
-        const int tok_rows = (un.n + TOKBOX - 1) / TOKBOX * TOKBOX;  // whole boxes; rows past n are unused
+        // a pair's unit: weight tiles 2t (even CTA) and 2t+1; the MMA's N
+        // tokens split in halves, the first half in the even CTA
+        const int tile = PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile;
+        const int n_mma = PAIR ? (un.n + 31) / 32 * 32 : un.n;
+        const int half = PAIR ? n_mma / 2 : n_mma;
+        const int tok_first = un.tok0 + static_cast<int>(rank) * half;
+        const int wrow = un.e * args.w_rows_per_expert + tile * C::kFeatPerTile;
+        const int tok_rows = (half + TOKBOX - 1) / TOKBOX * TOKBOX;  // whole boxes; rows past n are unused
         const bool reused = __ldg(args.offsets + un.e + 1) - __ldg(args.offsets + un.e) > BN;
         const uint64_t pol_w = reused ? pol_keep : pol_stream;
-        const uint32_t bytes = kABytes + tok_rows * kTokRowBytes;
+        const uint32_t bytes = kABytes + tok_rows * kTokRowBytes;  // per CTA (the same in both of a pair)
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitTimeoutNs, abort_flag)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + stage * C::kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], bytes);
+          if (!PAIR)
+            mbar_arrive_expect_tx(&full[stage], bytes);
+          else if (leader)
+            mbar_arrive_expect_tx(&full[stage], 2 * bytes);  // both CTAs' loads
           if (SWIGLU) {  // gate rows on top of the matching up rows
-            tma_load_2d(sa, &tm_w, &full[stage], kb * kBlockK, wrow, pol_w);
-            tma_load_2d(sa + kABytes / 2, &tm_w, &full[stage], kb * kBlockK, wrow + args.up_offset, pol_w);
+            load_2d(sa, &tm_w, stage, kb * kBlockK, wrow, pol_w);
+            load_2d(sa + kABytes / 2, &tm_w, stage, kb * kBlockK, wrow + args.up_offset, pol_w);
           } else {
-            tma_load_2d(sa, &tm_w, &full[stage], kb * kBlockK, wrow, pol_w);
+            load_2d(sa, &tm_w, stage, kb * kBlockK, wrow, pol_w);
           }
           if (deps_ready) {
-            load_tokens(stage, kb, un.tok0, tok_rows);
+            load_tokens(stage, kb, tok_first, tok_rows);
           } else {
             pend_stage[n_pend] = stage;
             pend_kb[n_pend] = kb;
-            pend_tok0[n_pend] = un.tok0;
+            pend_tok0[n_pend] = tok_first;
             pend_rows[n_pend] = tok_rows;
             if (++n_pend == STAGES) resolve_deps();
           }
@@ -311,31 +343,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!deps_ready) resolve_deps();  // fewer iterations than stages (or none)
       if (!ok) raise_timeout(args.err, abort_flag, kern);
       // every load this thread issued must have landed before the CTA exits
+      // (the odd CTA of a pair sees that through the release of its stages:
+      // the pair's MMA ran on them, so they had landed)
       for (int s = 0; s < STAGES; ++s) {
         if (issued <= s) break;
         const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
         int dummy = 0;
-        mbar_wait(&full[s], par, kWaitTimeoutNs, &dummy);
+        mbar_wait(PAIR && !leader ? &empty[s] : &full[s], par, kWaitTimeoutNs, &dummy);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (the even CTA of a pair issues for both)
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      Range rg(total_units, kblocks, blockIdx.x, ctas, args.stream_k != 0);
+      Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
       int u, kb0, kb1;
       while (ok && rg.next(u, kb0, kb1)) {
         const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, kWaitTimeoutNs, abort_flag)) {
+        const bool free_acc = PAIR ? mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, kWaitTimeoutNs, abort_flag)
+                                   : mbar_wait(&tempty[acc], acc_phase ^ 1u, kWaitTimeoutNs, abort_flag);
+        if (!free_acc) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(un.n));
+        const int n_mma = PAIR ? (un.n + 31) / 32 * 32 : un.n;
+        const uint32_t idesc = idesc_bf16_f32(PAIR ? 256 : 128, static_cast<uint32_t>(n_mma));
         const uint32_t d_acc = tmem_base + static_cast<uint32_t>(acc * C::kAccCols);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, kWaitTimeoutNs, abort_flag)) {
@@ -348,22 +385,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBlockK / 16; ++k) {
             const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;  // each segment starts a fresh sum
-            mma_bf16_ss(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc, accum);
+            if (PAIR)
+              mma_bf16_ss_pair(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc, accum);
+            else
+              mma_bf16_ss(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc, accum);
           }
-          mma_commit(&empty[stage]);
+          if (PAIR)
+            mma_commit_pair_mc(&empty[stage], 0x3);  // frees the stage in both CTAs
+          else
+            mma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
+        if (PAIR)
+          mma_commit_pair_mc(&tfull[acc], 0x3);
+        else
+          mma_commit(&tfull[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       if (!ok) raise_timeout(args.err, abort_flag, kern);
       // all MMAs this thread issued have finished before TMEM is released
-      mma_commit(done);
+      if (PAIR)
+        mma_commit_pair(done);
+      else
+        mma_commit(done);
       int dummy = 0;
       mbar_wait(done, 0, kWaitTimeoutNs, &dummy);
     }
@@ -382,7 +431,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     float* xb = xchg + pair * 2 * C::kXchgFloats;
     // this CTA's partial-sum slot: [BN columns][128 rows] fp32
     float* my_slot = args.partials + static_cast<int64_t>(blockIdx.x) * BN * 128;
-    Range rg(total_units, kblocks, blockIdx.x, ctas, args.stream_k != 0);
+    const uint32_t tempty_cl = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
+    Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
     int u, kb0, kb1;
     while (ok && rg.next(u, kb0, kb1)) {
       const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
@@ -415,7 +465,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int c_last = blockIdx.x;  // producers are the CTAs in (blockIdx.x, c_last] with non-empty ranges
         if (kb1 < kblocks)
           while (c_last + 1 < ctas && range_start(rg.W, c_last + 1, ctas) < unit_end) ++c_last;
-        const int feat_base = un.tile * C::kFeatPerTile;
+        const int feat_base = (PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile) * C::kFeatPerTile;
         for (int c0 = 0; c0 < un.n && ok; c0 += 16, ++xit) {
           uint32_t ra[16];
           tmem_ld_32x32b_x16(t_row + c0, ra);
@@ -480,7 +530,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) break;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(tempty_cl + 8u * acc);  // the even CTA's MMA waits for both CTAs
+        else
+          mbar_arrive(&tempty[acc]);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -488,36 +543,76 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   __syncthreads();
+  // a pair keeps both CTAs (their shared memory, barriers and TMEM, which the
+  // pair's MMAs and signals reach) until both are done
+  if (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
-template <bool SWIGLU, int BN, int STAGES, int TOKBOX>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR>
 cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, int num_sms,
                                cudaStream_t stream) {
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR>;
+  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR>;
   static int configured_device = -1;
+  static int max_pairs = 0;  // CTA pairs that fit on the configured device at once
   int dev = 0;
-  cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return e;
+    if (PAIR) {
+      cfg.gridDim = dim3(2 * (kMaxGemmCtas / 2));
+      cfg.attrs = attr + 1;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n <= 0) return cudaErrorInvalidConfiguration;
+      max_pairs = n;
+    }
     configured_device = dev;
   }
-  const int grid = num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas;
-  return launch_pdl(expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX>, dim3(grid), dim3(kGemmThreads),
-                    C::kSmemBytes, stream, tw, tx, a);
+  int grid;
+  if (PAIR) {
+    const int pairs = max_pairs < kMaxGemmCtas / 2 ? max_pairs : kMaxGemmCtas / 2;
+    grid = 2 * pairs;
+  } else {
+    grid = num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas;
+  }
+  cfg.gridDim = dim3(grid);
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tw, tx, a);
 }
 
 // Three tile plans by the expected tokens per expert (T*top_k/E):
 //   small (<= 16): 32-token units, deep weight pipelines (decode);
 //   mid   (<= 64): 64-token units, so most experts still fit one chunk;
-//   large (> 64) : 256-token units and 64-row token boxes (prefill).
+//   large (> 64) : 256-token units and 64-row token boxes (prefill), on CTA
+//                  pairs (M = 256 MMAs, each CTA loads half of the token tile)
+//                  when the expert's weight tiles come in pairs.
 constexpr int kGateUpBn[3] = {32, 64, 256}, kGateUpStages[3] = {10, 8, 4};  // stages of 20 / 24 / 48 KB
 constexpr int kDownBn[3] = {32, 64, 256}, kDownStages[3] = {10, 8, 4};      // stages of 20 / 24 / 48 KB
+constexpr int kPairStages = 6;                                              // stages of 32 KB
 // token rows per TMA box: small units hold few tokens (16-row boxes waste
 // nothing); large units hold up to 256 (64-row boxes: 4x fewer TMA requests)
 constexpr int kTokBox[3] = {16, 16, 64};
@@ -527,16 +622,24 @@ constexpr int kTokBox[3] = {16, 16, 64};
 int gemm_gate_up_bn(GemmPlan plan) { return kGateUpBn[static_cast<int>(plan)]; }
 int gemm_down_bn(GemmPlan plan) { return kDownBn[static_cast<int>(plan)]; }
 int gemm_tok_box_rows(GemmPlan plan) { return kTokBox[static_cast<int>(plan)]; }
+bool gemm_uses_pairs(GemmPlan plan, int tiles) { return plan == GemmPlan::kLarge && tiles % 2 == 0; }
+int gemm_unit_tiles(GemmPlan plan, int tiles) { return gemm_uses_pairs(plan, tiles) ? tiles / 2 : tiles; }
 
 cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
                                 GemmPlan plan, int num_sms, cudaStream_t stream) {
   switch (plan) {
     case GemmPlan::kSmall:
-      return launch_expert_gemm<true, kGateUpBn[0], kGateUpStages[0], kTokBox[0]>(tm_w13, tm_x, a, num_sms, stream);
+      return launch_expert_gemm<true, kGateUpBn[0], kGateUpStages[0], kTokBox[0], false>(tm_w13, tm_x, a, num_sms,
+                                                                                          stream);
     case GemmPlan::kMid:
-      return launch_expert_gemm<true, kGateUpBn[1], kGateUpStages[1], kTokBox[1]>(tm_w13, tm_x, a, num_sms, stream);
+      return launch_expert_gemm<true, kGateUpBn[1], kGateUpStages[1], kTokBox[1], false>(tm_w13, tm_x, a, num_sms,
+                                                                                          stream);
     default:
-      return launch_expert_gemm<true, kGateUpBn[2], kGateUpStages[2], kTokBox[2]>(tm_w13, tm_x, a, num_sms, stream);
+      if (a.pair)
+        return launch_expert_gemm<true, kGateUpBn[2], kPairStages, kTokBox[2], true>(tm_w13, tm_x, a, num_sms,
+                                                                                      stream);
+      return launch_expert_gemm<true, kGateUpBn[2], kGateUpStages[2], kTokBox[2], false>(tm_w13, tm_x, a, num_sms,
+                                                                                          stream);
   }
 }
 
@@ -544,11 +647,17 @@ cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act
                              GemmPlan plan, int num_sms, cudaStream_t stream) {
   switch (plan) {
     case GemmPlan::kSmall:
-      return launch_expert_gemm<false, kDownBn[0], kDownStages[0], kTokBox[0]>(tm_w2, tm_act, a, num_sms, stream);
+      return launch_expert_gemm<false, kDownBn[0], kDownStages[0], kTokBox[0], false>(tm_w2, tm_act, a, num_sms,
+                                                                                       stream);
     case GemmPlan::kMid:
-      return launch_expert_gemm<false, kDownBn[1], kDownStages[1], kTokBox[1]>(tm_w2, tm_act, a, num_sms, stream);
+      return launch_expert_gemm<false, kDownBn[1], kDownStages[1], kTokBox[1], false>(tm_w2, tm_act, a, num_sms,
+                                                                                       stream);
     default:
-      return launch_expert_gemm<false, kDownBn[2], kDownStages[2], kTokBox[2]>(tm_w2, tm_act, a, num_sms, stream);
+      if (a.pair)
+        return launch_expert_gemm<false, kDownBn[2], kPairStages, kTokBox[2], true>(tm_w2, tm_act, a, num_sms,
+                                                                                     stream);
+      return launch_expert_gemm<false, kDownBn[2], kDownStages[2], kTokBox[2], false>(tm_w2, tm_act, a, num_sms,
+                                                                                       stream);
   }
 }
 

@@ -234,6 +234,9 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   const Layout L = make_layout(s);
   const GemmPlan plan = moe::choose_plan(s.T, s.top_k, s.E);
   const int bn1 = moe::gemm_gate_up_bn(plan), bn2 = moe::gemm_down_bn(plan);
+  // work-unit tables count weight tiles, or pairs of them for CTA-pair GEMMs
+  const int tiles1 = s.I / moe::kGateUpTileFeat, tiles2 = s.H / moe::kDownTileFeat;
+  const int utiles1 = moe::gemm_unit_tiles(plan, tiles1), utiles2 = moe::gemm_unit_tiles(plan, tiles2);
   auto mark = [&](int i) {
     return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), cs) == cudaSuccess;
   };
@@ -258,15 +261,15 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   if (moe::align_fuses_topk(s.T, s.E)) {
     if (!mark(2)) return MOE_ERR_CUDA;
     ce = moe::launch_align(at<float>(workspace, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(workspace, L.ids),
-                           at<float>(workspace, L.w), N, s.E, moe::kPadRows, bn1, s.I / moe::kGateUpTileFeat, bn2,
-                           s.H / moe::kDownTileFeat, at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.offsets),
+                           at<float>(workspace, L.w), N, s.E, moe::kPadRows, bn1, utiles1, bn2, utiles2,
+                           at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.offsets),
                            at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.slot),
                            at<int32_t>(workspace, L.unit1), at<int32_t>(workspace, L.unit2), err,
                            at<int32_t>(workspace, L.flags), kGemmFlagInts, cs);
   } else {
     ce = moe::launch_align_multi(at<float>(workspace, L.logits), s.T, s.top_k, s.renormalize,
                                  at<int32_t>(workspace, L.ids), at<float>(workspace, L.w), s.E, moe::kPadRows, bn1,
-                                 s.I / moe::kGateUpTileFeat, bn2, s.H / moe::kDownTileFeat,
+                                 utiles1, bn2, utiles2,
                                  at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.offsets),
                                  at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.slot),
                                  at<int32_t>(workspace, L.unit1), at<int32_t>(workspace, L.unit2),
@@ -286,7 +289,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a1.unit_off = at<int32_t>(workspace, L.unit1);
   a1.E = s.E;
   a1.K = s.H;
-  a1.tiles_per_expert = s.I / moe::kGateUpTileFeat;
+  a1.tiles_per_expert = utiles1;
   a1.w_rows_per_expert = 2 * s.I;
   a1.up_offset = s.I;
   a1.n_out = s.I;
@@ -295,6 +298,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a1.partials = at<float>(workspace, L.partials);
   a1.flags = at<int32_t>(workspace, L.flags);
   a1.stream_k = plan == GemmPlan::kSmall;
+  a1.pair = moe::gemm_uses_pairs(plan, tiles1);
   if (moe::launch_gemm_gate_up(tm_w13, tm_xg, a1, plan, num_sms, cs) != cudaSuccess || !mark(5)) return MOE_ERR_CUDA;
 
   moe::ExpertGemmArgs a2{};
@@ -302,7 +306,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a2.unit_off = at<int32_t>(workspace, L.unit2);
   a2.E = s.E;
   a2.K = s.I;
-  a2.tiles_per_expert = s.H / moe::kDownTileFeat;
+  a2.tiles_per_expert = utiles2;
   a2.w_rows_per_expert = s.H;
   a2.up_offset = 0;
   a2.n_out = s.H;
@@ -311,6 +315,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a2.partials = at<float>(workspace, L.partials + partial_slots_bytes(s));  // own slots and flags: the
   a2.flags = at<int32_t>(workspace, L.flags) + moe::kMaxGemmCtas * 4;        // two GEMMs may overlap
   a2.stream_k = plan == GemmPlan::kSmall;
+  a2.pair = moe::gemm_uses_pairs(plan, tiles2);
   if (moe::launch_gemm_down(tm_w2, tm_act, a2, plan, num_sms, cs) != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
 
   if (moe::launch_combine(at<uint16_t>(workspace, L.out), at<int32_t>(workspace, L.slot), at<float>(workspace, L.w),

@@ -69,6 +69,7 @@ struct ExpertGemmArgs {
   float* partials;          // stream-K partial sums: [kMaxGemmCtas][BN][128] fp32
   int32_t* flags;           // [kMaxGemmCtas * 4], zero on entry; left zero on exit
   int stream_k;             // 1: equal K-block ranges per CTA; 0: whole units round-robin
+  int pair;                 // 1: CTA pairs, a unit = weight tiles 2t and 2t+1 (large plan only)
 };
 // persistent GEMM grid: min(SM count, kMaxGemmCtas) CTAs
 constexpr int kMaxGemmCtas = 256;
@@ -87,6 +88,10 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm
                                 GemmPlan plan, int num_sms, cudaStream_t stream);
 cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const ExpertGemmArgs& a,
                              GemmPlan plan, int num_sms, cudaStream_t stream);
+// Whether a GEMM with `tiles` weight tiles per expert runs on CTA pairs, and
+// the tiles per expert its work-unit table counts (pairs of tiles then).
+bool gemm_uses_pairs(GemmPlan plan, int tiles);
+int gemm_unit_tiles(GemmPlan plan, int tiles);
 // token rows per unit (B-operand width) and rows per TMA box of the token tile
 int gemm_gate_up_bn(GemmPlan plan);
 int gemm_down_bn(GemmPlan plan);

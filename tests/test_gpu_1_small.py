@@ -28,6 +28,8 @@ CASES = [
     ("deep_k", 64, 1024, 512, 8, 2, True, None, 2),
     ("prefill_chunks", 1024, 256, 256, 4, 2, True, None, 4),
     ("prefill_ragged_norenorm", 300, 384, 128, 6, 3, False, None, 5),
+    ("prefill_pairs_ragged", 700, 512, 384, 5, 2, True, None, 10),
+    ("prefill_skewed", 512, 256, 256, 16, 4, True, 1.2, 11),
     ("skewed_bias", 96, 256, 256, 32, 6, True, 1.2, 7),
     ("mid_multichunk", 200, 256, 256, 8, 2, True, None, 9),
     ("single_expert", 20, 128, 128, 1, 1, True, None, 6),
