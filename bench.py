@@ -280,17 +280,19 @@ def run_ours(args, wl, world, rank, local):
     kern_ev = {T: [new_events() for _ in range(args.steps)] for T in Ts}
     setup_s = time.time() - t_setup
 
+    ff = args.fused_front
+
     def one_step(step_idx=None, per_kernel=False):
         for T in Ts:
             flush_l2(step_idx or 0)
             if step_idx is None:
-                layer.forward(xs[T], ys[T])
+                layer.forward(xs[T], ys[T], fused_front=ff)
             elif per_kernel:
-                layer.forward(xs[T], ys[T], events=[e.cuda_event for e in kern_ev[T][step_idx]])
+                layer.forward(xs[T], ys[T], events=[e.cuda_event for e in kern_ev[T][step_idx]], fused_front=ff)
             else:
                 a, b = call_ev[T][step_idx]
                 a.record(stream)
-                layer.forward(xs[T], ys[T])
+                layer.forward(xs[T], ys[T], fused_front=ff)
                 b.record(stream)
 
     for _ in range(args.warmup):
@@ -352,6 +354,7 @@ def run_ours(args, wl, world, rank, local):
                          "weight_GB": round(lb["weights"] / 1e9, 4),
                          "weight_GBps": round(lb["weights"] / (us * 1e-6) / 1e9, 1),
                          "hbm_frac_of_8TBps": round(lb["weights"] / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
+                         "kernels_per_call": 4 if ff else binding.kernels_per_call(T, H, wl["I"], wl["E"], wl["k"]),
                          "kernel_us_median": {n: round(statistics.median(v) * 1e3, 2) for n, v in kt.items()}}
     ms_per_step = total_ms / args.steps
     tokens_per_step = sum(Ts)
@@ -411,10 +414,13 @@ def run_ours(args, wl, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator; random-init weights)",
         "config": {"workload": wl["label"], "tokens_per_step": tokens_per_step,
                    "layer_calls_per_step": len(Ts),
+                   "front_end": ("moe_forward_fused_front: norm .. gather in one cluster launch" if ff
+                                 else "moe_forward: multi-launch front end"),
                    "l2": "flushed before every layer call (256 MB write, then a 256 MB read of another buffer so "
                          "no dirty lines remain); flush outside the timed CUDA-event intervals",
                    "timing": "CUDA events on the launch stream around each plain moe_forward call; kernel times from "
-                             "a second pass of the same calls through moe_forward_events",
+                             "a second pass of the same calls through moe_forward_events (with 4 kernels per call, "
+                             "'norm_router' is the single-launch front end: norm, router, top-k, align and gather)",
                    "parallelism": f"replicas x{world} (no cross-GPU data path)", "per_T": per_T,
                    "kernel_ms_per_step": {n: round(v / args.steps, 4) for n, v in kern_ms.items()},
                    "wall_s_timed_region": round(t_wall, 3), "setup_s": round(setup_s, 1)},
@@ -422,7 +428,8 @@ def run_ours(args, wl, world, rank, local):
         "e2e": e2e,
         # kernels of the timed pass (top-k runs inside the align kernel for small T and E); the per-kernel pass
         # launches as many again
-        "gpu_launches": sum(args.steps * binding.kernels_per_call(T, wl["E"]) for T in Ts),
+        "gpu_launches": sum(args.steps * (4 if ff else binding.kernels_per_call(T, wl["H"], wl["I"], wl["E"], wl["k"]))
+                            for T in Ts),
         "clocks": clocks,
     }
     return out, host
@@ -439,6 +446,8 @@ def main():
                     help="CPU oracle sample: at most this many tokens of each batch per step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum timed CPU-oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused-front", action="store_true",
+                    help="time moe_forward_fused_front (norm .. gather in one cluster launch; T <= 64)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("bench: at least 3 warm-up steps are required; using 3", file=sys.stderr)

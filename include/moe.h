@@ -124,12 +124,17 @@ MOE_API moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const 
 #define MOE_FUSED_TOPK_MAX_T 256
 #define MOE_FUSED_TOPK_MAX_E 256
 
+/* Number of kernels one moe_forward call with this shape launches on the
+ * current device (0 for T = 0).  Host-only apart from querying the device. */
+MOE_API moe_status moe_kernels_per_call(const moe_shape* shape, int32_t* count);
+
 /* moe_forward, plus CUDA events recorded on `stream` around the kernels:
  * events[0] before kernel 1 and events[i] right after kernel i (i = 1..7),
  * so cudaEventElapsedTime(events[i-1], events[i]) is kernel i's time on the
  * stream (with top-k fused into the align kernel, events[2] follows events[1]
  * at once and the align interval includes the top-k; otherwise events[2] ends
- * the top-k/count kernel and events[3] the scan and scatter kernels).  `events` holds n_events >= MOE_NUM_KERNELS + 1 cudaEvent_t
+ * the top-k/count kernel and events[3] the scan and scatter kernels; with the
+ * single-launch front end, events[1] ends it and events[2..4] follow at once).  `events` holds n_events >= MOE_NUM_KERNELS + 1 cudaEvent_t
  * handles created by the caller (cudaEventCreate); the library records them
  * and does not create, wait on or destroy them.  Everything else is as for
  * moe_forward; with T = 0 no event is recorded. */
@@ -137,6 +142,26 @@ MOE_API moe_status moe_forward_events(const moe_shape* shape, const moe_bf16* x,
                                       const float* w_router, const float* router_bias, const moe_bf16* w13,
                                       const moe_bf16* w2, moe_bf16* y, void* workspace, size_t workspace_bytes,
                                       moe_stream_t stream, void* const* events, int32_t n_events);
+
+/* moe_forward with steps 1-4 (norm, router, top-k, align, gather) run as one
+ * launch of one thread-block cluster: the decode dispatch as a single kernel
+ * with a grid-wide barrier ("CuTeDSL chez Perplexity", "Synchronisation de la
+ * grille"), here the cluster's hardware barrier (4 launches per call).  For
+ * T <= MOE_FRONT_MAX_T and E <= MOE_FRONT_MAX_E on a device that runs a
+ * cluster of at least 8 such CTAs; other shapes return MOE_ERR_UNSUPPORTED
+ * before anything is enqueued.  Results are the same bits as moe_forward's;
+ * the padding rows of the gathered input (moe_views.xg) are not written.
+ * `events` is NULL, or as for moe_forward_events (the front end's time falls
+ * in events[0]..events[1]).  moe_forward stays the faster choice on GB300:
+ * there the expert GEMM cannot start its weight loads until the whole front
+ * end has finished, and 16 SMs read the router weights more slowly than the
+ * multi-launch router's grid. */
+#define MOE_FRONT_MAX_T 64
+#define MOE_FRONT_MAX_E 256
+MOE_API moe_status moe_forward_fused_front(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                                           const float* w_router, const float* router_bias, const moe_bf16* w13,
+                                           const moe_bf16* w2, moe_bf16* y, void* workspace, size_t workspace_bytes,
+                                           moe_stream_t stream, void* const* events, int32_t n_events);
 
 /* Routing front end only (RMSNorm, router, top-k, align with `pad_rows`
  * rows of padding granularity), with the results copied out:
@@ -214,6 +239,18 @@ MOE_API moe_status moe_device_status(const void* workspace, size_t workspace_byt
                              int32_t* detail);
 
 /* Static text for a status code. */
+/* Self-test of the failure path of the library's bounded device waits (no
+ * counterpart on the pages): enqueues one small kernel whose two waits -- on
+ * an mbarrier phase that nothing completes and on a flag in the workspace's
+ * error area that nothing sets -- give up after timeout_ns (1 .. 1e9) and
+ * record MOE_ERR_TIMEOUT, with kernel id 8 in detail[1], in the workspace's
+ * error word, then return normally.  moe_device_status() afterwards returns
+ * MOE_ERR_TIMEOUT; the CUDA context stays usable, and the next moe_forward on
+ * that workspace clears the word.  workspace: >= 64 bytes, 256-byte aligned;
+ * its first 64 bytes are overwritten. */
+MOE_API moe_status moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t timeout_ns,
+                                             moe_stream_t stream);
+
 MOE_API const char* moe_status_string(moe_status status);
 
 #ifdef __cplusplus

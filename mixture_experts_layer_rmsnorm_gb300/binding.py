@@ -64,10 +64,14 @@ def load(build: bool = True):
             lib.moe_forward_static_scratch.argtypes = [sp, p, p, p, p, p, p, p, p]
             lib.moe_workspace_views.argtypes = [sp, p, sz, ctypes.POINTER(MoeViews)]
             lib.moe_device_status.argtypes = [p, sz, p, ctypes.POINTER(ctypes.c_int32)]
+            lib.moe_kernels_per_call.argtypes = [sp, ctypes.POINTER(ctypes.c_int32)]
+            lib.moe_selftest_wait_timeout.argtypes = [p, sz, i64, p]
+            lib.moe_forward_fused_front.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_status_string.argtypes = [ctypes.c_int]
             lib.moe_status_string.restype = ctypes.c_char_p
             for f in ("moe_workspace_size", "moe_forward", "moe_forward_events", "moe_route_debug",
-                      "moe_workspace_views", "moe_device_status", "moe_forward_static_scratch"):
+                      "moe_workspace_views", "moe_device_status", "moe_forward_static_scratch",
+                      "moe_kernels_per_call", "moe_forward_fused_front", "moe_selftest_wait_timeout"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -94,14 +98,26 @@ def moe_forward(s: MoeShape, x, g_norm, w_router, router_bias, w13, w2, y, works
 
 
 MOE_NUM_KERNELS = 7
+MOE_FRONT_MAX_T = 64  # single-launch front end (norm .. gather) up to this many tokens ...
+MOE_FRONT_MAX_E = 256  # ... and experts
 MOE_FUSED_TOPK_MAX_T = 256  # top-k runs inside the align kernel up to this many tokens ...
 MOE_FUSED_TOPK_MAX_E = 256  # ... and experts
 
 
-def kernels_per_call(T: int, E: int) -> int:
-    """Kernel launches of one moe_forward call (T > 0)."""
-    fused = T <= MOE_FUSED_TOPK_MAX_T and E <= MOE_FUSED_TOPK_MAX_E
-    return 6 if fused else 8
+def moe_kernels_per_call(s: MoeShape) -> tuple[int, int]:
+    n = ctypes.c_int32(0)
+    st = load().moe_kernels_per_call(ctypes.byref(s), ctypes.byref(n))
+    return st, n.value
+
+
+def kernels_per_call(T: int, H: int, I: int, E: int, top_k: int) -> int:
+    """Kernel launches of one moe_forward call on the current device."""
+    st, n = moe_kernels_per_call(shape(T, H, I, E, top_k))
+    if st != MOE_OK:
+        raise MoeError(st, "moe_kernels_per_call")
+    return n
+
+
 KERNEL_NAMES = ("norm_router", "topk_softmax", "align", "gather", "gemm_gate_up_swiglu", "gemm_down", "combine")
 
 
@@ -111,6 +127,17 @@ def moe_forward_events(s: MoeShape, x, g_norm, w_router, router_bias, w13, w2, y
     arr = (ctypes.c_void_p * len(events))(*events)
     return load().moe_forward_events(ctypes.byref(s), x, g_norm, w_router, router_bias, w13, w2, y, workspace,
                                      workspace_bytes, stream, arr, len(events))
+
+
+def moe_forward_fused_front(s: MoeShape, x, g_norm, w_router, router_bias, w13, w2, y, workspace,
+                            workspace_bytes, stream, events=None) -> int:
+    """moe_forward with norm .. gather as one cluster launch (decode shapes only)."""
+    if events is None:
+        arr, n = None, 0
+    else:
+        arr, n = (ctypes.c_void_p * len(events))(*events), len(events)
+    return load().moe_forward_fused_front(ctypes.byref(s), x, g_norm, w_router, router_bias, w13, w2, y, workspace,
+                                          workspace_bytes, stream, arr, n)
 
 
 MOE_STATIC_SCRATCH_BYTES = 64 << 20
@@ -138,6 +165,10 @@ def moe_device_status(workspace, workspace_bytes, stream) -> tuple[int, list]:
     d = (ctypes.c_int32 * 4)()
     st = load().moe_device_status(workspace, workspace_bytes, stream, d)
     return st, list(d)
+
+
+def moe_selftest_wait_timeout(workspace, workspace_bytes, timeout_ns, stream) -> int:
+    return load().moe_selftest_wait_timeout(workspace, workspace_bytes, int(timeout_ns), stream)
 
 
 def _ptr(t):
@@ -181,9 +212,10 @@ class MoeLayer:
             raise MoeError(st, "moe_workspace_size")
         return n
 
-    def forward(self, x, y=None, stream=None, events=None):
+    def forward(self, x, y=None, stream=None, events=None, fused_front=False):
         """y = layer(x).  events: optional MOE_NUM_KERNELS + 1 cudaEvent_t handles
-        recorded around the kernels (moe_forward_events)."""
+        recorded around the kernels (moe_forward_events).  fused_front: run the
+        norm .. gather steps as one cluster launch (moe_forward_fused_front)."""
         import torch
         T = x.shape[0]
         self.ensure_capacity(T)
@@ -192,7 +224,9 @@ class MoeLayer:
         s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
         args = (self.shape(T), _ptr(x), _ptr(self.g_norm), _ptr(self.w_router), _ptr(self.bias), _ptr(self.w13),
                 _ptr(self.w2), _ptr(y), _ptr(self.workspace), self.workspace_bytes(T), s)
-        if events is None:
+        if fused_front:
+            st = moe_forward_fused_front(*args, events)
+        elif events is None:
             st = moe_forward(*args)
         else:
             st = moe_forward_events(*args, events)

@@ -3,10 +3,14 @@
 
 namespace moe {
 
-// Exclusive scan over a block of exactly 1024 threads (32 warps).  `tmp` is
-// 33 ints of shared memory.  Returns this thread's exclusive prefix; *total
-// receives the block total.  Contains __syncthreads(): all threads must call.
-__device__ __forceinline__ int block_exclusive_scan_1024(int v, int* tmp, int* total) {
+// Exclusive scan over a block of exactly NT threads (NT a multiple of 32, at
+// most 1024).  `tmp` is 33 ints of shared memory.  Returns this thread's
+// exclusive prefix; *total receives the block total.  Contains
+// __syncthreads(): all threads must call.
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int v, int* tmp, int* total) {
+  static_assert(NT % 32 == 0 && NT <= 1024, "block size");
+  constexpr int kWarps = NT / 32;
   constexpr unsigned kAll = 0xFFFFFFFFu;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int inc = v;
@@ -18,7 +22,7 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* tmp, int* t
   if (lane == 31) tmp[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    const int w = tmp[lane];
+    const int w = (lane < kWarps) ? tmp[lane] : 0;
     int winc = w;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -33,6 +37,10 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* tmp, int* t
   *total = tmp[32];
   __syncthreads();
   return r;
+}
+
+__device__ __forceinline__ int block_exclusive_scan_1024(int v, int* tmp, int* total) {
+  return block_exclusive_scan<1024>(v, tmp, total);
 }
 
 }  // namespace moe

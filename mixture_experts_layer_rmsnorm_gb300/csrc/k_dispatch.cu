@@ -14,7 +14,7 @@
 // run.
 #include <cuda_bf16.h>
 
-#include "block_scan.cuh"
+#include "align_core.cuh"
 #include "moe_kernels.cuh"
 #include "pdl.cuh"
 #include "topk.cuh"
@@ -56,18 +56,10 @@ __global__ void __launch_bounds__(kAlignThreads)
     __syncthreads();
   }
 
-  if (tid == 0) bad = 0;
-  for (int e = tid; e < E; e += kAlignThreads) cnt[e] = 0;
-  __syncthreads();
-  for (int i = tid; i < N; i += kAlignThreads) {
-    const int e = __ldcg(ids + i);
-    if (e < 0 || e >= E)
-      bad = 1;
-    else
-      atomicAdd(&cnt[e], 1);
-  }
-  __syncthreads();
-  if (bad) {
+  const bool ok = align_core<kAlignThreads>([&](int i) { return __ldcg(ids + i); }, N, E, pad, bn1, tiles1, bn2,
+                                             tiles2, cnt, cursor, wbase, scan_tmp, &bad, counts, offsets, sorted_ids,
+                                             slot_of, unit_off1, unit_off2);
+  if (!ok) {
     if (tid == 0) {
       err[1] = kKernAlign;
       err[0] = kErrDevice;
@@ -81,64 +73,6 @@ __global__ void __launch_bounds__(kAlignThreads)
       if (e < E) counts[e] = 0;
     }
     for (int i = tid; i < N; i += kAlignThreads) slot_of[i] = 0;
-    return;
-  }
-
-  // padded sizes, offsets and work-unit prefix sums (E <= 1024: one pass)
-  {
-    const int e = tid;
-    const int c = (e < E) ? cnt[e] : 0;
-    const int p = (c + pad - 1) / pad * pad;
-    const int u1 = (bn1 > 0) ? (p + bn1 - 1) / bn1 * tiles1 : 0;
-    const int u2 = (bn2 > 0) ? (p + bn2 - 1) / bn2 * tiles2 : 0;
-    int tot_p, tot_u1, tot_u2;
-    const int off = block_exclusive_scan_1024(p, scan_tmp, &tot_p);
-    const int o1 = block_exclusive_scan_1024(u1, scan_tmp, &tot_u1);
-    const int o2 = block_exclusive_scan_1024(u2, scan_tmp, &tot_u2);
-    if (e < E) {
-      counts[e] = c;
-      offsets[e] = off;
-      cursor[e] = off;
-      if (unit_off1) unit_off1[e] = o1;
-      if (unit_off2) unit_off2[e] = o2;
-      // padding rows of this expert's list
-      for (int q = off + c; q < off + p; ++q) sorted_ids[q] = N;
-    }
-    if (tid == 0) {
-      offsets[E] = tot_p;
-      if (unit_off1) unit_off1[E] = tot_u1;
-      if (unit_off2) unit_off2[E] = tot_u2;
-    }
-  }
-  __syncthreads();
-
-  // stable ranks, 1024 routing entries per round
-  for (int base = 0; base < N; base += kAlignThreads) {
-    const int i = base + tid;
-    const bool valid = i < N;
-    const int e = valid ? __ldcg(ids + i) : -1;
-    const unsigned same = __match_any_sync(kFull, e);
-    const int rank = __popc(same & ((1u << lane) - 1u));
-    for (int q = tid; q < kAlignWarps * E; q += kAlignThreads) wbase[q] = 0;
-    __syncthreads();
-    if (valid && rank == 0) wbase[warp * E + e] = __popc(same);
-    __syncthreads();
-    for (int ex = tid; ex < E; ex += kAlignThreads) {
-      int run = cursor[ex];
-      for (int w = 0; w < kAlignWarps; ++w) {
-        const int c = wbase[w * E + ex];
-        wbase[w * E + ex] = run;
-        run += c;
-      }
-      cursor[ex] = run;
-    }
-    __syncthreads();
-    if (valid) {
-      const int pos = wbase[warp * E + e] + rank;
-      sorted_ids[pos] = i;
-      slot_of[i] = pos;
-    }
-    __syncthreads();
   }
 }
 

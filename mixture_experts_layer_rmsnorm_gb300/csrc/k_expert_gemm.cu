@@ -13,12 +13,13 @@
 //
 // Gate/up: W13[e] holds W_gate^T in rows [0, I) and W_up^T in rows [I, 2I) (the
 // concatenated (d x 2 d_ff) weight of "4 · La fusion de noyaux", §4.2
-// "GEMM + GEMM").  A unit stacks the gate rows [i0, i0+64) on the matching up
-// rows [I+i0, I+i0+64) into one 128-row A tile, so one MMA per K step leaves
-// gate(i0+l) in TMEM lane l and up(i0+l) in lane 64+l.  The epilogue warp
-// reading lanes 64..127 hands its up values through shared memory to the warp
-// reading lanes 0..63, which applies SiLU(gate) * up to the accumulators
-// before the only store ("GEMM + épilogue", §4.2).
+// "GEMM + GEMM").  A unit covers 64 features [i0, i0+64): its 128-row A tile
+// interleaves them in groups of 16, gate rows i0+16g .. +15 then the matching
+// up rows, for g = 0..3 (one 5-D TMA box over the [E][2][I/16][16][H] view of
+// W13).  One MMA per K step then leaves, in the 32 TMEM lanes of epilogue warp
+// g, gate(i0+16g+l) in lane l and up(i0+16g+l) in lane 16+l, so the warp pairs
+// them with one shuffle and applies SiLU(gate) * up to the accumulators before
+// the only store ("GEMM + épilogue", §4.2).
 //
 // Work split.  Units are dealt round-robin to the persistent CTAs, except in
 // the decode tile plan (each weight tile read once, so no L2 reuse to keep),
@@ -34,9 +35,9 @@
 // before its epilogue, so it never waits on work that has not started.
 //
 // Roles in a CTA of 192 threads (persistent, one CTA per SM):
-//   warp 0 lane 0   TMA producer: weight tiles [128 x 64] (gate/up: two boxes
-//                   of 64 rows) and token tiles of TOKBOX rows per box, 128-byte
-//                   swizzle, into a STAGES-deep ring
+//   warp 0 lane 0   TMA producer: weight tiles [128 x 64] (one box) and token
+//                   tiles of TOKBOX rows per box, 128-byte swizzle, into a
+//                   STAGES-deep ring
 //   warp 1          owns the TMEM allocation; lane 0 issues tcgen05.mma and
 //                   tcgen05.commit (frees a ring slot / hands an accumulator
 //                   buffer to the epilogue)
@@ -45,9 +46,21 @@
 // Two accumulator buffers in TMEM let the epilogue of one range segment
 // overlap the MMAs of the next.  Every wait is bounded; a wait that runs out
 // sets the workspace error word and the kernel winds down.
+//
+// CTA pairs (prefill tiles).  A cluster of two CTAs on one TPC works as one
+// worker: a unit is weight tiles 2t (even CTA) and 2t+1 (odd CTA) x up to 256
+// tokens.  The even CTA's thread issues tcgen05.mma.cta_group::2 (M = 256):
+// each CTA supplies its 128 weight rows and half of the token tile from its
+// own shared memory and receives its 128 rows of the accumulator in its own
+// TMEM.  Both CTAs' TMA loads signal the even CTA's ring barrier; its MMA
+// commits release the ring slot and hand over the accumulator in both CTAs;
+// both CTAs' epilogue warps report a drained accumulator to the even CTA.
+// Per SM a stage holds half the token bytes of a one-CTA unit of the same
+// size, which leaves room for a 7-deep ring.
 #include <cuda_bf16.h>
 
 #include "moe_kernels.cuh"
+#include "bounded_wait.cuh"
 #include "pdl.cuh"
 #include "tc_ptx.cuh"
 
@@ -57,6 +70,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kGemmThreads = 192;
+constexpr int kTabMaxE = 256;
 constexpr int kABytes = kWeightBoxRows * kBlockK * 2;  // 16 KB weight tile per stage
 constexpr int kTokRowBytes = kBlockK * 2;              // 128 B per token row per stage
 
@@ -69,17 +83,16 @@ struct GemmCfg {
   static constexpr int kTmemNeed = 2 * kAccCols;
   static constexpr uint32_t kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                         : kTmemNeed <= 256 ? 256 : 512;
-  // gate/up hand-off: 2 warp pairs x 2 slots x [16 columns][32 lanes] fp32
-  static constexpr int kXchgFloats = 16 * 32;
-  static constexpr int kXchgBytes = SWIGLU ? 2 * 2 * kXchgFloats * 4 : 0;
   static constexpr int kBarBytes = 512;
-  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kXchgBytes + kBarBytes;
+  // one-CTA plans keep a shared-memory copy of the routing tables (E <= kTabMaxE)
+  static constexpr int kTabBytes = PAIR ? 0 : 2 * (kTabMaxE + 1) * 4;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + kTabBytes;
   static constexpr int kFeatPerTile = SWIGLU ? kGateUpTileFeat : kDownTileFeat;  // output features per unit
   static_assert(BN % TOKBOX == 0 && TOKBOX % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
   static_assert(!PAIR || (BN / 2) % TOKBOX == 0, "token boxes of a CTA pair");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
   static_assert(kTmemNeed <= 512, "TMEM has 512 columns");
-  static_assert((2 * STAGES + 5 + 8) * 8 + 8 <= kBarBytes, "barrier area");
+  static_assert((2 * STAGES + 5) * 8 + 8 <= kBarBytes, "barrier area");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -90,23 +103,25 @@ struct Unit {
 // Work unit u -> expert (binary search in the unit prefix sums), token chunk
 // and weight tile (tile index fastest, so CTAs running side by side share a
 // token chunk and walk the expert's weight tiles).
-__device__ __forceinline__ Unit decode_unit(int u, const int32_t* __restrict__ unit_off,
-                                            const int32_t* __restrict__ offsets, int E, int tiles, int bn) {
+// The tables are read through generic pointers: a copy in shared memory, or
+// global memory.
+__device__ __forceinline__ Unit decode_unit(int u, const int32_t* unit_off, const int32_t* offsets, int E, int tiles,
+                                            int bn) {
   int lo = 0, hi = E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(unit_off + mid) <= u)
+    if (unit_off[mid] <= u)
       lo = mid;
     else
       hi = mid;
   }
   Unit r;
   r.e = lo;
-  const int local = u - __ldg(unit_off + lo);
+  const int local = u - unit_off[lo];
   const int chunk = local / tiles;
   r.tile = local - chunk * tiles;
-  r.tok0 = __ldg(offsets + lo) + chunk * bn;
-  r.n = min(bn, __ldg(offsets + lo + 1) - r.tok0);
+  r.tok0 = offsets[lo] + chunk * bn;
+  r.n = min(bn, offsets[lo + 1] - r.tok0);
   return r;
 }
 
@@ -149,40 +164,7 @@ struct Range {
 
 __device__ __forceinline__ int64_t range_start(int64_t W, int cta, int ctas) { return W * cta / ctas; }
 
-__device__ __forceinline__ void raise_timeout(int32_t* err, volatile int* abort_flag, int kern) {
-  *abort_flag = 1;
-  if (atomicCAS(err, 0, kErrTimeout) == 0) atomicExch(err + 1, kern);
-}
-
 __device__ __forceinline__ uint16_t f2bf(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
-
-__device__ __forceinline__ int ld_acquire(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release(int32_t* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Bounded wait of one warp for a partial-sum flag; warp-uniform result.
-__device__ __forceinline__ bool wait_flag(const int32_t* flag, const volatile int* abort_flag) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) {
-    const uint64_t t0 = globaltimer_ns();
-    while (ld_acquire(flag) == 0) {
-      if (*abort_flag || globaltimer_ns() - t0 > kWaitTimeoutNs) {
-        ok = false;
-        break;
-      }
-      __nanosleep(64);
-    }
-  }
-  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-  if (ok) (void)ld_acquire(flag);  // every lane acquires before reading the partials
-  return ok;
-}
 
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -191,16 +173,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* xchg = reinterpret_cast<float*>(smem + STAGES * C::kStageBytes);  // [pair][slot][16][32] (gate/up)
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes + C::kXchgBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
-  uint64_t* xfull = done + 1;    // [pair][slot]: up values written
-  uint64_t* xempty = xfull + 4;  // [pair][slot]: up values consumed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xempty + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* tab = reinterpret_cast<int32_t*>(smem + STAGES * C::kStageBytes + C::kBarBytes);  // [2][kTabMaxE+1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kern = SWIGLU ? kKernGemm1 : kKernGemm2;
@@ -211,6 +191,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int worker = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int workers = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
+  // The routing tables come from a kernel at least two launches back, which
+  // has completed (see pdl.cuh); only the token / activation rows written by
+  // the immediately preceding kernel need the producer's pdl_wait below.
+  // After the single-launch front end the tables come from the previous
+  // kernel itself: then every thread waits for it first.
+  if (args.tables_from_parent) pdl_wait();
+  const int32_t* t_unit = args.unit_off;
+  const int32_t* t_off = args.offsets;
+  if (!PAIR && args.E <= kTabMaxE) {
+    for (int i = threadIdx.x; i <= args.E; i += kGemmThreads) {
+      tab[i] = __ldcg(args.unit_off + i);
+      tab[kTabMaxE + 1 + i] = __ldcg(args.offsets + i);
+    }
+    t_unit = tab;
+    t_off = tab + kTabMaxE + 1;  // visible to all threads after the barrier below
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -221,10 +217,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tempty[b], PAIR ? 8 : 4);  // the epilogue warps (of both CTAs of a pair)
     }
     mbar_init(done, 1);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&xfull[i], 1);
-      mbar_init(&xempty[i], 1);
-    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -245,10 +237,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // The routing tables come from a kernel at least two launches back, which
-  // has completed (see pdl.cuh); only the token / activation rows written by
-  // the immediately preceding kernel need the producer's pdl_wait below.
-  const int total_units = __ldg(args.unit_off + args.E);
+  const int total_units = t_unit[args.E];
   const int kblocks = args.K / kBlockK;
   const int ctas = workers;
 
@@ -282,6 +271,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         else
           tma_load_2d(dst, map, &full[st], c0, c1, pol);
       };
+      // gate/up A tile: box {64 K, 16 rows, gate+up, 4 groups, 1 expert}
+      auto load_gate_up = [&](void* dst, int st, int kb, int tile, int e, uint64_t pol) {
+        if (PAIR)
+          tma_load_5d_pair(dst, &tm_w, full_cl + 8u * st, kb * kBlockK, 0, 0, tile * 4, e, pol);
+        else
+          tma_load_5d(dst, &tm_w, &full[st], kb * kBlockK, 0, 0, tile * 4, e, pol);
+      };
       auto load_tokens = [&](int st, int kb, int tok0, int rows) {
         uint8_t* sb = smem + st * C::kStageBytes + kABytes;
         for (int r = 0; r < rows; r += TOKBOX) load_2d(sb + r * kTokRowBytes, &tm_x, st, kb * kBlockK, tok0 + r, pol_x);
@@ -296,7 +292,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
       int u, kb0, kb1;
       while (ok && rg.next(u, kb0, kb1)) {
-        const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
+        const Unit un = decode_unit(u, t_unit, t_off, args.E, args.tiles_per_expert, BN);
         // a pair's unit: weight tiles 2t (even CTA) and 2t+1; the MMA's N
         // tokens split in halves, the first half in the even CTA
         const int tile = PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile;
@@ -305,7 +301,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int tok_first = un.tok0 + static_cast<int>(rank) * half;
         const int wrow = un.e * args.w_rows_per_expert + tile * C::kFeatPerTile;
         const int tok_rows = (half + TOKBOX - 1) / TOKBOX * TOKBOX;  // whole boxes; rows past n are unused
-        const bool reused = __ldg(args.offsets + un.e + 1) - __ldg(args.offsets + un.e) > BN;
+        const bool reused = t_off[un.e + 1] - t_off[un.e] > BN;
         const uint64_t pol_w = reused ? pol_keep : pol_stream;
         const uint32_t bytes = kABytes + tok_rows * kTokRowBytes;  // per CTA (the same in both of a pair)
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -318,9 +314,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_arrive_expect_tx(&full[stage], bytes);
           else if (leader)
             mbar_arrive_expect_tx(&full[stage], 2 * bytes);  // both CTAs' loads
-          if (SWIGLU) {  // gate rows on top of the matching up rows
-            load_2d(sa, &tm_w, stage, kb * kBlockK, wrow, pol_w);
-            load_2d(sa + kABytes / 2, &tm_w, stage, kb * kBlockK, wrow + args.up_offset, pol_w);
+          if (SWIGLU) {  // 16 gate rows, the matching 16 up rows, x 4
+            load_gate_up(sa, stage, kb, tile, un.e, pol_w);
           } else {
             load_2d(sa, &tm_w, stage, kb * kBlockK, wrow, pol_w);
           }
@@ -363,7 +358,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
       int u, kb0, kb1;
       while (ok && rg.next(u, kb0, kb1)) {
-        const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
+        const Unit un = decode_unit(u, t_unit, t_off, args.E, args.tiles_per_expert, BN);
         const bool free_acc = PAIR ? mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, kWaitTimeoutNs, abort_flag)
                                    : mbar_wait(&tempty[acc], acc_phase ^ 1u, kWaitTimeoutNs, abort_flag);
         if (!free_acc) {
@@ -422,20 +417,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row = q * 32 + lane;  // this thread's TMEM lane = A-tile row
     int acc = 0;
     uint32_t acc_phase = 0;
-    uint32_t xit = 0;  // gate/up hand-off counter (slot = xit & 1)
     bool ok = true;
-    // gate/up: quarters 0,1 hold gate of features +0..31 / +32..63, quarters
-    // 2,3 the matching up values; pair p = q & 1 joins quarter p and p + 2
-    const int pair = q & 1;
-    const bool gate_warp = q < 2;
-    float* xb = xchg + pair * 2 * C::kXchgFloats;
+    // gate/up: warp quarter q holds features +16q .. +16q+15, gate in lanes
+    // 0..15 and up in lanes 16..31
+    const bool lo = lane < 16;
     // this CTA's partial-sum slot: [BN columns][128 rows] fp32
     float* my_slot = args.partials + static_cast<int64_t>(blockIdx.x) * BN * 128;
     const uint32_t tempty_cl = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
     Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
     int u, kb0, kb1;
     while (ok && rg.next(u, kb0, kb1)) {
-      const Unit un = decode_unit(u, args.unit_off, args.offsets, args.E, args.tiles_per_expert, BN);
+      const Unit un = decode_unit(u, t_unit, t_off, args.E, args.tiles_per_expert, BN);
       // warp-uniform outcome: tcgen05.ld below must be executed by all 32 lanes
       const bool got = mbar_wait(&tfull[acc], acc_phase, kWaitTimeoutNs, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) {
@@ -466,7 +458,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (kb1 < kblocks)
           while (c_last + 1 < ctas && range_start(rg.W, c_last + 1, ctas) < unit_end) ++c_last;
         const int feat_base = (PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile) * C::kFeatPerTile;
-        for (int c0 = 0; c0 < un.n && ok; c0 += 16, ++xit) {
+        for (int c0 = 0; c0 < un.n && ok; c0 += 16) {
           uint32_t ra[16];
           tmem_ld_32x32b_x16(t_row + c0, ra);
           tmem_ld_wait();
@@ -475,7 +467,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(ra[j]);
           for (int c = blockIdx.x + 1; c <= c_last; ++c) {
             if (range_start(rg.W, c, ctas) == range_start(rg.W, c + 1, ctas)) continue;  // empty range
-            if (c0 == 0 && !wait_flag(args.flags + c * 4 + q, abort_flag)) {
+            if (c0 == 0 && !wait_flag(args.flags + c * 4 + q, abort_flag, kWaitTimeoutNs)) {
               ok = false;
               break;
             }
@@ -489,38 +481,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) out[static_cast<int64_t>(j) * args.n_out] = f2bf(v[j]);
           } else {
-            const int slot_i = xit & 1;
-            const uint32_t par = (xit >> 1) & 1u;
-            float* xs = xb + slot_i * C::kXchgFloats;
-            if (!gate_warp) {
-              // hand the up values of these 16 tokens to the gate warp
-              const bool free_slot = mbar_wait(&xempty[pair * 2 + slot_i], par ^ 1u, kWaitTimeoutNs, abort_flag);
-              if (!__all_sync(0xFFFFFFFFu, free_slot)) {
-                ok = false;
-                break;
-              }
+            // lanes l and l+16 swap half of their columns: lane l keeps the
+            // gate values of columns 0..7 and receives the matching up values,
+            // lane l+16 keeps the up values of columns 8..15 and receives the
+            // gate values; each then finishes 8 outputs
+            float a[8];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) xs[j * 32 + lane] = v[j];
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&xfull[pair * 2 + slot_i]);
-            } else {
-              const bool have = mbar_wait(&xfull[pair * 2 + slot_i], par, kWaitTimeoutNs, abort_flag);
-              if (!__all_sync(0xFFFFFFFFu, have)) {
-                ok = false;
-                break;
-              }
-              uint16_t* out =
-                  args.out + static_cast<int64_t>(un.tok0 + c0) * args.n_out + feat_base + pair * 32 + lane;
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float g = v[j];
-                const float up = xs[j * 32 + lane];
-                const float a = __fdividef(g, 1.0f + __expf(-g)) * up;  // SiLU(gate) * up
-                out[static_cast<int64_t>(j) * args.n_out] = f2bf(a);
-              }
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&xempty[pair * 2 + slot_i]);
+            for (int j = 0; j < 8; ++j) {
+              const float mine = lo ? v[j] : v[j + 8];
+              const float other = __shfl_xor_sync(0xFFFFFFFFu, lo ? v[j + 8] : v[j], 16);
+              const float g = lo ? mine : other;
+              const float up = lo ? other : mine;
+              a[j] = __fdividef(g, 1.0f + __expf(-g)) * up;  // SiLU(gate) * up
             }
+            const int feat = feat_base + q * 16 + (lane & 15);
+            uint16_t* out = args.out + static_cast<int64_t>(un.tok0 + c0 + (lo ? 0 : 8)) * args.n_out + feat;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) out[static_cast<int64_t>(j) * args.n_out] = f2bf(a[j]);
           }
         }
         // the partial-sum flags read here are cleared for the next launch
@@ -612,10 +589,10 @@ cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, con
 //                  when the expert's weight tiles come in pairs.
 constexpr int kGateUpBn[3] = {32, 64, 256}, kGateUpStages[3] = {10, 8, 4};  // stages of 20 / 24 / 48 KB
 constexpr int kDownBn[3] = {32, 64, 256}, kDownStages[3] = {10, 8, 4};      // stages of 20 / 24 / 48 KB
-constexpr int kPairStages = 6;                                              // stages of 32 KB
+constexpr int kPairStages[2] = {7, 7};  // gate/up, down: stages of 32 KB
 // token rows per TMA box: small units hold few tokens (16-row boxes waste
-// nothing); large units hold up to 256 (64-row boxes: 4x fewer TMA requests)
-constexpr int kTokBox[3] = {16, 16, 64};
+// nothing); large units hold up to 256 (128-row boxes: 8x fewer TMA requests)
+constexpr int kTokBox[3] = {16, 16, 128};
 
 }  // namespace
 
@@ -636,7 +613,7 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm
                                                                                           stream);
     default:
       if (a.pair)
-        return launch_expert_gemm<true, kGateUpBn[2], kPairStages, kTokBox[2], true>(tm_w13, tm_x, a, num_sms,
+        return launch_expert_gemm<true, kGateUpBn[2], kPairStages[0], kTokBox[2], true>(tm_w13, tm_x, a, num_sms,
                                                                                       stream);
       return launch_expert_gemm<true, kGateUpBn[2], kGateUpStages[2], kTokBox[2], false>(tm_w13, tm_x, a, num_sms,
                                                                                           stream);
@@ -654,7 +631,7 @@ cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act
                                                                                        stream);
     default:
       if (a.pair)
-        return launch_expert_gemm<false, kDownBn[2], kPairStages, kTokBox[2], true>(tm_w2, tm_act, a, num_sms,
+        return launch_expert_gemm<false, kDownBn[2], kPairStages[1], kTokBox[2], true>(tm_w2, tm_act, a, num_sms,
                                                                                      stream);
       return launch_expert_gemm<false, kDownBn[2], kDownStages[2], kTokBox[2], false>(tm_w2, tm_act, a, num_sms,
                                                                                        stream);

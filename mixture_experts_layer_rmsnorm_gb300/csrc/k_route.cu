@@ -21,186 +21,30 @@
 
 #include "moe_kernels.cuh"
 #include "pdl.cuh"
+#include "route_tile.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kRouteWarps = 8;
-constexpr unsigned kFull = 0xFFFFFFFFu;
-
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
-  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-  return l | (h << 16);
-}
-
-__device__ __forceinline__ float warp_butterfly_sum(float v) {
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, off));
-  return v;
-}
-
 // grid = (ceil(T / TT), ceil(E / experts_per_cta)), block = 256, dyn smem = TT*H*2.
-// Each warp computes TE experts x TT tokens at a time.
 template <int TT, int TE>
-__global__ void __launch_bounds__(kRouteWarps * 32, (TT >= 8) ? 2 : 1)
+__global__ void __launch_bounds__(rt::kRouteWarps * 32, (TT >= 8) ? 2 : 1)
     norm_router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g,
                        const float* __restrict__ w_router, const float* __restrict__ bias, int T, int H, int E,
                        float eps, int experts_per_cta, uint16_t* __restrict__ h_out, float* __restrict__ logits,
                        int32_t* __restrict__ err) {
   extern __shared__ uint4 h_s[];  // [TT][H/8]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nch = H >> 3;
   const int t0 = blockIdx.x * TT;
   const int e0 = blockIdx.y * experts_per_cta;
-
   // The router rows this CTA will need and the norm gain do not depend on the
   // previous kernel: start pulling them into L2 now, so that their DRAM
   // latency overlaps the RMSNorm below.
-  {
-    const int e_hi = min(E, e0 + experts_per_cta);
-    const char* wb = reinterpret_cast<const char*>(w_router + static_cast<size_t>(e0) * H);
-    const size_t wbytes = static_cast<size_t>(max(e_hi - e0, 0)) * H * 4;
-    for (size_t off = static_cast<size_t>(threadIdx.x) * 128; off < wbytes; off += 128 * blockDim.x)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(wb + off));
-    const char* gb = reinterpret_cast<const char*>(g);
-    for (int off = threadIdx.x * 128; off < H * 2; off += 128 * blockDim.x)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(gb + off));
-  }
+  rt::route_prefetch(w_router, g, H, e0, min(E, e0 + experts_per_cta));
   pdl_wait();
   pdl_launch_dependents();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 4) err[threadIdx.x] = 0;
-
-  // ---- RMSNorm: one warp per token
-  for (int tt = warp; tt < TT; tt += kRouteWarps) {
-    const int t = t0 + tt;
-    if (t >= T) break;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
-    float ss = 0.0f;
-    int c = lane;
-    // 8 chunks' loads in flight, then their FMAs in chunk order
-    for (; c + 32 * 7 < nch; c += 32 * 8) {
-      uint4 v[8];
-#pragma unroll
-      for (int d = 0; d < 8; ++d) v[d] = __ldg(xr + c + 32 * d);
-#pragma unroll
-      for (int d = 0; d < 8; ++d) {
-        float f[8];
-        unpack8(v[d], f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ss = __fmaf_rn(f[i], f[i], ss);
-      }
-    }
-    for (; c < nch; c += 32) {
-      float f[8];
-      unpack8(__ldg(xr + c), f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ss = __fmaf_rn(f[i], f[i], ss);
-    }
-    ss = warp_butterfly_sum(ss);
-    const float ms = __fdiv_rn(ss, static_cast<float>(H));
-    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-    const uint4* gr = reinterpret_cast<const uint4*>(g);
-    uint4* hrow = reinterpret_cast<uint4*>(h_out + static_cast<size_t>(t) * H);
-#pragma unroll 4
-    for (int c = lane; c < nch; c += 32) {
-      float f[8], gg[8];
-      unpack8(__ldg(xr + c), f);
-      unpack8(__ldg(gr + c), gg);
-      uint4 o;
-      o.x = pack2_bf16(__fmul_rn(__fmul_rn(f[0], rstd), gg[0]), __fmul_rn(__fmul_rn(f[1], rstd), gg[1]));
-      o.y = pack2_bf16(__fmul_rn(__fmul_rn(f[2], rstd), gg[2]), __fmul_rn(__fmul_rn(f[3], rstd), gg[3]));
-      o.z = pack2_bf16(__fmul_rn(__fmul_rn(f[4], rstd), gg[4]), __fmul_rn(__fmul_rn(f[5], rstd), gg[5]));
-      o.w = pack2_bf16(__fmul_rn(__fmul_rn(f[6], rstd), gg[6]), __fmul_rn(__fmul_rn(f[7], rstd), gg[7]));
-      h_s[tt * nch + c] = o;
-      if (blockIdx.y == 0) hrow[c] = o;
-    }
-  }
-  __syncthreads();
-
-  // ---- logits: warp w takes expert groups e0 + (w + 8 r) * TE .. + TE
-  const int e_end = min(E, e0 + experts_per_cta);
-  const int ntok = min(TT, T - t0);
-  for (int eg = e0 + warp * TE; eg < e_end; eg += kRouteWarps * TE) {
-    float acc[TT][TE];
-#pragma unroll
-    for (int a = 0; a < TT; ++a)
-#pragma unroll
-      for (int b = 0; b < TE; ++b) acc[a][b] = 0.0f;
-    const float4* wrow[TE];
-#pragma unroll
-    for (int b = 0; b < TE; ++b) {
-      const int e = min(eg + b, E - 1);  // clamp: a tail expert's duplicate is computed but not stored
-      wrow[b] = reinterpret_cast<const float4*>(w_router + static_cast<size_t>(e) * H);
-    }
-    // DEPTH chunks of router weights in flight per lane, consumed in chunk
-    // order, so every accumulator keeps the canonical sequence
-    constexpr int DEPTH = (TE >= 4) ? 2 : (TE == 2 ? 4 : 8);
-    int c = lane;
-    for (; c + 32 * (DEPTH - 1) < nch; c += 32 * DEPTH) {
-      float4 wv[DEPTH][TE][2];
-#pragma unroll
-      for (int d = 0; d < DEPTH; ++d)
-#pragma unroll
-        for (int b = 0; b < TE; ++b) {
-          wv[d][b][0] = __ldg(wrow[b] + 2 * (c + 32 * d));
-          wv[d][b][1] = __ldg(wrow[b] + 2 * (c + 32 * d) + 1);
-        }
-#pragma unroll
-      for (int d = 0; d < DEPTH; ++d) {
-#pragma unroll
-        for (int a = 0; a < TT; ++a) {
-          float hv[8];
-          unpack8(h_s[a * nch + c + 32 * d], hv);
-#pragma unroll
-          for (int b = 0; b < TE; ++b) {
-            const float w[8] = {wv[d][b][0].x, wv[d][b][0].y, wv[d][b][0].z, wv[d][b][0].w,
-                                wv[d][b][1].x, wv[d][b][1].y, wv[d][b][1].z, wv[d][b][1].w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[a][b] = __fmaf_rn(hv[i], w[i], acc[a][b]);
-          }
-        }
-      }
-    }
-    for (; c < nch; c += 32) {
-      float w[TE][8];
-#pragma unroll
-      for (int b = 0; b < TE; ++b) {
-        const float4 p = __ldg(wrow[b] + 2 * c), q = __ldg(wrow[b] + 2 * c + 1);
-        w[b][0] = p.x; w[b][1] = p.y; w[b][2] = p.z; w[b][3] = p.w;
-        w[b][4] = q.x; w[b][5] = q.y; w[b][6] = q.z; w[b][7] = q.w;
-      }
-#pragma unroll
-      for (int a = 0; a < TT; ++a) {
-        float hv[8];
-        unpack8(h_s[a * nch + c], hv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int b = 0; b < TE; ++b) acc[a][b] = __fmaf_rn(hv[i], w[b][i], acc[a][b]);
-      }
-    }
-#pragma unroll
-    for (int a = 0; a < TT; ++a)
-#pragma unroll
-      for (int b = 0; b < TE; ++b) {
-        float v = warp_butterfly_sum(acc[a][b]);
-        const int e = eg + b;
-        if (lane == 0 && a < ntok && e < e_end) {
-          if (bias) v = __fadd_rn(v, bias[e]);
-          logits[static_cast<size_t>(t0 + a) * E + e] = v;
-        }
-      }
-  }
+  rt::norm_router_tile<TT, TE>(x, g, w_router, bias, T, H, E, eps, t0, e0, experts_per_cta, blockIdx.y == 0, h_out,
+                               logits, h_s);
 }
 
 template <int TT, int TE>
@@ -217,14 +61,14 @@ cudaError_t launch_nr(const uint16_t* x, const uint16_t* g, const float* wr, con
     configured_device = dev;
   }
   const int tiles = (T + TT - 1) / TT;
-  const int group = kRouteWarps * TE;
+  const int group = rt::kRouteWarps * TE;
   // fewer token tiles than SMs: one expert group per CTA spreads the work
   // (and the router weights) over the SMs; otherwise a CTA takes all experts
   // so that its tokens are normalised once
   int epc = group;
   if (tiles >= num_sms) epc = (E + group - 1) / group * group;
   dim3 grid(tiles, (E + epc - 1) / epc);
-  return launch_pdl(norm_router_kernel<TT, TE>, grid, dim3(kRouteWarps * 32), smem, stream, x, g, wr, bias, T, H, E,
+  return launch_pdl(norm_router_kernel<TT, TE>, grid, dim3(rt::kRouteWarps * 32), smem, stream, x, g, wr, bias, T, H, E,
                     eps, epc, h, logits, err);
 }
 

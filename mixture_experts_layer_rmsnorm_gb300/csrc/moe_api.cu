@@ -122,6 +122,21 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// W13 [E][2I][H] bf16 viewed as [E][2][I/16][16][H] (innermost last in the
+// names, first in the dims below): one box of {64, 16, 2, 4, 1} is a 128-row
+// gate/up tile whose 16-row groups alternate gate rows and the matching up rows.
+bool make_map_gate_up(CUtensorMap* m, const void* w13, uint64_t H, uint64_t I, uint64_t E) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[5] = {H, 16, 2, I / 16, E};
+  cuuint64_t strides[4] = {H * 2, I * H * 2, 16 * H * 2, 2 * I * H * 2};
+  cuuint32_t box[5] = {static_cast<cuuint32_t>(moe::kBlockK), 16, 2, moe::kGateUpTileFeat / 16, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(w13), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int num_sms_of_current_device() {
   static int cache[64] = {0};
   int dev = 0;
@@ -190,6 +205,18 @@ moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes) {
   return MOE_OK;
 }
 
+moe_status moe_kernels_per_call(const moe_shape* shape, int32_t* count) {
+  const moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!count) return MOE_ERR_INVALID_ARG;
+  const moe_shape& s = *shape;
+  if (s.T == 0)
+    *count = 0;
+  else
+    *count = moe::align_fuses_topk(s.T, s.E) ? 6 : 8;
+  return MOE_OK;
+}
+
 moe_status moe_workspace_views(const moe_shape* shape, void* workspace, size_t workspace_bytes, moe_views* v) {
   const moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
@@ -220,7 +247,8 @@ namespace moe {
 // first kernel and events[i] after the i-th of the seven kernels.
 moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
                         const float* router_bias, const moe_bf16* w13, const moe_bf16* w2, moe_bf16* y,
-                        void* workspace, size_t workspace_bytes, moe_stream_t stream, void* const* events) {
+                        void* workspace, size_t workspace_bytes, moe_stream_t stream, void* const* events,
+                        bool single_launch_front) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   const moe_shape& s = *shape;
@@ -231,6 +259,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int num_sms = num_sms_of_current_device();
   if (num_sms <= 0) return MOE_ERR_CUDA;
+  if (single_launch_front && !moe::front_fits(s.T, s.H, s.E, s.top_k)) return MOE_ERR_UNSUPPORTED;
   const Layout L = make_layout(s);
   const GemmPlan plan = moe::choose_plan(s.T, s.top_k, s.E);
   const int bn1 = moe::gemm_gate_up_bn(plan), bn2 = moe::gemm_down_bn(plan);
@@ -242,7 +271,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   };
 
   CUtensorMap tm_w13, tm_xg, tm_w2, tm_act;
-  if (!make_map(&tm_w13, w13, s.H, static_cast<uint64_t>(s.E) * 2 * s.I, moe::kWeightBoxRows / 2) ||
+  if (!make_map_gate_up(&tm_w13, w13, s.H, s.I, s.E) ||
       !make_map(&tm_xg, at<void>(workspace, L.xg), s.H, L.P_max, moe::gemm_tok_box_rows(plan)) ||
       !make_map(&tm_w2, w2, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows) ||
       !make_map(&tm_act, at<void>(workspace, L.act), s.I, L.P_max, moe::gemm_tok_box_rows(plan)))
@@ -250,39 +279,78 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
 
   int32_t* err = at<int32_t>(workspace, L.err);
   if (!mark(0)) return MOE_ERR_CUDA;
-  if (moe::launch_norm_router(x, g_norm, w_router, router_bias, s.T, s.H, s.E, s.eps, at<uint16_t>(workspace, L.h),
-                              at<float>(workspace, L.logits), err, num_sms, cs) != cudaSuccess || !mark(1))
-    return MOE_ERR_CUDA;
-  // small T and E: top-k and align in one single-CTA kernel (events[2] then
-  // follows events[1] at once); otherwise three multi-CTA kernels: top-k with
-  // per-block counts (ends at events[2]), scan and scatter (end at events[3])
   const int N = s.T * s.top_k;
-  cudaError_t ce;
-  if (moe::align_fuses_topk(s.T, s.E)) {
-    if (!mark(2)) return MOE_ERR_CUDA;
-    ce = moe::launch_align(at<float>(workspace, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(workspace, L.ids),
-                           at<float>(workspace, L.w), N, s.E, moe::kPadRows, bn1, utiles1, bn2, utiles2,
-                           at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.offsets),
-                           at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.slot),
-                           at<int32_t>(workspace, L.unit1), at<int32_t>(workspace, L.unit2), err,
-                           at<int32_t>(workspace, L.flags), kGemmFlagInts, cs);
+  // norm, router, top-k, align and gather in one launch (when asked for)
+  const bool front = single_launch_front;
+  if (front) {
+    moe::FrontArgs fa{};
+    fa.x = x;
+    fa.g = g_norm;
+    fa.w_router = w_router;
+    fa.bias = router_bias;
+    fa.T = s.T;
+    fa.H = s.H;
+    fa.E = s.E;
+    fa.k = s.top_k;
+    fa.renorm = s.renormalize;
+    fa.eps = s.eps;
+    fa.pad = moe::kPadRows;
+    fa.bn1 = bn1;
+    fa.tiles1 = utiles1;
+    fa.bn2 = bn2;
+    fa.tiles2 = utiles2;
+    fa.h = at<uint16_t>(workspace, L.h);
+    fa.logits = at<float>(workspace, L.logits);
+    fa.ids = at<int32_t>(workspace, L.ids);
+    fa.topk_w = at<float>(workspace, L.w);
+    fa.counts = at<int32_t>(workspace, L.counts);
+    fa.offsets = at<int32_t>(workspace, L.offsets);
+    fa.sorted_ids = at<int32_t>(workspace, L.sorted);
+    fa.slot_of = at<int32_t>(workspace, L.slot);
+    fa.unit_off1 = at<int32_t>(workspace, L.unit1);
+    fa.unit_off2 = at<int32_t>(workspace, L.unit2);
+    fa.err = err;
+    fa.flags = at<int32_t>(workspace, L.flags);
+    fa.n_flags = kGemmFlagInts;
+    fa.xg = at<uint16_t>(workspace, L.xg);
+    if (moe::launch_front(fa, cs) != cudaSuccess || !mark(1) || !mark(2) || !mark(3) || !mark(4))
+      return MOE_ERR_CUDA;
   } else {
-    ce = moe::launch_align_multi(at<float>(workspace, L.logits), s.T, s.top_k, s.renormalize,
-                                 at<int32_t>(workspace, L.ids), at<float>(workspace, L.w), s.E, moe::kPadRows, bn1,
-                                 utiles1, bn2, utiles2,
-                                 at<int32_t>(workspace, L.counts), at<int32_t>(workspace, L.offsets),
-                                 at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.slot),
-                                 at<int32_t>(workspace, L.unit1), at<int32_t>(workspace, L.unit2),
-                                 at<int32_t>(workspace, L.blk_counts), at<int32_t>(workspace, L.blk_base), err,
-                                 at<int32_t>(workspace, L.flags), kGemmFlagInts, cs,
-                                 events ? events[2] : nullptr);
+    if (moe::launch_norm_router(x, g_norm, w_router, router_bias, s.T, s.H, s.E, s.eps,
+                                at<uint16_t>(workspace, L.h), at<float>(workspace, L.logits), err, num_sms,
+                                cs) != cudaSuccess ||
+        !mark(1))
+      return MOE_ERR_CUDA;
+    // small T and E: top-k and align in one single-CTA kernel (events[2] then
+    // follows events[1] at once); otherwise three multi-CTA kernels: top-k with
+    // per-block counts (ends at events[2]), scan and scatter (end at events[3])
+    cudaError_t ce;
+    if (moe::align_fuses_topk(s.T, s.E)) {
+      if (!mark(2)) return MOE_ERR_CUDA;
+      ce = moe::launch_align(at<float>(workspace, L.logits), s.T, s.top_k, s.renormalize,
+                             at<int32_t>(workspace, L.ids), at<float>(workspace, L.w), N, s.E, moe::kPadRows, bn1,
+                             utiles1, bn2, utiles2, at<int32_t>(workspace, L.counts),
+                             at<int32_t>(workspace, L.offsets), at<int32_t>(workspace, L.sorted),
+                             at<int32_t>(workspace, L.slot), at<int32_t>(workspace, L.unit1),
+                             at<int32_t>(workspace, L.unit2), err, at<int32_t>(workspace, L.flags), kGemmFlagInts,
+                             cs);
+    } else {
+      ce = moe::launch_align_multi(at<float>(workspace, L.logits), s.T, s.top_k, s.renormalize,
+                                   at<int32_t>(workspace, L.ids), at<float>(workspace, L.w), s.E, moe::kPadRows, bn1,
+                                   utiles1, bn2, utiles2, at<int32_t>(workspace, L.counts),
+                                   at<int32_t>(workspace, L.offsets), at<int32_t>(workspace, L.sorted),
+                                   at<int32_t>(workspace, L.slot), at<int32_t>(workspace, L.unit1),
+                                   at<int32_t>(workspace, L.unit2), at<int32_t>(workspace, L.blk_counts),
+                                   at<int32_t>(workspace, L.blk_base), err, at<int32_t>(workspace, L.flags),
+                                   kGemmFlagInts, cs, events ? events[2] : nullptr);
+    }
+    if (ce != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
+    if (moe::launch_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
+                           at<int32_t>(workspace, L.offsets), s.E, N, s.top_k, s.H, L.P_max,
+                           at<uint16_t>(workspace, L.xg), cs) != cudaSuccess ||
+        !mark(4))
+      return MOE_ERR_CUDA;
   }
-  if (ce != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
-  if (moe::launch_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
-                         at<int32_t>(workspace, L.offsets), s.E, N, s.top_k, s.H, L.P_max,
-                         at<uint16_t>(workspace, L.xg), cs) != cudaSuccess ||
-      !mark(4))
-    return MOE_ERR_CUDA;
 
   moe::ExpertGemmArgs a1{};
   a1.offsets = at<int32_t>(workspace, L.offsets);
@@ -291,7 +359,6 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a1.K = s.H;
   a1.tiles_per_expert = utiles1;
   a1.w_rows_per_expert = 2 * s.I;
-  a1.up_offset = s.I;
   a1.n_out = s.I;
   a1.out = at<uint16_t>(workspace, L.act);
   a1.err = err;
@@ -299,6 +366,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a1.flags = at<int32_t>(workspace, L.flags);
   a1.stream_k = plan == GemmPlan::kSmall;
   a1.pair = moe::gemm_uses_pairs(plan, tiles1);
+  a1.tables_from_parent = front;
   if (moe::launch_gemm_gate_up(tm_w13, tm_xg, a1, plan, num_sms, cs) != cudaSuccess || !mark(5)) return MOE_ERR_CUDA;
 
   moe::ExpertGemmArgs a2{};
@@ -308,7 +376,6 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a2.K = s.I;
   a2.tiles_per_expert = utiles2;
   a2.w_rows_per_expert = s.H;
-  a2.up_offset = 0;
   a2.n_out = s.H;
   a2.out = at<uint16_t>(workspace, L.out);
   a2.err = err;
@@ -345,6 +412,19 @@ moe_status moe_forward_events(const moe_shape* shape, const moe_bf16* x, const m
     if (!events[i]) return MOE_ERR_INVALID_ARG;
   return moe::forward_impl(shape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes, stream,
                            events);
+}
+
+moe_status moe_forward_fused_front(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                                   const float* w_router, const float* router_bias, const moe_bf16* w13,
+                                   const moe_bf16* w2, moe_bf16* y, void* workspace, size_t workspace_bytes,
+                                   moe_stream_t stream, void* const* events, int32_t n_events) {
+  if (events) {
+    if (n_events < MOE_NUM_KERNELS + 1) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i <= MOE_NUM_KERNELS; ++i)
+      if (!events[i]) return MOE_ERR_INVALID_ARG;
+  }
+  return moe::forward_impl(shape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes, stream,
+                           events, true);
 }
 
 moe_status moe_route_debug(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
@@ -390,6 +470,16 @@ moe_status moe_device_status(const void* workspace, size_t workspace_bytes, moe_
   if (detail) std::memcpy(detail, w, sizeof(w));
   if (w[0] == moe::kErrTimeout) return MOE_ERR_TIMEOUT;
   if (w[0] == moe::kErrDevice) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+moe_status moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t timeout_ns,
+                                     moe_stream_t stream) {
+  if (!workspace || workspace_bytes < 64 || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  if (timeout_ns <= 0 || timeout_ns > 1000000000) return MOE_ERR_INVALID_ARG;
+  if (moe::launch_selftest_wait(static_cast<int32_t*>(workspace), static_cast<uint64_t>(timeout_ns),
+                                reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

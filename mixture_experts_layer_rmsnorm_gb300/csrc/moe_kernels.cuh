@@ -10,7 +10,7 @@ namespace moe {
 // error word codes (match moe_status) and kernel ids written with them
 enum : int32_t { kErrTimeout = 5, kErrDevice = 6 };
 enum : int32_t { kKernNormRouter = 1, kKernTopk = 2, kKernAlign = 3, kKernGather = 4, kKernGemm1 = 5,
-                 kKernGemm2 = 6, kKernCombine = 7 };
+                 kKernGemm2 = 6, kKernCombine = 7, kKernSelfTest = 8 };
 
 // rows of padding granularity of each expert's list in the expert GEMMs
 constexpr int kPadRows = 16;
@@ -49,20 +49,57 @@ cudaError_t launch_align_multi(const float* logits, int T, int k, int renorm, in
                                int32_t* blk_counts, int32_t* blk_base, int32_t* err, int32_t* flags, int n_flags,
                                cudaStream_t stream, void* count_done_event);
 
+// K1 + K1b + K2 + K3 for decode batches in one launch of one thread-block
+// cluster (k_front.cu): same outputs as launch_norm_router, launch_align and
+// launch_gather, except that padding rows of xg are left unwritten.
+constexpr int kFrontMaxT = 64;
+constexpr int kFrontMaxE = 256;
+constexpr int kFrontMaxSmem = 136 * 1024;
+struct FrontArgs {
+  const uint16_t* x;
+  const uint16_t* g;
+  const float* w_router;
+  const float* bias;
+  int T, H, E, k, renorm;
+  float eps;
+  int pad, bn1, tiles1, bn2, tiles2;  // align padding and the GEMMs' work-unit tables
+  uint16_t* h;
+  float* logits;
+  int32_t* ids;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_ids;
+  int32_t* slot_of;
+  int32_t* unit_off1;
+  int32_t* unit_off2;
+  int32_t* err;
+  int32_t* flags;  // the expert GEMMs' stream-K flags: zeroed
+  int n_flags;
+  uint16_t* xg;
+  // set by the launcher: router work items = token tiles x expert groups
+  int n_items, groups, experts_per_item;
+};
+// Whether the shape takes the single-launch front end on the current device.
+bool front_fits(int T, int H, int E, int k);
+cudaError_t launch_front(const FrontArgs& a, cudaStream_t stream);
+
 // K3: xg[p,:] = h[sorted_ids[p] / k, :] for real rows, zeros for padding rows.
 cudaError_t launch_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets, int E, int N,
                           int k, int H, int64_t P_max, uint16_t* xg, cudaStream_t stream);
 
 // K4 / K5: grouped expert GEMMs on tcgen05.  Weights are the MMA's A operand
-// (128 weight rows per tile), the tokens of one expert its B operand.
+// (128 weight rows per tile), the tokens of one expert its B operand.  The
+// gate/up GEMM reads W13 through a 5-D tensor map (64 features per tile:
+// 16 gate rows, the matching 16 up rows, x 4); the down GEMM reads W2 through
+// a 2-D map of 128-row boxes.
 struct ExpertGemmArgs {
   const int32_t* offsets;   // [E+1] padded row offsets
   const int32_t* unit_off;  // [E+1] prefix sums of work units
   int E;
   int K;                    // reduction length
   int tiles_per_expert;     // output features / 128
-  int w_rows_per_expert;    // 2I (gate/up) or H (down)
-  int up_offset;            // I for gate/up, unused for down
+  int w_rows_per_expert;    // weight rows per expert of the down GEMM's 2-D map (H)
   int n_out;                // output row length (I or H)
   uint16_t* out;            // [P_max, n_out] bf16
   int32_t* err;
@@ -70,6 +107,7 @@ struct ExpertGemmArgs {
   int32_t* flags;           // [kMaxGemmCtas * 4], zero on entry; left zero on exit
   int stream_k;             // 1: equal K-block ranges per CTA; 0: whole units round-robin
   int pair;                 // 1: CTA pairs, a unit = weight tiles 2t and 2t+1 (large plan only)
+  int tables_from_parent;   // 1: the routing tables come from the previous kernel (wait before reading)
 };
 // persistent GEMM grid: min(SM count, kMaxGemmCtas) CTAs
 constexpr int kMaxGemmCtas = 256;
@@ -120,6 +158,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+
+// Self-test of the bounded waits: one kernel whose two waits (an mbarrier
+// phase, a global flag) run out after timeout_ns and report MOE_ERR_TIMEOUT
+// with kernel id kKernSelfTest in the error word at `err` (>= 64 bytes).
+cudaError_t launch_selftest_wait(int32_t* err, uint64_t timeout_ns, cudaStream_t stream);
 
 // K6: y[t,:] = bf16(sum_j topk_w[t,j] * out_rows[slot_of[t*k+j], :]).
 cudaError_t launch_combine(const uint16_t* out_rows, const int32_t* slot_of, const float* topk_w, int T, int H,

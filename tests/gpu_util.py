@@ -35,11 +35,11 @@ class DeviceLayer:
                                       c.top_k, c.renormalize, c.eps, router_bias=dev_f32(li.bias),
                                       max_tokens=max_tokens or c.T)
 
-    def run(self, x: np.ndarray) -> dict:
+    def run(self, x: np.ndarray, fused_front: bool = False) -> dict:
         c = self.li.cfg
         T, H, I, E, k = x.shape[0], c.H, c.I, c.E, c.top_k
         xd = dev_bf16(x)
-        y = self.layer.forward(xd)
+        y = self.layer.forward(xd, fused_front=fused_front)
         torch.cuda.synchronize()
         st, det = self.layer.device_status(T)
         assert st == binding.MOE_OK, f"device status {st} {det}"

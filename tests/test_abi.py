@@ -48,6 +48,27 @@ def test_workspace_size_and_shape_checks():
         assert st == want, (s.H, s.I, s.E, s.top_k, st)
 
 
+def test_kernels_per_call_host_checks():
+    st, n = binding.moe_kernels_per_call(binding.shape(0, 128, 256, 8, 2))
+    assert st == binding.MOE_OK and n == 0
+    st, _ = binding.moe_kernels_per_call(binding.shape(4, 100, 256, 8, 2))
+    assert st == binding.MOE_ERR_UNSUPPORTED
+    # any device (or none): one of the three launch plans
+    st, n = binding.moe_kernels_per_call(binding.shape(4, 128, 256, 8, 2))
+    assert st == binding.MOE_OK and n in (4, 6, 8)
+    st, n = binding.moe_kernels_per_call(binding.shape(4096, 128, 256, 8, 2))
+    assert st == binding.MOE_OK and n == 8
+
+
+def test_selftest_wait_timeout_rejects_bad_arguments_without_a_gpu():
+    A = 1 << 20
+    assert binding.moe_selftest_wait_timeout(None, 64, 1000, None) == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_selftest_wait_timeout(A, 32, 1000, None) == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_selftest_wait_timeout(A + 16, 64, 1000, None) == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_selftest_wait_timeout(A, 64, 0, None) == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_selftest_wait_timeout(A, 64, 2_000_000_000, None) == binding.MOE_ERR_INVALID_ARG
+
+
 def test_forward_rejects_bad_arguments_without_a_gpu():
     # fake, aligned, never-dereferenced addresses: every case fails validation first
     s = binding.shape(4, 128, 256, 8, 2)

@@ -70,6 +70,32 @@ def test_layer_parity(case, o):
     gu.check_output(o, li, li.x, g["y"])
 
 
+FRONT_CASES = [c for c in CASES if c[1] <= binding.MOE_FRONT_MAX_T and c[4] <= binding.MOE_FRONT_MAX_E]
+
+
+@pytest.mark.parametrize("case", FRONT_CASES, ids=[c[0] for c in FRONT_CASES])
+def test_fused_front_parity(case, o):
+    """The single-launch front end: the same routing bits as the oracle, and the
+    same output bits as the multi-launch path."""
+    _, T, H, I, E, k, renorm, zipf, seed = case
+    li = _layer_inputs(T, H, I, E, k, renorm, zipf, seed)
+    dl = gu.DeviceLayer(li)
+    g = dl.run(li.x, fused_front=True)
+    gu.check_routing(o, li, li.x, g)
+    gu.check_output(o, li, li.x, g["y"])
+    ref = dl.run(li.x)
+    assert np.array_equal(g["y"], ref["y"]), "fused front end and multi-launch path disagree"
+    assert np.array_equal(g["slot"], ref["slot"])
+
+
+def test_fused_front_rejects_large_batches():
+    li = _layer_inputs(80, 128, 128, 4, 2, True, None, 0)
+    dl = gu.DeviceLayer(li)
+    with pytest.raises(binding.MoeError) as ei:
+        dl.run(li.x, fused_front=True)
+    assert ei.value.status == binding.MOE_ERR_UNSUPPORTED
+
+
 def test_zero_tokens_is_a_noop():
     li = _layer_inputs(4, 128, 128, 4, 2, True, None, 0)
     dl = gu.DeviceLayer(li)
