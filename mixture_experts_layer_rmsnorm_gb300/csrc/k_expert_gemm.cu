@@ -100,9 +100,12 @@ struct Unit {
   int e, tile, tok0, n;
 };
 
-// Work unit u -> expert (binary search in the unit prefix sums), token chunk
-// and weight tile (tile index fastest, so CTAs running side by side share a
-// token chunk and walk the expert's weight tiles).
+// Work unit u -> expert (binary search in the unit prefix sums), weight tile
+// and token chunk, chunk index fastest: the units that read the same weight
+// tile are neighbours, so CTAs running side by side read it from DRAM once
+// (with the tile index fastest, an expert's chunks fell into different waves
+// of the persistent grid and prefill re-read ~60% of the weights), while the
+// expert's few token chunks stay in L2 for all its tiles.
 // The tables are read through generic pointers: a copy in shared memory, or
 // global memory.
 __device__ __forceinline__ Unit decode_unit(int u, const int32_t* unit_off, const int32_t* offsets, int E, int tiles,
@@ -117,9 +120,11 @@ __device__ __forceinline__ Unit decode_unit(int u, const int32_t* unit_off, cons
   }
   Unit r;
   r.e = lo;
-  const int local = u - unit_off[lo];
-  const int chunk = local / tiles;
-  r.tile = local - chunk * tiles;
+  const int base = unit_off[lo];
+  const int chunks = (unit_off[lo + 1] - base) / tiles;  // >= 1: u lies in this expert's range
+  const int local = u - base;
+  r.tile = local / chunks;
+  const int chunk = local - r.tile * chunks;
   r.tok0 = offsets[lo] + chunk * bn;
   r.n = min(bn, offsets[lo + 1] - r.tok0);
   return r;
