@@ -66,6 +66,7 @@ class Oracle:
         lib.oracle_moe_forward.argtypes = [i64, i64, i64, i64, i, i, d, p, p, p, p, p, p, i64, p, i, i,
                                            p, p, p, p, p, p, p]
         lib.oracle_moe_forward.restype = i
+        lib.oracle_qk_norm_f64.argtypes = [i64, i64, p, p, d, d, p]
         lib.oracle_f64_to_bf16.argtypes = [d]
         lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
         lib.oracle_f32_to_bf16.argtypes = [f]
@@ -86,6 +87,14 @@ class Oracle:
         h = np.empty((T, H), np.uint16); he = np.empty((T, H), np.float64)
         self.lib.oracle_rmsnorm_f64(T, H, _p(x), _p(g), float(eps), _p(h), _p(he))
         return h, he
+
+    def qk_norm_f64(self, x, w, weight_bias, eps):
+        """QK-norm of head vectors x[..., D] (bf16 bits) with gain w[D] + weight_bias."""
+        x = _c(x, np.uint16); w = _c(w, np.uint16)
+        D = x.shape[-1]
+        out = np.empty(x.shape, np.uint16)
+        self.lib.oracle_qk_norm_f64(x.size // D, D, _p(x), _p(w), float(weight_bias), float(eps), _p(out))
+        return out
 
     def router_logits_f64(self, h, w_router, bias=None):
         h = _c(h, np.uint16); wr = _c(w_router, np.float32)

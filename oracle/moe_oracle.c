@@ -37,6 +37,10 @@
  *   Combine     y_t = sum_j w_tj * o_tj, accumulated in j order, cast to bf16
  *                 -- "CuTeDSL chez Perplexity", MoE dispatch/combine, "Local"
  *                    (weighted accumulation in registers into the output).
+ *   QK-norm     per attention head of Q and of K (head_dim D elements):
+ *               out_j = (w_j + weight_bias) * (x_j * rstd), rstd = 1/sqrt(mean x^2
+ *               + eps), with one weight vector w[D] for all heads of Q and one for
+ *               K, cast to x's type -- "CuTeDSL chez Perplexity", "Norme QK".
  *
  * The routing decision (which experts a token goes to) is an integer decided
  * by floating point, so it is taken here in the same precision the kernel
@@ -163,6 +167,27 @@ void oracle_rmsnorm_f64(int64_t T, int64_t H, const uint16_t* x, const uint16_t*
                         uint16_t* h, double* h_exact) {
   for (int64_t t = 0; t < T; ++t)
     rmsnorm_row_f64(H, x + t * H, g, eps, h ? h + t * H : NULL, h_exact ? h_exact + t * H : NULL);
+}
+
+/* ------------------------------------------------------------------ */
+/* QK-norm, fp64                                                        */
+/* ------------------------------------------------------------------ */
+
+/* rows head vectors of D elements each (a row = one head of one token):
+ * rstd = 1/sqrt((1/D) sum_j x_j^2 + eps); out_j = bf16((w_j + weight_bias) * (x_j * rstd)). */
+void oracle_qk_norm_f64(int64_t rows, int64_t D, const uint16_t* x, const uint16_t* w, double weight_bias,
+                        double eps, uint16_t* out) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const uint16_t* xr = x + r * D;
+    double ss = 0.0;
+    for (int64_t j = 0; j < D; ++j) {
+      double xv = bf16_to_f64(xr[j]);
+      ss += xv * xv;
+    }
+    double rstd = 1.0 / sqrt(ss / (double)D + eps);
+    for (int64_t j = 0; j < D; ++j)
+      out[r * D + j] = f64_to_bf16((bf16_to_f64(w[j]) + weight_bias) * (bf16_to_f64(xr[j]) * rstd));
+  }
 }
 
 /* ------------------------------------------------------------------ */

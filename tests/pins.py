@@ -107,6 +107,54 @@ def pin_rmsnorm_unit_gain(o):
     assert np.allclose((he ** 2).mean(axis=1), ms / (ms + eps), rtol=1e-13)
 
 
+# ------------------------------------------------------------------- QK-norm
+
+def pin_qknorm_power_of_two_heads(o):
+    # x = c (a power of two), eps = 0: mean(x^2) = c^2 and rstd = 1/|c| exactly, so
+    # x * rstd = sign(c) and out_j = sign(c) * (w_j + weight_bias) -- exact bf16
+    # values for these gains, known by hand
+    D = 64
+    w = np.resize(np.array([0.5, -0.25, 2.0, 0.0, -1.5, 0.75, 3.0, -2.0], np.float32), D)
+    for c in (0.25, -4.0):
+        x = bits(np.full((3, D), c))
+        out = o.qk_norm_f64(x, bits(w), 0.0, 0.0)
+        assert np.array_equal(out, np.broadcast_to(bits(np.sign(c) * w), (3, D)))
+        out = o.qk_norm_f64(x, bits(w), 1.0, 0.0)  # the bias is added to the gain
+        assert np.array_equal(out, np.broadcast_to(bits(np.sign(c) * (w + 1.0)), (3, D)))
+
+
+def pin_qknorm_torch(o):
+    # against torch.nn.functional.rms_norm in fp64 with weight w + weight_bias
+    # (a library routine), rounded once to bf16 by integer arithmetic
+    for D, wb, eps in ((64, 1.0, 1e-2), (128, 0.0, 1e-6), (256, 0.5, 1e-3)):
+        x = inputs.normal_bf16(21, 1, (7, 3, D))
+        w = inputs.normal_bf16(21, 2, (D,), 0.0, 0.3)
+        out = o.qk_norm_f64(x, w, wb, eps)
+        ref = F.rms_norm(torch.from_numpy(widen(x)), (D,), weight=torch.from_numpy(widen(w) + wb), eps=eps).numpy()
+        want = torch_bf16_bits_from_f64(ref)
+        # equal but where fp64 rounding of the two orders straddles a bf16 rounding boundary
+        diff = np.abs(out.astype(np.int32) - want.astype(np.int32))
+        assert diff.max() <= 1 and np.mean(diff == 0) > 0.999
+
+
+def pin_qknorm_per_head(o):
+    # each head is normalised on its own: scaling one head of a token leaves the
+    # others unchanged, and a head scaled by a power of two gives the same output
+    D = 128
+    x = inputs.normal_bf16(22, 1, (2, 4, D))
+    w = inputs.normal_bf16(22, 2, (D,), 1.0, 0.1)
+    base = o.qk_norm_f64(x, w, 0.0, 0.0)
+    x2 = widen(x).copy()
+    x2[:, 1] *= 64.0
+    out2 = o.qk_norm_f64(bits(x2.astype(np.float32)), w, 0.0, 0.0)
+    assert np.array_equal(out2, base)
+    # unit gain: mean(out^2) = ms / (ms + eps) up to the bf16 rounding of out
+    eps = 0.05
+    out = widen(o.qk_norm_f64(x, bits(np.ones(D, np.float32)), 0.0, eps))
+    ms = (widen(x) ** 2).mean(axis=-1)
+    assert np.allclose((out ** 2).mean(axis=-1), ms / (ms + eps), rtol=1e-2)
+
+
 # -------------------------------------------------------------------- router
 
 def pin_router_f64_numpy(o):

@@ -39,6 +39,12 @@ MUTATIONS = {
     "align_unpadded": ("int64_t padded = (counts[e] + pad - 1) / pad * pad;", "int64_t padded = counts[e];"),
     "h_not_rounded_to_bf16": ("if (h) h[j] = f64_to_bf16(v);", "if (h) h[j] = f32_to_bf16((float)v);"),
     "act_round_dropped": ("a[i] = round_act ? bf16_to_f64(f64_to_bf16(v)) : v;", "a[i] = v;"),
+    "qk_bias_dropped": ("(bf16_to_f64(w[j]) + weight_bias)", "(bf16_to_f64(w[j]))"),
+    "qk_bias_multiplied": ("(bf16_to_f64(w[j]) + weight_bias)", "(bf16_to_f64(w[j]) * weight_bias)"),
+    "qk_eps_dropped": ("sqrt(ss / (double)D + eps)", "sqrt(ss / (double)D)"),
+    "qk_sum_not_mean": ("sqrt(ss / (double)D + eps)", "sqrt(ss + eps)"),
+    "qk_x_unsquared": ("      ss += xv * xv;\n    }\n    double rstd = 1.0 / sqrt(ss / (double)D",
+                       "      ss += fabs(xv);\n    }\n    double rstd = 1.0 / sqrt(ss / (double)D"),
 }
 
 
