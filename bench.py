@@ -62,6 +62,11 @@ WORKLOADS = {
     "prefill_ncu": dict(H=4096, I=4096, E=8, k=8, Ts=[512], seed=0, zipf=None,
                         label="ncu case: T=512, H=I=4096, E=8, top_k=8 (prefill tiles, 512 tokens/expert)"),
 }
+# QK-norm ("CuTeDSL chez Perplexity", "Norme QK"): attention heads of a Qwen3-style layer
+QK_WORKLOADS = {
+    "qk_norm": dict(Hq=32, Hk=4, D=128, Ts=[1, 64, 4096], wb=0.0, eps=1e-6, seed=0,
+                    label="QK-norm sweep T in {1,64,4096}, 32 Q heads + 4 K heads, head_dim 128, bf16"),
+}
 KERNEL_SOURCES = {  # files whose content the ncu traffic figure of a kernel depends on
     "gemm_gate_up_swiglu": ["k_expert_gemm.cu", "tc_ptx.cuh", "moe_kernels.cuh", "moe_api.cu"],
     "gemm_down": ["k_expert_gemm.cu", "tc_ptx.cuh", "moe_kernels.cuh", "moe_api.cu"],
@@ -232,6 +237,151 @@ def cpu_oracle_rate(wl, host, per_batch_cap, reps=1, min_seconds=0.0, max_reps=5
             total_tok += sample.size
         r += 1
     return total_tok / total_s, total_tok, total_s, oracle.threads(), r
+
+
+# ----------------------------------------------------------------- QK-norm
+
+def qk_host_inputs(wl):
+    import numpy as np
+    from mixture_experts_layer_rmsnorm_gb300 import inputs
+    D, Hq, Hk, seed = wl["D"], wl["Hq"], wl["Hk"], wl["seed"]
+    qs = {T: inputs.normal_bf16(seed + 1000 * T, 31, (T, Hq, D)) for T in wl["Ts"]}
+    ks = {T: inputs.normal_bf16(seed + 1000 * T, 32, (T, Hk, D)) for T in wl["Ts"]}
+    qw = inputs.normal_bf16(seed, 33, (D,), 1.0, 0.1)
+    kw = inputs.normal_bf16(seed, 34, (D,), 1.0, 0.1)
+    return dict(qs=qs, ks=ks, qw=qw, kw=kw, np=np)
+
+
+def qk_cpu_rate(wl, host, min_seconds, max_tokens=256):
+    """Tokens/s of the CPU oracle's QK-norm on up to max_tokens tokens of each batch."""
+    import oracle
+    o = oracle.default()
+    ntok, secs, reps = 0, 0.0, 0
+    while secs < min_seconds and reps < 1000:
+        for T in wl["Ts"]:
+            n = min(T, max_tokens)
+            t0 = time.perf_counter()
+            o.qk_norm_f64(host["qs"][T][:n], host["qw"], wl["wb"], wl["eps"])
+            o.qk_norm_f64(host["ks"][T][:n], host["kw"], wl["wb"], wl["eps"])
+            secs += time.perf_counter() - t0
+            ntok += n
+        reps += 1
+    return ntok / secs, ntok, secs, reps
+
+
+def run_qk_norm(args, wl, world, rank, local):
+    import torch
+    from mixture_experts_layer_rmsnorm_gb300 import binding
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    host = qk_host_inputs(wl)
+    np = host["np"]
+    Ts, Hq, Hk, D = wl["Ts"], wl["Hq"], wl["Hk"], wl["D"]
+
+    def d16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+    qd = {T: d16(host["qs"][T]) for T in Ts}
+    kd = {T: d16(host["ks"][T]) for T in Ts}
+    qwd, kwd = d16(host["qw"]), d16(host["kw"])
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+
+    def call(T, q, k):
+        st = binding.moe_qk_norm(T, Hq, Hk, D, q.data_ptr(), k.data_ptr(), qwd.data_ptr(), kwd.data_ptr(),
+                                 wl["wb"], wl["eps"], stream.cuda_stream)
+        if st != binding.MOE_OK:
+            raise binding.MoeError(st, "moe_qk_norm")
+
+    # batches of 32 MB or more: R copies (R x bytes > 256 MB, twice L2) run back to
+    # back between one pair of events, so every call reads and writes HBM; smaller
+    # ones: one call after an L2 flush (their time is launch and memory latency)
+    reps = {}
+    for T in Ts:
+        nbytes = 2 * T * (Hq + Hk) * D * 2
+        reps[T] = 1 if nbytes < (32 << 20) else -(-(256 << 20) // nbytes) + 1
+    qcopies = {T: [qd[T]] + [qd[T].clone() for _ in range(reps[T] - 1)] for T in Ts}
+    kcopies = {T: [kd[T]] + [kd[T].clone() for _ in range(reps[T] - 1)] for T in Ts}
+
+    for _ in range(args.warmup):
+        for T in Ts:
+            for r in range(reps[T]):
+                call(T, qcopies[T][r], kcopies[T][r])
+    ev = {T: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)] for T in Ts}
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    for s_ in range(args.steps):
+        for T in Ts:
+            flush.fill_(s_ & 0xFF)
+            flush_rd.sum()
+            a, b = ev[T][s_]
+            a.record(stream)
+            for r in range(reps[T]):  # in place: each call normalises the previous call's output
+                call(T, qcopies[T][r], kcopies[T][r])
+            b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    per_T, total_ms, total_bytes = {}, 0.0, 0
+    for T in Ts:
+        ms = [a.elapsed_time(b) / reps[T] for a, b in ev[T]]
+        med = statistics.median(ms)
+        nbytes = 2 * T * (Hq + Hk) * D * 2 + 2 * D * 2
+        total_ms += sum(ms)
+        total_bytes += nbytes * len(ms)
+        per_T[str(T)] = {"us_median": round(med * 1e3, 2), "tokens_per_s": round(T / (med * 1e-3), 1),
+                         "bytes": nbytes, "GBps": round(nbytes / (med * 1e-3) / 1e9, 1),
+                         "timing": ("one call after an L2 flush" if reps[T] == 1 else
+                                    f"{reps[T]} calls on distinct buffers back to back, per-call mean")}
+    ms_step = reduce_max(total_ms / args.steps, world)
+    value = world * sum(Ts) / (ms_step * 1e-3)
+    peaks, peak_kind = load_peaks()
+    achieved = total_bytes / (total_ms * 1e-3) / 1e9
+    big = str(max(Ts))
+    roof = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+            "peak_source": f"hbm_gbs ({peak_kind}, copy bandwidth)", "kernel": "qk_norm_kernel<128>",
+            "algorithmic_per_launch": total_bytes / (args.steps * len(Ts)),
+            "avg_launch_us": round(total_ms / (args.steps * len(Ts)) * 1e3, 2),
+            "largest_T": {"T": int(big), "GBps": per_T[big]["GBps"],
+                          "frac": round(per_T[big]["GBps"] / peaks["hbm_gbs"], 4)}}
+    # end to end: pinned host q, k -> device, the call, the result back, every step
+    hq = {T: torch.from_numpy(host["qs"][T].view(np.int16)).pin_memory() for T in Ts}
+    hk = {T: torch.from_numpy(host["ks"][T].view(np.int16)).pin_memory() for T in Ts}
+    oq = {T: torch.empty_like(hq[T]).pin_memory() for T in Ts}
+    ok_ = {T: torch.empty_like(hk[T]).pin_memory() for T in Ts}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        for T in Ts:
+            qd[T].copy_(hq[T], non_blocking=True)
+            kd[T].copy_(hk[T], non_blocking=True)
+            call(T, qd[T], kd[T])
+            oq[T].copy_(qd[T], non_blocking=True)
+            ok_[T].copy_(kd[T], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / args.steps, world)
+    io = sum(2 * T * (Hq + Hk) * D for T in Ts)
+    out = {"metric": "QK-norm us & tokens/s; % HBM roofline", "value": round(value, 1), "unit": "tokens/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded generator)",
+           "config": {"workload": wl["label"], "Hq": Hq, "Hk": Hk, "head_dim": D, "weight_bias": wl["wb"],
+                      "eps": wl["eps"], "l2": "flushed before every call (256 MB write + 256 MB read), outside the "
+                                               "timed CUDA-event intervals",
+                      "parallelism": f"replicas x{world}", "per_T": per_T},
+           "roofline": roof,
+           "e2e": {"value": round(world * sum(Ts) / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                   "h2d_bytes_per_step": io, "d2h_bytes_per_step": io, "ms_per_step": round(e2e_ms, 4)},
+           "gpu_launches": args.steps * sum(reps.values()), "clocks": clocks}
+    return out, host
 
 
 # ----------------------------------------------------------------- our arm
@@ -440,7 +590,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS) + sorted(QK_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens-per-batch", type=int, default=32,
                     help="CPU oracle sample: at most this many tokens of each batch per step")
@@ -452,11 +602,38 @@ def main():
     if args.warmup < 3:
         print("bench: at least 3 warm-up steps are required; using 3", file=sys.stderr)
         args.warmup = 3
-    wl = WORKLOADS[args.workload]
     world, rank, local = dist_env()
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")
+    if args.workload in QK_WORKLOADS:
+        wl = QK_WORKLOADS[args.workload]
+        if args.impl == "reference":
+            if rank == 0:
+                host = qk_host_inputs(wl)
+                rate, ntok, secs, reps = qk_cpu_rate(wl, host, min_seconds=min(args.cpu_seconds, 5.0))
+                print(json.dumps({"impl": "reference", "metric": "QK-norm us & tokens/s; % HBM roofline",
+                                  "value": round(rate, 1), "unit": "tokens/s", "n_gpus": world, "steps": reps,
+                                  "warmup": 0, "higher_is_better": True, "dtype": "f64", "data": "synthetic",
+                                  "config": {"workload": wl["label"], "reference": "CPU oracle (fp64 C)"},
+                                  "cpu_baseline": {"value": round(rate, 1), "unit": "tokens/s", "cores": 1,
+                                                   "kind": "oracle", "sample": f"{ntok} tokens, {secs:.1f} s"},
+                                  "e2e": {"value": round(rate, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                          "d2h_bytes_per_step": 0}}), flush=True)
+        else:
+            out, host = run_qk_norm(args, wl, world, rank, local)
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                rate, ntok, secs, reps = qk_cpu_rate(wl, host, min_seconds=min(args.cpu_seconds, 5.0))
+                out["cpu_baseline"] = {"value": round(rate, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                       "sample": f"{ntok} tokens (up to 256 of each batch, {reps} passes), "
+                                                 f"{secs:.1f} s"}
+            if rank == 0:
+                print(json.dumps(out), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    wl = WORKLOADS[args.workload]
 
     if args.impl == "reference":
         if rank == 0:

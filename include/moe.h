@@ -239,6 +239,23 @@ MOE_API moe_status moe_device_status(const void* workspace, size_t workspace_byt
                              int32_t* detail);
 
 /* Static text for a status code. */
+/* QK-norm, in place: RMSNorm of every attention head of Q and of K
+ * ("CuTeDSL chez Perplexity", "Norme QK"):
+ *   out_j = bf16((w_j + weight_bias) * (x_j * rstd)),  rstd = 1/sqrt(mean_j x_j^2 + eps),
+ * over the D elements of each head, with q_weight[D] applied to every head of Q
+ * and k_weight[D] to every head of K.  Computed in fp32 in one fixed order
+ * (see k_qk_norm.cu), so the result is within one bf16 ulp of the exact value.
+ *   q [T, Hq, D] bf16, k [T, Hk, D] bf16: device, contiguous, 16-byte aligned,
+ *   overwritten with the result; q_weight / k_weight [D] bf16.
+ *   D: 64, 128 or 256.  Hq or Hk may be 0 (its pointers are then unused).
+ * Errors: MOE_ERR_INVALID_ARG for a bad D, negative sizes, null or misaligned
+ * pointers of a non-empty tensor, or a non-finite eps / weight_bias;
+ * MOE_ERR_UNSUPPORTED for T * (Hq + Hk) >= 2^31 heads; T = 0 is a no-op.
+ * Asynchronous on `stream`; no workspace. */
+MOE_API moe_status moe_qk_norm(int64_t T, int32_t Hq, int32_t Hk, int32_t D, moe_bf16* q, moe_bf16* k,
+                               const moe_bf16* q_weight, const moe_bf16* k_weight, float weight_bias, float eps,
+                               moe_stream_t stream);
+
 /* Self-test of the failure path of the library's bounded device waits (no
  * counterpart on the pages): enqueues one small kernel whose two waits -- on
  * an mbarrier phase that nothing completes and on a flag in the workspace's

@@ -66,12 +66,14 @@ def load(build: bool = True):
             lib.moe_device_status.argtypes = [p, sz, p, ctypes.POINTER(ctypes.c_int32)]
             lib.moe_kernels_per_call.argtypes = [sp, ctypes.POINTER(ctypes.c_int32)]
             lib.moe_selftest_wait_timeout.argtypes = [p, sz, i64, p]
+            lib.moe_qk_norm.argtypes = [i64, i32, i32, i32, p, p, p, p, ctypes.c_float, ctypes.c_float, p]
             lib.moe_forward_fused_front.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_status_string.argtypes = [ctypes.c_int]
             lib.moe_status_string.restype = ctypes.c_char_p
             for f in ("moe_workspace_size", "moe_forward", "moe_forward_events", "moe_route_debug",
                       "moe_workspace_views", "moe_device_status", "moe_forward_static_scratch",
-                      "moe_kernels_per_call", "moe_forward_fused_front", "moe_selftest_wait_timeout"):
+                      "moe_kernels_per_call", "moe_forward_fused_front", "moe_selftest_wait_timeout",
+                      "moe_qk_norm"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -165,6 +167,11 @@ def moe_device_status(workspace, workspace_bytes, stream) -> tuple[int, list]:
     d = (ctypes.c_int32 * 4)()
     st = load().moe_device_status(workspace, workspace_bytes, stream, d)
     return st, list(d)
+
+
+def moe_qk_norm(T, Hq, Hk, D, q, k, q_weight, k_weight, weight_bias, eps, stream) -> int:
+    return load().moe_qk_norm(int(T), int(Hq), int(Hk), int(D), q, k, q_weight, k_weight, float(weight_bias),
+                              float(eps), stream)
 
 
 def moe_selftest_wait_timeout(workspace, workspace_bytes, timeout_ns, stream) -> int:

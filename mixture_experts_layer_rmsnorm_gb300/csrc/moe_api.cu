@@ -473,6 +473,22 @@ moe_status moe_device_status(const void* workspace, size_t workspace_bytes, moe_
   return MOE_OK;
 }
 
+moe_status moe_qk_norm(int64_t T, int32_t Hq, int32_t Hk, int32_t D, moe_bf16* q, moe_bf16* k,
+                       const moe_bf16* q_weight, const moe_bf16* k_weight, float weight_bias, float eps,
+                       moe_stream_t stream) {
+  if (T < 0 || Hq < 0 || Hk < 0 || (D != 64 && D != 128 && D != 256)) return MOE_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || !std::isfinite(eps) || !std::isfinite(weight_bias)) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(Hq) + Hk > (1 << 20) || T * (static_cast<int64_t>(Hq) + Hk) >= (int64_t(1) << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if (T == 0 || Hq + Hk == 0) return MOE_OK;
+  if (Hq > 0 && (!q || !q_weight || !aligned(q, 16) || !aligned(q_weight, 16))) return MOE_ERR_INVALID_ARG;
+  if (Hk > 0 && (!k || !k_weight || !aligned(k, 16) || !aligned(k_weight, 16))) return MOE_ERR_INVALID_ARG;
+  if (moe::launch_qk_norm(q, k, q_weight, k_weight, T, Hq, Hk, D, weight_bias, eps,
+                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 moe_status moe_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t timeout_ns,
                                      moe_stream_t stream) {
   if (!workspace || workspace_bytes < 64 || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;

@@ -159,6 +159,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// QK-norm of q[T, Hq, D] and k[T, Hk, D] in place (k_qk_norm.cu); D = 64, 128 or 256.
+cudaError_t launch_qk_norm(uint16_t* q, uint16_t* k, const uint16_t* q_weight, const uint16_t* k_weight, int64_t T,
+                           int Hq, int Hk, int D, float weight_bias, float eps, cudaStream_t stream);
+
 // Self-test of the bounded waits: one kernel whose two waits (an mbarrier
 // phase, a global flag) run out after timeout_ns and report MOE_ERR_TIMEOUT
 // with kernel id kKernSelfTest in the error word at `err` (>= 64 bytes).

@@ -69,6 +69,22 @@ def test_selftest_wait_timeout_rejects_bad_arguments_without_a_gpu():
     assert binding.moe_selftest_wait_timeout(A, 64, 2_000_000_000, None) == binding.MOE_ERR_INVALID_ARG
 
 
+def test_qk_norm_rejects_bad_arguments_without_a_gpu():
+    A = 1 << 20
+    ok = dict(T=4, Hq=2, Hk=1, D=128, q=A, k=A, qw=A, kw=A, wb=0.0, eps=1e-6)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return binding.moe_qk_norm(a["T"], a["Hq"], a["Hk"], a["D"], a["q"], a["k"], a["qw"], a["kw"], a["wb"],
+                                   a["eps"], None)
+
+    assert call(T=0) == binding.MOE_OK                       # nothing to do, nothing touched
+    assert call(Hq=0, Hk=0) == binding.MOE_OK
+    for bad in (dict(D=100), dict(D=32), dict(T=-1), dict(Hq=-1), dict(q=None), dict(kw=None), dict(q=A + 8),
+                dict(eps=-1.0), dict(eps=float("nan")), dict(wb=float("inf"))):
+        assert call(**bad) == binding.MOE_ERR_INVALID_ARG, bad
+
+
 def test_forward_rejects_bad_arguments_without_a_gpu():
     # fake, aligned, never-dereferenced addresses: every case fails validation first
     s = binding.shape(4, 128, 256, 8, 2)
