@@ -37,6 +37,18 @@
  *   Combine     y_t = sum_j w_tj * o_tj, accumulated in j order, cast to bf16
  *                 -- "CuTeDSL chez Perplexity", MoE dispatch/combine, "Local"
  *                    (weighted accumulation in registers into the output).
+ *   MXFP8       block-scaled FP8: blocks of 32 consecutive elements along the
+ *               reduction dimension share a power-of-two scale X (an E8M0 byte);
+ *               each element is stored as an E4M3 code of v / X, with X chosen
+ *               from the block's absolute maximum
+ *                 -- "CuTeDSL chez Perplexity", "Prise en charge de Blackwell"
+ *                    (MXFP8 block scaling, absolute maximum over 32 elements).
+ *               The pages give no recipe for X; the plain one is the OCP
+ *               Microscaling rule X = 2^(floor(log2(amax)) - 8), 8 being the
+ *               largest E4M3 exponent, with codes rounded to nearest (ties to
+ *               even) and clamped to +-448.  The FP8 layer quantizes the expert
+ *               weights, the gathered token rows and the SwiGLU activations this
+ *               way and computes everything else as the bf16 layer does.
  *   QK-norm     per attention head of Q and of K (head_dim D elements):
  *               out_j = (w_j + weight_bias) * (x_j * rstd), rstd = 1/sqrt(mean x^2
  *               + eps), with one weight vector w[D] for all heads of Q and one for
@@ -167,6 +179,86 @@ void oracle_rmsnorm_f64(int64_t T, int64_t H, const uint16_t* x, const uint16_t*
                         uint16_t* h, double* h_exact) {
   for (int64_t t = 0; t < T; ++t)
     rmsnorm_row_f64(H, x + t * H, g, eps, h ? h + t * H : NULL, h_exact ? h_exact + t * H : NULL);
+}
+
+/* ------------------------------------------------------------------ */
+/* MXFP8: E4M3 codes with E8M0 block scales                             */
+/* ------------------------------------------------------------------ */
+
+/* E4M3 (bias 7, no infinities; exponent field 0: subnormal m * 2^-9): the value
+ * of a code.  The codes 0x7F / 0xFF (NaN) are never produced here. */
+double oracle_e4m3_decode(uint8_t c) {
+  int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+  return sgn ? -v : v;
+}
+
+/* Nearest E4M3 code of a finite v, ties to an even mantissa, |v| > 448 -> 448. */
+uint8_t oracle_e4m3_encode(double v) {
+  int sgn = signbit(v) ? 1 : 0;
+  double a = fabs(v);
+  int e, m;
+  if (a < ldexp(1.0, -6)) { /* subnormal grid: steps of 2^-9 */
+    double q = nearbyint(a / ldexp(1.0, -9)); /* 0 .. 8; 8 is the smallest normal */
+    if (q >= 8.0) {
+      e = 1;
+      m = 0;
+    } else {
+      e = 0;
+      m = (int)q;
+    }
+  } else {
+    int ex = (int)floor(log2(a));
+    if (ldexp(1.0, ex) > a) ex -= 1; /* guard the log2 of exact powers of two */
+    if (ldexp(1.0, ex + 1) <= a) ex += 1;
+    double q = nearbyint(a / ldexp(1.0, ex - 3)); /* 8 .. 16 */
+    if (q >= 16.0) {
+      q = 8.0;
+      ex += 1;
+    }
+    e = ex + 7;
+    m = (int)q - 8;
+    if (e > 15 || (e == 15 && m > 6)) { /* beyond 448: saturate */
+      e = 15;
+      m = 6;
+    }
+  }
+  return (uint8_t)((sgn << 7) | (e << 3) | m);
+}
+
+/* Block exponent of 32 values with absolute maximum amax:
+ * floor(log2(amax)) - 8, clamped to the E8M0 range [-127, 127]; -127 for amax = 0. */
+static int mx_block_exponent(double amax) {
+  if (amax == 0.0) return -127;
+  int ex = (int)floor(log2(amax));
+  if (ldexp(1.0, ex) > amax) ex -= 1;
+  if (ldexp(1.0, ex + 1) <= amax) ex += 1;
+  ex -= 8;
+  return ex < -127 ? -127 : (ex > 127 ? 127 : ex);
+}
+
+/* rows x K bf16 values (K a multiple of 32) -> codes [rows, K] and scales
+ * [rows, K/32] (E8M0 bytes: exponent + 127). */
+void oracle_mx_quantize(int64_t rows, int64_t K, const uint16_t* x, uint8_t* codes, uint8_t* scales) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < K / 32; ++b) {
+      const uint16_t* xb = x + r * K + b * 32;
+      double amax = 0.0;
+      for (int j = 0; j < 32; ++j) {
+        double a = fabs(bf16_to_f64(xb[j]));
+        if (a > amax) amax = a;
+      }
+      int ex = mx_block_exponent(amax);
+      scales[r * (K / 32) + b] = (uint8_t)(ex + 127);
+      for (int j = 0; j < 32; ++j) codes[r * K + b * 32 + j] = oracle_e4m3_encode(ldexp(bf16_to_f64(xb[j]), -ex));
+    }
+}
+
+/* values of codes [rows, K] with scales [rows, K/32] */
+void oracle_mx_dequantize(int64_t rows, int64_t K, const uint8_t* codes, const uint8_t* scales, double* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t j = 0; j < K; ++j)
+      out[r * K + j] = ldexp(oracle_e4m3_decode(codes[r * K + j]), (int)scales[r * (K / 32) + j / 32] - 127);
 }
 
 /* ------------------------------------------------------------------ */
@@ -410,6 +502,51 @@ static void expert_row_f64(int64_t H, int64_t I, const uint16_t* h16, const doub
   }
 }
 
+/* One token through one expert of the FP8 layer: h (bf16) quantized to MXFP8
+ * along H, the weights given as MXFP8 codes and scales, the bf16 SwiGLU
+ * activation quantized to MXFP8 along I; products and sums in fp64.
+ *   W13c [2I, H] codes, W13s [2I, H/32] scales; W2c [H, I], W2s [H, I/32]. */
+static void expert_row_mx_f64(int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c, const uint8_t* W13s,
+                              const uint8_t* W2c, const uint8_t* W2s, double* a, double* o) {
+  uint8_t* hc = (uint8_t*)malloc((size_t)H);
+  uint8_t* hs = (uint8_t*)malloc((size_t)(H / 32));
+  double* hq = (double*)malloc(sizeof(double) * (size_t)H);
+  oracle_mx_quantize(1, H, h16, hc, hs);
+  oracle_mx_dequantize(1, H, hc, hs, hq);
+  double* wrow = (double*)malloc(sizeof(double) * (size_t)(H > I ? H : I));
+  double* wrow2 = (double*)malloc(sizeof(double) * (size_t)H);
+  uint16_t* a16 = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
+  for (int64_t i = 0; i < I; ++i) {
+    oracle_mx_dequantize(1, H, W13c + i * H, W13s + i * (H / 32), wrow);
+    oracle_mx_dequantize(1, H, W13c + (I + i) * H, W13s + (I + i) * (H / 32), wrow2);
+    double gate = 0.0, up = 0.0;
+    for (int64_t j = 0; j < H; ++j) {
+      gate += hq[j] * wrow[j];
+      up += hq[j] * wrow2[j];
+    }
+    double silu = gate / (1.0 + exp(-gate));
+    a16[i] = f64_to_bf16(silu * up);
+  }
+  uint8_t* ac = (uint8_t*)malloc((size_t)I);
+  uint8_t* as = (uint8_t*)malloc((size_t)(I / 32));
+  oracle_mx_quantize(1, I, a16, ac, as);
+  oracle_mx_dequantize(1, I, ac, as, a);
+  for (int64_t n = 0; n < H; ++n) {
+    oracle_mx_dequantize(1, I, W2c + n * I, W2s + n * (I / 32), wrow);
+    double acc = 0.0;
+    for (int64_t i = 0; i < I; ++i) acc += a[i] * wrow[i];
+    o[n] = acc;
+  }
+  free(hc); free(hs); free(hq); free(wrow); free(wrow2); free(a16); free(ac); free(as);
+}
+
+void oracle_expert_mx_f64(int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c, const uint8_t* W13s,
+                          const uint8_t* W2c, const uint8_t* W2s, double* a_out, double* o) {
+  double* a = a_out ? a_out : (double*)malloc(sizeof(double) * (size_t)I);
+  expert_row_mx_f64(H, I, h16, W13c, W13s, W2c, W2s, a, o);
+  if (!a_out) free(a);
+}
+
 void oracle_expert_f64(int64_t H, int64_t I, const uint16_t* h16, const double* h64, const uint16_t* W13e,
                        const uint16_t* W2e, int round_act, double* a_out, double* o) {
   double* a = a_out ? a_out : (double*)malloc(sizeof(double) * (size_t)I);
@@ -428,6 +565,8 @@ typedef struct {
   const uint16_t *x, *g;
   const float *Wr, *bias;
   const uint16_t *W13, *W2;
+  /* FP8 layer (when W13c != NULL): MXFP8 weights */
+  const uint8_t *W13c, *W13s, *W2c, *W2s;
   int64_t ns;
   const int64_t* sample;
   /* per-sample scratch / outputs */
@@ -459,6 +598,13 @@ static void fwd_expert_item(int64_t it, void* p) {
   int j = (int)(it % c->k);
   int64_t e = c->ids[s * c->k + j];
   double* a = (double*)malloc(sizeof(double) * (size_t)c->I);
+  if (c->W13c) {
+    expert_row_mx_f64(c->H, c->I, c->h16 + s * c->H, c->W13c + e * 2 * c->I * c->H,
+                      c->W13s + e * 2 * c->I * (c->H / 32), c->W2c + e * c->H * c->I, c->W2s + e * c->H * (c->I / 32),
+                      a, c->o + it * c->H);
+    free(a);
+    return;
+  }
   const uint16_t* W13e = c->W13 + e * 2 * c->I * c->H;
   const uint16_t* W2e = c->W2 + e * c->H * c->I;
   if (c->round_inter)
@@ -475,11 +621,12 @@ static void fwd_expert_item(int64_t it, void* p) {
  * (fp64-path norm output), l32[s,E] (fp32 canonical logits), l64[s,E].
  * round_inter = 1 rounds h and the SwiGLU output to bf16 (the layer's storage
  * types); 0 keeps them in fp64 ("pure" mode).  Returns 0, or -1 on bad input. */
-int oracle_moe_forward(int64_t T, int64_t H, int64_t I, int64_t E, int k, int renorm, double eps,
-                       const uint16_t* x, const uint16_t* g, const float* Wr, const float* bias,
-                       const uint16_t* W13, const uint16_t* W2, int64_t ns, const int64_t* sample,
-                       int round_inter, int nthreads, int32_t* ids, double* w, double* y64, uint16_t* y16,
-                       uint16_t* h16_out, float* l32_out, double* l64_out) {
+static int moe_forward_any(int64_t T, int64_t H, int64_t I, int64_t E, int k, int renorm, double eps,
+                           const uint16_t* x, const uint16_t* g, const float* Wr, const float* bias,
+                           const uint16_t* W13, const uint16_t* W2, const uint8_t* W13c, const uint8_t* W13s,
+                           const uint8_t* W2c, const uint8_t* W2s, int64_t ns, const int64_t* sample,
+                           int round_inter, int nthreads, int32_t* ids, double* w, double* y64, uint16_t* y16,
+                           uint16_t* h16_out, float* l32_out, double* l64_out) {
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E || ns < 0) return -1;
   for (int64_t s = 0; s < ns; ++s) {
     int64_t t = sample ? sample[s] : s;
@@ -489,6 +636,7 @@ int oracle_moe_forward(int64_t T, int64_t H, int64_t I, int64_t E, int k, int re
   fwd_ctx c;
   c.T = T; c.H = H; c.I = I; c.E = E; c.k = k; c.renorm = renorm; c.round_inter = round_inter;
   c.eps = eps; c.x = x; c.g = g; c.Wr = Wr; c.bias = bias; c.W13 = W13; c.W2 = W2;
+  c.W13c = W13c; c.W13s = W13s; c.W2c = W2c; c.W2s = W2s;
   c.ns = ns; c.sample = sample;
   c.h16 = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(ns * H));
   c.h64 = (double*)malloc(sizeof(double) * (size_t)(ns * H));
@@ -514,4 +662,26 @@ int oracle_moe_forward(int64_t T, int64_t H, int64_t I, int64_t E, int k, int re
   return 0;
 }
 
-int oracle_version(void) { return 1; }
+int oracle_moe_forward(int64_t T, int64_t H, int64_t I, int64_t E, int k, int renorm, double eps,
+                       const uint16_t* x, const uint16_t* g, const float* Wr, const float* bias,
+                       const uint16_t* W13, const uint16_t* W2, int64_t ns, const int64_t* sample,
+                       int round_inter, int nthreads, int32_t* ids, double* w, double* y64, uint16_t* y16,
+                       uint16_t* h16_out, float* l32_out, double* l64_out) {
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, W13, W2, NULL, NULL, NULL, NULL, ns, sample,
+                         round_inter, nthreads, ids, w, y64, y16, h16_out, l32_out, l64_out);
+}
+
+/* The FP8 layer: the same routing; the experts with MXFP8 weights (codes and
+ * scales per expert as in expert_row_mx_f64, experts stacked) and MXFP8
+ * activations.  H and I multiples of 32. */
+int oracle_moe_forward_mx(int64_t T, int64_t H, int64_t I, int64_t E, int k, int renorm, double eps,
+                          const uint16_t* x, const uint16_t* g, const float* Wr, const float* bias,
+                          const uint8_t* W13c, const uint8_t* W13s, const uint8_t* W2c, const uint8_t* W2s,
+                          int64_t ns, const int64_t* sample, int nthreads, int32_t* ids, double* w, double* y64,
+                          uint16_t* y16) {
+  if (H % 32 || I % 32 || !W13c || !W13s || !W2c || !W2s) return -1;
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, ns, sample,
+                         1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
+}
+
+int oracle_version(void) { return 2; }

@@ -155,6 +155,113 @@ def pin_qknorm_per_head(o):
     assert np.allclose((out ** 2).mean(axis=-1), ms / (ms + eps), rtol=1e-2)
 
 
+# ---------------------------------------------------------------------- MXFP8
+
+def _torch_e4m3_bits(v32: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(v32, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def pin_e4m3_decode_torch(o):
+    # every finite code against torch's float8_e4m3fn (a library routine)
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = np.array([o.e4m3_decode(int(c)) for c in codes])
+    assert np.array_equal(ours, ref)
+
+
+def pin_e4m3_encode(o):
+    # hand-derived codes: 1.0, the largest finite value, saturation, the smallest
+    # subnormal, and ties to an even mantissa
+    assert o.e4m3_encode(1.0) == 0x38 and o.e4m3_encode(-1.0) == 0xB8
+    assert o.e4m3_encode(448.0) == 0x7E and o.e4m3_encode(500.0) == 0x7E and o.e4m3_encode(-1e6) == 0xFE
+    assert o.e4m3_encode(2.0 ** -9) == 0x01 and o.e4m3_encode(2.0 ** -10) == 0x00  # tie -> 0 (even)
+    assert o.e4m3_encode(3 * 2.0 ** -10) == 0x02                                   # tie -> 2 (even)
+    assert o.e4m3_encode(1.0625) == 0x38 and o.e4m3_encode(1.1875) == 0x3A
+    # in range: torch's round-to-nearest-even cast, on random values of all
+    # magnitudes and on every midpoint between neighbouring codes
+    rng = np.random.default_rng(7)
+    v = (rng.standard_normal(20000) * np.exp2(rng.uniform(-12, 8, 20000))).astype(np.float32)
+    v = v[np.abs(v) <= 448]
+    vals = np.array(sorted({o.e4m3_decode(c) for c in range(0x7F)}))
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    for arr in (v, mids, -mids):
+        ours = np.array([o.e4m3_encode(float(a)) for a in arr], np.uint8)
+        assert np.array_equal(ours, _torch_e4m3_bits(arr))
+
+
+def pin_mx_block_scale(o):
+    # block absolute maximum amax = r * 2^p: scale exponent p - 8, the maximum's
+    # code 256 * r (r = 1 -> 0x78, r = 1.75 -> 448 = 0x7E, r = 1.90625 -> 488, saturated)
+    for p, r, code in ((0, 1.0, 0x78), (-6, 1.75, 0x7E), (3, 1.90625, 0x7E), (-20, 1.5, 0x7C)):
+        x = np.zeros((1, 64), np.float32)
+        x[0, 5] = r * 2.0 ** p
+        x[0, 40] = -r * 2.0 ** p
+        x[0, 7] = 2.0 ** (p - 5)
+        codes, scales = o.mx_quantize(bits(x))
+        assert scales.tolist() == [[p - 8 + 127, p - 8 + 127]]
+        assert codes[0, 5] == code and codes[0, 40] == code | 0x80
+        assert o.e4m3_decode(int(codes[0, 7])) == 2.0 ** 3  # 2^(p-5) / 2^(p-8)
+    codes, scales = o.mx_quantize(np.zeros((2, 32), np.uint16))
+    assert np.all(codes == 0) and np.all(scales == 0)
+
+
+def pin_mx_roundtrip_error(o):
+    # dequantize(quantize(x)): at most half an E4M3 step per element, except the
+    # values above 448 X (block maxima with a mantissa above 1.75), clamped to 448 X
+    x = inputs.normal_bf16(23, 1, (16, 256), 0.0, 0.02)
+    codes, scales = o.mx_quantize(x)
+    d = o.mx_dequantize(codes, scales)
+    xv = widen(x)
+    X = np.exp2(np.repeat(scales.astype(np.float64) - 127, 32, axis=1))
+    r = np.abs(xv) / X
+    assert np.all(r < 512)  # the block maximum lies in [256, 512) X
+    sat = r > 448
+    assert np.array_equal(d[sat], np.sign(xv[sat]) * 448 * X[sat])
+    step = np.maximum(np.exp2(np.floor(np.log2(np.maximum(r, 2.0 ** -6))) - 3), 2.0 ** -9) * X
+    assert np.all(np.abs(d - xv)[~sat] <= step[~sat] / 2 * (1 + 1e-12))
+
+
+def _torch_mx_dequant(v64: np.ndarray) -> np.ndarray:
+    """Independent MXFP8 round trip of fp64 rows (values exact in bf16): block
+    exponents from frexp, codes from torch's fp8 cast of the clamped scaled values."""
+    v = v64.reshape(-1, 32)
+    amax = np.abs(v).max(axis=1)
+    _, e = np.frexp(amax)                   # amax = m * 2^e, m in [0.5, 1)
+    ex = np.where(amax > 0, e - 1 - 8, -127)
+    ex = np.clip(ex, -127, 127)
+    scaled = np.clip(v / np.exp2(ex)[:, None], -448, 448).astype(np.float32)
+    q = torch.from_numpy(scaled).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return (q * np.exp2(ex)[:, None]).reshape(v64.shape)
+
+
+def pin_mx_layer_torch(o):
+    # the FP8 layer against a torch restatement: the same routing, MXFP8 round
+    # trips of h, the weights and the bf16 activation, fp64 products and sums
+    T, H, I, E, k = 3, 64, 96, 4, 2
+    li = rand_layer(T, H, I, E, seed=24)
+    w13c, w13s = o.mx_quantize(li.w13)
+    w2c, w2s = o.mx_quantize(li.w2)
+    res = o.moe_forward_mx(li.x, li.g, li.w_router, None, w13c, w13s, w2c, w2s, k, True, 1e-6)
+    ref = o.moe_forward(li.x, li.g, li.w_router, None, li.w13, li.w2, k, True, 1e-6)
+    assert np.array_equal(res["ids"], ref["ids"]) and np.allclose(res["w"], ref["w"], rtol=0, atol=0)
+    W13 = _torch_mx_dequant(widen(li.w13))
+    W2 = _torch_mx_dequant(widen(li.w2))
+    y = np.zeros((T, H))
+    for t in range(T):
+        hq = _torch_mx_dequant(widen(ref["h16"][t]))
+        for j in range(k):
+            e = int(res["ids"][t, j])
+            gate = W13[e, :I] @ hq
+            up = W13[e, I:] @ hq
+            a = widen(torch_bf16_bits_from_f64(gate / (1 + np.exp(-gate)) * up))
+            y[t] += res["w"][t, j] * (W2[e] @ _torch_mx_dequant(a))
+    assert np.allclose(res["y64"], y, rtol=1e-12, atol=1e-15)
+    # and close to the bf16 layer: the MXFP8 error of a 64-long dot product
+    rel = np.linalg.norm(res["y64"] - ref["y64"]) / np.linalg.norm(ref["y64"])
+    assert 1e-4 < rel < 0.1
+
+
 # -------------------------------------------------------------------- router
 
 def pin_router_f64_numpy(o):

@@ -39,6 +39,14 @@ MUTATIONS = {
     "align_unpadded": ("int64_t padded = (counts[e] + pad - 1) / pad * pad;", "int64_t padded = counts[e];"),
     "h_not_rounded_to_bf16": ("if (h) h[j] = f64_to_bf16(v);", "if (h) h[j] = f32_to_bf16((float)v);"),
     "act_round_dropped": ("a[i] = round_act ? bf16_to_f64(f64_to_bf16(v)) : v;", "a[i] = v;"),
+    "mx_emax_7": ("  ex -= 8;\n  return ex < -127", "  ex -= 7;\n  return ex < -127"),
+    "e4m3_round_half_up": ("double q = nearbyint(a / ldexp(1.0, ex - 3));", "double q = floor(a / ldexp(1.0, ex - 3) + 0.5);"),
+    "e4m3_no_saturation": ("      e = 15;\n      m = 6;", "      e = 15;\n      m = 7;"),
+    "e4m3_subnormal_scale": ("double v = e == 0 ? ldexp((double)m, -9)", "double v = e == 0 ? ldexp((double)m, -10)"),
+    "mx_act_not_quantized": ("  oracle_mx_quantize(1, I, a16, ac, as);\n  oracle_mx_dequantize(1, I, ac, as, a);",
+                             "  for (int64_t i = 0; i < I; ++i) a[i] = bf16_to_f64(a16[i]);"),
+    "mx_token_not_quantized": ("  oracle_mx_dequantize(1, H, hc, hs, hq);",
+                               "  for (int64_t j = 0; j < H; ++j) hq[j] = bf16_to_f64(h16[j]);"),
     "qk_bias_dropped": ("(bf16_to_f64(w[j]) + weight_bias)", "(bf16_to_f64(w[j]))"),
     "qk_bias_multiplied": ("(bf16_to_f64(w[j]) + weight_bias)", "(bf16_to_f64(w[j]) * weight_bias)"),
     "qk_eps_dropped": ("sqrt(ss / (double)D + eps)", "sqrt(ss / (double)D)"),
