@@ -228,6 +228,18 @@ typedef struct {
   int64_t P_max;      /* T*top_k + E*15: the most padded rows any routing can need */
 } moe_views;
 
+/* Device addresses of the MXFP8 layer's extra intermediates (its token codes
+ * are in moe_views.xg).  Scales in the layout described above. */
+typedef struct {
+  void* x_codes;    /* [P_max, H] E4M3 codes of the gathered token rows */
+  void* x_scales;   /* their scales */
+  void* act_codes;  /* [P_max, I] E4M3 codes of the SwiGLU activations */
+  void* act_scales; /* their scales */
+} moe_mx_views;
+
+MOE_API moe_status moe_workspace_views_mx(const moe_shape* shape, void* workspace, size_t workspace_bytes,
+                                          moe_views* views, moe_mx_views* mx_views);
+
 MOE_API moe_status moe_workspace_views(const moe_shape* shape, void* workspace, size_t workspace_bytes,
                                moe_views* views);
 
@@ -239,6 +251,50 @@ MOE_API moe_status moe_device_status(const void* workspace, size_t workspace_byt
                              int32_t* detail);
 
 /* Static text for a status code. */
+/* ---- FP8 expert weights (MXFP8) --------------------------------------
+ * Block-scaled FP8 ("CuTeDSL chez Perplexity", "Prise en charge de Blackwell":
+ * MXFP8, an absolute maximum over 32 elements): every 32 consecutive elements
+ * along the reduction dimension share a power-of-two scale X = 2^E (one E8M0
+ * byte, E + 127) with E = floor(log2(amax)) - 8 clamped to [-127, 127] (-127 for
+ * an all-zero block); each element is stored as the E4M3 code of x / X, rounded
+ * to nearest even and clamped to +-448.
+ * Codes keep the matrix layout (one byte per element).  Scales are stored for
+ * the block-scaled tensor-core MMA: per 128-row group and 128-element chunk of
+ * the reduction dimension a 512-byte tile, byte r*16 + 4*j + b holding the
+ * scale of row 32*j + r of the group and 32-element block b of the chunk.  For
+ * W13 the rows of a group are the gate/up GEMM's tile rows: group e*(I/64) + t
+ * holds features [64t, 64t+64) of expert e as, for g = 0..3, the 16 gate rows
+ * 64t+16g .. +15 then the 16 matching up rows.  W2 groups are 128 consecutive
+ * rows. */
+
+/* Byte sizes of the MXFP8 copies of W13 and W2 for this shape. */
+MOE_API moe_status moe_mx_weight_sizes(const moe_shape* shape, size_t* w13_codes, size_t* w13_scales,
+                                       size_t* w2_codes, size_t* w2_scales);
+
+/* Quantize the bf16 expert weights (layouts as for moe_forward) to MXFP8 on
+ * the device (asynchronous on `stream`).  All pointers device, 16-byte aligned,
+ * sized by moe_mx_weight_sizes. */
+MOE_API moe_status moe_mx_quantize_weights(const moe_shape* shape, const moe_bf16* w13, const moe_bf16* w2,
+                                           uint8_t* w13_codes, uint8_t* w13_scales, uint8_t* w2_codes,
+                                           uint8_t* w2_scales, moe_stream_t stream);
+
+/* Workspace bytes of moe_forward_mx (larger than moe_workspace_size's). */
+MOE_API moe_status moe_workspace_size_mx(const moe_shape* shape, size_t* bytes);
+
+/* The layer with MXFP8 expert weights: the same norm, router, top-k and
+ * combine as moe_forward; each expert's input rows (the bf16 h) and its bf16
+ * SwiGLU activations are quantized to MXFP8 the same way and the two expert
+ * GEMMs run on the block-scaled tensor cores (tcgen05.mma kind::mxf8f6f4,
+ * fp32 accumulation).  Expert lists are padded to 32 rows.  Decode shapes:
+ * T * top_k <= 64 * E and E <= 256 (else MOE_ERR_UNSUPPORTED).  events: NULL
+ * or as for moe_forward_events (events[1] ends routing and align, events[4]
+ * the gather + quantize, events[6] the activation quantize + down GEMM). */
+MOE_API moe_status moe_forward_mx(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                                  const float* w_router, const float* router_bias, const uint8_t* w13_codes,
+                                  const uint8_t* w13_scales, const uint8_t* w2_codes, const uint8_t* w2_scales,
+                                  moe_bf16* y, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                                  void* const* events, int32_t n_events);
+
 /* QK-norm, in place: RMSNorm of every attention head of Q and of K
  * ("CuTeDSL chez Perplexity", "Norme QK"):
  *   out_j = bf16((w_j + weight_bias) * (x_j * rstd)),  rstd = 1/sqrt(mean_j x_j^2 + eps),

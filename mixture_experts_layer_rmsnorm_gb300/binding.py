@@ -36,6 +36,11 @@ class MoeViews(ctypes.Structure):
                 ("P_max", ctypes.c_int64)]
 
 
+class MoeMxViews(ctypes.Structure):
+    _fields_ = [("x_codes", ctypes.c_void_p), ("x_scales", ctypes.c_void_p), ("act_codes", ctypes.c_void_p),
+                ("act_scales", ctypes.c_void_p)]
+
+
 class MoeError(RuntimeError):
     def __init__(self, status: int, where: str):
         super().__init__(f"{where}: {moe_status_string(status)} (status {status})")
@@ -67,13 +72,20 @@ def load(build: bool = True):
             lib.moe_kernels_per_call.argtypes = [sp, ctypes.POINTER(ctypes.c_int32)]
             lib.moe_selftest_wait_timeout.argtypes = [p, sz, i64, p]
             lib.moe_qk_norm.argtypes = [i64, i32, i32, i32, p, p, p, p, ctypes.c_float, ctypes.c_float, p]
+            psz = ctypes.POINTER(sz)
+            lib.moe_mx_weight_sizes.argtypes = [sp, psz, psz, psz, psz]
+            lib.moe_mx_quantize_weights.argtypes = [sp, p, p, p, p, p, p, p]
+            lib.moe_workspace_size_mx.argtypes = [sp, psz]
+            lib.moe_workspace_views_mx.argtypes = [sp, p, sz, ctypes.POINTER(MoeViews), ctypes.POINTER(MoeMxViews)]
+            lib.moe_forward_mx.argtypes = [sp, p, p, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_forward_fused_front.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_status_string.argtypes = [ctypes.c_int]
             lib.moe_status_string.restype = ctypes.c_char_p
             for f in ("moe_workspace_size", "moe_forward", "moe_forward_events", "moe_route_debug",
                       "moe_workspace_views", "moe_device_status", "moe_forward_static_scratch",
                       "moe_kernels_per_call", "moe_forward_fused_front", "moe_selftest_wait_timeout",
-                      "moe_qk_norm"):
+                      "moe_qk_norm", "moe_mx_weight_sizes", "moe_mx_quantize_weights", "moe_workspace_size_mx",
+                      "moe_workspace_views_mx", "moe_forward_mx"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -178,6 +190,39 @@ def moe_selftest_wait_timeout(workspace, workspace_bytes, timeout_ns, stream) ->
     return load().moe_selftest_wait_timeout(workspace, workspace_bytes, int(timeout_ns), stream)
 
 
+def moe_mx_weight_sizes(s: MoeShape) -> tuple[int, tuple[int, int, int, int]]:
+    v = [ctypes.c_size_t(0) for _ in range(4)]
+    st = load().moe_mx_weight_sizes(ctypes.byref(s), *[ctypes.byref(a) for a in v])
+    return st, tuple(a.value for a in v)
+
+
+def moe_mx_quantize_weights(s: MoeShape, w13, w2, w13_codes, w13_scales, w2_codes, w2_scales, stream) -> int:
+    return load().moe_mx_quantize_weights(ctypes.byref(s), w13, w2, w13_codes, w13_scales, w2_codes, w2_scales,
+                                          stream)
+
+
+def moe_workspace_size_mx(s: MoeShape) -> tuple[int, int]:
+    n = ctypes.c_size_t(0)
+    st = load().moe_workspace_size_mx(ctypes.byref(s), ctypes.byref(n))
+    return st, n.value
+
+
+def moe_workspace_views_mx(s: MoeShape, workspace, workspace_bytes) -> tuple[int, MoeViews, MoeMxViews]:
+    v, mv = MoeViews(), MoeMxViews()
+    st = load().moe_workspace_views_mx(ctypes.byref(s), workspace, workspace_bytes, ctypes.byref(v), ctypes.byref(mv))
+    return st, v, mv
+
+
+def moe_forward_mx(s: MoeShape, x, g_norm, w_router, router_bias, w13_codes, w13_scales, w2_codes, w2_scales, y,
+                   workspace, workspace_bytes, stream, events=None) -> int:
+    if events is None:
+        arr, n = None, 0
+    else:
+        arr, n = (ctypes.c_void_p * len(events))(*events), len(events)
+    return load().moe_forward_mx(ctypes.byref(s), x, g_norm, w_router, router_bias, w13_codes, w13_scales, w2_codes,
+                                 w2_scales, y, workspace, workspace_bytes, stream, arr, n)
+
+
 def _ptr(t):
     return None if t is None else t.data_ptr()
 
@@ -210,6 +255,9 @@ class MoeLayer:
         st, n = moe_workspace_size(self.shape(max(T, 1)))
         if st != MOE_OK:
             raise MoeError(st, "moe_workspace_size")
+        st, n_mx = moe_workspace_size_mx(self.shape(max(T, 1)))
+        if st == MOE_OK:
+            n = max(n, n_mx)  # room for the MXFP8 forward as well
         self.workspace = torch.empty(n, dtype=torch.uint8, device=self.device)
         self.max_tokens = max(T, 1)
 
@@ -240,6 +288,48 @@ class MoeLayer:
         if st != MOE_OK:
             raise MoeError(st, "moe_forward")
         return y
+
+    def quantize_mx(self, stream=None):
+        """Make the MXFP8 copies of W13 and W2 (moe_mx_quantize_weights) for forward_mx."""
+        import torch
+        st, (n13c, n13s, n2c, n2s) = moe_mx_weight_sizes(self.shape(1))
+        if st != MOE_OK:
+            raise MoeError(st, "moe_mx_weight_sizes")
+        u8 = dict(dtype=torch.uint8, device=self.device)
+        self.w13_codes, self.w13_scales = torch.empty(n13c, **u8), torch.empty(n13s, **u8)
+        self.w2_codes, self.w2_scales = torch.empty(n2c, **u8), torch.empty(n2s, **u8)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        st = moe_mx_quantize_weights(self.shape(1), _ptr(self.w13), _ptr(self.w2), _ptr(self.w13_codes),
+                                     _ptr(self.w13_scales), _ptr(self.w2_codes), _ptr(self.w2_scales), s)
+        if st != MOE_OK:
+            raise MoeError(st, "moe_mx_quantize_weights")
+
+    def workspace_bytes_mx(self, T) -> int:
+        st, n = moe_workspace_size_mx(self.shape(T))
+        if st != MOE_OK:
+            raise MoeError(st, "moe_workspace_size_mx")
+        return n
+
+    def forward_mx(self, x, y=None, stream=None, events=None):
+        """y = layer(x) with the MXFP8 expert weights (call quantize_mx first)."""
+        import torch
+        T = x.shape[0]
+        self.ensure_capacity(T)
+        if y is None:
+            y = torch.empty((T, self.H), dtype=x.dtype, device=x.device)
+        s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
+        st = moe_forward_mx(self.shape(T), _ptr(x), _ptr(self.g_norm), _ptr(self.w_router), _ptr(self.bias),
+                            _ptr(self.w13_codes), _ptr(self.w13_scales), _ptr(self.w2_codes), _ptr(self.w2_scales),
+                            _ptr(y), _ptr(self.workspace), self.workspace_bytes_mx(T), s, events)
+        if st != MOE_OK:
+            raise MoeError(st, "moe_forward_mx")
+        return y
+
+    def views_mx(self, T):
+        st, v, mv = moe_workspace_views_mx(self.shape(T), _ptr(self.workspace), self.workspace_bytes_mx(T))
+        if st != MOE_OK:
+            raise MoeError(st, "moe_workspace_views_mx")
+        return v, mv
 
     def views(self, T):
         st, v = moe_workspace_views(self.shape(T), _ptr(self.workspace), self.workspace_bytes(T))

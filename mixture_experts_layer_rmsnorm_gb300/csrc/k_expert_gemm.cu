@@ -74,13 +74,21 @@ constexpr int kTabMaxE = 256;
 constexpr int kABytes = kWeightBoxRows * kBlockK * 2;  // 16 KB weight tile per stage
 constexpr int kTokRowBytes = kBlockK * 2;              // 128 B per token row per stage
 
-template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false>
 struct GemmCfg {
   // a CTA pair splits the unit's tokens: each CTA holds half of the B tile
   static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * kTokRowBytes;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  // MXFP8: one byte per element, so a 128-byte row holds 128 elements of K;
+  // each stage also carries its scale tiles: 512 bytes for the 128 weight rows
+  // and 512 for the unit's token chunk
+  static constexpr int kKPerStage = MX ? 128 : kBlockK;
+  static constexpr int kSfBytes = MX ? 2 * 512 : 0;
+  static constexpr int kStageBytes = (kABytes + kBBytes + kSfBytes + 1023) / 1024 * 1024;
   static constexpr int kAccCols = BN;  // fp32 TMEM columns per accumulator buffer
-  static constexpr int kTmemNeed = 2 * kAccCols;
+  // TMEM columns of one stage's scales: weight scales at +0, token scales at
+  // +16 (4 columns each; slots of 32 keep both addresses 16-column aligned)
+  static constexpr int kSfCols = MX ? 32 : 0;
+  static constexpr int kTmemNeed = 2 * kAccCols + STAGES * kSfCols;
   static constexpr uint32_t kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                         : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kBarBytes = 512;
@@ -90,6 +98,7 @@ struct GemmCfg {
   static constexpr int kFeatPerTile = SWIGLU ? kGateUpTileFeat : kDownTileFeat;  // output features per unit
   static_assert(BN % TOKBOX == 0 && TOKBOX % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
   static_assert(!PAIR || (BN / 2) % TOKBOX == 0, "token boxes of a CTA pair");
+  static_assert(!(MX && PAIR) && (!MX || (BN % 32 == 0 && BN <= 128)), "MXFP8 units: one CTA, 32..128 tokens");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
   static_assert(kTmemNeed <= 512, "TMEM has 512 columns");
   static_assert((2 * STAGES + 5) * 8 + 8 <= kBarBytes, "barrier area");
@@ -171,11 +180,11 @@ __device__ __forceinline__ int64_t range_start(int64_t W, int cta, int ctas) { r
 
 __device__ __forceinline__ uint16_t f2bf(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
-template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const ExpertGemmArgs args) {
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
@@ -243,7 +252,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int total_units = t_unit[args.E];
-  const int kblocks = args.K / kBlockK;
+  const int kblocks = args.K / C::kKPerStage;
   const int ctas = workers;
 
   if (warp == 0) {
@@ -267,7 +276,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // rows after pdl_wait.
       bool deps_ready = false;
       int n_pend = 0;
-      int pend_stage[STAGES], pend_kb[STAGES], pend_tok0[STAGES], pend_rows[STAGES];
+      int pend_stage[STAGES], pend_kb[STAGES], pend_tok0[STAGES], pend_rows[STAGES], pend_chunk[STAGES];
       // a CTA pair signals every load on the even CTA's full barrier
       const uint32_t full_cl = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;
       auto load_2d = [&](void* dst, const CUtensorMap* map, int st, int c0, int c1, uint64_t pol) {
@@ -279,19 +288,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // gate/up A tile: box {64 K, 16 rows, gate+up, 4 groups, 1 expert}
       auto load_gate_up = [&](void* dst, int st, int kb, int tile, int e, uint64_t pol) {
         if (PAIR)
-          tma_load_5d_pair(dst, &tm_w, full_cl + 8u * st, kb * kBlockK, 0, 0, tile * 4, e, pol);
+          tma_load_5d_pair(dst, &tm_w, full_cl + 8u * st, kb * C::kKPerStage, 0, 0, tile * 4, e, pol);
         else
-          tma_load_5d(dst, &tm_w, &full[st], kb * kBlockK, 0, 0, tile * 4, e, pol);
+          tma_load_5d(dst, &tm_w, &full[st], kb * C::kKPerStage, 0, 0, tile * 4, e, pol);
       };
-      auto load_tokens = [&](int st, int kb, int tok0, int rows) {
+      // chunk: the unit's token chunk (MXFP8 token scales are stored per chunk)
+      auto load_tokens = [&](int st, int kb, int tok0, int rows, int chunk) {
         uint8_t* sb = smem + st * C::kStageBytes + kABytes;
-        for (int r = 0; r < rows; r += TOKBOX) load_2d(sb + r * kTokRowBytes, &tm_x, st, kb * kBlockK, tok0 + r, pol_x);
+        for (int r = 0; r < rows; r += TOKBOX)
+          load_2d(sb + r * kTokRowBytes, &tm_x, st, kb * C::kKPerStage, tok0 + r, pol_x);
+        if (MX)
+          bulk_load(sb + C::kBBytes + 512, args.x_scales + (static_cast<size_t>(chunk) * kblocks + kb) * 512, 512,
+                    &full[st], pol_x);
       };
       auto resolve_deps = [&]() {
         pdl_wait();
         pdl_launch_dependents();
         deps_ready = true;
-        for (int i = 0; i < n_pend; ++i) load_tokens(pend_stage[i], pend_kb[i], pend_tok0[i], pend_rows[i]);
+        for (int i = 0; i < n_pend; ++i)
+          load_tokens(pend_stage[i], pend_kb[i], pend_tok0[i], pend_rows[i], pend_chunk[i]);
         n_pend = 0;
       };
       Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
@@ -308,7 +323,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int tok_rows = (half + TOKBOX - 1) / TOKBOX * TOKBOX;  // whole boxes; rows past n are unused
         const bool reused = t_off[un.e + 1] - t_off[un.e] > BN;
         const uint64_t pol_w = reused ? pol_keep : pol_stream;
-        const uint32_t bytes = kABytes + tok_rows * kTokRowBytes;  // per CTA (the same in both of a pair)
+        const uint32_t bytes = kABytes + tok_rows * kTokRowBytes + C::kSfBytes;  // per CTA (the same in both of a pair)
+        const int chunk = MX ? t_unit[un.e] / args.tiles_per_expert + (un.tok0 - t_off[un.e]) / BN : 0;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitTimeoutNs, abort_flag)) {
             ok = false;
@@ -322,15 +338,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (SWIGLU) {  // 16 gate rows, the matching 16 up rows, x 4
             load_gate_up(sa, stage, kb, tile, un.e, pol_w);
           } else {
-            load_2d(sa, &tm_w, stage, kb * kBlockK, wrow, pol_w);
+            load_2d(sa, &tm_w, stage, kb * C::kKPerStage, wrow, pol_w);
           }
+          if (MX)  // the weight tile's scales (static: loaded before the parent kernel ends)
+            bulk_load(sa + kABytes + C::kBBytes,
+                      args.w_scales + (static_cast<size_t>(un.e * args.tiles_per_expert + tile) * kblocks + kb) * 512,
+                      512, &full[stage], pol_w);
           if (deps_ready) {
-            load_tokens(stage, kb, tok_first, tok_rows);
+            load_tokens(stage, kb, tok_first, tok_rows, chunk);
           } else {
             pend_stage[n_pend] = stage;
             pend_kb[n_pend] = kb;
             pend_tok0[n_pend] = tok_first;
             pend_rows[n_pend] = tok_rows;
+            pend_chunk[n_pend] = chunk;
             if (++n_pend == STAGES) resolve_deps();
           }
           ++issued;
@@ -382,13 +403,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
           const uint32_t sb = sa + kABytes;
+          if (MX) {
+            // this stage's scales into its TMEM columns, then 4 MMAs of K = 32
+            const uint32_t sf_t = tmem_base + static_cast<uint32_t>(2 * C::kAccCols + stage * C::kSfCols);
+            const uint32_t sf_s = sb + C::kBBytes;
+            tmem_cp_32x128b_x4(sf_t, sf_s);
+            tmem_cp_32x128b_x4(sf_t + 16, sf_s + 512);
+            const uint32_t sfb_t = sf_t + 16;
 #pragma unroll
-          for (int k = 0; k < kBlockK / 16; ++k) {
-            const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;  // each segment starts a fresh sum
-            if (PAIR)
-              mma_bf16_ss_pair(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc, accum);
-            else
-              mma_bf16_ss(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc, accum);
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+              mma_mxf8_ss(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32),
+                          idesc_mxf8(128, static_cast<uint32_t>(n_mma), k, k), sf_t, sfb_t, accum);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < kBlockK / 16; ++k) {
+              const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;  // each segment starts a fresh sum
+              if (PAIR)
+                mma_bf16_ss_pair(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc,
+                                 accum);
+              else
+                mma_bf16_ss(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), idesc, accum);
+            }
           }
           if (PAIR)
             mma_commit_pair_mc(&empty[stage], 0x3);  // frees the stage in both CTAs
@@ -537,11 +574,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false>
 cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, int num_sms,
                                cudaStream_t stream) {
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR>;
-  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>;
+  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>;
   static int configured_device = -1;
   static int max_pairs = 0;  // CTA pairs that fit on the configured device at once
   int dev = 0;
@@ -599,7 +636,38 @@ constexpr int kPairStages[2] = {7, 7};  // gate/up, down: stages of 32 KB
 // nothing); large units hold up to 256 (128-row boxes: 8x fewer TMA requests)
 constexpr int kTokBox[3] = {16, 16, 128};
 
+// MXFP8 decode plans: 32-token units, 10 stages of 22 KB; 64-token units, 8 of 26 KB
+constexpr int kMxStages[2] = {10, 8};
+
 }  // namespace
+
+cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
+                                   GemmPlan plan, int num_sms, cudaStream_t stream) {
+  switch (plan) {
+    case GemmPlan::kSmall:
+      return launch_expert_gemm<true, kGateUpBn[0], kMxStages[0], kTokBox[0], false, true>(tm_w13, tm_x, a, num_sms,
+                                                                                            stream);
+    case GemmPlan::kMid:
+      return launch_expert_gemm<true, kGateUpBn[1], kMxStages[1], kTokBox[1], false, true>(tm_w13, tm_x, a, num_sms,
+                                                                                            stream);
+    default:
+      return cudaErrorNotSupported;
+  }
+}
+
+cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const ExpertGemmArgs& a,
+                                GemmPlan plan, int num_sms, cudaStream_t stream) {
+  switch (plan) {
+    case GemmPlan::kSmall:
+      return launch_expert_gemm<false, kDownBn[0], kMxStages[0], kTokBox[0], false, true>(tm_w2, tm_act, a, num_sms,
+                                                                                           stream);
+    case GemmPlan::kMid:
+      return launch_expert_gemm<false, kDownBn[1], kMxStages[1], kTokBox[1], false, true>(tm_w2, tm_act, a, num_sms,
+                                                                                           stream);
+    default:
+      return cudaErrorNotSupported;
+  }
+}
 
 int gemm_gate_up_bn(GemmPlan plan) { return kGateUpBn[static_cast<int>(plan)]; }
 int gemm_down_bn(GemmPlan plan) { return kDownBn[static_cast<int>(plan)]; }

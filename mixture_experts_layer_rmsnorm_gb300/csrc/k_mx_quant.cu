@@ -1,0 +1,166 @@
+// k_mx_quant.cu -- MXFP8 quantization: bf16 rows -> E4M3 codes + E8M0 scales.
+//
+// Block scaling over 32 consecutive elements ("CuTeDSL chez Perplexity",
+// "Prise en charge de Blackwell": MXFP8 with an absolute maximum over 32
+// elements).  Recipe (the OCP Microscaling rule; the pages give none): for a
+// block with absolute maximum amax, X = 2^E with E = floor(log2(amax)) - 8
+// (8 = the largest E4M3 exponent), clamped to [-127, 127], E = -127 for an
+// all-zero block; each element is stored as the E4M3 code of x / X, rounded
+// to nearest even and clamped to +-448 (cvt.rn.satfinite); the scale byte is
+// E + 127.
+//
+// Codes keep the rows' layout ([rows, K], one byte per element).  Scales are
+// stored for the tensor cores' block-scaled MMA: per 128-row group and per
+// 128-element chunk of K, one 512-byte tile of 32 rows x 16 bytes in which
+// byte r*16 + 4*j + b is the scale of row 32*j + r of the group and K-block b
+// of the chunk -- the layout tcgen05.cp .32x128b.warpx4 copies into TMEM so
+// that the MMA finds row m's scale in lane m, column m/32, byte b.
+// Scale row of a matrix row: W13 rows are reordered into the gate/up GEMM's
+// tile rows (64 features per tile: 16 gate rows, the matching 16 up rows, x 4);
+// W2 keeps its row index.  Token rows (gathered inputs, activations) are
+// grouped by the expert GEMMs' token chunks instead: the rows
+// [offsets[e] + c*bn, +bn) of expert e form chunk unit_off[e] / tiles + c, and
+// its scales one 512-byte tile per 128 elements of K with byte r*16 + 4*j + b
+// for row offsets[e] + c*bn + 32*j + r (bn <= 128, offsets multiples of 32), so
+// that a unit's token scales start at TMEM column 0.
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "moe_kernels.cuh"
+#include "pdl.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kQuantWarps = 8;
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// two E4M3 codes (round to nearest even, saturating): lo in bits 0-7, hi in 8-15
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// byte offset of the scale of (scale row R, K-block kb) for K elements per row
+__device__ __forceinline__ size_t scale_offset(int64_t R, int kb, int K) {
+  const int64_t g = R >> 7;
+  const int rr = static_cast<int>(R & 127);
+  return (static_cast<size_t>(g) * (K / 128) + kb / 4) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (kb & 3);
+}
+
+// Token row p (< offsets[E]) -> chunk-relative scale position: the "scale row"
+// chunk * 128 + 32 * j + r, so that scale_offset() lands in the chunk's tile.
+__device__ __forceinline__ int64_t token_scale_row(int p, const int32_t* offsets, const int32_t* unit_off, int E,
+                                                   int tiles, int bn) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldcg(offsets + mid) <= p)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int within = p - __ldcg(offsets + lo);
+  const int c = within / bn, in_chunk = within - c * bn;
+  const int64_t chunk = __ldcg(unit_off + lo) / tiles + c;
+  return chunk * 128 + in_chunk;  // in_chunk = 32 * j + r
+}
+
+// One warp per row.  MODE 0: rows of a matrix (W2); MODE 1: gathered token
+// rows (row p <- h[sorted_ids[p] / k], zeros for padding rows), rows below
+// offsets[E] only, chunk-grouped scales; MODE 2: rows of W13, scales in gate/up
+// tile-row order; MODE 3: activation rows below offsets[E], chunk-grouped scales.
+template <int MODE>
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    mx_quantize_kernel(const uint16_t* __restrict__ src, int64_t rows, int K, const int32_t* __restrict__ sorted_ids,
+                       const int32_t* __restrict__ offsets, const int32_t* __restrict__ unit_off, int tiles, int bn,
+                       int E, int N, int k, int I, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  pdl_wait();  // the rows (and routing tables) may come from the previous kernel
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  if ((MODE == 1 || MODE == 3) && row >= __ldcg(offsets + E)) return;
+  const uint16_t* s = nullptr;
+  int64_t R = row;  // scale row
+  if (MODE == 1 || MODE == 3) R = token_scale_row(static_cast<int>(row), offsets, unit_off, E, tiles, bn);
+  if (MODE == 1) {
+    const int id = __ldcg(sorted_ids + row);
+    if (id >= 0 && id < N) s = src + static_cast<int64_t>(id / k) * K;
+  } else {
+    s = src + row * K;
+    if (MODE == 2) {
+      const int64_t e = row / (2 * I);
+      const int i = static_cast<int>(row - e * 2 * I);
+      const int up = i >= I, f = up ? i - I : i;
+      const int m = 32 * ((f & 63) >> 4) + 16 * up + (f & 15);
+      R = (e * (I / 64) + (f >> 6)) * 128 + m;
+    }
+  }
+  const int nch = K >> 3;  // 8-element chunks; a 32-block is 4 neighbouring lanes
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    const int c = c0 + lane;
+    const bool on = c < nch;  // whole 4-lane groups are on or off (nch is a multiple of 4)
+    float x[8];
+    unpack8(on && s ? *reinterpret_cast<const uint4*>(s + c * 8) : make_uint4(0, 0, 0, 0), x);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    int ex = amax > 0.0f ? ilogbf(amax) - 8 : -127;
+    ex = ex < -127 ? -127 : (ex > 127 ? 127 : ex);
+    const float inv = ldexpf(1.0f, -ex);  // exact power of two
+    uint32_t w0 = e4m3x2(x[0] * inv, x[1] * inv) | (e4m3x2(x[2] * inv, x[3] * inv) << 16);
+    uint32_t w1 = e4m3x2(x[4] * inv, x[5] * inv) | (e4m3x2(x[6] * inv, x[7] * inv) << 16);
+    if (on) {
+      *reinterpret_cast<uint2*>(codes + row * K + c * 8) = make_uint2(w0, w1);
+      if ((lane & 3) == 0) scales[scale_offset(R, c >> 2, K)] = static_cast<uint8_t>(ex + 127);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_mx_quantize_rows(const uint16_t* src, int64_t rows, int K, uint8_t* codes, uint8_t* scales,
+                                    cudaStream_t stream) {
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  return launch_pdl(mx_quantize_kernel<0>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0, stream,
+                    src, rows, K, nullptr, nullptr, nullptr, 1, 32, 0, 0, 1, 0, codes, scales);
+}
+
+cudaError_t launch_mx_quantize_act(const uint16_t* act, int64_t rows, int K, const int32_t* offsets,
+                                   const int32_t* unit_off, int tiles, int bn, int E, uint8_t* codes, uint8_t* scales,
+                                   cudaStream_t stream) {
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  return launch_pdl(mx_quantize_kernel<3>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0, stream,
+                    act, rows, K, nullptr, offsets, unit_off, tiles, bn, E, 0, 1, 0, codes, scales);
+}
+
+cudaError_t launch_mx_quantize_w13(const uint16_t* w13, int E, int H, int I, uint8_t* codes, uint8_t* scales,
+                                   cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(E) * 2 * I;
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  return launch_pdl(mx_quantize_kernel<2>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0, stream,
+                    w13, rows, H, nullptr, nullptr, nullptr, 1, 32, 0, 0, 1, I, codes, scales);
+}
+
+cudaError_t launch_mx_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets,
+                             const int32_t* unit_off, int tiles, int bn, int E, int N, int k, int H, int64_t rows,
+                             uint8_t* codes, uint8_t* scales, cudaStream_t stream) {
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  return launch_pdl(mx_quantize_kernel<1>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0, stream,
+                    h, rows, H, sorted_ids, offsets, unit_off, tiles, bn, E, N, k, 0, codes, scales);
+}
+
+}  // namespace moe

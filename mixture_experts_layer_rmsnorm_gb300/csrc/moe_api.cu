@@ -31,8 +31,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
   size_t err, h, logits, ids, w, counts, offsets, unit1, unit2, sorted, slot, flags, blk_counts, blk_base, partials, xg,
-      act, out, total;
-  int64_t P_max;       // padded rows with 16-row padding
+      act, out, xs, aq, as, total;
+  int64_t P_max;       // padded rows: 16-row padding (bf16), 32-row padding rounded to 128 (MXFP8)
   int64_t sorted_cap;  // sorted_ids entries (room for debug padding up to 256)
 };
 
@@ -44,10 +44,12 @@ size_t partial_slots_bytes(const moe_shape& s) {
   return static_cast<size_t>(moe::kMaxGemmCtas) * moe::gemm_gate_up_bn(moe::choose_plan(s.T, s.top_k, s.E)) * 128 * 4;
 }
 
-Layout make_layout(const moe_shape& s) {
+// mx: the MXFP8 layer (token rows padded to 32 per expert; xg holds E4M3
+// codes, plus token and activation scales and activation codes).
+Layout make_layout(const moe_shape& s, bool mx = false) {
   Layout L{};
   const int64_t T = s.T, H = s.H, I = s.I, E = s.E, k = s.top_k;
-  L.P_max = T * k + E * (moe::kPadRows - 1);
+  L.P_max = mx ? (T * k + E * (moe::kPadRowsMx - 1) + 127) / 128 * 128 : T * k + E * (moe::kPadRows - 1);
   L.sorted_cap = T * k + E * (kMaxDebugPad - 1);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -75,6 +77,11 @@ Layout make_layout(const moe_shape& s) {
   L.xg = take(static_cast<size_t>(L.P_max * H * 2));
   L.act = take(static_cast<size_t>(L.P_max * I * 2));
   L.out = take(static_cast<size_t>(L.P_max * H * 2));
+  if (mx) {  // token scales per token chunk: at most P_max / 32 chunks (each >= 32 rows)
+    L.xs = take(static_cast<size_t>(L.P_max / 32) * (H / 128) * 512);
+    L.aq = take(static_cast<size_t>(L.P_max * I));
+    L.as = take(static_cast<size_t>(L.P_max / 32) * (I / 128) * 512);
+  }
   L.total = off;
   return L;
 }
@@ -137,6 +144,32 @@ bool make_map_gate_up(CUtensorMap* m, const void* w13, uint64_t H, uint64_t I, u
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// E4M3 codes [rows, inner] (one byte per element), boxes of 128 x box_rows.
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// W13 codes viewed as [E][2][I/16][16][H] like the bf16 map: boxes of 128 x 16 x 2 x 4 x 1.
+bool make_map_gate_up_u8(CUtensorMap* m, const void* w13c, uint64_t H, uint64_t I, uint64_t E) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[5] = {H, 16, 2, I / 16, E};
+  cuuint64_t strides[4] = {H, I * H, 16 * H, 2 * I * H};
+  cuuint32_t box[5] = {128, 16, 2, moe::kGateUpTileFeat / 16, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(w13c), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int num_sms_of_current_device() {
   static int cache[64] = {0};
   int dev = 0;
@@ -156,11 +189,11 @@ T* at(void* ws, size_t off) {
 }
 
 moe_status check_inputs(const moe_shape* s, const void* x, const void* g, const float* wr, const float* bias,
-                        void* ws, size_t ws_bytes) {
+                        void* ws, size_t ws_bytes, bool mx = false) {
   if (!x || !g || !wr || !ws) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(g, 16) || !aligned(wr, 16) || (bias && !aligned(bias, 4)) || !aligned(ws, kAlign))
     return MOE_ERR_INVALID_ARG;
-  if (ws_bytes < make_layout(*s).total) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < make_layout(*s, mx).total) return MOE_ERR_WORKSPACE;
   return MOE_OK;
 }
 
@@ -392,9 +425,175 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   return MOE_OK;
 }
 
+// The MXFP8 layer: the bf16 layer's routing, then MXFP8 token rows and
+// weights in block-scaled tcgen05 GEMMs (decode tile plans).
+moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
+                           const float* router_bias, const uint8_t* w13c, const uint8_t* w13s, const uint8_t* w2c,
+                           const uint8_t* w2s, moe_bf16* y, void* workspace, size_t workspace_bytes,
+                           moe_stream_t stream, void* const* events) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  const moe_shape& s = *shape;
+  if (s.T == 0) return MOE_OK;
+  const GemmPlan plan = moe::choose_plan(s.T, s.top_k, s.E);
+  if (plan == GemmPlan::kLarge || s.E > 256) return MOE_ERR_UNSUPPORTED;
+  st = check_inputs(shape, x, g_norm, w_router, router_bias, workspace, workspace_bytes, true);
+  if (st != MOE_OK) return st;
+  if (!w13c || !w13s || !w2c || !w2s || !y || !aligned(w13c, 16) || !aligned(w13s, 16) || !aligned(w2c, 16) ||
+      !aligned(w2s, 16) || !aligned(y, 16))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int num_sms = num_sms_of_current_device();
+  if (num_sms <= 0) return MOE_ERR_CUDA;
+  const Layout L = make_layout(s, true);
+  const int bn1 = moe::gemm_gate_up_bn(plan), bn2 = moe::gemm_down_bn(plan);
+  const int tiles1 = s.I / moe::kGateUpTileFeat, tiles2 = s.H / moe::kDownTileFeat;
+  auto mark = [&](int i) {
+    return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), cs) == cudaSuccess;
+  };
+  CUtensorMap tm_w13, tm_xq, tm_w2, tm_aq;
+  if (!make_map_gate_up_u8(&tm_w13, w13c, s.H, s.I, s.E) ||
+      !make_map_u8(&tm_xq, at<void>(workspace, L.xg), s.H, L.P_max, moe::gemm_tok_box_rows(plan)) ||
+      !make_map_u8(&tm_w2, w2c, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows) ||
+      !make_map_u8(&tm_aq, at<void>(workspace, L.aq), s.I, L.P_max, moe::gemm_tok_box_rows(plan)))
+    return MOE_ERR_CUDA;
+  int32_t* err = at<int32_t>(workspace, L.err);
+  if (!mark(0)) return MOE_ERR_CUDA;
+  st = run_front(s, L, x, g_norm, w_router, router_bias, moe::kPadRowsMx, bn1, bn2, workspace, cs, num_sms);
+  if (st != MOE_OK) return st;
+  if (!mark(1) || !mark(2) || !mark(3)) return MOE_ERR_CUDA;
+  const int N = s.T * s.top_k;
+  if (moe::launch_mx_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
+                            at<int32_t>(workspace, L.offsets), at<int32_t>(workspace, L.unit1), tiles1, bn1, s.E, N,
+                            s.top_k, s.H, L.P_max, at<uint8_t>(workspace, L.xg), at<uint8_t>(workspace, L.xs),
+                            cs) != cudaSuccess ||
+      !mark(4))
+    return MOE_ERR_CUDA;
+
+  moe::ExpertGemmArgs a1{};
+  a1.offsets = at<int32_t>(workspace, L.offsets);
+  a1.unit_off = at<int32_t>(workspace, L.unit1);
+  a1.E = s.E;
+  a1.K = s.H;
+  a1.tiles_per_expert = tiles1;
+  a1.w_rows_per_expert = 2 * s.I;
+  a1.n_out = s.I;
+  a1.out = at<uint16_t>(workspace, L.act);
+  a1.err = err;
+  a1.partials = at<float>(workspace, L.partials);
+  a1.flags = at<int32_t>(workspace, L.flags);
+  a1.stream_k = plan == GemmPlan::kSmall;
+  a1.w_scales = w13s;
+  a1.x_scales = at<uint8_t>(workspace, L.xs);
+  if (moe::launch_gemm_gate_up_mx(tm_w13, tm_xq, a1, plan, num_sms, cs) != cudaSuccess || !mark(5))
+    return MOE_ERR_CUDA;
+  // the activations (bf16) -> MXFP8, rows below offsets[E]
+  if (moe::launch_mx_quantize_act(at<uint16_t>(workspace, L.act), L.P_max, s.I, at<int32_t>(workspace, L.offsets),
+                                  at<int32_t>(workspace, L.unit1), tiles1, bn1, s.E, at<uint8_t>(workspace, L.aq),
+                                  at<uint8_t>(workspace, L.as), cs) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe::ExpertGemmArgs a2{};
+  a2.offsets = at<int32_t>(workspace, L.offsets);
+  a2.unit_off = at<int32_t>(workspace, L.unit2);
+  a2.E = s.E;
+  a2.K = s.I;
+  a2.tiles_per_expert = tiles2;
+  a2.w_rows_per_expert = s.H;
+  a2.n_out = s.H;
+  a2.out = at<uint16_t>(workspace, L.out);
+  a2.err = err;
+  a2.partials = at<float>(workspace, L.partials + partial_slots_bytes(s));
+  a2.flags = at<int32_t>(workspace, L.flags) + moe::kMaxGemmCtas * 4;
+  a2.stream_k = plan == GemmPlan::kSmall;
+  a2.w_scales = w2s;
+  a2.x_scales = at<uint8_t>(workspace, L.as);
+  if (moe::launch_gemm_down_mx(tm_w2, tm_aq, a2, plan, num_sms, cs) != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
+  if (moe::launch_combine(at<uint16_t>(workspace, L.out), at<int32_t>(workspace, L.slot), at<float>(workspace, L.w),
+                          s.T, s.H, s.top_k, y, cs) != cudaSuccess ||
+      !mark(7))
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 }  // namespace moe
 
 extern "C" {
+
+moe_status moe_mx_weight_sizes(const moe_shape* shape, size_t* w13_codes, size_t* w13_scales, size_t* w2_codes,
+                               size_t* w2_scales) {
+  const moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!w13_codes || !w13_scales || !w2_codes || !w2_scales) return MOE_ERR_INVALID_ARG;
+  const int64_t E = shape->E, H = shape->H, I = shape->I;
+  *w13_codes = static_cast<size_t>(E * 2 * I * H);
+  *w13_scales = moe::mx_scale_bytes(E * 2 * I, H);
+  *w2_codes = static_cast<size_t>(E * H * I);
+  *w2_scales = moe::mx_scale_bytes(E * H, I);
+  return MOE_OK;
+}
+
+moe_status moe_mx_quantize_weights(const moe_shape* shape, const moe_bf16* w13, const moe_bf16* w2, uint8_t* w13_codes,
+                                   uint8_t* w13_scales, uint8_t* w2_codes, uint8_t* w2_scales, moe_stream_t stream) {
+  const moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!w13 || !w2 || !w13_codes || !w13_scales || !w2_codes || !w2_scales || !aligned(w13, 16) || !aligned(w2, 16) ||
+      !aligned(w13_codes, 16) || !aligned(w13_scales, 16) || !aligned(w2_codes, 16) || !aligned(w2_scales, 16))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const moe_shape& s = *shape;
+  if (moe::launch_mx_quantize_w13(w13, s.E, s.H, s.I, w13_codes, w13_scales, cs) != cudaSuccess ||
+      moe::launch_mx_quantize_rows(w2, static_cast<int64_t>(s.E) * s.H, s.I, w2_codes, w2_scales, cs) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_size_mx(const moe_shape* shape, size_t* bytes) {
+  const moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(*shape, true).total;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_views_mx(const moe_shape* shape, void* workspace, size_t workspace_bytes, moe_views* v,
+                                  moe_mx_views* mv) {
+  const moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!workspace || !v || !mv) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*shape, true);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  v->error_word = at<void>(workspace, L.err);
+  v->h = at<void>(workspace, L.h);
+  v->logits = at<void>(workspace, L.logits);
+  v->topk_ids = at<void>(workspace, L.ids);
+  v->topk_w = at<void>(workspace, L.w);
+  v->counts = at<void>(workspace, L.counts);
+  v->offsets = at<void>(workspace, L.offsets);
+  v->sorted_ids = at<void>(workspace, L.sorted);
+  v->slot_of = at<void>(workspace, L.slot);
+  v->xg = at<void>(workspace, L.xg);
+  v->act = at<void>(workspace, L.act);
+  v->out_rows = at<void>(workspace, L.out);
+  v->P_max = L.P_max;
+  mv->x_codes = at<void>(workspace, L.xg);
+  mv->x_scales = at<void>(workspace, L.xs);
+  mv->act_codes = at<void>(workspace, L.aq);
+  mv->act_scales = at<void>(workspace, L.as);
+  return MOE_OK;
+}
+
+moe_status moe_forward_mx(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
+                          const float* router_bias, const uint8_t* w13_codes, const uint8_t* w13_scales,
+                          const uint8_t* w2_codes, const uint8_t* w2_scales, moe_bf16* y, void* workspace,
+                          size_t workspace_bytes, moe_stream_t stream, void* const* events, int32_t n_events) {
+  if (events) {
+    if (n_events < MOE_NUM_KERNELS + 1) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i <= MOE_NUM_KERNELS; ++i)
+      if (!events[i]) return MOE_ERR_INVALID_ARG;
+  }
+  return moe::forward_mx_impl(shape, x, g_norm, w_router, router_bias, w13_codes, w13_scales, w2_codes, w2_scales, y,
+                              workspace, workspace_bytes, stream, events);
+}
 
 moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
                        const float* router_bias, const moe_bf16* w13, const moe_bf16* w2, moe_bf16* y,

@@ -108,6 +108,8 @@ struct ExpertGemmArgs {
   int stream_k;             // 1: equal K-block ranges per CTA; 0: whole units round-robin
   int pair;                 // 1: CTA pairs, a unit = weight tiles 2t and 2t+1 (large plan only)
   int tables_from_parent;   // 1: the routing tables come from the previous kernel (wait before reading)
+  const uint8_t* w_scales;  // MXFP8 GEMMs: weight scales (512-byte tiles per 128 rows x 128 of K)
+  const uint8_t* x_scales;  // MXFP8 GEMMs: token scales, one 512-byte tile per token chunk and 128 of K
 };
 // persistent GEMM grid: min(SM count, kMaxGemmCtas) CTAs
 constexpr int kMaxGemmCtas = 256;
@@ -130,6 +132,16 @@ cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act
 // the tiles per expert its work-unit table counts (pairs of tiles then).
 bool gemm_uses_pairs(GemmPlan plan, int tiles);
 int gemm_unit_tiles(GemmPlan plan, int tiles);
+// The same GEMMs on MXFP8 operands (block-scaled tcgen05 MMA; decode tile
+// plans only: kSmall or kMid).  tm_w / tm_x map E4M3 codes (one byte per
+// element); a.w_scales / a.x_scales hold the E8M0 scales.
+cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
+                                   GemmPlan plan, int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const ExpertGemmArgs& a,
+                                GemmPlan plan, int num_sms, cudaStream_t stream);
+// rows of padding granularity of each expert's list for the MXFP8 GEMMs (a
+// token scale group is 32 rows)
+constexpr int kPadRowsMx = 32;
 // token rows per unit (B-operand width) and rows per TMA box of the token tile
 int gemm_gate_up_bn(GemmPlan plan);
 int gemm_down_bn(GemmPlan plan);
@@ -158,6 +170,23 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+
+// MXFP8 quantization (k_mx_quant.cu): E4M3 codes [rows, K] in the rows'
+// layout, E8M0 scales in the block-scaled MMA's tile layout (512 bytes per
+// 128-row group and 128-element chunk of K).  K and rows: multiples of 128.
+cudaError_t launch_mx_quantize_rows(const uint16_t* src, int64_t rows, int K, uint8_t* codes, uint8_t* scales,
+                                    cudaStream_t stream);
+cudaError_t launch_mx_quantize_w13(const uint16_t* w13, int E, int H, int I, uint8_t* codes, uint8_t* scales,
+                                   cudaStream_t stream);
+// token rows (gathered inputs / activations below offsets[E]): scales grouped
+// by the GEMMs' token chunks (bn rows of an expert, chunk unit_off[e]/tiles + c)
+cudaError_t launch_mx_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets,
+                             const int32_t* unit_off, int tiles, int bn, int E, int N, int k, int H, int64_t rows,
+                             uint8_t* codes, uint8_t* scales, cudaStream_t stream);
+cudaError_t launch_mx_quantize_act(const uint16_t* act, int64_t rows, int K, const int32_t* offsets,
+                                   const int32_t* unit_off, int tiles, int bn, int E, uint8_t* codes, uint8_t* scales,
+                                   cudaStream_t stream);
+inline size_t mx_scale_bytes(int64_t rows, int64_t K) { return static_cast<size_t>(rows / 128) * (K / 128) * 512; }
 
 // QK-norm of q[T, Hq, D] and k[T, Hk, D] in place (k_qk_norm.cu); D = 64, 128 or 256.
 cudaError_t launch_qk_norm(uint16_t* q, uint16_t* k, const uint16_t* q_weight, const uint16_t* k_weight, int64_t T,

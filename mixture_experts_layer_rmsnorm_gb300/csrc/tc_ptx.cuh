@@ -187,6 +187,17 @@ __device__ __forceinline__ void tma_load_5d_pair(void* smem_dst, const CUtensorM
       : "memory");
 }
 
+// Bulk (non-tensor) copy of `bytes` (a multiple of 16; 16-byte aligned
+// addresses) from global memory into this CTA's shared memory, counted on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 // Allocate `ncols` TMEM columns (power of two >= 32); the base address is
@@ -271,6 +282,34 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
                : "memory");
 }
 
+// Block-scaled MMA on MXFP8 operands (E4M3 codes, one E8M0 scale per 32
+// elements of K; K = 32 per instruction).  Row m of A takes its scale from
+// TMEM lane m, column sfa + m/32, byte sf_a_id (instruction descriptor); column
+// n of B from column sfb + n/32, lane (m's lane quarter) * 32 + n % 32, byte
+// sf_b_id -- the layout tcgen05.cp .32x128b.warpx4 leaves (measured on GB300).
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::
+          "r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy a 32-row x 16-byte tile (rows 16 bytes apart) from shared memory to
+// TMEM columns [taddr, taddr + 4), the same 32 rows in each lane quarter.
+// One thread; ordered before the tcgen05.mma this thread issues next.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16 >> 4) << 16;   // leading byte offset (one 16-byte column)
+  d |= static_cast<uint64_t>(128 >> 4) << 32;  // stride byte offset: 8-row groups 128 bytes apart
+  d |= static_cast<uint64_t>(1) << 46;         // fixed 0b001; no swizzle
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -312,6 +351,14 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: A and B E4M3
+// (format 0), K-major, UE8M0 scales (bit 23); scale bytes sf_a / sf_b in bits
+// 29-30 / 4-5; N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ __forceinline__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32_t sf_a,
+                                                                  uint32_t sf_b) {
+  return (sf_b << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sf_a << 29);
 }
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, dense.

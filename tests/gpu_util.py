@@ -70,7 +70,7 @@ class DeviceLayer:
         return a[idx].cpu().numpy().view(np.uint16), o[idx].cpu().numpy().view(np.uint16)
 
 
-def check_routing(o, li: inputs.LayerInputs, x: np.ndarray, g: dict):
+def check_routing(o, li: inputs.LayerInputs, x: np.ndarray, g: dict, pad: int = PAD):
     """Bit-exact checks of h, logits, expert ids and the align outputs; the
     routing weights within fp32 rounding of the oracle's fp64 softmax."""
     c = li.cfg
@@ -82,7 +82,7 @@ def check_routing(o, li: inputs.LayerInputs, x: np.ndarray, g: dict):
     l64 = o.router_logits_f64(h32, li.w_router, li.bias)
     w_ref = o.route_weights_f64(l64, ids, c.renormalize)
     assert np.allclose(g["w"], w_ref, rtol=2e-5, atol=1e-7), f"weights: max err {np.abs(g['w'] - w_ref).max()}"
-    counts, offsets, sorted_ids, slot_of = o.align(ids, c.E, PAD)
+    counts, offsets, sorted_ids, slot_of = o.align(ids, c.E, pad)
     assert np.array_equal(g["counts"], counts)
     assert np.array_equal(g["offsets"], offsets)
     assert np.array_equal(g["sorted"], sorted_ids)
@@ -103,3 +103,21 @@ def check_output(o, li: inputs.LayerInputs, x: np.ndarray, y_bits: np.ndarray, s
     assert rel <= REL_FRO_TOL, f"relative Frobenius error {rel:.3e} > {REL_FRO_TOL}"
     assert mx <= MAX_ABS_TOL, f"max abs error {mx:.3e} > {MAX_ABS_TOL}"
     return rel, mx
+
+
+def ungroup_mx_scales(buf: np.ndarray, rows: int, K: int) -> np.ndarray:
+    """Scales in the block-scaled MMA's tile layout (512 bytes per 128-row group
+    and 128-element chunk: byte r*16 + 4*j + b = row 32*j + r, block b) ->
+    [rows, K/32] in scale-row order."""
+    ng, kc = rows // 128, K // 128
+    t = np.asarray(buf, np.uint8)[: ng * kc * 512].reshape(ng, kc, 32, 4, 4)  # [g][c][r][j][b]
+    return t.transpose(0, 3, 2, 1, 4).reshape(ng * 128, kc * 4)
+
+
+def w13_scale_rows(E: int, I: int) -> np.ndarray:
+    """Scale row of each W13 row (e*2I + i): the gate/up GEMM's tile-row order."""
+    i = np.arange(2 * I)
+    up, f = i // I, i % I
+    m = 32 * ((f % 64) // 16) + 16 * up + f % 16
+    R = [(e * (I // 64) + f // 64) * 128 + m for e in range(E)]
+    return np.concatenate(R)
