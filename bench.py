@@ -430,19 +430,32 @@ def run_ours(args, wl, world, rank, local):
     kern_ev = {T: [new_events() for _ in range(args.steps)] for T in Ts}
     setup_s = time.time() - t_setup
 
-    ff = args.fused_front
+    ff, mx = args.fused_front, args.mx
+    if mx:
+        layer.quantize_mx()
+
+    def fwd(x, y, events=None):
+        if mx:
+            return layer.forward_mx(x, y, events=events)
+        return layer.forward(x, y, events=events, fused_front=ff)
+
+    def kpc(T):  # our kernels per layer call
+        if ff:
+            return 4
+        n = binding.kernels_per_call(T, H, wl["I"], wl["E"], wl["k"])
+        return n + 1 if mx else n  # MXFP8: + the activation quantize
 
     def one_step(step_idx=None, per_kernel=False):
         for T in Ts:
             flush_l2(step_idx or 0)
             if step_idx is None:
-                layer.forward(xs[T], ys[T], fused_front=ff)
+                fwd(xs[T], ys[T])
             elif per_kernel:
-                layer.forward(xs[T], ys[T], events=[e.cuda_event for e in kern_ev[T][step_idx]], fused_front=ff)
+                fwd(xs[T], ys[T], events=[e.cuda_event for e in kern_ev[T][step_idx]])
             else:
                 a, b = call_ev[T][step_idx]
                 a.record(stream)
-                layer.forward(xs[T], ys[T], fused_front=ff)
+                fwd(xs[T], ys[T])
                 b.record(stream)
 
     for _ in range(args.warmup):
@@ -456,7 +469,7 @@ def run_ours(args, wl, world, rank, local):
     # routing facts (touched experts) of each batch, from the last warm-up call
     touched = {}
     for T in Ts:
-        layer.forward(xs[T], ys[T])
+        fwd(xs[T], ys[T])
         ids = layer.view_tensor(T, "topk_ids", torch.int32, (T, wl["k"])).cpu().numpy()
         touched[T] = accounting.n_touched(ids, wl["E"])
     torch.cuda.synchronize()
@@ -497,14 +510,14 @@ def run_ours(args, wl, world, rank, local):
                 kern_ms[n] += dt
                 kt[n].append(dt)
         total_ms += sum(calls)
-        lb = accounting.layer_bytes(T, H, wl["I"], wl["E"], wl["k"], touched[T])
+        lb = accounting.layer_bytes(T, H, wl["I"], wl["E"], wl["k"], touched[T], mx)
         us = statistics.median(calls) * 1e3
         per_T[str(T)] = {"us_median": round(us, 2), "us_mean": round(sum(calls) / len(calls) * 1e3, 2),
                          "tokens_per_s": round(T / (us * 1e-6), 1), "experts_touched": touched[T],
                          "weight_GB": round(lb["weights"] / 1e9, 4),
                          "weight_GBps": round(lb["weights"] / (us * 1e-6) / 1e9, 1),
                          "hbm_frac_of_8TBps": round(lb["weights"] / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
-                         "kernels_per_call": 4 if ff else binding.kernels_per_call(T, H, wl["I"], wl["E"], wl["k"]),
+                         "kernels_per_call": kpc(T),
                          "kernel_us_median": {n: round(statistics.median(v) * 1e3, 2) for n, v in kt.items()}}
     ms_per_step = total_ms / args.steps
     tokens_per_step = sum(Ts)
@@ -525,12 +538,12 @@ def run_ours(args, wl, world, rank, local):
         roof["peak_source"] = f"bf16_tflops ({peak_kind})"
     else:
         if dom == "gemm_gate_up_swiglu":
-            per = [accounting.gemm1_kernel_bytes(T, H, wl["I"], wl["k"], touched[T]) for T in Ts]
+            per = [accounting.gemm1_kernel_bytes(T, H, wl["I"], wl["k"], touched[T], mx) for T in Ts]
         elif dom == "gemm_down":
-            per = [accounting.gemm2_kernel_bytes(T, H, wl["I"], wl["k"], touched[T]) for T in Ts]
+            per = [accounting.gemm2_kernel_bytes(T, H, wl["I"], wl["k"], touched[T], mx) for T in Ts]
         else:
-            per = [accounting.layer_bytes(T, H, wl["I"], wl["E"], wl["k"], touched[T])["total"] for T in Ts]
-        traffic = ncu_traffic_per_launch(dom, args.workload)
+            per = [accounting.layer_bytes(T, H, wl["I"], wl["E"], wl["k"], touched[T], mx)["total"] for T in Ts]
+        traffic = None if mx else ncu_traffic_per_launch(dom, args.workload)
         roof = roofline("hbm", sum(per) / len(per), avg_s, peaks["hbm_gbs"], traffic)
         roof["peak_source"] = f"hbm_gbs ({peak_kind}, copy bandwidth)"
     roof["kernel"] = dom
@@ -548,7 +561,7 @@ def run_ours(args, wl, world, rank, local):
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
             xs[T].copy_(pinned_x[T], non_blocking=True)
-            layer.forward(xs[T], ys[T])
+            fwd(xs[T], ys[T])
             pinned_y[T].copy_(ys[T], non_blocking=True)
             b.record(stream)
             b.synchronize()
@@ -561,9 +574,12 @@ def run_ours(args, wl, world, rank, local):
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator; random-init weights)",
+        "vs_baseline": None, "dtype": "mxfp8 (e4m3 + e8m0 per 32) x mxfp8, fp32 accumulation" if mx else "bf16",
+        "data": "synthetic (seeded generator; random-init weights)",
         "config": {"workload": wl["label"], "tokens_per_step": tokens_per_step,
                    "layer_calls_per_step": len(Ts),
+                   "expert_weights": ("MXFP8 (moe_forward_mx; weight bytes counted as codes + scales)" if mx
+                                      else "bf16"),
                    "front_end": ("moe_forward_fused_front: norm .. gather in one cluster launch" if ff
                                  else "moe_forward: multi-launch front end"),
                    "l2": "flushed before every layer call (256 MB write, then a 256 MB read of another buffer so "
@@ -578,8 +594,7 @@ def run_ours(args, wl, world, rank, local):
         "e2e": e2e,
         # kernels of the timed pass (top-k runs inside the align kernel for small T and E); the per-kernel pass
         # launches as many again
-        "gpu_launches": sum(args.steps * (4 if ff else binding.kernels_per_call(T, wl["H"], wl["I"], wl["E"], wl["k"]))
-                            for T in Ts),
+        "gpu_launches": sum(args.steps * kpc(T) for T in Ts),
         "clocks": clocks,
     }
     return out, host
@@ -596,6 +611,8 @@ def main():
                     help="CPU oracle sample: at most this many tokens of each batch per step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum timed CPU-oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mx", action="store_true",
+                    help="time moe_forward_mx: MXFP8 expert weights and activations (decode shapes)")
     ap.add_argument("--fused-front", action="store_true",
                     help="time moe_forward_fused_front (norm .. gather in one cluster launch; T <= 64)")
     args = ap.parse_args()

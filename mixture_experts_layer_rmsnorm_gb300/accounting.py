@@ -39,13 +39,20 @@ def n_touched(topk_ids: np.ndarray, E: int) -> int:
     return int(np.unique(np.asarray(topk_ids).reshape(-1)).size) if np.asarray(topk_ids).size else 0
 
 
-def expert_weight_bytes(H: int, I: int) -> dict:
-    """Bytes of one expert's weights: gate/up (W13) and down (W2)."""
+def mx_bytes(n_elems: int) -> int:
+    """MXFP8 bytes of n elements: one E4M3 code each plus one E8M0 scale per 32."""
+    return n_elems + n_elems // 32
+
+
+def expert_weight_bytes(H: int, I: int, mx: bool = False) -> dict:
+    """Bytes of one expert's weights: gate/up (W13) and down (W2); mx: MXFP8 copies."""
+    if mx:
+        return {"w13": mx_bytes(2 * I * H), "w2": mx_bytes(H * I)}
     return {"w13": 2 * I * H * BF16, "w2": H * I * BF16}
 
 
-def layer_bytes(T: int, H: int, I: int, E: int, k: int, touched: int) -> dict:
-    ew = expert_weight_bytes(H, I)
+def layer_bytes(T: int, H: int, I: int, E: int, k: int, touched: int, mx: bool = False) -> dict:
+    ew = expert_weight_bytes(H, I, mx)
     d = {
         "weights_w13": touched * ew["w13"],
         "weights_w2": touched * ew["w2"],
@@ -64,11 +71,15 @@ def layer_flops(T: int, H: int, I: int, E: int, k: int) -> dict:
     return {"gemm1": g1, "gemm2": g2, "router": r, "total": g1 + g2 + r}
 
 
-def gemm1_kernel_bytes(T: int, H: int, I: int, k: int, touched: int) -> int:
+def gemm1_kernel_bytes(T: int, H: int, I: int, k: int, touched: int, mx: bool = False) -> int:
     """Algorithmic bytes of the gate/up expert GEMM: touched W13, the T*k
-    gathered token rows read once, the T*k activation rows written once."""
+    gathered token rows read once, the T*k activation rows (bf16) written once."""
+    if mx:
+        return mx_bytes(touched * 2 * I * H) + mx_bytes(T * k * H) + T * k * I * BF16
     return touched * 2 * I * H * BF16 + T * k * H * BF16 + T * k * I * BF16
 
 
-def gemm2_kernel_bytes(T: int, H: int, I: int, k: int, touched: int) -> int:
+def gemm2_kernel_bytes(T: int, H: int, I: int, k: int, touched: int, mx: bool = False) -> int:
+    if mx:
+        return mx_bytes(touched * H * I) + mx_bytes(T * k * I) + T * k * H * BF16
     return touched * H * I * BF16 + T * k * I * BF16 + T * k * H * BF16
