@@ -219,11 +219,24 @@ def make_host_inputs(wl):
     return dict(g=g, wr=wr, bias=bias, w13=w13, w2=w2, xs=xs)
 
 
-def cpu_oracle_rate(wl, host, per_batch_cap, reps=1, min_seconds=0.0, max_reps=50):
-    """Tokens/s of the CPU oracle (as it stands, all host cores) on a bounded
-    sample: from each of the workload's batches, up to per_batch_cap tokens
-    spread over the batch; repeated `reps` times, or more until min_seconds of
-    CPU work have been timed (at most max_reps)."""
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                low = ln.lower()
+                if low.startswith("model name") or low.startswith("cpu part") or low.startswith("hardware"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def cpu_oracle_rate(wl, host, per_batch_cap, reps=1, min_seconds=0.0, max_reps=50, nthreads=None):
+    """Tokens/s of the CPU oracle (as it stands; all host cores unless nthreads)
+    on a bounded sample: from each of the workload's batches, up to
+    per_batch_cap tokens spread over the batch; repeated `reps` times, or more
+    until min_seconds of CPU work have been timed (at most max_reps)."""
     import numpy as np
     import oracle
     total_tok, total_s, r = 0, 0.0, 0
@@ -232,11 +245,11 @@ def cpu_oracle_rate(wl, host, per_batch_cap, reps=1, min_seconds=0.0, max_reps=5
             sample = np.unique(np.linspace(0, T - 1, min(T, per_batch_cap)).astype(np.int64))
             t0 = time.perf_counter()
             oracle.moe_forward(host["xs"][T], host["g"], host["wr"], host["bias"], host["w13"], host["w2"], wl["k"],
-                               True, 1e-6, sample=sample)
+                               True, 1e-6, sample=sample, nthreads=nthreads)
             total_s += time.perf_counter() - t0
             total_tok += sample.size
         r += 1
-    return total_tok / total_s, total_tok, total_s, oracle.threads(), r
+    return total_tok / total_s, total_tok, total_s, nthreads or oracle.threads(), r
 
 
 # ----------------------------------------------------------------- QK-norm
@@ -496,6 +509,18 @@ def run_ours(args, wl, world, rank, local):
         one_step(s, per_kernel=True)
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    # extra, not the headline: the same calls with the L2 left warm (no flush),
+    # each batch called `reps` times back to back
+    warm = {}
+    for T in Ts:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fwd(xs[T], ys[T])
+        a.record(stream)
+        for _ in range(args.steps):
+            fwd(xs[T], ys[T])
+        b.record(stream)
+        torch.cuda.synchronize()
+        warm[T] = a.elapsed_time(b) / args.steps
 
     # per-call device times (plain calls) and per-kernel times (second pass)
     per_T = {}
@@ -518,6 +543,7 @@ def run_ours(args, wl, world, rank, local):
                          "weight_GBps": round(lb["weights"] / (us * 1e-6) / 1e9, 1),
                          "hbm_frac_of_8TBps": round(lb["weights"] / (us * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
                          "kernels_per_call": kpc(T),
+                         "us_unflushed_mean": round(warm[T] * 1e3, 2),
                          "kernel_us_median": {n: round(statistics.median(v) * 1e3, 2) for n, v in kt.items()}}
     ms_per_step = total_ms / args.steps
     tokens_per_step = sum(Ts)
@@ -679,9 +705,15 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cap = args.ref_tokens_per_batch
         rate, ntok, secs, cores, reps = cpu_oracle_rate(wl, host, cap, reps=1, min_seconds=args.cpu_seconds)
+        # one thread, a smaller sample (a token each from every batch)
+        r1, n1, s1, _, p1 = cpu_oracle_rate(wl, host, 1, reps=1, min_seconds=min(3.0, args.cpu_seconds), max_reps=3,
+                                            nthreads=1)
         out["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                               "cpu": cpu_model(),
                                "sample": f"{ntok} tokens: {reps} passes over up to {cap} tokens of each batch "
-                                         f"T={wl['Ts']} ({secs:.1f} s)"}
+                                         f"T={wl['Ts']} ({secs:.1f} s)",
+                               "single_thread": {"value": round(r1, 3), "unit": "tokens/s",
+                                                 "sample": f"{n1} tokens in {p1} passes ({s1:.1f} s)"}}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
