@@ -17,7 +17,7 @@
 namespace moe {
 
 // NT threads (E <= NT) call it together.  id_at(i) returns ids[i] (0 <= i < N).
-// Shared scratch: cnt[E], cursor[E], wbase[NT/32][E], scan_tmp[33], *bad.
+// Shared scratch: cnt[E], cursor[E], wbase[E][NT/32], scan_tmp[3 * 33], *bad.
 // Outputs may live in shared or global memory; unit_off1/2 may be null (a
 // table is only written when its bn > 0).  Returns false, having written no
 // output, when an id lies outside [0, E) (the result is uniform over the CTA).
@@ -48,10 +48,11 @@ __device__ bool align_core(IdAt id_at, int N, int E, int pad, int bn1, int tiles
     const int p = (c + pad - 1) / pad * pad;
     const int u1 = (bn1 > 0) ? (p + bn1 - 1) / bn1 * tiles1 : 0;
     const int u2 = (bn2 > 0) ? (p + bn2 - 1) / bn2 * tiles2 : 0;
-    int tot_p, tot_u1, tot_u2;
-    const int off = block_exclusive_scan<NT>(p, scan_tmp, &tot_p);
-    const int o1 = block_exclusive_scan<NT>(u1, scan_tmp, &tot_u1);
-    const int o2 = block_exclusive_scan<NT>(u2, scan_tmp, &tot_u2);
+    const int v3[3] = {p, u1, u2};
+    int pre[3], tot[3];
+    block_exclusive_scan3<NT>(v3, scan_tmp, pre, tot);
+    const int off = pre[0], o1 = pre[1], o2 = pre[2];
+    const int tot_p = tot[0], tot_u1 = tot[1], tot_u2 = tot[2];
     if (e < E) {
       counts[e] = c;
       offsets[e] = off;
@@ -77,20 +78,26 @@ __device__ bool align_core(IdAt id_at, int N, int E, int pad, int bn1, int tiles
     const int rank = __popc(same & ((1u << lane) - 1u));
     for (int q = tid; q < kWarps * E; q += NT) wbase[q] = 0;
     __syncthreads();
-    if (valid && rank == 0) wbase[warp * E + e] = __popc(same);
+    if (valid && rank == 0) wbase[e * kWarps + warp] = __popc(same);
     __syncthreads();
-    for (int ex = tid; ex < E; ex += NT) {
-      int run = cursor[ex];
-      for (int w = 0; w < kWarps; ++w) {
-        const int c = wbase[w * E + ex];
-        wbase[w * E + ex] = run;
-        run += c;
+    // per expert, an exclusive scan over the warps' counts (one warp per
+    // expert, lane w = warp w), offset by the expert's cursor
+    for (int ex = warp; ex < E; ex += kWarps) {
+      const int c = (lane < kWarps) ? wbase[ex * kWarps + lane] : 0;
+      int inc = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, inc, off);
+        if (lane >= off) inc += o;
       }
-      cursor[ex] = run;
+      const int cur = cursor[ex];
+      if (lane < kWarps) wbase[ex * kWarps + lane] = cur + inc - c;
+      __syncwarp();
+      if (lane == 31) cursor[ex] = cur + inc;
     }
     __syncthreads();
     if (valid) {
-      const int pos = wbase[warp * E + e] + rank;
+      const int pos = wbase[e * kWarps + warp] + rank;
       sorted_ids[pos] = i;
       slot_of[i] = pos;
     }

@@ -27,11 +27,11 @@ constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
 
 // One CTA of 1024 threads.  Dynamic shared memory: cnt[E], cursor[E],
-// wbase[32][E] (ints).  With FUSED_TOPK the CTA first selects the top-k
-// experts of all T tokens from the logits (one warp per token; used for small
-// T, where a separate launch costs more than the work), then aligns.
-// The routing ids are read with L2-coherent loads: in the fused form this
-// kernel wrote them itself.
+// wbase[E][32] (ints), and ids_s[N] in the fused form.  With FUSED_TOPK the CTA
+// first selects the top-k experts of all T tokens from the logits (one warp
+// per token; used for small T, where a separate launch costs more than the
+// work), keeps a copy of the ids in shared memory and aligns from it.
+// Otherwise the routing ids are read with L2-coherent loads.
 template <int FUSED_VPL>  // 0: ids given; else top-k first, with FUSED_VPL logits per lane
 __global__ void __launch_bounds__(kAlignThreads)
     align_kernel(const float* __restrict__ logits, int T, int k, int renorm, float* __restrict__ topk_w,
@@ -42,8 +42,9 @@ __global__ void __launch_bounds__(kAlignThreads)
   extern __shared__ int sm[];
   int* cnt = sm;                 // [E]
   int* cursor = sm + E;          // [E]
-  int* wbase = sm + 2 * E;       // [32][E]
-  __shared__ int scan_tmp[kAlignWarps + 1];
+  int* wbase = sm + 2 * E;       // [E][32]
+  int* ids_s = wbase + kAlignWarps * E;  // [N], fused form only
+  __shared__ int scan_tmp[3 * 33];
   __shared__ int bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_wait();
@@ -52,13 +53,14 @@ __global__ void __launch_bounds__(kAlignThreads)
   if constexpr (FUSED_VPL > 0) {
     for (int t = warp; t < T; t += kAlignWarps)
       topk_softmax_warp<FUSED_VPL>(logits + static_cast<size_t>(t) * E, E, k, renorm,
-                                   ids + static_cast<size_t>(t) * k, topk_w + static_cast<size_t>(t) * k);
+                                   ids + static_cast<size_t>(t) * k, topk_w + static_cast<size_t>(t) * k,
+                                   ids_s + static_cast<size_t>(t) * k);
     __syncthreads();
   }
 
-  const bool ok = align_core<kAlignThreads>([&](int i) { return __ldcg(ids + i); }, N, E, pad, bn1, tiles1, bn2,
-                                             tiles2, cnt, cursor, wbase, scan_tmp, &bad, counts, offsets, sorted_ids,
-                                             slot_of, unit_off1, unit_off2);
+  const bool ok = align_core<kAlignThreads>(
+      [&](int i) { return FUSED_VPL > 0 ? ids_s[i] : __ldcg(ids + i); }, N, E, pad, bn1, tiles1, bn2, tiles2, cnt,
+      cursor, wbase, scan_tmp, &bad, counts, offsets, sorted_ids, slot_of, unit_off1, unit_off2);
   if (!ok) {
     if (tid == 0) {
       err[1] = kKernAlign;
@@ -164,7 +166,7 @@ cudaError_t launch_align_t(const float* logits, int T, int k, int renorm, int32_
                            int E, int pad, int bn1, int tiles1, int bn2, int tiles2, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_ids, int32_t* slot_of, int32_t* unit_off1, int32_t* unit_off2,
                            int32_t* err, int32_t* flags, int n_flags, cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(2 + kAlignWarps) * E * sizeof(int);
+  const size_t smem = (static_cast<size_t>(2 + kAlignWarps) * E + (VPL > 0 ? N : 0)) * sizeof(int);
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);

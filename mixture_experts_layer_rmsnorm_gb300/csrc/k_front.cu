@@ -44,7 +44,7 @@ __host__ __device__ inline size_t front_align_ints(int N, int E) {
          + 2 * E + kFrontWarps * E                  // cnt, cursor, wbase
          + E + 3 * (E + 1)                          // counts, offsets, two unit tables
          + p_cap + N                                // sorted_ids, slot_of
-         + 33 + 1;                                  // scan scratch, error flag
+         + 3 * 33 + 1;                              // scan scratch, error flag
 }
 
 template <int TT, int TE, int VPL>
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kFrontThreads, 1) front_kernel(const __grid_co
   uint4* h_s = reinterpret_cast<uint4*>(fsm);
   for (int it = c; it < a.n_items; it += C) {
     const int tt = it / a.groups, eg = it % a.groups;
-    rt::norm_router_tile<TT, TE>(a.x, a.g, a.w_router, a.bias, a.T, a.H, a.E, a.eps, tt * TT,
+    rt::norm_router_tile<TT, TE, false>(a.x, a.g, a.w_router, a.bias, a.T, a.H, a.E, a.eps, tt * TT,
                                  eg * a.experts_per_item, a.experts_per_item, eg == 0, a.h, a.logits, h_s);
     __syncthreads();  // h_s is reused by the next item
   }
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kFrontThreads, 1) front_kernel(const __grid_co
   int32_t* s_sorted = s_unit2 + (E + 1);
   int32_t* s_slot = s_sorted + p_cap;
   int* scan_tmp = s_slot + N;
-  int* bad = scan_tmp + 33;
+  int* bad = scan_tmp + 3 * 33;
 
   for (int t = warp; t < a.T; t += kFrontWarps)
     topk_softmax_warp<VPL>(a.logits + static_cast<size_t>(t) * E, E, a.k, a.renorm, s_ids + t * a.k,

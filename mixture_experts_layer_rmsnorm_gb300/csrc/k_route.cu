@@ -78,7 +78,8 @@ cudaError_t launch_norm_router(const uint16_t* x, const uint16_t* g, const float
                                int T, int H, int E, float eps, uint16_t* h, float* logits, int32_t* err,
                                int num_sms, cudaStream_t stream) {
   if (T <= 3) return launch_nr<1, 1>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
-  if (T <= 64 || H > 8192)
+  if (T <= 64) return launch_nr<4, 1>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
+  if (H > 8192)
     return launch_nr<4, 2>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
   return launch_nr<8, 4>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
 }

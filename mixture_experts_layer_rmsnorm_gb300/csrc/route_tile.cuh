@@ -60,11 +60,70 @@ __device__ __forceinline__ void route_prefetch(const float* w_router, const uint
     asm volatile("prefetch.global.L2 [%0];" ::"l"(gb + off));
 }
 
+// h = bf16((x * rstd) * g) for the chunks [8c, 8c+8) of one row
+__device__ __forceinline__ uint4 norm_chunk(const uint4& xv, const uint4& gv, float rstd) {
+  float f[8], gg[8];
+  unpack8(xv, f);
+  unpack8(gv, gg);
+  uint4 o;
+  o.x = pack2_bf16(__fmul_rn(__fmul_rn(f[0], rstd), gg[0]), __fmul_rn(__fmul_rn(f[1], rstd), gg[1]));
+  o.y = pack2_bf16(__fmul_rn(__fmul_rn(f[2], rstd), gg[2]), __fmul_rn(__fmul_rn(f[3], rstd), gg[3]));
+  o.z = pack2_bf16(__fmul_rn(__fmul_rn(f[4], rstd), gg[4]), __fmul_rn(__fmul_rn(f[5], rstd), gg[5]));
+  o.w = pack2_bf16(__fmul_rn(__fmul_rn(f[6], rstd), gg[6]), __fmul_rn(__fmul_rn(f[7], rstd), gg[7]));
+  return o;
+}
+
+__device__ __forceinline__ float rms_rstd(float ss, int H, float eps) {
+  ss = warp_butterfly_sum(ss);
+  const float ms = __fdiv_rn(ss, static_cast<float>(H));
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+// One round of the logits loop: chunks c0 + 32 d (d < DEPTH) of TE router
+// rows, all loaded before the first FMA, then accumulated in chunk order.
+// MASKED: skip the chunks at or past nch.
+template <int TT, int TE, int DEPTH, bool MASKED>
+__device__ __forceinline__ void gemv_round(const float4* const (&wrow)[TE], const uint4* h_s, int nch, int c0,
+                                           float (&acc)[TT][TE]) {
+  float4 wv[DEPTH][TE][2];
+#pragma unroll
+  for (int d = 0; d < DEPTH; ++d)
+#pragma unroll
+    for (int b = 0; b < TE; ++b) {
+      if (!MASKED || c0 + 32 * d < nch) {
+        wv[d][b][0] = __ldg(wrow[b] + 2 * (c0 + 32 * d));
+        wv[d][b][1] = __ldg(wrow[b] + 2 * (c0 + 32 * d) + 1);
+      }
+    }
+#pragma unroll
+  for (int d = 0; d < DEPTH; ++d) {
+    const int c = c0 + 32 * d;
+    if (!MASKED || c < nch) {
+#pragma unroll
+      for (int a = 0; a < TT; ++a) {
+        float hv[8];
+        unpack8(h_s[a * nch + c], hv);
+#pragma unroll
+        for (int b = 0; b < TE; ++b) {
+          const float w[8] = {wv[d][b][0].x, wv[d][b][0].y, wv[d][b][0].z, wv[d][b][0].w,
+                              wv[d][b][1].x, wv[d][b][1].y, wv[d][b][1].z, wv[d][b][1].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[a][b] = __fmaf_rn(hv[i], w[i], acc[a][b]);
+        }
+      }
+    }
+  }
+}
+
 // Tokens [t0, t0+TT) x experts [e0, e0+experts_per_cta): RMSNorm of the
 // tokens into h_s (TT*H bf16 of shared memory; also to h_out when write_h),
 // then the fp32 logits.  Each warp computes TE experts x TT tokens at a time.
 // The CTA's kRouteWarps*32 threads call it together (it synchronises them).
-template <int TT, int TE>
+// Both phases are bound by memory latency at small T, so a lane issues the
+// loads of a whole pass (up to kRegChunks chunks of x and g, DEPTH chunks of
+// router weights per expert) before it uses any of them.  DEEP = false halves
+// both depths, for callers that need the registers for other work.
+template <int TT, int TE, bool DEEP = true>
 __device__ __forceinline__ void norm_router_tile(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g,
                                                  const float* __restrict__ w_router, const float* __restrict__ bias,
                                                  int T, int H, int E, float eps, int t0, int e0, int experts_per_cta,
@@ -73,48 +132,74 @@ __device__ __forceinline__ void norm_router_tile(const uint16_t* __restrict__ x,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nch = H >> 3;
   // ---- RMSNorm: one warp per token
+  constexpr int kRegChunks = (TT >= 8 || !DEEP) ? 8 : 16;  // per lane: rows up to 256 * kRegChunks elements in registers
   for (int tt = warp; tt < TT; tt += kRouteWarps) {
     const int t = t0 + tt;
     if (t >= T) break;
     const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * H);
-    float ss = 0.0f;
-    int c = lane;
-    // 8 chunks' loads in flight, then their FMAs in chunk order
-    for (; c + 32 * 7 < nch; c += 32 * 8) {
-      uint4 v[8];
+    const uint4* gr = reinterpret_cast<const uint4*>(g);
+    uint4* hrow = reinterpret_cast<uint4*>(h_out + static_cast<size_t>(t) * H);
+    if (TT < 8 && nch <= 32 * kRegChunks) {
+      // the whole row: x and g loads all in flight, one pass
+      uint4 xv[kRegChunks], gv[kRegChunks];
 #pragma unroll
-      for (int d = 0; d < 8; ++d) v[d] = __ldg(xr + c + 32 * d);
+      for (int d = 0; d < kRegChunks; ++d) {
+        const int c = lane + 32 * d;
+        if (c < nch) {
+          xv[d] = __ldg(xr + c);
+          gv[d] = __ldg(gr + c);
+        }
+      }
+      float ss = 0.0f;
 #pragma unroll
-      for (int d = 0; d < 8; ++d) {
+      for (int d = 0; d < kRegChunks; ++d) {
+        if (lane + 32 * d < nch) {
+          float f[8];
+          unpack8(xv[d], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ss = __fmaf_rn(f[i], f[i], ss);
+        }
+      }
+      const float rstd = rms_rstd(ss, H, eps);
+#pragma unroll
+      for (int d = 0; d < kRegChunks; ++d) {
+        const int c = lane + 32 * d;
+        if (c < nch) {
+          const uint4 o = norm_chunk(xv[d], gv[d], rstd);
+          h_s[tt * nch + c] = o;
+          if (write_h) hrow[c] = o;
+        }
+      }
+    } else {
+      // longer rows: 8 chunks' loads in flight, then their FMAs in chunk order;
+      // a second pass for h
+      float ss = 0.0f;
+      int c = lane;
+      for (; c + 32 * 7 < nch; c += 32 * 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int d = 0; d < 8; ++d) v[d] = __ldg(xr + c + 32 * d);
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+          float f[8];
+          unpack8(v[d], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ss = __fmaf_rn(f[i], f[i], ss);
+        }
+      }
+      for (; c < nch; c += 32) {
         float f[8];
-        unpack8(v[d], f);
+        unpack8(__ldg(xr + c), f);
 #pragma unroll
         for (int i = 0; i < 8; ++i) ss = __fmaf_rn(f[i], f[i], ss);
       }
-    }
-    for (; c < nch; c += 32) {
-      float f[8];
-      unpack8(__ldg(xr + c), f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ss = __fmaf_rn(f[i], f[i], ss);
-    }
-    ss = warp_butterfly_sum(ss);
-    const float ms = __fdiv_rn(ss, static_cast<float>(H));
-    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
-    const uint4* gr = reinterpret_cast<const uint4*>(g);
-    uint4* hrow = reinterpret_cast<uint4*>(h_out + static_cast<size_t>(t) * H);
+      const float rstd = rms_rstd(ss, H, eps);
 #pragma unroll 4
-    for (int c = lane; c < nch; c += 32) {
-      float f[8], gg[8];
-      unpack8(__ldg(xr + c), f);
-      unpack8(__ldg(gr + c), gg);
-      uint4 o;
-      o.x = pack2_bf16(__fmul_rn(__fmul_rn(f[0], rstd), gg[0]), __fmul_rn(__fmul_rn(f[1], rstd), gg[1]));
-      o.y = pack2_bf16(__fmul_rn(__fmul_rn(f[2], rstd), gg[2]), __fmul_rn(__fmul_rn(f[3], rstd), gg[3]));
-      o.z = pack2_bf16(__fmul_rn(__fmul_rn(f[4], rstd), gg[4]), __fmul_rn(__fmul_rn(f[5], rstd), gg[5]));
-      o.w = pack2_bf16(__fmul_rn(__fmul_rn(f[6], rstd), gg[6]), __fmul_rn(__fmul_rn(f[7], rstd), gg[7]));
-      h_s[tt * nch + c] = o;
-      if (write_h) hrow[c] = o;
+      for (int c2 = lane; c2 < nch; c2 += 32) {
+        const uint4 o = norm_chunk(__ldg(xr + c2), __ldg(gr + c2), rstd);
+        h_s[tt * nch + c2] = o;
+        if (write_h) hrow[c2] = o;
+      }
     }
   }
   __syncthreads();
@@ -122,6 +207,9 @@ __device__ __forceinline__ void norm_router_tile(const uint16_t* __restrict__ x,
   // ---- logits: warp w takes expert groups e0 + (w + 8 r) * TE .. + TE
   const int e_end = min(E, e0 + experts_per_cta);
   const int ntok = min(TT, T - t0);
+  // DEPTH chunks of router weights in flight per lane (32 B each per expert),
+  // consumed in chunk order, so every accumulator keeps the canonical sequence
+  constexpr int DEPTH = ((TE >= 4) ? 2 : (TE == 2 ? 8 : 16)) / (DEEP || TE >= 4 ? 1 : 2);
   for (int eg = e0 + warp * TE; eg < e_end; eg += kRouteWarps * TE) {
     float acc[TT][TE];
 #pragma unroll
@@ -134,52 +222,13 @@ __device__ __forceinline__ void norm_router_tile(const uint16_t* __restrict__ x,
       const int e = min(eg + b, E - 1);  // clamp: a tail expert's duplicate is computed but not stored
       wrow[b] = reinterpret_cast<const float4*>(w_router + static_cast<size_t>(e) * H);
     }
-    // DEPTH chunks of router weights in flight per lane, consumed in chunk
-    // order, so every accumulator keeps the canonical sequence
-    constexpr int DEPTH = (TE >= 4) ? 2 : (TE == 2 ? 4 : 8);
-    int c = lane;
-    for (; c + 32 * (DEPTH - 1) < nch; c += 32 * DEPTH) {
-      float4 wv[DEPTH][TE][2];
-#pragma unroll
-      for (int d = 0; d < DEPTH; ++d)
-#pragma unroll
-        for (int b = 0; b < TE; ++b) {
-          wv[d][b][0] = __ldg(wrow[b] + 2 * (c + 32 * d));
-          wv[d][b][1] = __ldg(wrow[b] + 2 * (c + 32 * d) + 1);
-        }
-#pragma unroll
-      for (int d = 0; d < DEPTH; ++d) {
-#pragma unroll
-        for (int a = 0; a < TT; ++a) {
-          float hv[8];
-          unpack8(h_s[a * nch + c + 32 * d], hv);
-#pragma unroll
-          for (int b = 0; b < TE; ++b) {
-            const float w[8] = {wv[d][b][0].x, wv[d][b][0].y, wv[d][b][0].z, wv[d][b][0].w,
-                                wv[d][b][1].x, wv[d][b][1].y, wv[d][b][1].z, wv[d][b][1].w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[a][b] = __fmaf_rn(hv[i], w[i], acc[a][b]);
-          }
-        }
-      }
-    }
-    for (; c < nch; c += 32) {
-      float w[TE][8];
-#pragma unroll
-      for (int b = 0; b < TE; ++b) {
-        const float4 p = __ldg(wrow[b] + 2 * c), q = __ldg(wrow[b] + 2 * c + 1);
-        w[b][0] = p.x; w[b][1] = p.y; w[b][2] = p.z; w[b][3] = p.w;
-        w[b][4] = q.x; w[b][5] = q.y; w[b][6] = q.z; w[b][7] = q.w;
-      }
-#pragma unroll
-      for (int a = 0; a < TT; ++a) {
-        float hv[8];
-        unpack8(h_s[a * nch + c], hv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int b = 0; b < TE; ++b) acc[a][b] = __fmaf_rn(hv[i], w[b][i], acc[a][b]);
-      }
+    // full rounds of DEPTH chunks, then one round with the chunks past the row masked off
+    int c0 = lane;
+    for (; c0 + 32 * (DEPTH - 1) < nch; c0 += 32 * DEPTH) gemv_round<TT, TE, DEPTH, false>(wrow, h_s, nch, c0, acc);
+    if constexpr (DEPTH > 2) {
+      if (c0 < nch) gemv_round<TT, TE, DEPTH, true>(wrow, h_s, nch, c0, acc);
+    } else {
+      for (; c0 < nch; c0 += 32) gemv_round<TT, TE, 1, false>(wrow, h_s, nch, c0, acc);
     }
 #pragma unroll
     for (int a = 0; a < TT; ++a)

@@ -7,50 +7,71 @@
 
 namespace moe {
 
+// Order-preserving key of a logit for unsigned comparison: larger value ->
+// larger key; -0 and +0 share a key; 0 is kept for "not a candidate" (NaN,
+// an expert already taken, a lane past E), so NaN is never selected.
+__device__ __forceinline__ uint32_t topk_key(float v) {
+  if (v != v) return 0u;
+  if (v == 0.0f) v = 0.0f;  // -0 -> +0: equal logits tie on the expert index
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);  // -inf -> 0x007FFFFF > 0
+}
+
 // Warp-cooperative (all 32 lanes call it with the same arguments).
 // l[E] (E <= 32 * VPL): the token's fp32 logits; VPL = values per lane.  Writes ids[k] (largest logit
 // first; equal logits: lower expert index first) and w[k]: the softmax over
 // all E taken at the selected experts, or over the selected ones only
 // (renormalised) when renorm != 0.  k <= 32.  The logits are read with
 // L2-coherent loads, so they may have been written earlier in the same kernel.
+// ids_s: optional second copy of ids (e.g. in shared memory).  Each selection
+// is a warp max of keys, then a warp min of the expert index among the lanes
+// holding that key (two redux.sync).  A step with no candidate left selects
+// expert INT_MAX (reported by the align as an id out of range).
 template <int VPL>
 __device__ __forceinline__ void topk_softmax_warp(const float* l, int E, int k, int renorm, int32_t* ids,
-                                                  float* w) {
+                                                  float* w, int32_t* ids_s = nullptr) {
   constexpr unsigned kAll = 0xFFFFFFFFu;
   const int lane = threadIdx.x & 31;
   float v[VPL];
+  uint32_t key[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
     v[i] = (e < E) ? __ldcg(l + e) : -FLT_MAX;
+    key[i] = (e < E) ? topk_key(v[i]) : 0u;
   }
-  uint32_t taken = 0;
   float my_v = 0.0f;  // lane j keeps the j-th selection
   int my_e = 0;
   for (int j = 0; j < k; ++j) {
+    // this lane's best candidate: largest key, lowest expert index on ties
+    uint32_t bk = 0u;
+    int bi = 0;
     float bv = -INFINITY;
-    int be = INT_MAX;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
+    for (int i = 0; i < VPL; ++i)
+      if (key[i] > bk) {
+        bk = key[i];
+        bi = i;
         bv = v[i];
-        be = e;
       }
-    }
+    const uint32_t mk = __reduce_max_sync(kAll, bk);
+    const uint32_t cand = (mk != 0u && bk == mk) ? static_cast<uint32_t>(lane + 32 * bi) : 0xFFFFFFFFu;
+    const uint32_t be = __reduce_min_sync(kAll, cand);
+    int sel = INT_MAX;
+    float sv = -INFINITY;
+    if (mk != 0u) {
+      sel = static_cast<int>(be);
+      if ((sel & 31) == lane) {
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      const float ov = __shfl_xor_sync(kAll, bv, off);
-      const int oe = __shfl_xor_sync(kAll, be, off);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
+        for (int i = 0; i < VPL; ++i)
+          if (i == (sel >> 5)) key[i] = 0u;  // taken
       }
     }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    sv = __shfl_sync(kAll, bv, sel & 31);  // the selected lane's own best is the selection
+    if (mk == 0u) sv = -INFINITY;
     if (lane == j) {
-      my_v = bv;
-      my_e = be;
+      my_v = sv;
+      my_e = sel;
     }
   }
   const float m = __shfl_sync(kAll, my_v, 0);  // the largest logit
@@ -67,6 +88,7 @@ __device__ __forceinline__ void topk_softmax_warp(const float* l, int E, int k, 
   if (lane < k) {
     ids[lane] = my_e;
     w[lane] = expf(my_v - m) / s;
+    if (ids_s) ids_s[lane] = my_e;
   }
 }
 

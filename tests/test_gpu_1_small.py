@@ -8,6 +8,8 @@ The shapes span several weight tiles, several token chunks per expert, ragged
 tails, both launch plans (decode tiles and prefill tiles) and the degenerate
 cases (T = 0, T = 1, E = 1, k = E, unnormalised weights, a router bias).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -94,6 +96,52 @@ def test_fused_front_rejects_large_batches():
     with pytest.raises(binding.MoeError) as ei:
         dl.run(li.x, fused_front=True)
     assert ei.value.status == binding.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("T", [5, 64, 300], ids=["fused_topk_T5", "fused_topk_T64", "multi_cta_T300"])
+def test_tied_logits_pick_the_lower_expert(o, T):
+    """Exactly equal logits are selected lowest expert index first, as the
+    oracle's top-k does, in the single-CTA top-k + align and in the multi-CTA
+    top-k.  Even tokens repeat token 0; with its normalised row u, experts 2, 5
+    and 11 get the router row u (equal largest logits), experts 7, 9 and 13 a
+    zero row (equal zero logits) and the others negative multiples of u, so
+    those tokens select [2, 5, 11, 7, 9, 13] in that order."""
+    E, k = 16, 6
+    li = _layer_inputs(T, 256, 256, E, k, True, None, 21)
+    x = li.x.copy()
+    x[0::2] = x[0]
+    h32, _, _ = o.route_f32(x[:1], li.g, li.cfg.eps, li.w_router, None)
+    u = gu.widen(h32[0]).astype(np.float32) / 64.0
+    wr = li.w_router.copy()
+    for e in range(E):
+        wr[e] = -(1.0 + e / 8.0) * u
+    wr[[2, 5, 11]] = u
+    wr[[7, 9, 13]] = 0.0
+    li = dataclasses.replace(li, x=x, w_router=wr)
+    dl = gu.DeviceLayer(li)
+    g = dl.run(x)
+    ids = gu.check_routing(o, li, x, g)
+    assert (ids[0::2] == np.array([2, 5, 11, 7, 9, 13])).all()
+    gu.check_output(o, li, x, g["y"])
+
+
+@pytest.mark.parametrize("T", [3, 300], ids=["fused_topk", "multi_cta_topk"])
+def test_non_finite_input_is_reported(o, T):
+    """A token whose row holds an infinity has NaN logits, so no expert can be
+    selected: the align reports MOE_ERR_DEVICE (the single-CTA form leaves an
+    empty routing, the multi-CTA form routes the token to expert 0), nothing
+    faults, and the next call on the same workspace is clean."""
+    li = _layer_inputs(T, 256, 256, 8, 2, True, None, 22)
+    bad = li.x.copy()
+    bad[T // 2, 17] = 0x7F80  # +inf
+    dl = gu.DeviceLayer(li)
+    L = dl.layer
+    L.forward(gu.dev_bf16(bad))
+    torch.cuda.synchronize()
+    st, det = L.device_status(T)
+    assert st == binding.MOE_ERR_DEVICE, (st, det)
+    g = dl.run(li.x)
+    gu.check_routing(o, li, li.x, g)
 
 
 def test_zero_tokens_is_a_noop():
