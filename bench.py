@@ -443,20 +443,19 @@ def run_ours(args, wl, world, rank, local):
     kern_ev = {T: [new_events() for _ in range(args.steps)] for T in Ts}
     setup_s = time.time() - t_setup
 
-    ff, mx = args.fused_front, args.mx
+    ff, mx, fc = args.fused_front, args.mx, args.fused_combine
     if mx:
         layer.quantize_mx()
 
     def fwd(x, y, events=None):
         if mx:
             return layer.forward_mx(x, y, events=events)
-        return layer.forward(x, y, events=events, fused_front=ff)
+        return layer.forward(x, y, events=events, fused_front=ff, fused_combine=fc)
 
     def kpc(T):  # our kernels per layer call
-        if ff:
-            return 4
-        n = binding.kernels_per_call(T, H, wl["I"], wl["E"], wl["k"])
-        return n + 1 if mx else n  # MXFP8: + the activation quantize
+        call = (binding.MOE_CALL_FORWARD_MX if mx else binding.MOE_CALL_FORWARD_FUSED_FRONT if ff else
+                binding.MOE_CALL_FORWARD_FUSED_COMBINE if fc else binding.MOE_CALL_FORWARD)
+        return binding.kernels_per_call(T, H, wl["I"], wl["E"], wl["k"], call)
 
     def one_step(step_idx=None, per_kernel=False):
         for T in Ts:
@@ -608,6 +607,8 @@ def run_ours(args, wl, world, rank, local):
                                       else "bf16"),
                    "front_end": ("moe_forward_fused_front: norm .. gather in one cluster launch" if ff
                                  else "moe_forward: multi-launch front end"),
+                   "combine": ("moe_forward_fused_combine: in the down GEMM's epilogue" if fc
+                               else "separate kernel"),
                    "l2": "flushed before every layer call (256 MB write, then a 256 MB read of another buffer so "
                          "no dirty lines remain); flush outside the timed CUDA-event intervals",
                    "timing": "CUDA events on the launch stream around each plain moe_forward call; kernel times from "
@@ -641,7 +642,11 @@ def main():
                     help="time moe_forward_mx: MXFP8 expert weights and activations (decode shapes)")
     ap.add_argument("--fused-front", action="store_true",
                     help="time moe_forward_fused_front (norm .. gather in one cluster launch; T <= 64)")
+    ap.add_argument("--fused-combine", action="store_true",
+                    help="time moe_forward_fused_combine (the combine in the down GEMM's epilogue)")
     args = ap.parse_args()
+    if sum([args.mx, args.fused_front, args.fused_combine]) > 1:
+        ap.error("--mx, --fused-front and --fused-combine are separate entry points; pick one")
     if args.warmup < 3:
         print("bench: at least 3 warm-up steps are required; using 3", file=sys.stderr)
         args.warmup = 3

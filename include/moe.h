@@ -113,13 +113,14 @@ MOE_API moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const 
                        const moe_bf16* w2, moe_bf16* y, void* workspace, size_t workspace_bytes,
                        moe_stream_t stream);
 
-/* The kernels of one moe_forward call, in order:
+/* The steps of one moe_forward call, in order:
  *   1 RMSNorm + router logits, 2 top-k + softmax, 3 expert align, 4 gather,
  *   5 gate/up grouped GEMM + SwiGLU, 6 down grouped GEMM, 7 weighted combine.
  * For T <= MOE_FUSED_TOPK_MAX_T and E <= MOE_FUSED_TOPK_MAX_E, steps 2 and 3
- * run as one single-CTA kernel (6 launches per call); otherwise step 2 is one
- * multi-CTA kernel (top-k with per-block expert counts) and step 3 two (scan,
- * scatter), 8 launches per call. */
+ * run as one single-CTA kernel; otherwise step 2 is one multi-CTA kernel
+ * (top-k with per-block expert counts) and step 3 two (scan, scatter).
+ * So 6 launches per call (8 with the multi-CTA top-k and align);
+ * moe_kernels_per_call_of gives the count for each entry point. */
 #define MOE_NUM_KERNELS 7
 #define MOE_FUSED_TOPK_MAX_T 256
 #define MOE_FUSED_TOPK_MAX_E 256
@@ -127,6 +128,17 @@ MOE_API moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const 
 /* Number of kernels one moe_forward call with this shape launches on the
  * current device (0 for T = 0).  Host-only apart from querying the device. */
 MOE_API moe_status moe_kernels_per_call(const moe_shape* shape, int32_t* count);
+
+/* The same for each entry point: call = MOE_CALL_FORWARD (moe_forward,
+ * moe_forward_events, moe_forward_static_scratch), MOE_CALL_FORWARD_FUSED_FRONT
+ * (moe_forward_fused_front), MOE_CALL_FORWARD_MX (moe_forward_mx) or
+ * MOE_CALL_FORWARD_FUSED_COMBINE (moe_forward_fused_combine).  Another value
+ * of call: MOE_ERR_INVALID_ARG.  Host-only. */
+#define MOE_CALL_FORWARD 0
+#define MOE_CALL_FORWARD_FUSED_FRONT 1
+#define MOE_CALL_FORWARD_MX 2
+#define MOE_CALL_FORWARD_FUSED_COMBINE 3
+MOE_API moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t* count);
 
 /* moe_forward, plus CUDA events recorded on `stream` around the kernels:
  * events[0] before kernel 1 and events[i] right after kernel i (i = 1..7),
@@ -162,6 +174,27 @@ MOE_API moe_status moe_forward_fused_front(const moe_shape* shape, const moe_bf1
                                            const float* w_router, const float* router_bias, const moe_bf16* w13,
                                            const moe_bf16* w2, moe_bf16* y, void* workspace, size_t workspace_bytes,
                                            moe_stream_t stream, void* const* events, int32_t n_events);
+
+/* moe_forward with step 7 (the top-k weighted combine) in the epilogue of
+ * step 6, the down GEMM ("4 · La fusion de noyaux", §4.2 "GEMM + épilogue",
+ * with one counter per piece of output as in §4.2 "GEMM + GEMM"): a unit of
+ * the down GEMM that has stored its output rows of a 128-feature tile counts
+ * one arrival per routed row in a per-(tile, token) counter of the workspace
+ * (zeroed by the gather kernel), and the arrival that completes a token's k
+ * rows sums them in routing-slot order j = 0..k-1 into y, with the separate
+ * combine kernel's arithmetic: the same output bits as moe_forward, 5 launches
+ * (7 with the multi-CTA top-k and align).  No thread ever waits on a counter.
+ * `events` is NULL, or as for moe_forward_events (events[7] then follows
+ * events[6] at once).  moe_forward stays the faster choice on GB300: the
+ * epilogue's chain of store, fence, counter atomic and reads of the other
+ * rows is as long as the kernel boundary it saves in decode, and in prefill
+ * the epilogue waits on rows read back from DRAM and holds up the tensor
+ * cores. */
+MOE_API moe_status moe_forward_fused_combine(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                                             const float* w_router, const float* router_bias, const moe_bf16* w13,
+                                             const moe_bf16* w2, moe_bf16* y, void* workspace,
+                                             size_t workspace_bytes, moe_stream_t stream, void* const* events,
+                                             int32_t n_events);
 
 /* Routing front end only (RMSNorm, router, top-k, align with `pad_rows`
  * rows of padding granularity), with the results copied out:

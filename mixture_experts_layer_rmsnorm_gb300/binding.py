@@ -70,6 +70,7 @@ def load(build: bool = True):
             lib.moe_workspace_views.argtypes = [sp, p, sz, ctypes.POINTER(MoeViews)]
             lib.moe_device_status.argtypes = [p, sz, p, ctypes.POINTER(ctypes.c_int32)]
             lib.moe_kernels_per_call.argtypes = [sp, ctypes.POINTER(ctypes.c_int32)]
+            lib.moe_kernels_per_call_of.argtypes = [sp, i32, ctypes.POINTER(ctypes.c_int32)]
             lib.moe_selftest_wait_timeout.argtypes = [p, sz, i64, p]
             lib.moe_qk_norm.argtypes = [i64, i32, i32, i32, p, p, p, p, ctypes.c_float, ctypes.c_float, p]
             psz = ctypes.POINTER(sz)
@@ -79,13 +80,15 @@ def load(build: bool = True):
             lib.moe_workspace_views_mx.argtypes = [sp, p, sz, ctypes.POINTER(MoeViews), ctypes.POINTER(MoeMxViews)]
             lib.moe_forward_mx.argtypes = [sp, p, p, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_forward_fused_front.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
+            lib.moe_forward_fused_combine.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_status_string.argtypes = [ctypes.c_int]
             lib.moe_status_string.restype = ctypes.c_char_p
             for f in ("moe_workspace_size", "moe_forward", "moe_forward_events", "moe_route_debug",
                       "moe_workspace_views", "moe_device_status", "moe_forward_static_scratch",
-                      "moe_kernels_per_call", "moe_forward_fused_front", "moe_selftest_wait_timeout",
+                      "moe_kernels_per_call", "moe_kernels_per_call_of", "moe_forward_fused_front",
+                      "moe_selftest_wait_timeout",
                       "moe_qk_norm", "moe_mx_weight_sizes", "moe_mx_quantize_weights", "moe_workspace_size_mx",
-                      "moe_workspace_views_mx", "moe_forward_mx"):
+                      "moe_workspace_views_mx", "moe_forward_mx", "moe_forward_fused_combine"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -124,11 +127,20 @@ def moe_kernels_per_call(s: MoeShape) -> tuple[int, int]:
     return st, n.value
 
 
-def kernels_per_call(T: int, H: int, I: int, E: int, top_k: int) -> int:
-    """Kernel launches of one moe_forward call on the current device."""
-    st, n = moe_kernels_per_call(shape(T, H, I, E, top_k))
+MOE_CALL_FORWARD, MOE_CALL_FORWARD_FUSED_FRONT, MOE_CALL_FORWARD_MX, MOE_CALL_FORWARD_FUSED_COMBINE = 0, 1, 2, 3
+
+
+def moe_kernels_per_call_of(s: MoeShape, call: int) -> tuple[int, int]:
+    n = ctypes.c_int32(0)
+    st = load().moe_kernels_per_call_of(ctypes.byref(s), int(call), ctypes.byref(n))
+    return st, n.value
+
+
+def kernels_per_call(T: int, H: int, I: int, E: int, top_k: int, call: int = MOE_CALL_FORWARD) -> int:
+    """Kernel launches of one call of the entry point `call` (MOE_CALL_*)."""
+    st, n = moe_kernels_per_call_of(shape(T, H, I, E, top_k), call)
     if st != MOE_OK:
-        raise MoeError(st, "moe_kernels_per_call")
+        raise MoeError(st, "moe_kernels_per_call_of")
     return n
 
 
@@ -152,6 +164,17 @@ def moe_forward_fused_front(s: MoeShape, x, g_norm, w_router, router_bias, w13, 
         arr, n = (ctypes.c_void_p * len(events))(*events), len(events)
     return load().moe_forward_fused_front(ctypes.byref(s), x, g_norm, w_router, router_bias, w13, w2, y, workspace,
                                           workspace_bytes, stream, arr, n)
+
+
+def moe_forward_fused_combine(s: MoeShape, x, g_norm, w_router, router_bias, w13, w2, y, workspace,
+                              workspace_bytes, stream, events=None) -> int:
+    """moe_forward with the top-k weighted combine in the down GEMM's epilogue."""
+    if events is None:
+        arr, n = None, 0
+    else:
+        arr, n = (ctypes.c_void_p * len(events))(*events), len(events)
+    return load().moe_forward_fused_combine(ctypes.byref(s), x, g_norm, w_router, router_bias, w13, w2, y,
+                                            workspace, workspace_bytes, stream, arr, n)
 
 
 MOE_STATIC_SCRATCH_BYTES = 64 << 20
@@ -267,10 +290,12 @@ class MoeLayer:
             raise MoeError(st, "moe_workspace_size")
         return n
 
-    def forward(self, x, y=None, stream=None, events=None, fused_front=False):
+    def forward(self, x, y=None, stream=None, events=None, fused_front=False, fused_combine=False):
         """y = layer(x).  events: optional MOE_NUM_KERNELS + 1 cudaEvent_t handles
         recorded around the kernels (moe_forward_events).  fused_front: run the
-        norm .. gather steps as one cluster launch (moe_forward_fused_front)."""
+        norm .. gather steps as one cluster launch (moe_forward_fused_front).
+        fused_combine: the combine in the down GEMM's epilogue
+        (moe_forward_fused_combine)."""
         import torch
         T = x.shape[0]
         self.ensure_capacity(T)
@@ -279,8 +304,12 @@ class MoeLayer:
         s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
         args = (self.shape(T), _ptr(x), _ptr(self.g_norm), _ptr(self.w_router), _ptr(self.bias), _ptr(self.w13),
                 _ptr(self.w2), _ptr(y), _ptr(self.workspace), self.workspace_bytes(T), s)
+        if fused_front and fused_combine:
+            raise ValueError("fused_front and fused_combine are separate entry points")
         if fused_front:
             st = moe_forward_fused_front(*args, events)
+        elif fused_combine:
+            st = moe_forward_fused_combine(*args, events)
         elif events is None:
             st = moe_forward(*args)
         else:

@@ -78,12 +78,17 @@ __global__ void __launch_bounds__(kAlignThreads)
   }
 }
 
-// One warp per padded row; 8 rows per block of 256 threads.
+// One warp per padded row; 8 rows per block of 256 threads.  The grid also
+// zeroes clear[0, n_clear).
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ h, const int32_t* __restrict__ sorted_ids,
                                                      const int32_t* __restrict__ offsets, int E, int N, int k, int H,
-                                                     int64_t P_max, uint16_t* __restrict__ xg) {
+                                                     int64_t P_max, uint16_t* __restrict__ xg,
+                                                     int32_t* __restrict__ clear, int64_t n_clear) {
   pdl_wait();
   pdl_launch_dependents();
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n_clear;
+       i += static_cast<int64_t>(gridDim.x) * 256)
+    clear[i] = 0;
   const int64_t p = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (p >= P_max || p >= offsets[E]) return;
@@ -202,11 +207,11 @@ cudaError_t launch_align(const float* logits, int T, int k, int renorm, int32_t*
 
 
 cudaError_t launch_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets, int E, int N, int k,
-                          int H, int64_t P_max, uint16_t* xg, cudaStream_t stream) {
+                          int H, int64_t P_max, uint16_t* xg, int32_t* clear, int64_t n_clear, cudaStream_t stream) {
   const int64_t blocks = (P_max + 7) / 8;
   if (blocks == 0) return cudaSuccess;
   return launch_pdl(gather_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, h, sorted_ids, offsets, E,
-                    N, k, H, P_max, xg);
+                    N, k, H, P_max, xg, clear, n_clear);
 }
 
 cudaError_t launch_combine(const uint16_t* out_rows, const int32_t* slot_of, const float* topk_w, int T, int H, int k,

@@ -101,7 +101,7 @@ struct GemmCfg {
   static_assert(!(MX && PAIR) && (!MX || (BN % 32 == 0 && BN <= 128)), "MXFP8 units: one CTA, 32..128 tokens");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
   static_assert(kTmemNeed <= 512, "TMEM has 512 columns");
-  static_assert((2 * STAGES + 5) * 8 + 8 <= kBarBytes, "barrier area");
+  static_assert((2 * STAGES + 7) * 8 + 32 <= kBarBytes, "barrier area");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -180,6 +180,89 @@ __device__ __forceinline__ int64_t range_start(int64_t W, int cta, int ctas) { r
 
 __device__ __forceinline__ uint16_t f2bf(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
+// The four epilogue warps meet: each warp's lane 0 arrives on `bar` (count 4)
+// and every lane waits for the phase, bounded like every other wait.
+// Warp-uniform result; false when the wait ran out or the CTA is aborting.
+__device__ __forceinline__ bool epilogue_rendezvous(uint64_t* bar, uint32_t& phase, int lane,
+                                                    const volatile int* abort) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool got = mbar_wait(bar, phase, kWaitTimeoutNs, abort);
+  phase ^= 1u;
+  return __all_sync(0xFFFFFFFFu, got);
+}
+
+// The top-k weighted combine of the down GEMM, for the unit whose output rows
+// of weight tile `tile` (features [128 tile, +128)) this CTA has just stored:
+// the combine moves into the GEMM's epilogue ("4 · La fusion de noyaux", §4.2
+// "GEMM + épilogue"), ordered by one counter per piece of output (§4.2
+// "GEMM + GEMM"), here per (tile, token); nothing ever waits on a counter.
+// 1. Every epilogue thread fences its stores; the warps meet.
+// 2. Thread r takes unit rows r, r + 128: a real row of token t counts one
+//    arrival at combine_cnt[tile][t]; the arrival that makes it k marks the
+//    row in `mask` (every other row of t in this tile is then stored and
+//    visible: each was fenced before its own arrival).
+// 3. The warps meet; 8 groups of 16 threads finish the marked rows' tokens
+//    (group g: rows g, g + 8, ...), each thread 8 features:
+//    y = bf16(sum_j w_j * out_j) over j = 0..k-1 in order
+//    (fp32 fma from 0, the separate combine kernel's arithmetic), reading the
+//    rows through L2.  4. The warps meet again before the mask is reused.
+template <int BN>
+__device__ __noinline__ bool combine_unit(const ExpertGemmArgs& a, const Unit& un, int tile, int row, int lane,
+                                          uint64_t* bar, uint32_t& phase, uint32_t* mask, const volatile int* abort) {
+  const int T = a.n_routed / a.top_k;
+  __threadfence();
+  if (!epilogue_rendezvous(bar, phase, lane, abort)) return false;
+  int32_t* cnt = a.combine_cnt + static_cast<int64_t>(tile) * T;
+  for (int i = row; i < un.n; i += 128) {
+    const int sid = __ldg(a.sorted_ids + un.tok0 + i);
+    if (sid < a.n_routed && atomicAdd(cnt + sid / a.top_k, 1) == a.top_k - 1) atomicOr(mask + (i >> 5), 1u << (i & 31));
+  }
+  __threadfence();
+  if (!epilogue_rendezvous(bar, phase, lane, abort)) return false;
+  const int grp = row >> 4, chunk = row & 15;  // 8 groups x 16 chunks of 8 features
+  const int64_t col = static_cast<int64_t>(tile) * 128 + chunk * 8;
+  for (int i = grp; i < un.n; i += 8) {
+    if (!((mask[i >> 5] >> (i & 31)) & 1u)) continue;
+    const int t = __ldg(a.sorted_ids + un.tok0 + i) / a.top_k;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+    for (int j0 = 0; j0 < a.top_k; j0 += 8) {
+      uint4 v[8];
+      float wj[8];
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        if (j0 + d < a.top_k) {
+          const int64_t r = static_cast<int64_t>(t) * a.top_k + j0 + d;
+          wj[d] = __ldg(a.topk_w + r);
+          v[d] = __ldcg(reinterpret_cast<const uint4*>(a.out + static_cast<int64_t>(__ldg(a.slot_of + r)) * a.n_out + col));
+        }
+      }
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        if (j0 + d < a.top_k) {
+          const uint32_t wv[4] = {v[d].x, v[d].y, v[d].z, v[d].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[2 * e] = fmaf(wj[d], __uint_as_float(wv[e] << 16), acc[2 * e]);
+            acc[2 * e + 1] = fmaf(wj[d], __uint_as_float(wv[e] & 0xFFFF0000u), acc[2 * e + 1]);
+          }
+        }
+      }
+    }
+    uint4 o;
+    o.x = static_cast<uint32_t>(f2bf(acc[0])) | (static_cast<uint32_t>(f2bf(acc[1])) << 16);
+    o.y = static_cast<uint32_t>(f2bf(acc[2])) | (static_cast<uint32_t>(f2bf(acc[3])) << 16);
+    o.z = static_cast<uint32_t>(f2bf(acc[4])) | (static_cast<uint32_t>(f2bf(acc[5])) << 16);
+    o.w = static_cast<uint32_t>(f2bf(acc[6])) | (static_cast<uint32_t>(f2bf(acc[7])) << 16);
+    *reinterpret_cast<uint4*>(a.y + static_cast<int64_t>(t) * a.n_out + col) = o;
+  }
+  if (!epilogue_rendezvous(bar, phase, lane, abort)) return false;
+  if (row < BN / 32) mask[row] = 0;  // cleared before any thread marks rows of the next unit (next rendezvous)
+  return true;
+}
+
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
@@ -194,6 +277,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* cbar = done + 2;                                       // the epilogue warps' rendezvous (fused combine)
+  uint32_t* cmask = reinterpret_cast<uint32_t*>(cbar + 1);         // [8]: unit rows that complete a token
   int32_t* tab = reinterpret_cast<int32_t*>(smem + STAGES * C::kStageBytes + C::kBarBytes);  // [2][kTabMaxE+1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -231,6 +316,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tempty[b], PAIR ? 8 : 4);  // the epilogue warps (of both CTAs of a pair)
     }
     mbar_init(done, 1);
+    mbar_init(cbar, 4);  // one arrival per epilogue warp
+    for (int i = 0; i < 8; ++i) cmask[i] = 0;
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -465,6 +552,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const bool lo = lane < 16;
     // this CTA's partial-sum slot: [BN columns][128 rows] fp32
     float* my_slot = args.partials + static_cast<int64_t>(blockIdx.x) * BN * 128;
+    uint32_t cbar_phase = 0;  // uses of the combine rendezvous so far, mod 2
     const uint32_t tempty_cl = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
     Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
     int u, kb0, kb1;
@@ -557,6 +645,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
+      if (!SWIGLU && kb0 == 0 && args.fuse_combine) {
+        const int tile = PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile;
+        ok = combine_unit<BN>(args, un, tile, row, lane, cbar, cbar_phase, cmask, abort_flag);
+        if (!ok) break;
+      }
     }
     if (!ok && lane == 0) raise_timeout(args.err, abort_flag, kern);
   }

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(kFrontThreads, 1) front_kernel(const __grid_co
   pdl_launch_dependents();
   if (c == 0 && tid < 4) a.err[tid] = 0;
   for (int i = c * kFrontThreads + tid; i < a.n_flags; i += C * kFrontThreads) a.flags[i] = 0;
+  for (int i = c * kFrontThreads + tid; i < a.n_combine_cnt; i += C * kFrontThreads) a.combine_cnt[i] = 0;
 
   // ---- 1. norm + logits of this CTA's work items
   uint4* h_s = reinterpret_cast<uint4*>(fsm);

@@ -30,8 +30,9 @@ constexpr int kMaxDebugPad = 256;
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-  size_t err, h, logits, ids, w, counts, offsets, unit1, unit2, sorted, slot, flags, blk_counts, blk_base, partials, xg,
-      act, out, xs, aq, as, total;
+  size_t err, h, logits, ids, w, counts, offsets, unit1, unit2, sorted, slot, flags, ccnt, blk_counts, blk_base,
+      partials, xg, act, out, xs, aq, as, total;
+  int64_t n_ccnt;      // combine arrival counters of the down GEMM: [H / 128][T]
   int64_t P_max;       // padded rows: 16-row padding (bf16), 32-row padding rounded to 128 (MXFP8)
   int64_t sorted_cap;  // sorted_ids entries (room for debug padding up to 256)
 };
@@ -70,6 +71,8 @@ Layout make_layout(const moe_shape& s, bool mx = false) {
   L.slot = take(static_cast<size_t>(T * k * 4));
   // stream-K flags and partial sums of the expert GEMMs (slot = BN x 128 fp32 per CTA)
   L.flags = take(static_cast<size_t>(kGemmFlagInts) * 4);
+  L.n_ccnt = (H / 128) * T;
+  L.ccnt = take(static_cast<size_t>(L.n_ccnt) * 4);
   // per-block counts / bases of the multi-CTA align
   L.blk_counts = take(static_cast<size_t>((T + moe::kAlignTokPerBlk - 1) / moe::kAlignTokPerBlk) * E * 4);
   L.blk_base = take(static_cast<size_t>((T + moe::kAlignTokPerBlk - 1) / moe::kAlignTokPerBlk) * E * 4);
@@ -238,16 +241,30 @@ moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes) {
   return MOE_OK;
 }
 
-moe_status moe_kernels_per_call(const moe_shape* shape, int32_t* count) {
+moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t* count) {
   const moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
-  if (!count) return MOE_ERR_INVALID_ARG;
+  if (!count || call < MOE_CALL_FORWARD || call > MOE_CALL_FORWARD_FUSED_COMBINE) return MOE_ERR_INVALID_ARG;
   const moe_shape& s = *shape;
-  if (s.T == 0)
+  if (s.T == 0) {
     *count = 0;
+    return MOE_OK;
+  }
+  // router, top-k + align (1 kernel, or 3), gather, the two GEMMs, combine
+  const int front = 1 + (moe::align_fuses_topk(s.T, s.E) ? 1 : 3) + 1;
+  if (call == MOE_CALL_FORWARD)
+    *count = front + 3;
+  else if (call == MOE_CALL_FORWARD_FUSED_FRONT)
+    *count = 1 + 3;
+  else if (call == MOE_CALL_FORWARD_MX)
+    *count = front + 4;  // + the activation quantize between the GEMMs
   else
-    *count = moe::align_fuses_topk(s.T, s.E) ? 6 : 8;
+    *count = front + 2;  // the combine runs inside the down GEMM
   return MOE_OK;
+}
+
+moe_status moe_kernels_per_call(const moe_shape* shape, int32_t* count) {
+  return moe_kernels_per_call_of(shape, MOE_CALL_FORWARD, count);
 }
 
 moe_status moe_workspace_views(const moe_shape* shape, void* workspace, size_t workspace_bytes, moe_views* v) {
@@ -276,12 +293,24 @@ moe_status moe_workspace_views(const moe_shape* shape, void* workspace, size_t w
 
 namespace moe {
 
+// The down GEMM's arguments for the top-k weighted combine in its epilogue.
+void set_fused_combine(moe::ExpertGemmArgs& a, const moe_shape& s, const Layout& L, void* workspace, moe_bf16* y) {
+  a.fuse_combine = 1;
+  a.combine_cnt = at<int32_t>(workspace, L.ccnt);
+  a.sorted_ids = at<int32_t>(workspace, L.sorted);
+  a.slot_of = at<int32_t>(workspace, L.slot);
+  a.topk_w = at<float>(workspace, L.w);
+  a.y = reinterpret_cast<uint16_t*>(y);
+  a.top_k = s.top_k;
+  a.n_routed = s.T * s.top_k;
+}
+
 // The forward pass; when `events` is given, events[0] is recorded before the
 // first kernel and events[i] after the i-th of the seven kernels.
 moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
                         const float* router_bias, const moe_bf16* w13, const moe_bf16* w2, moe_bf16* y,
                         void* workspace, size_t workspace_bytes, moe_stream_t stream, void* const* events,
-                        bool single_launch_front) {
+                        bool single_launch_front, bool fused_combine) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   const moe_shape& s = *shape;
@@ -345,6 +374,8 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
     fa.err = err;
     fa.flags = at<int32_t>(workspace, L.flags);
     fa.n_flags = kGemmFlagInts;
+    fa.combine_cnt = at<int32_t>(workspace, L.ccnt);
+    fa.n_combine_cnt = fused_combine ? static_cast<int>(L.n_ccnt) : 0;
     fa.xg = at<uint16_t>(workspace, L.xg);
     if (moe::launch_front(fa, cs) != cudaSuccess || !mark(1) || !mark(2) || !mark(3) || !mark(4))
       return MOE_ERR_CUDA;
@@ -380,7 +411,8 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
     if (ce != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
     if (moe::launch_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
                            at<int32_t>(workspace, L.offsets), s.E, N, s.top_k, s.H, L.P_max,
-                           at<uint16_t>(workspace, L.xg), cs) != cudaSuccess ||
+                           at<uint16_t>(workspace, L.xg), at<int32_t>(workspace, L.ccnt),
+                           fused_combine ? L.n_ccnt : 0, cs) != cudaSuccess ||
         !mark(4))
       return MOE_ERR_CUDA;
   }
@@ -416,12 +448,14 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a2.flags = at<int32_t>(workspace, L.flags) + moe::kMaxGemmCtas * 4;        // two GEMMs may overlap
   a2.stream_k = plan == GemmPlan::kSmall;
   a2.pair = moe::gemm_uses_pairs(plan, tiles2);
+  if (fused_combine) set_fused_combine(a2, s, L, workspace, y);
   if (moe::launch_gemm_down(tm_w2, tm_act, a2, plan, num_sms, cs) != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
 
-  if (moe::launch_combine(at<uint16_t>(workspace, L.out), at<int32_t>(workspace, L.slot), at<float>(workspace, L.w),
-                          s.T, s.H, s.top_k, y, cs) != cudaSuccess ||
-      !mark(7))
+  if (!fused_combine &&
+      moe::launch_combine(at<uint16_t>(workspace, L.out), at<int32_t>(workspace, L.slot), at<float>(workspace, L.w),
+                          s.T, s.H, s.top_k, y, cs) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (!mark(7)) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
@@ -624,6 +658,19 @@ moe_status moe_forward_fused_front(const moe_shape* shape, const moe_bf16* x, co
   }
   return moe::forward_impl(shape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes, stream,
                            events, true);
+}
+
+moe_status moe_forward_fused_combine(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                                     const float* w_router, const float* router_bias, const moe_bf16* w13,
+                                     const moe_bf16* w2, moe_bf16* y, void* workspace, size_t workspace_bytes,
+                                     moe_stream_t stream, void* const* events, int32_t n_events) {
+  if (events) {
+    if (n_events < MOE_NUM_KERNELS + 1) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i <= MOE_NUM_KERNELS; ++i)
+      if (!events[i]) return MOE_ERR_INVALID_ARG;
+  }
+  return moe::forward_impl(shape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes, stream,
+                           events, false, true);
 }
 
 moe_status moe_route_debug(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,

@@ -76,6 +76,8 @@ struct FrontArgs {
   int32_t* err;
   int32_t* flags;  // the expert GEMMs' stream-K flags: zeroed
   int n_flags;
+  int32_t* combine_cnt;  // the down GEMM's combine arrival counters: zeroed
+  int n_combine_cnt;
   uint16_t* xg;
   // set by the launcher: router work items = token tiles x expert groups
   int n_items, groups, experts_per_item;
@@ -84,9 +86,11 @@ struct FrontArgs {
 bool front_fits(int T, int H, int E, int k);
 cudaError_t launch_front(const FrontArgs& a, cudaStream_t stream);
 
-// K3: xg[p,:] = h[sorted_ids[p] / k, :] for real rows, zeros for padding rows.
+// K3: xg[p,:] = h[sorted_ids[p] / k, :] for real rows, zeros for padding rows;
+// also zeroes clear[0, n_clear) (the down GEMM's combine arrival counters).
 cudaError_t launch_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets, int E, int N,
-                          int k, int H, int64_t P_max, uint16_t* xg, cudaStream_t stream);
+                          int k, int H, int64_t P_max, uint16_t* xg, int32_t* clear, int64_t n_clear,
+                          cudaStream_t stream);
 
 // K4 / K5: grouped expert GEMMs on tcgen05.  Weights are the MMA's A operand
 // (128 weight rows per tile), the tokens of one expert its B operand.  The
@@ -110,6 +114,20 @@ struct ExpertGemmArgs {
   int tables_from_parent;   // 1: the routing tables come from the previous kernel (wait before reading)
   const uint8_t* w_scales;  // MXFP8 GEMMs: weight scales (512-byte tiles per 128 rows x 128 of K)
   const uint8_t* x_scales;  // MXFP8 GEMMs: token scales, one 512-byte tile per token chunk and 128 of K
+  // Down GEMM with the top-k weighted combine in its epilogue (fuse_combine = 1):
+  // a unit that has stored its output rows of a 128-feature tile counts one
+  // arrival per real row at combine_cnt[tile * T + t]; the arrival that
+  // completes token t's k rows writes y[t, tile] = bf16(sum_j topk_w[t,j] *
+  // out[slot_of[t*k+j], tile]) in j order, from the bf16 rows, with the
+  // arithmetic of the separate combine kernel.
+  int fuse_combine;
+  int32_t* combine_cnt;       // [n_out / 128][T] ints, zero on entry
+  const int32_t* sorted_ids;  // [P] flat routing index t*k+j of each row; >= n_routed: padding
+  const int32_t* slot_of;     // [T*k] row of each routed token
+  const float* topk_w;        // [T*k]
+  uint16_t* y;                // [T, n_out] bf16
+  int top_k;
+  int n_routed;               // T*k
 };
 // persistent GEMM grid: min(SM count, kMaxGemmCtas) CTAs
 constexpr int kMaxGemmCtas = 256;

@@ -53,11 +53,21 @@ def test_kernels_per_call_host_checks():
     assert st == binding.MOE_OK and n == 0
     st, _ = binding.moe_kernels_per_call(binding.shape(4, 100, 256, 8, 2))
     assert st == binding.MOE_ERR_UNSUPPORTED
-    # any device (or none): one of the three launch plans
+    # small T: norm/router, top-k + align, gather, the two GEMMs, combine;
+    # large T: the top-k and align take three kernels
     st, n = binding.moe_kernels_per_call(binding.shape(4, 128, 256, 8, 2))
-    assert st == binding.MOE_OK and n in (4, 6, 8)
+    assert st == binding.MOE_OK and n == 6
     st, n = binding.moe_kernels_per_call(binding.shape(4096, 128, 256, 8, 2))
     assert st == binding.MOE_OK and n == 8
+    s4 = binding.shape(4, 128, 256, 8, 2)
+    assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD) == (binding.MOE_OK, 6)
+    assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_FUSED_FRONT) == (binding.MOE_OK, 4)
+    assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_MX) == (binding.MOE_OK, 7)
+    assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_FUSED_COMBINE) == (binding.MOE_OK, 5)
+    s4096 = binding.shape(4096, 128, 256, 8, 2)
+    assert binding.moe_kernels_per_call_of(s4096, binding.MOE_CALL_FORWARD_FUSED_COMBINE) == (binding.MOE_OK, 7)
+    assert binding.moe_kernels_per_call_of(s4, 4)[0] == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_kernels_per_call_of(s4, -1)[0] == binding.MOE_ERR_INVALID_ARG
 
 
 def test_selftest_wait_timeout_rejects_bad_arguments_without_a_gpu():

@@ -90,6 +90,26 @@ def test_fused_front_parity(case, o):
     assert np.array_equal(g["slot"], ref["slot"])
 
 
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_fused_combine_parity(case, o):
+    """The combine in the down GEMM's epilogue: the same output bits as the
+    separate combine kernel (same rows, same order, same fp32 arithmetic), so
+    within the oracle's tolerance too; and the same bits on a second call
+    (arrival counters are zeroed per call)."""
+    _, T, H, I, E, k, renorm, zipf, seed = case
+    li = _layer_inputs(T, H, I, E, k, renorm, zipf, seed)
+    dl = gu.DeviceLayer(li)
+    ref = dl.run(li.x)
+    xd = gu.dev_bf16(li.x)
+    for _ in range(2):
+        y = dl.layer.forward(xd, fused_combine=True)
+        torch.cuda.synchronize()
+        st, det = dl.layer.device_status(T)
+        assert st == binding.MOE_OK, (st, det)
+        assert np.array_equal(y.cpu().numpy().view(np.uint16), ref["y"]), "fused combine differs from the kernel"
+    gu.check_output(o, li, li.x, ref["y"])
+
+
 def test_fused_front_rejects_large_batches():
     li = _layer_inputs(80, 128, 128, 4, 2, True, None, 0)
     dl = gu.DeviceLayer(li)
