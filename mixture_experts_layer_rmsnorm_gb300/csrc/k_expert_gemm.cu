@@ -729,8 +729,10 @@ constexpr int kPairStages[2] = {7, 7};  // gate/up, down: stages of 32 KB
 // nothing); large units hold up to 256 (128-row boxes: 8x fewer TMA requests)
 constexpr int kTokBox[3] = {16, 16, 128};
 
-// MXFP8 decode plans: 32-token units, 10 stages of 22 KB; 64-token units, 8 of 26 KB
-constexpr int kMxStages[2] = {10, 8};
+// MXFP8 plans (one CTA per unit): 32-token units, 10 stages of 22 KB; 64-token
+// units, 8 of 26 KB; prefill: 128-token units, 6 of 33 KB (TMEM: two 128-column
+// accumulators + 6 x 32 scale columns)
+constexpr int kMxBn[3] = {32, 64, 128}, kMxStages[3] = {10, 8, 6};
 
 }  // namespace
 
@@ -738,13 +740,14 @@ cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap&
                                    GemmPlan plan, int num_sms, cudaStream_t stream) {
   switch (plan) {
     case GemmPlan::kSmall:
-      return launch_expert_gemm<true, kGateUpBn[0], kMxStages[0], kTokBox[0], false, true>(tm_w13, tm_x, a, num_sms,
-                                                                                            stream);
+      return launch_expert_gemm<true, kMxBn[0], kMxStages[0], kTokBox[0], false, true>(tm_w13, tm_x, a, num_sms,
+                                                                                        stream);
     case GemmPlan::kMid:
-      return launch_expert_gemm<true, kGateUpBn[1], kMxStages[1], kTokBox[1], false, true>(tm_w13, tm_x, a, num_sms,
-                                                                                            stream);
+      return launch_expert_gemm<true, kMxBn[1], kMxStages[1], kTokBox[1], false, true>(tm_w13, tm_x, a, num_sms,
+                                                                                        stream);
     default:
-      return cudaErrorNotSupported;
+      return launch_expert_gemm<true, kMxBn[2], kMxStages[2], kTokBox[2], false, true>(tm_w13, tm_x, a, num_sms,
+                                                                                        stream);
   }
 }
 
@@ -752,15 +755,18 @@ cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_
                                 GemmPlan plan, int num_sms, cudaStream_t stream) {
   switch (plan) {
     case GemmPlan::kSmall:
-      return launch_expert_gemm<false, kDownBn[0], kMxStages[0], kTokBox[0], false, true>(tm_w2, tm_act, a, num_sms,
-                                                                                           stream);
+      return launch_expert_gemm<false, kMxBn[0], kMxStages[0], kTokBox[0], false, true>(tm_w2, tm_act, a, num_sms,
+                                                                                         stream);
     case GemmPlan::kMid:
-      return launch_expert_gemm<false, kDownBn[1], kMxStages[1], kTokBox[1], false, true>(tm_w2, tm_act, a, num_sms,
-                                                                                           stream);
+      return launch_expert_gemm<false, kMxBn[1], kMxStages[1], kTokBox[1], false, true>(tm_w2, tm_act, a, num_sms,
+                                                                                         stream);
     default:
-      return cudaErrorNotSupported;
+      return launch_expert_gemm<false, kMxBn[2], kMxStages[2], kTokBox[2], false, true>(tm_w2, tm_act, a, num_sms,
+                                                                                         stream);
   }
 }
+
+int gemm_bn_mx(GemmPlan plan) { return kMxBn[static_cast<int>(plan)]; }
 
 int gemm_gate_up_bn(GemmPlan plan) { return kGateUpBn[static_cast<int>(plan)]; }
 int gemm_down_bn(GemmPlan plan) { return kDownBn[static_cast<int>(plan)]; }

@@ -470,7 +470,7 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   const moe_shape& s = *shape;
   if (s.T == 0) return MOE_OK;
   const GemmPlan plan = moe::choose_plan(s.T, s.top_k, s.E);
-  if (plan == GemmPlan::kLarge || s.E > 256) return MOE_ERR_UNSUPPORTED;
+  if (s.E > 256) return MOE_ERR_UNSUPPORTED;
   st = check_inputs(shape, x, g_norm, w_router, router_bias, workspace, workspace_bytes, true);
   if (st != MOE_OK) return st;
   if (!w13c || !w13s || !w2c || !w2s || !y || !aligned(w13c, 16) || !aligned(w13s, 16) || !aligned(w2c, 16) ||
@@ -480,7 +480,7 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   const int num_sms = num_sms_of_current_device();
   if (num_sms <= 0) return MOE_ERR_CUDA;
   const Layout L = make_layout(s, true);
-  const int bn1 = moe::gemm_gate_up_bn(plan), bn2 = moe::gemm_down_bn(plan);
+  const int bn1 = moe::gemm_bn_mx(plan), bn2 = bn1;
   const int tiles1 = s.I / moe::kGateUpTileFeat, tiles2 = s.H / moe::kDownTileFeat;
   auto mark = [&](int i) {
     return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), cs) == cudaSuccess;

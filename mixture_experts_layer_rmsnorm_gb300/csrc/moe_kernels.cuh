@@ -150,8 +150,8 @@ cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act
 // the tiles per expert its work-unit table counts (pairs of tiles then).
 bool gemm_uses_pairs(GemmPlan plan, int tiles);
 int gemm_unit_tiles(GemmPlan plan, int tiles);
-// The same GEMMs on MXFP8 operands (block-scaled tcgen05 MMA; decode tile
-// plans only: kSmall or kMid).  tm_w / tm_x map E4M3 codes (one byte per
+// The same GEMMs on MXFP8 operands (block-scaled tcgen05 MMA; one CTA per
+// unit in every plan, gemm_bn_mx(plan) tokens per unit).  tm_w / tm_x map E4M3 codes (one byte per
 // element); a.w_scales / a.x_scales hold the E8M0 scales.
 cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
                                    GemmPlan plan, int num_sms, cudaStream_t stream);
@@ -162,6 +162,7 @@ cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_
 constexpr int kPadRowsMx = 32;
 // token rows per unit (B-operand width) and rows per TMA box of the token tile
 int gemm_gate_up_bn(GemmPlan plan);
+int gemm_bn_mx(GemmPlan plan);  // token rows per unit of both MXFP8 GEMMs
 int gemm_down_bn(GemmPlan plan);
 int gemm_tok_box_rows(GemmPlan plan);
 constexpr int kWeightBoxRows = 128;  // A-operand rows of one unit (one MMA's M)

@@ -24,6 +24,10 @@ CASES = [
     ("mx_mid_multichunk", 200, 256, 256, 8, 2, True, None, 9),
     ("mx_bias_norenorm", 3, 384, 256, 20, 5, False, 1.2, 14),
     ("mx_deep_k", 64, 1024, 512, 8, 2, True, None, 2),
+    # prefill plan: 128-token units, several chunks per expert, ragged tails
+    ("mx_prefill_chunks", 1024, 256, 256, 4, 2, True, None, 4),
+    ("mx_prefill_ragged_norenorm", 300, 384, 128, 6, 3, False, None, 5),
+    ("mx_prefill_skewed", 512, 256, 256, 16, 4, True, 1.2, 11),
 ]
 
 
@@ -72,7 +76,7 @@ def test_mx_layer_parity(case, o):
     gu.check_routing(o, li, li.x, g, pad=32)
     # gathered token rows: codes and scales bit for bit on the real rows; the
     # scales are grouped by the GEMMs' token chunks (bn rows of an expert)
-    bn = 32 if T * k <= 16 * E else 64
+    bn = 32 if T * k <= 16 * E else 64 if T * k <= 64 * E else 128  # the GEMMs' token rows per unit
     n_chunks = v.P_max // 32
     xcodes = view(mv.x_codes, torch.uint8, (v.P_max, H))
     xs = gu.ungroup_mx_scales(view(mv.x_scales, torch.uint8, (n_chunks * (H // 128) * 512,)), n_chunks * 128, H)
@@ -94,8 +98,8 @@ def test_mx_layer_parity(case, o):
     assert np.abs(err).max() <= gu.MAX_ABS_TOL
 
 
-def test_mx_rejects_prefill_plan():
-    cfg = inputs.LayerConfig(T=512, H=128, I=128, E=4, top_k=2, seed=0)
+def test_mx_rejects_more_than_256_experts():
+    cfg = inputs.LayerConfig(T=4, H=128, I=128, E=300, top_k=2, seed=0)
     li = inputs.make_layer_inputs(cfg)
     dl = gu.DeviceLayer(li)
     dl.layer.quantize_mx()
