@@ -563,7 +563,8 @@ def run_ours(args, wl, world, rank, local):
             roof = roofline("tensor", sum(per) / len(per), avg_s, 2.0 * peaks["bf16_tflops"], None)
             roof["peak_source"] = f"2 x bf16_tflops ({peak_kind}; nominal dense fp8 / bf16 ratio)"
         else:
-            roof = roofline("tensor", sum(per) / len(per), avg_s, peaks["bf16_tflops"], None)
+            roof = roofline("tensor", sum(per) / len(per), avg_s, peaks["bf16_tflops"],
+                            ncu_traffic_per_launch(dom, args.workload))
             roof["peak_source"] = f"bf16_tflops ({peak_kind})"
     else:
         if dom == "gemm_gate_up_swiglu":
