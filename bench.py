@@ -57,6 +57,9 @@ WORKLOADS = {
                        label="ncu case: T=64, H=I=4096, E=16, top_k=8 (decode tiles, 32 tokens/expert)"),
     "router_ncu": dict(H=4096, I=256, E=64, k=8, Ts=[1, 64], seed=0, zipf=None,
                        label="ncu case: router of the decode layer (H=4096, E=64) with small experts (I=256)"),
+    "router_prefill_ncu": dict(H=4096, I=256, E=64, k=8, Ts=[4096], seed=0, zipf=None,
+                               label="ncu case: router of the prefill layer (T=4096, H=4096, E=64) with small "
+                                     "experts (I=256)"),
     "t1_ncu": dict(H=4096, I=4096, E=8, k=8, Ts=[1], seed=0, zipf=None,
                    label="ncu case: T=1, H=I=4096, E=8, top_k=8 (all 8 experts touched, as decode T=1)"),
     "prefill_ncu": dict(H=4096, I=4096, E=8, k=8, Ts=[512], seed=0, zipf=None,
