@@ -80,15 +80,22 @@ struct GemmCfg {
   static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * kTokRowBytes;
   // MXFP8: one byte per element, so a 128-byte row holds 128 elements of K;
   // each stage also carries its scale tiles: 512 bytes for the 128 weight rows
-  // and 512 for the unit's token chunk
+  // and 512 per 128 token rows of the unit's token chunk (a CTA of a pair needs
+  // the scales of all 256 tokens: the pair MMA reads them from its own TMEM)
   static constexpr int kKPerStage = MX ? 128 : kBlockK;
-  static constexpr int kSfBytes = MX ? 2 * 512 : 0;
+  static constexpr int kSfTokBytes = MX ? (BN > 128 ? 1024 : 512) : 0;
+  static constexpr int kSfBytes = MX ? 512 + kSfTokBytes : 0;
   static constexpr int kStageBytes = (kABytes + kBBytes + kSfBytes + 1023) / 1024 * 1024;
   static constexpr int kAccCols = BN;  // fp32 TMEM columns per accumulator buffer
-  // TMEM columns of one stage's scales: weight scales at +0, token scales at
-  // +16 (4 columns each; slots of 32 keep both addresses 16-column aligned)
+  // accumulator buffers: two (the epilogue of one unit overlaps the MMAs of the
+  // next); one for MXFP8 pairs, whose 256 columns leave no room for a second
+  // next to the scale slots
+  static constexpr int kAccBufs = (MX && PAIR) ? 1 : 2;
+  // TMEM columns of one stage's scales: weight scales at +0 (4 columns), token
+  // scales at +16 (4 columns per 128 tokens); slots of 32 keep both addresses
+  // 16-column aligned
   static constexpr int kSfCols = MX ? 32 : 0;
-  static constexpr int kTmemNeed = 2 * kAccCols + STAGES * kSfCols;
+  static constexpr int kTmemNeed = kAccBufs * kAccCols + STAGES * kSfCols;
   static constexpr uint32_t kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                         : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kBarBytes = 512;
@@ -98,7 +105,8 @@ struct GemmCfg {
   static constexpr int kFeatPerTile = SWIGLU ? kGateUpTileFeat : kDownTileFeat;  // output features per unit
   static_assert(BN % TOKBOX == 0 && TOKBOX % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
   static_assert(!PAIR || (BN / 2) % TOKBOX == 0, "token boxes of a CTA pair");
-  static_assert(!(MX && PAIR) && (!MX || (BN % 32 == 0 && BN <= 128)), "MXFP8 units: one CTA, 32..128 tokens");
+  static_assert(!MX || (PAIR ? BN == 256 : (BN % 32 == 0 && BN <= 128)),
+                "MXFP8 units: one CTA with 32..128 tokens, or a CTA pair with 256");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
   static_assert(kTmemNeed <= 512, "TMEM has 512 columns");
   static_assert((2 * STAGES + 7) * 8 + 32 <= kBarBytes, "barrier area");
@@ -266,6 +274,7 @@ __device__ __noinline__ bool combine_unit(const ExpertGemmArgs& a, const Unit& u
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                       const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_sx,
                        const ExpertGemmArgs args) {
   using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>;
   extern __shared__ uint8_t smem_raw[];
@@ -384,9 +393,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint8_t* sb = smem + st * C::kStageBytes + kABytes;
         for (int r = 0; r < rows; r += TOKBOX)
           load_2d(sb + r * kTokRowBytes, &tm_x, st, kb * C::kKPerStage, tok0 + r, pol_x);
-        if (MX)
+        if (MX && PAIR) {
+          // both 512-byte scale tiles of the 256-token chunk, in each CTA (tensor
+          // map tm_sx: one tile = a box of 2 rows x 256 bytes)
+          for (int h = 0; h < 2; ++h)
+            load_2d(sb + C::kBBytes + 512 + 512 * h, &tm_sx, st, 0,
+                    2 * ((2 * chunk + h) * kblocks + kb), pol_x);
+        } else if (MX) {
           bulk_load(sb + C::kBBytes + 512, args.x_scales + (static_cast<size_t>(chunk) * kblocks + kb) * 512, 512,
                     &full[st], pol_x);
+        }
       };
       auto resolve_deps = [&]() {
         pdl_wait();
@@ -427,10 +443,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else {
             load_2d(sa, &tm_w, stage, kb * C::kKPerStage, wrow, pol_w);
           }
-          if (MX)  // the weight tile's scales (static: loaded before the parent kernel ends)
-            bulk_load(sa + kABytes + C::kBBytes,
-                      args.w_scales + (static_cast<size_t>(un.e * args.tiles_per_expert + tile) * kblocks + kb) * 512,
-                      512, &full[stage], pol_w);
+          if (MX) {  // the weight tile's scales (static: loaded before the parent kernel ends)
+            const int wtiles = PAIR ? 2 * args.tiles_per_expert : args.tiles_per_expert;  // 128-row tiles per expert
+            const int64_t wt = static_cast<int64_t>(un.e * wtiles + tile) * kblocks + kb;
+            if (PAIR)
+              load_2d(sa + kABytes + C::kBBytes, &tm_sw, stage, 0, static_cast<int>(2 * wt), pol_w);
+            else
+              bulk_load(sa + kABytes + C::kBBytes, args.w_scales + static_cast<size_t>(wt) * 512, 512, &full[stage],
+                        pol_w);
+          }
           if (deps_ready) {
             load_tokens(stage, kb, tok_first, tok_rows, chunk);
           } else {
@@ -492,16 +513,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sb = sa + kABytes;
           if (MX) {
             // this stage's scales into its TMEM columns, then 4 MMAs of K = 32
-            const uint32_t sf_t = tmem_base + static_cast<uint32_t>(2 * C::kAccCols + stage * C::kSfCols);
+            // (a pair: each CTA's own tiles into its own TMEM, by one copy)
+            const uint32_t sf_t =
+                tmem_base + static_cast<uint32_t>(C::kAccBufs * C::kAccCols + stage * C::kSfCols);
             const uint32_t sf_s = sb + C::kBBytes;
-            tmem_cp_32x128b_x4(sf_t, sf_s);
-            tmem_cp_32x128b_x4(sf_t + 16, sf_s + 512);
             const uint32_t sfb_t = sf_t + 16;
+            if (PAIR) {
+              tmem_cp_32x128b_x4_pair(sf_t, sf_s);
+              tmem_cp_32x128b_x4_pair(sfb_t, sf_s + 512);      // tokens 0..127: columns +0..+3
+              tmem_cp_32x128b_x4_pair(sfb_t + 4, sf_s + 1024);  // tokens 128..255: columns +4..+7
+            } else {
+              tmem_cp_32x128b_x4(sf_t, sf_s);
+              tmem_cp_32x128b_x4(sfb_t, sf_s + 512);
+            }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-              mma_mxf8_ss(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32),
-                          idesc_mxf8(128, static_cast<uint32_t>(n_mma), k, k), sf_t, sfb_t, accum);
+              const uint32_t id = idesc_mxf8(PAIR ? 256 : 128, static_cast<uint32_t>(n_mma), k, k);
+              if (PAIR)
+                mma_mxf8_ss_pair(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), id, sf_t,
+                                 sfb_t, accum);
+              else
+                mma_mxf8_ss(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), id, sf_t, sfb_t,
+                            accum);
             }
           } else {
 #pragma unroll
@@ -528,8 +562,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mma_commit_pair_mc(&tfull[acc], 0x3);
         else
           mma_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == C::kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       if (!ok) raise_timeout(args.err, abort_flag, kern);
       // all MMAs this thread issued have finished before TMEM is released
@@ -643,8 +679,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         else
           mbar_arrive(&tempty[acc]);
       }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
+      if (++acc == C::kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
       if (!SWIGLU && kb0 == 0 && args.fuse_combine) {
         const int tile = PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile;
         ok = combine_unit<BN>(args, un, tile, row, lane, cbar, cbar_phase, cmask, abort_flag);
@@ -669,7 +707,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false>
 cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, int num_sms,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const CUtensorMap* tsw = nullptr,
+                               const CUtensorMap* tsx = nullptr) {
+  static const CUtensorMap kNoMap = {};  // the scale maps of MXFP8 pairs; unused elsewhere
   using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>;
   auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>;
   static int configured_device = -1;
@@ -713,7 +753,7 @@ cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, con
   cfg.gridDim = dim3(grid);
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tw, tx, a);
+  return cudaLaunchKernelEx(&cfg, kernel, tw, tx, tsw ? *tsw : kNoMap, tsx ? *tsx : kNoMap, a);
 }
 
 // Three tile plans by the expected tokens per expert (T*top_k/E):
@@ -729,15 +769,19 @@ constexpr int kPairStages[2] = {7, 7};  // gate/up, down: stages of 32 KB
 // nothing); large units hold up to 256 (128-row boxes: 8x fewer TMA requests)
 constexpr int kTokBox[3] = {16, 16, 128};
 
-// MXFP8 plans (one CTA per unit): 32-token units, 10 stages of 22 KB; 64-token
-// units, 8 of 26 KB; prefill: 128-token units, 6 of 33 KB (TMEM: two 128-column
-// accumulators + 6 x 32 scale columns)
+// MXFP8 plans: one CTA per unit of 32 tokens (10 stages of 22 KB), 64 tokens
+// (8 of 26 KB) or, in prefill, 128 tokens (6 of 33 KB; TMEM: two 128-column
+// accumulators + 6 x 32 scale columns); prefill on CTA pairs when the weight
+// tiles come in pairs: 256-token units, 6 stages of 34 KB per CTA (one
+// 256-column accumulator + 6 x 32 scale columns)
 constexpr int kMxBn[3] = {32, 64, 128}, kMxStages[3] = {10, 8, 6};
+constexpr int kMxPairStages = 6;
 
 }  // namespace
 
-cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
-                                   GemmPlan plan, int num_sms, cudaStream_t stream) {
+cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const CUtensorMap& tm_sw,
+                                   const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
+                                   cudaStream_t stream) {
   switch (plan) {
     case GemmPlan::kSmall:
       return launch_expert_gemm<true, kMxBn[0], kMxStages[0], kTokBox[0], false, true>(tm_w13, tm_x, a, num_sms,
@@ -746,13 +790,17 @@ cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap&
       return launch_expert_gemm<true, kMxBn[1], kMxStages[1], kTokBox[1], false, true>(tm_w13, tm_x, a, num_sms,
                                                                                         stream);
     default:
+      if (a.pair)
+        return launch_expert_gemm<true, 256, kMxPairStages, kTokBox[2], true, true>(tm_w13, tm_x, a, num_sms, stream,
+                                                                                    &tm_sw, &tm_sx);
       return launch_expert_gemm<true, kMxBn[2], kMxStages[2], kTokBox[2], false, true>(tm_w13, tm_x, a, num_sms,
                                                                                         stream);
   }
 }
 
-cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const ExpertGemmArgs& a,
-                                GemmPlan plan, int num_sms, cudaStream_t stream) {
+cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const CUtensorMap& tm_sw,
+                                const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
+                                cudaStream_t stream) {
   switch (plan) {
     case GemmPlan::kSmall:
       return launch_expert_gemm<false, kMxBn[0], kMxStages[0], kTokBox[0], false, true>(tm_w2, tm_act, a, num_sms,
@@ -761,12 +809,15 @@ cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_
       return launch_expert_gemm<false, kMxBn[1], kMxStages[1], kTokBox[1], false, true>(tm_w2, tm_act, a, num_sms,
                                                                                          stream);
     default:
+      if (a.pair)
+        return launch_expert_gemm<false, 256, kMxPairStages, kTokBox[2], true, true>(tm_w2, tm_act, a, num_sms,
+                                                                                     stream, &tm_sw, &tm_sx);
       return launch_expert_gemm<false, kMxBn[2], kMxStages[2], kTokBox[2], false, true>(tm_w2, tm_act, a, num_sms,
                                                                                          stream);
   }
 }
 
-int gemm_bn_mx(GemmPlan plan) { return kMxBn[static_cast<int>(plan)]; }
+int gemm_bn_mx(GemmPlan plan, bool pair) { return pair ? 256 : kMxBn[static_cast<int>(plan)]; }
 
 int gemm_gate_up_bn(GemmPlan plan) { return kGateUpBn[static_cast<int>(plan)]; }
 int gemm_down_bn(GemmPlan plan) { return kDownBn[static_cast<int>(plan)]; }

@@ -20,9 +20,10 @@
 // W2 keeps its row index.  Token rows (gathered inputs, activations) are
 // grouped by the expert GEMMs' token chunks instead: the rows
 // [offsets[e] + c*bn, +bn) of expert e form chunk unit_off[e] / tiles + c, and
-// its scales one 512-byte tile per 128 elements of K with byte r*16 + 4*j + b
-// for row offsets[e] + c*bn + 32*j + r (bn <= 128, offsets multiples of 32), so
-// that a unit's token scales start at TMEM column 0.
+// its scales ceil(bn / 128) 512-byte tiles per 128 elements of K, tile h with
+// byte r*16 + 4*j + b for row offsets[e] + c*bn + 128*h + 32*j + r (bn <= 128,
+// or 256 for CTA-pair units; offsets multiples of 32), so that a unit's token
+// scales start at TMEM column 0.
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -59,7 +60,8 @@ __device__ __forceinline__ size_t scale_offset(int64_t R, int kb, int K) {
 }
 
 // Token row p (< offsets[E]) -> chunk-relative scale position: the "scale row"
-// chunk * 128 + 32 * j + r, so that scale_offset() lands in the chunk's tile.
+// chunk * 128 * G + in_chunk with G = ceil(bn / 128) tiles per chunk, so that
+// scale_offset() lands in tile G * chunk + in_chunk / 128.
 __device__ __forceinline__ int64_t token_scale_row(int p, const int32_t* offsets, const int32_t* unit_off, int E,
                                                    int tiles, int bn) {
   int lo = 0, hi = E;
@@ -73,7 +75,7 @@ __device__ __forceinline__ int64_t token_scale_row(int p, const int32_t* offsets
   const int within = p - __ldcg(offsets + lo);
   const int c = within / bn, in_chunk = within - c * bn;
   const int64_t chunk = __ldcg(unit_off + lo) / tiles + c;
-  return chunk * 128 + in_chunk;  // in_chunk = 32 * j + r
+  return chunk * 128 * ((bn + 127) / 128) + in_chunk;  // in_chunk % 128 = 32 * j + r
 }
 
 // One warp per row.  MODE 0: rows of a matrix (W2); MODE 1: gathered token

@@ -81,9 +81,9 @@ Layout make_layout(const moe_shape& s, bool mx = false) {
   L.act = take(static_cast<size_t>(L.P_max * I * 2));
   L.out = take(static_cast<size_t>(L.P_max * H * 2));
   if (mx) {  // token scales per token chunk: at most P_max / 32 chunks (each >= 32 rows)
-    L.xs = take(static_cast<size_t>(L.P_max / 32) * (H / 128) * 512);
+    L.xs = take(static_cast<size_t>(L.P_max / 32) * 2 * (H / 128) * 512);
     L.aq = take(static_cast<size_t>(L.P_max * I));
-    L.as = take(static_cast<size_t>(L.P_max / 32) * (I / 128) * 512);
+    L.as = take(static_cast<size_t>(L.P_max / 32) * 2 * (I / 128) * 512);
   }
   L.total = off;
   return L;
@@ -160,6 +160,20 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MXFP8 scale tiles (512 bytes each) viewed as [2 * n_tiles][256] bytes: tile
+// i is the box of 2 rows at row 2i (no swizzle: its bytes land in order).
+bool make_map_scales(CUtensorMap* m, const void* base, uint64_t n_tiles) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {256, 2 * n_tiles};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {256, 2};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // W13 codes viewed as [E][2][I/16][16][H] like the bf16 map: boxes of 128 x 16 x 2 x 4 x 1.
 bool make_map_gate_up_u8(CUtensorMap* m, const void* w13c, uint64_t H, uint64_t I, uint64_t E) {
   auto fn = encode_fn();
@@ -202,7 +216,8 @@ moe_status check_inputs(const moe_shape* s, const void* x, const void* g, const 
 
 // K1 + K1b + K2 with the given padding; unit tables only when bn1/bn2 > 0.
 moe_status run_front(const moe_shape& s, const Layout& L, const moe_bf16* x, const moe_bf16* g, const float* wr,
-                     const float* bias, int pad, int bn1, int bn2, void* ws, cudaStream_t st, int num_sms) {
+                     const float* bias, int pad, int bn1, int utiles1, int bn2, int utiles2, void* ws,
+                     cudaStream_t st, int num_sms) {
   int32_t* err = at<int32_t>(ws, L.err);
   if (moe::launch_norm_router(x, g, wr, bias, s.T, s.H, s.E, s.eps, at<uint16_t>(ws, L.h), at<float>(ws, L.logits),
                               err, num_sms, st) != cudaSuccess)
@@ -210,15 +225,15 @@ moe_status run_front(const moe_shape& s, const Layout& L, const moe_bf16* x, con
   cudaError_t ce;
   if (moe::align_fuses_topk(s.T, s.E))
     ce = moe::launch_align(at<float>(ws, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(ws, L.ids),
-                           at<float>(ws, L.w), s.T * s.top_k, s.E, pad, bn1, s.I / moe::kGateUpTileFeat, bn2,
-                           s.H / moe::kDownTileFeat, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+                           at<float>(ws, L.w), s.T * s.top_k, s.E, pad, bn1, utiles1, bn2,
+                           utiles2, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                            at<int32_t>(ws, L.sorted), at<int32_t>(ws, L.slot),
                            bn1 > 0 ? at<int32_t>(ws, L.unit1) : nullptr, bn2 > 0 ? at<int32_t>(ws, L.unit2) : nullptr,
                            err, at<int32_t>(ws, L.flags), kGemmFlagInts, st);
   else
     ce = moe::launch_align_multi(at<float>(ws, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(ws, L.ids),
-                                 at<float>(ws, L.w), s.E, pad, bn1, s.I / moe::kGateUpTileFeat, bn2,
-                                 s.H / moe::kDownTileFeat, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+                                 at<float>(ws, L.w), s.E, pad, bn1, utiles1, bn2,
+                                 utiles2, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                                  at<int32_t>(ws, L.sorted), at<int32_t>(ws, L.slot),
                                  bn1 > 0 ? at<int32_t>(ws, L.unit1) : nullptr,
                                  bn2 > 0 ? at<int32_t>(ws, L.unit2) : nullptr, at<int32_t>(ws, L.blk_counts),
@@ -480,25 +495,35 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   const int num_sms = num_sms_of_current_device();
   if (num_sms <= 0) return MOE_ERR_CUDA;
   const Layout L = make_layout(s, true);
-  const int bn1 = moe::gemm_bn_mx(plan), bn2 = bn1;
   const int tiles1 = s.I / moe::kGateUpTileFeat, tiles2 = s.H / moe::kDownTileFeat;
+  // prefill: CTA pairs where the weight tiles come in pairs (256-token units)
+  const bool pair1 = moe::gemm_uses_pairs(plan, tiles1), pair2 = moe::gemm_uses_pairs(plan, tiles2);
+  const int bn1 = moe::gemm_bn_mx(plan, pair1), bn2 = moe::gemm_bn_mx(plan, pair2);
+  const int utiles1 = pair1 ? tiles1 / 2 : tiles1, utiles2 = pair2 ? tiles2 / 2 : tiles2;
   auto mark = [&](int i) {
     return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), cs) == cudaSuccess;
   };
-  CUtensorMap tm_w13, tm_xq, tm_w2, tm_aq;
+  const uint64_t n_tok_tiles1 = static_cast<uint64_t>(L.P_max / 32) * 2 * (s.H / 128);
+  const uint64_t n_tok_tiles2 = static_cast<uint64_t>(L.P_max / 32) * 2 * (s.I / 128);
+  CUtensorMap tm_w13, tm_xq, tm_w2, tm_aq, tm_s13, tm_sxq, tm_s2, tm_saq;
   if (!make_map_gate_up_u8(&tm_w13, w13c, s.H, s.I, s.E) ||
       !make_map_u8(&tm_xq, at<void>(workspace, L.xg), s.H, L.P_max, moe::gemm_tok_box_rows(plan)) ||
       !make_map_u8(&tm_w2, w2c, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows) ||
-      !make_map_u8(&tm_aq, at<void>(workspace, L.aq), s.I, L.P_max, moe::gemm_tok_box_rows(plan)))
+      !make_map_u8(&tm_aq, at<void>(workspace, L.aq), s.I, L.P_max, moe::gemm_tok_box_rows(plan)) ||
+      !make_map_scales(&tm_s13, w13s, static_cast<uint64_t>(s.E) * (2 * s.I / 128) * (s.H / 128)) ||
+      !make_map_scales(&tm_sxq, at<void>(workspace, L.xs), n_tok_tiles1) ||
+      !make_map_scales(&tm_s2, w2s, static_cast<uint64_t>(s.E) * (s.H / 128) * (s.I / 128)) ||
+      !make_map_scales(&tm_saq, at<void>(workspace, L.as), n_tok_tiles2))
     return MOE_ERR_CUDA;
   int32_t* err = at<int32_t>(workspace, L.err);
   if (!mark(0)) return MOE_ERR_CUDA;
-  st = run_front(s, L, x, g_norm, w_router, router_bias, moe::kPadRowsMx, bn1, bn2, workspace, cs, num_sms);
+  st = run_front(s, L, x, g_norm, w_router, router_bias, moe::kPadRowsMx, bn1, utiles1, bn2, utiles2, workspace, cs,
+                 num_sms);
   if (st != MOE_OK) return st;
   if (!mark(1) || !mark(2) || !mark(3)) return MOE_ERR_CUDA;
   const int N = s.T * s.top_k;
   if (moe::launch_mx_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
-                            at<int32_t>(workspace, L.offsets), at<int32_t>(workspace, L.unit1), tiles1, bn1, s.E, N,
+                            at<int32_t>(workspace, L.offsets), at<int32_t>(workspace, L.unit1), utiles1, bn1, s.E, N,
                             s.top_k, s.H, L.P_max, at<uint8_t>(workspace, L.xg), at<uint8_t>(workspace, L.xs),
                             cs) != cudaSuccess ||
       !mark(4))
@@ -509,7 +534,7 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   a1.unit_off = at<int32_t>(workspace, L.unit1);
   a1.E = s.E;
   a1.K = s.H;
-  a1.tiles_per_expert = tiles1;
+  a1.tiles_per_expert = utiles1;
   a1.w_rows_per_expert = 2 * s.I;
   a1.n_out = s.I;
   a1.out = at<uint16_t>(workspace, L.act);
@@ -517,13 +542,15 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   a1.partials = at<float>(workspace, L.partials);
   a1.flags = at<int32_t>(workspace, L.flags);
   a1.stream_k = plan == GemmPlan::kSmall;
+  a1.pair = pair1;
   a1.w_scales = w13s;
   a1.x_scales = at<uint8_t>(workspace, L.xs);
-  if (moe::launch_gemm_gate_up_mx(tm_w13, tm_xq, a1, plan, num_sms, cs) != cudaSuccess || !mark(5))
+  if (moe::launch_gemm_gate_up_mx(tm_w13, tm_xq, tm_s13, tm_sxq, a1, plan, num_sms, cs) != cudaSuccess || !mark(5))
     return MOE_ERR_CUDA;
-  // the activations (bf16) -> MXFP8, rows below offsets[E]
+  // the activations (bf16) -> MXFP8, rows below offsets[E], their scales in
+  // the down GEMM's token chunks
   if (moe::launch_mx_quantize_act(at<uint16_t>(workspace, L.act), L.P_max, s.I, at<int32_t>(workspace, L.offsets),
-                                  at<int32_t>(workspace, L.unit1), tiles1, bn1, s.E, at<uint8_t>(workspace, L.aq),
+                                  at<int32_t>(workspace, L.unit2), utiles2, bn2, s.E, at<uint8_t>(workspace, L.aq),
                                   at<uint8_t>(workspace, L.as), cs) != cudaSuccess)
     return MOE_ERR_CUDA;
   moe::ExpertGemmArgs a2{};
@@ -531,7 +558,7 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   a2.unit_off = at<int32_t>(workspace, L.unit2);
   a2.E = s.E;
   a2.K = s.I;
-  a2.tiles_per_expert = tiles2;
+  a2.tiles_per_expert = utiles2;
   a2.w_rows_per_expert = s.H;
   a2.n_out = s.H;
   a2.out = at<uint16_t>(workspace, L.out);
@@ -539,9 +566,11 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   a2.partials = at<float>(workspace, L.partials + partial_slots_bytes(s));
   a2.flags = at<int32_t>(workspace, L.flags) + moe::kMaxGemmCtas * 4;
   a2.stream_k = plan == GemmPlan::kSmall;
+  a2.pair = pair2;
   a2.w_scales = w2s;
   a2.x_scales = at<uint8_t>(workspace, L.as);
-  if (moe::launch_gemm_down_mx(tm_w2, tm_aq, a2, plan, num_sms, cs) != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
+  if (moe::launch_gemm_down_mx(tm_w2, tm_aq, tm_s2, tm_saq, a2, plan, num_sms, cs) != cudaSuccess || !mark(6))
+    return MOE_ERR_CUDA;
   if (moe::launch_combine(at<uint16_t>(workspace, L.out), at<int32_t>(workspace, L.slot), at<float>(workspace, L.w),
                           s.T, s.H, s.top_k, y, cs) != cudaSuccess ||
       !mark(7))
@@ -695,7 +724,7 @@ moe_status moe_route_debug(const moe_shape* shape, const moe_bf16* x, const moe_
   }
   const int num_sms = num_sms_of_current_device();
   if (num_sms <= 0) return MOE_ERR_CUDA;
-  st = run_front(s, L, x, g_norm, w_router, router_bias, pad_rows, 0, 0, workspace, cs, num_sms);
+  st = run_front(s, L, x, g_norm, w_router, router_bias, pad_rows, 0, 1, 0, 1, workspace, cs, num_sms);
   if (st != MOE_OK) return st;
   const size_t tk = static_cast<size_t>(s.T) * s.top_k;
   if (cudaMemcpyAsync(topk_ids, at<void>(workspace, L.ids), tk * 4, cudaMemcpyDeviceToDevice, cs) != cudaSuccess ||

@@ -150,19 +150,25 @@ cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act
 // the tiles per expert its work-unit table counts (pairs of tiles then).
 bool gemm_uses_pairs(GemmPlan plan, int tiles);
 int gemm_unit_tiles(GemmPlan plan, int tiles);
-// The same GEMMs on MXFP8 operands (block-scaled tcgen05 MMA; one CTA per
-// unit in every plan, gemm_bn_mx(plan) tokens per unit).  tm_w / tm_x map E4M3 codes (one byte per
+// The same GEMMs on MXFP8 operands (block-scaled tcgen05 MMA):
+// gemm_bn_mx(plan, a.pair) tokens per unit, on CTA pairs in the large plan when
+// a.pair is set (weight tiles in pairs).  tm_sw / tm_sx map the weight and
+// token scales as [tiles * 2][256] bytes (one 512-byte tile = a box of 2 rows);
+// only the pair instances read them (the others load tiles from a.w_scales /
+// a.x_scales directly).  tm_w / tm_x map E4M3 codes (one byte per
 // element); a.w_scales / a.x_scales hold the E8M0 scales.
-cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
-                                   GemmPlan plan, int num_sms, cudaStream_t stream);
-cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const ExpertGemmArgs& a,
-                                GemmPlan plan, int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const CUtensorMap& tm_sw,
+                                   const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
+                                   cudaStream_t stream);
+cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const CUtensorMap& tm_sw,
+                                const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
+                                cudaStream_t stream);
 // rows of padding granularity of each expert's list for the MXFP8 GEMMs (a
 // token scale group is 32 rows)
 constexpr int kPadRowsMx = 32;
 // token rows per unit (B-operand width) and rows per TMA box of the token tile
 int gemm_gate_up_bn(GemmPlan plan);
-int gemm_bn_mx(GemmPlan plan);  // token rows per unit of both MXFP8 GEMMs
+int gemm_bn_mx(GemmPlan plan, bool pair);  // token rows per unit of an MXFP8 GEMM (pair: on CTA pairs)
 int gemm_down_bn(GemmPlan plan);
 int gemm_tok_box_rows(GemmPlan plan);
 constexpr int kWeightBoxRows = 128;  // A-operand rows of one unit (one MMA's M)

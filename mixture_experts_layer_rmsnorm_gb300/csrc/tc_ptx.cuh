@@ -301,13 +301,40 @@ __device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, ui
 // Copy a 32-row x 16-byte tile (rows 16 bytes apart) from shared memory to
 // TMEM columns [taddr, taddr + 4), the same 32 rows in each lane quarter.
 // One thread; ordered before the tcgen05.mma this thread issues next.
-__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint32_t saddr) {
+__device__ __forceinline__ uint64_t cp_desc_32x128b(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>(16 >> 4) << 16;   // leading byte offset (one 16-byte column)
   d |= static_cast<uint64_t>(128 >> 4) << 32;  // stride byte offset: 8-row groups 128 bytes apart
   d |= static_cast<uint64_t>(1) << 46;         // fixed 0b001; no swizzle
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
+  return d;
+}
+
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint32_t saddr) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(cp_desc_32x128b(saddr))
+               : "memory");
+}
+
+// The same copy for a CTA pair, issued by the even CTA: each CTA's tile at
+// `saddr` of its own shared memory lands in its own TMEM at `taddr` (measured
+// on GB300).
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint32_t saddr) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(cp_desc_32x128b(saddr))
+               : "memory");
+}
+
+// Block-scaled MMA over a CTA pair (M = 256: 128 rows per CTA); each CTA's
+// scales come from its own TMEM at sfa_tmem / sfb_tmem (the B scales of all N
+// columns in both CTAs).  Issued by the even CTA.
+__device__ __forceinline__ void mma_mxf8_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::
+          "r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far

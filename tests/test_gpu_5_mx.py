@@ -76,10 +76,13 @@ def test_mx_layer_parity(case, o):
     gu.check_routing(o, li, li.x, g, pad=32)
     # gathered token rows: codes and scales bit for bit on the real rows; the
     # scales are grouped by the GEMMs' token chunks (bn rows of an expert)
-    bn = 32 if T * k <= 16 * E else 64 if T * k <= 64 * E else 128  # the GEMMs' token rows per unit
-    n_chunks = v.P_max // 32
+    # the gate/up GEMM's token rows per unit: 32 / 64 / 128 by plan, 256 on CTA
+    # pairs (prefill plan, I / 64 even); a chunk's scales take ceil(bn / 128) tiles
+    bn = 32 if T * k <= 16 * E else 64 if T * k <= 64 * E else (256 if (I // 64) % 2 == 0 else 128)
+    G = -(-bn // 128)
+    n_groups = 2 * (v.P_max // 32)
     xcodes = view(mv.x_codes, torch.uint8, (v.P_max, H))
-    xs = gu.ungroup_mx_scales(view(mv.x_scales, torch.uint8, (n_chunks * (H // 128) * 512,)), n_chunks * 128, H)
+    xs = gu.ungroup_mx_scales(view(mv.x_scales, torch.uint8, (n_groups * (H // 128) * 512,)), n_groups * 128, H)
     real = np.nonzero(g["sorted"] < T * k)[0]
     hc, hs = o.mx_quantize(g["h"][g["sorted"][real] // k])
     assert np.array_equal(xcodes[real], hc)
@@ -87,7 +90,7 @@ def test_mx_layer_parity(case, o):
     chunk0 = np.concatenate([[0], np.cumsum(-(-np.diff(offs) // bn))])  # chunks before each expert
     e_of = np.searchsorted(offs, real, side="right") - 1
     within = real - offs[e_of]
-    srow = (chunk0[e_of] + within // bn) * 128 + within % bn
+    srow = (chunk0[e_of] + within // bn) * 128 * G + within % bn
     assert np.array_equal(xs[srow], hs)
     # the layer output against the oracle's FP8 layer
     r = o.moe_forward_mx(li.x, li.g, li.w_router, li.bias, w13c, w13s, w2c, w2s, k, renorm, cfg.eps)
