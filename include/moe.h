@@ -268,6 +268,8 @@ typedef struct {
   void* x_scales;   /* their scales */
   void* act_codes;  /* [P_max, I] E4M3 codes of the SwiGLU activations */
   void* act_scales; /* their scales */
+  int32_t x_chunk_rows;    /* token rows per scale chunk of x_scales (the gate/up GEMM's unit) */
+  int32_t act_chunk_rows;  /* the same for act_scales (the down GEMM's unit) */
 } moe_mx_views;
 
 MOE_API moe_status moe_workspace_views_mx(const moe_shape* shape, void* workspace, size_t workspace_bytes,

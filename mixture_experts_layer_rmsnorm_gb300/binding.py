@@ -38,7 +38,7 @@ class MoeViews(ctypes.Structure):
 
 class MoeMxViews(ctypes.Structure):
     _fields_ = [("x_codes", ctypes.c_void_p), ("x_scales", ctypes.c_void_p), ("act_codes", ctypes.c_void_p),
-                ("act_scales", ctypes.c_void_p)]
+                ("act_scales", ctypes.c_void_p), ("x_chunk_rows", ctypes.c_int32), ("act_chunk_rows", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):

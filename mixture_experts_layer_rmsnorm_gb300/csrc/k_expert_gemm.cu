@@ -34,7 +34,7 @@
 // quarter.  The finishing CTA adds the partials of the following CTAs
 // before its epilogue, so it never waits on work that has not started.
 //
-// Roles in a CTA of 192 threads (persistent, one CTA per SM):
+// Roles in a CTA of 192 threads (320 for MXFP8 pairs; persistent, one CTA per SM):
 //   warp 0 lane 0   TMA producer: weight tiles [128 x 64] (one box) and token
 //                   tiles of TOKBOX rows per box, 128-byte swizzle, into a
 //                   STAGES-deep ring
@@ -42,7 +42,9 @@
 //                   tcgen05.commit (frees a ring slot / hands an accumulator
 //                   buffer to the epilogue)
 //   warps 2..5      epilogue: tcgen05.ld of their TMEM lane quarter, partial
-//                   sums, SwiGLU or plain bf16 convert, global stores
+//                   sums, SwiGLU or plain bf16 convert, global stores (warps
+//                   2..9, two per quarter, for MXFP8 pairs: their single
+//                   accumulator buffer must drain quickly)
 // Two accumulator buffers in TMEM let the epilogue of one range segment
 // overlap the MMAs of the next.  Every wait is bounded; a wait that runs out
 // sets the workspace error word and the kernel winds down.
@@ -69,7 +71,6 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kGemmThreads = 192;
 constexpr int kTabMaxE = 256;
 constexpr int kABytes = kWeightBoxRows * kBlockK * 2;  // 16 KB weight tile per stage
 constexpr int kTokRowBytes = kBlockK * 2;              // 128 B per token row per stage
@@ -90,7 +91,13 @@ struct GemmCfg {
   // accumulator buffers: two (the epilogue of one unit overlaps the MMAs of the
   // next); one for MXFP8 pairs, whose 256 columns leave no room for a second
   // next to the scale slots
-  static constexpr int kAccBufs = (MX && PAIR) ? 1 : 2;
+  static constexpr int kSfColsPerStage = MX ? 32 : 0;
+  static constexpr int kAccBufs = (2 * BN + STAGES * kSfColsPerStage <= 512) ? 2 : 1;
+  // epilogue warps: 4 (one per TMEM lane quarter); 8 with a single accumulator
+  // buffer (two per quarter, alternate 16-column groups), which halves the time
+  // the MMAs of the next unit wait for it
+  static constexpr int kEpiWarps = kAccBufs == 1 ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
   // TMEM columns of one stage's scales: weight scales at +0 (4 columns), token
   // scales at +16 (4 columns per 128 tokens); slots of 32 keep both addresses
   // 16-column aligned
@@ -105,8 +112,9 @@ struct GemmCfg {
   static constexpr int kFeatPerTile = SWIGLU ? kGateUpTileFeat : kDownTileFeat;  // output features per unit
   static_assert(BN % TOKBOX == 0 && TOKBOX % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
   static_assert(!PAIR || (BN / 2) % TOKBOX == 0, "token boxes of a CTA pair");
-  static_assert(!MX || (PAIR ? BN == 256 : (BN % 32 == 0 && BN <= 128)),
-                "MXFP8 units: one CTA with 32..128 tokens, or a CTA pair with 256");
+  static_assert(!MX || (PAIR ? (BN == 256 || BN == 128) : (BN % 32 == 0 && BN <= 128)),
+                "MXFP8 units: one CTA with 32..128 tokens, or a CTA pair with 128 or 256");
+  static_assert(kAccBufs == 2 || (MX && PAIR), "a single accumulator buffer only for MXFP8 pairs");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
   static_assert(kTmemNeed <= 512, "TMEM has 512 columns");
   static_assert((2 * STAGES + 7) * 8 + 32 <= kBarBytes, "barrier area");
@@ -272,7 +280,7 @@ __device__ __noinline__ bool combine_unit(const ExpertGemmArgs& a, const Unit& u
 }
 
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>::kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_sx,
                        const ExpertGemmArgs args) {
@@ -308,7 +316,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int32_t* t_unit = args.unit_off;
   const int32_t* t_off = args.offsets;
   if (!PAIR && args.E <= kTabMaxE) {
-    for (int i = threadIdx.x; i <= args.E; i += kGemmThreads) {
+    for (int i = threadIdx.x; i <= args.E; i += C::kThreads) {
       tab[i] = __ldcg(args.unit_off + i);
       tab[kTabMaxE + 1 + i] = __ldcg(args.offsets + i);
     }
@@ -322,7 +330,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], PAIR ? 8 : 4);  // the epilogue warps (of both CTAs of a pair)
+      mbar_init(&tempty[b], (PAIR ? 2 : 1) * C::kEpiWarps);  // the epilogue warps (of both CTAs of a pair)
     }
     mbar_init(done, 1);
     mbar_init(cbar, 4);  // one arrival per epilogue warp
@@ -394,11 +402,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int r = 0; r < rows; r += TOKBOX)
           load_2d(sb + r * kTokRowBytes, &tm_x, st, kb * C::kKPerStage, tok0 + r, pol_x);
         if (MX && PAIR) {
-          // both 512-byte scale tiles of the 256-token chunk, in each CTA (tensor
-          // map tm_sx: one tile = a box of 2 rows x 256 bytes)
-          for (int h = 0; h < 2; ++h)
-            load_2d(sb + C::kBBytes + 512 + 512 * h, &tm_sx, st, 0,
-                    2 * ((2 * chunk + h) * kblocks + kb), pol_x);
+          // the 512-byte scale tiles of the whole token chunk (one per 128 tokens),
+          // in each CTA (tensor map tm_sx: one tile = a box of 2 rows x 256 bytes)
+          constexpr int G = C::kSfTokBytes / 512;
+          for (int h = 0; h < G; ++h)
+            load_2d(sb + C::kBBytes + 512 + 512 * h, &tm_sx, st, 0, 2 * ((G * chunk + h) * kblocks + kb), pol_x);
         } else if (MX) {
           bulk_load(sb + C::kBBytes + 512, args.x_scales + (static_cast<size_t>(chunk) * kblocks + kb) * 512, 512,
                     &full[st], pol_x);
@@ -520,8 +528,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t sfb_t = sf_t + 16;
             if (PAIR) {
               tmem_cp_32x128b_x4_pair(sf_t, sf_s);
-              tmem_cp_32x128b_x4_pair(sfb_t, sf_s + 512);      // tokens 0..127: columns +0..+3
-              tmem_cp_32x128b_x4_pair(sfb_t + 4, sf_s + 1024);  // tokens 128..255: columns +4..+7
+              tmem_cp_32x128b_x4_pair(sfb_t, sf_s + 512);  // tokens 0..127: columns +0..+3
+              if (C::kSfTokBytes > 512)
+                tmem_cp_32x128b_x4_pair(sfb_t + 4, sf_s + 1024);  // tokens 128..255: columns +4..+7
             } else {
               tmem_cp_32x128b_x4(sf_t, sf_s);
               tmem_cp_32x128b_x4(sfb_t, sf_s + 512);
@@ -577,8 +586,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_wait(done, 0, kWaitTimeoutNs, &dummy);
     }
   } else {
-    // ---------------- epilogue: warps 2..5, TMEM lane quarter = warp % 4
+    // ---------------- epilogue: warps 2.., TMEM lane quarter = warp % 4; with
+    // 8 epilogue warps, group egrp of the two warps of a quarter takes the
+    // 16-column groups egrp, egrp + 2, ... (no stream-K then: large plan only)
     const int q = warp & 3;
+    const int egrp = (warp - 2) >> 2;
+    const int c_first = 16 * egrp, c_step = 16 * (C::kEpiWarps / 4);
     const int row = q * 32 + lane;  // this thread's TMEM lane = A-tile row
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -605,7 +618,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
       if (kb0 > 0) {
         // a later part of a unit started by an earlier CTA: hand over the partial sums
-        for (int c0 = 0; c0 < un.n; c0 += 16) {
+        for (int c0 = c_first; c0 < un.n; c0 += c_step) {
           uint32_t ra[16];
           tmem_ld_32x32b_x16(t_row + c0, ra);
           tmem_ld_wait();
@@ -624,24 +637,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (kb1 < kblocks)
           while (c_last + 1 < ctas && range_start(rg.W, c_last + 1, ctas) < unit_end) ++c_last;
         const int feat_base = (PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile) * C::kFeatPerTile;
-        for (int c0 = 0; c0 < un.n && ok; c0 += 16) {
+        for (int c0 = c_first; c0 < un.n && ok; c0 += c_step) {
           uint32_t ra[16];
           tmem_ld_32x32b_x16(t_row + c0, ra);
           tmem_ld_wait();
           float v[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(ra[j]);
+          bool good = true;
           for (int c = blockIdx.x + 1; c <= c_last; ++c) {
             if (range_start(rg.W, c, ctas) == range_start(rg.W, c + 1, ctas)) continue;  // empty range
-            if (c0 == 0 && !wait_flag(args.flags + c * 4 + q, abort_flag, kWaitTimeoutNs)) {
-              ok = false;
+            if (c0 == c_first && !wait_flag(args.flags + c * 4 + q, abort_flag, kWaitTimeoutNs)) {
+              good = false;
               break;
             }
             const float* slot = args.partials + static_cast<int64_t>(c) * BN * 128;
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] += __ldcg(slot + (c0 + j) * 128 + row);
           }
-          if (!ok) break;
+          if (!__all_sync(0xFFFFFFFFu, good)) {  // warp-uniform: the shuffles below need every lane
+            ok = false;
+            break;
+          }
           if (!SWIGLU) {
             uint16_t* out = args.out + static_cast<int64_t>(un.tok0 + c0) * args.n_out + feat_base + row;
 #pragma unroll
@@ -683,7 +700,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
-      if (!SWIGLU && kb0 == 0 && args.fuse_combine) {
+      if (!SWIGLU && kb0 == 0 && args.fuse_combine && C::kEpiWarps == 4) {
         const int tile = PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile;
         ok = combine_unit<BN>(args, un, tile, row, lane, cbar, cbar_phase, cmask, abort_flag);
         if (!ok) break;
@@ -718,7 +735,7 @@ cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, con
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -775,7 +792,9 @@ constexpr int kTokBox[3] = {16, 16, 128};
 // tiles come in pairs: 256-token units, 6 stages of 34 KB per CTA (one
 // 256-column accumulator + 6 x 32 scale columns)
 constexpr int kMxBn[3] = {32, 64, 128}, kMxStages[3] = {10, 8, 6};
-constexpr int kMxPairStages = 6;
+constexpr int kMxPairBn = 256;                              // tokens per pair unit (128: two accumulators)
+constexpr int kMxPairStages = kMxPairBn == 256 ? 6 : 8;     // 34 KB / 25 KB stages per CTA
+constexpr int kMxPairTokBox = kMxPairBn / 2;                // each CTA loads half of the unit's tokens
 
 }  // namespace
 
@@ -791,8 +810,9 @@ cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap&
                                                                                         stream);
     default:
       if (a.pair)
-        return launch_expert_gemm<true, 256, kMxPairStages, kTokBox[2], true, true>(tm_w13, tm_x, a, num_sms, stream,
-                                                                                    &tm_sw, &tm_sx);
+        return launch_expert_gemm<true, kMxPairBn, kMxPairStages, kMxPairTokBox, true, true>(tm_w13, tm_x, a,
+                                                                                            num_sms, stream, &tm_sw,
+                                                                                            &tm_sx);
       return launch_expert_gemm<true, kMxBn[2], kMxStages[2], kTokBox[2], false, true>(tm_w13, tm_x, a, num_sms,
                                                                                         stream);
   }
@@ -810,14 +830,16 @@ cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_
                                                                                          stream);
     default:
       if (a.pair)
-        return launch_expert_gemm<false, 256, kMxPairStages, kTokBox[2], true, true>(tm_w2, tm_act, a, num_sms,
-                                                                                     stream, &tm_sw, &tm_sx);
+        return launch_expert_gemm<false, kMxPairBn, kMxPairStages, kMxPairTokBox, true, true>(tm_w2, tm_act, a,
+                                                                                             num_sms, stream, &tm_sw,
+                                                                                             &tm_sx);
       return launch_expert_gemm<false, kMxBn[2], kMxStages[2], kTokBox[2], false, true>(tm_w2, tm_act, a, num_sms,
                                                                                          stream);
   }
 }
 
-int gemm_bn_mx(GemmPlan plan, bool pair) { return pair ? 256 : kMxBn[static_cast<int>(plan)]; }
+int gemm_bn_mx(GemmPlan plan, bool pair) { return pair ? kMxPairBn : kMxBn[static_cast<int>(plan)]; }
+int gemm_tok_box_rows_mx(GemmPlan plan, bool pair) { return pair ? kMxPairTokBox : kTokBox[static_cast<int>(plan)]; }
 
 int gemm_gate_up_bn(GemmPlan plan) { return kGateUpBn[static_cast<int>(plan)]; }
 int gemm_down_bn(GemmPlan plan) { return kDownBn[static_cast<int>(plan)]; }

@@ -507,9 +507,9 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   const uint64_t n_tok_tiles2 = static_cast<uint64_t>(L.P_max / 32) * 2 * (s.I / 128);
   CUtensorMap tm_w13, tm_xq, tm_w2, tm_aq, tm_s13, tm_sxq, tm_s2, tm_saq;
   if (!make_map_gate_up_u8(&tm_w13, w13c, s.H, s.I, s.E) ||
-      !make_map_u8(&tm_xq, at<void>(workspace, L.xg), s.H, L.P_max, moe::gemm_tok_box_rows(plan)) ||
+      !make_map_u8(&tm_xq, at<void>(workspace, L.xg), s.H, L.P_max, moe::gemm_tok_box_rows_mx(plan, pair1)) ||
       !make_map_u8(&tm_w2, w2c, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows) ||
-      !make_map_u8(&tm_aq, at<void>(workspace, L.aq), s.I, L.P_max, moe::gemm_tok_box_rows(plan)) ||
+      !make_map_u8(&tm_aq, at<void>(workspace, L.aq), s.I, L.P_max, moe::gemm_tok_box_rows_mx(plan, pair2)) ||
       !make_map_scales(&tm_s13, w13s, static_cast<uint64_t>(s.E) * (2 * s.I / 128) * (s.H / 128)) ||
       !make_map_scales(&tm_sxq, at<void>(workspace, L.xs), n_tok_tiles1) ||
       !make_map_scales(&tm_s2, w2s, static_cast<uint64_t>(s.E) * (s.H / 128) * (s.I / 128)) ||
@@ -642,6 +642,10 @@ moe_status moe_workspace_views_mx(const moe_shape* shape, void* workspace, size_
   mv->x_scales = at<void>(workspace, L.xs);
   mv->act_codes = at<void>(workspace, L.aq);
   mv->act_scales = at<void>(workspace, L.as);
+  const moe_shape& s = *shape;
+  const GemmPlan plan = moe::choose_plan(s.T, s.top_k, s.E);
+  mv->x_chunk_rows = moe::gemm_bn_mx(plan, moe::gemm_uses_pairs(plan, s.I / moe::kGateUpTileFeat));
+  mv->act_chunk_rows = moe::gemm_bn_mx(plan, moe::gemm_uses_pairs(plan, s.H / moe::kDownTileFeat));
   return MOE_OK;
 }
 

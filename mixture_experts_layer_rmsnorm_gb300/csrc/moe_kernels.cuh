@@ -169,6 +169,7 @@ constexpr int kPadRowsMx = 32;
 // token rows per unit (B-operand width) and rows per TMA box of the token tile
 int gemm_gate_up_bn(GemmPlan plan);
 int gemm_bn_mx(GemmPlan plan, bool pair);  // token rows per unit of an MXFP8 GEMM (pair: on CTA pairs)
+int gemm_tok_box_rows_mx(GemmPlan plan, bool pair);  // token rows per TMA box of that GEMM
 int gemm_down_bn(GemmPlan plan);
 int gemm_tok_box_rows(GemmPlan plan);
 constexpr int kWeightBoxRows = 128;  // A-operand rows of one unit (one MMA's M)

@@ -76,9 +76,11 @@ def test_mx_layer_parity(case, o):
     gu.check_routing(o, li, li.x, g, pad=32)
     # gathered token rows: codes and scales bit for bit on the real rows; the
     # scales are grouped by the GEMMs' token chunks (bn rows of an expert)
-    # the gate/up GEMM's token rows per unit: 32 / 64 / 128 by plan, 256 on CTA
-    # pairs (prefill plan, I / 64 even); a chunk's scales take ceil(bn / 128) tiles
-    bn = 32 if T * k <= 16 * E else 64 if T * k <= 64 * E else (256 if (I // 64) % 2 == 0 else 128)
+    # the gate/up GEMM's token rows per unit (its scale chunks): 32 / 64 by
+    # decode plan, 128 or 256 in prefill; a chunk's scales take ceil(bn / 128) tiles
+    bn = mv.x_chunk_rows
+    small_mid = 32 if T * k <= 16 * E else 64 if T * k <= 64 * E else None
+    assert bn == small_mid if small_mid else bn in (128, 256)
     G = -(-bn // 128)
     n_groups = 2 * (v.P_max // 32)
     xcodes = view(mv.x_codes, torch.uint8, (v.P_max, H))
