@@ -615,6 +615,18 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
       }
       tc_fence_after();
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * C::kAccCols);
+      // hand the accumulator buffer back to the MMA thread (the even CTA's, for a pair)
+      bool released = false;
+      auto release_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR)
+            mbar_arrive_cluster(tempty_cl + 8u * acc);  // the even CTA's MMA waits for both CTAs
+          else
+            mbar_arrive(&tempty[acc]);
+        }
+      };
 
       if (kb0 > 0) {
         // a later part of a unit started by an earlier CTA: hand over the partial sums
@@ -637,28 +649,8 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
         if (kb1 < kblocks)
           while (c_last + 1 < ctas && range_start(rg.W, c_last + 1, ctas) < unit_end) ++c_last;
         const int feat_base = (PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile) * C::kFeatPerTile;
-        for (int c0 = c_first; c0 < un.n && ok; c0 += c_step) {
-          uint32_t ra[16];
-          tmem_ld_32x32b_x16(t_row + c0, ra);
-          tmem_ld_wait();
-          float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(ra[j]);
-          bool good = true;
-          for (int c = blockIdx.x + 1; c <= c_last; ++c) {
-            if (range_start(rg.W, c, ctas) == range_start(rg.W, c + 1, ctas)) continue;  // empty range
-            if (c0 == c_first && !wait_flag(args.flags + c * 4 + q, abort_flag, kWaitTimeoutNs)) {
-              good = false;
-              break;
-            }
-            const float* slot = args.partials + static_cast<int64_t>(c) * BN * 128;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += __ldcg(slot + (c0 + j) * 128 + row);
-          }
-          if (!__all_sync(0xFFFFFFFFu, good)) {  // warp-uniform: the shuffles below need every lane
-            ok = false;
-            break;
-          }
+        // SwiGLU (gate/up GEMM) or plain convert of one 16-column group, and its stores
+        auto emit_chunk = [&](int c0, float (&v)[16]) {
           if (!SWIGLU) {
             uint16_t* out = args.out + static_cast<int64_t>(un.tok0 + c0) * args.n_out + feat_base + row;
 #pragma unroll
@@ -682,20 +674,59 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
 #pragma unroll
             for (int j = 0; j < 8; ++j) out[static_cast<int64_t>(j) * args.n_out] = f2bf(a[j]);
           }
+        };
+        if constexpr (C::kAccBufs == 1) {
+          // a single accumulator buffer (MXFP8 pairs: no stream-K): all of this
+          // warp's columns to registers, hand the buffer back to the MMAs, then
+          // the math and the stores
+          constexpr int kMine = BN / 16 / (C::kEpiWarps / 4);
+          uint32_t ra[kMine][16];
+#pragma unroll
+          for (int i = 0; i < kMine; ++i)
+            if (c_first + i * c_step < un.n) tmem_ld_32x32b_x16(t_row + c_first + i * c_step, ra[i]);
+          tmem_ld_wait();
+          release_acc();
+          released = true;
+#pragma unroll
+          for (int i = 0; i < kMine; ++i) {
+            if (c_first + i * c_step >= un.n) break;
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(ra[i][j]);
+            emit_chunk(c_first + i * c_step, v);
+          }
+        } else {
+          for (int c0 = c_first; c0 < un.n && ok; c0 += c_step) {
+            uint32_t ra[16];
+            tmem_ld_32x32b_x16(t_row + c0, ra);
+            tmem_ld_wait();
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(ra[j]);
+            bool good = true;
+            for (int c = blockIdx.x + 1; c <= c_last; ++c) {
+              if (range_start(rg.W, c, ctas) == range_start(rg.W, c + 1, ctas)) continue;  // empty range
+              if (c0 == c_first && !wait_flag(args.flags + c * 4 + q, abort_flag, kWaitTimeoutNs)) {
+                good = false;
+                break;
+              }
+              const float* slot = args.partials + static_cast<int64_t>(c) * BN * 128;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += __ldcg(slot + (c0 + j) * 128 + row);
+            }
+            if (!__all_sync(0xFFFFFFFFu, good)) {  // warp-uniform: the shuffles below need every lane
+              ok = false;
+              break;
+            }
+            emit_chunk(c0, v);
+          }
+          // the partial-sum flags read here are cleared for the next launch
+          if (ok && lane == 0)
+            for (int c = blockIdx.x + 1; c <= c_last; ++c) args.flags[c * 4 + q] = 0;
         }
-        // the partial-sum flags read here are cleared for the next launch
-        if (ok && lane == 0)
-          for (int c = blockIdx.x + 1; c <= c_last; ++c) args.flags[c * 4 + q] = 0;
       }
       if (!ok) break;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (PAIR)
-          mbar_arrive_cluster(tempty_cl + 8u * acc);  // the even CTA's MMA waits for both CTAs
-        else
-          mbar_arrive(&tempty[acc]);
-      }
+      if (!released) release_acc();
       if (++acc == C::kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
