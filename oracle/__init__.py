@@ -77,6 +77,16 @@ class Oracle:
         lib.oracle_moe_forward_mx.argtypes = [i64, i64, i64, i64, i, i, d, p, p, p, p, p, p, p, p, i64, p, i,
                                               p, p, p, p]
         lib.oracle_moe_forward_mx.restype = i
+        lib.oracle_e2m1_encode.argtypes = [d]
+        lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+        lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_decode.restype = d
+        lib.oracle_mx4_quantize.argtypes = [i64, i64, p, p, p]
+        lib.oracle_mx4_dequantize.argtypes = [i64, i64, p, p, p]
+        lib.oracle_expert_mx4_f64.argtypes = [i64, i64, p, p, p, p, p, p, p]
+        lib.oracle_moe_forward_mx4.argtypes = [i64, i64, i64, i64, i, i, d, p, p, p, p, p, p, p, p, i64, p, i,
+                                               p, p, p, p]
+        lib.oracle_moe_forward_mx4.restype = i
         lib.oracle_f64_to_bf16.argtypes = [d]
         lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
         lib.oracle_f32_to_bf16.argtypes = [f]
@@ -129,6 +139,44 @@ class Oracle:
         self.lib.oracle_mx_dequantize(codes.size // K, K, _p(codes), _p(scales), _p(out))
         return out
 
+    def e2m1_encode(self, v: float) -> int:
+        return int(self.lib.oracle_e2m1_encode(float(v)))
+
+    def e2m1_decode(self, c: int) -> float:
+        return float(self.lib.oracle_e2m1_decode(int(c)))
+
+    def mx4_quantize(self, x):
+        """MXFP4 of bf16 rows x[..., K]: (E2M1 codes [..., K] uint8 one per byte, scales [..., K/32] uint8)."""
+        x = _c(x, np.uint16)
+        K = x.shape[-1]
+        rows = x.size // K
+        codes = np.empty(x.shape, np.uint8)
+        scales = np.empty(x.shape[:-1] + (K // 32,), np.uint8)
+        self.lib.oracle_mx4_quantize(rows, K, _p(x), _p(codes), _p(scales))
+        return codes, scales
+
+    def mx4_dequantize(self, codes, scales):
+        codes = _c(codes, np.uint8); scales = _c(scales, np.uint8)
+        K = codes.shape[-1]
+        out = np.empty(codes.shape, np.float64)
+        self.lib.oracle_mx4_dequantize(codes.size // K, K, _p(codes), _p(scales), _p(out))
+        return out
+
+    def expert_mx4_f64(self, h, w13c, w13s, w2c, w2s):
+        """One token (bf16 h) through one expert with MXFP4 weights: (activation [I], output [H]) f64."""
+        h = _c(h, np.uint16)
+        w13c = _c(w13c, np.uint8); w13s = _c(w13s, np.uint8); w2c = _c(w2c, np.uint8); w2s = _c(w2s, np.uint8)
+        H = h.shape[-1]; I = w13c.shape[0] // 2
+        a = np.empty(I, np.float64); o = np.empty(H, np.float64)
+        self.lib.oracle_expert_mx4_f64(H, I, _p(h), _p(w13c), _p(w13s), _p(w2c), _p(w2s), _p(a), _p(o))
+        return a, o
+
+    def moe_forward_mx4(self, x, g, w_router, bias, w13c, w13s, w2c, w2s, top_k, renorm, eps, sample=None,
+                        nthreads=None):
+        """The FP4-weight layer (MXFP4 weights, MXFP8 tokens and activations); as moe_forward_mx."""
+        return self.moe_forward_mx(x, g, w_router, bias, w13c, w13s, w2c, w2s, top_k, renorm, eps, sample,
+                                   nthreads, _fn=self.lib.oracle_moe_forward_mx4)
+
     def expert_mx_f64(self, h, w13c, w13s, w2c, w2s):
         """One token (bf16 h) through one FP8 expert: (activation [I] f64 after MXFP8, output [H] f64)."""
         h = _c(h, np.uint16)
@@ -139,7 +187,7 @@ class Oracle:
         return a, o
 
     def moe_forward_mx(self, x, g, w_router, bias, w13c, w13s, w2c, w2s, top_k, renorm, eps, sample=None,
-                       nthreads=None):
+                       nthreads=None, _fn=None):
         """The FP8 layer (MXFP8 weights and activations) for the sampled tokens:
         ids [S,k], w [S,k], y64 [S,H], y16 [S,H] bf16 bits, sample [S]."""
         x = _c(x, np.uint16); g = _c(g, np.uint16); wr = _c(w_router, np.float32)
@@ -150,10 +198,10 @@ class Oracle:
         S = smp.size; k = int(top_k)
         out = dict(ids=np.empty((S, k), np.int32), w=np.empty((S, k), np.float64),
                    y64=np.empty((S, H), np.float64), y16=np.empty((S, H), np.uint16), sample=smp)
-        rc = self.lib.oracle_moe_forward_mx(T, H, I, E, k, int(bool(renorm)), float(eps), _p(x), _p(g), _p(wr),
-                                            _p(b), _p(w13c), _p(w13s), _p(w2c), _p(w2s), S, _p(smp),
-                                            nthreads or threads(), _p(out["ids"]), _p(out["w"]), _p(out["y64"]),
-                                            _p(out["y16"]))
+        fn = _fn or self.lib.oracle_moe_forward_mx
+        rc = fn(T, H, I, E, k, int(bool(renorm)), float(eps), _p(x), _p(g), _p(wr), _p(b), _p(w13c), _p(w13s),
+                _p(w2c), _p(w2s), S, _p(smp), nthreads or threads(), _p(out["ids"]), _p(out["w"]), _p(out["y64"]),
+                _p(out["y16"]))
         if rc != 0:
             raise ValueError("oracle_moe_forward_mx: bad arguments")
         return out

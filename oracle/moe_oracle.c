@@ -49,6 +49,13 @@
  *               even) and clamped to +-448.  The FP8 layer quantizes the expert
  *               weights, the gathered token rows and the SwiGLU activations this
  *               way and computes everything else as the bf16 layer does.
+ *   MXFP4       the same block scaling with E2M1 elements (magnitudes 0, 0.5,
+ *               1, 1.5, 2, 3, 4, 6): X = 2^(floor(log2(amax)) - 2), codes rounded
+ *               to nearest (ties to the even mantissa bit) and clamped to +-6
+ *                 -- "CuTeDSL chez Perplexity", "Prise en charge de Blackwell"
+ *                    (block-scaled 4-bit formats beside MXFP8).
+ *               The FP4 layer stores only the expert weights this way; its
+ *               token rows and activations are MXFP8 as above.
  *   QK-norm     per attention head of Q and of K (head_dim D elements):
  *               out_j = (w_j + weight_bias) * (x_j * rstd), rstd = 1/sqrt(mean x^2
  *               + eps), with one weight vector w[D] for all heads of Q and one for
@@ -226,16 +233,19 @@ uint8_t oracle_e4m3_encode(double v) {
   return (uint8_t)((sgn << 7) | (e << 3) | m);
 }
 
-/* Block exponent of 32 values with absolute maximum amax:
- * floor(log2(amax)) - 8, clamped to the E8M0 range [-127, 127]; -127 for amax = 0. */
-static int mx_block_exponent(double amax) {
+/* Block exponent of 32 values with absolute maximum amax: floor(log2(amax))
+ * minus the element format's largest exponent (8 for E4M3, 2 for E2M1),
+ * clamped to the E8M0 range [-127, 127]; -127 for amax = 0. */
+static int mx_block_exponent_of(double amax, int emax) {
   if (amax == 0.0) return -127;
   int ex = (int)floor(log2(amax));
   if (ldexp(1.0, ex) > amax) ex -= 1;
   if (ldexp(1.0, ex + 1) <= amax) ex += 1;
-  ex -= 8;
+  ex -= emax;
   return ex < -127 ? -127 : (ex > 127 ? 127 : ex);
 }
+
+static int mx_block_exponent(double amax) { return mx_block_exponent_of(amax, 8); }
 
 /* rows x K bf16 values (K a multiple of 32) -> codes [rows, K] and scales
  * [rows, K/32] (E8M0 bytes: exponent + 127). */
@@ -259,6 +269,70 @@ void oracle_mx_dequantize(int64_t rows, int64_t K, const uint8_t* codes, const u
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t j = 0; j < K; ++j)
       out[r * K + j] = ldexp(oracle_e4m3_decode(codes[r * K + j]), (int)scales[r * (K / 32) + j / 32] - 127);
+}
+
+/* ------------------------------------------------------------------ */
+/* MXFP4: E2M1 codes with E8M0 block scales                             */
+/* ------------------------------------------------------------------ */
+
+/* E2M1 (1 sign bit, 2 exponent bits with bias 1, 1 mantissa bit; no
+ * infinities or NaN; exponent field 0: subnormal m * 0.5): the value of a
+ * 4-bit code.  Magnitudes of the codes 0..7: 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double oracle_e2m1_decode(uint8_t c) {
+  int e = (c >> 1) & 3, m = c & 1;
+  double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+  return (c & 8) ? -v : v;
+}
+
+/* Nearest E2M1 code of a finite v, ties to an even mantissa bit, |v| > 6 -> 6
+ * (a tie always lies between neighbours of different mantissa parity). */
+uint8_t oracle_e2m1_encode(double v) {
+  int sgn = signbit(v) ? 1 : 0;
+  double a = fabs(v);
+  int best = 0;
+  double bd = INFINITY;
+  for (int c = 0; c < 8; ++c) {
+    double d = fabs(a - oracle_e2m1_decode((uint8_t)c));
+    if (d < bd || (d == bd && (c & 1) == 0)) {
+      bd = d;
+      best = c;
+    }
+  }
+  return (uint8_t)((sgn << 3) | best);
+}
+
+/* rows x K bf16 values (K a multiple of 32) -> E2M1 codes [rows, K] (one per
+ * byte, 0..15) and E8M0 scales [rows, K/32]: the MXFP8 rule with the E2M1
+ * element format (block exponent floor(log2(amax)) - 2). */
+void oracle_mx4_quantize(int64_t rows, int64_t K, const uint16_t* x, uint8_t* codes, uint8_t* scales) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < K / 32; ++b) {
+      const uint16_t* xb = x + r * K + b * 32;
+      double amax = 0.0;
+      for (int j = 0; j < 32; ++j) {
+        double a = fabs(bf16_to_f64(xb[j]));
+        if (a > amax) amax = a;
+      }
+      int ex = mx_block_exponent_of(amax, 2);
+      scales[r * (K / 32) + b] = (uint8_t)(ex + 127);
+      for (int j = 0; j < 32; ++j) codes[r * K + b * 32 + j] = oracle_e2m1_encode(ldexp(bf16_to_f64(xb[j]), -ex));
+    }
+}
+
+/* values of E2M1 codes [rows, K] with scales [rows, K/32] */
+void oracle_mx4_dequantize(int64_t rows, int64_t K, const uint8_t* codes, const uint8_t* scales, double* out) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t j = 0; j < K; ++j)
+      out[r * K + j] = ldexp(oracle_e2m1_decode(codes[r * K + j]), (int)scales[r * (K / 32) + j / 32] - 127);
+}
+
+/* weight rows of the low-precision layers: E4M3 (wfmt 0) or E2M1 (wfmt 1) codes */
+static void mx_weight_dequantize(int wfmt, int64_t rows, int64_t K, const uint8_t* codes, const uint8_t* scales,
+                                 double* out) {
+  if (wfmt)
+    oracle_mx4_dequantize(rows, K, codes, scales, out);
+  else
+    oracle_mx_dequantize(rows, K, codes, scales, out);
 }
 
 /* ------------------------------------------------------------------ */
@@ -503,11 +577,12 @@ static void expert_row_f64(int64_t H, int64_t I, const uint16_t* h16, const doub
 }
 
 /* One token through one expert of the FP8 layer: h (bf16) quantized to MXFP8
- * along H, the weights given as MXFP8 codes and scales, the bf16 SwiGLU
- * activation quantized to MXFP8 along I; products and sums in fp64.
+ * along H, the weights given as MXFP8 codes and scales (wfmt 0; wfmt 1:
+ * MXFP4, E2M1 codes), the bf16 SwiGLU activation quantized to MXFP8 along I;
+ * products and sums in fp64.
  *   W13c [2I, H] codes, W13s [2I, H/32] scales; W2c [H, I], W2s [H, I/32]. */
-static void expert_row_mx_f64(int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c, const uint8_t* W13s,
-                              const uint8_t* W2c, const uint8_t* W2s, double* a, double* o) {
+static void expert_row_mx_f64(int wfmt, int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c,
+                              const uint8_t* W13s, const uint8_t* W2c, const uint8_t* W2s, double* a, double* o) {
   uint8_t* hc = (uint8_t*)malloc((size_t)H);
   uint8_t* hs = (uint8_t*)malloc((size_t)(H / 32));
   double* hq = (double*)malloc(sizeof(double) * (size_t)H);
@@ -517,8 +592,8 @@ static void expert_row_mx_f64(int64_t H, int64_t I, const uint16_t* h16, const u
   double* wrow2 = (double*)malloc(sizeof(double) * (size_t)H);
   uint16_t* a16 = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
   for (int64_t i = 0; i < I; ++i) {
-    oracle_mx_dequantize(1, H, W13c + i * H, W13s + i * (H / 32), wrow);
-    oracle_mx_dequantize(1, H, W13c + (I + i) * H, W13s + (I + i) * (H / 32), wrow2);
+    mx_weight_dequantize(wfmt, 1, H, W13c + i * H, W13s + i * (H / 32), wrow);
+    mx_weight_dequantize(wfmt, 1, H, W13c + (I + i) * H, W13s + (I + i) * (H / 32), wrow2);
     double gate = 0.0, up = 0.0;
     for (int64_t j = 0; j < H; ++j) {
       gate += hq[j] * wrow[j];
@@ -532,7 +607,7 @@ static void expert_row_mx_f64(int64_t H, int64_t I, const uint16_t* h16, const u
   oracle_mx_quantize(1, I, a16, ac, as);
   oracle_mx_dequantize(1, I, ac, as, a);
   for (int64_t n = 0; n < H; ++n) {
-    oracle_mx_dequantize(1, I, W2c + n * I, W2s + n * (I / 32), wrow);
+    mx_weight_dequantize(wfmt, 1, I, W2c + n * I, W2s + n * (I / 32), wrow);
     double acc = 0.0;
     for (int64_t i = 0; i < I; ++i) acc += a[i] * wrow[i];
     o[n] = acc;
@@ -543,7 +618,15 @@ static void expert_row_mx_f64(int64_t H, int64_t I, const uint16_t* h16, const u
 void oracle_expert_mx_f64(int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c, const uint8_t* W13s,
                           const uint8_t* W2c, const uint8_t* W2s, double* a_out, double* o) {
   double* a = a_out ? a_out : (double*)malloc(sizeof(double) * (size_t)I);
-  expert_row_mx_f64(H, I, h16, W13c, W13s, W2c, W2s, a, o);
+  expert_row_mx_f64(0, H, I, h16, W13c, W13s, W2c, W2s, a, o);
+  if (!a_out) free(a);
+}
+
+/* the same with MXFP4 weights (E2M1 codes, one per byte) */
+void oracle_expert_mx4_f64(int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c, const uint8_t* W13s,
+                           const uint8_t* W2c, const uint8_t* W2s, double* a_out, double* o) {
+  double* a = a_out ? a_out : (double*)malloc(sizeof(double) * (size_t)I);
+  expert_row_mx_f64(1, H, I, h16, W13c, W13s, W2c, W2s, a, o);
   if (!a_out) free(a);
 }
 
@@ -565,8 +648,9 @@ typedef struct {
   const uint16_t *x, *g;
   const float *Wr, *bias;
   const uint16_t *W13, *W2;
-  /* FP8 layer (when W13c != NULL): MXFP8 weights */
+  /* FP8 layer (when W13c != NULL): MXFP8 weights (wfmt 0) or MXFP4 weights (wfmt 1) */
   const uint8_t *W13c, *W13s, *W2c, *W2s;
+  int wfmt;
   int64_t ns;
   const int64_t* sample;
   /* per-sample scratch / outputs */
@@ -599,7 +683,7 @@ static void fwd_expert_item(int64_t it, void* p) {
   int64_t e = c->ids[s * c->k + j];
   double* a = (double*)malloc(sizeof(double) * (size_t)c->I);
   if (c->W13c) {
-    expert_row_mx_f64(c->H, c->I, c->h16 + s * c->H, c->W13c + e * 2 * c->I * c->H,
+    expert_row_mx_f64(c->wfmt, c->H, c->I, c->h16 + s * c->H, c->W13c + e * 2 * c->I * c->H,
                       c->W13s + e * 2 * c->I * (c->H / 32), c->W2c + e * c->H * c->I, c->W2s + e * c->H * (c->I / 32),
                       a, c->o + it * c->H);
     free(a);
@@ -624,7 +708,7 @@ static void fwd_expert_item(int64_t it, void* p) {
 static int moe_forward_any(int64_t T, int64_t H, int64_t I, int64_t E, int k, int renorm, double eps,
                            const uint16_t* x, const uint16_t* g, const float* Wr, const float* bias,
                            const uint16_t* W13, const uint16_t* W2, const uint8_t* W13c, const uint8_t* W13s,
-                           const uint8_t* W2c, const uint8_t* W2s, int64_t ns, const int64_t* sample,
+                           const uint8_t* W2c, const uint8_t* W2s, int wfmt, int64_t ns, const int64_t* sample,
                            int round_inter, int nthreads, int32_t* ids, double* w, double* y64, uint16_t* y16,
                            uint16_t* h16_out, float* l32_out, double* l64_out) {
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E || ns < 0) return -1;
@@ -636,7 +720,7 @@ static int moe_forward_any(int64_t T, int64_t H, int64_t I, int64_t E, int k, in
   fwd_ctx c;
   c.T = T; c.H = H; c.I = I; c.E = E; c.k = k; c.renorm = renorm; c.round_inter = round_inter;
   c.eps = eps; c.x = x; c.g = g; c.Wr = Wr; c.bias = bias; c.W13 = W13; c.W2 = W2;
-  c.W13c = W13c; c.W13s = W13s; c.W2c = W2c; c.W2s = W2s;
+  c.W13c = W13c; c.W13s = W13s; c.W2c = W2c; c.W2s = W2s; c.wfmt = wfmt;
   c.ns = ns; c.sample = sample;
   c.h16 = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(ns * H));
   c.h64 = (double*)malloc(sizeof(double) * (size_t)(ns * H));
@@ -667,7 +751,7 @@ int oracle_moe_forward(int64_t T, int64_t H, int64_t I, int64_t E, int k, int re
                        const uint16_t* W13, const uint16_t* W2, int64_t ns, const int64_t* sample,
                        int round_inter, int nthreads, int32_t* ids, double* w, double* y64, uint16_t* y16,
                        uint16_t* h16_out, float* l32_out, double* l64_out) {
-  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, W13, W2, NULL, NULL, NULL, NULL, ns, sample,
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, W13, W2, NULL, NULL, NULL, NULL, 0, ns, sample,
                          round_inter, nthreads, ids, w, y64, y16, h16_out, l32_out, l64_out);
 }
 
@@ -680,8 +764,20 @@ int oracle_moe_forward_mx(int64_t T, int64_t H, int64_t I, int64_t E, int k, int
                           int64_t ns, const int64_t* sample, int nthreads, int32_t* ids, double* w, double* y64,
                           uint16_t* y16) {
   if (H % 32 || I % 32 || !W13c || !W13s || !W2c || !W2s) return -1;
-  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, ns, sample,
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, 0, ns, sample,
                          1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
 }
 
-int oracle_version(void) { return 2; }
+/* The FP4-weight layer: as oracle_moe_forward_mx with MXFP4 expert weights
+ * (E2M1 codes, one per byte, and E8M0 scales), MXFP8 tokens and activations. */
+int oracle_moe_forward_mx4(int64_t T, int64_t H, int64_t I, int64_t E, int k, int renorm, double eps,
+                           const uint16_t* x, const uint16_t* g, const float* Wr, const float* bias,
+                           const uint8_t* W13c, const uint8_t* W13s, const uint8_t* W2c, const uint8_t* W2s,
+                           int64_t ns, const int64_t* sample, int nthreads, int32_t* ids, double* w, double* y64,
+                           uint16_t* y16) {
+  if (H % 32 || I % 32 || !W13c || !W13s || !W2c || !W2s) return -1;
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, 1, ns, sample,
+                         1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
+}
+
+int oracle_version(void) { return 3; }

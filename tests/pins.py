@@ -262,6 +262,113 @@ def pin_mx_layer_torch(o):
     assert 1e-4 < rel < 0.1
 
 
+# ---------------------------------------------------------------------- MXFP4
+
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # the OCP E2M1 table (codes 0..7)
+
+
+def _rne_e2m1(a: np.ndarray) -> np.ndarray:
+    """E2M1 rounding restated per binade with numpy's round-half-even rint:
+    steps of 0.5 below 2, 1 below 4, 2 below 8; the value 8 saturates to 6."""
+    a = np.abs(a)
+    q = np.where(a < 2, np.rint(a * 2) / 2, np.where(a < 4, np.rint(a), 2 * np.rint(a / 2)))
+    return np.minimum(q, 6.0)
+
+
+def pin_e2m1_decode(o):
+    for c in range(16):
+        v = E2M1_MAGNITUDES[c & 7]
+        assert o.e2m1_decode(c) == (-v if c & 8 else v)
+
+
+def pin_e2m1_encode(o):
+    # hand-derived: ties go to the even mantissa bit (0.25 -> 0, 0.75 -> 1,
+    # 1.25 -> 1, 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4), above 6 saturates
+    for v, c in ((0.25, 0), (0.26, 1), (0.75, 2), (1.25, 2), (1.75, 4), (2.5, 4), (3.5, 6), (5.0, 6), (5.5, 7),
+                 (7.0, 7), (1e9, 7), (-0.3, 9), (-6.0, 15), (-1e9, 15)):
+        assert o.e2m1_encode(v) == c, (v, c)
+    # random values of all magnitudes and every midpoint between neighbours
+    rng = np.random.default_rng(8)
+    v = rng.standard_normal(20000) * np.exp2(rng.uniform(-4, 4, 20000))
+    mids = (np.array(E2M1_MAGNITUDES[:-1]) + np.array(E2M1_MAGNITUDES[1:])) / 2
+    for arr in (v, mids, -mids):
+        got = np.array([o.e2m1_decode(o.e2m1_encode(float(a))) for a in arr])
+        assert np.array_equal(np.abs(got), _rne_e2m1(arr)) and np.all((got == 0) | (np.sign(got) == np.sign(arr)))
+
+
+def pin_mx4_block_scale(o):
+    # block absolute maximum amax = r * 2^p: scale exponent p - 2, the maximum's
+    # value 4 r (r = 1 -> 4 = code 6, r = 1.5 -> 6 = code 7, r = 1.75 -> 7,
+    # saturated to 6); an element 2^(p-3) becomes 0.5 (code 1)
+    for p, r, code in ((0, 1.0, 6), (-6, 1.5, 7), (3, 1.75, 7), (-20, 1.25, 6)):
+        x = np.zeros((1, 64), np.float32)
+        x[0, 5] = r * 2.0 ** p
+        x[0, 40] = -r * 2.0 ** p
+        x[0, 7] = 2.0 ** (p - 3)
+        codes, scales = o.mx4_quantize(bits(x))
+        assert scales.tolist() == [[p - 2 + 127, p - 2 + 127]]
+        assert codes[0, 5] == code and codes[0, 40] == code | 8 and codes[0, 7] == 1
+    codes, scales = o.mx4_quantize(np.zeros((2, 32), np.uint16))
+    assert np.all(codes == 0) and np.all(scales == 0)
+
+
+def pin_mx4_roundtrip_error(o):
+    # dequantize(quantize(x)): at most half an E2M1 step of the value's binade
+    # (0.25 X below 2 X, 0.5 X below 4 X, 1 X above), except the values above
+    # 6 X (block maxima with a mantissa above 1.5), clamped to 6 X
+    x = inputs.normal_bf16(25, 1, (16, 256), 0.0, 0.02)
+    codes, scales = o.mx4_quantize(x)
+    d = o.mx4_dequantize(codes, scales)
+    xv = widen(x)
+    X = np.exp2(np.repeat(scales.astype(np.float64) - 127, 32, axis=1))
+    r = np.abs(xv) / X
+    assert np.all(r < 8) and np.all(r.reshape(-1, 32).max(axis=1) >= 4)  # block maxima in [4, 8) X
+    sat = r > 6
+    assert np.array_equal(d[sat], np.sign(xv[sat]) * 6 * X[sat])
+    half = np.where(r < 2, 0.25, np.where(r < 4, 0.5, 1.0)) * X
+    assert np.all(np.abs(d - xv)[~sat] <= half[~sat] * (1 + 1e-12))
+
+
+def _np_mx4_dequant(v64: np.ndarray) -> np.ndarray:
+    """Independent MXFP4 round trip of fp64 rows (values exact in bf16): block
+    exponents from frexp, values from the per-binade rint restatement."""
+    v = v64.reshape(-1, 32)
+    amax = np.abs(v).max(axis=1)
+    _, e = np.frexp(amax)                   # amax = m * 2^e, m in [0.5, 1)
+    ex = np.clip(np.where(amax > 0, e - 1 - 2, -127), -127, 127)
+    s = v / np.exp2(ex)[:, None]
+    q = np.sign(s) * _rne_e2m1(s)
+    return (q * np.exp2(ex)[:, None]).reshape(v64.shape)
+
+
+def pin_mx4_layer_restated(o):
+    # the FP4-weight layer against a restatement: the same routing, MXFP4 round
+    # trips of the weights (numpy), MXFP8 round trips of h and of the bf16
+    # activation (torch's fp8 cast), fp64 products and sums
+    T, H, I, E, k = 3, 64, 96, 4, 2
+    li = rand_layer(T, H, I, E, seed=26)
+    w13c, w13s = o.mx4_quantize(li.w13)
+    w2c, w2s = o.mx4_quantize(li.w2)
+    res = o.moe_forward_mx4(li.x, li.g, li.w_router, None, w13c, w13s, w2c, w2s, k, True, 1e-6)
+    ref = o.moe_forward(li.x, li.g, li.w_router, None, li.w13, li.w2, k, True, 1e-6)
+    assert np.array_equal(res["ids"], ref["ids"])
+    W13 = _np_mx4_dequant(widen(li.w13))
+    W2 = _np_mx4_dequant(widen(li.w2))
+    y = np.zeros((T, H))
+    for t in range(T):
+        hq = _torch_mx_dequant(widen(ref["h16"][t]))
+        for j in range(k):
+            e = int(res["ids"][t, j])
+            gate = W13[e, :I] @ hq
+            up = W13[e, I:] @ hq
+            a = widen(torch_bf16_bits_from_f64(gate / (1 + np.exp(-gate)) * up))
+            y[t] += res["w"][t, j] * (W2[e] @ _torch_mx_dequant(a))
+    assert np.allclose(res["y64"], y, rtol=1e-12, atol=1e-15)
+    # further from the bf16 layer than the FP8-weight layer, but close
+    rel = np.linalg.norm(res["y64"] - ref["y64"]) / np.linalg.norm(ref["y64"])
+    assert 1e-3 < rel < 0.5
+
+
 # -------------------------------------------------------------------- router
 
 def pin_router_f64_numpy(o):

@@ -39,7 +39,7 @@ MUTATIONS = {
     "align_unpadded": ("int64_t padded = (counts[e] + pad - 1) / pad * pad;", "int64_t padded = counts[e];"),
     "h_not_rounded_to_bf16": ("if (h) h[j] = f64_to_bf16(v);", "if (h) h[j] = f32_to_bf16((float)v);"),
     "act_round_dropped": ("a[i] = round_act ? bf16_to_f64(f64_to_bf16(v)) : v;", "a[i] = v;"),
-    "mx_emax_7": ("  ex -= 8;\n  return ex < -127", "  ex -= 7;\n  return ex < -127"),
+    "mx_emax_7": ("return mx_block_exponent_of(amax, 8); }", "return mx_block_exponent_of(amax, 7); }"),
     "e4m3_round_half_up": ("double q = nearbyint(a / ldexp(1.0, ex - 3));", "double q = floor(a / ldexp(1.0, ex - 3) + 0.5);"),
     "e4m3_no_saturation": ("      e = 15;\n      m = 6;", "      e = 15;\n      m = 7;"),
     "e4m3_subnormal_scale": ("double v = e == 0 ? ldexp((double)m, -9)", "double v = e == 0 ? ldexp((double)m, -10)"),
@@ -47,6 +47,13 @@ MUTATIONS = {
                              "  for (int64_t i = 0; i < I; ++i) a[i] = bf16_to_f64(a16[i]);"),
     "mx_token_not_quantized": ("  oracle_mx_dequantize(1, H, hc, hs, hq);",
                                "  for (int64_t j = 0; j < H; ++j) hq[j] = bf16_to_f64(h16[j]);"),
+    "mx4_emax_1": ("int ex = mx_block_exponent_of(amax, 2);", "int ex = mx_block_exponent_of(amax, 1);"),
+    "e2m1_tie_to_odd": ("if (d < bd || (d == bd && (c & 1) == 0)) {", "if (d < bd || (d == bd && (c & 1) == 1)) {"),
+    "e2m1_binade_off": ("double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);",
+                        "double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e);"),
+    "mx4_weights_as_e4m3": ("  if (wfmt)\n    oracle_mx4_dequantize(rows, K, codes, scales, out);",
+                            "  if (0)\n    oracle_mx4_dequantize(rows, K, codes, scales, out);"),
+    "e2m1_sign_dropped": ("  return (uint8_t)((sgn << 3) | best);", "  return (uint8_t)best;"),
     "qk_bias_dropped": ("(bf16_to_f64(w[j]) + weight_bias)", "(bf16_to_f64(w[j]))"),
     "qk_bias_multiplied": ("(bf16_to_f64(w[j]) + weight_bias)", "(bf16_to_f64(w[j]) * weight_bias)"),
     "qk_eps_dropped": ("sqrt(ss / (double)D + eps)", "sqrt(ss / (double)D)"),
