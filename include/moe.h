@@ -131,13 +131,15 @@ MOE_API moe_status moe_kernels_per_call(const moe_shape* shape, int32_t* count);
 
 /* The same for each entry point: call = MOE_CALL_FORWARD (moe_forward,
  * moe_forward_events, moe_forward_static_scratch), MOE_CALL_FORWARD_FUSED_FRONT
- * (moe_forward_fused_front), MOE_CALL_FORWARD_MX (moe_forward_mx) or
- * MOE_CALL_FORWARD_FUSED_COMBINE (moe_forward_fused_combine).  Another value
- * of call: MOE_ERR_INVALID_ARG.  Host-only. */
+ * (moe_forward_fused_front), MOE_CALL_FORWARD_MX (moe_forward_mx),
+ * MOE_CALL_FORWARD_FUSED_COMBINE (moe_forward_fused_combine) or
+ * MOE_CALL_FORWARD_MXFP4 (moe_forward_mxfp4).  Another value of call:
+ * MOE_ERR_INVALID_ARG.  Host-only. */
 #define MOE_CALL_FORWARD 0
 #define MOE_CALL_FORWARD_FUSED_FRONT 1
 #define MOE_CALL_FORWARD_MX 2
 #define MOE_CALL_FORWARD_FUSED_COMBINE 3
+#define MOE_CALL_FORWARD_MXFP4 4
 MOE_API moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t* count);
 
 /* moe_forward, plus CUDA events recorded on `stream` around the kernels:
@@ -281,7 +283,13 @@ MOE_API moe_status moe_workspace_views(const moe_shape* shape, void* workspace, 
 /* Waits for `stream`, then reads the workspace's error word: MOE_OK, or the
  * device-side error of the last call that used this workspace
  * (MOE_ERR_TIMEOUT / MOE_ERR_DEVICE).  detail (may be NULL) receives the
- * four raw int32 words. */
+ * four raw int32 words: the code, the id of the kernel that recorded it
+ * (1 norm/router, 2 top-k, 3 align, 4 gather, 5 gate/up GEMM, 6 down GEMM,
+ * 7 combine, 8 self-test), for the expert GEMMs a bit mask of the waits that
+ * ran out (bit 1 producer: ring slot free; 2 MMA: accumulator free; 3 MMA:
+ * ring slot loaded; 4 epilogue: accumulator complete; 5 epilogue: stream-K
+ * partial sums; 6 epilogue: fused-combine rendezvous), and the index of the
+ * CTA that recorded the timeout. */
 MOE_API moe_status moe_device_status(const void* workspace, size_t workspace_bytes, moe_stream_t stream,
                              int32_t* detail);
 
@@ -330,6 +338,43 @@ MOE_API moe_status moe_forward_mx(const moe_shape* shape, const moe_bf16* x, con
                                   const uint8_t* w13_scales, const uint8_t* w2_codes, const uint8_t* w2_scales,
                                   moe_bf16* y, void* workspace, size_t workspace_bytes, moe_stream_t stream,
                                   void* const* events, int32_t n_events);
+
+/* ---- FP4 expert weights (MXFP4) --------------------------------------
+ * Block-scaled 4-bit weights (the same pages list Blackwell's block-scaled
+ * FP4 formats beside MXFP8, "CuTeDSL chez Perplexity", "Prise en charge de
+ * Blackwell"; the OCP Microscaling rule with E2M1 elements): every 32
+ * consecutive elements along the reduction dimension share X = 2^E (one E8M0
+ * byte, E + 127) with E = floor(log2(amax)) - 2 clamped to [-127, 127] (-127
+ * for an all-zero block); each element is the E2M1 code of x / X (magnitudes
+ * 0, 0.5, 1, 1.5, 2, 3, 4, 6; sign in bit 3) rounded to nearest with ties to
+ * the even code and clamped to +-6.  Codes: the matrix layout with two codes
+ * per byte, element 2i in the low nibble of byte i ([rows, K/2] bytes).
+ * Scales: the MXFP8 layout above (the same tiles, the same W13 row order). */
+
+/* Byte sizes of the MXFP4 copies of W13 and W2 for this shape (codes: half
+ * the MXFP8 sizes; scales: the same). */
+MOE_API moe_status moe_mxfp4_weight_sizes(const moe_shape* shape, size_t* w13_codes, size_t* w13_scales,
+                                          size_t* w2_codes, size_t* w2_scales);
+
+/* Quantize the bf16 expert weights (layouts as for moe_forward) to MXFP4 on
+ * the device (asynchronous on `stream`).  All pointers device, sized by
+ * moe_mxfp4_weight_sizes; codes 32-byte aligned (the tensor maps' rule for
+ * packed 4-bit data), the rest 16-byte aligned; else MOE_ERR_INVALID_ARG. */
+MOE_API moe_status moe_mxfp4_quantize_weights(const moe_shape* shape, const moe_bf16* w13, const moe_bf16* w2,
+                                              uint8_t* w13_codes, uint8_t* w13_scales, uint8_t* w2_codes,
+                                              uint8_t* w2_scales, moe_stream_t stream);
+
+/* The layer with MXFP4 expert weights (W4A8): as moe_forward_mx (the same
+ * routing, MXFP8 token rows and activations, tile plans, workspace
+ * moe_workspace_size_mx and views moe_workspace_views_mx, events), with the
+ * weights as E2M1 codes in the block-scaled MMA (tcgen05.mma
+ * kind::mxf8f6f4, A = E2M1 weights, B = E4M3 tokens, fp32 accumulation).
+ * Weight codes 32-byte aligned, else MOE_ERR_INVALID_ARG. */
+MOE_API moe_status moe_forward_mxfp4(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                                     const float* w_router, const float* router_bias, const uint8_t* w13_codes,
+                                     const uint8_t* w13_scales, const uint8_t* w2_codes, const uint8_t* w2_scales,
+                                     moe_bf16* y, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                                     void* const* events, int32_t n_events);
 
 /* QK-norm, in place: RMSNorm of every attention head of Q and of K
  * ("CuTeDSL chez Perplexity", "Norme QK"):

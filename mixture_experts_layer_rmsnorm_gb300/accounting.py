@@ -44,14 +44,27 @@ def mx_bytes(n_elems: int) -> int:
     return n_elems + n_elems // 32
 
 
-def expert_weight_bytes(H: int, I: int, mx: bool = False) -> dict:
-    """Bytes of one expert's weights: gate/up (W13) and down (W2); mx: MXFP8 copies."""
+def mx4_bytes(n_elems: int) -> int:
+    """MXFP4 bytes of n elements: E2M1 codes two per byte plus one E8M0 scale per 32."""
+    return n_elems // 2 + n_elems // 32
+
+
+def weight_bytes(n_elems: int, mx) -> int:
+    """Bytes of n weight elements: bf16 (mx false), MXFP8 (mx true) or MXFP4 (mx == "mxfp4")."""
+    if mx == "mxfp4":
+        return mx4_bytes(n_elems)
+    return mx_bytes(n_elems) if mx else n_elems * BF16
+
+
+def expert_weight_bytes(H: int, I: int, mx=False) -> dict:
+    """Bytes of one expert's weights: gate/up (W13) and down (W2); mx: MXFP8
+    copies (true) or MXFP4 copies ("mxfp4")."""
     if mx:
-        return {"w13": mx_bytes(2 * I * H), "w2": mx_bytes(H * I)}
+        return {"w13": weight_bytes(2 * I * H, mx), "w2": weight_bytes(H * I, mx)}
     return {"w13": 2 * I * H * BF16, "w2": H * I * BF16}
 
 
-def layer_bytes(T: int, H: int, I: int, E: int, k: int, touched: int, mx: bool = False) -> dict:
+def layer_bytes(T: int, H: int, I: int, E: int, k: int, touched: int, mx=False) -> dict:
     ew = expert_weight_bytes(H, I, mx)
     d = {
         "weights_w13": touched * ew["w13"],
@@ -71,15 +84,16 @@ def layer_flops(T: int, H: int, I: int, E: int, k: int) -> dict:
     return {"gemm1": g1, "gemm2": g2, "router": r, "total": g1 + g2 + r}
 
 
-def gemm1_kernel_bytes(T: int, H: int, I: int, k: int, touched: int, mx: bool = False) -> int:
+def gemm1_kernel_bytes(T: int, H: int, I: int, k: int, touched: int, mx=False) -> int:
     """Algorithmic bytes of the gate/up expert GEMM: touched W13, the T*k
-    gathered token rows read once, the T*k activation rows (bf16) written once."""
+    gathered token rows read once, the T*k activation rows (bf16) written once.
+    mx: MXFP8 (true) or MXFP4 ("mxfp4") weights, MXFP8 token rows."""
     if mx:
-        return mx_bytes(touched * 2 * I * H) + mx_bytes(T * k * H) + T * k * I * BF16
+        return weight_bytes(touched * 2 * I * H, mx) + mx_bytes(T * k * H) + T * k * I * BF16
     return touched * 2 * I * H * BF16 + T * k * H * BF16 + T * k * I * BF16
 
 
-def gemm2_kernel_bytes(T: int, H: int, I: int, k: int, touched: int, mx: bool = False) -> int:
+def gemm2_kernel_bytes(T: int, H: int, I: int, k: int, touched: int, mx=False) -> int:
     if mx:
-        return mx_bytes(touched * H * I) + mx_bytes(T * k * I) + T * k * H * BF16
+        return weight_bytes(touched * H * I, mx) + mx_bytes(T * k * I) + T * k * H * BF16
     return touched * H * I * BF16 + T * k * I * BF16 + T * k * H * BF16

@@ -12,9 +12,16 @@
 
 namespace moe {
 
-__device__ __forceinline__ void raise_timeout(int32_t* err, volatile int* abort_flag, int kern) {
+// where (> 0): which wait of the kernel ran out, recorded as bit `where` of
+// err[2]; a wait that ended because the CTA was already winding down (its
+// abort flag set) adds no bit.  err[3]: the CTA that recorded the timeout.
+__device__ __forceinline__ void raise_timeout(int32_t* err, volatile int* abort_flag, int kern, int where = 0) {
+  if (where > 0 && !*abort_flag) atomicOr(err + 2, 1 << where);
+  if (atomicCAS(err, 0, kErrTimeout) == 0) {
+    atomicExch(err + 1, kern);
+    atomicExch(err + 3, static_cast<int32_t>(blockIdx.x));
+  }
   *abort_flag = 1;
-  if (atomicCAS(err, 0, kErrTimeout) == 0) atomicExch(err + 1, kern);
 }
 
 __device__ __forceinline__ int ld_acquire(const int32_t* p) {

@@ -75,7 +75,7 @@ constexpr int kTabMaxE = 256;
 constexpr int kABytes = kWeightBoxRows * kBlockK * 2;  // 16 KB weight tile per stage
 constexpr int kTokRowBytes = kBlockK * 2;              // 128 B per token row per stage
 
-template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false>
 struct GemmCfg {
   // a CTA pair splits the unit's tokens: each CTA holds half of the B tile
   static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * kTokRowBytes;
@@ -84,6 +84,11 @@ struct GemmCfg {
   // and 512 per 128 token rows of the unit's token chunk (a CTA of a pair needs
   // the scales of all 256 tokens: the pair MMA reads them from its own TMEM)
   static constexpr int kKPerStage = MX ? 128 : kBlockK;
+  // MXFP4 weights (W4): two E2M1 codes per byte in global memory; the TMA's
+  // 16U4_ALIGN16B type spreads each 8 bytes (16 codes) over 16 bytes of shared
+  // memory, so the tile's image and descriptors are those of an FP8 tile while
+  // the barrier counts only the 64 data bytes per 128-element row
+  static constexpr int kWTxBytes = W4 ? kABytes / 2 : kABytes;
   static constexpr int kSfTokBytes = MX ? (BN > 128 ? 1024 : 512) : 0;
   static constexpr int kSfBytes = MX ? 512 + kSfTokBytes : 0;
   static constexpr int kStageBytes = (kABytes + kBBytes + kSfBytes + 1023) / 1024 * 1024;
@@ -115,6 +120,7 @@ struct GemmCfg {
   static_assert(!MX || (PAIR ? (BN == 256 || BN == 128) : (BN % 32 == 0 && BN <= 128)),
                 "MXFP8 units: one CTA with 32..128 tokens, or a CTA pair with 128 or 256");
   static_assert(kAccBufs == 2 || (MX && PAIR), "a single accumulator buffer only for MXFP8 pairs");
+  static_assert(!W4 || MX, "FP4 weights only with block-scaled MXFP8 tokens");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
   static_assert(kTmemNeed <= 512, "TMEM has 512 columns");
   static_assert((2 * STAGES + 7) * 8 + 32 <= kBarBytes, "barrier area");
@@ -123,6 +129,16 @@ struct GemmCfg {
 
 struct Unit {
   int e, tile, tok0, n;
+};
+
+// The waits of the kernel, as recorded in the error word's detail bits.
+enum : int {
+  kWaitRingSlotFree = 1,  // producer: a ring slot consumed by the MMAs
+  kWaitAccFree = 2,       // MMA: an accumulator buffer drained by the epilogue
+  kWaitRingSlotFull = 3,  // MMA: a ring slot's loads landed
+  kWaitAccFull = 4,       // epilogue: an accumulator's MMAs complete
+  kWaitPartials = 5,      // epilogue: a later CTA's stream-K partial sums
+  kWaitCombine = 6        // epilogue: the fused combine's rendezvous
 };
 
 // Work unit u -> expert (binary search in the unit prefix sums), weight tile
@@ -279,12 +295,12 @@ __device__ __noinline__ bool combine_unit(const ExpertGemmArgs& a, const Unit& u
   return true;
 }
 
-template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false>
-__global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>::kThreads, 1)
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false>
+__global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4>::kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_sx,
                        const ExpertGemmArgs args) {
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
@@ -434,7 +450,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
         const int tok_rows = (half + TOKBOX - 1) / TOKBOX * TOKBOX;  // whole boxes; rows past n are unused
         const bool reused = t_off[un.e + 1] - t_off[un.e] > BN;
         const uint64_t pol_w = reused ? pol_keep : pol_stream;
-        const uint32_t bytes = kABytes + tok_rows * kTokRowBytes + C::kSfBytes;  // per CTA (the same in both of a pair)
+        const uint32_t bytes = C::kWTxBytes + tok_rows * kTokRowBytes + C::kSfBytes;  // per CTA (both of a pair)
         const int chunk = MX ? t_unit[un.e] / args.tiles_per_expert + (un.tok0 - t_off[un.e]) / BN : 0;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitTimeoutNs, abort_flag)) {
@@ -478,7 +494,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
         }
       }
       if (!deps_ready) resolve_deps();  // fewer iterations than stages (or none)
-      if (!ok) raise_timeout(args.err, abort_flag, kern);
+      if (!ok) raise_timeout(args.err, abort_flag, kern, kWaitRingSlotFree);
       // every load this thread issued must have landed before the CTA exits
       // (the odd CTA of a pair sees that through the release of its stages:
       // the pair's MMA ran on them, so they had landed)
@@ -497,6 +513,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      int where = 0;  // the wait that ran out
       Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
       int u, kb0, kb1;
       while (ok && rg.next(u, kb0, kb1)) {
@@ -505,6 +522,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
                                    : mbar_wait(&tempty[acc], acc_phase ^ 1u, kWaitTimeoutNs, abort_flag);
         if (!free_acc) {
           ok = false;
+          where = kWaitAccFree;
           break;
         }
         tc_fence_after();
@@ -514,6 +532,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, kWaitTimeoutNs, abort_flag)) {
             ok = false;
+            where = kWaitRingSlotFull;
             break;
           }
           tc_fence_after();
@@ -538,7 +557,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-              const uint32_t id = idesc_mxf8(PAIR ? 256 : 128, static_cast<uint32_t>(n_mma), k, k);
+              const uint32_t id = idesc_mxf8(PAIR ? 256 : 128, static_cast<uint32_t>(n_mma), k, k, W4 ? kFmtE2M1 : 0);
               if (PAIR)
                 mma_mxf8_ss_pair(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), id, sf_t,
                                  sfb_t, accum);
@@ -576,7 +595,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
           acc_phase ^= 1u;
         }
       }
-      if (!ok) raise_timeout(args.err, abort_flag, kern);
+      if (!ok) raise_timeout(args.err, abort_flag, kern, where);
       // all MMAs this thread issued have finished before TMEM is released
       if (PAIR)
         mma_commit_pair(done);
@@ -596,6 +615,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
+    int where = 0;  // the wait that ran out
     // gate/up: warp quarter q holds features +16q .. +16q+15, gate in lanes
     // 0..15 and up in lanes 16..31
     const bool lo = lane < 16;
@@ -611,6 +631,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
       const bool got = mbar_wait(&tfull[acc], acc_phase, kWaitTimeoutNs, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) {
         ok = false;
+        where = kWaitAccFull;
         break;
       }
       tc_fence_after();
@@ -716,6 +737,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
             }
             if (!__all_sync(0xFFFFFFFFu, good)) {  // warp-uniform: the shuffles below need every lane
               ok = false;
+              where = kWaitPartials;
               break;
             }
             emit_chunk(c0, v);
@@ -734,10 +756,13 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
       if (!SWIGLU && kb0 == 0 && args.fuse_combine && C::kEpiWarps == 4) {
         const int tile = PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile;
         ok = combine_unit<BN>(args, un, tile, row, lane, cbar, cbar_phase, cmask, abort_flag);
-        if (!ok) break;
+        if (!ok) {
+          where = kWaitCombine;
+          break;
+        }
       }
     }
-    if (!ok && lane == 0) raise_timeout(args.err, abort_flag, kern);
+    if (!ok && lane == 0) raise_timeout(args.err, abort_flag, kern, where);
   }
 
   __syncthreads();
@@ -753,13 +778,13 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>:
   }
 }
 
-template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false>
 cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, int num_sms,
                                cudaStream_t stream, const CUtensorMap* tsw = nullptr,
                                const CUtensorMap* tsx = nullptr) {
   static const CUtensorMap kNoMap = {};  // the scale maps of MXFP8 pairs; unused elsewhere
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>;
-  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4>;
+  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4>;
   static int configured_device = -1;
   static int max_pairs = 0;  // CTA pairs that fit on the configured device at once
   int dev = 0;
@@ -827,46 +852,40 @@ constexpr int kMxPairBn = 256;                              // tokens per pair u
 constexpr int kMxPairStages = kMxPairBn == 256 ? 6 : 8;     // 34 KB / 25 KB stages per CTA
 constexpr int kMxPairTokBox = kMxPairBn / 2;                // each CTA loads half of the unit's tokens
 
+// The block-scaled GEMMs of one tile plan; W4: E2M1 weight codes.
+template <bool SWIGLU, bool W4>
+cudaError_t launch_mx(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& tsw, const CUtensorMap& tsx,
+                      const ExpertGemmArgs& a, GemmPlan plan, int num_sms, cudaStream_t stream) {
+  switch (plan) {
+    case GemmPlan::kSmall:
+      return launch_expert_gemm<SWIGLU, kMxBn[0], kMxStages[0], kTokBox[0], false, true, W4>(tw, tx, a, num_sms,
+                                                                                            stream);
+    case GemmPlan::kMid:
+      return launch_expert_gemm<SWIGLU, kMxBn[1], kMxStages[1], kTokBox[1], false, true, W4>(tw, tx, a, num_sms,
+                                                                                            stream);
+    default:
+      if (a.pair)
+        return launch_expert_gemm<SWIGLU, kMxPairBn, kMxPairStages, kMxPairTokBox, true, true, W4>(
+            tw, tx, a, num_sms, stream, &tsw, &tsx);
+      return launch_expert_gemm<SWIGLU, kMxBn[2], kMxStages[2], kTokBox[2], false, true, W4>(tw, tx, a, num_sms,
+                                                                                            stream);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const CUtensorMap& tm_sw,
                                    const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
-                                   cudaStream_t stream) {
-  switch (plan) {
-    case GemmPlan::kSmall:
-      return launch_expert_gemm<true, kMxBn[0], kMxStages[0], kTokBox[0], false, true>(tm_w13, tm_x, a, num_sms,
-                                                                                        stream);
-    case GemmPlan::kMid:
-      return launch_expert_gemm<true, kMxBn[1], kMxStages[1], kTokBox[1], false, true>(tm_w13, tm_x, a, num_sms,
-                                                                                        stream);
-    default:
-      if (a.pair)
-        return launch_expert_gemm<true, kMxPairBn, kMxPairStages, kMxPairTokBox, true, true>(tm_w13, tm_x, a,
-                                                                                            num_sms, stream, &tm_sw,
-                                                                                            &tm_sx);
-      return launch_expert_gemm<true, kMxBn[2], kMxStages[2], kTokBox[2], false, true>(tm_w13, tm_x, a, num_sms,
-                                                                                        stream);
-  }
+                                   cudaStream_t stream, bool fp4_weights) {
+  return fp4_weights ? launch_mx<true, true>(tm_w13, tm_x, tm_sw, tm_sx, a, plan, num_sms, stream)
+                     : launch_mx<true, false>(tm_w13, tm_x, tm_sw, tm_sx, a, plan, num_sms, stream);
 }
 
 cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const CUtensorMap& tm_sw,
                                 const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
-                                cudaStream_t stream) {
-  switch (plan) {
-    case GemmPlan::kSmall:
-      return launch_expert_gemm<false, kMxBn[0], kMxStages[0], kTokBox[0], false, true>(tm_w2, tm_act, a, num_sms,
-                                                                                         stream);
-    case GemmPlan::kMid:
-      return launch_expert_gemm<false, kMxBn[1], kMxStages[1], kTokBox[1], false, true>(tm_w2, tm_act, a, num_sms,
-                                                                                         stream);
-    default:
-      if (a.pair)
-        return launch_expert_gemm<false, kMxPairBn, kMxPairStages, kMxPairTokBox, true, true>(tm_w2, tm_act, a,
-                                                                                             num_sms, stream, &tm_sw,
-                                                                                             &tm_sx);
-      return launch_expert_gemm<false, kMxBn[2], kMxStages[2], kTokBox[2], false, true>(tm_w2, tm_act, a, num_sms,
-                                                                                         stream);
-  }
+                                cudaStream_t stream, bool fp4_weights) {
+  return fp4_weights ? launch_mx<false, true>(tm_w2, tm_act, tm_sw, tm_sx, a, plan, num_sms, stream)
+                     : launch_mx<false, false>(tm_w2, tm_act, tm_sw, tm_sx, a, plan, num_sms, stream);
 }
 
 int gemm_bn_mx(GemmPlan plan, bool pair) { return pair ? kMxPairBn : kMxBn[static_cast<int>(plan)]; }

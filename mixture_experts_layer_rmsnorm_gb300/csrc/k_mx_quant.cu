@@ -1,4 +1,5 @@
-// k_mx_quant.cu -- MXFP8 quantization: bf16 rows -> E4M3 codes + E8M0 scales.
+// k_mx_quant.cu -- MXFP8 quantization: bf16 rows -> E4M3 codes + E8M0 scales;
+// MXFP4 quantization of the expert weights: bf16 rows -> E2M1 codes + E8M0 scales.
 //
 // Block scaling over 32 consecutive elements ("CuTeDSL chez Perplexity",
 // "Prise en charge de Blackwell": MXFP8 with an absolute maximum over 32
@@ -9,7 +10,12 @@
 // to nearest even and clamped to +-448 (cvt.rn.satfinite); the scale byte is
 // E + 127.
 //
-// Codes keep the rows' layout ([rows, K], one byte per element).  Scales are
+// MXFP4 (the same pages name Blackwell's block-scaled 4-bit formats beside
+// MXFP8; the same OCP rule): E = floor(log2(amax)) - 2 (2 = the largest E2M1
+// exponent), codes E2M1 of x / X rounded to nearest even and clamped to +-6.
+//
+// Codes keep the rows' layout ([rows, K], one byte per element; MXFP4: [rows,
+// K/2] bytes, element 2i in the low nibble of byte i).  Scales are
 // stored for the tensor cores' block-scaled MMA: per 128-row group and per
 // 128-element chunk of K, one 512-byte tile of 32 rows x 16 bytes in which
 // byte r*16 + 4*j + b is the scale of row 32*j + r of the group and K-block b
@@ -52,6 +58,21 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
+// eight E2M1 codes (round to nearest even, saturating to +-6): element i in
+// bits 4i .. 4i+3
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
 // byte offset of the scale of (scale row R, K-block kb) for K elements per row
 __device__ __forceinline__ size_t scale_offset(int64_t R, int kb, int K) {
   const int64_t g = R >> 7;
@@ -82,7 +103,9 @@ __device__ __forceinline__ int64_t token_scale_row(int p, const int32_t* offsets
 // rows (row p <- h[sorted_ids[p] / k], zeros for padding rows), rows below
 // offsets[E] only, chunk-grouped scales; MODE 2: rows of W13, scales in gate/up
 // tile-row order; MODE 3: activation rows below offsets[E], chunk-grouped scales.
-template <int MODE>
+// FP4 (weights, MODE 0 and 2): E2M1 codes, packed two per byte, and the block
+// exponent floor(log2 amax) - 2 (2 = the largest E2M1 exponent).
+template <int MODE, bool FP4 = false>
 __global__ void __launch_bounds__(kQuantWarps * 32)
     mx_quantize_kernel(const uint16_t* __restrict__ src, int64_t rows, int K, const int32_t* __restrict__ sorted_ids,
                        const int32_t* __restrict__ offsets, const int32_t* __restrict__ unit_off, int tiles, int bn,
@@ -120,15 +143,21 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-    int ex = amax > 0.0f ? ilogbf(amax) - 8 : -127;
+    int ex = amax > 0.0f ? ilogbf(amax) - (FP4 ? 2 : 8) : -127;
     ex = ex < -127 ? -127 : (ex > 127 ? 127 : ex);
     const float inv = ldexpf(1.0f, -ex);  // exact power of two
-    uint32_t w0 = e4m3x2(x[0] * inv, x[1] * inv) | (e4m3x2(x[2] * inv, x[3] * inv) << 16);
-    uint32_t w1 = e4m3x2(x[4] * inv, x[5] * inv) | (e4m3x2(x[6] * inv, x[7] * inv) << 16);
-    if (on) {
-      *reinterpret_cast<uint2*>(codes + row * K + c * 8) = make_uint2(w0, w1);
-      if ((lane & 3) == 0) scales[scale_offset(R, c >> 2, K)] = static_cast<uint8_t>(ex + 127);
+    if (FP4) {
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = x[i] * inv;
+      const uint32_t w = e2m1x8(y);
+      if (on) *reinterpret_cast<uint32_t*>(codes + row * (K / 2) + c * 4) = w;
+    } else {
+      const uint32_t w0 = e4m3x2(x[0] * inv, x[1] * inv) | (e4m3x2(x[2] * inv, x[3] * inv) << 16);
+      const uint32_t w1 = e4m3x2(x[4] * inv, x[5] * inv) | (e4m3x2(x[6] * inv, x[7] * inv) << 16);
+      if (on) *reinterpret_cast<uint2*>(codes + row * K + c * 8) = make_uint2(w0, w1);
     }
+    if (on && (lane & 3) == 0) scales[scale_offset(R, c >> 2, K)] = static_cast<uint8_t>(ex + 127);
   }
 }
 
@@ -155,6 +184,21 @@ cudaError_t launch_mx_quantize_w13(const uint16_t* w13, int E, int H, int I, uin
   const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
   return launch_pdl(mx_quantize_kernel<2>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0, stream,
                     w13, rows, H, nullptr, nullptr, nullptr, 1, 32, 0, 0, 1, I, codes, scales);
+}
+
+cudaError_t launch_mx4_quantize_rows(const uint16_t* src, int64_t rows, int K, uint8_t* codes, uint8_t* scales,
+                                     cudaStream_t stream) {
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  return launch_pdl(mx_quantize_kernel<0, true>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0,
+                    stream, src, rows, K, nullptr, nullptr, nullptr, 1, 32, 0, 0, 1, 0, codes, scales);
+}
+
+cudaError_t launch_mx4_quantize_w13(const uint16_t* w13, int E, int H, int I, uint8_t* codes, uint8_t* scales,
+                                    cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(E) * 2 * I;
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  return launch_pdl(mx_quantize_kernel<2, true>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0,
+                    stream, w13, rows, H, nullptr, nullptr, nullptr, 1, 32, 0, 0, 1, I, codes, scales);
 }
 
 cudaError_t launch_mx_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets,

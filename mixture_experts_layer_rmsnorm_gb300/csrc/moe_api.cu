@@ -187,6 +187,37 @@ bool make_map_gate_up_u8(CUtensorMap* m, const void* w13c, uint64_t H, uint64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// E2M1 codes [rows, inner], two per byte (inner / 2 bytes per row), boxes of
+// 128 x box_rows; 16U4_ALIGN16B spreads each 8 code bytes over 16 bytes of
+// shared memory, so a box lands as the image of an E4M3 box of the same shape.
+// inner: a multiple of 128 (the type's rule; the row stride is then a multiple
+// of 32 bytes); base: 32-byte aligned.
+bool make_map_u4(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner / 2};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// W13 E2M1 codes viewed as [E][2][I/16][16][H] like the bf16 map (dimensions
+// in elements, strides in bytes of the packed codes).
+bool make_map_gate_up_u4(CUtensorMap* m, const void* w13c, uint64_t H, uint64_t I, uint64_t E) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[5] = {H, 16, 2, I / 16, E};
+  cuuint64_t strides[4] = {H / 2, I * H / 2, 16 * H / 2, 2 * I * H / 2};
+  cuuint32_t box[5] = {128, 16, 2, moe::kGateUpTileFeat / 16, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 5, const_cast<void*>(w13c), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int num_sms_of_current_device() {
   static int cache[64] = {0};
   int dev = 0;
@@ -259,7 +290,7 @@ moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes) {
 moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t* count) {
   const moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
-  if (!count || call < MOE_CALL_FORWARD || call > MOE_CALL_FORWARD_FUSED_COMBINE) return MOE_ERR_INVALID_ARG;
+  if (!count || call < MOE_CALL_FORWARD || call > MOE_CALL_FORWARD_MXFP4) return MOE_ERR_INVALID_ARG;
   const moe_shape& s = *shape;
   if (s.T == 0) {
     *count = 0;
@@ -271,7 +302,7 @@ moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t
     *count = front + 3;
   else if (call == MOE_CALL_FORWARD_FUSED_FRONT)
     *count = 1 + 3;
-  else if (call == MOE_CALL_FORWARD_MX)
+  else if (call == MOE_CALL_FORWARD_MX || call == MOE_CALL_FORWARD_MXFP4)
     *count = front + 4;  // + the activation quantize between the GEMMs
   else
     *count = front + 2;  // the combine runs inside the down GEMM
@@ -475,11 +506,11 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
 }
 
 // The MXFP8 layer: the bf16 layer's routing, then MXFP8 token rows and
-// weights in block-scaled tcgen05 GEMMs (decode tile plans).
+// weights in block-scaled tcgen05 GEMMs; fp4: MXFP4 weights (E2M1 codes).
 moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
                            const float* router_bias, const uint8_t* w13c, const uint8_t* w13s, const uint8_t* w2c,
                            const uint8_t* w2s, moe_bf16* y, void* workspace, size_t workspace_bytes,
-                           moe_stream_t stream, void* const* events) {
+                           moe_stream_t stream, void* const* events, bool fp4 = false) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   const moe_shape& s = *shape;
@@ -488,8 +519,9 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   if (s.E > 256) return MOE_ERR_UNSUPPORTED;
   st = check_inputs(shape, x, g_norm, w_router, router_bias, workspace, workspace_bytes, true);
   if (st != MOE_OK) return st;
-  if (!w13c || !w13s || !w2c || !w2s || !y || !aligned(w13c, 16) || !aligned(w13s, 16) || !aligned(w2c, 16) ||
-      !aligned(w2s, 16) || !aligned(y, 16))
+  const size_t code_align = fp4 ? 32 : 16;  // the 16U4_ALIGN16B tensor maps want 32-byte bases
+  if (!w13c || !w13s || !w2c || !w2s || !y || !aligned(w13c, code_align) || !aligned(w13s, 16) ||
+      !aligned(w2c, code_align) || !aligned(w2s, 16) || !aligned(y, 16))
     return MOE_ERR_INVALID_ARG;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int num_sms = num_sms_of_current_device();
@@ -506,9 +538,12 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   const uint64_t n_tok_tiles1 = static_cast<uint64_t>(L.P_max / 32) * 2 * (s.H / 128);
   const uint64_t n_tok_tiles2 = static_cast<uint64_t>(L.P_max / 32) * 2 * (s.I / 128);
   CUtensorMap tm_w13, tm_xq, tm_w2, tm_aq, tm_s13, tm_sxq, tm_s2, tm_saq;
-  if (!make_map_gate_up_u8(&tm_w13, w13c, s.H, s.I, s.E) ||
+  const bool maps_w = fp4 ? make_map_gate_up_u4(&tm_w13, w13c, s.H, s.I, s.E) &&
+                                 make_map_u4(&tm_w2, w2c, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows)
+                           : make_map_gate_up_u8(&tm_w13, w13c, s.H, s.I, s.E) &&
+                                 make_map_u8(&tm_w2, w2c, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows);
+  if (!maps_w ||
       !make_map_u8(&tm_xq, at<void>(workspace, L.xg), s.H, L.P_max, moe::gemm_tok_box_rows_mx(plan, pair1)) ||
-      !make_map_u8(&tm_w2, w2c, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows) ||
       !make_map_u8(&tm_aq, at<void>(workspace, L.aq), s.I, L.P_max, moe::gemm_tok_box_rows_mx(plan, pair2)) ||
       !make_map_scales(&tm_s13, w13s, static_cast<uint64_t>(s.E) * (2 * s.I / 128) * (s.H / 128)) ||
       !make_map_scales(&tm_sxq, at<void>(workspace, L.xs), n_tok_tiles1) ||
@@ -545,7 +580,8 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   a1.pair = pair1;
   a1.w_scales = w13s;
   a1.x_scales = at<uint8_t>(workspace, L.xs);
-  if (moe::launch_gemm_gate_up_mx(tm_w13, tm_xq, tm_s13, tm_sxq, a1, plan, num_sms, cs) != cudaSuccess || !mark(5))
+  if (moe::launch_gemm_gate_up_mx(tm_w13, tm_xq, tm_s13, tm_sxq, a1, plan, num_sms, cs, fp4) != cudaSuccess ||
+      !mark(5))
     return MOE_ERR_CUDA;
   // the activations (bf16) -> MXFP8, rows below offsets[E], their scales in
   // the down GEMM's token chunks
@@ -569,7 +605,7 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   a2.pair = pair2;
   a2.w_scales = w2s;
   a2.x_scales = at<uint8_t>(workspace, L.as);
-  if (moe::launch_gemm_down_mx(tm_w2, tm_aq, tm_s2, tm_saq, a2, plan, num_sms, cs) != cudaSuccess || !mark(6))
+  if (moe::launch_gemm_down_mx(tm_w2, tm_aq, tm_s2, tm_saq, a2, plan, num_sms, cs, fp4) != cudaSuccess || !mark(6))
     return MOE_ERR_CUDA;
   if (moe::launch_combine(at<uint16_t>(workspace, L.out), at<int32_t>(workspace, L.slot), at<float>(workspace, L.w),
                           s.T, s.H, s.top_k, y, cs) != cudaSuccess ||
@@ -606,6 +642,32 @@ moe_status moe_mx_quantize_weights(const moe_shape* shape, const moe_bf16* w13, 
   const moe_shape& s = *shape;
   if (moe::launch_mx_quantize_w13(w13, s.E, s.H, s.I, w13_codes, w13_scales, cs) != cudaSuccess ||
       moe::launch_mx_quantize_rows(w2, static_cast<int64_t>(s.E) * s.H, s.I, w2_codes, w2_scales, cs) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_mxfp4_weight_sizes(const moe_shape* shape, size_t* w13_codes, size_t* w13_scales, size_t* w2_codes,
+                                  size_t* w2_scales) {
+  const moe_status st = moe_mx_weight_sizes(shape, w13_codes, w13_scales, w2_codes, w2_scales);
+  if (st != MOE_OK) return st;
+  *w13_codes /= 2;  // two E2M1 codes per byte
+  *w2_codes /= 2;
+  return MOE_OK;
+}
+
+moe_status moe_mxfp4_quantize_weights(const moe_shape* shape, const moe_bf16* w13, const moe_bf16* w2,
+                                      uint8_t* w13_codes, uint8_t* w13_scales, uint8_t* w2_codes, uint8_t* w2_scales,
+                                      moe_stream_t stream) {
+  const moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!w13 || !w2 || !w13_codes || !w13_scales || !w2_codes || !w2_scales || !aligned(w13, 16) || !aligned(w2, 16) ||
+      !aligned(w13_codes, 32) || !aligned(w13_scales, 16) || !aligned(w2_codes, 32) || !aligned(w2_scales, 16))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const moe_shape& s = *shape;
+  if (moe::launch_mx4_quantize_w13(w13, s.E, s.H, s.I, w13_codes, w13_scales, cs) != cudaSuccess ||
+      moe::launch_mx4_quantize_rows(w2, static_cast<int64_t>(s.E) * s.H, s.I, w2_codes, w2_scales, cs) !=
+          cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -660,6 +722,20 @@ moe_status moe_forward_mx(const moe_shape* shape, const moe_bf16* x, const moe_b
   }
   return moe::forward_mx_impl(shape, x, g_norm, w_router, router_bias, w13_codes, w13_scales, w2_codes, w2_scales, y,
                               workspace, workspace_bytes, stream, events);
+}
+
+moe_status moe_forward_mxfp4(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                             const float* w_router, const float* router_bias, const uint8_t* w13_codes,
+                             const uint8_t* w13_scales, const uint8_t* w2_codes, const uint8_t* w2_scales,
+                             moe_bf16* y, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                             void* const* events, int32_t n_events) {
+  if (events) {
+    if (n_events < MOE_NUM_KERNELS + 1) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i <= MOE_NUM_KERNELS; ++i)
+      if (!events[i]) return MOE_ERR_INVALID_ARG;
+  }
+  return moe::forward_mx_impl(shape, x, g_norm, w_router, router_bias, w13_codes, w13_scales, w2_codes, w2_scales, y,
+                              workspace, workspace_bytes, stream, events, true);
 }
 
 moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,

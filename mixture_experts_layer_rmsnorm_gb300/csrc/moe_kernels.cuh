@@ -155,14 +155,16 @@ int gemm_unit_tiles(GemmPlan plan, int tiles);
 // a.pair is set (weight tiles in pairs).  tm_sw / tm_sx map the weight and
 // token scales as [tiles * 2][256] bytes (one 512-byte tile = a box of 2 rows);
 // only the pair instances read them (the others load tiles from a.w_scales /
-// a.x_scales directly).  tm_w / tm_x map E4M3 codes (one byte per
-// element); a.w_scales / a.x_scales hold the E8M0 scales.
+// a.x_scales directly).  tm_x maps E4M3 codes (one byte per element); tm_w
+// E4M3 codes too, or with fp4_weights E2M1 codes (two per byte, a
+// 16U4_ALIGN16B map with the same boxes); a.w_scales / a.x_scales hold the
+// E8M0 scales.
 cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const CUtensorMap& tm_sw,
                                    const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
-                                   cudaStream_t stream);
+                                   cudaStream_t stream, bool fp4_weights = false);
 cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const CUtensorMap& tm_sw,
                                 const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
-                                cudaStream_t stream);
+                                cudaStream_t stream, bool fp4_weights = false);
 // rows of padding granularity of each expert's list for the MXFP8 GEMMs (a
 // token scale group is 32 rows)
 constexpr int kPadRowsMx = 32;
@@ -204,6 +206,12 @@ cudaError_t launch_mx_quantize_rows(const uint16_t* src, int64_t rows, int K, ui
                                     cudaStream_t stream);
 cudaError_t launch_mx_quantize_w13(const uint16_t* w13, int E, int H, int I, uint8_t* codes, uint8_t* scales,
                                    cudaStream_t stream);
+// MXFP4 weights: the same scale layout, E2M1 codes two per byte ([rows, K/2]
+// bytes, element 2i in the low nibble of byte i), exponent floor(log2 amax) - 2
+cudaError_t launch_mx4_quantize_rows(const uint16_t* src, int64_t rows, int K, uint8_t* codes, uint8_t* scales,
+                                     cudaStream_t stream);
+cudaError_t launch_mx4_quantize_w13(const uint16_t* w13, int E, int H, int I, uint8_t* codes, uint8_t* scales,
+                                    cudaStream_t stream);
 // token rows (gathered inputs / activations below offsets[E]): scales grouped
 // by the GEMMs' token chunks (bn rows of an expert, chunk unit_off[e]/tiles + c)
 cudaError_t launch_mx_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets,

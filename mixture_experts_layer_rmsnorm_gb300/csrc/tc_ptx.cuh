@@ -380,13 +380,15 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::mxf8f6f4 with block scaling: A and B E4M3
-// (format 0), K-major, UE8M0 scales (bit 23); scale bytes sf_a / sf_b in bits
-// 29-30 / 4-5; N >> 3 at bit 17, M >> 4 at bit 24.
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: B E4M3 (format
+// 0), A E4M3 (a_fmt 0) or E2M1 (a_fmt 5) in bits 7-9, both K-major, UE8M0
+// scales (bit 23); scale bytes sf_a / sf_b in bits 29-30 / 4-5; N >> 3 at
+// bit 17, M >> 4 at bit 24.
 __host__ __device__ __forceinline__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32_t sf_a,
-                                                                  uint32_t sf_b) {
-  return (sf_b << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sf_a << 29);
+                                                                  uint32_t sf_b, uint32_t a_fmt = 0) {
+  return (sf_b << 4) | (a_fmt << 7) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sf_a << 29);
 }
+constexpr uint32_t kFmtE2M1 = 5;
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, dense.
 //   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format (1 = bf16);

@@ -63,10 +63,12 @@ def test_kernels_per_call_host_checks():
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD) == (binding.MOE_OK, 6)
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_FUSED_FRONT) == (binding.MOE_OK, 4)
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_MX) == (binding.MOE_OK, 7)
+    assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_MXFP4) == (binding.MOE_OK, 7)
+    assert binding.moe_kernels_per_call_of(s4, 5)[0] == binding.MOE_ERR_INVALID_ARG
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_FUSED_COMBINE) == (binding.MOE_OK, 5)
     s4096 = binding.shape(4096, 128, 256, 8, 2)
     assert binding.moe_kernels_per_call_of(s4096, binding.MOE_CALL_FORWARD_FUSED_COMBINE) == (binding.MOE_OK, 7)
-    assert binding.moe_kernels_per_call_of(s4, 4)[0] == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_kernels_per_call_of(s4, 6)[0] == binding.MOE_ERR_INVALID_ARG
     assert binding.moe_kernels_per_call_of(s4, -1)[0] == binding.MOE_ERR_INVALID_ARG
 
 
@@ -118,6 +120,28 @@ def test_forward_rejects_bad_arguments_without_a_gpu():
     # T = 0 is a no-op that touches no pointer
     assert binding.moe_forward(binding.shape(0, 128, 256, 8, 2), None, None, None, None, None, None, None, None, 0,
                                None) == binding.MOE_OK
+
+
+def test_mxfp4_sizes_and_argument_checks_without_a_gpu():
+    s = binding.shape(4, 256, 384, 8, 2)
+    st, (c13, s13, c2, s2) = binding.moe_mxfp4_weight_sizes(s)
+    assert st == binding.MOE_OK
+    assert (c13, c2) == (8 * 2 * 384 * 256 // 2, 8 * 256 * 384 // 2)  # two E2M1 codes per byte
+    assert (s13, s2) == binding.moe_mx_weight_sizes(s)[1][1::2]      # the MXFP8 scale tiles
+    _, need = binding.moe_workspace_size_mx(s)
+    A = 1 << 20
+
+    def fwd(w13c=A, w2c=A, w13s=A):
+        return binding.moe_forward_mxfp4(s, A, A, A, None, w13c, w13s, w2c, A, A, A, need, None)
+
+    assert fwd(w13c=A + 16) == binding.MOE_ERR_INVALID_ARG  # packed codes: 32-byte aligned
+    assert fwd(w2c=A + 16) == binding.MOE_ERR_INVALID_ARG
+    assert fwd(w13s=None) == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_forward_mxfp4(s, A, A, A, None, A, A, A, A, A, A, need - 1, None) == binding.MOE_ERR_WORKSPACE
+    assert binding.moe_mxfp4_quantize_weights(s, A, A, A + 16, A, A, A, None) == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_mxfp4_quantize_weights(s, A, A, A, A, A + 48, A, None) == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_mxfp4_quantize_weights(binding.shape(4, 100, 384, 8, 2), A, A, A, A, A, A, None) == \
+        binding.MOE_ERR_UNSUPPORTED
 
 
 def test_route_debug_rejects_bad_arguments_without_a_gpu():

@@ -1,10 +1,12 @@
-"""GPU parity of the FP8 layer (MXFP8 expert weights, block-scaled tcgen05 MMA).
+"""GPU parity of the block-scaled layers: MXFP8 expert weights (E4M3 codes) and
+MXFP4 expert weights (E2M1 codes, two per byte), both with MXFP8 token rows and
+activations, on the block-scaled tcgen05 MMA.
 
-Every quantization decision is exact on both sides, so the E4M3 codes and E8M0
-scales of the weights and of the gathered token rows are compared bit for bit
-with the oracle's quantizer; the routing bit for bit as in the bf16 layer
-(lists padded to 32 rows); the layer output against the oracle's FP8 layer
-(the same recipe, fp64 arithmetic) within the layer tolerance.
+Every quantization decision is exact on both sides, so the weight codes and
+E8M0 scales and those of the gathered token rows are compared bit for bit with
+the oracle's quantizers; the routing bit for bit as in the bf16 layer (lists
+padded to 32 rows); the layer output against the oracle's layer of the same
+format (the same recipe, fp64 arithmetic) within the layer tolerance.
 """
 import numpy as np
 import pytest
@@ -36,27 +38,45 @@ def o():
     return oracle.default()
 
 
+def unpack_e2m1(packed, shape_):
+    """Two E2M1 codes per byte, element 2i in the low nibble of byte i -> one code per byte."""
+    b = packed.reshape(-1)
+    out = np.empty(b.size * 2, np.uint8)
+    out[0::2] = b & 0xF
+    out[1::2] = b >> 4
+    return out.reshape(shape_)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_mx_layer_parity(case, o):
+def test_mx_layer_parity(case, fmt, o):
     _, T, H, I, E, k, renorm, zipf, seed = case
     cfg = inputs.LayerConfig(T=T, H=H, I=I, E=E, top_k=k, renormalize=renorm, seed=seed, zipf_bias=zipf)
     li = inputs.make_layer_inputs(cfg)
     dl = gu.DeviceLayer(li)
     L = dl.layer
-    L.quantize_mx()
+    fp4 = fmt == "mxfp4"
+    if fp4:
+        L.quantize_mxfp4()
+        codes13, scales13, codes2, scales2 = L.w13_codes4, L.w13_scales4, L.w2_codes4, L.w2_scales4
+        quantize, unpack = o.mx4_quantize, unpack_e2m1
+    else:
+        L.quantize_mx()
+        codes13, scales13, codes2, scales2 = L.w13_codes, L.w13_scales, L.w2_codes, L.w2_scales
+        quantize, unpack = o.mx_quantize, lambda c, shp: c.reshape(shp)
     torch.cuda.synchronize()
     # weights: codes and scales bit for bit
-    w13c, w13s = o.mx_quantize(li.w13)
-    w2c, w2s = o.mx_quantize(li.w2)
-    assert np.array_equal(L.w13_codes.cpu().numpy().reshape(E, 2 * I, H), w13c)
-    assert np.array_equal(L.w2_codes.cpu().numpy().reshape(E, H, I), w2c)
-    s13 = gu.ungroup_mx_scales(L.w13_scales.cpu().numpy(), E * 2 * I, H)[gu.w13_scale_rows(E, I)]
+    w13c, w13s = quantize(li.w13)
+    w2c, w2s = quantize(li.w2)
+    assert np.array_equal(unpack(codes13.cpu().numpy(), (E, 2 * I, H)), w13c)
+    assert np.array_equal(unpack(codes2.cpu().numpy(), (E, H, I)), w2c)
+    s13 = gu.ungroup_mx_scales(scales13.cpu().numpy(), E * 2 * I, H)[gu.w13_scale_rows(E, I)]
     assert np.array_equal(s13.reshape(E, 2 * I, H // 32), w13s)
-    s2 = gu.ungroup_mx_scales(L.w2_scales.cpu().numpy(), E * H, I)
+    s2 = gu.ungroup_mx_scales(scales2.cpu().numpy(), E * H, I)
     assert np.array_equal(s2.reshape(E, H, I // 32), w2s)
 
     xd = gu.dev_bf16(li.x)
-    y = L.forward_mx(xd)
+    y = L.forward_mxfp4(xd) if fp4 else L.forward_mx(xd)
     torch.cuda.synchronize()
     st, det = L.device_status(T)
     assert st == binding.MOE_OK, (st, det)
@@ -94,8 +114,9 @@ def test_mx_layer_parity(case, o):
     within = real - offs[e_of]
     srow = (chunk0[e_of] + within // bn) * 128 * G + within % bn
     assert np.array_equal(xs[srow], hs)
-    # the layer output against the oracle's FP8 layer
-    r = o.moe_forward_mx(li.x, li.g, li.w_router, li.bias, w13c, w13s, w2c, w2s, k, renorm, cfg.eps)
+    # the layer output against the oracle's layer of the same weight format
+    fwd = o.moe_forward_mx4 if fp4 else o.moe_forward_mx
+    r = fwd(li.x, li.g, li.w_router, li.bias, w13c, w13s, w2c, w2s, k, renorm, cfg.eps)
     yg = gu.widen(y.cpu().numpy().view(np.uint16))
     err = yg - r["y64"]
     rel = np.linalg.norm(err) / np.linalg.norm(r["y64"])
@@ -111,3 +132,48 @@ def test_mx_rejects_more_than_256_experts():
     with pytest.raises(binding.MoeError) as ei:
         dl.layer.forward_mx(gu.dev_bf16(li.x))
     assert ei.value.status == binding.MOE_ERR_UNSUPPORTED
+
+
+def test_mxfp4_codes_every_value_class(o):
+    """E2M1 quantizer on rows built to hit every code, every tie between
+    neighbouring magnitudes, saturation, signed zeros, tiny and huge blocks."""
+    rng = np.random.default_rng(41)
+    mags = np.array([0.0, 0.25, 0.5, 0.75, 1.0, 1.25, 1.5, 1.75, 2.0, 2.5, 3.0, 3.5, 4.0, 5.0, 6.0, 7.0])
+    rows = []
+    for p in (-130, -100, -8, 0, 5, 100):
+        for _ in range(8):
+            v = rng.choice(mags, 32) * rng.choice([-1.0, 1.0], 32)
+            v[0] = 4.0 * rng.choice([1.0, 1.5])  # block maximum fixes the scale at 2^p
+            rows.append(v * 2.0 ** p)
+    x = torch.tensor(np.array(rows).reshape(8, -1), dtype=torch.float64).to(torch.bfloat16)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    R, K = xb.shape  # 8 x 192 -> pad K to a multiple of 128
+    xpad = np.zeros((128, 256), np.uint16)
+    xpad[:R, :K] = xb
+    codes = torch.empty(128 * 128, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(512 * 2, dtype=torch.uint8, device="cuda")
+    # W2 of a one-expert layer with H = 128 rows and I = 256: its quantizer runs on plain rows
+    s = binding.shape(1, 128, 256, 1, 1)
+    w13 = torch.zeros((1, 512, 128), dtype=torch.int16, device="cuda")
+    w2 = torch.from_numpy(xpad.view(np.int16)).cuda()
+    c13 = torch.empty(512 * 128 // 2, dtype=torch.uint8, device="cuda")
+    s13 = torch.empty(4 * 512, dtype=torch.uint8, device="cuda")
+    st = binding.moe_mxfp4_quantize_weights(s, w13.data_ptr(), w2.data_ptr(), c13.data_ptr(), s13.data_ptr(),
+                                            codes.data_ptr(), scales.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == binding.MOE_OK
+    torch.cuda.synchronize()
+    oc, os_ = o.mx4_quantize(xpad)
+    assert np.array_equal(unpack_e2m1(codes.cpu().numpy(), (128, 256)), oc)
+    assert np.array_equal(gu.ungroup_mx_scales(scales.cpu().numpy(), 128, 256), os_)
+
+
+def test_mxfp4_rejects_unaligned_codes():
+    cfg = inputs.LayerConfig(T=4, H=128, I=128, E=4, top_k=2, seed=0)
+    li = inputs.make_layer_inputs(cfg)
+    dl = gu.DeviceLayer(li)
+    L = dl.layer
+    L.quantize_mxfp4()
+    L.w13_codes4 = L.w13_codes4[16:]  # 16-byte aligned, not 32
+    with pytest.raises(binding.MoeError) as ei:
+        L.forward_mxfp4(gu.dev_bf16(li.x))
+    assert ei.value.status == binding.MOE_ERR_INVALID_ARG
