@@ -87,6 +87,9 @@ class Oracle:
         lib.oracle_moe_forward_mx4.argtypes = [i64, i64, i64, i64, i, i, d, p, p, p, p, p, p, p, p, i64, p, i,
                                                p, p, p, p]
         lib.oracle_moe_forward_mx4.restype = i
+        lib.oracle_moe_forward_mx4a4.argtypes = [i64, i64, i64, i64, i, i, d, p, p, p, p, p, p, p, p, i64, p, i,
+                                                 p, p, p, p]
+        lib.oracle_moe_forward_mx4a4.restype = i
         lib.oracle_f64_to_bf16.argtypes = [d]
         lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
         lib.oracle_f32_to_bf16.argtypes = [f]
@@ -176,6 +179,12 @@ class Oracle:
         """The FP4-weight layer (MXFP4 weights, MXFP8 tokens and activations); as moe_forward_mx."""
         return self.moe_forward_mx(x, g, w_router, bias, w13c, w13s, w2c, w2s, top_k, renorm, eps, sample,
                                    nthreads, _fn=self.lib.oracle_moe_forward_mx4)
+
+    def moe_forward_mx4a4(self, x, g, w_router, bias, w13c, w13s, w2c, w2s, top_k, renorm, eps, sample=None,
+                          nthreads=None):
+        """The MXFP4 layer (MXFP4 weights, MXFP4 tokens and activations); as moe_forward_mx."""
+        return self.moe_forward_mx(x, g, w_router, bias, w13c, w13s, w2c, w2s, top_k, renorm, eps, sample,
+                                   nthreads, _fn=self.lib.oracle_moe_forward_mx4a4)
 
     def expert_mx_f64(self, h, w13c, w13s, w2c, w2s):
         """One token (bf16 h) through one FP8 expert: (activation [I] f64 after MXFP8, output [H] f64)."""

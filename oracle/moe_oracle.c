@@ -335,6 +335,22 @@ static void mx_weight_dequantize(int wfmt, int64_t rows, int64_t K, const uint8_
     oracle_mx_dequantize(rows, K, codes, scales, out);
 }
 
+/* one row of K bf16 token values through MXFP8 (afmt 0) or MXFP4 (afmt 1)
+ * quantization and back */
+static void mx_token_roundtrip(int afmt, int64_t K, const uint16_t* x16, double* out) {
+  uint8_t* c = (uint8_t*)malloc((size_t)K);
+  uint8_t* sc = (uint8_t*)malloc((size_t)(K / 32));
+  if (afmt) {
+    oracle_mx4_quantize(1, K, x16, c, sc);
+    oracle_mx4_dequantize(1, K, c, sc, out);
+  } else {
+    oracle_mx_quantize(1, K, x16, c, sc);
+    oracle_mx_dequantize(1, K, c, sc, out);
+  }
+  free(c);
+  free(sc);
+}
+
 /* ------------------------------------------------------------------ */
 /* QK-norm, fp64                                                        */
 /* ------------------------------------------------------------------ */
@@ -576,18 +592,16 @@ static void expert_row_f64(int64_t H, int64_t I, const uint16_t* h16, const doub
   }
 }
 
-/* One token through one expert of the FP8 layer: h (bf16) quantized to MXFP8
- * along H, the weights given as MXFP8 codes and scales (wfmt 0; wfmt 1:
- * MXFP4, E2M1 codes), the bf16 SwiGLU activation quantized to MXFP8 along I;
- * products and sums in fp64.
+/* One token through one expert of the block-scaled layers: h (bf16) quantized
+ * along H to MXFP8 (afmt 0) or MXFP4 (afmt 1), the weights given as MXFP8
+ * codes and scales (wfmt 0) or MXFP4 codes (wfmt 1, E2M1, one per byte), the
+ * bf16 SwiGLU activation quantized along I in the token format; products and
+ * sums in fp64.
  *   W13c [2I, H] codes, W13s [2I, H/32] scales; W2c [H, I], W2s [H, I/32]. */
-static void expert_row_mx_f64(int wfmt, int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c,
+static void expert_row_mx_f64(int wfmt, int afmt, int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c,
                               const uint8_t* W13s, const uint8_t* W2c, const uint8_t* W2s, double* a, double* o) {
-  uint8_t* hc = (uint8_t*)malloc((size_t)H);
-  uint8_t* hs = (uint8_t*)malloc((size_t)(H / 32));
   double* hq = (double*)malloc(sizeof(double) * (size_t)H);
-  oracle_mx_quantize(1, H, h16, hc, hs);
-  oracle_mx_dequantize(1, H, hc, hs, hq);
+  mx_token_roundtrip(afmt, H, h16, hq);
   double* wrow = (double*)malloc(sizeof(double) * (size_t)(H > I ? H : I));
   double* wrow2 = (double*)malloc(sizeof(double) * (size_t)H);
   uint16_t* a16 = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
@@ -602,23 +616,20 @@ static void expert_row_mx_f64(int wfmt, int64_t H, int64_t I, const uint16_t* h1
     double silu = gate / (1.0 + exp(-gate));
     a16[i] = f64_to_bf16(silu * up);
   }
-  uint8_t* ac = (uint8_t*)malloc((size_t)I);
-  uint8_t* as = (uint8_t*)malloc((size_t)(I / 32));
-  oracle_mx_quantize(1, I, a16, ac, as);
-  oracle_mx_dequantize(1, I, ac, as, a);
+  mx_token_roundtrip(afmt, I, a16, a);
   for (int64_t n = 0; n < H; ++n) {
     mx_weight_dequantize(wfmt, 1, I, W2c + n * I, W2s + n * (I / 32), wrow);
     double acc = 0.0;
     for (int64_t i = 0; i < I; ++i) acc += a[i] * wrow[i];
     o[n] = acc;
   }
-  free(hc); free(hs); free(hq); free(wrow); free(wrow2); free(a16); free(ac); free(as);
+  free(hq); free(wrow); free(wrow2); free(a16);
 }
 
 void oracle_expert_mx_f64(int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c, const uint8_t* W13s,
                           const uint8_t* W2c, const uint8_t* W2s, double* a_out, double* o) {
   double* a = a_out ? a_out : (double*)malloc(sizeof(double) * (size_t)I);
-  expert_row_mx_f64(0, H, I, h16, W13c, W13s, W2c, W2s, a, o);
+  expert_row_mx_f64(0, 0, H, I, h16, W13c, W13s, W2c, W2s, a, o);
   if (!a_out) free(a);
 }
 
@@ -626,7 +637,7 @@ void oracle_expert_mx_f64(int64_t H, int64_t I, const uint16_t* h16, const uint8
 void oracle_expert_mx4_f64(int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c, const uint8_t* W13s,
                            const uint8_t* W2c, const uint8_t* W2s, double* a_out, double* o) {
   double* a = a_out ? a_out : (double*)malloc(sizeof(double) * (size_t)I);
-  expert_row_mx_f64(1, H, I, h16, W13c, W13s, W2c, W2s, a, o);
+  expert_row_mx_f64(1, 0, H, I, h16, W13c, W13s, W2c, W2s, a, o);
   if (!a_out) free(a);
 }
 
@@ -648,9 +659,10 @@ typedef struct {
   const uint16_t *x, *g;
   const float *Wr, *bias;
   const uint16_t *W13, *W2;
-  /* FP8 layer (when W13c != NULL): MXFP8 weights (wfmt 0) or MXFP4 weights (wfmt 1) */
+  /* block-scaled layers (when W13c != NULL): MXFP8 weights (wfmt 0) or MXFP4
+   * weights (wfmt 1); MXFP8 (afmt 0) or MXFP4 (afmt 1) tokens and activations */
   const uint8_t *W13c, *W13s, *W2c, *W2s;
-  int wfmt;
+  int wfmt, afmt;
   int64_t ns;
   const int64_t* sample;
   /* per-sample scratch / outputs */
@@ -683,7 +695,7 @@ static void fwd_expert_item(int64_t it, void* p) {
   int64_t e = c->ids[s * c->k + j];
   double* a = (double*)malloc(sizeof(double) * (size_t)c->I);
   if (c->W13c) {
-    expert_row_mx_f64(c->wfmt, c->H, c->I, c->h16 + s * c->H, c->W13c + e * 2 * c->I * c->H,
+    expert_row_mx_f64(c->wfmt, c->afmt, c->H, c->I, c->h16 + s * c->H, c->W13c + e * 2 * c->I * c->H,
                       c->W13s + e * 2 * c->I * (c->H / 32), c->W2c + e * c->H * c->I, c->W2s + e * c->H * (c->I / 32),
                       a, c->o + it * c->H);
     free(a);
@@ -708,7 +720,8 @@ static void fwd_expert_item(int64_t it, void* p) {
 static int moe_forward_any(int64_t T, int64_t H, int64_t I, int64_t E, int k, int renorm, double eps,
                            const uint16_t* x, const uint16_t* g, const float* Wr, const float* bias,
                            const uint16_t* W13, const uint16_t* W2, const uint8_t* W13c, const uint8_t* W13s,
-                           const uint8_t* W2c, const uint8_t* W2s, int wfmt, int64_t ns, const int64_t* sample,
+                           const uint8_t* W2c, const uint8_t* W2s, int wfmt, int afmt, int64_t ns,
+                           const int64_t* sample,
                            int round_inter, int nthreads, int32_t* ids, double* w, double* y64, uint16_t* y16,
                            uint16_t* h16_out, float* l32_out, double* l64_out) {
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E || ns < 0) return -1;
@@ -720,7 +733,7 @@ static int moe_forward_any(int64_t T, int64_t H, int64_t I, int64_t E, int k, in
   fwd_ctx c;
   c.T = T; c.H = H; c.I = I; c.E = E; c.k = k; c.renorm = renorm; c.round_inter = round_inter;
   c.eps = eps; c.x = x; c.g = g; c.Wr = Wr; c.bias = bias; c.W13 = W13; c.W2 = W2;
-  c.W13c = W13c; c.W13s = W13s; c.W2c = W2c; c.W2s = W2s; c.wfmt = wfmt;
+  c.W13c = W13c; c.W13s = W13s; c.W2c = W2c; c.W2s = W2s; c.wfmt = wfmt; c.afmt = afmt;
   c.ns = ns; c.sample = sample;
   c.h16 = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(ns * H));
   c.h64 = (double*)malloc(sizeof(double) * (size_t)(ns * H));
@@ -751,7 +764,7 @@ int oracle_moe_forward(int64_t T, int64_t H, int64_t I, int64_t E, int k, int re
                        const uint16_t* W13, const uint16_t* W2, int64_t ns, const int64_t* sample,
                        int round_inter, int nthreads, int32_t* ids, double* w, double* y64, uint16_t* y16,
                        uint16_t* h16_out, float* l32_out, double* l64_out) {
-  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, W13, W2, NULL, NULL, NULL, NULL, 0, ns, sample,
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, W13, W2, NULL, NULL, NULL, NULL, 0, 0, ns, sample,
                          round_inter, nthreads, ids, w, y64, y16, h16_out, l32_out, l64_out);
 }
 
@@ -764,7 +777,7 @@ int oracle_moe_forward_mx(int64_t T, int64_t H, int64_t I, int64_t E, int k, int
                           int64_t ns, const int64_t* sample, int nthreads, int32_t* ids, double* w, double* y64,
                           uint16_t* y16) {
   if (H % 32 || I % 32 || !W13c || !W13s || !W2c || !W2s) return -1;
-  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, 0, ns, sample,
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, 0, 0, ns, sample,
                          1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
 }
 
@@ -776,8 +789,21 @@ int oracle_moe_forward_mx4(int64_t T, int64_t H, int64_t I, int64_t E, int k, in
                            int64_t ns, const int64_t* sample, int nthreads, int32_t* ids, double* w, double* y64,
                            uint16_t* y16) {
   if (H % 32 || I % 32 || !W13c || !W13s || !W2c || !W2s) return -1;
-  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, 1, ns, sample,
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, 1, 0, ns, sample,
                          1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
 }
 
-int oracle_version(void) { return 3; }
+/* The MXFP4 layer: MXFP4 expert weights and MXFP4 tokens and activations
+ * (h and the SwiGLU activation quantized to E2M1 codes with E8M0 scales per 32
+ * elements), otherwise as oracle_moe_forward_mx. */
+int oracle_moe_forward_mx4a4(int64_t T, int64_t H, int64_t I, int64_t E, int k, int renorm, double eps,
+                             const uint16_t* x, const uint16_t* g, const float* Wr, const float* bias,
+                             const uint8_t* W13c, const uint8_t* W13s, const uint8_t* W2c, const uint8_t* W2s,
+                             int64_t ns, const int64_t* sample, int nthreads, int32_t* ids, double* w, double* y64,
+                             uint16_t* y16) {
+  if (H % 32 || I % 32 || !W13c || !W13s || !W2c || !W2s) return -1;
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, 1, 1, ns,
+                         sample, 1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
+}
+
+int oracle_version(void) { return 4; }

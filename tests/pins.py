@@ -369,6 +369,34 @@ def pin_mx4_layer_restated(o):
     assert 1e-3 < rel < 0.5
 
 
+def pin_mx4a4_layer_restated(o):
+    # the MXFP4 layer (FP4 weights, FP4 tokens and activations) against a
+    # restatement: numpy MXFP4 round trips of the weights, of h and of the bf16
+    # activation, fp64 products and sums
+    T, H, I, E, k = 3, 64, 96, 4, 2
+    li = rand_layer(T, H, I, E, seed=27)
+    w13c, w13s = o.mx4_quantize(li.w13)
+    w2c, w2s = o.mx4_quantize(li.w2)
+    res = o.moe_forward_mx4a4(li.x, li.g, li.w_router, None, w13c, w13s, w2c, w2s, k, True, 1e-6)
+    ref = o.moe_forward(li.x, li.g, li.w_router, None, li.w13, li.w2, k, True, 1e-6)
+    assert np.array_equal(res["ids"], ref["ids"])
+    W13 = _np_mx4_dequant(widen(li.w13))
+    W2 = _np_mx4_dequant(widen(li.w2))
+    y = np.zeros((T, H))
+    for t in range(T):
+        hq = _np_mx4_dequant(widen(ref["h16"][t]))
+        for j in range(k):
+            e = int(res["ids"][t, j])
+            gate = W13[e, :I] @ hq
+            up = W13[e, I:] @ hq
+            a = widen(torch_bf16_bits_from_f64(gate / (1 + np.exp(-gate)) * up))
+            y[t] += res["w"][t, j] * (W2[e] @ _np_mx4_dequant(a))
+    assert np.allclose(res["y64"], y, rtol=1e-12, atol=1e-15)
+    # the FP4 tokens move the result further from the W4A8 layer's
+    w4a8 = o.moe_forward_mx4(li.x, li.g, li.w_router, None, w13c, w13s, w2c, w2s, k, True, 1e-6)
+    assert np.linalg.norm(res["y64"] - w4a8["y64"]) > 1e-3 * np.linalg.norm(w4a8["y64"])
+
+
 # -------------------------------------------------------------------- router
 
 def pin_router_f64_numpy(o):

@@ -43,9 +43,9 @@ MUTATIONS = {
     "e4m3_round_half_up": ("double q = nearbyint(a / ldexp(1.0, ex - 3));", "double q = floor(a / ldexp(1.0, ex - 3) + 0.5);"),
     "e4m3_no_saturation": ("      e = 15;\n      m = 6;", "      e = 15;\n      m = 7;"),
     "e4m3_subnormal_scale": ("double v = e == 0 ? ldexp((double)m, -9)", "double v = e == 0 ? ldexp((double)m, -10)"),
-    "mx_act_not_quantized": ("  oracle_mx_quantize(1, I, a16, ac, as);\n  oracle_mx_dequantize(1, I, ac, as, a);",
+    "mx_act_not_quantized": ("  mx_token_roundtrip(afmt, I, a16, a);",
                              "  for (int64_t i = 0; i < I; ++i) a[i] = bf16_to_f64(a16[i]);"),
-    "mx_token_not_quantized": ("  oracle_mx_dequantize(1, H, hc, hs, hq);",
+    "mx_token_not_quantized": ("  mx_token_roundtrip(afmt, H, h16, hq);",
                                "  for (int64_t j = 0; j < H; ++j) hq[j] = bf16_to_f64(h16[j]);"),
     "mx4_emax_1": ("int ex = mx_block_exponent_of(amax, 2);", "int ex = mx_block_exponent_of(amax, 1);"),
     "e2m1_tie_to_odd": ("if (d < bd || (d == bd && (c & 1) == 0)) {", "if (d < bd || (d == bd && (c & 1) == 1)) {"),
@@ -54,6 +54,8 @@ MUTATIONS = {
     "mx4_weights_as_e4m3": ("  if (wfmt)\n    oracle_mx4_dequantize(rows, K, codes, scales, out);",
                             "  if (0)\n    oracle_mx4_dequantize(rows, K, codes, scales, out);"),
     "e2m1_sign_dropped": ("  return (uint8_t)((sgn << 3) | best);", "  return (uint8_t)best;"),
+    "mx4a4_tokens_as_mxfp8": ("  if (afmt) {\n    oracle_mx4_quantize(1, K, x16, c, sc);",
+                              "  if (0) {\n    oracle_mx4_quantize(1, K, x16, c, sc);"),
     "qk_bias_dropped": ("(bf16_to_f64(w[j]) + weight_bias)", "(bf16_to_f64(w[j]))"),
     "qk_bias_multiplied": ("(bf16_to_f64(w[j]) + weight_bias)", "(bf16_to_f64(w[j]) * weight_bias)"),
     "qk_eps_dropped": ("sqrt(ss / (double)D + eps)", "sqrt(ss / (double)D)"),
