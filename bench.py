@@ -447,21 +447,22 @@ def run_ours(args, wl, world, rank, local):
     setup_s = time.time() - t_setup
 
     ff, fc = args.fused_front, args.fused_combine
-    mx = "mxfp4" if args.mxfp4 else args.mx  # weight format for the byte counts
-    if args.mxfp4:
+    mx = "mxfp4a4" if args.mxfp4a4 else "mxfp4" if args.mxfp4 else args.mx  # formats for the byte counts
+    if args.mxfp4 or args.mxfp4a4:
         layer.quantize_mxfp4()
     elif mx:
         layer.quantize_mx()
 
     def fwd(x, y, events=None):
-        if args.mxfp4:
-            return layer.forward_mxfp4(x, y, events=events)
+        if args.mxfp4 or args.mxfp4a4:
+            return layer.forward_mxfp4(x, y, events=events, fp4_tokens=args.mxfp4a4)
         if mx:
             return layer.forward_mx(x, y, events=events)
         return layer.forward(x, y, events=events, fused_front=ff, fused_combine=fc)
 
     def kpc(T):  # our kernels per layer call
-        call = (binding.MOE_CALL_FORWARD_MXFP4 if args.mxfp4 else binding.MOE_CALL_FORWARD_MX if mx else
+        call = (binding.MOE_CALL_FORWARD_MXFP4A4 if args.mxfp4a4 else
+                binding.MOE_CALL_FORWARD_MXFP4 if args.mxfp4 else binding.MOE_CALL_FORWARD_MX if mx else
                 binding.MOE_CALL_FORWARD_FUSED_FRONT if ff else
                 binding.MOE_CALL_FORWARD_FUSED_COMBINE if fc else binding.MOE_CALL_FORWARD)
         return binding.kernels_per_call(T, H, wl["I"], wl["E"], wl["k"], call)
@@ -568,7 +569,10 @@ def run_ours(args, wl, world, rank, local):
         fl = accounting.layer_flops
         per = [fl(T, H, wl["I"], wl["E"], wl["k"])["gemm1" if dom == "gemm_gate_up_swiglu" else "gemm2"]
                for T in Ts]
-        if mx:  # block-scaled FP8 / FP4xFP8 MMAs (kind::mxf8f6f4, the FP8 rate): the measured bf16 peak x
+        if mx == "mxfp4a4":  # kind::mxf4: the measured bf16 peak x the nominal dense ratio 13.5 / 2.25
+            roof = roofline("tensor", sum(per) / len(per), avg_s, 6.0 * peaks["bf16_tflops"], None)
+            roof["peak_source"] = f"6 x bf16_tflops ({peak_kind}; nominal dense fp4 / bf16 ratio)"
+        elif mx:  # block-scaled FP8 / FP4xFP8 MMAs (kind::mxf8f6f4, the FP8 rate): the measured bf16 peak x
             # the nominal dense ratio 4.5 / 2.25
             roof = roofline("tensor", sum(per) / len(per), avg_s, 2.0 * peaks["bf16_tflops"], None)
             roof["peak_source"] = f"2 x bf16_tflops ({peak_kind}; nominal dense fp8 / bf16 ratio)"
@@ -614,12 +618,15 @@ def run_ours(args, wl, world, rank, local):
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": ("mxfp4 (e2m1 + e8m0 per 32) x mxfp8, fp32 accumulation" if args.mxfp4 else
+        "vs_baseline": None, "dtype": ("mxfp4 (e2m1 + e8m0 per 32) x mxfp4, fp32 accumulation" if args.mxfp4a4 else
+                  "mxfp4 (e2m1 + e8m0 per 32) x mxfp8, fp32 accumulation" if args.mxfp4 else
                   "mxfp8 (e4m3 + e8m0 per 32) x mxfp8, fp32 accumulation" if mx else "bf16"),
         "data": "synthetic (seeded generator; random-init weights)",
         "config": {"workload": wl["label"], "tokens_per_step": tokens_per_step,
                    "layer_calls_per_step": len(Ts),
-                   "expert_weights": ("MXFP4 (moe_forward_mxfp4; weight bytes counted as codes + scales)"
+                   "expert_weights": ("MXFP4 weights and tokens (moe_forward_mxfp4a4; bytes counted as codes + "
+                                      "scales)" if args.mxfp4a4 else
+                                      "MXFP4 (moe_forward_mxfp4; weight bytes counted as codes + scales)"
                                       if args.mxfp4 else
                                       "MXFP8 (moe_forward_mx; weight bytes counted as codes + scales)" if mx
                                       else "bf16"),
@@ -656,6 +663,8 @@ def main():
                     help="CPU oracle sample: at most this many tokens of each batch per step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum timed CPU-oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mxfp4a4", action="store_true",
+                    help="time moe_forward_mxfp4a4: the MXFP4 layer (MXFP4 weights, token rows and activations)")
     ap.add_argument("--mxfp4", action="store_true",
                     help="time moe_forward_mxfp4: MXFP4 expert weights, MXFP8 token rows and activations")
     ap.add_argument("--mx", action="store_true",
@@ -665,8 +674,8 @@ def main():
     ap.add_argument("--fused-combine", action="store_true",
                     help="time moe_forward_fused_combine (the combine in the down GEMM's epilogue)")
     args = ap.parse_args()
-    if sum([args.mx, args.mxfp4, args.fused_front, args.fused_combine]) > 1:
-        ap.error("--mx, --mxfp4, --fused-front and --fused-combine are separate entry points; pick one")
+    if sum([args.mx, args.mxfp4, args.mxfp4a4, args.fused_front, args.fused_combine]) > 1:
+        ap.error("--mx, --mxfp4, --mxfp4a4, --fused-front and --fused-combine are separate entry points; pick one")
     if args.warmup < 3:
         print("bench: at least 3 warm-up steps are required; using 3", file=sys.stderr)
         args.warmup = 3

@@ -132,14 +132,16 @@ MOE_API moe_status moe_kernels_per_call(const moe_shape* shape, int32_t* count);
 /* The same for each entry point: call = MOE_CALL_FORWARD (moe_forward,
  * moe_forward_events, moe_forward_static_scratch), MOE_CALL_FORWARD_FUSED_FRONT
  * (moe_forward_fused_front), MOE_CALL_FORWARD_MX (moe_forward_mx),
- * MOE_CALL_FORWARD_FUSED_COMBINE (moe_forward_fused_combine) or
- * MOE_CALL_FORWARD_MXFP4 (moe_forward_mxfp4).  Another value of call:
- * MOE_ERR_INVALID_ARG.  Host-only. */
+ * MOE_CALL_FORWARD_FUSED_COMBINE (moe_forward_fused_combine),
+ * MOE_CALL_FORWARD_MXFP4 (moe_forward_mxfp4) or MOE_CALL_FORWARD_MXFP4A4
+ * (moe_forward_mxfp4a4).  Another value of call: MOE_ERR_INVALID_ARG.
+ * Host-only. */
 #define MOE_CALL_FORWARD 0
 #define MOE_CALL_FORWARD_FUSED_FRONT 1
 #define MOE_CALL_FORWARD_MX 2
 #define MOE_CALL_FORWARD_FUSED_COMBINE 3
 #define MOE_CALL_FORWARD_MXFP4 4
+#define MOE_CALL_FORWARD_MXFP4A4 5
 MOE_API moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t* count);
 
 /* moe_forward, plus CUDA events recorded on `stream` around the kernels:
@@ -375,6 +377,19 @@ MOE_API moe_status moe_forward_mxfp4(const moe_shape* shape, const moe_bf16* x, 
                                      const uint8_t* w13_scales, const uint8_t* w2_codes, const uint8_t* w2_scales,
                                      moe_bf16* y, void* workspace, size_t workspace_bytes, moe_stream_t stream,
                                      void* const* events, int32_t n_events);
+
+/* The MXFP4 layer (W4A4): as moe_forward_mxfp4 (the same MXFP4 weights from
+ * moe_mxfp4_quantize_weights, workspace, views and events), with each expert's
+ * input rows and its SwiGLU activations quantized to MXFP4 by the same rule
+ * as the weights, and both expert GEMMs on packed E2M1 operands (tcgen05.mma
+ * kind::mxf4, two E8M0 scales per row per MMA of K = 64, fp32 accumulation).
+ * H and I multiples of 256 (else MOE_ERR_UNSUPPORTED); weight codes 32-byte
+ * aligned. */
+MOE_API moe_status moe_forward_mxfp4a4(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                                       const float* w_router, const float* router_bias, const uint8_t* w13_codes,
+                                       const uint8_t* w13_scales, const uint8_t* w2_codes, const uint8_t* w2_scales,
+                                       moe_bf16* y, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                                       void* const* events, int32_t n_events);
 
 /* QK-norm, in place: RMSNorm of every attention head of Q and of K
  * ("CuTeDSL chez Perplexity", "Norme QK"):

@@ -50,10 +50,16 @@ def mx4_bytes(n_elems: int) -> int:
 
 
 def weight_bytes(n_elems: int, mx) -> int:
-    """Bytes of n weight elements: bf16 (mx false), MXFP8 (mx true) or MXFP4 (mx == "mxfp4")."""
-    if mx == "mxfp4":
+    """Bytes of n weight elements: bf16 (mx false), MXFP8 (mx true) or MXFP4
+    (mx == "mxfp4", FP4 weights with MXFP8 tokens, or "mxfp4a4", the MXFP4 layer)."""
+    if mx in ("mxfp4", "mxfp4a4"):
         return mx4_bytes(n_elems)
     return mx_bytes(n_elems) if mx else n_elems * BF16
+
+
+def token_bytes(n_elems: int, mx) -> int:
+    """Bytes of n quantized token elements: MXFP4 in the MXFP4 layer, else MXFP8."""
+    return mx4_bytes(n_elems) if mx == "mxfp4a4" else mx_bytes(n_elems)
 
 
 def expert_weight_bytes(H: int, I: int, mx=False) -> dict:
@@ -87,13 +93,14 @@ def layer_flops(T: int, H: int, I: int, E: int, k: int) -> dict:
 def gemm1_kernel_bytes(T: int, H: int, I: int, k: int, touched: int, mx=False) -> int:
     """Algorithmic bytes of the gate/up expert GEMM: touched W13, the T*k
     gathered token rows read once, the T*k activation rows (bf16) written once.
-    mx: MXFP8 (true) or MXFP4 ("mxfp4") weights, MXFP8 token rows."""
+    mx: MXFP8 (true) or MXFP4 ("mxfp4") weights with MXFP8 token rows, or
+    the MXFP4 layer ("mxfp4a4")."""
     if mx:
-        return weight_bytes(touched * 2 * I * H, mx) + mx_bytes(T * k * H) + T * k * I * BF16
+        return weight_bytes(touched * 2 * I * H, mx) + token_bytes(T * k * H, mx) + T * k * I * BF16
     return touched * 2 * I * H * BF16 + T * k * H * BF16 + T * k * I * BF16
 
 
 def gemm2_kernel_bytes(T: int, H: int, I: int, k: int, touched: int, mx=False) -> int:
     if mx:
-        return weight_bytes(touched * H * I, mx) + mx_bytes(T * k * I) + T * k * H * BF16
+        return weight_bytes(touched * H * I, mx) + token_bytes(T * k * I, mx) + T * k * H * BF16
     return touched * H * I * BF16 + T * k * I * BF16 + T * k * H * BF16

@@ -82,6 +82,7 @@ def load(build: bool = True):
             lib.moe_mxfp4_weight_sizes.argtypes = [sp, psz, psz, psz, psz]
             lib.moe_mxfp4_quantize_weights.argtypes = [sp, p, p, p, p, p, p, p]
             lib.moe_forward_mxfp4.argtypes = [sp, p, p, p, p, p, p, p, p, p, p, sz, p, p, i32]
+            lib.moe_forward_mxfp4a4.argtypes = [sp, p, p, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_forward_fused_front.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_forward_fused_combine.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_status_string.argtypes = [ctypes.c_int]
@@ -92,7 +93,8 @@ def load(build: bool = True):
                       "moe_selftest_wait_timeout",
                       "moe_qk_norm", "moe_mx_weight_sizes", "moe_mx_quantize_weights", "moe_workspace_size_mx",
                       "moe_workspace_views_mx", "moe_forward_mx", "moe_forward_fused_combine",
-                      "moe_mxfp4_weight_sizes", "moe_mxfp4_quantize_weights", "moe_forward_mxfp4"):
+                      "moe_mxfp4_weight_sizes", "moe_mxfp4_quantize_weights", "moe_forward_mxfp4",
+                      "moe_forward_mxfp4a4"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -132,7 +134,7 @@ def moe_kernels_per_call(s: MoeShape) -> tuple[int, int]:
 
 
 (MOE_CALL_FORWARD, MOE_CALL_FORWARD_FUSED_FRONT, MOE_CALL_FORWARD_MX, MOE_CALL_FORWARD_FUSED_COMBINE,
- MOE_CALL_FORWARD_MXFP4) = 0, 1, 2, 3, 4
+ MOE_CALL_FORWARD_MXFP4, MOE_CALL_FORWARD_MXFP4A4) = 0, 1, 2, 3, 4, 5
 
 
 def moe_kernels_per_call_of(s: MoeShape, call: int) -> tuple[int, int]:
@@ -272,6 +274,16 @@ def moe_forward_mxfp4(s: MoeShape, x, g_norm, w_router, router_bias, w13_codes, 
                                     w2_codes, w2_scales, y, workspace, workspace_bytes, stream, arr, n)
 
 
+def moe_forward_mxfp4a4(s: MoeShape, x, g_norm, w_router, router_bias, w13_codes, w13_scales, w2_codes, w2_scales,
+                        y, workspace, workspace_bytes, stream, events=None) -> int:
+    if events is None:
+        arr, n = None, 0
+    else:
+        arr, n = (ctypes.c_void_p * len(events))(*events), len(events)
+    return load().moe_forward_mxfp4a4(ctypes.byref(s), x, g_norm, w_router, router_bias, w13_codes, w13_scales,
+                                      w2_codes, w2_scales, y, workspace, workspace_bytes, stream, arr, n)
+
+
 def _ptr(t):
     return None if t is None else t.data_ptr()
 
@@ -374,20 +386,23 @@ class MoeLayer:
         if st != MOE_OK:
             raise MoeError(st, "moe_mxfp4_quantize_weights")
 
-    def forward_mxfp4(self, x, y=None, stream=None, events=None):
-        """y = layer(x) with the MXFP4 expert weights (call quantize_mxfp4 first)."""
+    def forward_mxfp4(self, x, y=None, stream=None, events=None, fp4_tokens=False):
+        """y = layer(x) with the MXFP4 expert weights (call quantize_mxfp4 first);
+        fp4_tokens: the MXFP4 layer, with token rows and activations in MXFP4
+        too (moe_forward_mxfp4a4), else MXFP8 tokens (moe_forward_mxfp4)."""
         import torch
         T = x.shape[0]
         self.ensure_capacity(T)
         if y is None:
             y = torch.empty((T, self.H), dtype=x.dtype, device=x.device)
         s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
-        st = moe_forward_mxfp4(self.shape(T), _ptr(x), _ptr(self.g_norm), _ptr(self.w_router), _ptr(self.bias),
-                               _ptr(self.w13_codes4), _ptr(self.w13_scales4), _ptr(self.w2_codes4),
-                               _ptr(self.w2_scales4), _ptr(y), _ptr(self.workspace), self.workspace_bytes_mx(T), s,
-                               events)
+        fn, name = (moe_forward_mxfp4a4, "moe_forward_mxfp4a4") if fp4_tokens else (moe_forward_mxfp4,
+                                                                                   "moe_forward_mxfp4")
+        st = fn(self.shape(T), _ptr(x), _ptr(self.g_norm), _ptr(self.w_router), _ptr(self.bias),
+                _ptr(self.w13_codes4), _ptr(self.w13_scales4), _ptr(self.w2_codes4), _ptr(self.w2_scales4), _ptr(y),
+                _ptr(self.workspace), self.workspace_bytes_mx(T), s, events)
         if st != MOE_OK:
-            raise MoeError(st, "moe_forward_mxfp4")
+            raise MoeError(st, name)
         return y
 
     def workspace_bytes_mx(self, T) -> int:

@@ -75,7 +75,8 @@ constexpr int kTabMaxE = 256;
 constexpr int kABytes = kWeightBoxRows * kBlockK * 2;  // 16 KB weight tile per stage
 constexpr int kTokRowBytes = kBlockK * 2;              // 128 B per token row per stage
 
-template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
+          bool A4 = false>
 struct GemmCfg {
   // a CTA pair splits the unit's tokens: each CTA holds half of the B tile
   static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * kTokRowBytes;
@@ -83,14 +84,21 @@ struct GemmCfg {
   // each stage also carries its scale tiles: 512 bytes for the 128 weight rows
   // and 512 per 128 token rows of the unit's token chunk (a CTA of a pair needs
   // the scales of all 256 tokens: the pair MMA reads them from its own TMEM)
-  static constexpr int kKPerStage = MX ? 128 : kBlockK;
+  // A4 (the MXFP4 layer): tokens are packed E2M1 codes too, so a 128-byte row
+  // holds 256 elements of K, a stage issues 4 kind::mxf4 MMAs of K = 64 and
+  // carries two scale tiles (two 128-element chunks) per operand
+  static constexpr int kKPerStage = A4 ? 256 : MX ? 128 : kBlockK;
+  static constexpr int kBoxX = MX ? 128 : kBlockK;    // TMA x coordinate per stage (elements of the map's type)
+  static constexpr int kChunks = A4 ? 2 : 1;          // 128-element scale chunks per stage
   // MXFP4 weights (W4): two E2M1 codes per byte in global memory; the TMA's
   // 16U4_ALIGN16B type spreads each 8 bytes (16 codes) over 16 bytes of shared
   // memory, so the tile's image and descriptors are those of an FP8 tile while
   // the barrier counts only the 64 data bytes per 128-element row
-  static constexpr int kWTxBytes = W4 ? kABytes / 2 : kABytes;
-  static constexpr int kSfTokBytes = MX ? (BN > 128 ? 1024 : 512) : 0;
-  static constexpr int kSfBytes = MX ? 512 + kSfTokBytes : 0;
+  static constexpr int kWTxBytes = (W4 && !A4) ? kABytes / 2 : kABytes;
+  static constexpr int kSfTokTiles = MX ? (BN > 128 ? 2 : 1) : 0;  // 512-byte token scale tiles per chunk
+  static constexpr int kSfTokBytes = kSfTokTiles * 512 * kChunks;
+  static constexpr int kSfWBytes = MX ? 512 * kChunks : 0;
+  static constexpr int kSfBytes = kSfWBytes + kSfTokBytes;
   static constexpr int kStageBytes = (kABytes + kBBytes + kSfBytes + 1023) / 1024 * 1024;
   static constexpr int kAccCols = BN;  // fp32 TMEM columns per accumulator buffer
   // accumulator buffers: two (the epilogue of one unit overlaps the MMAs of the
@@ -120,7 +128,10 @@ struct GemmCfg {
   static_assert(!MX || (PAIR ? (BN == 256 || BN == 128) : (BN % 32 == 0 && BN <= 128)),
                 "MXFP8 units: one CTA with 32..128 tokens, or a CTA pair with 128 or 256");
   static_assert(kAccBufs == 2 || (MX && PAIR), "a single accumulator buffer only for MXFP8 pairs");
-  static_assert(!W4 || MX, "FP4 weights only with block-scaled MXFP8 tokens");
+  static_assert(!W4 || MX, "FP4 weights only with block-scaled tokens");
+  static_assert(!A4 || W4, "FP4 tokens only with FP4 weights");
+  static_assert(!MX || (4 * kChunks <= 16 && 16 + 4 * kChunks * kSfTokTiles <= kSfCols),
+                "scale columns of a stage: weight tiles from +0, token tiles from +16");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
   static_assert(kTmemNeed <= 512, "TMEM has 512 columns");
   static_assert((2 * STAGES + 7) * 8 + 32 <= kBarBytes, "barrier area");
@@ -295,12 +306,13 @@ __device__ __noinline__ bool combine_unit(const ExpertGemmArgs& a, const Unit& u
   return true;
 }
 
-template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false>
-__global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4>::kThreads, 1)
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
+          bool A4 = false>
+__global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4>::kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_sx,
                        const ExpertGemmArgs args) {
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
@@ -408,24 +420,28 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
       // gate/up A tile: box {64 K, 16 rows, gate+up, 4 groups, 1 expert}
       auto load_gate_up = [&](void* dst, int st, int kb, int tile, int e, uint64_t pol) {
         if (PAIR)
-          tma_load_5d_pair(dst, &tm_w, full_cl + 8u * st, kb * C::kKPerStage, 0, 0, tile * 4, e, pol);
+          tma_load_5d_pair(dst, &tm_w, full_cl + 8u * st, kb * C::kBoxX, 0, 0, tile * 4, e, pol);
         else
-          tma_load_5d(dst, &tm_w, &full[st], kb * C::kKPerStage, 0, 0, tile * 4, e, pol);
+          tma_load_5d(dst, &tm_w, &full[st], kb * C::kBoxX, 0, 0, tile * 4, e, pol);
       };
       // chunk: the unit's token chunk (MXFP8 token scales are stored per chunk)
       auto load_tokens = [&](int st, int kb, int tok0, int rows, int chunk) {
         uint8_t* sb = smem + st * C::kStageBytes + kABytes;
         for (int r = 0; r < rows; r += TOKBOX)
-          load_2d(sb + r * kTokRowBytes, &tm_x, st, kb * C::kKPerStage, tok0 + r, pol_x);
+          load_2d(sb + r * kTokRowBytes, &tm_x, st, kb * C::kBoxX, tok0 + r, pol_x);
         if (MX && PAIR) {
-          // the 512-byte scale tiles of the whole token chunk (one per 128 tokens),
-          // in each CTA (tensor map tm_sx: one tile = a box of 2 rows x 256 bytes)
-          constexpr int G = C::kSfTokBytes / 512;
-          for (int h = 0; h < G; ++h)
-            load_2d(sb + C::kBBytes + 512 + 512 * h, &tm_sx, st, 0, 2 * ((G * chunk + h) * kblocks + kb), pol_x);
-        } else if (MX) {
-          bulk_load(sb + C::kBBytes + 512, args.x_scales + (static_cast<size_t>(chunk) * kblocks + kb) * 512, 512,
-                    &full[st], pol_x);
+          // the 512-byte scale tiles of the whole token chunk (one per 128 tokens
+          // and 128-element K chunk; tile (h, c) at 512 (c G + h)), in each CTA
+          // (tensor map tm_sx: one tile = a box of 2 rows x 256 bytes)
+          constexpr int G = C::kSfTokTiles;
+          for (int c = 0; c < C::kChunks; ++c)
+            for (int h = 0; h < G; ++h)
+              load_2d(sb + C::kBBytes + C::kSfWBytes + 512 * (c * G + h), &tm_sx, st, 0,
+                      2 * (((G * chunk + h) * kblocks + kb) * C::kChunks + c), pol_x);
+        } else if (MX) {  // one tile per K chunk, the chunks of a stage adjacent
+          bulk_load(sb + C::kBBytes + C::kSfWBytes,
+                    args.x_scales + (static_cast<size_t>(chunk) * kblocks + kb) * C::kChunks * 512,
+                    512 * C::kChunks, &full[st], pol_x);
         }
       };
       auto resolve_deps = [&]() {
@@ -465,16 +481,18 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
           if (SWIGLU) {  // 16 gate rows, the matching 16 up rows, x 4
             load_gate_up(sa, stage, kb, tile, un.e, pol_w);
           } else {
-            load_2d(sa, &tm_w, stage, kb * C::kKPerStage, wrow, pol_w);
+            load_2d(sa, &tm_w, stage, kb * C::kBoxX, wrow, pol_w);
           }
           if (MX) {  // the weight tile's scales (static: loaded before the parent kernel ends)
             const int wtiles = PAIR ? 2 * args.tiles_per_expert : args.tiles_per_expert;  // 128-row tiles per expert
-            const int64_t wt = static_cast<int64_t>(un.e * wtiles + tile) * kblocks + kb;
-            if (PAIR)
-              load_2d(sa + kABytes + C::kBBytes, &tm_sw, stage, 0, static_cast<int>(2 * wt), pol_w);
-            else
-              bulk_load(sa + kABytes + C::kBBytes, args.w_scales + static_cast<size_t>(wt) * 512, 512, &full[stage],
-                        pol_w);
+            const int64_t wt = (static_cast<int64_t>(un.e * wtiles + tile) * kblocks + kb) * C::kChunks;
+            if (PAIR) {
+              for (int c = 0; c < C::kChunks; ++c)
+                load_2d(sa + kABytes + C::kBBytes + 512 * c, &tm_sw, stage, 0, static_cast<int>(2 * (wt + c)), pol_w);
+            } else {
+              bulk_load(sa + kABytes + C::kBBytes, args.w_scales + static_cast<size_t>(wt) * 512, 512 * C::kChunks,
+                        &full[stage], pol_w);
+            }
           }
           if (deps_ready) {
             load_tokens(stage, kb, tok_first, tok_rows, chunk);
@@ -545,25 +563,43 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
                 tmem_base + static_cast<uint32_t>(C::kAccBufs * C::kAccCols + stage * C::kSfCols);
             const uint32_t sf_s = sb + C::kBBytes;
             const uint32_t sfb_t = sf_t + 16;
-            if (PAIR) {
-              tmem_cp_32x128b_x4_pair(sf_t, sf_s);
-              tmem_cp_32x128b_x4_pair(sfb_t, sf_s + 512);  // tokens 0..127: columns +0..+3
-              if (C::kSfTokBytes > 512)
-                tmem_cp_32x128b_x4_pair(sfb_t + 4, sf_s + 1024);  // tokens 128..255: columns +4..+7
-            } else {
-              tmem_cp_32x128b_x4(sf_t, sf_s);
-              tmem_cp_32x128b_x4(sfb_t, sf_s + 512);
+            // weight tile of chunk c -> columns +4c; token tile (h, c) -> +16 + 4 (c G + h)
+            // (tokens 128h .. 128h+127 of chunk c)
+            constexpr int G = C::kSfTokTiles;
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) {
+              if (PAIR)
+                tmem_cp_32x128b_x4_pair(sf_t + 4 * c, sf_s + 512 * c);
+              else
+                tmem_cp_32x128b_x4(sf_t + 4 * c, sf_s + 512 * c);
+#pragma unroll
+              for (int h = 0; h < G; ++h) {
+                const uint32_t src = sf_s + C::kSfWBytes + 512 * (c * G + h);
+                if (PAIR)
+                  tmem_cp_32x128b_x4_pair(sfb_t + 4 * (c * G + h), src);
+                else
+                  tmem_cp_32x128b_x4(sfb_t + 4 * (c * G + h), src);
+              }
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
-              const uint32_t id = idesc_mxf8(PAIR ? 256 : 128, static_cast<uint32_t>(n_mma), k, k, W4 ? kFmtE2M1 : 0);
-              if (PAIR)
-                mma_mxf8_ss_pair(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), id, sf_t,
-                                 sfb_t, accum);
-              else
-                mma_mxf8_ss(d_acc, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32), id, sf_t, sfb_t,
-                            accum);
+              const uint64_t ad = sdesc_kmajor_sw128(sa + k * 32), bd = sdesc_kmajor_sw128(sb + k * 32);
+              if (A4) {  // MMA k: K elements 64k .. 64k+63 = chunk k/2, blocks 2 (k&1), +1
+                const uint32_t c = static_cast<uint32_t>(k >> 1), sid = 2u * static_cast<uint32_t>(k & 1);
+                const uint32_t id = idesc_mxf4(PAIR ? 256 : 128, static_cast<uint32_t>(n_mma), sid, sid);
+                if (PAIR)
+                  mma_mxf4_ss_pair(d_acc, ad, bd, id, sf_t + 4 * c, sfb_t + 4 * G * c, accum);
+                else
+                  mma_mxf4_ss(d_acc, ad, bd, id, sf_t + 4 * c, sfb_t + 4 * G * c, accum);
+              } else {
+                const uint32_t id =
+                    idesc_mxf8(PAIR ? 256 : 128, static_cast<uint32_t>(n_mma), k, k, W4 ? kFmtE2M1 : 0);
+                if (PAIR)
+                  mma_mxf8_ss_pair(d_acc, ad, bd, id, sf_t, sfb_t, accum);
+                else
+                  mma_mxf8_ss(d_acc, ad, bd, id, sf_t, sfb_t, accum);
+              }
             }
           } else {
 #pragma unroll
@@ -778,13 +814,14 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
   }
 }
 
-template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false>
+template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
+          bool A4 = false>
 cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, int num_sms,
                                cudaStream_t stream, const CUtensorMap* tsw = nullptr,
                                const CUtensorMap* tsx = nullptr) {
   static const CUtensorMap kNoMap = {};  // the scale maps of MXFP8 pairs; unused elsewhere
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4>;
-  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4>;
+  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4>;
   static int configured_device = -1;
   static int max_pairs = 0;  // CTA pairs that fit on the configured device at once
   int dev = 0;
@@ -852,23 +889,24 @@ constexpr int kMxPairBn = 256;                              // tokens per pair u
 constexpr int kMxPairStages = kMxPairBn == 256 ? 6 : 8;     // 34 KB / 25 KB stages per CTA
 constexpr int kMxPairTokBox = kMxPairBn / 2;                // each CTA loads half of the unit's tokens
 
-// The block-scaled GEMMs of one tile plan; W4: E2M1 weight codes.
-template <bool SWIGLU, bool W4>
+// The block-scaled GEMMs of one tile plan; W4: E2M1 weight codes; A4: E2M1
+// token codes too (kind::mxf4).
+template <bool SWIGLU, bool W4, bool A4 = false>
 cudaError_t launch_mx(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& tsw, const CUtensorMap& tsx,
                       const ExpertGemmArgs& a, GemmPlan plan, int num_sms, cudaStream_t stream) {
   switch (plan) {
     case GemmPlan::kSmall:
-      return launch_expert_gemm<SWIGLU, kMxBn[0], kMxStages[0], kTokBox[0], false, true, W4>(tw, tx, a, num_sms,
-                                                                                            stream);
+      return launch_expert_gemm<SWIGLU, kMxBn[0], kMxStages[0], kTokBox[0], false, true, W4, A4>(tw, tx, a,
+                                                                                                num_sms, stream);
     case GemmPlan::kMid:
-      return launch_expert_gemm<SWIGLU, kMxBn[1], kMxStages[1], kTokBox[1], false, true, W4>(tw, tx, a, num_sms,
-                                                                                            stream);
+      return launch_expert_gemm<SWIGLU, kMxBn[1], kMxStages[1], kTokBox[1], false, true, W4, A4>(tw, tx, a,
+                                                                                                num_sms, stream);
     default:
       if (a.pair)
-        return launch_expert_gemm<SWIGLU, kMxPairBn, kMxPairStages, kMxPairTokBox, true, true, W4>(
+        return launch_expert_gemm<SWIGLU, kMxPairBn, kMxPairStages, kMxPairTokBox, true, true, W4, A4>(
             tw, tx, a, num_sms, stream, &tsw, &tsx);
-      return launch_expert_gemm<SWIGLU, kMxBn[2], kMxStages[2], kTokBox[2], false, true, W4>(tw, tx, a, num_sms,
-                                                                                            stream);
+      return launch_expert_gemm<SWIGLU, kMxBn[2], kMxStages[2], kTokBox[2], false, true, W4, A4>(tw, tx, a,
+                                                                                                num_sms, stream);
   }
 }
 
@@ -876,16 +914,28 @@ cudaError_t launch_mx(const CUtensorMap& tw, const CUtensorMap& tx, const CUtens
 
 cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const CUtensorMap& tm_sw,
                                    const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
-                                   cudaStream_t stream, bool fp4_weights) {
-  return fp4_weights ? launch_mx<true, true>(tm_w13, tm_x, tm_sw, tm_sx, a, plan, num_sms, stream)
-                     : launch_mx<true, false>(tm_w13, tm_x, tm_sw, tm_sx, a, plan, num_sms, stream);
+                                   cudaStream_t stream, MxKind kind) {
+  switch (kind) {
+    case MxKind::kW4A8:
+      return launch_mx<true, true>(tm_w13, tm_x, tm_sw, tm_sx, a, plan, num_sms, stream);
+    case MxKind::kW4A4:
+      return launch_mx<true, true, true>(tm_w13, tm_x, tm_sw, tm_sx, a, plan, num_sms, stream);
+    default:
+      return launch_mx<true, false>(tm_w13, tm_x, tm_sw, tm_sx, a, plan, num_sms, stream);
+  }
 }
 
 cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const CUtensorMap& tm_sw,
                                 const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
-                                cudaStream_t stream, bool fp4_weights) {
-  return fp4_weights ? launch_mx<false, true>(tm_w2, tm_act, tm_sw, tm_sx, a, plan, num_sms, stream)
-                     : launch_mx<false, false>(tm_w2, tm_act, tm_sw, tm_sx, a, plan, num_sms, stream);
+                                cudaStream_t stream, MxKind kind) {
+  switch (kind) {
+    case MxKind::kW4A8:
+      return launch_mx<false, true>(tm_w2, tm_act, tm_sw, tm_sx, a, plan, num_sms, stream);
+    case MxKind::kW4A4:
+      return launch_mx<false, true, true>(tm_w2, tm_act, tm_sw, tm_sx, a, plan, num_sms, stream);
+    default:
+      return launch_mx<false, false>(tm_w2, tm_act, tm_sw, tm_sx, a, plan, num_sms, stream);
+  }
 }
 
 int gemm_bn_mx(GemmPlan plan, bool pair) { return pair ? kMxPairBn : kMxBn[static_cast<int>(plan)]; }

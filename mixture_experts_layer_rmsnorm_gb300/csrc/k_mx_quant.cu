@@ -103,8 +103,10 @@ __device__ __forceinline__ int64_t token_scale_row(int p, const int32_t* offsets
 // rows (row p <- h[sorted_ids[p] / k], zeros for padding rows), rows below
 // offsets[E] only, chunk-grouped scales; MODE 2: rows of W13, scales in gate/up
 // tile-row order; MODE 3: activation rows below offsets[E], chunk-grouped scales.
-// FP4 (weights, MODE 0 and 2): E2M1 codes, packed two per byte, and the block
-// exponent floor(log2 amax) - 2 (2 = the largest E2M1 exponent).
+// FP4: E2M1 codes, packed two per byte, and the block exponent
+// floor(log2 amax) - 2 (2 = the largest E2M1 exponent): the weights of both
+// FP4 layers (MODE 0 and 2), the token rows and activations of the MXFP4 layer
+// (MODE 1 and 3).
 template <int MODE, bool FP4 = false>
 __global__ void __launch_bounds__(kQuantWarps * 32)
     mx_quantize_kernel(const uint16_t* __restrict__ src, int64_t rows, int K, const int32_t* __restrict__ sorted_ids,
@@ -199,6 +201,22 @@ cudaError_t launch_mx4_quantize_w13(const uint16_t* w13, int E, int H, int I, ui
   const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
   return launch_pdl(mx_quantize_kernel<2, true>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0,
                     stream, w13, rows, H, nullptr, nullptr, nullptr, 1, 32, 0, 0, 1, I, codes, scales);
+}
+
+cudaError_t launch_mx4_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets,
+                              const int32_t* unit_off, int tiles, int bn, int E, int N, int k, int H, int64_t rows,
+                              uint8_t* codes, uint8_t* scales, cudaStream_t stream) {
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  return launch_pdl(mx_quantize_kernel<1, true>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0,
+                    stream, h, rows, H, sorted_ids, offsets, unit_off, tiles, bn, E, N, k, 0, codes, scales);
+}
+
+cudaError_t launch_mx4_quantize_act(const uint16_t* act, int64_t rows, int K, const int32_t* offsets,
+                                    const int32_t* unit_off, int tiles, int bn, int E, uint8_t* codes,
+                                    uint8_t* scales, cudaStream_t stream) {
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  return launch_pdl(mx_quantize_kernel<3, true>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0,
+                    stream, act, rows, K, nullptr, offsets, unit_off, tiles, bn, E, 0, 1, 0, codes, scales);
 }
 
 cudaError_t launch_mx_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets,

@@ -290,7 +290,7 @@ moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes) {
 moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t* count) {
   const moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
-  if (!count || call < MOE_CALL_FORWARD || call > MOE_CALL_FORWARD_MXFP4) return MOE_ERR_INVALID_ARG;
+  if (!count || call < MOE_CALL_FORWARD || call > MOE_CALL_FORWARD_MXFP4A4) return MOE_ERR_INVALID_ARG;
   const moe_shape& s = *shape;
   if (s.T == 0) {
     *count = 0;
@@ -302,7 +302,7 @@ moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t
     *count = front + 3;
   else if (call == MOE_CALL_FORWARD_FUSED_FRONT)
     *count = 1 + 3;
-  else if (call == MOE_CALL_FORWARD_MX || call == MOE_CALL_FORWARD_MXFP4)
+  else if (call == MOE_CALL_FORWARD_MX || call == MOE_CALL_FORWARD_MXFP4 || call == MOE_CALL_FORWARD_MXFP4A4)
     *count = front + 4;  // + the activation quantize between the GEMMs
   else
     *count = front + 2;  // the combine runs inside the down GEMM
@@ -505,21 +505,26 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   return MOE_OK;
 }
 
-// The MXFP8 layer: the bf16 layer's routing, then MXFP8 token rows and
-// weights in block-scaled tcgen05 GEMMs; fp4: MXFP4 weights (E2M1 codes).
+// The block-scaled layers: the bf16 layer's routing, then quantized token
+// rows and weights in block-scaled tcgen05 GEMMs.  kind: MXFP8 weights and
+// tokens (kW8A8), MXFP4 weights with MXFP8 tokens (kW4A8), or MXFP4 weights
+// and tokens (kW4A4: packed codes, 256 elements of K per GEMM stage, so H and
+// I multiples of 256).
 moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
                            const float* router_bias, const uint8_t* w13c, const uint8_t* w13s, const uint8_t* w2c,
                            const uint8_t* w2s, moe_bf16* y, void* workspace, size_t workspace_bytes,
-                           moe_stream_t stream, void* const* events, bool fp4 = false) {
+                           moe_stream_t stream, void* const* events, MxKind kind = MxKind::kW8A8) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   const moe_shape& s = *shape;
   if (s.T == 0) return MOE_OK;
   const GemmPlan plan = moe::choose_plan(s.T, s.top_k, s.E);
   if (s.E > 256) return MOE_ERR_UNSUPPORTED;
+  const bool fp4 = kind != MxKind::kW8A8, a4 = kind == MxKind::kW4A4;
+  if (a4 && (s.H % 256 != 0 || s.I % 256 != 0)) return MOE_ERR_UNSUPPORTED;
   st = check_inputs(shape, x, g_norm, w_router, router_bias, workspace, workspace_bytes, true);
   if (st != MOE_OK) return st;
-  const size_t code_align = fp4 ? 32 : 16;  // the 16U4_ALIGN16B tensor maps want 32-byte bases
+  const size_t code_align = fp4 ? 32 : 16;  // the 4-bit tensor maps want 32-byte bases (one rule for both layers)
   if (!w13c || !w13s || !w2c || !w2s || !y || !aligned(w13c, code_align) || !aligned(w13s, 16) ||
       !aligned(w2c, code_align) || !aligned(w2s, 16) || !aligned(y, 16))
     return MOE_ERR_INVALID_ARG;
@@ -538,13 +543,17 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   const uint64_t n_tok_tiles1 = static_cast<uint64_t>(L.P_max / 32) * 2 * (s.H / 128);
   const uint64_t n_tok_tiles2 = static_cast<uint64_t>(L.P_max / 32) * 2 * (s.I / 128);
   CUtensorMap tm_w13, tm_xq, tm_w2, tm_aq, tm_s13, tm_sxq, tm_s2, tm_saq;
-  const bool maps_w = fp4 ? make_map_gate_up_u4(&tm_w13, w13c, s.H, s.I, s.E) &&
-                                 make_map_u4(&tm_w2, w2c, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows)
-                           : make_map_gate_up_u8(&tm_w13, w13c, s.H, s.I, s.E) &&
-                                 make_map_u8(&tm_w2, w2c, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows);
+  // kW4A8: 4-bit weight maps (the TMA spreads the codes to the E4M3 image);
+  // kW4A4: byte maps over the packed codes (H / 2 and I / 2 bytes per row)
+  const uint64_t kx1 = a4 ? s.H / 2 : s.H, kx2 = a4 ? s.I / 2 : s.I;
+  const bool maps_w = kind == MxKind::kW4A8
+                          ? make_map_gate_up_u4(&tm_w13, w13c, s.H, s.I, s.E) &&
+                                make_map_u4(&tm_w2, w2c, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows)
+                          : make_map_gate_up_u8(&tm_w13, w13c, kx1, s.I, s.E) &&
+                                make_map_u8(&tm_w2, w2c, kx2, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows);
   if (!maps_w ||
-      !make_map_u8(&tm_xq, at<void>(workspace, L.xg), s.H, L.P_max, moe::gemm_tok_box_rows_mx(plan, pair1)) ||
-      !make_map_u8(&tm_aq, at<void>(workspace, L.aq), s.I, L.P_max, moe::gemm_tok_box_rows_mx(plan, pair2)) ||
+      !make_map_u8(&tm_xq, at<void>(workspace, L.xg), kx1, L.P_max, moe::gemm_tok_box_rows_mx(plan, pair1)) ||
+      !make_map_u8(&tm_aq, at<void>(workspace, L.aq), kx2, L.P_max, moe::gemm_tok_box_rows_mx(plan, pair2)) ||
       !make_map_scales(&tm_s13, w13s, static_cast<uint64_t>(s.E) * (2 * s.I / 128) * (s.H / 128)) ||
       !make_map_scales(&tm_sxq, at<void>(workspace, L.xs), n_tok_tiles1) ||
       !make_map_scales(&tm_s2, w2s, static_cast<uint64_t>(s.E) * (s.H / 128) * (s.I / 128)) ||
@@ -557,10 +566,10 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   if (st != MOE_OK) return st;
   if (!mark(1) || !mark(2) || !mark(3)) return MOE_ERR_CUDA;
   const int N = s.T * s.top_k;
-  if (moe::launch_mx_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
-                            at<int32_t>(workspace, L.offsets), at<int32_t>(workspace, L.unit1), utiles1, bn1, s.E, N,
-                            s.top_k, s.H, L.P_max, at<uint8_t>(workspace, L.xg), at<uint8_t>(workspace, L.xs),
-                            cs) != cudaSuccess ||
+  auto gather = a4 ? moe::launch_mx4_gather : moe::launch_mx_gather;
+  if (gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.offsets),
+             at<int32_t>(workspace, L.unit1), utiles1, bn1, s.E, N, s.top_k, s.H, L.P_max,
+             at<uint8_t>(workspace, L.xg), at<uint8_t>(workspace, L.xs), cs) != cudaSuccess ||
       !mark(4))
     return MOE_ERR_CUDA;
 
@@ -580,14 +589,15 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   a1.pair = pair1;
   a1.w_scales = w13s;
   a1.x_scales = at<uint8_t>(workspace, L.xs);
-  if (moe::launch_gemm_gate_up_mx(tm_w13, tm_xq, tm_s13, tm_sxq, a1, plan, num_sms, cs, fp4) != cudaSuccess ||
+  if (moe::launch_gemm_gate_up_mx(tm_w13, tm_xq, tm_s13, tm_sxq, a1, plan, num_sms, cs, kind) != cudaSuccess ||
       !mark(5))
     return MOE_ERR_CUDA;
   // the activations (bf16) -> MXFP8, rows below offsets[E], their scales in
   // the down GEMM's token chunks
-  if (moe::launch_mx_quantize_act(at<uint16_t>(workspace, L.act), L.P_max, s.I, at<int32_t>(workspace, L.offsets),
-                                  at<int32_t>(workspace, L.unit2), utiles2, bn2, s.E, at<uint8_t>(workspace, L.aq),
-                                  at<uint8_t>(workspace, L.as), cs) != cudaSuccess)
+  auto quantize_act = a4 ? moe::launch_mx4_quantize_act : moe::launch_mx_quantize_act;
+  if (quantize_act(at<uint16_t>(workspace, L.act), L.P_max, s.I, at<int32_t>(workspace, L.offsets),
+                   at<int32_t>(workspace, L.unit2), utiles2, bn2, s.E, at<uint8_t>(workspace, L.aq),
+                   at<uint8_t>(workspace, L.as), cs) != cudaSuccess)
     return MOE_ERR_CUDA;
   moe::ExpertGemmArgs a2{};
   a2.offsets = at<int32_t>(workspace, L.offsets);
@@ -605,7 +615,7 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   a2.pair = pair2;
   a2.w_scales = w2s;
   a2.x_scales = at<uint8_t>(workspace, L.as);
-  if (moe::launch_gemm_down_mx(tm_w2, tm_aq, tm_s2, tm_saq, a2, plan, num_sms, cs, fp4) != cudaSuccess || !mark(6))
+  if (moe::launch_gemm_down_mx(tm_w2, tm_aq, tm_s2, tm_saq, a2, plan, num_sms, cs, kind) != cudaSuccess || !mark(6))
     return MOE_ERR_CUDA;
   if (moe::launch_combine(at<uint16_t>(workspace, L.out), at<int32_t>(workspace, L.slot), at<float>(workspace, L.w),
                           s.T, s.H, s.top_k, y, cs) != cudaSuccess ||
@@ -735,7 +745,21 @@ moe_status moe_forward_mxfp4(const moe_shape* shape, const moe_bf16* x, const mo
       if (!events[i]) return MOE_ERR_INVALID_ARG;
   }
   return moe::forward_mx_impl(shape, x, g_norm, w_router, router_bias, w13_codes, w13_scales, w2_codes, w2_scales, y,
-                              workspace, workspace_bytes, stream, events, true);
+                              workspace, workspace_bytes, stream, events, moe::MxKind::kW4A8);
+}
+
+moe_status moe_forward_mxfp4a4(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                               const float* w_router, const float* router_bias, const uint8_t* w13_codes,
+                               const uint8_t* w13_scales, const uint8_t* w2_codes, const uint8_t* w2_scales,
+                               moe_bf16* y, void* workspace, size_t workspace_bytes, moe_stream_t stream,
+                               void* const* events, int32_t n_events) {
+  if (events) {
+    if (n_events < MOE_NUM_KERNELS + 1) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i <= MOE_NUM_KERNELS; ++i)
+      if (!events[i]) return MOE_ERR_INVALID_ARG;
+  }
+  return moe::forward_mx_impl(shape, x, g_norm, w_router, router_bias, w13_codes, w13_scales, w2_codes, w2_scales, y,
+                              workspace, workspace_bytes, stream, events, moe::MxKind::kW4A4);
 }
 
 moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,

@@ -156,15 +156,18 @@ int gemm_unit_tiles(GemmPlan plan, int tiles);
 // token scales as [tiles * 2][256] bytes (one 512-byte tile = a box of 2 rows);
 // only the pair instances read them (the others load tiles from a.w_scales /
 // a.x_scales directly).  tm_x maps E4M3 codes (one byte per element); tm_w
-// E4M3 codes too, or with fp4_weights E2M1 codes (two per byte, a
-// 16U4_ALIGN16B map with the same boxes); a.w_scales / a.x_scales hold the
-// E8M0 scales.
+// E4M3 codes too, or for kW4A8 E2M1 codes (two per byte, a 16U4_ALIGN16B map
+// with the same boxes); a.w_scales / a.x_scales hold the E8M0 scales.
+// The operand formats of the block-scaled GEMMs: E4M3 x E4M3, E2M1 weights x
+// E4M3 tokens (both kind::mxf8f6f4), E2M1 x E2M1 (kind::mxf4; tm_w and tm_x
+// then map the packed code bytes, 256 elements of K per stage).
+enum class MxKind { kW8A8, kW4A8, kW4A4 };
 cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const CUtensorMap& tm_sw,
                                    const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
-                                   cudaStream_t stream, bool fp4_weights = false);
+                                   cudaStream_t stream, MxKind kind = MxKind::kW8A8);
 cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const CUtensorMap& tm_sw,
                                 const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
-                                cudaStream_t stream, bool fp4_weights = false);
+                                cudaStream_t stream, MxKind kind = MxKind::kW8A8);
 // rows of padding granularity of each expert's list for the MXFP8 GEMMs (a
 // token scale group is 32 rows)
 constexpr int kPadRowsMx = 32;
@@ -220,6 +223,14 @@ cudaError_t launch_mx_gather(const uint16_t* h, const int32_t* sorted_ids, const
 cudaError_t launch_mx_quantize_act(const uint16_t* act, int64_t rows, int K, const int32_t* offsets,
                                    const int32_t* unit_off, int tiles, int bn, int E, uint8_t* codes, uint8_t* scales,
                                    cudaStream_t stream);
+// the MXFP4 layer's token rows and activations: E2M1 codes two per byte
+// ([rows, K/2] bytes), scales as above
+cudaError_t launch_mx4_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets,
+                              const int32_t* unit_off, int tiles, int bn, int E, int N, int k, int H, int64_t rows,
+                              uint8_t* codes, uint8_t* scales, cudaStream_t stream);
+cudaError_t launch_mx4_quantize_act(const uint16_t* act, int64_t rows, int K, const int32_t* offsets,
+                                    const int32_t* unit_off, int tiles, int bn, int E, uint8_t* codes,
+                                    uint8_t* scales, cudaStream_t stream);
 inline size_t mx_scale_bytes(int64_t rows, int64_t K) { return static_cast<size_t>(rows / 128) * (K / 128) * 512; }
 
 // QK-norm of q[T, Hq, D] and k[T, Hk, D] in place (k_qk_norm.cu); D = 64, 128 or 256.

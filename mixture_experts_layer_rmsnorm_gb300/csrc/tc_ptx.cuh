@@ -298,6 +298,33 @@ __device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// Block-scaled MMA on packed E2M1 operands (kind::mxf4, K = 64: one 32-byte
+// step of a 128-byte K-major row holds 64 codes, two per byte, the even
+// element in the low nibble); two UE8M0 scales per row per MMA, the bytes
+// sf_id and sf_id + 1 (sf_id 0 or 2) of the row's 32-bit TMEM word (measured on
+// GB300 against host sums).
+__device__ __forceinline__ void mma_mxf4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::
+          "r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf4_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::
+          "r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Copy a 32-row x 16-byte tile (rows 16 bytes apart) from shared memory to
 // TMEM columns [taddr, taddr + 4), the same 32 rows in each lane quarter.
 // One thread; ordered before the tcgen05.mma this thread issues next.
@@ -389,6 +416,13 @@ __host__ __device__ __forceinline__ constexpr uint32_t idesc_mxf8(uint32_t M, ui
   return (sf_b << 4) | (a_fmt << 7) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sf_a << 29);
 }
 constexpr uint32_t kFmtE2M1 = 5;
+
+// Instruction descriptor, kind::mxf4: A and B E2M1 (format 1 in bits 7-9 and
+// 10-12), K-major, UE8M0 scales (bit 23); scale ids (0 or 2) in bits 29-30 / 4-5.
+__host__ __device__ __forceinline__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32_t sf_a,
+                                                                  uint32_t sf_b) {
+  return (sf_b << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sf_a << 29);
+}
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, dense.
 //   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format (1 = bf16);

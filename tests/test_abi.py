@@ -64,7 +64,8 @@ def test_kernels_per_call_host_checks():
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_FUSED_FRONT) == (binding.MOE_OK, 4)
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_MX) == (binding.MOE_OK, 7)
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_MXFP4) == (binding.MOE_OK, 7)
-    assert binding.moe_kernels_per_call_of(s4, 5)[0] == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_MXFP4A4) == (binding.MOE_OK, 7)
+    assert binding.moe_kernels_per_call_of(s4, 6)[0] == binding.MOE_ERR_INVALID_ARG
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_FUSED_COMBINE) == (binding.MOE_OK, 5)
     s4096 = binding.shape(4096, 128, 256, 8, 2)
     assert binding.moe_kernels_per_call_of(s4096, binding.MOE_CALL_FORWARD_FUSED_COMBINE) == (binding.MOE_OK, 7)
@@ -135,6 +136,12 @@ def test_mxfp4_sizes_and_argument_checks_without_a_gpu():
         return binding.moe_forward_mxfp4(s, A, A, A, None, w13c, w13s, w2c, A, A, A, need, None)
 
     assert fwd(w13c=A + 16) == binding.MOE_ERR_INVALID_ARG  # packed codes: 32-byte aligned
+    s512 = binding.shape(4, 256, 512, 8, 2)
+    _, need512 = binding.moe_workspace_size_mx(s512)
+    assert binding.moe_forward_mxfp4a4(s512, A, A, A, None, A + 16, A, A, A, A, A, need512, None) == \
+        binding.MOE_ERR_INVALID_ARG
+    # the MXFP4 layer: H and I multiples of 256 (this shape has I = 384)
+    assert binding.moe_forward_mxfp4a4(s, A, A, A, None, A, A, A, A, A, A, need, None) == binding.MOE_ERR_UNSUPPORTED
     assert fwd(w2c=A + 16) == binding.MOE_ERR_INVALID_ARG
     assert fwd(w13s=None) == binding.MOE_ERR_INVALID_ARG
     assert binding.moe_forward_mxfp4(s, A, A, A, None, A, A, A, A, A, A, need - 1, None) == binding.MOE_ERR_WORKSPACE

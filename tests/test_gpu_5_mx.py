@@ -30,7 +30,12 @@ CASES = [
     ("mx_prefill_chunks", 1024, 256, 256, 4, 2, True, None, 4),
     ("mx_prefill_ragged_norenorm", 300, 384, 128, 6, 3, False, None, 5),
     ("mx_prefill_skewed", 512, 256, 256, 16, 4, True, 1.2, 11),
+    # shapes for the MXFP4 layer too (H and I multiples of 256)
+    ("a4_ragged_decode", 37, 256, 512, 16, 4, True, None, 21),
+    ("a4_bias_norenorm", 3, 512, 256, 20, 5, False, 1.2, 22),
+    ("a4_prefill_ragged_norenorm", 300, 512, 256, 6, 3, False, None, 23),
 ]
+FORMATS = ["mxfp8", "mxfp4", "mxfp4a4"]
 
 
 @pytest.fixture(scope="module")
@@ -47,15 +52,18 @@ def unpack_e2m1(packed, shape_):
     return out.reshape(shape_)
 
 
-@pytest.mark.parametrize("fmt", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_mx_layer_parity(case, fmt, o):
     _, T, H, I, E, k, renorm, zipf, seed = case
+    a4 = fmt == "mxfp4a4"
+    if a4 and (H % 256 or I % 256):
+        pytest.skip("the MXFP4 layer takes H and I multiples of 256")
     cfg = inputs.LayerConfig(T=T, H=H, I=I, E=E, top_k=k, renormalize=renorm, seed=seed, zipf_bias=zipf)
     li = inputs.make_layer_inputs(cfg)
     dl = gu.DeviceLayer(li)
     L = dl.layer
-    fp4 = fmt == "mxfp4"
+    fp4 = fmt != "mxfp8"
     if fp4:
         L.quantize_mxfp4()
         codes13, scales13, codes2, scales2 = L.w13_codes4, L.w13_scales4, L.w2_codes4, L.w2_scales4
@@ -76,7 +84,7 @@ def test_mx_layer_parity(case, fmt, o):
     assert np.array_equal(s2.reshape(E, H, I // 32), w2s)
 
     xd = gu.dev_bf16(li.x)
-    y = L.forward_mxfp4(xd) if fp4 else L.forward_mx(xd)
+    y = L.forward_mxfp4(xd, fp4_tokens=a4) if fp4 else L.forward_mx(xd)
     torch.cuda.synchronize()
     st, det = L.device_status(T)
     assert st == binding.MOE_OK, (st, det)
@@ -103,10 +111,13 @@ def test_mx_layer_parity(case, fmt, o):
     assert bn == small_mid if small_mid else bn in (128, 256)
     G = -(-bn // 128)
     n_groups = 2 * (v.P_max // 32)
-    xcodes = view(mv.x_codes, torch.uint8, (v.P_max, H))
+    if a4:  # E2M1 token codes, two per byte
+        xcodes = unpack_e2m1(view(mv.x_codes, torch.uint8, (v.P_max, H // 2)), (v.P_max, H))
+    else:
+        xcodes = view(mv.x_codes, torch.uint8, (v.P_max, H))
     xs = gu.ungroup_mx_scales(view(mv.x_scales, torch.uint8, (n_groups * (H // 128) * 512,)), n_groups * 128, H)
     real = np.nonzero(g["sorted"] < T * k)[0]
-    hc, hs = o.mx_quantize(g["h"][g["sorted"][real] // k])
+    hc, hs = (o.mx4_quantize if a4 else o.mx_quantize)(g["h"][g["sorted"][real] // k])
     assert np.array_equal(xcodes[real], hc)
     offs = g["offsets"]
     chunk0 = np.concatenate([[0], np.cumsum(-(-np.diff(offs) // bn))])  # chunks before each expert
@@ -115,7 +126,7 @@ def test_mx_layer_parity(case, fmt, o):
     srow = (chunk0[e_of] + within // bn) * 128 * G + within % bn
     assert np.array_equal(xs[srow], hs)
     # the layer output against the oracle's layer of the same weight format
-    fwd = o.moe_forward_mx4 if fp4 else o.moe_forward_mx
+    fwd = o.moe_forward_mx4a4 if a4 else o.moe_forward_mx4 if fp4 else o.moe_forward_mx
     r = fwd(li.x, li.g, li.w_router, li.bias, w13c, w13s, w2c, w2s, k, renorm, cfg.eps)
     yg = gu.widen(y.cpu().numpy().view(np.uint16))
     err = yg - r["y64"]
@@ -177,3 +188,14 @@ def test_mxfp4_rejects_unaligned_codes():
     with pytest.raises(binding.MoeError) as ei:
         L.forward_mxfp4(gu.dev_bf16(li.x))
     assert ei.value.status == binding.MOE_ERR_INVALID_ARG
+
+
+def test_mxfp4a4_rejects_h_not_multiple_of_256():
+    cfg = inputs.LayerConfig(T=4, H=384, I=256, E=4, top_k=2, seed=0)
+    li = inputs.make_layer_inputs(cfg)
+    dl = gu.DeviceLayer(li)
+    L = dl.layer
+    L.quantize_mxfp4()
+    with pytest.raises(binding.MoeError) as ei:
+        L.forward_mxfp4(gu.dev_bf16(li.x), fp4_tokens=True)
+    assert ei.value.status == binding.MOE_ERR_UNSUPPORTED
