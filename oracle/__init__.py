@@ -90,6 +90,11 @@ class Oracle:
         lib.oracle_moe_forward_mx4a4.argtypes = [i64, i64, i64, i64, i, i, d, p, p, p, p, p, p, p, p, i64, p, i,
                                                  p, p, p, p]
         lib.oracle_moe_forward_mx4a4.restype = i
+        lib.oracle_nv4_quantize.argtypes = [i64, i64, p, i, p, p, p]
+        lib.oracle_nv4_dequantize.argtypes = [i64, i64, p, p, p, i, p]
+        lib.oracle_moe_forward_nv4.argtypes = [i64, i64, i64, i64, i, i, d, p, p, p, p, p, p, p, p, p, p, i64, p,
+                                               i, p, p, p, p]
+        lib.oracle_moe_forward_nv4.restype = i
         lib.oracle_f64_to_bf16.argtypes = [d]
         lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
         lib.oracle_f32_to_bf16.argtypes = [f]
@@ -163,6 +168,54 @@ class Oracle:
         K = codes.shape[-1]
         out = np.empty(codes.shape, np.float64)
         self.lib.oracle_mx4_dequantize(codes.size // K, K, _p(codes), _p(scales), _p(out))
+        return out
+
+    def nv4_quantize(self, x, per_row):
+        """NVFP4 of bf16 rows x[..., K]: (E2M1 codes [..., K] one per byte, E4M3
+        block scales [..., K/16], fp32 tensor scales: [rows] per row, else [1])."""
+        x = _c(x, np.uint16)
+        K = x.shape[-1]
+        rows = x.size // K
+        codes = np.empty(x.shape, np.uint8)
+        scales = np.empty(x.shape[:-1] + (K // 16,), np.uint8)
+        g = np.empty(rows if per_row else 1, np.float32)
+        self.lib.oracle_nv4_quantize(rows, K, _p(x), int(bool(per_row)), _p(codes), _p(scales), _p(g))
+        return codes, scales, g
+
+    def nv4_quantize_experts(self, w):
+        """NVFP4 of expert weights w[E, rows, K] with one tensor scale per expert matrix:
+        (codes [E, rows, K], scales [E, rows, K/16], g [E])."""
+        w = _c(w, np.uint16)
+        cs = [self.nv4_quantize(w[e], per_row=False) for e in range(w.shape[0])]
+        return (np.stack([c[0] for c in cs]), np.stack([c[1] for c in cs]),
+                np.concatenate([c[2] for c in cs]).astype(np.float32))
+
+    def nv4_dequantize(self, codes, scales, g, per_row):
+        codes = _c(codes, np.uint8); scales = _c(scales, np.uint8); g = _c(g, np.float32)
+        K = codes.shape[-1]
+        out = np.empty(codes.shape, np.float64)
+        self.lib.oracle_nv4_dequantize(codes.size // K, K, _p(codes), _p(scales), _p(g), int(bool(per_row)), _p(out))
+        return out
+
+    def moe_forward_nv4(self, x, g, w_router, bias, w13c, w13s, w13g, w2c, w2s, w2g, top_k, renorm, eps,
+                        sample=None, nthreads=None):
+        """The NVFP4 layer (NVFP4 weights with a tensor scale per expert matrix,
+        NVFP4 tokens and activations with one per row): ids, w, y64, y16, sample."""
+        x = _c(x, np.uint16); g = _c(g, np.uint16); wr = _c(w_router, np.float32)
+        w13c = _c(w13c, np.uint8); w13s = _c(w13s, np.uint8); w2c = _c(w2c, np.uint8); w2s = _c(w2s, np.uint8)
+        w13g = _c(w13g, np.float32); w2g = _c(w2g, np.float32)
+        T, H = x.shape; E = wr.shape[0]; I = w13c.shape[1] // 2
+        b = None if bias is None else _c(bias, np.float32)
+        smp = np.arange(T, dtype=np.int64) if sample is None else _c(sample, np.int64)
+        S = smp.size; k = int(top_k)
+        out = dict(ids=np.empty((S, k), np.int32), w=np.empty((S, k), np.float64),
+                   y64=np.empty((S, H), np.float64), y16=np.empty((S, H), np.uint16), sample=smp)
+        rc = self.lib.oracle_moe_forward_nv4(T, H, I, E, k, int(bool(renorm)), float(eps), _p(x), _p(g), _p(wr),
+                                             _p(b), _p(w13c), _p(w13s), _p(w13g), _p(w2c), _p(w2s), _p(w2g), S,
+                                             _p(smp), int(nthreads or threads()), _p(out["ids"]), _p(out["w"]),
+                                             _p(out["y64"]), _p(out["y16"]))
+        if rc != 0:
+            raise ValueError("oracle_moe_forward_nv4: bad input")
         return out
 
     def expert_mx4_f64(self, h, w13c, w13s, w2c, w2s):

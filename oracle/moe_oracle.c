@@ -326,21 +326,101 @@ void oracle_mx4_dequantize(int64_t rows, int64_t K, const uint8_t* codes, const 
       out[r * K + j] = ldexp(oracle_e2m1_decode(codes[r * K + j]), (int)scales[r * (K / 32) + j / 32] - 127);
 }
 
-/* weight rows of the low-precision layers: E4M3 (wfmt 0) or E2M1 (wfmt 1) codes */
+/* ------------------------------------------------------------------ */
+/* NVFP4: E2M1 codes, an E4M3 scale per 16 elements, an fp32 scale per    */
+/* tensor                                                                 */
+/* ------------------------------------------------------------------ */
+
+/* Second-level (per tensor) scale of NVFP4: g = amax / (448 * 6), so that the
+ * largest block scale is the largest E4M3 value; 1 for an all-zero tensor.
+ * fp32, as the kernels compute it. */
+static float nv4_global_of(float amax) { return amax > 0.0f ? amax / 2688.0f : 1.0f; }
+
+/* rows x K bf16 values (K a multiple of 16) -> E2M1 codes [rows, K] (one per
+ * byte), E4M3 block scales [rows, K/16] and fp32 tensor scales: one for all
+ * rows (per_row 0, g_out[0]) or one per row (per_row 1, g_out[r]).  The block
+ * scale and the codes are integers decided by fp32 arithmetic (the scales are
+ * not powers of two), so they are taken in fp32 in the kernels' order:
+ *   s_b = E4M3(amax_b / (6 g))   nearest, ties to even, saturating to 448
+ *   X_b = value(s_b) * g
+ *   q   = E2M1(x / X_b)          nearest, ties to even, saturating to 6; 0 where X_b = 0. */
+void oracle_nv4_quantize(int64_t rows, int64_t K, const uint16_t* x, int per_row, uint8_t* codes, uint8_t* scales,
+                         float* g_out) {
+  float amax_t = 0.0f;
+  if (!per_row) {
+    for (int64_t i = 0; i < rows * K; ++i) {
+      float a = fabsf(bf16_to_f32(x[i]));
+      if (a > amax_t) amax_t = a;
+    }
+    g_out[0] = nv4_global_of(amax_t);
+  }
+  for (int64_t r = 0; r < rows; ++r) {
+    const uint16_t* xr = x + r * K;
+    float g;
+    if (per_row) {
+      float amax_r = 0.0f;
+      for (int64_t j = 0; j < K; ++j) {
+        float a = fabsf(bf16_to_f32(xr[j]));
+        if (a > amax_r) amax_r = a;
+      }
+      g = nv4_global_of(amax_r);
+      g_out[r] = g;
+    } else {
+      g = g_out[0];
+    }
+    const float six_g = 6.0f * g;
+    for (int64_t b = 0; b < K / 16; ++b) {
+      float amax_b = 0.0f;
+      for (int j = 0; j < 16; ++j) {
+        float a = fabsf(bf16_to_f32(xr[b * 16 + j]));
+        if (a > amax_b) amax_b = a;
+      }
+      const float u = amax_b / six_g;
+      const uint8_t sc = oracle_e4m3_encode((double)u);
+      scales[r * (K / 16) + b] = sc;
+      const float X = (float)oracle_e4m3_decode(sc) * g;
+      for (int j = 0; j < 16; ++j) {
+        const float v = bf16_to_f32(xr[b * 16 + j]);
+        codes[r * K + b * 16 + j] = X > 0.0f ? oracle_e2m1_encode((double)(v / X)) : 0;
+      }
+    }
+  }
+}
+
+/* values of NVFP4 codes [rows, K] with block scales [rows, K/16] and tensor
+ * scales g (g[0] for all rows, or g[r] per row): q * value(s) * g, in fp64 */
+void oracle_nv4_dequantize(int64_t rows, int64_t K, const uint8_t* codes, const uint8_t* scales, const float* g,
+                           int per_row, double* out) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const double gr = (double)(per_row ? g[r] : g[0]);
+    for (int64_t j = 0; j < K; ++j)
+      out[r * K + j] = oracle_e2m1_decode(codes[r * K + j]) * oracle_e4m3_decode(scales[r * (K / 16) + j / 16]) * gr;
+  }
+}
+
+/* weight rows of the low-precision layers: E4M3 (wfmt 0) or E2M1 (wfmt 1) codes
+ * with E8M0 scales per 32; NVFP4 (wfmt 2): E2M1 codes, E4M3 scales per 16 and the
+ * matrix's tensor scale g */
 static void mx_weight_dequantize(int wfmt, int64_t rows, int64_t K, const uint8_t* codes, const uint8_t* scales,
-                                 double* out) {
-  if (wfmt)
+                                 float g, double* out) {
+  if (wfmt == 2)
+    oracle_nv4_dequantize(rows, K, codes, scales, &g, 0, out);
+  else if (wfmt)
     oracle_mx4_dequantize(rows, K, codes, scales, out);
   else
     oracle_mx_dequantize(rows, K, codes, scales, out);
 }
 
-/* one row of K bf16 token values through MXFP8 (afmt 0) or MXFP4 (afmt 1)
- * quantization and back */
+/* one row of K bf16 token values through MXFP8 (afmt 0), MXFP4 (afmt 1) or
+ * NVFP4 with a per-row tensor scale (afmt 2) quantization and back */
 static void mx_token_roundtrip(int afmt, int64_t K, const uint16_t* x16, double* out) {
   uint8_t* c = (uint8_t*)malloc((size_t)K);
-  uint8_t* sc = (uint8_t*)malloc((size_t)(K / 32));
-  if (afmt) {
+  uint8_t* sc = (uint8_t*)malloc((size_t)(K / 16));
+  if (afmt == 2) {  /* NVFP4 with the row as the tensor */
+    float g;
+    oracle_nv4_quantize(1, K, x16, 1, c, sc, &g);
+    oracle_nv4_dequantize(1, K, c, sc, &g, 1, out);
+  } else if (afmt) {
     oracle_mx4_quantize(1, K, x16, c, sc);
     oracle_mx4_dequantize(1, K, c, sc, out);
   } else {
@@ -599,15 +679,17 @@ static void expert_row_f64(int64_t H, int64_t I, const uint16_t* h16, const doub
  * sums in fp64.
  *   W13c [2I, H] codes, W13s [2I, H/32] scales; W2c [H, I], W2s [H, I/32]. */
 static void expert_row_mx_f64(int wfmt, int afmt, int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c,
-                              const uint8_t* W13s, const uint8_t* W2c, const uint8_t* W2s, double* a, double* o) {
+                              const uint8_t* W13s, float g13, const uint8_t* W2c, const uint8_t* W2s, float g2,
+                              double* a, double* o) {
+  const int64_t bs = wfmt == 2 ? 16 : 32;  /* elements per scale */
   double* hq = (double*)malloc(sizeof(double) * (size_t)H);
   mx_token_roundtrip(afmt, H, h16, hq);
   double* wrow = (double*)malloc(sizeof(double) * (size_t)(H > I ? H : I));
   double* wrow2 = (double*)malloc(sizeof(double) * (size_t)H);
   uint16_t* a16 = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)I);
   for (int64_t i = 0; i < I; ++i) {
-    mx_weight_dequantize(wfmt, 1, H, W13c + i * H, W13s + i * (H / 32), wrow);
-    mx_weight_dequantize(wfmt, 1, H, W13c + (I + i) * H, W13s + (I + i) * (H / 32), wrow2);
+    mx_weight_dequantize(wfmt, 1, H, W13c + i * H, W13s + i * (H / bs), g13, wrow);
+    mx_weight_dequantize(wfmt, 1, H, W13c + (I + i) * H, W13s + (I + i) * (H / bs), g13, wrow2);
     double gate = 0.0, up = 0.0;
     for (int64_t j = 0; j < H; ++j) {
       gate += hq[j] * wrow[j];
@@ -618,7 +700,7 @@ static void expert_row_mx_f64(int wfmt, int afmt, int64_t H, int64_t I, const ui
   }
   mx_token_roundtrip(afmt, I, a16, a);
   for (int64_t n = 0; n < H; ++n) {
-    mx_weight_dequantize(wfmt, 1, I, W2c + n * I, W2s + n * (I / 32), wrow);
+    mx_weight_dequantize(wfmt, 1, I, W2c + n * I, W2s + n * (I / bs), g2, wrow);
     double acc = 0.0;
     for (int64_t i = 0; i < I; ++i) acc += a[i] * wrow[i];
     o[n] = acc;
@@ -629,7 +711,7 @@ static void expert_row_mx_f64(int wfmt, int afmt, int64_t H, int64_t I, const ui
 void oracle_expert_mx_f64(int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c, const uint8_t* W13s,
                           const uint8_t* W2c, const uint8_t* W2s, double* a_out, double* o) {
   double* a = a_out ? a_out : (double*)malloc(sizeof(double) * (size_t)I);
-  expert_row_mx_f64(0, 0, H, I, h16, W13c, W13s, W2c, W2s, a, o);
+  expert_row_mx_f64(0, 0, H, I, h16, W13c, W13s, 1.0f, W2c, W2s, 1.0f, a, o);
   if (!a_out) free(a);
 }
 
@@ -637,7 +719,7 @@ void oracle_expert_mx_f64(int64_t H, int64_t I, const uint16_t* h16, const uint8
 void oracle_expert_mx4_f64(int64_t H, int64_t I, const uint16_t* h16, const uint8_t* W13c, const uint8_t* W13s,
                            const uint8_t* W2c, const uint8_t* W2s, double* a_out, double* o) {
   double* a = a_out ? a_out : (double*)malloc(sizeof(double) * (size_t)I);
-  expert_row_mx_f64(1, 0, H, I, h16, W13c, W13s, W2c, W2s, a, o);
+  expert_row_mx_f64(1, 0, H, I, h16, W13c, W13s, 1.0f, W2c, W2s, 1.0f, a, o);
   if (!a_out) free(a);
 }
 
@@ -662,6 +744,7 @@ typedef struct {
   /* block-scaled layers (when W13c != NULL): MXFP8 weights (wfmt 0) or MXFP4
    * weights (wfmt 1); MXFP8 (afmt 0) or MXFP4 (afmt 1) tokens and activations */
   const uint8_t *W13c, *W13s, *W2c, *W2s;
+  const float *W13g, *W2g; /* NVFP4: tensor scale per expert matrix */
   int wfmt, afmt;
   int64_t ns;
   const int64_t* sample;
@@ -695,9 +778,10 @@ static void fwd_expert_item(int64_t it, void* p) {
   int64_t e = c->ids[s * c->k + j];
   double* a = (double*)malloc(sizeof(double) * (size_t)c->I);
   if (c->W13c) {
+    const int64_t bs = c->wfmt == 2 ? 16 : 32;
     expert_row_mx_f64(c->wfmt, c->afmt, c->H, c->I, c->h16 + s * c->H, c->W13c + e * 2 * c->I * c->H,
-                      c->W13s + e * 2 * c->I * (c->H / 32), c->W2c + e * c->H * c->I, c->W2s + e * c->H * (c->I / 32),
-                      a, c->o + it * c->H);
+                      c->W13s + e * 2 * c->I * (c->H / bs), c->W13g ? c->W13g[e] : 1.0f, c->W2c + e * c->H * c->I,
+                      c->W2s + e * c->H * (c->I / bs), c->W2g ? c->W2g[e] : 1.0f, a, c->o + it * c->H);
     free(a);
     return;
   }
@@ -720,8 +804,8 @@ static void fwd_expert_item(int64_t it, void* p) {
 static int moe_forward_any(int64_t T, int64_t H, int64_t I, int64_t E, int k, int renorm, double eps,
                            const uint16_t* x, const uint16_t* g, const float* Wr, const float* bias,
                            const uint16_t* W13, const uint16_t* W2, const uint8_t* W13c, const uint8_t* W13s,
-                           const uint8_t* W2c, const uint8_t* W2s, int wfmt, int afmt, int64_t ns,
-                           const int64_t* sample,
+                           const uint8_t* W2c, const uint8_t* W2s, const float* W13g, const float* W2g, int wfmt,
+                           int afmt, int64_t ns, const int64_t* sample,
                            int round_inter, int nthreads, int32_t* ids, double* w, double* y64, uint16_t* y16,
                            uint16_t* h16_out, float* l32_out, double* l64_out) {
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E || ns < 0) return -1;
@@ -734,6 +818,7 @@ static int moe_forward_any(int64_t T, int64_t H, int64_t I, int64_t E, int k, in
   c.T = T; c.H = H; c.I = I; c.E = E; c.k = k; c.renorm = renorm; c.round_inter = round_inter;
   c.eps = eps; c.x = x; c.g = g; c.Wr = Wr; c.bias = bias; c.W13 = W13; c.W2 = W2;
   c.W13c = W13c; c.W13s = W13s; c.W2c = W2c; c.W2s = W2s; c.wfmt = wfmt; c.afmt = afmt;
+  c.W13g = W13g; c.W2g = W2g;
   c.ns = ns; c.sample = sample;
   c.h16 = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(ns * H));
   c.h64 = (double*)malloc(sizeof(double) * (size_t)(ns * H));
@@ -764,8 +849,8 @@ int oracle_moe_forward(int64_t T, int64_t H, int64_t I, int64_t E, int k, int re
                        const uint16_t* W13, const uint16_t* W2, int64_t ns, const int64_t* sample,
                        int round_inter, int nthreads, int32_t* ids, double* w, double* y64, uint16_t* y16,
                        uint16_t* h16_out, float* l32_out, double* l64_out) {
-  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, W13, W2, NULL, NULL, NULL, NULL, 0, 0, ns, sample,
-                         round_inter, nthreads, ids, w, y64, y16, h16_out, l32_out, l64_out);
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, W13, W2, NULL, NULL, NULL, NULL, NULL, NULL, 0,
+                         0, ns, sample, round_inter, nthreads, ids, w, y64, y16, h16_out, l32_out, l64_out);
 }
 
 /* The FP8 layer: the same routing; the experts with MXFP8 weights (codes and
@@ -777,8 +862,8 @@ int oracle_moe_forward_mx(int64_t T, int64_t H, int64_t I, int64_t E, int k, int
                           int64_t ns, const int64_t* sample, int nthreads, int32_t* ids, double* w, double* y64,
                           uint16_t* y16) {
   if (H % 32 || I % 32 || !W13c || !W13s || !W2c || !W2s) return -1;
-  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, 0, 0, ns, sample,
-                         1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, NULL, NULL,
+                         0, 0, ns, sample, 1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
 }
 
 /* The FP4-weight layer: as oracle_moe_forward_mx with MXFP4 expert weights
@@ -789,8 +874,8 @@ int oracle_moe_forward_mx4(int64_t T, int64_t H, int64_t I, int64_t E, int k, in
                            int64_t ns, const int64_t* sample, int nthreads, int32_t* ids, double* w, double* y64,
                            uint16_t* y16) {
   if (H % 32 || I % 32 || !W13c || !W13s || !W2c || !W2s) return -1;
-  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, 1, 0, ns, sample,
-                         1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, NULL, NULL,
+                         1, 0, ns, sample, 1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
 }
 
 /* The MXFP4 layer: MXFP4 expert weights and MXFP4 tokens and activations
@@ -802,8 +887,22 @@ int oracle_moe_forward_mx4a4(int64_t T, int64_t H, int64_t I, int64_t E, int k, 
                              int64_t ns, const int64_t* sample, int nthreads, int32_t* ids, double* w, double* y64,
                              uint16_t* y16) {
   if (H % 32 || I % 32 || !W13c || !W13s || !W2c || !W2s) return -1;
-  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, 1, 1, ns,
-                         sample, 1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, NULL, NULL,
+                         1, 1, ns, sample, 1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
 }
 
-int oracle_version(void) { return 4; }
+/* The NVFP4 layer: NVFP4 expert weights (E2M1 codes [E, rows, K] one per
+ * byte, E4M3 scales [E, rows, K/16], tensor scales W13g[E], W2g[E]: one per
+ * expert matrix) and NVFP4 tokens and activations (one tensor scale per row),
+ * otherwise as oracle_moe_forward_mx.  H and I multiples of 16. */
+int oracle_moe_forward_nv4(int64_t T, int64_t H, int64_t I, int64_t E, int k, int renorm, double eps,
+                           const uint16_t* x, const uint16_t* g, const float* Wr, const float* bias,
+                           const uint8_t* W13c, const uint8_t* W13s, const float* W13g, const uint8_t* W2c,
+                           const uint8_t* W2s, const float* W2g, int64_t ns, const int64_t* sample, int nthreads,
+                           int32_t* ids, double* w, double* y64, uint16_t* y16) {
+  if (H % 16 || I % 16 || !W13c || !W13s || !W13g || !W2c || !W2s || !W2g) return -1;
+  return moe_forward_any(T, H, I, E, k, renorm, eps, x, g, Wr, bias, NULL, NULL, W13c, W13s, W2c, W2s, W13g, W2g, 2,
+                         2, ns, sample, 1, nthreads, ids, w, y64, y16, NULL, NULL, NULL);
+}
+
+int oracle_version(void) { return 5; }

@@ -397,6 +397,116 @@ def pin_mx4a4_layer_restated(o):
     assert np.linalg.norm(res["y64"] - w4a8["y64"]) > 1e-3 * np.linalg.norm(w4a8["y64"])
 
 
+# --------------------------------------------------------------------- NVFP4
+
+
+def pin_nv4_hand_cases(o):
+    # tensor maximum 2688 = 448 * 6 -> tensor scale 1; per 16-element block:
+    # amax 6 -> scale 1.0 (E4M3 0x38), codes of 6, 3, -1.5, 0.5, 0 = 7, 5, 11, 1, 0;
+    # amax 2688 -> scale 448 (0x7E), 2688 -> code 7; amax 0.75 -> scale 0.125 (0x20),
+    # 0.75 -> 7, 0.25 -> 4; amax 5 -> 5/6 rounds to 0.8125 (0x35) and 5 / 0.8125
+    # saturates to 6 (code 7); an all-zero block -> scale 0, codes 0
+    x = np.zeros((1, 80), np.float64)
+    x[0, :5] = [6, 3, -1.5, 0.5, 0]
+    x[0, 16] = 2688
+    x[0, 32:34] = [0.75, 0.25]
+    x[0, 48] = 5
+    for per_row in (True, False):
+        c, sc, g = o.nv4_quantize(torch_bf16_bits_from_f64(x), per_row=per_row)
+        assert g.tolist() == [1.0]
+        assert sc.tolist() == [[0x38, 0x7E, 0x20, 0x35, 0]]
+        assert c[0, :5].tolist() == [7, 5, 11, 1, 0] and c[0, 16] == 7 and c[0, 32:34].tolist() == [7, 4]
+        assert c[0, 48] == 7 and not c[0, 64:].any()
+    # a tensor of zeros: tensor scale 1, every scale and code 0
+    c, sc, g = o.nv4_quantize(np.zeros((2, 32), np.uint16), per_row=False)
+    assert g.tolist() == [1.0] and not sc.any() and not c.any()
+
+
+def _np_nv4(x16: np.ndarray, per_row: bool):
+    """NVFP4 restated with numpy float32 arithmetic, torch's E4M3 cast for the
+    block scales and the per-binade rint for E2M1: (codes, scales, g)."""
+    import torch
+    x = widen(x16).astype(np.float32)
+    R, K = x.shape
+    amax_r = np.abs(x).max(axis=1) if per_row else np.full(R, np.abs(x).max(), np.float32)
+    g = np.where(amax_r > 0, amax_r / np.float32(2688), np.float32(1)).astype(np.float32)
+    blk = np.abs(x).reshape(R, K // 16, 16).max(axis=2)
+    u = (blk / (np.float32(6) * g)[:, None]).astype(np.float32)
+    s8 = torch.from_numpy(np.minimum(u, np.float32(448))).to(torch.float8_e4m3fn)
+    sc = s8.view(torch.uint8).numpy()
+    X = (s8.to(torch.float32).numpy() * g[:, None]).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):  # X = 0 blocks take code 0 below
+        q = (x.reshape(R, K // 16, 16) / X[:, :, None]).astype(np.float32)
+    mag = _rne_e2m1(q.astype(np.float64))
+    code = np.searchsorted(np.array(E2M1_MAGNITUDES), mag)
+    code = code | np.where(np.signbit(q), 8, 0)
+    code = np.where(X[:, :, None] > 0, code, 0).reshape(R, K).astype(np.uint8)
+    return code, sc, (g if per_row else g[:1])
+
+
+def pin_nv4_restated(o):
+    rng = np.random.default_rng(31)
+    for per_row in (True, False):
+        x = rng.standard_normal((24, 256)) * np.exp2(rng.uniform(-12, 8, (24, 1)))
+        x[3, 16:32] = 0.0                      # an all-zero block
+        x[5, :] = x[5, :] * 1e-3               # a row far below the tensor maximum
+        x16 = torch_bf16_bits_from_f64(x)
+        c, sc, g = o.nv4_quantize(x16, per_row=per_row)
+        c2, sc2, g2 = _np_nv4(x16, per_row)
+        assert np.array_equal(g, g2) and np.array_equal(sc, sc2) and np.array_equal(c, c2)
+
+
+def pin_nv4_roundtrip_error(o):
+    # |x - q X| is at most half an E2M1 step of x/X's binade (0.25 X, 0.5 X, X),
+    # except above 6 X, where it saturates to 6 X
+    x16 = inputs.normal_bf16(33, 1, (16, 256), 0.0, 0.02)
+    c, sc, g = o.nv4_quantize(x16, per_row=True)
+    d = o.nv4_dequantize(c, sc, g, per_row=True)
+    x = widen(x16)
+    X = np.repeat(np.array([[o.e4m3_decode(int(b)) for b in row] for row in sc]), 16, axis=1) * \
+        g.astype(np.float64)[:, None]
+    r = np.abs(x) / X
+    sat = r > 6
+    assert np.allclose(d[sat], np.sign(x[sat]) * 6 * X[sat], rtol=1e-12)
+    half = np.where(r < 2, 0.25, np.where(r < 4, 0.5, 1.0)) * X
+    assert np.all(np.abs(d - x)[~sat] <= half[~sat] * (1 + 1e-6))
+    assert np.linalg.norm(d - x) < 0.1 * np.linalg.norm(x)
+
+
+def pin_nv4_layer_restated(o):
+    # the NVFP4 layer against a restatement whose round trips use _np_nv4
+    T, H, I, E, k = 3, 64, 96, 4, 2
+    li = rand_layer(T, H, I, E, seed=28)
+    w13c, w13s, w13g = o.nv4_quantize_experts(li.w13)
+    w2c, w2s, w2g = o.nv4_quantize_experts(li.w2)
+    res = o.moe_forward_nv4(li.x, li.g, li.w_router, None, w13c, w13s, w13g, w2c, w2s, w2g, k, True, 1e-6)
+    ref = o.moe_forward(li.x, li.g, li.w_router, None, li.w13, li.w2, k, True, 1e-6)
+    assert np.array_equal(res["ids"], ref["ids"])
+
+    def deq(x16, per_row):
+        c, sc, g = _np_nv4(np.atleast_2d(x16), per_row)
+        vals = np.array(E2M1_MAGNITUDES)[c & 7] * np.where(c & 8, -1.0, 1.0)
+        import torch
+        sv = torch.from_numpy(sc.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+        gg = g.astype(np.float64)[:, None] if per_row else np.float64(g[0])
+        return vals * np.repeat(sv, 16, axis=1) * gg
+
+    W13 = np.stack([deq(li.w13[e], False) for e in range(E)])
+    W2 = np.stack([deq(li.w2[e], False) for e in range(E)])
+    y = np.zeros((T, H))
+    for t in range(T):
+        hq = deq(ref["h16"][t], True)[0]
+        for j in range(k):
+            e = int(res["ids"][t, j])
+            gate = W13[e, :I] @ hq
+            up = W13[e, I:] @ hq
+            a = torch_bf16_bits_from_f64(gate / (1 + np.exp(-gate)) * up)
+            y[t] += res["w"][t, j] * (W2[e] @ deq(a, True)[0])
+    assert np.allclose(res["y64"], y, rtol=1e-12, atol=1e-15)
+    rel = np.linalg.norm(res["y64"] - ref["y64"]) / np.linalg.norm(ref["y64"])
+    assert 1e-3 < rel < 0.5
+
+
 # -------------------------------------------------------------------- router
 
 def pin_router_f64_numpy(o):

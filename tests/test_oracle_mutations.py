@@ -51,11 +51,18 @@ MUTATIONS = {
     "e2m1_tie_to_odd": ("if (d < bd || (d == bd && (c & 1) == 0)) {", "if (d < bd || (d == bd && (c & 1) == 1)) {"),
     "e2m1_binade_off": ("double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);",
                         "double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e);"),
-    "mx4_weights_as_e4m3": ("  if (wfmt)\n    oracle_mx4_dequantize(rows, K, codes, scales, out);",
-                            "  if (0)\n    oracle_mx4_dequantize(rows, K, codes, scales, out);"),
+    "mx4_weights_as_e4m3": ("  else if (wfmt)\n    oracle_mx4_dequantize(rows, K, codes, scales, out);",
+                            "  else if (0)\n    oracle_mx4_dequantize(rows, K, codes, scales, out);"),
     "e2m1_sign_dropped": ("  return (uint8_t)((sgn << 3) | best);", "  return (uint8_t)best;"),
-    "mx4a4_tokens_as_mxfp8": ("  if (afmt) {\n    oracle_mx4_quantize(1, K, x16, c, sc);",
-                              "  if (0) {\n    oracle_mx4_quantize(1, K, x16, c, sc);"),
+    "mx4a4_tokens_as_mxfp8": ("  } else if (afmt) {\n    oracle_mx4_quantize(1, K, x16, c, sc);",
+                              "  } else if (0) {\n    oracle_mx4_quantize(1, K, x16, c, sc);"),
+    "nv4_global_scale_ignored": ("static float nv4_global_of(float amax) { return amax > 0.0f ? amax / 2688.0f : 1.0f; }",
+                                 "static float nv4_global_of(float amax) { return amax > 0.0f ? 1.0f : 1.0f; }"),
+    "nv4_block_scale_not_six": ("    const float six_g = 6.0f * g;", "    const float six_g = 4.0f * g;"),
+    "nv4_scale_skips_global": ("      const float X = (float)oracle_e4m3_decode(sc) * g;",
+                               "      const float X = (float)oracle_e4m3_decode(sc);"),
+    "nv4_token_tensor_scale": ("    oracle_nv4_quantize(1, K, x16, 1, c, sc, &g);\n    oracle_nv4_dequantize(1, K, c, sc, &g, 1, out);",
+                               "    oracle_nv4_quantize(1, K, x16, 1, c, sc, &g);\n    g = 1.0f;\n    oracle_nv4_dequantize(1, K, c, sc, &g, 1, out);"),
     "qk_bias_dropped": ("(bf16_to_f64(w[j]) + weight_bias)", "(bf16_to_f64(w[j]))"),
     "qk_bias_multiplied": ("(bf16_to_f64(w[j]) + weight_bias)", "(bf16_to_f64(w[j]) * weight_bias)"),
     "qk_eps_dropped": ("sqrt(ss / (double)D + eps)", "sqrt(ss / (double)D)"),
