@@ -447,13 +447,18 @@ def run_ours(args, wl, world, rank, local):
     setup_s = time.time() - t_setup
 
     ff, fc = args.fused_front, args.fused_combine
-    mx = "mxfp4a4" if args.mxfp4a4 else "mxfp4" if args.mxfp4 else args.mx  # formats for the byte counts
-    if args.mxfp4 or args.mxfp4a4:
+    mx = ("nvfp4" if args.nvfp4 else "mxfp4a4" if args.mxfp4a4 else "mxfp4" if args.mxfp4
+          else args.mx)  # formats for the byte counts
+    if args.nvfp4:
+        layer.quantize_nvfp4()
+    elif args.mxfp4 or args.mxfp4a4:
         layer.quantize_mxfp4()
     elif mx:
         layer.quantize_mx()
 
     def fwd(x, y, events=None):
+        if args.nvfp4:
+            return layer.forward_nvfp4(x, y, events=events)
         if args.mxfp4 or args.mxfp4a4:
             return layer.forward_mxfp4(x, y, events=events, fp4_tokens=args.mxfp4a4)
         if mx:
@@ -461,7 +466,8 @@ def run_ours(args, wl, world, rank, local):
         return layer.forward(x, y, events=events, fused_front=ff, fused_combine=fc)
 
     def kpc(T):  # our kernels per layer call
-        call = (binding.MOE_CALL_FORWARD_MXFP4A4 if args.mxfp4a4 else
+        call = (binding.MOE_CALL_FORWARD_NVFP4 if args.nvfp4 else
+                binding.MOE_CALL_FORWARD_MXFP4A4 if args.mxfp4a4 else
                 binding.MOE_CALL_FORWARD_MXFP4 if args.mxfp4 else binding.MOE_CALL_FORWARD_MX if mx else
                 binding.MOE_CALL_FORWARD_FUSED_FRONT if ff else
                 binding.MOE_CALL_FORWARD_FUSED_COMBINE if fc else binding.MOE_CALL_FORWARD)
@@ -569,7 +575,8 @@ def run_ours(args, wl, world, rank, local):
         fl = accounting.layer_flops
         per = [fl(T, H, wl["I"], wl["E"], wl["k"])["gemm1" if dom == "gemm_gate_up_swiglu" else "gemm2"]
                for T in Ts]
-        if mx == "mxfp4a4":  # kind::mxf4: the measured bf16 peak x the nominal dense ratio 13.5 / 2.25
+        if mx in ("mxfp4a4", "nvfp4"):  # kind::mxf4 / mxf4nvf4: the measured bf16 peak x the nominal dense
+            # ratio 13.5 / 2.25
             roof = roofline("tensor", sum(per) / len(per), avg_s, 6.0 * peaks["bf16_tflops"], None)
             roof["peak_source"] = f"6 x bf16_tflops ({peak_kind}; nominal dense fp4 / bf16 ratio)"
         elif mx:  # block-scaled FP8 / FP4xFP8 MMAs (kind::mxf8f6f4, the FP8 rate): the measured bf16 peak x
@@ -618,13 +625,16 @@ def run_ours(args, wl, world, rank, local):
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": ("mxfp4 (e2m1 + e8m0 per 32) x mxfp4, fp32 accumulation" if args.mxfp4a4 else
+        "vs_baseline": None, "dtype": ("nvfp4 (e2m1 + e4m3 per 16 + fp32 per tensor) x nvfp4, fp32 accumulation" if args.nvfp4 else
+                  "mxfp4 (e2m1 + e8m0 per 32) x mxfp4, fp32 accumulation" if args.mxfp4a4 else
                   "mxfp4 (e2m1 + e8m0 per 32) x mxfp8, fp32 accumulation" if args.mxfp4 else
                   "mxfp8 (e4m3 + e8m0 per 32) x mxfp8, fp32 accumulation" if mx else "bf16"),
         "data": "synthetic (seeded generator; random-init weights)",
         "config": {"workload": wl["label"], "tokens_per_step": tokens_per_step,
                    "layer_calls_per_step": len(Ts),
-                   "expert_weights": ("MXFP4 weights and tokens (moe_forward_mxfp4a4; bytes counted as codes + "
+                   "expert_weights": ("NVFP4 weights and tokens (moe_forward_nvfp4; bytes counted as codes + "
+                                      "block scales)" if args.nvfp4 else
+                                      "MXFP4 weights and tokens (moe_forward_mxfp4a4; bytes counted as codes + "
                                       "scales)" if args.mxfp4a4 else
                                       "MXFP4 (moe_forward_mxfp4; weight bytes counted as codes + scales)"
                                       if args.mxfp4 else
@@ -663,6 +673,8 @@ def main():
                     help="CPU oracle sample: at most this many tokens of each batch per step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum timed CPU-oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--nvfp4", action="store_true",
+                    help="time moe_forward_nvfp4: the NVFP4 layer (NVFP4 weights, token rows and activations)")
     ap.add_argument("--mxfp4a4", action="store_true",
                     help="time moe_forward_mxfp4a4: the MXFP4 layer (MXFP4 weights, token rows and activations)")
     ap.add_argument("--mxfp4", action="store_true",
@@ -674,8 +686,9 @@ def main():
     ap.add_argument("--fused-combine", action="store_true",
                     help="time moe_forward_fused_combine (the combine in the down GEMM's epilogue)")
     args = ap.parse_args()
-    if sum([args.mx, args.mxfp4, args.mxfp4a4, args.fused_front, args.fused_combine]) > 1:
-        ap.error("--mx, --mxfp4, --mxfp4a4, --fused-front and --fused-combine are separate entry points; pick one")
+    if sum([args.mx, args.mxfp4, args.mxfp4a4, args.nvfp4, args.fused_front, args.fused_combine]) > 1:
+        ap.error("--mx, --mxfp4, --mxfp4a4, --nvfp4, --fused-front and --fused-combine are separate entry points; "
+                 "pick one")
     if args.warmup < 3:
         print("bench: at least 3 warm-up steps are required; using 3", file=sys.stderr)
         args.warmup = 3

@@ -133,15 +133,16 @@ MOE_API moe_status moe_kernels_per_call(const moe_shape* shape, int32_t* count);
  * moe_forward_events, moe_forward_static_scratch), MOE_CALL_FORWARD_FUSED_FRONT
  * (moe_forward_fused_front), MOE_CALL_FORWARD_MX (moe_forward_mx),
  * MOE_CALL_FORWARD_FUSED_COMBINE (moe_forward_fused_combine),
- * MOE_CALL_FORWARD_MXFP4 (moe_forward_mxfp4) or MOE_CALL_FORWARD_MXFP4A4
- * (moe_forward_mxfp4a4).  Another value of call: MOE_ERR_INVALID_ARG.
- * Host-only. */
+ * MOE_CALL_FORWARD_MXFP4 (moe_forward_mxfp4), MOE_CALL_FORWARD_MXFP4A4
+ * (moe_forward_mxfp4a4) or MOE_CALL_FORWARD_NVFP4 (moe_forward_nvfp4).
+ * Another value of call: MOE_ERR_INVALID_ARG.  Host-only. */
 #define MOE_CALL_FORWARD 0
 #define MOE_CALL_FORWARD_FUSED_FRONT 1
 #define MOE_CALL_FORWARD_MX 2
 #define MOE_CALL_FORWARD_FUSED_COMBINE 3
 #define MOE_CALL_FORWARD_MXFP4 4
 #define MOE_CALL_FORWARD_MXFP4A4 5
+#define MOE_CALL_FORWARD_NVFP4 6
 MOE_API moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t* count);
 
 /* moe_forward, plus CUDA events recorded on `stream` around the kernels:
@@ -265,8 +266,9 @@ typedef struct {
   int64_t P_max;      /* T*top_k + E*15: the most padded rows any routing can need */
 } moe_views;
 
-/* Device addresses of the MXFP8 layer's extra intermediates (its token codes
- * are in moe_views.xg).  Scales in the layout described above. */
+/* Device addresses of the block-scaled layers' extra intermediates (MXFP8,
+ * MXFP4 and NVFP4; their token codes are in moe_views.xg, two per byte for the
+ * FP4 layers).  Scales in the layouts described below. */
 typedef struct {
   void* x_codes;    /* [P_max, H] E4M3 codes of the gathered token rows */
   void* x_scales;   /* their scales */
@@ -274,6 +276,9 @@ typedef struct {
   void* act_scales; /* their scales */
   int32_t x_chunk_rows;    /* token rows per scale chunk of x_scales (the gate/up GEMM's unit) */
   int32_t act_chunk_rows;  /* the same for act_scales (the down GEMM's unit) */
+  void* x_gscale;          /* NVFP4 layer: [P_max] fp32 tensor scale of each gathered token row */
+  void* act_gscale;        /* NVFP4 layer: [P_max] fp32 tensor scale of each activation row */
+  int32_t nv_chunk_rows;   /* NVFP4 layer: token rows per scale chunk, both GEMMs (one CTA per unit) */
 } moe_mx_views;
 
 MOE_API moe_status moe_workspace_views_mx(const moe_shape* shape, void* workspace, size_t workspace_bytes,
@@ -390,6 +395,47 @@ MOE_API moe_status moe_forward_mxfp4a4(const moe_shape* shape, const moe_bf16* x
                                        const uint8_t* w13_scales, const uint8_t* w2_codes, const uint8_t* w2_scales,
                                        moe_bf16* y, void* workspace, size_t workspace_bytes, moe_stream_t stream,
                                        void* const* events, int32_t n_events);
+
+/* ---- NVFP4 (E2M1 codes, E4M3 scales per 16, fp32 tensor scales) ---------
+ * NVFP4 (the same pages name it beside MXFP8 / MXFP4, with an absolute
+ * maximum over 16 elements; its published two-level form): every 16
+ * consecutive elements along the reduction dimension share an E4M3 scale s
+ * (sign 0), every tensor an fp32 scale g = amax_tensor / (448 * 6) (1 for an
+ * all-zero tensor); s = E4M3(amax_16 / (6 g)) (nearest even, saturating to
+ * 448) and each element the E2M1 code of x / (value(s) * g) (0 where that is
+ * 0), each step one fp32 operation in this order.  The tensor of a weight is
+ * one expert matrix (W13_e, W2_e); that of the token rows and activations one
+ * row.  Codes: two per byte as for MXFP4.  Scales: 512-byte tiles per 128
+ * rows and 64 elements of K, byte r*16 + 4*j + b = the scale of row 32*j + r
+ * and 16-element block b of the 64 (W13 rows in the gate/up tile-row order as
+ * for MXFP8). */
+
+/* Byte sizes of the NVFP4 copies of W13 and W2 (their tensor scales: E floats
+ * each, caller-sized). */
+MOE_API moe_status moe_nvfp4_weight_sizes(const moe_shape* shape, size_t* w13_codes, size_t* w13_scales,
+                                          size_t* w2_codes, size_t* w2_scales);
+
+/* Quantize the bf16 expert weights to NVFP4 on the device (asynchronous on
+ * `stream`): codes and block scales sized by moe_nvfp4_weight_sizes, tensor
+ * scales w13_gscale[E], w2_gscale[E] (fp32; they hold the absolute maxima
+ * until the last kernel of the call has run).  Codes 32-byte aligned, scales
+ * 16-byte, tensor scales 4-byte aligned; else MOE_ERR_INVALID_ARG. */
+MOE_API moe_status moe_nvfp4_quantize_weights(const moe_shape* shape, const moe_bf16* w13, const moe_bf16* w2,
+                                              uint8_t* w13_codes, uint8_t* w13_scales, float* w13_gscale,
+                                              uint8_t* w2_codes, uint8_t* w2_scales, float* w2_gscale,
+                                              moe_stream_t stream);
+
+/* The NVFP4 layer: as moe_forward_mxfp4a4 with NVFP4 weights, token rows and
+ * activations (tcgen05.mma kind::mxf4nvf4, scale_vec::4X: four E4M3 scales per
+ * row per MMA of K = 64; the fp32 tensor scales of the expert matrix and of the
+ * token row multiply each accumulator in the epilogue), one CTA per work unit
+ * in every tile plan.  H and I multiples of 256 (else MOE_ERR_UNSUPPORTED). */
+MOE_API moe_status moe_forward_nvfp4(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                                     const float* w_router, const float* router_bias, const uint8_t* w13_codes,
+                                     const uint8_t* w13_scales, const float* w13_gscale, const uint8_t* w2_codes,
+                                     const uint8_t* w2_scales, const float* w2_gscale, moe_bf16* y, void* workspace,
+                                     size_t workspace_bytes, moe_stream_t stream, void* const* events,
+                                     int32_t n_events);
 
 /* QK-norm, in place: RMSNorm of every attention head of Q and of K
  * ("CuTeDSL chez Perplexity", "Norme QK"):

@@ -49,16 +49,28 @@ def mx4_bytes(n_elems: int) -> int:
     return n_elems // 2 + n_elems // 32
 
 
+def nv4_bytes(n_elems: int) -> int:
+    """NVFP4 bytes of n elements: E2M1 codes two per byte plus one E4M3 scale per 16
+    (the fp32 tensor scales, one per matrix or row, are left out)."""
+    return n_elems // 2 + n_elems // 16
+
+
 def weight_bytes(n_elems: int, mx) -> int:
-    """Bytes of n weight elements: bf16 (mx false), MXFP8 (mx true) or MXFP4
-    (mx == "mxfp4", FP4 weights with MXFP8 tokens, or "mxfp4a4", the MXFP4 layer)."""
+    """Bytes of n weight elements: bf16 (mx false), MXFP8 (mx true), MXFP4
+    (mx == "mxfp4", FP4 weights with MXFP8 tokens, or "mxfp4a4", the MXFP4 layer)
+    or NVFP4 (mx == "nvfp4")."""
+    if mx == "nvfp4":
+        return nv4_bytes(n_elems)
     if mx in ("mxfp4", "mxfp4a4"):
         return mx4_bytes(n_elems)
     return mx_bytes(n_elems) if mx else n_elems * BF16
 
 
 def token_bytes(n_elems: int, mx) -> int:
-    """Bytes of n quantized token elements: MXFP4 in the MXFP4 layer, else MXFP8."""
+    """Bytes of n quantized token elements: MXFP4 in the MXFP4 layer, NVFP4 in
+    the NVFP4 layer, else MXFP8."""
+    if mx == "nvfp4":
+        return nv4_bytes(n_elems)
     return mx4_bytes(n_elems) if mx == "mxfp4a4" else mx_bytes(n_elems)
 
 

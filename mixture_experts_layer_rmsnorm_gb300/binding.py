@@ -38,7 +38,8 @@ class MoeViews(ctypes.Structure):
 
 class MoeMxViews(ctypes.Structure):
     _fields_ = [("x_codes", ctypes.c_void_p), ("x_scales", ctypes.c_void_p), ("act_codes", ctypes.c_void_p),
-                ("act_scales", ctypes.c_void_p), ("x_chunk_rows", ctypes.c_int32), ("act_chunk_rows", ctypes.c_int32)]
+                ("act_scales", ctypes.c_void_p), ("x_chunk_rows", ctypes.c_int32), ("act_chunk_rows", ctypes.c_int32),
+                ("x_gscale", ctypes.c_void_p), ("act_gscale", ctypes.c_void_p), ("nv_chunk_rows", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -83,6 +84,9 @@ def load(build: bool = True):
             lib.moe_mxfp4_quantize_weights.argtypes = [sp, p, p, p, p, p, p, p]
             lib.moe_forward_mxfp4.argtypes = [sp, p, p, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_forward_mxfp4a4.argtypes = [sp, p, p, p, p, p, p, p, p, p, p, sz, p, p, i32]
+            lib.moe_nvfp4_weight_sizes.argtypes = [sp, psz, psz, psz, psz]
+            lib.moe_nvfp4_quantize_weights.argtypes = [sp, p, p, p, p, p, p, p, p, p]
+            lib.moe_forward_nvfp4.argtypes = [sp, p, p, p, p, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_forward_fused_front.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_forward_fused_combine.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_status_string.argtypes = [ctypes.c_int]
@@ -94,7 +98,8 @@ def load(build: bool = True):
                       "moe_qk_norm", "moe_mx_weight_sizes", "moe_mx_quantize_weights", "moe_workspace_size_mx",
                       "moe_workspace_views_mx", "moe_forward_mx", "moe_forward_fused_combine",
                       "moe_mxfp4_weight_sizes", "moe_mxfp4_quantize_weights", "moe_forward_mxfp4",
-                      "moe_forward_mxfp4a4"):
+                      "moe_forward_mxfp4a4", "moe_nvfp4_weight_sizes", "moe_nvfp4_quantize_weights",
+                      "moe_forward_nvfp4"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -134,7 +139,7 @@ def moe_kernels_per_call(s: MoeShape) -> tuple[int, int]:
 
 
 (MOE_CALL_FORWARD, MOE_CALL_FORWARD_FUSED_FRONT, MOE_CALL_FORWARD_MX, MOE_CALL_FORWARD_FUSED_COMBINE,
- MOE_CALL_FORWARD_MXFP4, MOE_CALL_FORWARD_MXFP4A4) = 0, 1, 2, 3, 4, 5
+ MOE_CALL_FORWARD_MXFP4, MOE_CALL_FORWARD_MXFP4A4, MOE_CALL_FORWARD_NVFP4) = 0, 1, 2, 3, 4, 5, 6
 
 
 def moe_kernels_per_call_of(s: MoeShape, call: int) -> tuple[int, int]:
@@ -284,6 +289,29 @@ def moe_forward_mxfp4a4(s: MoeShape, x, g_norm, w_router, router_bias, w13_codes
                                       w2_codes, w2_scales, y, workspace, workspace_bytes, stream, arr, n)
 
 
+def moe_nvfp4_weight_sizes(s: MoeShape) -> tuple[int, tuple[int, int, int, int]]:
+    v = [ctypes.c_size_t(0) for _ in range(4)]
+    st = load().moe_nvfp4_weight_sizes(ctypes.byref(s), *[ctypes.byref(a) for a in v])
+    return st, tuple(a.value for a in v)
+
+
+def moe_nvfp4_quantize_weights(s: MoeShape, w13, w2, w13_codes, w13_scales, w13_gscale, w2_codes, w2_scales,
+                               w2_gscale, stream) -> int:
+    return load().moe_nvfp4_quantize_weights(ctypes.byref(s), w13, w2, w13_codes, w13_scales, w13_gscale, w2_codes,
+                                             w2_scales, w2_gscale, stream)
+
+
+def moe_forward_nvfp4(s: MoeShape, x, g_norm, w_router, router_bias, w13_codes, w13_scales, w13_gscale, w2_codes,
+                      w2_scales, w2_gscale, y, workspace, workspace_bytes, stream, events=None) -> int:
+    if events is None:
+        arr, n = None, 0
+    else:
+        arr, n = (ctypes.c_void_p * len(events))(*events), len(events)
+    return load().moe_forward_nvfp4(ctypes.byref(s), x, g_norm, w_router, router_bias, w13_codes, w13_scales,
+                                    w13_gscale, w2_codes, w2_scales, w2_gscale, y, workspace, workspace_bytes, stream,
+                                    arr, n)
+
+
 def _ptr(t):
     return None if t is None else t.data_ptr()
 
@@ -403,6 +431,40 @@ class MoeLayer:
                 _ptr(self.workspace), self.workspace_bytes_mx(T), s, events)
         if st != MOE_OK:
             raise MoeError(st, name)
+        return y
+
+    def quantize_nvfp4(self, stream=None):
+        """Make the NVFP4 copies of W13 and W2 (moe_nvfp4_quantize_weights) for forward_nvfp4."""
+        import torch
+        st, (n13c, n13s, n2c, n2s) = moe_nvfp4_weight_sizes(self.shape(1))
+        if st != MOE_OK:
+            raise MoeError(st, "moe_nvfp4_weight_sizes")
+        u8 = dict(dtype=torch.uint8, device=self.device)
+        self.w13_codes_nv, self.w13_scales_nv = torch.empty(n13c, **u8), torch.empty(n13s, **u8)
+        self.w2_codes_nv, self.w2_scales_nv = torch.empty(n2c, **u8), torch.empty(n2s, **u8)
+        self.w13_gscale_nv = torch.empty(self.E, dtype=torch.float32, device=self.device)
+        self.w2_gscale_nv = torch.empty(self.E, dtype=torch.float32, device=self.device)
+        s = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        st = moe_nvfp4_quantize_weights(self.shape(1), _ptr(self.w13), _ptr(self.w2), _ptr(self.w13_codes_nv),
+                                        _ptr(self.w13_scales_nv), _ptr(self.w13_gscale_nv), _ptr(self.w2_codes_nv),
+                                        _ptr(self.w2_scales_nv), _ptr(self.w2_gscale_nv), s)
+        if st != MOE_OK:
+            raise MoeError(st, "moe_nvfp4_quantize_weights")
+
+    def forward_nvfp4(self, x, y=None, stream=None, events=None):
+        """y = layer(x), the NVFP4 layer (call quantize_nvfp4 first)."""
+        import torch
+        T = x.shape[0]
+        self.ensure_capacity(T)
+        if y is None:
+            y = torch.empty((T, self.H), dtype=x.dtype, device=x.device)
+        s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
+        st = moe_forward_nvfp4(self.shape(T), _ptr(x), _ptr(self.g_norm), _ptr(self.w_router), _ptr(self.bias),
+                               _ptr(self.w13_codes_nv), _ptr(self.w13_scales_nv), _ptr(self.w13_gscale_nv),
+                               _ptr(self.w2_codes_nv), _ptr(self.w2_scales_nv), _ptr(self.w2_gscale_nv), _ptr(y),
+                               _ptr(self.workspace), self.workspace_bytes_mx(T), s, events)
+        if st != MOE_OK:
+            raise MoeError(st, "moe_forward_nvfp4")
         return y
 
     def workspace_bytes_mx(self, T) -> int:

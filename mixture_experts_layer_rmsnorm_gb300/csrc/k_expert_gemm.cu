@@ -76,7 +76,7 @@ constexpr int kABytes = kWeightBoxRows * kBlockK * 2;  // 16 KB weight tile per 
 constexpr int kTokRowBytes = kBlockK * 2;              // 128 B per token row per stage
 
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
-          bool A4 = false>
+          bool A4 = false, bool NV = false>
 struct GemmCfg {
   // a CTA pair splits the unit's tokens: each CTA holds half of the B tile
   static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * kTokRowBytes;
@@ -89,7 +89,9 @@ struct GemmCfg {
   // carries two scale tiles (two 128-element chunks) per operand
   static constexpr int kKPerStage = A4 ? 256 : MX ? 128 : kBlockK;
   static constexpr int kBoxX = MX ? 128 : kBlockK;    // TMA x coordinate per stage (elements of the map's type)
-  static constexpr int kChunks = A4 ? 2 : 1;          // 128-element scale chunks per stage
+  // scale tiles per operand per stage (a tile: 128 rows x 128 elements of K
+  // with 32-element blocks, or x 64 elements with NVFP4's 16-element blocks)
+  static constexpr int kChunks = NV ? 4 : A4 ? 2 : 1;
   // MXFP4 weights (W4): two E2M1 codes per byte in global memory; the TMA's
   // 16U4_ALIGN16B type spreads each 8 bytes (16 codes) over 16 bytes of shared
   // memory, so the tile's image and descriptors are those of an FP8 tile while
@@ -130,6 +132,7 @@ struct GemmCfg {
   static_assert(kAccBufs == 2 || (MX && PAIR), "a single accumulator buffer only for MXFP8 pairs");
   static_assert(!W4 || MX, "FP4 weights only with block-scaled tokens");
   static_assert(!A4 || W4, "FP4 tokens only with FP4 weights");
+  static_assert(!NV || (A4 && !PAIR), "NVFP4: both operands E2M1, one-CTA units (TMEM columns of the scales)");
   static_assert(!MX || (4 * kChunks <= 16 && 16 + 4 * kChunks * kSfTokTiles <= kSfCols),
                 "scale columns of a stage: weight tiles from +0, token tiles from +16");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
@@ -307,12 +310,12 @@ __device__ __noinline__ bool combine_unit(const ExpertGemmArgs& a, const Unit& u
 }
 
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
-          bool A4 = false>
-__global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4>::kThreads, 1)
+          bool A4 = false, bool NV = false>
+__global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV>::kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_sx,
                        const ExpertGemmArgs args) {
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
@@ -585,7 +588,10 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
             for (int k = 0; k < 4; ++k) {
               const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
               const uint64_t ad = sdesc_kmajor_sw128(sa + k * 32), bd = sdesc_kmajor_sw128(sb + k * 32);
-              if (A4) {  // MMA k: K elements 64k .. 64k+63 = chunk k/2, blocks 2 (k&1), +1
+              if (NV) {  // MMA k: K elements 64k .. 64k+63 = tile k, its 4 scales one word
+                const uint32_t id = idesc_nvf4(128, static_cast<uint32_t>(n_mma));
+                mma_nvf4_ss(d_acc, ad, bd, id, sf_t + 4 * k, sfb_t + 4 * k, accum);
+              } else if (A4) {  // MMA k: K elements 64k .. 64k+63 = chunk k/2, blocks 2 (k&1), +1
                 const uint32_t c = static_cast<uint32_t>(k >> 1), sid = 2u * static_cast<uint32_t>(k & 1);
                 const uint32_t id = idesc_mxf4(PAIR ? 256 : 128, static_cast<uint32_t>(n_mma), sid, sid);
                 if (PAIR)
@@ -708,6 +714,12 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
         const int feat_base = (PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile) * C::kFeatPerTile;
         // SwiGLU (gate/up GEMM) or plain convert of one 16-column group, and its stores
         auto emit_chunk = [&](int c0, float (&v)[16]) {
+          if (NV) {  // NVFP4 tensor scales: the expert matrix's times each token row's
+            const float gw = __ldg(args.w_gscale + un.e);
+            const float* gx = args.x_gscale + un.tok0 + c0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], __fmul_rn(gw, __ldcg(gx + j)));
+          }
           if (!SWIGLU) {
             uint16_t* out = args.out + static_cast<int64_t>(un.tok0 + c0) * args.n_out + feat_base + row;
 #pragma unroll
@@ -815,13 +827,13 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
 }
 
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
-          bool A4 = false>
+          bool A4 = false, bool NV = false>
 cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, int num_sms,
                                cudaStream_t stream, const CUtensorMap* tsw = nullptr,
                                const CUtensorMap* tsx = nullptr) {
   static const CUtensorMap kNoMap = {};  // the scale maps of MXFP8 pairs; unused elsewhere
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4>;
-  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV>;
+  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV>;
   static int configured_device = -1;
   static int max_pairs = 0;  // CTA pairs that fit on the configured device at once
   int dev = 0;
@@ -910,6 +922,26 @@ cudaError_t launch_mx(const CUtensorMap& tw, const CUtensorMap& tx, const CUtens
   }
 }
 
+// NVFP4 plans: one CTA per unit of 32 / 64 / 128 tokens, 9 / 7 / 6 stages of
+// 24 / 28 / 36 KB (4 KB of scale tiles per stage)
+constexpr int kNvStages[3] = {9, 7, 6};
+
+template <bool SWIGLU>
+cudaError_t launch_nv(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, GemmPlan plan,
+                      int num_sms, cudaStream_t stream) {
+  switch (plan) {
+    case GemmPlan::kSmall:
+      return launch_expert_gemm<SWIGLU, kMxBn[0], kNvStages[0], kTokBox[0], false, true, true, true, true>(
+          tw, tx, a, num_sms, stream);
+    case GemmPlan::kMid:
+      return launch_expert_gemm<SWIGLU, kMxBn[1], kNvStages[1], kTokBox[1], false, true, true, true, true>(
+          tw, tx, a, num_sms, stream);
+    default:
+      return launch_expert_gemm<SWIGLU, kMxBn[2], kNvStages[2], kTokBox[2], false, true, true, true, true>(
+          tw, tx, a, num_sms, stream);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const CUtensorMap& tm_sw,
@@ -920,6 +952,8 @@ cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap&
       return launch_mx<true, true>(tm_w13, tm_x, tm_sw, tm_sx, a, plan, num_sms, stream);
     case MxKind::kW4A4:
       return launch_mx<true, true, true>(tm_w13, tm_x, tm_sw, tm_sx, a, plan, num_sms, stream);
+    case MxKind::kNV4:
+      return launch_nv<true>(tm_w13, tm_x, a, plan, num_sms, stream);
     default:
       return launch_mx<true, false>(tm_w13, tm_x, tm_sw, tm_sx, a, plan, num_sms, stream);
   }
@@ -933,6 +967,8 @@ cudaError_t launch_gemm_down_mx(const CUtensorMap& tm_w2, const CUtensorMap& tm_
       return launch_mx<false, true>(tm_w2, tm_act, tm_sw, tm_sx, a, plan, num_sms, stream);
     case MxKind::kW4A4:
       return launch_mx<false, true, true>(tm_w2, tm_act, tm_sw, tm_sx, a, plan, num_sms, stream);
+    case MxKind::kNV4:
+      return launch_nv<false>(tm_w2, tm_act, a, plan, num_sms, stream);
     default:
       return launch_mx<false, false>(tm_w2, tm_act, tm_sw, tm_sx, a, plan, num_sms, stream);
   }

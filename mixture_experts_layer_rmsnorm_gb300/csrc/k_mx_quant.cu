@@ -163,7 +163,188 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
   }
 }
 
+// ------------------------------------------------------------------ NVFP4
+// E2M1 codes (two per byte), one E4M3 scale per 16 elements, one fp32 scale
+// per tensor (NVFP4's two-level scaling; the same pages name NVFP4 with an
+// absolute maximum over 16 elements): g = amax_tensor / (448 * 6) (1 for an
+// all-zero tensor), s = E4M3(amax_16 / (6 g)), q = E2M1(x / (value(s) g)), 0
+// where value(s) g = 0.  The scales are not powers of two, so each step is one
+// explicitly rounded fp32 operation in this order.  Scale tiles: per 128-row
+// group and 64-element chunk of K one 512-byte tile, byte r*16 + 4*j + b = row
+// 32*j + r, 16-element block b of the chunk (the MXFP8 tile with 16-element
+// blocks: a 32-bit TMEM word then holds the 4 scales of one K = 64 MMA).
+
+__device__ __forceinline__ float nv4_global_of(float amax) {
+  return amax > 0.0f ? __fdiv_rn(amax, 2688.0f) : 1.0f;
+}
+
+// E4M3 code of a non-negative fp32 value (nearest even, saturating to 448) and its value
+__device__ __forceinline__ uint32_t e4m3_code(float u) { return e4m3x2(u, 0.0f) & 0xFFu; }
+// value of a non-negative E4M3 code (exponent bias 7, 3 mantissa bits; exponent
+// field 0: m * 2^-9), built exactly as fp32 bits
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : static_cast<float>(m) * 0x1p-9f;
+}
+
+__device__ __forceinline__ size_t nv4_scale_offset(int64_t R, int blk, int K) {
+  const int64_t g = R >> 7;
+  const int rr = static_cast<int>(R & 127);
+  return (static_cast<size_t>(g) * (K / 64) + blk / 4) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (blk & 3);
+}
+
+// Per expert matrix, the absolute maximum of its rows (rows_per_tensor rows
+// each) into amax[e] (zeroed before; fp32 bit patterns of non-negative values
+// order as integers).  One warp per row.
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    nv4_amax_kernel(const uint16_t* __restrict__ src, int64_t rows, int K, int64_t rows_per_tensor,
+                    float* __restrict__ amax) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const uint16_t* s = src + row * K;
+  float m = 0.0f;
+  for (int c = lane; c < K / 8; c += 32) {
+    float x[8];
+    unpack8(*reinterpret_cast<const uint4*>(s + c * 8), x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if (lane == 0) atomicMax(reinterpret_cast<int*>(amax + row / rows_per_tensor), __float_as_int(m));
+}
+
+// amax[e] -> g[e] in place
+__global__ void nv4_global_kernel(float* __restrict__ amax_to_g, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) amax_to_g[i] = nv4_global_of(amax_to_g[i]);
+}
+
+// One warp per row.  MODE 0: matrix rows, g from tensor_amax[row / rows_per_tensor];
+// MODE 1: gathered token rows, MODE 3: activation rows (rows below offsets[E],
+// chunk-grouped scales, g of the row itself, written to g_rows[row]); MODE 2:
+// W13 rows in gate/up tile-row order, g from tensor_amax[expert].
+template <int MODE>
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    nv4_quantize_kernel(const uint16_t* __restrict__ src, int64_t rows, int K, const int32_t* __restrict__ sorted_ids,
+                        const int32_t* __restrict__ offsets, const int32_t* __restrict__ unit_off, int tiles, int bn,
+                        int E, int N, int k, int I, int64_t rows_per_tensor, const float* __restrict__ tensor_amax,
+                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, float* __restrict__ g_rows) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  if ((MODE == 1 || MODE == 3) && row >= __ldcg(offsets + E)) return;
+  const uint16_t* s = nullptr;
+  int64_t R = row;  // scale row
+  if (MODE == 1 || MODE == 3) R = token_scale_row(static_cast<int>(row), offsets, unit_off, E, tiles, bn);
+  if (MODE == 1) {
+    const int id = __ldcg(sorted_ids + row);
+    if (id >= 0 && id < N) s = src + static_cast<int64_t>(id / k) * K;
+  } else {
+    s = src + row * K;
+    if (MODE == 2) {
+      const int64_t e = row / (2 * I);
+      const int i = static_cast<int>(row - e * 2 * I);
+      const int up = i >= I, f = up ? i - I : i;
+      const int m = 32 * ((f & 63) >> 4) + 16 * up + (f & 15);
+      R = (e * (I / 64) + (f >> 6)) * 128 + m;
+    }
+  }
+  const int nch = K >> 3;  // 8-element chunks; a 16-block is 2 neighbouring lanes
+  float g;
+  if (MODE == 1 || MODE == 3) {
+    float m = 0.0f;
+    for (int c = lane; c < nch; c += 32) {
+      float x[8];
+      unpack8(s ? *reinterpret_cast<const uint4*>(s + c * 8) : make_uint4(0, 0, 0, 0), x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(x[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    g = nv4_global_of(m);
+    if (lane == 0) g_rows[row] = g;
+  } else {
+    g = nv4_global_of(__ldg(tensor_amax + row / rows_per_tensor));
+  }
+  const float six_g = __fmul_rn(6.0f, g);
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    const int c = c0 + lane;
+    const bool on = c < nch;  // whole lane pairs are on or off (nch is a multiple of 32 for K % 256 == 0)
+    float x[8];
+    unpack8(on && s ? *reinterpret_cast<const uint4*>(s + c * 8) : make_uint4(0, 0, 0, 0), x);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    const uint32_t sc = e4m3_code(__fdiv_rn(amax, six_g));
+    const float X = __fmul_rn(e4m3_value(sc), g);
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = X > 0.0f ? __fdiv_rn(x[i], X) : 0.0f;
+    uint32_t w = e2m1x8(y);
+    if (!(X > 0.0f)) w = 0;  // code 0 (not a signed zero) where the block scale is 0
+    if (on) {
+      *reinterpret_cast<uint32_t*>(codes + row * (K / 2) + c * 4) = w;
+      if ((lane & 1) == 0) scales[nv4_scale_offset(R, c >> 1, K)] = static_cast<uint8_t>(sc);
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_nv4_weight_amax(const uint16_t* src, int64_t rows, int K, int64_t rows_per_tensor, float* amax,
+                                   int n_tensors, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float) * n_tensors, stream);
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  nv4_amax_kernel<<<static_cast<unsigned>(blocks), kQuantWarps * 32, 0, stream>>>(src, rows, K, rows_per_tensor,
+                                                                                   amax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv4_global(float* amax_to_g, int n, cudaStream_t stream) {
+  nv4_global_kernel<<<(n + 127) / 128, 128, 0, stream>>>(amax_to_g, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nv4_quantize_rows(const uint16_t* src, int64_t rows, int K, int64_t rows_per_tensor,
+                                     const float* tensor_amax, uint8_t* codes, uint8_t* scales, cudaStream_t stream) {
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  return launch_pdl(nv4_quantize_kernel<0>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0, stream,
+                    src, rows, K, nullptr, nullptr, nullptr, 1, 32, 0, 0, 1, 0, rows_per_tensor, tensor_amax, codes,
+                    scales, nullptr);
+}
+
+cudaError_t launch_nv4_quantize_w13(const uint16_t* w13, int E, int H, int I, const float* tensor_amax,
+                                    uint8_t* codes, uint8_t* scales, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(E) * 2 * I;
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  return launch_pdl(nv4_quantize_kernel<2>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0, stream,
+                    w13, rows, H, nullptr, nullptr, nullptr, 1, 32, 0, 0, 1, I, static_cast<int64_t>(2) * I,
+                    tensor_amax, codes, scales, nullptr);
+}
+
+cudaError_t launch_nv4_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets,
+                              const int32_t* unit_off, int tiles, int bn, int E, int N, int k, int H, int64_t rows,
+                              uint8_t* codes, uint8_t* scales, float* g_rows, cudaStream_t stream) {
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  return launch_pdl(nv4_quantize_kernel<1>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0, stream,
+                    h, rows, H, sorted_ids, offsets, unit_off, tiles, bn, E, N, k, 0, static_cast<int64_t>(1),
+                    nullptr, codes, scales, g_rows);
+}
+
+cudaError_t launch_nv4_quantize_act(const uint16_t* act, int64_t rows, int K, const int32_t* offsets,
+                                    const int32_t* unit_off, int tiles, int bn, int E, uint8_t* codes,
+                                    uint8_t* scales, float* g_rows, cudaStream_t stream) {
+  const int64_t blocks = (rows + kQuantWarps - 1) / kQuantWarps;
+  return launch_pdl(nv4_quantize_kernel<3>, dim3(static_cast<unsigned>(blocks)), dim3(kQuantWarps * 32), 0, stream,
+                    act, rows, K, nullptr, offsets, unit_off, tiles, bn, E, 0, 1, 0, static_cast<int64_t>(1), nullptr,
+                    codes, scales, g_rows);
+}
 
 cudaError_t launch_mx_quantize_rows(const uint16_t* src, int64_t rows, int K, uint8_t* codes, uint8_t* scales,
                                     cudaStream_t stream) {

@@ -31,7 +31,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
   size_t err, h, logits, ids, w, counts, offsets, unit1, unit2, sorted, slot, flags, ccnt, blk_counts, blk_base,
-      partials, xg, act, out, xs, aq, as, total;
+      partials, xg, act, out, xs, aq, as, gx, ga, total;
   int64_t n_ccnt;      // combine arrival counters of the down GEMM: [H / 128][T]
   int64_t P_max;       // padded rows: 16-row padding (bf16), 32-row padding rounded to 128 (MXFP8)
   int64_t sorted_cap;  // sorted_ids entries (room for debug padding up to 256)
@@ -84,6 +84,10 @@ Layout make_layout(const moe_shape& s, bool mx = false) {
     L.xs = take(static_cast<size_t>(L.P_max / 32) * 2 * (H / 128) * 512);
     L.aq = take(static_cast<size_t>(L.P_max * I));
     L.as = take(static_cast<size_t>(L.P_max / 32) * 2 * (I / 128) * 512);
+    // NVFP4: fp32 tensor scale of each gathered token row and activation row
+    // (its token scales, one 512-byte tile per <= 128 rows and 64 of K, fit xs / as)
+    L.gx = take(static_cast<size_t>(L.P_max) * 4);
+    L.ga = take(static_cast<size_t>(L.P_max) * 4);
   }
   L.total = off;
   return L;
@@ -290,7 +294,7 @@ moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes) {
 moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t* count) {
   const moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
-  if (!count || call < MOE_CALL_FORWARD || call > MOE_CALL_FORWARD_MXFP4A4) return MOE_ERR_INVALID_ARG;
+  if (!count || call < MOE_CALL_FORWARD || call > MOE_CALL_FORWARD_NVFP4) return MOE_ERR_INVALID_ARG;
   const moe_shape& s = *shape;
   if (s.T == 0) {
     *count = 0;
@@ -302,7 +306,8 @@ moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t
     *count = front + 3;
   else if (call == MOE_CALL_FORWARD_FUSED_FRONT)
     *count = 1 + 3;
-  else if (call == MOE_CALL_FORWARD_MX || call == MOE_CALL_FORWARD_MXFP4 || call == MOE_CALL_FORWARD_MXFP4A4)
+  else if (call == MOE_CALL_FORWARD_MX || call == MOE_CALL_FORWARD_MXFP4 || call == MOE_CALL_FORWARD_MXFP4A4 ||
+           call == MOE_CALL_FORWARD_NVFP4)
     *count = front + 4;  // + the activation quantize between the GEMMs
   else
     *count = front + 2;  // the combine runs inside the down GEMM
@@ -513,15 +518,18 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
 moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
                            const float* router_bias, const uint8_t* w13c, const uint8_t* w13s, const uint8_t* w2c,
                            const uint8_t* w2s, moe_bf16* y, void* workspace, size_t workspace_bytes,
-                           moe_stream_t stream, void* const* events, MxKind kind = MxKind::kW8A8) {
+                           moe_stream_t stream, void* const* events, MxKind kind = MxKind::kW8A8,
+                           const float* w13g = nullptr, const float* w2g = nullptr) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   const moe_shape& s = *shape;
   if (s.T == 0) return MOE_OK;
   const GemmPlan plan = moe::choose_plan(s.T, s.top_k, s.E);
   if (s.E > 256) return MOE_ERR_UNSUPPORTED;
-  const bool fp4 = kind != MxKind::kW8A8, a4 = kind == MxKind::kW4A4;
+  const bool fp4 = kind != MxKind::kW8A8, nv = kind == MxKind::kNV4;
+  const bool a4 = kind == MxKind::kW4A4 || nv;  // packed E2M1 token codes too
   if (a4 && (s.H % 256 != 0 || s.I % 256 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (nv && (!w13g || !w2g || !aligned(w13g, 4) || !aligned(w2g, 4))) return MOE_ERR_INVALID_ARG;
   st = check_inputs(shape, x, g_norm, w_router, router_bias, workspace, workspace_bytes, true);
   if (st != MOE_OK) return st;
   const size_t code_align = fp4 ? 32 : 16;  // the 4-bit tensor maps want 32-byte bases (one rule for both layers)
@@ -534,7 +542,8 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   const Layout L = make_layout(s, true);
   const int tiles1 = s.I / moe::kGateUpTileFeat, tiles2 = s.H / moe::kDownTileFeat;
   // prefill: CTA pairs where the weight tiles come in pairs (256-token units)
-  const bool pair1 = moe::gemm_uses_pairs(plan, tiles1), pair2 = moe::gemm_uses_pairs(plan, tiles2);
+  // (NVFP4: one CTA per unit in every plan; its scale tiles take the TMEM a pair's accumulator needs)
+  const bool pair1 = !nv && moe::gemm_uses_pairs(plan, tiles1), pair2 = !nv && moe::gemm_uses_pairs(plan, tiles2);
   const int bn1 = moe::gemm_bn_mx(plan, pair1), bn2 = moe::gemm_bn_mx(plan, pair2);
   const int utiles1 = pair1 ? tiles1 / 2 : tiles1, utiles2 = pair2 ? tiles2 / 2 : tiles2;
   auto mark = [&](int i) {
@@ -566,12 +575,19 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   if (st != MOE_OK) return st;
   if (!mark(1) || !mark(2) || !mark(3)) return MOE_ERR_CUDA;
   const int N = s.T * s.top_k;
-  auto gather = a4 ? moe::launch_mx4_gather : moe::launch_mx_gather;
-  if (gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.offsets),
-             at<int32_t>(workspace, L.unit1), utiles1, bn1, s.E, N, s.top_k, s.H, L.P_max,
-             at<uint8_t>(workspace, L.xg), at<uint8_t>(workspace, L.xs), cs) != cudaSuccess ||
-      !mark(4))
-    return MOE_ERR_CUDA;
+  cudaError_t ge;
+  if (nv) {
+    ge = moe::launch_nv4_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
+                                at<int32_t>(workspace, L.offsets), at<int32_t>(workspace, L.unit1), utiles1, bn1, s.E,
+                                N, s.top_k, s.H, L.P_max, at<uint8_t>(workspace, L.xg), at<uint8_t>(workspace, L.xs),
+                                at<float>(workspace, L.gx), cs);
+  } else {
+    auto gather = a4 ? moe::launch_mx4_gather : moe::launch_mx_gather;
+    ge = gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted), at<int32_t>(workspace, L.offsets),
+                at<int32_t>(workspace, L.unit1), utiles1, bn1, s.E, N, s.top_k, s.H, L.P_max,
+                at<uint8_t>(workspace, L.xg), at<uint8_t>(workspace, L.xs), cs);
+  }
+  if (ge != cudaSuccess || !mark(4)) return MOE_ERR_CUDA;
 
   moe::ExpertGemmArgs a1{};
   a1.offsets = at<int32_t>(workspace, L.offsets);
@@ -589,16 +605,24 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   a1.pair = pair1;
   a1.w_scales = w13s;
   a1.x_scales = at<uint8_t>(workspace, L.xs);
+  a1.w_gscale = w13g;
+  a1.x_gscale = nv ? at<float>(workspace, L.gx) : nullptr;
   if (moe::launch_gemm_gate_up_mx(tm_w13, tm_xq, tm_s13, tm_sxq, a1, plan, num_sms, cs, kind) != cudaSuccess ||
       !mark(5))
     return MOE_ERR_CUDA;
   // the activations (bf16) -> MXFP8, rows below offsets[E], their scales in
   // the down GEMM's token chunks
-  auto quantize_act = a4 ? moe::launch_mx4_quantize_act : moe::launch_mx_quantize_act;
-  if (quantize_act(at<uint16_t>(workspace, L.act), L.P_max, s.I, at<int32_t>(workspace, L.offsets),
-                   at<int32_t>(workspace, L.unit2), utiles2, bn2, s.E, at<uint8_t>(workspace, L.aq),
-                   at<uint8_t>(workspace, L.as), cs) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (nv) {
+    ge = moe::launch_nv4_quantize_act(at<uint16_t>(workspace, L.act), L.P_max, s.I, at<int32_t>(workspace, L.offsets),
+                                      at<int32_t>(workspace, L.unit2), utiles2, bn2, s.E, at<uint8_t>(workspace, L.aq),
+                                      at<uint8_t>(workspace, L.as), at<float>(workspace, L.ga), cs);
+  } else {
+    auto quantize_act = a4 ? moe::launch_mx4_quantize_act : moe::launch_mx_quantize_act;
+    ge = quantize_act(at<uint16_t>(workspace, L.act), L.P_max, s.I, at<int32_t>(workspace, L.offsets),
+                      at<int32_t>(workspace, L.unit2), utiles2, bn2, s.E, at<uint8_t>(workspace, L.aq),
+                      at<uint8_t>(workspace, L.as), cs);
+  }
+  if (ge != cudaSuccess) return MOE_ERR_CUDA;
   moe::ExpertGemmArgs a2{};
   a2.offsets = at<int32_t>(workspace, L.offsets);
   a2.unit_off = at<int32_t>(workspace, L.unit2);
@@ -615,6 +639,8 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   a2.pair = pair2;
   a2.w_scales = w2s;
   a2.x_scales = at<uint8_t>(workspace, L.as);
+  a2.w_gscale = w2g;
+  a2.x_gscale = nv ? at<float>(workspace, L.ga) : nullptr;
   if (moe::launch_gemm_down_mx(tm_w2, tm_aq, tm_s2, tm_saq, a2, plan, num_sms, cs, kind) != cudaSuccess || !mark(6))
     return MOE_ERR_CUDA;
   if (moe::launch_combine(at<uint16_t>(workspace, L.out), at<int32_t>(workspace, L.slot), at<float>(workspace, L.w),
@@ -682,6 +708,43 @@ moe_status moe_mxfp4_quantize_weights(const moe_shape* shape, const moe_bf16* w1
   return MOE_OK;
 }
 
+moe_status moe_nvfp4_weight_sizes(const moe_shape* shape, size_t* w13_codes, size_t* w13_scales, size_t* w2_codes,
+                                  size_t* w2_scales) {
+  const moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!w13_codes || !w13_scales || !w2_codes || !w2_scales) return MOE_ERR_INVALID_ARG;
+  const int64_t E = shape->E, H = shape->H, I = shape->I;
+  *w13_codes = static_cast<size_t>(E * 2 * I * H / 2);
+  *w13_scales = moe::nv4_scale_bytes(E * 2 * I, H);
+  *w2_codes = static_cast<size_t>(E * H * I / 2);
+  *w2_scales = moe::nv4_scale_bytes(E * H, I);
+  return MOE_OK;
+}
+
+moe_status moe_nvfp4_quantize_weights(const moe_shape* shape, const moe_bf16* w13, const moe_bf16* w2,
+                                      uint8_t* w13_codes, uint8_t* w13_scales, float* w13_gscale, uint8_t* w2_codes,
+                                      uint8_t* w2_scales, float* w2_gscale, moe_stream_t stream) {
+  const moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!w13 || !w2 || !w13_codes || !w13_scales || !w13_gscale || !w2_codes || !w2_scales || !w2_gscale ||
+      !aligned(w13, 16) || !aligned(w2, 16) || !aligned(w13_codes, 32) || !aligned(w13_scales, 16) ||
+      !aligned(w2_codes, 32) || !aligned(w2_scales, 16) || !aligned(w13_gscale, 4) || !aligned(w2_gscale, 4))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const moe_shape& s = *shape;
+  const int64_t r13 = static_cast<int64_t>(s.E) * 2 * s.I, r2 = static_cast<int64_t>(s.E) * s.H;
+  // the tensor-scale arrays hold each expert matrix's absolute maximum until
+  // the codes are written, then its tensor scale
+  if (moe::launch_nv4_weight_amax(w13, r13, s.H, 2 * s.I, w13_gscale, s.E, cs) != cudaSuccess ||
+      moe::launch_nv4_weight_amax(w2, r2, s.I, s.H, w2_gscale, s.E, cs) != cudaSuccess ||
+      moe::launch_nv4_quantize_w13(w13, s.E, s.H, s.I, w13_gscale, w13_codes, w13_scales, cs) != cudaSuccess ||
+      moe::launch_nv4_quantize_rows(w2, r2, s.I, s.H, w2_gscale, w2_codes, w2_scales, cs) != cudaSuccess ||
+      moe::launch_nv4_global(w13_gscale, s.E, cs) != cudaSuccess ||
+      moe::launch_nv4_global(w2_gscale, s.E, cs) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 moe_status moe_workspace_size_mx(const moe_shape* shape, size_t* bytes) {
   const moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
@@ -718,6 +781,9 @@ moe_status moe_workspace_views_mx(const moe_shape* shape, void* workspace, size_
   const GemmPlan plan = moe::choose_plan(s.T, s.top_k, s.E);
   mv->x_chunk_rows = moe::gemm_bn_mx(plan, moe::gemm_uses_pairs(plan, s.I / moe::kGateUpTileFeat));
   mv->act_chunk_rows = moe::gemm_bn_mx(plan, moe::gemm_uses_pairs(plan, s.H / moe::kDownTileFeat));
+  mv->x_gscale = at<void>(workspace, L.gx);
+  mv->act_gscale = at<void>(workspace, L.ga);
+  mv->nv_chunk_rows = moe::gemm_bn_mx(plan, false);
   return MOE_OK;
 }
 
@@ -760,6 +826,20 @@ moe_status moe_forward_mxfp4a4(const moe_shape* shape, const moe_bf16* x, const 
   }
   return moe::forward_mx_impl(shape, x, g_norm, w_router, router_bias, w13_codes, w13_scales, w2_codes, w2_scales, y,
                               workspace, workspace_bytes, stream, events, moe::MxKind::kW4A4);
+}
+
+moe_status moe_forward_nvfp4(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                             const float* w_router, const float* router_bias, const uint8_t* w13_codes,
+                             const uint8_t* w13_scales, const float* w13_gscale, const uint8_t* w2_codes,
+                             const uint8_t* w2_scales, const float* w2_gscale, moe_bf16* y, void* workspace,
+                             size_t workspace_bytes, moe_stream_t stream, void* const* events, int32_t n_events) {
+  if (events) {
+    if (n_events < MOE_NUM_KERNELS + 1) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i <= MOE_NUM_KERNELS; ++i)
+      if (!events[i]) return MOE_ERR_INVALID_ARG;
+  }
+  return moe::forward_mx_impl(shape, x, g_norm, w_router, router_bias, w13_codes, w13_scales, w2_codes, w2_scales, y,
+                              workspace, workspace_bytes, stream, events, moe::MxKind::kNV4, w13_gscale, w2_gscale);
 }
 
 moe_status moe_forward(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,

@@ -114,6 +114,8 @@ struct ExpertGemmArgs {
   int tables_from_parent;   // 1: the routing tables come from the previous kernel (wait before reading)
   const uint8_t* w_scales;  // MXFP8 GEMMs: weight scales (512-byte tiles per 128 rows x 128 of K)
   const uint8_t* x_scales;  // MXFP8 GEMMs: token scales, one 512-byte tile per token chunk and 128 of K
+  const float* w_gscale;    // NVFP4 GEMMs: fp32 tensor scale per expert matrix [E]
+  const float* x_gscale;    // NVFP4 GEMMs: fp32 tensor scale per token row
   // Down GEMM with the top-k weighted combine in its epilogue (fuse_combine = 1):
   // a unit that has stored its output rows of a 128-feature tile counts one
   // arrival per real row at combine_cnt[tile * T + t]; the arrival that
@@ -160,8 +162,10 @@ int gemm_unit_tiles(GemmPlan plan, int tiles);
 // with the same boxes); a.w_scales / a.x_scales hold the E8M0 scales.
 // The operand formats of the block-scaled GEMMs: E4M3 x E4M3, E2M1 weights x
 // E4M3 tokens (both kind::mxf8f6f4), E2M1 x E2M1 (kind::mxf4; tm_w and tm_x
-// then map the packed code bytes, 256 elements of K per stage).
-enum class MxKind { kW8A8, kW4A8, kW4A4 };
+// then map the packed code bytes, 256 elements of K per stage); NVFP4 on both
+// (kind::mxf4nvf4, E4M3 scales per 16 elements, one-CTA units only, the fp32
+// tensor scales a.w_gscale[e] * a.x_gscale[row] applied in the epilogue).
+enum class MxKind { kW8A8, kW4A8, kW4A4, kNV4 };
 cudaError_t launch_gemm_gate_up_mx(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const CUtensorMap& tm_sw,
                                    const CUtensorMap& tm_sx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
                                    cudaStream_t stream, MxKind kind = MxKind::kW8A8);
@@ -231,6 +235,26 @@ cudaError_t launch_mx4_gather(const uint16_t* h, const int32_t* sorted_ids, cons
 cudaError_t launch_mx4_quantize_act(const uint16_t* act, int64_t rows, int K, const int32_t* offsets,
                                     const int32_t* unit_off, int tiles, int bn, int E, uint8_t* codes,
                                     uint8_t* scales, cudaStream_t stream);
+// NVFP4 (k_mx_quant.cu): E2M1 codes two per byte, E4M3 scales per 16 elements
+// in 512-byte tiles per 128 rows and 64 elements of K, fp32 tensor scales.
+// Weights: the absolute maximum per expert matrix (rows_per_tensor rows) into
+// amax[] (launch_nv4_weight_amax), the codes and scales from it, then amax[]
+// turned into the tensor scales in place (launch_nv4_global).  Token rows and
+// activations: one tensor scale per row, written to g_rows[row].
+cudaError_t launch_nv4_weight_amax(const uint16_t* src, int64_t rows, int K, int64_t rows_per_tensor, float* amax,
+                                   int n_tensors, cudaStream_t stream);
+cudaError_t launch_nv4_global(float* amax_to_g, int n, cudaStream_t stream);
+cudaError_t launch_nv4_quantize_rows(const uint16_t* src, int64_t rows, int K, int64_t rows_per_tensor,
+                                     const float* tensor_amax, uint8_t* codes, uint8_t* scales, cudaStream_t stream);
+cudaError_t launch_nv4_quantize_w13(const uint16_t* w13, int E, int H, int I, const float* tensor_amax,
+                                    uint8_t* codes, uint8_t* scales, cudaStream_t stream);
+cudaError_t launch_nv4_gather(const uint16_t* h, const int32_t* sorted_ids, const int32_t* offsets,
+                              const int32_t* unit_off, int tiles, int bn, int E, int N, int k, int H, int64_t rows,
+                              uint8_t* codes, uint8_t* scales, float* g_rows, cudaStream_t stream);
+cudaError_t launch_nv4_quantize_act(const uint16_t* act, int64_t rows, int K, const int32_t* offsets,
+                                    const int32_t* unit_off, int tiles, int bn, int E, uint8_t* codes,
+                                    uint8_t* scales, float* g_rows, cudaStream_t stream);
+inline size_t nv4_scale_bytes(int64_t rows, int64_t K) { return static_cast<size_t>(rows / 128) * (K / 64) * 512; }
 inline size_t mx_scale_bytes(int64_t rows, int64_t K) { return static_cast<size_t>(rows / 128) * (K / 128) * 512; }
 
 // QK-norm of q[T, Hq, D] and k[T, Hk, D] in place (k_qk_norm.cu); D = 64, 128 or 256.

@@ -298,6 +298,20 @@ __device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// NVFP4 MMA (kind::mxf4nvf4, scale_vec::4X): packed E2M1 operands as for
+// kind::mxf4, one UE4M3 scale per 16 elements, i.e. the 4 bytes of the row's
+// 32-bit TMEM word for one MMA of K = 64 (scale id 0; measured on GB300).
+__device__ __forceinline__ void mma_nvf4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::
+          "r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Block-scaled MMA on packed E2M1 operands (kind::mxf4, K = 64: one 32-byte
 // step of a 128-byte K-major row holds 64 codes, two per byte, the even
 // element in the low nibble); two UE8M0 scales per row per MMA, the bytes
@@ -416,6 +430,12 @@ __host__ __device__ __forceinline__ constexpr uint32_t idesc_mxf8(uint32_t M, ui
   return (sf_b << 4) | (a_fmt << 7) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sf_a << 29);
 }
 constexpr uint32_t kFmtE2M1 = 5;
+
+// Instruction descriptor, kind::mxf4nvf4 with UE4M3 scales: A and B E2M1
+// (format 1), scale type bit 23 = 0, scale ids 0.
+__host__ __device__ __forceinline__ constexpr uint32_t idesc_nvf4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
 
 // Instruction descriptor, kind::mxf4: A and B E2M1 (format 1 in bits 7-9 and
 // 10-12), K-major, UE8M0 scales (bit 23); scale ids (0 or 2) in bits 29-30 / 4-5.

@@ -65,11 +65,12 @@ def test_kernels_per_call_host_checks():
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_MX) == (binding.MOE_OK, 7)
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_MXFP4) == (binding.MOE_OK, 7)
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_MXFP4A4) == (binding.MOE_OK, 7)
-    assert binding.moe_kernels_per_call_of(s4, 6)[0] == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_NVFP4) == (binding.MOE_OK, 7)
+    assert binding.moe_kernels_per_call_of(s4, 7)[0] == binding.MOE_ERR_INVALID_ARG
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_FUSED_COMBINE) == (binding.MOE_OK, 5)
     s4096 = binding.shape(4096, 128, 256, 8, 2)
     assert binding.moe_kernels_per_call_of(s4096, binding.MOE_CALL_FORWARD_FUSED_COMBINE) == (binding.MOE_OK, 7)
-    assert binding.moe_kernels_per_call_of(s4, 6)[0] == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_kernels_per_call_of(s4, 7)[0] == binding.MOE_ERR_INVALID_ARG
     assert binding.moe_kernels_per_call_of(s4, -1)[0] == binding.MOE_ERR_INVALID_ARG
 
 
@@ -149,6 +150,32 @@ def test_mxfp4_sizes_and_argument_checks_without_a_gpu():
     assert binding.moe_mxfp4_quantize_weights(s, A, A, A, A, A + 48, A, None) == binding.MOE_ERR_INVALID_ARG
     assert binding.moe_mxfp4_quantize_weights(binding.shape(4, 100, 384, 8, 2), A, A, A, A, A, A, None) == \
         binding.MOE_ERR_UNSUPPORTED
+
+
+def test_nvfp4_sizes_and_argument_checks_without_a_gpu():
+    s = binding.shape(4, 256, 512, 8, 2)
+    st, (c13, s13, c2, s2) = binding.moe_nvfp4_weight_sizes(s)
+    assert st == binding.MOE_OK
+    assert (c13, c2) == (8 * 2 * 512 * 256 // 2, 8 * 256 * 512 // 2)
+    assert (s13, s2) == (8 * 2 * 512 * 256 // 16, 8 * 256 * 512 // 16)  # one E4M3 byte per 16 elements
+    _, need = binding.moe_workspace_size_mx(s)
+    A = 1 << 20
+
+    def fwd(**kw):
+        a = dict(c13=A, g13=A, g2=A, nbytes=need, shape=s)
+        a.update(kw)
+        return binding.moe_forward_nvfp4(a["shape"], A, A, A, None, a["c13"], A, a["g13"], A, A, a["g2"], A, A,
+                                         a["nbytes"], None)
+
+    assert fwd(c13=A + 16) == binding.MOE_ERR_INVALID_ARG
+    assert fwd(g13=None) == binding.MOE_ERR_INVALID_ARG
+    assert fwd(g2=A + 2) == binding.MOE_ERR_INVALID_ARG
+    assert fwd(nbytes=need - 1) == binding.MOE_ERR_WORKSPACE
+    assert fwd(shape=binding.shape(4, 256, 384, 8, 2)) == binding.MOE_ERR_UNSUPPORTED
+    q = binding.moe_nvfp4_quantize_weights
+    assert q(s, A, A, A + 16, A, A, A, A, A, None) == binding.MOE_ERR_INVALID_ARG
+    assert q(s, A, A, A, A, None, A, A, A, None) == binding.MOE_ERR_INVALID_ARG
+    assert q(s, A, A, A, A, A, A, A, A + 1, None) == binding.MOE_ERR_INVALID_ARG
 
 
 def test_route_debug_rejects_bad_arguments_without_a_gpu():

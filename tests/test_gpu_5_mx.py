@@ -35,7 +35,7 @@ CASES = [
     ("a4_bias_norenorm", 3, 512, 256, 20, 5, False, 1.2, 22),
     ("a4_prefill_ragged_norenorm", 300, 512, 256, 6, 3, False, None, 23),
 ]
-FORMATS = ["mxfp8", "mxfp4", "mxfp4a4"]
+FORMATS = ["mxfp8", "mxfp4", "mxfp4a4", "nvfp4"]
 
 
 @pytest.fixture(scope="module")
@@ -56,15 +56,20 @@ def unpack_e2m1(packed, shape_):
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_mx_layer_parity(case, fmt, o):
     _, T, H, I, E, k, renorm, zipf, seed = case
-    a4 = fmt == "mxfp4a4"
+    nv = fmt == "nvfp4"
+    a4 = fmt == "mxfp4a4" or nv  # packed E2M1 token codes
     if a4 and (H % 256 or I % 256):
-        pytest.skip("the MXFP4 layer takes H and I multiples of 256")
+        pytest.skip("the MXFP4 and NVFP4 layers take H and I multiples of 256")
     cfg = inputs.LayerConfig(T=T, H=H, I=I, E=E, top_k=k, renormalize=renorm, seed=seed, zipf_bias=zipf)
     li = inputs.make_layer_inputs(cfg)
     dl = gu.DeviceLayer(li)
     L = dl.layer
     fp4 = fmt != "mxfp8"
-    if fp4:
+    if nv:
+        L.quantize_nvfp4()
+        codes13, scales13, codes2, scales2 = L.w13_codes_nv, L.w13_scales_nv, L.w2_codes_nv, L.w2_scales_nv
+        quantize, unpack = None, unpack_e2m1
+    elif fp4:
         L.quantize_mxfp4()
         codes13, scales13, codes2, scales2 = L.w13_codes4, L.w13_scales4, L.w2_codes4, L.w2_scales4
         quantize, unpack = o.mx4_quantize, unpack_e2m1
@@ -73,18 +78,27 @@ def test_mx_layer_parity(case, fmt, o):
         codes13, scales13, codes2, scales2 = L.w13_codes, L.w13_scales, L.w2_codes, L.w2_scales
         quantize, unpack = o.mx_quantize, lambda c, shp: c.reshape(shp)
     torch.cuda.synchronize()
-    # weights: codes and scales bit for bit
-    w13c, w13s = quantize(li.w13)
-    w2c, w2s = quantize(li.w2)
+    # weights: codes and scales (and NVFP4's tensor scales) bit for bit; an
+    # NVFP4 scale tile covers 64 elements of K with 16-element blocks, i.e. the
+    # MXFP8 tile of a matrix twice as wide
+    if nv:
+        w13c, w13s, w13g = o.nv4_quantize_experts(li.w13)
+        w2c, w2s, w2g = o.nv4_quantize_experts(li.w2)
+        assert np.array_equal(L.w13_gscale_nv.cpu().numpy(), w13g)
+        assert np.array_equal(L.w2_gscale_nv.cpu().numpy(), w2g)
+    else:
+        w13c, w13s = quantize(li.w13)
+        w2c, w2s = quantize(li.w2)
+    wide, bs = (2, 16) if nv else (1, 32)
     assert np.array_equal(unpack(codes13.cpu().numpy(), (E, 2 * I, H)), w13c)
     assert np.array_equal(unpack(codes2.cpu().numpy(), (E, H, I)), w2c)
-    s13 = gu.ungroup_mx_scales(scales13.cpu().numpy(), E * 2 * I, H)[gu.w13_scale_rows(E, I)]
-    assert np.array_equal(s13.reshape(E, 2 * I, H // 32), w13s)
-    s2 = gu.ungroup_mx_scales(scales2.cpu().numpy(), E * H, I)
-    assert np.array_equal(s2.reshape(E, H, I // 32), w2s)
+    s13 = gu.ungroup_mx_scales(scales13.cpu().numpy(), E * 2 * I, wide * H)[gu.w13_scale_rows(E, I)]
+    assert np.array_equal(s13.reshape(E, 2 * I, H // bs), w13s)
+    s2 = gu.ungroup_mx_scales(scales2.cpu().numpy(), E * H, wide * I)
+    assert np.array_equal(s2.reshape(E, H, I // bs), w2s)
 
     xd = gu.dev_bf16(li.x)
-    y = L.forward_mxfp4(xd, fp4_tokens=a4) if fp4 else L.forward_mx(xd)
+    y = L.forward_nvfp4(xd) if nv else L.forward_mxfp4(xd, fp4_tokens=a4) if fp4 else L.forward_mx(xd)
     torch.cuda.synchronize()
     st, det = L.device_status(T)
     assert st == binding.MOE_OK, (st, det)
@@ -106,18 +120,23 @@ def test_mx_layer_parity(case, fmt, o):
     # scales are grouped by the GEMMs' token chunks (bn rows of an expert)
     # the gate/up GEMM's token rows per unit (its scale chunks): 32 / 64 by
     # decode plan, 128 or 256 in prefill; a chunk's scales take ceil(bn / 128) tiles
-    bn = mv.x_chunk_rows
+    bn = mv.nv_chunk_rows if nv else mv.x_chunk_rows
     small_mid = 32 if T * k <= 16 * E else 64 if T * k <= 64 * E else None
-    assert bn == small_mid if small_mid else bn in (128, 256)
+    assert bn == small_mid if small_mid else bn in ((128,) if nv else (128, 256))
     G = -(-bn // 128)
-    n_groups = 2 * (v.P_max // 32)
+    n_groups = (1 if nv else 2) * (v.P_max // 32)
     if a4:  # E2M1 token codes, two per byte
         xcodes = unpack_e2m1(view(mv.x_codes, torch.uint8, (v.P_max, H // 2)), (v.P_max, H))
     else:
         xcodes = view(mv.x_codes, torch.uint8, (v.P_max, H))
-    xs = gu.ungroup_mx_scales(view(mv.x_scales, torch.uint8, (n_groups * (H // 128) * 512,)), n_groups * 128, H)
+    xs = gu.ungroup_mx_scales(view(mv.x_scales, torch.uint8, (n_groups * (wide * H // 128) * 512,)), n_groups * 128,
+                              wide * H)
     real = np.nonzero(g["sorted"] < T * k)[0]
-    hc, hs = (o.mx4_quantize if a4 else o.mx_quantize)(g["h"][g["sorted"][real] // k])
+    if nv:
+        hc, hs, hg = o.nv4_quantize(g["h"][g["sorted"][real] // k], per_row=True)
+        assert np.array_equal(view(mv.x_gscale, torch.float32, (v.P_max,))[real], hg)
+    else:
+        hc, hs = (o.mx4_quantize if a4 else o.mx_quantize)(g["h"][g["sorted"][real] // k])
     assert np.array_equal(xcodes[real], hc)
     offs = g["offsets"]
     chunk0 = np.concatenate([[0], np.cumsum(-(-np.diff(offs) // bn))])  # chunks before each expert
@@ -126,8 +145,11 @@ def test_mx_layer_parity(case, fmt, o):
     srow = (chunk0[e_of] + within // bn) * 128 * G + within % bn
     assert np.array_equal(xs[srow], hs)
     # the layer output against the oracle's layer of the same weight format
-    fwd = o.moe_forward_mx4a4 if a4 else o.moe_forward_mx4 if fp4 else o.moe_forward_mx
-    r = fwd(li.x, li.g, li.w_router, li.bias, w13c, w13s, w2c, w2s, k, renorm, cfg.eps)
+    if nv:
+        r = o.moe_forward_nv4(li.x, li.g, li.w_router, li.bias, w13c, w13s, w13g, w2c, w2s, w2g, k, renorm, cfg.eps)
+    else:
+        fwd = o.moe_forward_mx4a4 if a4 else o.moe_forward_mx4 if fp4 else o.moe_forward_mx
+        r = fwd(li.x, li.g, li.w_router, li.bias, w13c, w13s, w2c, w2s, k, renorm, cfg.eps)
     yg = gu.widen(y.cpu().numpy().view(np.uint16))
     err = yg - r["y64"]
     rel = np.linalg.norm(err) / np.linalg.norm(r["y64"])
