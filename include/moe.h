@@ -295,8 +295,9 @@ MOE_API moe_status moe_workspace_views(const moe_shape* shape, void* workspace, 
  * 7 combine, 8 self-test), for the expert GEMMs a bit mask of the waits that
  * ran out (bit 1 producer: ring slot free; 2 MMA: accumulator free; 3 MMA:
  * ring slot loaded; 4 epilogue: accumulator complete; 5 epilogue: stream-K
- * partial sums; 6 epilogue: fused-combine rendezvous), and the index of the
- * CTA that recorded the timeout. */
+ * partial sums; 6 epilogue: fused-combine rendezvous; 7 MMA: a stage's scales
+ * written to TMEM; 8 scale warps: ring slot loaded), and the index of the CTA
+ * that recorded the timeout. */
 MOE_API moe_status moe_device_status(const void* workspace, size_t workspace_bytes, moe_stream_t stream,
                              int32_t* detail);
 

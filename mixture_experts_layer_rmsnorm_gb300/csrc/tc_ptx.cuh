@@ -400,6 +400,16 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Store 4 consecutive 32-bit columns of this warp's TMEM lane quarter (thread
+// i -> lane (quarter base + i)); warp-collective.  tmem_st_wait() before the
+// data is signalled to another thread.
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint4& v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Shared-memory matrix descriptor for a K-major bf16 tile written by TMA with
 // 128-byte swizzling: rows of 64 elements (128 B), 8-row groups 1024 B apart.
 //   bits  0-13  start address >> 4
