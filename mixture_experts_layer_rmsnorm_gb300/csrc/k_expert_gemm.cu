@@ -34,7 +34,8 @@
 // quarter.  The finishing CTA adds the partials of the following CTAs
 // before its epilogue, so it never waits on work that has not started.
 //
-// Roles in a CTA of 192 threads (320 for MXFP8 pairs; persistent, one CTA per SM):
+// Roles in a CTA of 192 threads (320 for block-scaled pairs and for the FP4
+// layers' one-CTA units; persistent, one CTA per SM):
 //   warp 0 lane 0   TMA producer: weight tiles [128 x 64] (one box) and token
 //                   tiles of TOKBOX rows per box, 128-byte swizzle, into a
 //                   STAGES-deep ring
@@ -43,8 +44,17 @@
 //                   buffer to the epilogue)
 //   warps 2..5      epilogue: tcgen05.ld of their TMEM lane quarter, partial
 //                   sums, SwiGLU or plain bf16 convert, global stores (warps
-//                   2..9, two per quarter, for MXFP8 pairs: their single
-//                   accumulator buffer must drain quickly)
+//                   2..9, two per quarter, for block-scaled pairs: their
+//                   single accumulator buffer must drain quickly)
+//   warps 6..9      FP4 layers, one-CTA units: scale warps, one per TMEM lane
+//                   quarter, writing each stage's scale tiles into TMEM with
+//                   tcgen05.st (elsewhere the MMA thread copies them with
+//                   tcgen05.cp before its MMAs)
+// Block-scaled operands (MX): E4M3 (MXFP8), E2M1 weights spread by the 4-bit
+// TMA type to the E4M3 image (W4), packed E2M1 tokens too (A4, kind::mxf4, 256
+// elements of K per stage) or NVFP4 (NV, kind::mxf4nvf4, E4M3 scales per 16
+// and the fp32 tensor scales applied in the epilogue); scales in 512-byte tiles
+// copied per stage into TMEM columns next to the accumulators.
 // Two accumulator buffers in TMEM let the epilogue of one range segment
 // overlap the MMAs of the next.  Every wait is bounded; a wait that runs out
 // sets the workspace error word and the kernel winds down.
