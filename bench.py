@@ -28,6 +28,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -87,11 +88,19 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source without comments, whitespace runs collapsed: what the
+    compiled kernel depends on (a comment edit keeps the counters valid)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return re.sub(r"\s+", " ", text).strip()
+
+
 def kernel_source_sha(name: str) -> str:
     h = hashlib.sha256()
     for fn in KERNEL_SOURCES.get(name, []):
-        with open(os.path.join(ROOT, "mixture_experts_layer_rmsnorm_gb300", "csrc", fn), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "mixture_experts_layer_rmsnorm_gb300", "csrc", fn), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -42,6 +42,12 @@ def test_kernel_source_sha_is_stable():
     assert a == bench.kernel_source_sha("gemm_gate_up_swiglu") and len(a) == 16
 
 
+def test_kernel_source_hash_ignores_comments_only():
+    code = "int f(int x) {\n  return x + 1;  // one\n}\n"
+    assert bench._code_only(code) == bench._code_only("/* doc */\n" + code.replace("// one", "// two\n\n"))
+    assert bench._code_only(code) != bench._code_only(code.replace("x + 1", "x + 2"))
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
