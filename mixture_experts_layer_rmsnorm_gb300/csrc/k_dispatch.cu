@@ -15,6 +15,7 @@
 #include <cuda_bf16.h>
 
 #include "align_core.cuh"
+#include "launch_config.cuh"
 #include "moe_kernels.cuh"
 #include "pdl.cuh"
 #include "topk.cuh"
@@ -22,7 +23,6 @@
 namespace moe {
 namespace {
 
-constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
 
@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kAlignThreads)
   int* ids_s = wbase + kAlignWarps * E;  // [N], fused form only
   __shared__ int scan_tmp[3 * 33];
   __shared__ int bad;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   pdl_wait();
   pdl_launch_dependents();
   for (int i = tid; i < n_flags; i += kAlignThreads) flags[i] = 0;
@@ -172,15 +172,11 @@ cudaError_t launch_align_t(const float* logits, int T, int k, int renorm, int32_
                            int32_t* sorted_ids, int32_t* slot_of, int32_t* unit_off1, int32_t* unit_off2,
                            int32_t* err, int32_t* flags, int n_flags, cudaStream_t stream) {
   const size_t smem = (static_cast<size_t>(2 + kAlignWarps) * E + (VPL > 0 ? N : 0)) * sizeof(int);
-  static int configured_device = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(align_kernel<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
+  static PerDevice config;
+  const cudaError_t e = config.get([](int&) {
+    return cudaFuncSetAttribute(align_kernel<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+  });
+  if (e != cudaSuccess) return e;
   return launch_pdl(align_kernel<VPL>, dim3(1), dim3(kAlignThreads), smem, stream, logits, T, k, renorm, topk_w,
                     topk_ids, N, E, pad, bn1, tiles1, bn2, tiles2, counts, offsets, sorted_ids, slot_of, unit_off1,
                     unit_off2, err, flags, n_flags);

@@ -71,6 +71,7 @@
 // size, which leaves room for a 7-deep ring.
 #include <cuda_bf16.h>
 
+#include "launch_config.cuh"
 #include "moe_kernels.cuh"
 #include "bounded_wait.cuh"
 #include "pdl.cuh"
@@ -907,11 +908,7 @@ cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, con
   static const CUtensorMap kNoMap = {};  // the scale maps of MXFP8 pairs; unused elsewhere
   using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV>;
   auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV>;
-  static int configured_device = -1;
-  static int max_pairs = 0;  // CTA pairs that fit on the configured device at once
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  static PerDevice config;  // the smem attribute, and the CTA pairs that fit on the device at once
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
@@ -923,21 +920,25 @@ cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, con
   attr[1].val.clusterDim.x = PAIR ? 2 : 1;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
-    if (e != cudaSuccess) return e;
-    if (PAIR) {
-      cfg.gridDim = dim3(2 * (kMaxGemmCtas / 2));
-      cfg.attrs = attr + 1;
-      cfg.numAttrs = 1;
-      int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
-      if (e != cudaSuccess) return e;
-      if (n <= 0) return cudaErrorInvalidConfiguration;
-      max_pairs = n;
-    }
-    configured_device = dev;
-  }
+  int max_pairs = 0;
+  cudaError_t e = config.get(
+      [&](int& pairs) -> cudaError_t {
+        cudaError_t ce =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
+        if (ce != cudaSuccess || !PAIR) return ce;
+        cudaLaunchConfig_t q = cfg;
+        q.gridDim = dim3(2 * (kMaxGemmCtas / 2));
+        q.attrs = attr + 1;
+        q.numAttrs = 1;
+        int n = 0;
+        ce = cudaOccupancyMaxActiveClusters(&n, kernel, &q);
+        if (ce != cudaSuccess) return ce;
+        if (n <= 0) return cudaErrorInvalidConfiguration;
+        pairs = n;
+        return cudaSuccess;
+      },
+      &max_pairs);
+  if (e != cudaSuccess) return e;
   int grid;
   if (PAIR) {
     const int pairs = max_pairs < kMaxGemmCtas / 2 ? max_pairs : kMaxGemmCtas / 2;

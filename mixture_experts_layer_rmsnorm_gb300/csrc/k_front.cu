@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 
 #include "align_core.cuh"
+#include "launch_config.cuh"
 #include "moe_kernels.cuh"
 #include "pdl.cuh"
 #include "route_tile.cuh"
@@ -161,37 +162,36 @@ struct FrontLauncher {
   // Cluster size to use on the current device (16 when the device allows a
   // non-portable cluster of 16 of these CTAs, else 8), 0 if none fits.
   static int cluster_size() {
-    static int dev_done = -1;
-    static int size = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev_done == dev) return size;
-    auto kernel = front_kernel<TT, TE, VPL>;
-    size = 0;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFrontMaxSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return 0;
-    for (int want : {16, 8}) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(want);
-      cfg.blockDim = dim3(kFrontThreads);
-      cfg.dynamicSmemBytes = kFrontMaxSmem;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = want;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n >= 1) {
-        size = want;
-        break;
+    static PerDevice config;  // the attributes and the cluster size, once per device
+    int size = 0;
+    const cudaError_t e = config.get([](int& found) -> cudaError_t {
+      auto kernel = front_kernel<TT, TE, VPL>;
+      found = 0;
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFrontMaxSmem) != cudaSuccess ||
+          cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return cudaErrorNotSupported;
+      for (int want : {16, 8}) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(want);
+        cfg.blockDim = dim3(kFrontThreads);
+        cfg.dynamicSmemBytes = kFrontMaxSmem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = want;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n >= 1) {
+          found = want;
+          return cudaSuccess;
+        }
+        cudaGetLastError();  // a refused size leaves no sticky error
       }
-      cudaGetLastError();  // a refused size leaves no sticky error
-    }
-    dev_done = dev;
-    return size;
+      return cudaSuccess;  // no size fits: 0
+    }, &size);
+    return e == cudaSuccess ? size : 0;
   }
   static cudaError_t launch(FrontArgs a, cudaStream_t stream) {
     const int C = cluster_size();

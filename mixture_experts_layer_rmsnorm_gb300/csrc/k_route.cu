@@ -19,6 +19,7 @@
 #include <cfloat>
 #include <climits>
 
+#include "launch_config.cuh"
 #include "moe_kernels.cuh"
 #include "pdl.cuh"
 #include "route_tile.cuh"
@@ -51,15 +52,11 @@ template <int TT, int TE>
 cudaError_t launch_nr(const uint16_t* x, const uint16_t* g, const float* wr, const float* bias, int T, int H, int E,
                       float eps, uint16_t* h, float* logits, int32_t* err, int num_sms, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(TT) * H * 2;
-  static int configured_device = -1;  // attribute is per device; re-set when the device changes
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured_device != dev) {
-    cudaError_t e = cudaFuncSetAttribute(norm_router_kernel<TT, TE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         200 * 1024);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
+  static PerDevice config;  // the attribute is per device
+  const cudaError_t ce = config.get([](int&) {
+    return cudaFuncSetAttribute(norm_router_kernel<TT, TE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  });
+  if (ce != cudaSuccess) return ce;
   const int tiles = (T + TT - 1) / TT;
   const int group = rt::kRouteWarps * TE;
   // fewer token tiles than SMs: one expert group per CTA spreads the work
