@@ -221,3 +221,44 @@ def test_mxfp4a4_rejects_h_not_multiple_of_256():
     with pytest.raises(binding.MoeError) as ei:
         L.forward_mxfp4(gu.dev_bf16(li.x), fp4_tokens=True)
     assert ei.value.status == binding.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("span", [(-4, 4), (-120, 120), (-30, -20)])
+def test_nvfp4_weight_quantizer_extreme_ranges(o, span):
+    """NVFP4 weights whose rows span 2^lo .. 2^hi: one tensor scale for the
+    matrix sends the small rows' block scales to 0 (codes 0) or into E4M3's
+    subnormals; codes, block scales and the tensor scale bit for bit with the
+    oracle's fp32 decisions."""
+    lo, hi = span
+    rng = np.random.default_rng(hi - lo)
+    E, H, I = 2, 256, 256
+    w13 = rng.standard_normal((E, 2 * I, H)) * np.exp2(rng.uniform(lo, hi, (E, 2 * I, 1)))
+    w2 = rng.standard_normal((E, H, I)) * np.exp2(rng.uniform(lo, hi, (E, H, 1)))
+    w13[0, 3, :16] = 0.0  # an all-zero block
+    w13[1, 5, :] *= -1.0
+    w13[1, 7, 16:32] = [6, 3, 1.5, -0.5, 0, -0.0, 4, 2, 1, 0.75, 0.25, 5, -6, 7, 2.5, 3.5]  # ties and signs
+    b13 = torch.tensor(w13).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    b2 = torch.tensor(w2).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    s_ = binding.shape(1, H, I, E, 1)
+    st, (n13c, n13s, n2c, n2s) = binding.moe_nvfp4_weight_sizes(s_)
+    dev = lambda a: torch.from_numpy(a.view(np.int16)).cuda()
+    u8 = lambda n: torch.empty(n, dtype=torch.uint8, device="cuda")
+    c13, sc13, c2, sc2 = u8(n13c), u8(n13s), u8(n2c), u8(n2s)
+    g13 = torch.empty(E, dtype=torch.float32, device="cuda")
+    g2 = torch.empty(E, dtype=torch.float32, device="cuda")
+    d13, d2 = dev(b13), dev(b2)  # held until the asynchronous quantize has run
+    st = binding.moe_nvfp4_quantize_weights(s_, d13.data_ptr(), d2.data_ptr(), c13.data_ptr(),
+                                            sc13.data_ptr(), g13.data_ptr(), c2.data_ptr(), sc2.data_ptr(),
+                                            g2.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == binding.MOE_OK
+    torch.cuda.synchronize()
+    oc13, os13, og13 = o.nv4_quantize_experts(b13)
+    oc2, os2, og2 = o.nv4_quantize_experts(b2)
+    assert np.array_equal(g13.cpu().numpy(), og13) and np.array_equal(g2.cpu().numpy(), og2)
+    assert np.array_equal(unpack_e2m1(c13.cpu().numpy(), (E, 2 * I, H)), oc13)
+    assert np.array_equal(unpack_e2m1(c2.cpu().numpy(), (E, H, I)), oc2)
+    s13 = gu.ungroup_mx_scales(sc13.cpu().numpy(), E * 2 * I, 2 * H)[gu.w13_scale_rows(E, I)]
+    assert np.array_equal(s13.reshape(E, 2 * I, H // 16), os13)
+    assert np.array_equal(gu.ungroup_mx_scales(sc2.cpu().numpy(), E * H, 2 * I).reshape(E, H, I // 16), os2)
+    if hi - lo > 100:
+        assert (os13 == 0).sum() > 0, "some blocks' scales should underflow to 0 under one tensor scale"
