@@ -336,8 +336,9 @@ MOE_API moe_status moe_workspace_size_mx(const moe_shape* shape, size_t* bytes);
  * combine as moe_forward; each expert's input rows (the bf16 h) and its bf16
  * SwiGLU activations are quantized to MXFP8 the same way and the two expert
  * GEMMs run on the block-scaled tensor cores (tcgen05.mma kind::mxf8f6f4,
- * fp32 accumulation), one CTA per work unit of 32, 64 or 128 token rows (by
- * T * top_k / E as for moe_forward's tile plans).  Expert lists are padded to
+ * fp32 accumulation), in work units of 32 token rows (T * top_k / E <= 16)
+ * or else 128, or 256 on CTA pairs where an expert's weight tiles come in
+ * pairs (the tile plans of moe_forward).  Expert lists are padded to
  * 32 rows.  E <= 256 (else MOE_ERR_UNSUPPORTED).  events: NULL
  * or as for moe_forward_events (events[1] ends routing and align, events[4]
  * the gather + quantize, events[6] the activation quantize + down GEMM). */

@@ -952,25 +952,30 @@ cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, con
   return cudaLaunchKernelEx(&cfg, kernel, tw, tx, tsw ? *tsw : kNoMap, tsx ? *tsx : kNoMap, a);
 }
 
-// Three tile plans by the expected tokens per expert (T*top_k/E):
-//   small (<= 16): 32-token units, deep weight pipelines (decode);
-//   mid   (<= 64): 64-token units, so most experts still fit one chunk;
-//   large (> 64) : 256-token units and 64-row token boxes (prefill), on CTA
-//                  pairs (M = 256 MMAs, each CTA loads half of the token tile)
-//                  when the expert's weight tiles come in pairs.
-constexpr int kGateUpBn[3] = {32, 64, 256}, kGateUpStages[3] = {10, 8, 4};  // stages of 20 / 24 / 48 KB
-constexpr int kDownBn[3] = {32, 64, 256}, kDownStages[3] = {10, 8, 4};      // stages of 20 / 24 / 48 KB
+// Two tile plans by the expected tokens per expert (T*top_k/E):
+//   small (<= 16): 32-token units, deep weight pipelines, stream-K (decode);
+//   large (> 16) : units of up to 256 tokens (the MMA's N follows the chunk's
+//                  rows) and 128-row token boxes, on CTA pairs (M = 256 MMAs,
+//                  each CTA loads half of the token tile) when the expert's
+//                  weight tiles come in pairs.
+// Between 16 and 64 rows per expert a one-CTA plan of 64-token units was
+// slower than the large plan except under uniform routing at 32 rows per
+// expert (by 1-2%): 17% slower under skewed routing, where the hot experts'
+// weight tiles were streamed once per 64-token chunk, and 36% slower at 64
+// rows per expert.
+constexpr int kGateUpBn[2] = {32, 256}, kGateUpStages[2] = {10, 4};  // stages of 20 / 48 KB
+constexpr int kDownBn[2] = {32, 256}, kDownStages[2] = {10, 4};      // stages of 20 / 48 KB
 constexpr int kPairStages[2] = {7, 7};  // gate/up, down: stages of 32 KB
 // token rows per TMA box: small units hold few tokens (16-row boxes waste
 // nothing); large units hold up to 256 (128-row boxes: 8x fewer TMA requests)
-constexpr int kTokBox[3] = {16, 16, 128};
+constexpr int kTokBox[2] = {16, 128};
 
-// MXFP8 plans: one CTA per unit of 32 tokens (10 stages of 22 KB), 64 tokens
-// (8 of 26 KB) or, in prefill, 128 tokens (6 of 33 KB; TMEM: two 128-column
+// MXFP8 plans: one CTA per unit of 32 tokens (10 stages of 22 KB) or, in
+// the large plan, 128 tokens (6 of 33 KB; TMEM: two 128-column
 // accumulators + 6 x 32 scale columns); prefill on CTA pairs when the weight
 // tiles come in pairs: 256-token units, 6 stages of 34 KB per CTA (one
 // 256-column accumulator + 6 x 32 scale columns)
-constexpr int kMxBn[3] = {32, 64, 128}, kMxStages[3] = {10, 8, 6};
+constexpr int kMxBn[2] = {32, 128}, kMxStages[2] = {10, 6};
 constexpr int kMxPairBn = 256;                              // tokens per pair unit (128: two accumulators)
 constexpr int kMxPairStages = kMxPairBn == 256 ? 6 : 8;     // 34 KB / 25 KB stages per CTA
 constexpr int kMxPairTokBox = kMxPairBn / 2;                // each CTA loads half of the unit's tokens
@@ -984,21 +989,18 @@ cudaError_t launch_mx(const CUtensorMap& tw, const CUtensorMap& tx, const CUtens
     case GemmPlan::kSmall:
       return launch_expert_gemm<SWIGLU, kMxBn[0], kMxStages[0], kTokBox[0], false, true, W4, A4>(tw, tx, a,
                                                                                                 num_sms, stream);
-    case GemmPlan::kMid:
-      return launch_expert_gemm<SWIGLU, kMxBn[1], kMxStages[1], kTokBox[1], false, true, W4, A4>(tw, tx, a,
-                                                                                                num_sms, stream);
     default:
       if (a.pair)
         return launch_expert_gemm<SWIGLU, kMxPairBn, kMxPairStages, kMxPairTokBox, true, true, W4, A4>(
             tw, tx, a, num_sms, stream, &tsw, &tsx);
-      return launch_expert_gemm<SWIGLU, kMxBn[2], kMxStages[2], kTokBox[2], false, true, W4, A4>(tw, tx, a,
+      return launch_expert_gemm<SWIGLU, kMxBn[1], kMxStages[1], kTokBox[1], false, true, W4, A4>(tw, tx, a,
                                                                                                 num_sms, stream);
   }
 }
 
-// NVFP4 plans: one CTA per unit of 32 / 64 / 128 tokens, 9 / 7 / 6 stages of
-// 24 / 28 / 36 KB (4 KB of scale tiles per stage)
-constexpr int kNvStages[3] = {9, 7, 6};
+// NVFP4 plans: one CTA per unit of 32 / 128 tokens, 9 / 6 stages of 24 / 36 KB
+// (4 KB of scale tiles per stage)
+constexpr int kNvStages[2] = {9, 6};
 
 template <bool SWIGLU>
 cudaError_t launch_nv(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, GemmPlan plan,
@@ -1007,11 +1009,8 @@ cudaError_t launch_nv(const CUtensorMap& tw, const CUtensorMap& tx, const Expert
     case GemmPlan::kSmall:
       return launch_expert_gemm<SWIGLU, kMxBn[0], kNvStages[0], kTokBox[0], false, true, true, true, true>(
           tw, tx, a, num_sms, stream);
-    case GemmPlan::kMid:
-      return launch_expert_gemm<SWIGLU, kMxBn[1], kNvStages[1], kTokBox[1], false, true, true, true, true>(
-          tw, tx, a, num_sms, stream);
     default:
-      return launch_expert_gemm<SWIGLU, kMxBn[2], kNvStages[2], kTokBox[2], false, true, true, true, true>(
+      return launch_expert_gemm<SWIGLU, kMxBn[1], kNvStages[1], kTokBox[1], false, true, true, true, true>(
           tw, tx, a, num_sms, stream);
   }
 }
@@ -1056,6 +1055,13 @@ int gemm_down_bn(GemmPlan plan) { return kDownBn[static_cast<int>(plan)]; }
 int gemm_tok_box_rows(GemmPlan plan) { return kTokBox[static_cast<int>(plan)]; }
 bool gemm_uses_pairs(GemmPlan plan, int tiles) { return plan == GemmPlan::kLarge && tiles % 2 == 0; }
 int gemm_unit_tiles(GemmPlan plan, int tiles) { return gemm_uses_pairs(plan, tiles) ? tiles / 2 : tiles; }
+// The block-scaled layers take CTA pairs only above 64 rows per expert: with
+// thinner token chunks the per-stage scale copies of a pair's MMA thread, not
+// the weight stream, set the pace (the MXFP4 layer at 32 rows per expert: 19%
+// slower on pairs than on one-CTA units).
+bool gemm_uses_pairs_mx(GemmPlan plan, int tiles, int64_t T, int64_t top_k, int64_t E) {
+  return gemm_uses_pairs(plan, tiles) && T * top_k > 64 * E;
+}
 
 cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
                                 GemmPlan plan, int num_sms, cudaStream_t stream) {
@@ -1063,14 +1069,11 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm
     case GemmPlan::kSmall:
       return launch_expert_gemm<true, kGateUpBn[0], kGateUpStages[0], kTokBox[0], false>(tm_w13, tm_x, a, num_sms,
                                                                                           stream);
-    case GemmPlan::kMid:
-      return launch_expert_gemm<true, kGateUpBn[1], kGateUpStages[1], kTokBox[1], false>(tm_w13, tm_x, a, num_sms,
-                                                                                          stream);
     default:
       if (a.pair)
-        return launch_expert_gemm<true, kGateUpBn[2], kPairStages[0], kTokBox[2], true>(tm_w13, tm_x, a, num_sms,
+        return launch_expert_gemm<true, kGateUpBn[1], kPairStages[0], kTokBox[1], true>(tm_w13, tm_x, a, num_sms,
                                                                                       stream);
-      return launch_expert_gemm<true, kGateUpBn[2], kGateUpStages[2], kTokBox[2], false>(tm_w13, tm_x, a, num_sms,
+      return launch_expert_gemm<true, kGateUpBn[1], kGateUpStages[1], kTokBox[1], false>(tm_w13, tm_x, a, num_sms,
                                                                                           stream);
   }
 }
@@ -1081,14 +1084,11 @@ cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act
     case GemmPlan::kSmall:
       return launch_expert_gemm<false, kDownBn[0], kDownStages[0], kTokBox[0], false>(tm_w2, tm_act, a, num_sms,
                                                                                        stream);
-    case GemmPlan::kMid:
-      return launch_expert_gemm<false, kDownBn[1], kDownStages[1], kTokBox[1], false>(tm_w2, tm_act, a, num_sms,
-                                                                                       stream);
     default:
       if (a.pair)
-        return launch_expert_gemm<false, kDownBn[2], kPairStages[1], kTokBox[2], true>(tm_w2, tm_act, a, num_sms,
+        return launch_expert_gemm<false, kDownBn[1], kPairStages[1], kTokBox[1], true>(tm_w2, tm_act, a, num_sms,
                                                                                      stream);
-      return launch_expert_gemm<false, kDownBn[2], kDownStages[2], kTokBox[2], false>(tm_w2, tm_act, a, num_sms,
+      return launch_expert_gemm<false, kDownBn[1], kDownStages[1], kTokBox[1], false>(tm_w2, tm_act, a, num_sms,
                                                                                        stream);
   }
 }

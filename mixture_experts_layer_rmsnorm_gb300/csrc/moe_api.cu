@@ -541,9 +541,10 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   if (num_sms <= 0) return MOE_ERR_CUDA;
   const Layout L = make_layout(s, true);
   const int tiles1 = s.I / moe::kGateUpTileFeat, tiles2 = s.H / moe::kDownTileFeat;
-  // prefill: CTA pairs where the weight tiles come in pairs (256-token units)
+  // dense prefill: CTA pairs where the weight tiles come in pairs (256-token units)
   // (NVFP4: one CTA per unit in every plan; its scale tiles take the TMEM a pair's accumulator needs)
-  const bool pair1 = !nv && moe::gemm_uses_pairs(plan, tiles1), pair2 = !nv && moe::gemm_uses_pairs(plan, tiles2);
+  const bool pair1 = !nv && moe::gemm_uses_pairs_mx(plan, tiles1, s.T, s.top_k, s.E);
+  const bool pair2 = !nv && moe::gemm_uses_pairs_mx(plan, tiles2, s.T, s.top_k, s.E);
   const int bn1 = moe::gemm_bn_mx(plan, pair1), bn2 = moe::gemm_bn_mx(plan, pair2);
   const int utiles1 = pair1 ? tiles1 / 2 : tiles1, utiles2 = pair2 ? tiles2 / 2 : tiles2;
   auto mark = [&](int i) {
@@ -779,8 +780,9 @@ moe_status moe_workspace_views_mx(const moe_shape* shape, void* workspace, size_
   mv->act_scales = at<void>(workspace, L.as);
   const moe_shape& s = *shape;
   const GemmPlan plan = moe::choose_plan(s.T, s.top_k, s.E);
-  mv->x_chunk_rows = moe::gemm_bn_mx(plan, moe::gemm_uses_pairs(plan, s.I / moe::kGateUpTileFeat));
-  mv->act_chunk_rows = moe::gemm_bn_mx(plan, moe::gemm_uses_pairs(plan, s.H / moe::kDownTileFeat));
+  const int tiles1 = s.I / moe::kGateUpTileFeat, tiles2 = s.H / moe::kDownTileFeat;
+  mv->x_chunk_rows = moe::gemm_bn_mx(plan, moe::gemm_uses_pairs_mx(plan, tiles1, s.T, s.top_k, s.E));
+  mv->act_chunk_rows = moe::gemm_bn_mx(plan, moe::gemm_uses_pairs_mx(plan, tiles2, s.T, s.top_k, s.E));
   mv->x_gscale = at<void>(workspace, L.gx);
   mv->act_gscale = at<void>(workspace, L.ga);
   mv->nv_chunk_rows = moe::gemm_bn_mx(plan, false);

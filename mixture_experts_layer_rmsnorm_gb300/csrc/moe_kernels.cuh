@@ -135,12 +135,9 @@ struct ExpertGemmArgs {
 constexpr int kMaxGemmCtas = 256;
 
 // tile plan of the expert GEMMs, by the expected tokens per expert
-enum class GemmPlan { kSmall = 0, kMid = 1, kLarge = 2 };
+enum class GemmPlan { kSmall = 0, kLarge = 1 };
 inline GemmPlan choose_plan(int64_t T, int64_t top_k, int64_t E) {
-  const int64_t tk = T * top_k;
-  if (tk <= 16 * E) return GemmPlan::kSmall;
-  if (tk <= 64 * E) return GemmPlan::kMid;
-  return GemmPlan::kLarge;
+  return T * top_k <= 16 * E ? GemmPlan::kSmall : GemmPlan::kLarge;
 }
 
 // Encodes nothing itself: the tensor maps are built by the caller.
@@ -152,6 +149,7 @@ cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act
 // the tiles per expert its work-unit table counts (pairs of tiles then).
 bool gemm_uses_pairs(GemmPlan plan, int tiles);
 int gemm_unit_tiles(GemmPlan plan, int tiles);
+bool gemm_uses_pairs_mx(GemmPlan plan, int tiles, int64_t T, int64_t top_k, int64_t E);  // block-scaled layers
 // The same GEMMs on MXFP8 operands (block-scaled tcgen05 MMA):
 // gemm_bn_mx(plan, a.pair) tokens per unit, on CTA pairs in the large plan when
 // a.pair is set (weight tiles in pairs).  tm_sw / tm_sx map the weight and

@@ -33,7 +33,7 @@ CASES = [
     ("prefill_pairs_ragged", 700, 512, 384, 5, 2, True, None, 10),
     ("prefill_skewed", 512, 256, 256, 16, 4, True, 1.2, 11),
     ("skewed_bias", 96, 256, 256, 32, 6, True, 1.2, 7),
-    ("mid_multichunk", 200, 256, 256, 8, 2, True, None, 9),
+    ("multichunk_50_per_expert", 200, 256, 256, 8, 2, True, None, 9),
     ("single_expert", 20, 128, 128, 1, 1, True, None, 6),
     ("k_equals_E", 9, 128, 256, 4, 4, True, None, 8),
 ]

@@ -23,7 +23,7 @@ CASES = [
     ("mx_tiny", 4, 128, 256, 8, 2, True, None, 0),
     ("mx_T1", 1, 256, 256, 16, 4, True, None, 3),
     ("mx_ragged_decode", 37, 256, 384, 16, 4, True, None, 1),
-    ("mx_mid_multichunk", 200, 256, 256, 8, 2, True, None, 9),
+    ("mx_multichunk_50_per_expert", 200, 256, 256, 8, 2, True, None, 9),
     ("mx_bias_norenorm", 3, 384, 256, 20, 5, False, 1.2, 14),
     ("mx_deep_k", 64, 1024, 512, 8, 2, True, None, 2),
     # prefill plan: 128-token units, several chunks per expert, ragged tails
@@ -118,11 +118,10 @@ def test_mx_layer_parity(case, fmt, o):
     gu.check_routing(o, li, li.x, g, pad=32)
     # gathered token rows: codes and scales bit for bit on the real rows; the
     # scales are grouped by the GEMMs' token chunks (bn rows of an expert)
-    # the gate/up GEMM's token rows per unit (its scale chunks): 32 / 64 by
+    # the gate/up GEMM's token rows per unit (its scale chunks): 32 in the
     # decode plan, 128 or 256 in prefill; a chunk's scales take ceil(bn / 128) tiles
     bn = mv.nv_chunk_rows if nv else mv.x_chunk_rows
-    small_mid = 32 if T * k <= 16 * E else 64 if T * k <= 64 * E else None
-    assert bn == small_mid if small_mid else bn in ((128,) if nv else (128, 256))
+    assert bn == 32 if T * k <= 16 * E else bn in ((128,) if nv else (128, 256))
     G = -(-bn // 128)
     n_groups = (1 if nv else 2) * (v.P_max // 32)
     if a4:  # E2M1 token codes, two per byte
