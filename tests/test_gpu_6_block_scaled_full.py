@@ -1,7 +1,9 @@
 """GPU parity of the block-scaled layers at the decode and prefill workloads'
-full sizes (H = I = 4096, E = 64, top_k = 8; T = 8 and T = 4096), in the launch
-configuration the benchmark times: the MXFP8 layer, MXFP4 weights with MXFP8
-tokens, the MXFP4 layer and the NVFP4 layer.
+full sizes (H = I = 4096, E = 64, top_k = 8; T = 8 and T = 4096) and at the
+fine-grained workload's T = 1024 (H = 7168, I = 2048, E = 256, top_k = 8: 32
+rows per expert, one-CTA 128-token units), in the launch configuration the
+benchmark times: the MXFP8 layer, MXFP4 weights with MXFP8 tokens, the MXFP4
+layer and the NVFP4 layer.
 
 The outputs of sampled tokens are compared with the oracle's layer of the same
 format within the layer tolerance.  The oracle quantizes only the weights of
@@ -34,10 +36,7 @@ def layer():
     cfg = inputs.WORKLOADS["prefill_T4096"]  # decode and prefill share the layer's weights
     li = inputs.make_layer_inputs(inputs.LayerConfig(T=1, H=cfg.H, I=cfg.I, E=cfg.E, top_k=cfg.top_k, seed=cfg.seed))
     dl = gu.DeviceLayer(li, max_tokens=4096)
-    dl.layer.quantize_mx()
-    dl.layer.quantize_mxfp4()
-    dl.layer.quantize_nvfp4()
-    torch.cuda.synchronize()
+    _quantize_all(dl)
     yield dl
     del dl
     gc.collect()
@@ -91,9 +90,43 @@ class OracleWeights:
 _cache = {}
 
 
+def _quantize_all(dl):
+    dl.layer.quantize_mx()
+    dl.layer.quantize_mxfp4()
+    dl.layer.quantize_nvfp4()
+    torch.cuda.synchronize()
+
+
+@pytest.fixture(scope="module")
+def finegrained_layer():
+    cfg = inputs.WORKLOADS["finegrained_T1024"]
+    li = inputs.make_layer_inputs(inputs.LayerConfig(T=1, H=cfg.H, I=cfg.I, E=cfg.E, top_k=cfg.top_k, seed=cfg.seed))
+    dl = gu.DeviceLayer(li, max_tokens=1024)
+    _quantize_all(dl)
+    yield dl
+    del dl
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("T", [8, 4096])
 @pytest.mark.parametrize("fmt", FORMATS)
 def test_block_scaled_full(layer, o, fmt, T):
+    if fmt not in _cache:
+        _cache[fmt] = OracleWeights(o, layer.li, fmt)
+    _check(layer, o, fmt, T, _cache[fmt])
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_block_scaled_finegrained(finegrained_layer, o, fmt):
+    # the oracle's weight copies of this layer (11 GB per format) are not kept,
+    # nor those of the decode/prefill layer from here on
+    _cache.clear()
+    _check(finegrained_layer, o, fmt, 1024, OracleWeights(o, finegrained_layer.li, fmt))
+    gc.collect()
+
+
+def _check(layer, o, fmt, T, ow):
     li = layer.li
     cfg = inputs.LayerConfig(T=T, H=li.cfg.H, I=li.cfg.I, E=li.cfg.E, top_k=li.cfg.top_k, seed=li.cfg.seed)
     x = inputs.make_tokens(cfg)
@@ -113,9 +146,6 @@ def test_block_scaled_full(layer, o, fmt, T):
     # the experts the oracle's own routing gives the sampled tokens
     _, logits, _ = o.route_f32(x[sample], li.g, li.cfg.eps, li.w_router, li.bias)
     experts = np.unique(o.topk(logits, li.cfg.top_k))
-    if fmt not in _cache:
-        _cache[fmt] = OracleWeights(o, li, fmt)
-    ow = _cache[fmt]
     ow.ensure(experts)
     r = ow.forward(x, sample)
     assert set(np.unique(r["ids"]).tolist()) <= ow.done
