@@ -631,6 +631,10 @@ def run_ours(args, wl, world, rank, local):
            "h2d_bytes_per_step": sum(T * H * 2 for T in Ts), "d2h_bytes_per_step": sum(T * H * 2 for T in Ts),
            "ms_per_step": round(e2e_ms_step, 4)}
 
+    prefill = None
+    if args.workload == "decode" and not args.no_prefill and not ff:
+        prefill = prefill_section(args, wl, layer, fwd, flush_l2, stream, gpu_index, world, d16, mx)
+
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
@@ -668,7 +672,97 @@ def run_ours(args, wl, world, rank, local):
         "gpu_launches": sum(args.steps * kpc(T) for T in Ts),
         "clocks": clocks,
     }
+    if prefill is not None:
+        out["prefill"] = prefill
     return out, host
+
+
+PREFILL_T = 4096
+PREFILL_MIN_TIMED_S = 2.5  # long enough for >= 10 clock samples at 200 ms
+
+
+def prefill_section(args, wl, layer, fwd, flush_l2, stream, gpu_index, world, d16, mx):
+    """The prefill configuration (T = 4096 on the decode layer's weights: the
+    same H, I, E, top_k and seed) through the same entry point: flushed calls
+    timed with CUDA events on the launch stream, repeated until the timed
+    region lasts at least PREFILL_MIN_TIMED_S (clock samples during it), then
+    a per-kernel pass of `steps` calls; the gate/up GEMM's tensor roofline."""
+    import numpy as np
+    import torch
+    from mixture_experts_layer_rmsnorm_gb300 import accounting, binding, inputs
+
+    T, H, I, E, k = PREFILL_T, wl["H"], wl["I"], wl["E"], wl["k"]
+    cfg = inputs.LayerConfig(T=T, H=H, I=I, E=E, top_k=k, seed=wl["seed"], zipf_bias=wl["zipf"])
+    x = d16(inputs.make_tokens(cfg))
+    y = torch.empty((T, H), dtype=torch.int16, device=x.device)
+    for _ in range(args.warmup):
+        flush_l2(0)
+        fwd(x, y)
+    torch.cuda.synchronize()
+    st, det = layer.device_status(T)
+    if st != binding.MOE_OK:
+        raise binding.MoeError(st, f"device status after prefill warm-up (detail {det})")
+    ids = layer.view_tensor(T, "topk_ids", torch.int32, (T, k)).cpu().numpy()
+    touched = accounting.n_touched(ids, E)
+    # one flushed call's time sets how many calls fill the timed region
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush_l2(1)
+    a.record(stream)
+    fwd(x, y)
+    b.record(stream)
+    torch.cuda.synchronize()
+    est_s = a.elapsed_time(b) * 1e-3 + 2e-4  # + the flush
+    n_calls = max(args.steps, int(PREFILL_MIN_TIMED_S / est_s) + 1)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_calls)]
+    sampler = ClockSampler(gpu_index)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    for i in range(n_calls):
+        flush_l2(i)
+        evs[i][0].record(stream)
+        fwd(x, y)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    calls = [e0.elapsed_time(e1) for e0, e1 in evs]
+    nk = binding.MOE_NUM_KERNELS
+    kern = {n: [] for n in binding.KERNEL_NAMES}
+    for i in range(args.steps):
+        ke = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+        for e in ke:
+            e.record(stream)
+        flush_l2(i)
+        fwd(x, y, events=[e.cuda_event for e in ke])
+        torch.cuda.synchronize()
+        for j, n in enumerate(binding.KERNEL_NAMES):
+            kern[n].append(ke[j].elapsed_time(ke[j + 1]))
+    torch.cuda.synchronize()
+    med_ms = statistics.median(calls)
+    ms_max = reduce_max(med_ms, world)
+    peaks, peak_kind = load_peaks()
+    fl = accounting.layer_flops(T, H, I, E, k)
+    ratio = 6.0 if mx in ("mxfp4a4", "nvfp4") else 2.0 if mx else 1.0  # MMA kind / bf16 nominal dense rate
+    peak_b, peak_s = ratio * peaks["bf16_tflops"], ratio * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    g1_ms = statistics.median(kern["gemm_gate_up_swiglu"])
+    roof = roofline("tensor", fl["gemm1"], g1_ms * 1e-3, peak_b,
+                    None if mx else ncu_traffic_per_launch("gemm_gate_up_swiglu", "prefill"))
+    roof.update({"kernel": "gemm_gate_up_swiglu", "algorithmic_per_launch": fl["gemm1"],
+                 "avg_launch_us": round(g1_ms * 1e3, 2),
+                 "peak_source": (f"{ratio:g} x " if ratio != 1.0 else "") + f"bf16_tflops ({peak_kind}, burst)",
+                 "peak_sustained": peak_s, "frac_of_sustained": round(fl["gemm1"] / (g1_ms * 1e-3) / 1e12 / peak_s, 4)})
+    layer_tf = fl["total"] / (med_ms * 1e-3) / 1e12
+    return {"workload": f"prefill T={T}, H={H}, I={I}, E={E}, top_k={k} (the decode layer's weights)",
+            "T": T, "experts_touched": touched, "calls_timed": n_calls,
+            "us_median": round(med_ms * 1e3, 2), "us_mean": round(sum(calls) / len(calls) * 1e3, 2),
+            "us_min": round(min(calls) * 1e3, 2), "tokens_per_s": round(world * T / (ms_max * 1e-3), 1),
+            "layer_tflops": round(layer_tf, 2), "layer_frac_of_peak": round(layer_tf / peak_b, 4),
+            "layer_frac_of_sustained": round(layer_tf / peak_s, 4),
+            "flops": {n: int(v) for n, v in fl.items()},
+            "kernel_us_median": {n: round(statistics.median(v) * 1e3, 2) for n, v in kern.items()},
+            "roofline": roof, "clocks": clocks,
+            "timing": "flushed calls (256 MB write + 256 MB read before each), CUDA events on the launch stream; "
+                      "kernel times from a second pass through moe_forward_events"}
 
 
 def main():
@@ -682,6 +776,8 @@ def main():
                     help="CPU oracle sample: at most this many tokens of each batch per step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum timed CPU-oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode workload: skip the prefill (T=4096) object of the JSON line")
     ap.add_argument("--nvfp4", action="store_true",
                     help="time moe_forward_nvfp4: the NVFP4 layer (NVFP4 weights, token rows and activations)")
     ap.add_argument("--mxfp4a4", action="store_true",

@@ -42,7 +42,10 @@
  *     returned by moe_device_status().
  *   - The library keeps no state between calls except per-device kernel
  *     attributes set once; it is reentrant as long as concurrent calls use
- *     different workspaces.
+ *     different workspaces.  One exception: moe_forward_static_scratch keeps
+ *     its scratch in one device array per GPU that every call of it on that
+ *     GPU shares (and caches that array's address), so its callers must
+ *     serialise their calls although they pass no workspace.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -78,10 +81,16 @@ typedef enum {
 /* Layer shape and routing options.
  *   T            tokens (>= 0; moe_forward with T = 0 returns MOE_OK at once and
  *                touches no pointer)
- *   H            hidden size, a multiple of 128, <= 16384
- *   I            expert intermediate size, a multiple of 128, <= 16384
+ *   H            hidden size, a multiple of 128 (the down GEMM's weight tile
+ *                is 128 output features), <= 16384 (the router keeps its
+ *                tokens' rows of h in shared memory)
+ *   I            expert intermediate size, a multiple of 64 (the gate/up
+ *                GEMM's unit is 64 features, the down GEMM's K block 64
+ *                elements; 128 for the block-scaled layers, whose scale tiles
+ *                cover 128 elements of K), <= 16384
  *   E            experts, 1..1024
- *   top_k        experts per token, 1..min(E, 32)
+ *   top_k        experts per token, 1..min(E, 32) (one lane of the selecting
+ *                warp per selected expert)
  *   renormalize  nonzero: the top_k weights are divided by their sum
  *   eps          RMSNorm epsilon (>= 0, finite)                              */
 typedef struct {
@@ -234,7 +243,8 @@ MOE_API moe_status moe_route_debug(const moe_shape* shape, const moe_bf16* x, co
  * for moe_forward.
  *   - Shapes whose moe_workspace_size() exceeds MOE_STATIC_SCRATCH_BYTES are
  *     rejected with MOE_ERR_WORKSPACE before anything is enqueued (e.g. the
- *     decode layer H = I = 4096, E = 64, top_k = 8 fits for T <= 129).
+ *     decode layer H = I = 4096, E = 64, top_k = 8 fits for T <= 128: at
+ *     T = 129 its tile plan changes and it needs 117 MB).
  *   - The first call on a device (with that device current) looks up the
  *     array's device address once (cudaGetSymbolAddress) and keeps it; make
  *     that first call before any stream capture.
@@ -243,10 +253,26 @@ MOE_API moe_status moe_route_debug(const moe_shape* shape, const moe_bf16* x, co
  *     has to be cleared between calls.  Calls whose work overlaps on the GPU
  *     (other streams, other host threads) race on the array: serialise them.
  *   - The intermediate tensors are not exposed (no moe_workspace_views).
+ *     Device-detected errors go to the error word at the start of the array;
+ *     moe_static_scratch_device_status() reads it.
  *   - No cudaMalloc, cudaFree or allocating library routine is called. */
 MOE_API moe_status moe_forward_static_scratch(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
                                               const float* w_router, const float* router_bias, const moe_bf16* w13,
                                               const moe_bf16* w2, moe_bf16* y, moe_stream_t stream);
+
+/* The size of that array as compiled into the library (the value of
+ * MOE_STATIC_SCRATCH_BYTES the library was built with), for bindings that
+ * cannot read the macro.  Host-only; makes no CUDA call. */
+MOE_API moe_status moe_static_scratch_bytes(size_t* bytes);
+
+/* moe_device_status for moe_forward_static_scratch: waits for `stream`, then
+ * reads the error word of the current device's static array (the one the
+ * last moe_forward_static_scratch call on this device used; it is cleared by
+ * the first kernel of every such call).  Returns MOE_OK, MOE_ERR_TIMEOUT or
+ * MOE_ERR_DEVICE as moe_device_status does; `detail` (int32[4] or NULL)
+ * receives the word.  Like the first moe_forward_static_scratch call, the
+ * first call of either on a device looks up the array's address. */
+MOE_API moe_status moe_static_scratch_device_status(moe_stream_t stream, int32_t* detail);
 
 /* Device pointers to the intermediate tensors inside a workspace, valid for
  * the shape it was sized for (layout only; makes no CUDA call). */

@@ -68,6 +68,8 @@ def load(build: bool = True):
             lib.moe_forward_events.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_route_debug.argtypes = [sp, p, p, p, p, i32, p, p, p, p, i64, p, sz, p]
             lib.moe_forward_static_scratch.argtypes = [sp, p, p, p, p, p, p, p, p]
+            lib.moe_static_scratch_bytes.argtypes = [ctypes.POINTER(sz)]
+            lib.moe_static_scratch_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_int32)]
             lib.moe_workspace_views.argtypes = [sp, p, sz, ctypes.POINTER(MoeViews)]
             lib.moe_device_status.argtypes = [p, sz, p, ctypes.POINTER(ctypes.c_int32)]
             lib.moe_kernels_per_call.argtypes = [sp, ctypes.POINTER(ctypes.c_int32)]
@@ -93,6 +95,7 @@ def load(build: bool = True):
             lib.moe_status_string.restype = ctypes.c_char_p
             for f in ("moe_workspace_size", "moe_forward", "moe_forward_events", "moe_route_debug",
                       "moe_workspace_views", "moe_device_status", "moe_forward_static_scratch",
+                      "moe_static_scratch_bytes", "moe_static_scratch_device_status",
                       "moe_kernels_per_call", "moe_kernels_per_call_of", "moe_forward_fused_front",
                       "moe_selftest_wait_timeout",
                       "moe_qk_norm", "moe_mx_weight_sizes", "moe_mx_quantize_weights", "moe_workspace_size_mx",
@@ -189,7 +192,18 @@ def moe_forward_fused_combine(s: MoeShape, x, g_norm, w_router, router_bias, w13
                                             workspace, workspace_bytes, stream, arr, n)
 
 
-MOE_STATIC_SCRATCH_BYTES = 64 << 20
+def moe_static_scratch_bytes() -> tuple[int, int]:
+    """Size of the library's fixed device scratch array, as compiled into it."""
+    n = ctypes.c_size_t(0)
+    st = load().moe_static_scratch_bytes(ctypes.byref(n))
+    return st, n.value
+
+
+def moe_static_scratch_device_status(stream) -> tuple[int, list]:
+    """moe_device_status for moe_forward_static_scratch (the current device's array)."""
+    d = (ctypes.c_int32 * 4)()
+    st = load().moe_static_scratch_device_status(stream, d)
+    return st, list(d)
 
 
 def moe_forward_static_scratch(s: MoeShape, x, g_norm, w_router, router_bias, w13, w2, y, stream) -> int:

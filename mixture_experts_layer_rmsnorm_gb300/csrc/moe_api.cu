@@ -98,13 +98,25 @@ moe_status check_shape(const moe_shape* s) {
   if (s->T < 0 || s->H <= 0 || s->I <= 0 || s->E <= 0 || s->top_k <= 0 || s->top_k > s->E)
     return MOE_ERR_INVALID_ARG;
   if (!(s->eps >= 0.0f) || !std::isfinite(s->eps)) return MOE_ERR_INVALID_ARG;
-  if (s->H % 128 != 0 || s->I % 128 != 0 || s->H > 16384 || s->I > 16384 || s->E > 1024 || s->top_k > 32)
+  // H: 128 output features per down-GEMM weight tile; I: 64 features per
+  // gate/up unit and 64 elements of K per down-GEMM stage; H <= 16384: the
+  // router keeps its tokens' h rows in shared memory; top_k <= 32: one lane
+  // of the selecting warp per selected expert
+  if (s->H % 128 != 0 || s->I % 64 != 0 || s->H > 16384 || s->I > 16384 || s->E > 1024 || s->top_k > 32)
     return MOE_ERR_UNSUPPORTED;
   // 32-bit row indices inside the kernels
   const int64_t rows = static_cast<int64_t>(s->T) * s->top_k + static_cast<int64_t>(s->E) * (kMaxDebugPad - 1);
   if (rows >= (int64_t(1) << 30)) return MOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(s->E) * 2 * s->I >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
+}
+
+// The block-scaled layers: scale tiles cover 128 elements of K (and a
+// block-scaled GEMM stage at least 128), so I must be a multiple of 128 too.
+moe_status check_shape_mx(const moe_shape* s) {
+  const moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  return s->I % 128 != 0 ? MOE_ERR_UNSUPPORTED : MOE_OK;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -520,7 +532,7 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
                            const uint8_t* w2s, moe_bf16* y, void* workspace, size_t workspace_bytes,
                            moe_stream_t stream, void* const* events, MxKind kind = MxKind::kW8A8,
                            const float* w13g = nullptr, const float* w2g = nullptr) {
-  moe_status st = check_shape(shape);
+  moe_status st = check_shape_mx(shape);
   if (st != MOE_OK) return st;
   const moe_shape& s = *shape;
   if (s.T == 0) return MOE_OK;
@@ -657,7 +669,7 @@ extern "C" {
 
 moe_status moe_mx_weight_sizes(const moe_shape* shape, size_t* w13_codes, size_t* w13_scales, size_t* w2_codes,
                                size_t* w2_scales) {
-  const moe_status st = check_shape(shape);
+  const moe_status st = check_shape_mx(shape);
   if (st != MOE_OK) return st;
   if (!w13_codes || !w13_scales || !w2_codes || !w2_scales) return MOE_ERR_INVALID_ARG;
   const int64_t E = shape->E, H = shape->H, I = shape->I;
@@ -670,7 +682,7 @@ moe_status moe_mx_weight_sizes(const moe_shape* shape, size_t* w13_codes, size_t
 
 moe_status moe_mx_quantize_weights(const moe_shape* shape, const moe_bf16* w13, const moe_bf16* w2, uint8_t* w13_codes,
                                    uint8_t* w13_scales, uint8_t* w2_codes, uint8_t* w2_scales, moe_stream_t stream) {
-  const moe_status st = check_shape(shape);
+  const moe_status st = check_shape_mx(shape);
   if (st != MOE_OK) return st;
   if (!w13 || !w2 || !w13_codes || !w13_scales || !w2_codes || !w2_scales || !aligned(w13, 16) || !aligned(w2, 16) ||
       !aligned(w13_codes, 16) || !aligned(w13_scales, 16) || !aligned(w2_codes, 16) || !aligned(w2_scales, 16))
@@ -695,7 +707,7 @@ moe_status moe_mxfp4_weight_sizes(const moe_shape* shape, size_t* w13_codes, siz
 moe_status moe_mxfp4_quantize_weights(const moe_shape* shape, const moe_bf16* w13, const moe_bf16* w2,
                                       uint8_t* w13_codes, uint8_t* w13_scales, uint8_t* w2_codes, uint8_t* w2_scales,
                                       moe_stream_t stream) {
-  const moe_status st = check_shape(shape);
+  const moe_status st = check_shape_mx(shape);
   if (st != MOE_OK) return st;
   if (!w13 || !w2 || !w13_codes || !w13_scales || !w2_codes || !w2_scales || !aligned(w13, 16) || !aligned(w2, 16) ||
       !aligned(w13_codes, 32) || !aligned(w13_scales, 16) || !aligned(w2_codes, 32) || !aligned(w2_scales, 16))
@@ -711,7 +723,7 @@ moe_status moe_mxfp4_quantize_weights(const moe_shape* shape, const moe_bf16* w1
 
 moe_status moe_nvfp4_weight_sizes(const moe_shape* shape, size_t* w13_codes, size_t* w13_scales, size_t* w2_codes,
                                   size_t* w2_scales) {
-  const moe_status st = check_shape(shape);
+  const moe_status st = check_shape_mx(shape);
   if (st != MOE_OK) return st;
   if (!w13_codes || !w13_scales || !w2_codes || !w2_scales) return MOE_ERR_INVALID_ARG;
   const int64_t E = shape->E, H = shape->H, I = shape->I;
@@ -725,7 +737,7 @@ moe_status moe_nvfp4_weight_sizes(const moe_shape* shape, size_t* w13_codes, siz
 moe_status moe_nvfp4_quantize_weights(const moe_shape* shape, const moe_bf16* w13, const moe_bf16* w2,
                                       uint8_t* w13_codes, uint8_t* w13_scales, float* w13_gscale, uint8_t* w2_codes,
                                       uint8_t* w2_scales, float* w2_gscale, moe_stream_t stream) {
-  const moe_status st = check_shape(shape);
+  const moe_status st = check_shape_mx(shape);
   if (st != MOE_OK) return st;
   if (!w13 || !w2 || !w13_codes || !w13_scales || !w13_gscale || !w2_codes || !w2_scales || !w2_gscale ||
       !aligned(w13, 16) || !aligned(w2, 16) || !aligned(w13_codes, 32) || !aligned(w13_scales, 16) ||
@@ -747,7 +759,7 @@ moe_status moe_nvfp4_quantize_weights(const moe_shape* shape, const moe_bf16* w1
 }
 
 moe_status moe_workspace_size_mx(const moe_shape* shape, size_t* bytes) {
-  const moe_status st = check_shape(shape);
+  const moe_status st = check_shape_mx(shape);
   if (st != MOE_OK) return st;
   if (!bytes) return MOE_ERR_INVALID_ARG;
   *bytes = make_layout(*shape, true).total;
@@ -756,7 +768,7 @@ moe_status moe_workspace_size_mx(const moe_shape* shape, size_t* bytes) {
 
 moe_status moe_workspace_views_mx(const moe_shape* shape, void* workspace, size_t workspace_bytes, moe_views* v,
                                   moe_mx_views* mv) {
-  const moe_status st = check_shape(shape);
+  const moe_status st = check_shape_mx(shape);
   if (st != MOE_OK) return st;
   if (!workspace || !v || !mv) return MOE_ERR_INVALID_ARG;
   const Layout L = make_layout(*shape, true);
@@ -964,7 +976,7 @@ const char* moe_status_string(moe_status status) {
   switch (status) {
     case MOE_OK: return "ok";
     case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, misaligned pointer or bad shape value)";
-    case MOE_ERR_UNSUPPORTED: return "unsupported shape (H, I multiples of 128 up to 16384; E <= 1024; top_k <= 32)";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape (H a multiple of 128, I of 64 (128 for block-scaled layers), both up to 16384; E <= 1024; top_k <= 32)";
     case MOE_ERR_WORKSPACE: return "workspace smaller than moe_workspace_size()";
     case MOE_ERR_CUDA: return "a CUDA call or kernel launch failed";
     case MOE_ERR_TIMEOUT: return "a bounded device-side wait ran out";

@@ -48,6 +48,21 @@ moe_status static_scratch_of_current_device(void** out) {
 
 }  // namespace
 
+extern "C" MOE_API moe_status moe_static_scratch_bytes(size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = static_cast<size_t>(MOE_STATIC_SCRATCH_BYTES);
+  return MOE_OK;
+}
+
+// The error word at the start of the array (the workspace layout puts it at
+// offset 0), read after the stream has finished the caller's work.
+extern "C" MOE_API moe_status moe_static_scratch_device_status(moe_stream_t stream, int32_t* detail) {
+  void* scratch = nullptr;
+  const moe_status st = static_scratch_of_current_device(&scratch);
+  if (st != MOE_OK) return st;
+  return moe_device_status(scratch, MOE_STATIC_SCRATCH_BYTES, stream, detail);
+}
+
 extern "C" MOE_API moe_status moe_forward_static_scratch(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
                                                  const float* w_router, const float* router_bias,
                                                  const moe_bf16* w13, const moe_bf16* w2, moe_bf16* y,

@@ -35,7 +35,7 @@ def test_workspace_size_and_shape_checks():
     assert st == binding.MOE_OK and n > 3 * 33728 * 4096 * 2
     bad = [
         (binding.shape(4, 100, 256, 8, 2), binding.MOE_ERR_UNSUPPORTED),   # H not a multiple of 128
-        (binding.shape(4, 128, 200, 8, 2), binding.MOE_ERR_UNSUPPORTED),   # I not a multiple of 128
+        (binding.shape(4, 128, 200, 8, 2), binding.MOE_ERR_UNSUPPORTED),   # I not a multiple of 64
         (binding.shape(4, 128, 256, 8, 9), binding.MOE_ERR_INVALID_ARG),   # top_k > E
         (binding.shape(4, 128, 256, 2048, 2), binding.MOE_ERR_UNSUPPORTED),  # E > 1024
         (binding.shape(4, 128, 256, 64, 33), binding.MOE_ERR_UNSUPPORTED),  # top_k > 32
@@ -46,6 +46,43 @@ def test_workspace_size_and_shape_checks():
     for s, want in bad:
         st, _ = binding.moe_workspace_size(s)
         assert st == want, (s.H, s.I, s.E, s.top_k, st)
+
+
+def test_shape_rule_at_its_edges():
+    """The supported shapes: H a multiple of 128 (the down GEMM's 128-feature
+    weight tile) up to 16384 (the router's shared-memory rows of h); I a
+    multiple of 64 (the gate/up GEMM's 64-feature unit, the down GEMM's
+    64-element K block) up to 16384, and of 128 for the block-scaled layers
+    (128-element scale tiles); 1 <= top_k <= min(E, 32) (one lane of the
+    selecting warp per selected expert); E <= 1024."""
+    ok, uns, inv = binding.MOE_OK, binding.MOE_ERR_UNSUPPORTED, binding.MOE_ERR_INVALID_ARG
+    cases = [
+        ((4, 128, 64, 8, 2), ok), ((4, 128, 192, 8, 2), ok), ((4, 128, 96, 8, 2), uns), ((4, 128, 32, 8, 2), uns),
+        ((4, 16384, 256, 8, 2), ok), ((4, 16512, 256, 8, 2), uns), ((4, 128, 16384, 8, 2), ok),
+        ((4, 128, 16448, 8, 2), uns), ((4, 128, 256, 1024, 2), ok), ((4, 128, 256, 1025, 2), uns),
+        ((4, 128, 256, 64, 32), ok), ((4, 128, 256, 64, 33), uns), ((4, 128, 256, 8, 8), ok),
+        ((4, 128, 256, 8, 9), inv), ((4, 128, 256, 8, 0), inv), ((4, 128, 256, 1, 1), ok),
+    ]
+    for (T, H, I, E, k), want in cases:
+        st, _ = binding.moe_workspace_size(binding.shape(T, H, I, E, k))
+        assert st == want, ((T, H, I, E, k), st, want)
+    # block-scaled layers: I a multiple of 128
+    for (T, H, I, E, k), want in [((4, 256, 192, 8, 2), uns), ((4, 256, 384, 8, 2), ok), ((4, 256, 128, 8, 2), ok)]:
+        st, _ = binding.moe_workspace_size_mx(binding.shape(T, H, I, E, k))
+        assert st == want, ((T, H, I, E, k), st, want)
+        st, _ = binding.moe_mx_weight_sizes(binding.shape(T, H, I, E, k))
+        assert st == want
+
+
+def test_static_scratch_size_and_limit_without_a_gpu():
+    st, cap = binding.moe_static_scratch_bytes()
+    assert st == binding.MOE_OK and cap == 64 << 20
+    _, need128 = binding.moe_workspace_size(binding.shape(128, 4096, 4096, 64, 8))
+    _, need129 = binding.moe_workspace_size(binding.shape(129, 4096, 4096, 64, 8))
+    assert need128 <= cap < need129
+    A = 1 << 20  # never dereferenced: the size check comes first
+    assert binding.moe_forward_static_scratch(binding.shape(129, 4096, 4096, 64, 8), A, A, A, None, A, A, A,
+                                              None) == binding.MOE_ERR_WORKSPACE
 
 
 def test_kernels_per_call_host_checks():

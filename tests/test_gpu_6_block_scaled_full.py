@@ -5,8 +5,9 @@ rows per expert, one-CTA 128-token units), in the launch configuration the
 benchmark times: the MXFP8 layer, MXFP4 weights with MXFP8 tokens, the MXFP4
 layer and the NVFP4 layer.
 
-The outputs of sampled tokens are compared with the oracle's layer of the same
-format within the layer tolerance.  The oracle quantizes only the weights of
+The outputs of sampled tokens (every token at T = 8, 32 spread over the larger
+batches) are compared with the oracle's layer of the same format within the
+layer tolerance.  The oracle quantizes only the weights of
 the experts its own routing selects for the sampled tokens (in parallel; the
 other experts' codes stay zero and a correct routing never reads them).
 """
@@ -142,7 +143,8 @@ def _check(layer, o, fmt, T, ow):
     st, det = L.device_status(T)
     assert st == 0, (st, det)
     yb = y.cpu().numpy().view(np.uint16)
-    sample = np.unique(np.linspace(0, T - 1, 4).astype(np.int64))
+    # every token of a decode batch; 32 tokens spread over a prefill-size batch
+    sample = np.unique(np.linspace(0, T - 1, min(T, 32)).astype(np.int64))
     # the experts the oracle's own routing gives the sampled tokens
     _, logits, _ = o.route_f32(x[sample], li.g, li.cfg.eps, li.w_router, li.bias)
     experts = np.unique(o.topk(logits, li.cfg.top_k))
