@@ -78,8 +78,9 @@ __global__ void __launch_bounds__(kAlignThreads)
   }
 }
 
-// One warp per padded row; 8 rows per block of 256 threads.  The grid also
-// zeroes clear[0, n_clear).
+// One warp per padded row; 8 rows per block of 256 threads.  Padding rows
+// are not written: each feeds only its own MMA column, whose results are
+// never read.  The grid also zeroes clear[0, n_clear).
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ h, const int32_t* __restrict__ sorted_ids,
                                                      const int32_t* __restrict__ offsets, int E, int N, int k, int H,
                                                      int64_t P_max, uint16_t* __restrict__ xg,
@@ -93,16 +94,12 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
   const int lane = threadIdx.x & 31;
   if (p >= P_max || p >= offsets[E]) return;
   const int src = sorted_ids[p];
+  if (src >= N || src < 0) return;  // padding row
   const int nch = H >> 3;
   uint4* dst = reinterpret_cast<uint4*>(xg + p * H);
-  if (src >= N || src < 0) {
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int c = lane; c < nch; c += 32) dst[c] = z;
-  } else {
-    const uint4* s = reinterpret_cast<const uint4*>(h + static_cast<int64_t>(src / k) * H);
+  const uint4* s = reinterpret_cast<const uint4*>(h + static_cast<int64_t>(src / k) * H);
 #pragma unroll 4
-    for (int c = lane; c < nch; c += 32) dst[c] = __ldg(s + c);
-  }
+  for (int c = lane; c < nch; c += 32) dst[c] = __ldg(s + c);
 }
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
@@ -120,16 +117,27 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
   return l | (hh << 16);
 }
 
-// One block per token; each thread owns 8 consecutive outputs (128-bit loads
-// and stores) and accumulates over the k routed rows in order j = 0..k-1.
+// Block (t, s) covers token t's output chunks [s * cpb, (s + 1) * cpb) of 8
+// features; each thread owns 8 consecutive outputs (128-bit loads and stores)
+// and accumulates over the k routed rows in order j = 0..k-1.  A token's slots
+// and weights come from the align, at least two launches back, so they are
+// read before the wait for the down GEMM (see pdl.cuh).
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ rows, const int32_t* __restrict__ slot_of,
-                                                      const float* __restrict__ w, int T, int H, int k,
+                                                      const float* __restrict__ w, int T, int H, int k, int cpb,
                                                       uint16_t* __restrict__ y) {
+  __shared__ int s_slot[32];
+  __shared__ float s_w[32];
+  const int t = blockIdx.x;
+  if (threadIdx.x < k) {
+    s_slot[threadIdx.x] = slot_of[static_cast<int64_t>(t) * k + threadIdx.x];
+    s_w[threadIdx.x] = w[static_cast<int64_t>(t) * k + threadIdx.x];
+  }
+  __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
-  const int t = blockIdx.x;
   const int nch = H >> 3;
-  for (int c = threadIdx.x; c < nch; c += blockDim.x) {
+  const int c_end = min(nch, static_cast<int>(blockIdx.y + 1) * cpb);
+  for (int c = static_cast<int>(blockIdx.y) * cpb + threadIdx.x; c < c_end; c += blockDim.x) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -140,9 +148,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 #pragma unroll
       for (int d = 0; d < 8; ++d) {
         if (j0 + d < k) {
-          const int slot = slot_of[static_cast<int64_t>(t) * k + j0 + d];
-          wj[d] = w[static_cast<int64_t>(t) * k + j0 + d];
-          v[d] = __ldg(reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(slot) * H) + c);
+          wj[d] = s_w[j0 + d];
+          v[d] = __ldg(reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(s_slot[j0 + d]) * H) + c);
         }
       }
 #pragma unroll
@@ -213,8 +220,20 @@ cudaError_t launch_gather(const uint16_t* h, const int32_t* sorted_ids, const in
 cudaError_t launch_combine(const uint16_t* out_rows, const int32_t* slot_of, const float* topk_w, int T, int H, int k,
                            uint16_t* y, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  const int threads = (H / 8 >= 256) ? 256 : ((H / 8 + 31) / 32 * 32);
-  return launch_pdl(combine_kernel, dim3(T), dim3(threads), 0, stream, out_rows, slot_of, topk_w, T, H, k, y);
+  const int nch = H / 8;
+  // few tokens: each token's row split over CTAs of 64 threads, one chunk of
+  // 8 outputs per thread (the row loads of a thread are one round trip);
+  // many tokens: one CTA of up to 256 threads per token
+  int threads, cpb;
+  if (T < 256) {
+    threads = nch >= 64 ? 64 : (nch + 31) / 32 * 32;
+    cpb = threads;
+  } else {
+    threads = nch >= 256 ? 256 : (nch + 31) / 32 * 32;
+    cpb = nch;
+  }
+  const dim3 grid(T, (nch + cpb - 1) / cpb);
+  return launch_pdl(combine_kernel, grid, dim3(threads), 0, stream, out_rows, slot_of, topk_w, T, H, k, cpb, y);
 }
 
 }  // namespace moe

@@ -87,7 +87,7 @@ constexpr int kABytes = kWeightBoxRows * kBlockK * 2;  // 16 KB weight tile per 
 constexpr int kTokRowBytes = kBlockK * 2;              // 128 B per token row per stage
 
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
-          bool A4 = false, bool NV = false>
+          bool A4 = false, bool NV = false, bool FUSED = false>
 struct GemmCfg {
   // a CTA pair splits the unit's tokens: each CTA holds half of the B tile
   static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * kTokRowBytes;
@@ -140,8 +140,9 @@ struct GemmCfg {
   static constexpr uint32_t kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                         : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kBarBytes = 512;
-  // one-CTA plans keep a shared-memory copy of the routing tables (E <= kTabMaxE)
-  static constexpr int kTabBytes = PAIR ? 0 : 2 * (kTabMaxE + 1) * 4;
+  // one-CTA plans keep a shared-memory copy of the routing tables (E <= kTabMaxE):
+  // offsets and the unit prefix sums (of both GEMMs in the fused kernel)
+  static constexpr int kTabBytes = PAIR ? 0 : (FUSED ? 3 : 2) * (kTabMaxE + 1) * 4;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + kTabBytes;
   static constexpr int kFeatPerTile = SWIGLU ? kGateUpTileFeat : kDownTileFeat;  // output features per unit
   static_assert(BN % TOKBOX == 0 && TOKBOX % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
@@ -152,6 +153,8 @@ struct GemmCfg {
   static_assert(!W4 || MX, "FP4 weights only with block-scaled tokens");
   static_assert(!A4 || W4, "FP4 tokens only with FP4 weights");
   static_assert(!NV || (A4 && !PAIR), "NVFP4: both operands E2M1, one-CTA units (TMEM columns of the scales)");
+  static_assert(!FUSED || (SWIGLU && !PAIR && !MX && kEpiWarps == 4),
+                "the fused gate/up -> down kernel: bf16, one-CTA units, four epilogue warps");
   static_assert(!MX || (4 * kChunks <= 16 && 16 + 4 * kChunks * kSfTokTiles <= kSfCols),
                 "scale columns of a stage: weight tiles from +0, token tiles from +16");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
@@ -173,7 +176,8 @@ enum : int {
   kWaitPartials = 5,      // epilogue: a later CTA's stream-K partial sums
   kWaitCombine = 6,       // epilogue: the fused combine's rendezvous
   kWaitScales = 7,        // MMA: a stage's scales written to TMEM by the scale warps
-  kWaitScaleLoads = 8     // scale warps: a ring slot's loads landed
+  kWaitScaleLoads = 8,    // scale warps: a ring slot's loads landed
+  kWaitActReady = 9       // fused kernel, producer: a gate/up unit's activation rows stored
 };
 
 // Work unit u -> expert (binary search in the unit prefix sums), weight tile
@@ -244,6 +248,31 @@ struct Range {
 };
 
 __device__ __forceinline__ int64_t range_start(int64_t W, int cta, int ctas) { return W * cta / ctas; }
+
+// The segments of a CTA, tagged with their GEMM: its range of the gate/up
+// GEMM (phase 0), then, in the fused kernel, its range of the down GEMM
+// (phase 1), each split like a kernel of its own.
+struct Work {
+  Range r0, r1;
+  int phase;
+  __device__ Work(int units0, int kblocks0, int units1, int kblocks1, int cta, int ctas, bool sk)
+      : r0(units0, kblocks0, cta, ctas, sk), r1(units1, kblocks1, cta, ctas, sk), phase(0) {}
+  __device__ bool next(int& ph, int& u, int& kb0, int& kb1) {
+    if (phase == 0) {
+      if (r0.next(u, kb0, kb1)) {
+        ph = 0;
+        return true;
+      }
+      phase = 1;
+    }
+    if (r1.next(u, kb0, kb1)) {
+      ph = 1;
+      return true;
+    }
+    return false;
+  }
+  __device__ const Range& range(int ph) const { return ph ? r1 : r0; }
+};
 
 __device__ __forceinline__ uint16_t f2bf(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
@@ -330,13 +359,15 @@ __device__ __noinline__ bool combine_unit(const ExpertGemmArgs& a, const Unit& u
   return true;
 }
 
+// FUSED: the gate/up GEMM (args, tm_w, tm_x) and then the down GEMM (args2;
+// tm_sw maps W2, tm_sx the activations) in one persistent launch.
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
-          bool A4 = false, bool NV = false>
-__global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV>::kThreads, 1)
+          bool A4 = false, bool NV = false, bool FUSED = false>
+__global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED>::kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_sx,
-                       const ExpertGemmArgs args) {
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV>;
+                       const __grid_constant__ ExpertGemmArgs args, const __grid_constant__ ExpertGemmArgs args2) {
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
@@ -349,7 +380,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
   uint64_t* cbar = done + 2;                                       // the epilogue warps' rendezvous (fused combine)
   uint32_t* cmask = reinterpret_cast<uint32_t*>(cbar + 1);         // [8]: unit rows that complete a token
   uint64_t* sfull = reinterpret_cast<uint64_t*>(cmask + 8);        // [STAGES]: a stage's scales are in TMEM
-  int32_t* tab = reinterpret_cast<int32_t*>(smem + STAGES * C::kStageBytes + C::kBarBytes);  // [2][kTabMaxE+1]
+  int32_t* tab = reinterpret_cast<int32_t*>(smem + STAGES * C::kStageBytes + C::kBarBytes);  // [2 or 3][kTabMaxE+1]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kern = SWIGLU ? kKernGemm1 : kKernGemm2;
@@ -368,13 +399,16 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
   if (args.tables_from_parent) pdl_wait();
   const int32_t* t_unit = args.unit_off;
   const int32_t* t_off = args.offsets;
+  const int32_t* t_unit2 = args2.unit_off;  // fused kernel: the down GEMM's units
   if (!PAIR && args.E <= kTabMaxE) {
     for (int i = threadIdx.x; i <= args.E; i += C::kThreads) {
       tab[i] = __ldcg(args.unit_off + i);
       tab[kTabMaxE + 1 + i] = __ldcg(args.offsets + i);
+      if (FUSED) tab[2 * (kTabMaxE + 1) + i] = __ldcg(args2.unit_off + i);
     }
     t_unit = tab;
     t_off = tab + kTabMaxE + 1;  // visible to all threads after the barrier below
+    if (FUSED) t_unit2 = tab + 2 * (kTabMaxE + 1);
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -411,13 +445,23 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
 
   const int total_units = t_unit[args.E];
   const int kblocks = args.K / C::kKPerStage;
+  const int total_units2 = FUSED ? t_unit2[args.E] : 0;
+  const int kblocks2 = FUSED ? args2.K / C::kKPerStage : 1;
   const int ctas = workers;
+  // per phase: its GEMM's arguments, unit table, kind and output features per unit
+  auto gemm_args = [&](int ph) -> const ExpertGemmArgs& { return (FUSED && ph) ? args2 : args; };
+  auto unit_tab = [&](int ph) { return (FUSED && ph) ? t_unit2 : t_unit; };
+  auto is_swiglu = [&](int ph) { return FUSED ? ph == 0 : SWIGLU; };
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
       prefetch_tensormap(&tm_w);
       prefetch_tensormap(&tm_x);
+      if (FUSED) {
+        prefetch_tensormap(&tm_sw);
+        prefetch_tensormap(&tm_sx);
+      }
       // A weight tile is read by every token chunk of its expert: streamed once
       // (evict first) when the expert's tokens fit one chunk, kept (evict last)
       // when more chunks will read it.  Token tiles are re-read by every
@@ -429,12 +473,18 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
       uint32_t phase = 0;
       int64_t issued = 0;
       bool ok = true;
-      // Until the previous kernel has completed, only weight tiles are loaded:
-      // the first ring-full of stages gets its weights at once and its token
-      // rows after pdl_wait.
+      int where = kWaitRingSlotFree;  // the wait that ran out
+      // The token (or activation) loads of the stages wait in a FIFO until
+      // their rows exist: the gate/up GEMM's token rows until the previous
+      // kernel has completed (pdl_wait), so the first ring-full of stages gets
+      // its weight tiles at once and its token rows after; in the fused
+      // kernel, a down-GEMM stage's activation rows until the gate/up unit
+      // that writes them (same expert and token chunk, weight tile = the
+      // stage's K block) has counted the stores of its four epilogue warps.
       bool deps_ready = false;
-      int n_pend = 0;
+      int n_pend = 0, pend_head = 0;
       int pend_stage[STAGES], pend_kb[STAGES], pend_tok0[STAGES], pend_rows[STAGES], pend_chunk[STAGES];
+      int pend_ready[STAGES];  // fused kernel: the awaited gate/up unit of a down-GEMM stage, or -1
       // a CTA pair signals every load on the even CTA's full barrier
       const uint32_t full_cl = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;
       auto load_2d = [&](void* dst, const CUtensorMap* map, int st, int c0, int c1, uint64_t pol) {
@@ -453,8 +503,9 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
       // chunk: the unit's token chunk (MXFP8 token scales are stored per chunk)
       auto load_tokens = [&](int st, int kb, int tok0, int rows, int chunk) {
         uint8_t* sb = smem + st * C::kStageBytes + kABytes;
+        const int row0 = args.tokens_from_h ? 0 : tok0;  // one token: its row of h, then zeros
         for (int r = 0; r < rows; r += TOKBOX)
-          load_2d(sb + r * kTokRowBytes, &tm_x, st, kb * C::kBoxX, tok0 + r, pol_x);
+          load_2d(sb + r * kTokRowBytes, &tm_x, st, kb * C::kBoxX, row0 + r, pol_x);
         if (MX && PAIR) {
           // the 512-byte scale tiles of the whole token chunk (one per 128 tokens
           // and 128-element K chunk; tile (h, c) at 512 (c G + h)), in each CTA
@@ -470,33 +521,82 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
                     512 * C::kChunks, &full[st], pol_x);
         }
       };
+      // fused kernel: a down-GEMM stage's activation rows (written by this
+      // kernel's gate/up epilogues through the generic proxy, read here by TMA)
+      auto load_act = [&](int st, int kb, int tok0, int rows) {
+        uint8_t* sb = smem + st * C::kStageBytes + kABytes;
+        fence_proxy_async_global();
+        for (int r = 0; r < rows; r += TOKBOX) tma_load_2d(sb + r * kTokRowBytes, &tm_sx, &full[st], kb * C::kBoxX,
+                                                           tok0 + r, pol_x);
+      };
       auto resolve_deps = [&]() {
         pdl_wait();
         pdl_launch_dependents();
         deps_ready = true;
-        for (int i = 0; i < n_pend; ++i)
-          load_tokens(pend_stage[i], pend_kb[i], pend_tok0[i], pend_rows[i], pend_chunk[i]);
-        n_pend = 0;
       };
-      Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
-      int u, kb0, kb1;
-      while (ok && rg.next(u, kb0, kb1)) {
-        const Unit un = decode_unit(u, t_unit, t_off, args.E, args.tiles_per_expert, BN);
+      auto issue_head = [&]() {
+        const int i = pend_head;
+        if (FUSED && pend_ready[i] >= 0)
+          load_act(pend_stage[i], pend_kb[i], pend_tok0[i], pend_rows[i]);
+        else
+          load_tokens(pend_stage[i], pend_kb[i], pend_tok0[i], pend_rows[i], pend_chunk[i]);
+        pend_head = pend_head + 1 == STAGES ? 0 : pend_head + 1;
+        --n_pend;
+      };
+      // whether the FIFO head's rows exist: polled, or waited for (bounded)
+      auto head_ready = [&](bool wait) -> bool {
+        const int r = pend_ready[pend_head];
+        if (!deps_ready) {
+          if (!wait && !(FUSED && r >= 0)) return false;
+          resolve_deps();
+        }
+        if (!FUSED || r < 0) return true;
+        if (ld_acquire(args.ready + r) >= C::kEpiWarps) return true;
+        if (!wait) return false;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire(args.ready + r) < C::kEpiWarps) {
+          if (*abort_flag || globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+          __nanosleep(64);
+        }
+        return true;
+      };
+      Work rg(total_units, kblocks, total_units2, kblocks2, worker, ctas, args.stream_k != 0);
+      int ph, u, kb0, kb1;
+      while (ok && rg.next(ph, u, kb0, kb1)) {
+        const ExpertGemmArgs& A = gemm_args(ph);
+        const bool sw = is_swiglu(ph);
+        const Unit un = decode_unit(u, unit_tab(ph), t_off, args.E, A.tiles_per_expert, BN);
         // a pair's unit: weight tiles 2t (even CTA) and 2t+1; the MMA's N
         // tokens split in halves, the first half in the even CTA
         const int tile = PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile;
         const int n_mma = PAIR ? (un.n + 31) / 32 * 32 : un.n;
         const int half = PAIR ? n_mma / 2 : n_mma;
         const int tok_first = un.tok0 + static_cast<int>(rank) * half;
-        const int wrow = un.e * args.w_rows_per_expert + tile * C::kFeatPerTile;
+        const int wrow = un.e * A.w_rows_per_expert + tile * (sw ? kGateUpTileFeat : kDownTileFeat);
         const int tok_rows = (half + TOKBOX - 1) / TOKBOX * TOKBOX;  // whole boxes; rows past n are unused
         const bool reused = t_off[un.e + 1] - t_off[un.e] > BN;
         const uint64_t pol_w = reused ? pol_keep : pol_stream;
         const uint32_t bytes = C::kWTxBytes + tok_rows * kTokRowBytes + C::kSfBytes;  // per CTA (both of a pair)
         const int chunk = MX ? t_unit[un.e] / args.tiles_per_expert + (un.tok0 - t_off[un.e]) / BN : 0;
+        // fused kernel, down GEMM: K block kb of this unit is gate/up unit
+        // (expert, tile kb, the same token chunk) = rd_base + kb * chunks
+        int rd_base = -1, rd_step = 0;
+        if (FUSED && ph == 1) {
+          rd_step = (t_unit[un.e + 1] - t_unit[un.e]) / args.tiles_per_expert;
+          rd_base = t_unit[un.e] + (un.tok0 - t_off[un.e]) / BN;
+        }
         for (int kb = kb0; kb < kb1; ++kb) {
+          if (n_pend == STAGES) {  // the slot about to be refilled still waits for its token rows
+            if (!head_ready(true)) {
+              ok = false;
+              where = kWaitActReady;
+              break;
+            }
+            issue_head();
+          }
           if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitTimeoutNs, abort_flag)) {
             ok = false;
+            where = kWaitRingSlotFree;
             break;
           }
           uint8_t* sa = smem + stage * C::kStageBytes;
@@ -504,10 +604,10 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
             mbar_arrive_expect_tx(&full[stage], bytes);
           else if (leader)
             mbar_arrive_expect_tx(&full[stage], 2 * bytes);  // both CTAs' loads
-          if (SWIGLU) {  // 16 gate rows, the matching 16 up rows, x 4
+          if (sw) {  // 16 gate rows, the matching 16 up rows, x 4
             load_gate_up(sa, stage, kb, tile, un.e, pol_w);
           } else {
-            load_2d(sa, &tm_w, stage, kb * C::kBoxX, wrow, pol_w);
+            load_2d(sa, FUSED ? &tm_sw : &tm_w, stage, kb * C::kBoxX, wrow, pol_w);
           }
           if (MX) {  // the weight tile's scales (static: loaded before the parent kernel ends)
             const int wtiles = PAIR ? 2 * args.tiles_per_expert : args.tiles_per_expert;  // 128-row tiles per expert
@@ -520,16 +620,15 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
                         &full[stage], pol_w);
             }
           }
-          if (deps_ready) {
-            load_tokens(stage, kb, tok_first, tok_rows, chunk);
-          } else {
-            pend_stage[n_pend] = stage;
-            pend_kb[n_pend] = kb;
-            pend_tok0[n_pend] = tok_first;
-            pend_rows[n_pend] = tok_rows;
-            pend_chunk[n_pend] = chunk;
-            if (++n_pend == STAGES) resolve_deps();
-          }
+          const int slot = (pend_head + n_pend) % STAGES;
+          pend_stage[slot] = stage;
+          pend_kb[slot] = kb;
+          pend_tok0[slot] = tok_first;
+          pend_rows[slot] = tok_rows;
+          pend_chunk[slot] = chunk;
+          pend_ready[slot] = rd_base >= 0 ? rd_base + kb * rd_step : -1;
+          ++n_pend;
+          while (n_pend > 0 && head_ready(false)) issue_head();
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -537,8 +636,19 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
           }
         }
       }
-      if (!deps_ready) resolve_deps();  // fewer iterations than stages (or none)
-      if (!ok) raise_timeout(args.err, abort_flag, kern, kWaitRingSlotFree);
+      // the token loads still waiting (fewer iterations than stages, or the
+      // last ones); after a wait that ran out they are issued all the same
+      // (the call reports the timeout), so that every stage's loads land
+      while (n_pend > 0) {
+        if (ok && !head_ready(true)) {
+          ok = false;
+          where = kWaitActReady;
+        }
+        if (!deps_ready) resolve_deps();
+        issue_head();
+      }
+      if (!deps_ready) resolve_deps();
+      if (!ok) raise_timeout(args.err, abort_flag, kern, where);
       // every load this thread issued must have landed before the CTA exits
       // (the odd CTA of a pair sees that through the release of its stages:
       // the pair's MMA ran on them, so they had landed)
@@ -558,10 +668,10 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
       uint32_t acc_phase = 0;
       bool ok = true;
       int where = 0;  // the wait that ran out
-      Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
-      int u, kb0, kb1;
-      while (ok && rg.next(u, kb0, kb1)) {
-        const Unit un = decode_unit(u, t_unit, t_off, args.E, args.tiles_per_expert, BN);
+      Work rg(total_units, kblocks, total_units2, kblocks2, worker, ctas, args.stream_k != 0);
+      int ph, u, kb0, kb1;
+      while (ok && rg.next(ph, u, kb0, kb1)) {
+        const Unit un = decode_unit(u, unit_tab(ph), t_off, args.E, gemm_args(ph).tiles_per_expert, BN);
         const bool free_acc = PAIR ? mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, kWaitTimeoutNs, abort_flag)
                                    : mbar_wait(&tempty[acc], acc_phase ^ 1u, kWaitTimeoutNs, abort_flag);
         if (!free_acc) {
@@ -735,14 +845,18 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
     // gate/up: warp quarter q holds features +16q .. +16q+15, gate in lanes
     // 0..15 and up in lanes 16..31
     const bool lo = lane < 16;
-    // this CTA's partial-sum slot: [BN columns][128 rows] fp32
-    float* my_slot = args.partials + static_cast<int64_t>(blockIdx.x) * BN * 128;
     uint32_t cbar_phase = 0;  // uses of the combine rendezvous so far, mod 2
     const uint32_t tempty_cl = PAIR ? mapa_shared(smem_u32(tempty), 0) : 0u;
-    Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
-    int u, kb0, kb1;
-    while (ok && rg.next(u, kb0, kb1)) {
-      const Unit un = decode_unit(u, t_unit, t_off, args.E, args.tiles_per_expert, BN);
+    Work rg(total_units, kblocks, total_units2, kblocks2, worker, ctas, args.stream_k != 0);
+    int ph, u, kb0, kb1;
+    while (ok && rg.next(ph, u, kb0, kb1)) {
+      const ExpertGemmArgs& A = gemm_args(ph);
+      const bool sw = is_swiglu(ph);
+      const int kb_total = ph ? kblocks2 : kblocks;
+      const int64_t W = rg.range(ph).W;
+      // this CTA's partial-sum slot of this GEMM: [BN columns][128 rows] fp32
+      float* my_slot = A.partials + static_cast<int64_t>(blockIdx.x) * BN * 128;
+      const Unit un = decode_unit(u, unit_tab(ph), t_off, args.E, A.tiles_per_expert, BN);
       // warp-uniform outcome: tcgen05.ld below must be executed by all 32 lanes
       const bool got = mbar_wait(&tfull[acc], acc_phase, kWaitTimeoutNs, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) {
@@ -776,16 +890,17 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
         }
         __threadfence();
         __syncwarp();
-        if (lane == 0) st_release(args.flags + blockIdx.x * 4 + q, 1);
+        if (lane == 0) st_release(A.flags + blockIdx.x * 4 + q, 1);
       } else {
         // this CTA finishes the unit: the CTAs after it whose (non-empty)
         // ranges start inside the unit hold its later K-blocks and have
         // written their partial sums as their first work
-        const int64_t unit_end = static_cast<int64_t>(u + 1) * kblocks;
+        const int64_t unit_end = static_cast<int64_t>(u + 1) * kb_total;
         int c_last = blockIdx.x;  // producers are the CTAs in (blockIdx.x, c_last] with non-empty ranges
-        if (kb1 < kblocks)
-          while (c_last + 1 < ctas && range_start(rg.W, c_last + 1, ctas) < unit_end) ++c_last;
-        const int feat_base = (PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile) * C::kFeatPerTile;
+        if (kb1 < kb_total)
+          while (c_last + 1 < ctas && range_start(W, c_last + 1, ctas) < unit_end) ++c_last;
+        const int feat_base =
+            (PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile) * (sw ? kGateUpTileFeat : kDownTileFeat);
         // SwiGLU (gate/up GEMM) or plain convert of one 16-column group, and its stores
         auto emit_chunk = [&](int c0, float (&v)[16]) {
           if (NV) {  // NVFP4 tensor scales: the expert matrix's times each token row's
@@ -794,10 +909,10 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], __fmul_rn(gw, __ldcg(gx + j)));
           }
-          if (!SWIGLU) {
-            uint16_t* out = args.out + static_cast<int64_t>(un.tok0 + c0) * args.n_out + feat_base + row;
+          if (!sw) {
+            uint16_t* out = A.out + static_cast<int64_t>(un.tok0 + c0) * A.n_out + feat_base + row;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) out[static_cast<int64_t>(j) * args.n_out] = f2bf(v[j]);
+            for (int j = 0; j < 16; ++j) out[static_cast<int64_t>(j) * A.n_out] = f2bf(v[j]);
           } else {
             // lanes l and l+16 swap half of their columns: lane l keeps the
             // gate values of columns 0..7 and receives the matching up values,
@@ -813,9 +928,9 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
               a[j] = __fdividef(g, 1.0f + __expf(-g)) * up;  // SiLU(gate) * up
             }
             const int feat = feat_base + q * 16 + (lane & 15);
-            uint16_t* out = args.out + static_cast<int64_t>(un.tok0 + c0 + (lo ? 0 : 8)) * args.n_out + feat;
+            uint16_t* out = A.out + static_cast<int64_t>(un.tok0 + c0 + (lo ? 0 : 8)) * A.n_out + feat;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) out[static_cast<int64_t>(j) * args.n_out] = f2bf(a[j]);
+            for (int j = 0; j < 8; ++j) out[static_cast<int64_t>(j) * A.n_out] = f2bf(a[j]);
           }
         };
         if constexpr (C::kAccBufs == 1) {
@@ -848,12 +963,12 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
             for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(ra[j]);
             bool good = true;
             for (int c = blockIdx.x + 1; c <= c_last; ++c) {
-              if (range_start(rg.W, c, ctas) == range_start(rg.W, c + 1, ctas)) continue;  // empty range
-              if (c0 == c_first && !wait_flag(args.flags + c * 4 + q, abort_flag, kWaitTimeoutNs)) {
+              if (range_start(W, c, ctas) == range_start(W, c + 1, ctas)) continue;  // empty range
+              if (c0 == c_first && !wait_flag(A.flags + c * 4 + q, abort_flag, kWaitTimeoutNs)) {
                 good = false;
                 break;
               }
-              const float* slot = args.partials + static_cast<int64_t>(c) * BN * 128;
+              const float* slot = A.partials + static_cast<int64_t>(c) * BN * 128;
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[j] += __ldcg(slot + (c0 + j) * 128 + row);
             }
@@ -866,7 +981,16 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
           }
           // the partial-sum flags read here are cleared for the next launch
           if (ok && lane == 0)
-            for (int c = blockIdx.x + 1; c <= c_last; ++c) args.flags[c * 4 + q] = 0;
+            for (int c = blockIdx.x + 1; c <= c_last; ++c) A.flags[c * 4 + q] = 0;
+        }
+        // fused kernel: the unit's activation rows of this lane quarter are
+        // stored; count this warp in the unit's counter (the down GEMM's
+        // producers wait for all four, then read the rows by TMA)
+        if (FUSED && ph == 0 && ok) {
+          fence_proxy_async_global();
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) red_release_add(args.ready + u, 1);
         }
       }
       if (!ok) break;
@@ -875,7 +999,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
         acc = 0;
         acc_phase ^= 1u;
       }
-      if (!SWIGLU && kb0 == 0 && args.fuse_combine && C::kEpiWarps == 4) {
+      if (!SWIGLU && !FUSED && kb0 == 0 && args.fuse_combine && C::kEpiWarps == 4) {
         const int tile = PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile;
         ok = combine_unit<BN>(args, un, tile, row, lane, cbar, cbar_phase, cmask, abort_flag);
         if (!ok) {
@@ -900,14 +1024,16 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
   }
 }
 
+// tsw / tsx: the scale maps of MXFP8 pairs, or the fused kernel's W2 and
+// activation maps; a2: the fused kernel's down GEMM.
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
-          bool A4 = false, bool NV = false>
+          bool A4 = false, bool NV = false, bool FUSED = false>
 cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, int num_sms,
                                cudaStream_t stream, const CUtensorMap* tsw = nullptr,
-                               const CUtensorMap* tsx = nullptr) {
-  static const CUtensorMap kNoMap = {};  // the scale maps of MXFP8 pairs; unused elsewhere
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV>;
-  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV>;
+                               const CUtensorMap* tsx = nullptr, const ExpertGemmArgs* a2 = nullptr) {
+  static const CUtensorMap kNoMap = {};  // unused map arguments
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED>;
+  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED>;
   static PerDevice config;  // the smem attribute, and the CTA pairs that fit on the device at once
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::kThreads);
@@ -949,7 +1075,7 @@ cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, con
   cfg.gridDim = dim3(grid);
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tw, tx, tsw ? *tsw : kNoMap, tsx ? *tsx : kNoMap, a);
+  return cudaLaunchKernelEx(&cfg, kernel, tw, tx, tsw ? *tsw : kNoMap, tsx ? *tsx : kNoMap, a, a2 ? *a2 : a);
 }
 
 // Two tile plans by the expected tokens per expert (T*top_k/E):
@@ -1076,6 +1202,13 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm
       return launch_expert_gemm<true, kGateUpBn[1], kGateUpStages[1], kTokBox[1], false>(tm_w13, tm_x, a, num_sms,
                                                                                           stream);
   }
+}
+
+cudaError_t launch_gemm_fused_mlp(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const CUtensorMap& tm_w2,
+                                  const CUtensorMap& tm_act, const ExpertGemmArgs& a1, const ExpertGemmArgs& a2,
+                                  int num_sms, cudaStream_t stream) {
+  return launch_expert_gemm<true, kGateUpBn[0], kGateUpStages[0], kTokBox[0], false, false, false, false, false, true>(
+      tm_w13, tm_x, a1, num_sms, stream, &tm_w2, &tm_act, &a2);
 }
 
 cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const ExpertGemmArgs& a,

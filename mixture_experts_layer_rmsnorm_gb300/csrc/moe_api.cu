@@ -33,6 +33,8 @@ struct Layout {
   size_t err, h, logits, ids, w, counts, offsets, unit1, unit2, sorted, slot, flags, ccnt, blk_counts, blk_base,
       partials, xg, act, out, xs, aq, as, gx, ga, total;
   int64_t n_ccnt;      // combine arrival counters of the down GEMM: [H / 128][T]
+  int64_t n_flags;     // ints at `flags` cleared by the align: stream-K flags, then (small tile plan) the
+                       // fused kernel's per-unit completion counters
   int64_t P_max;       // padded rows: 16-row padding (bf16), 32-row padding rounded to 128 (MXFP8)
   int64_t sorted_cap;  // sorted_ids entries (room for debug padding up to 256)
 };
@@ -70,7 +72,9 @@ Layout make_layout(const moe_shape& s, bool mx = false) {
   L.sorted = take(static_cast<size_t>(L.sorted_cap * 4));
   L.slot = take(static_cast<size_t>(T * k * 4));
   // stream-K flags and partial sums of the expert GEMMs (slot = BN x 128 fp32 per CTA)
-  L.flags = take(static_cast<size_t>(kGemmFlagInts) * 4);
+  const bool small = moe::choose_plan(T, k, E) == moe::GemmPlan::kSmall;
+  L.n_flags = kGemmFlagInts + (small && !mx ? moe::fused_mlp_ready_ints(L.P_max, I) : 0);
+  L.flags = take(static_cast<size_t>(L.n_flags) * 4);
   L.n_ccnt = (H / 128) * T;
   L.ccnt = take(static_cast<size_t>(L.n_ccnt) * 4);
   // per-block counts / bases of the multi-CTA align
@@ -276,7 +280,7 @@ moe_status run_front(const moe_shape& s, const Layout& L, const moe_bf16* x, con
                            utiles2, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
                            at<int32_t>(ws, L.sorted), at<int32_t>(ws, L.slot),
                            bn1 > 0 ? at<int32_t>(ws, L.unit1) : nullptr, bn2 > 0 ? at<int32_t>(ws, L.unit2) : nullptr,
-                           err, at<int32_t>(ws, L.flags), kGemmFlagInts, st);
+                           err, at<int32_t>(ws, L.flags), static_cast<int>(L.n_flags), st);
   else
     ce = moe::launch_align_multi(at<float>(ws, L.logits), s.T, s.top_k, s.renormalize, at<int32_t>(ws, L.ids),
                                  at<float>(ws, L.w), s.E, pad, bn1, utiles1, bn2,
@@ -284,7 +288,7 @@ moe_status run_front(const moe_shape& s, const Layout& L, const moe_bf16* x, con
                                  at<int32_t>(ws, L.sorted), at<int32_t>(ws, L.slot),
                                  bn1 > 0 ? at<int32_t>(ws, L.unit1) : nullptr,
                                  bn2 > 0 ? at<int32_t>(ws, L.unit2) : nullptr, at<int32_t>(ws, L.blk_counts),
-                                 at<int32_t>(ws, L.blk_base), err, at<int32_t>(ws, L.flags), kGemmFlagInts, st,
+                                 at<int32_t>(ws, L.blk_base), err, at<int32_t>(ws, L.flags), static_cast<int>(L.n_flags), st,
                                  nullptr);
   if (ce != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -314,10 +318,12 @@ moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t
   }
   // router, top-k + align (1 kernel, or 3), gather, the two GEMMs, combine
   const int front = 1 + (moe::align_fuses_topk(s.T, s.E) ? 1 : 3) + 1;
+  const bool one_mlp = moe::fused_mlp(moe::choose_plan(s.T, s.top_k, s.E), false);  // one launch for both GEMMs
   if (call == MOE_CALL_FORWARD)
-    *count = front + 3;
+    *count = front + 3 - (moe::tokens_from_h(s.T, false, false) ? 1 : 0) - (one_mlp ? 1 : 0);  // no gather for
+                                                                                                  // one token
   else if (call == MOE_CALL_FORWARD_FUSED_FRONT)
-    *count = 1 + 3;
+    *count = 1 + 3 - (one_mlp ? 1 : 0);
   else if (call == MOE_CALL_FORWARD_MX || call == MOE_CALL_FORWARD_MXFP4 || call == MOE_CALL_FORWARD_MXFP4A4 ||
            call == MOE_CALL_FORWARD_NVFP4)
     *count = front + 4;  // + the activation quantize between the GEMMs
@@ -395,9 +401,14 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
     return !events || cudaEventRecord(static_cast<cudaEvent_t>(events[i]), cs) == cudaSuccess;
   };
 
+  // One token: every expert's list is that token's row of h (padded to 16
+  // rows), so the gate/up GEMM reads its token tiles straight from h, rows
+  // past T reading as zeros, and no gather runs.
+  const bool tokens_from_h = moe::tokens_from_h(s.T, single_launch_front, fused_combine);
   CUtensorMap tm_w13, tm_xg, tm_w2, tm_act;
   if (!make_map_gate_up(&tm_w13, w13, s.H, s.I, s.E) ||
-      !make_map(&tm_xg, at<void>(workspace, L.xg), s.H, L.P_max, moe::gemm_tok_box_rows(plan)) ||
+      !(tokens_from_h ? make_map(&tm_xg, at<void>(workspace, L.h), s.H, s.T, moe::gemm_tok_box_rows(plan))
+                      : make_map(&tm_xg, at<void>(workspace, L.xg), s.H, L.P_max, moe::gemm_tok_box_rows(plan))) ||
       !make_map(&tm_w2, w2, s.I, static_cast<uint64_t>(s.E) * s.H, moe::kWeightBoxRows) ||
       !make_map(&tm_act, at<void>(workspace, L.act), s.I, L.P_max, moe::gemm_tok_box_rows(plan)))
     return MOE_ERR_CUDA;
@@ -436,7 +447,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
     fa.unit_off2 = at<int32_t>(workspace, L.unit2);
     fa.err = err;
     fa.flags = at<int32_t>(workspace, L.flags);
-    fa.n_flags = kGemmFlagInts;
+    fa.n_flags = static_cast<int>(L.n_flags);
     fa.combine_cnt = at<int32_t>(workspace, L.ccnt);
     fa.n_combine_cnt = fused_combine ? static_cast<int>(L.n_ccnt) : 0;
     fa.xg = at<uint16_t>(workspace, L.xg);
@@ -459,7 +470,8 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
                              utiles1, bn2, utiles2, at<int32_t>(workspace, L.counts),
                              at<int32_t>(workspace, L.offsets), at<int32_t>(workspace, L.sorted),
                              at<int32_t>(workspace, L.slot), at<int32_t>(workspace, L.unit1),
-                             at<int32_t>(workspace, L.unit2), err, at<int32_t>(workspace, L.flags), kGemmFlagInts,
+                             at<int32_t>(workspace, L.unit2), err, at<int32_t>(workspace, L.flags),
+                             static_cast<int>(L.n_flags),
                              cs);
     } else {
       ce = moe::launch_align_multi(at<float>(workspace, L.logits), s.T, s.top_k, s.renormalize,
@@ -469,15 +481,16 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
                                    at<int32_t>(workspace, L.slot), at<int32_t>(workspace, L.unit1),
                                    at<int32_t>(workspace, L.unit2), at<int32_t>(workspace, L.blk_counts),
                                    at<int32_t>(workspace, L.blk_base), err, at<int32_t>(workspace, L.flags),
-                                   kGemmFlagInts, cs, events ? events[2] : nullptr);
+                                   static_cast<int>(L.n_flags), cs, events ? events[2] : nullptr);
     }
     if (ce != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
-    if (moe::launch_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
+    if (!tokens_from_h &&
+        moe::launch_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
                            at<int32_t>(workspace, L.offsets), s.E, N, s.top_k, s.H, L.P_max,
                            at<uint16_t>(workspace, L.xg), at<int32_t>(workspace, L.ccnt),
-                           fused_combine ? L.n_ccnt : 0, cs) != cudaSuccess ||
-        !mark(4))
+                           fused_combine ? L.n_ccnt : 0, cs) != cudaSuccess)
       return MOE_ERR_CUDA;
+    if (!mark(4)) return MOE_ERR_CUDA;
   }
 
   moe::ExpertGemmArgs a1{};
@@ -494,8 +507,9 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a1.flags = at<int32_t>(workspace, L.flags);
   a1.stream_k = plan == GemmPlan::kSmall;
   a1.pair = moe::gemm_uses_pairs(plan, tiles1);
-  a1.tables_from_parent = front;
-  if (moe::launch_gemm_gate_up(tm_w13, tm_xg, a1, plan, num_sms, cs) != cudaSuccess || !mark(5)) return MOE_ERR_CUDA;
+  a1.tables_from_parent = front || tokens_from_h;  // the align is then the GEMM's parent
+  a1.tokens_from_h = tokens_from_h;
+  a1.ready = at<int32_t>(workspace, L.flags) + kGemmFlagInts;
 
   moe::ExpertGemmArgs a2{};
   a2.offsets = at<int32_t>(workspace, L.offsets);
@@ -512,7 +526,17 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a2.stream_k = plan == GemmPlan::kSmall;
   a2.pair = moe::gemm_uses_pairs(plan, tiles2);
   if (fused_combine) set_fused_combine(a2, s, L, workspace, y);
-  if (moe::launch_gemm_down(tm_w2, tm_act, a2, plan, num_sms, cs) != cudaSuccess || !mark(6)) return MOE_ERR_CUDA;
+  if (moe::fused_mlp(plan, fused_combine)) {
+    // both GEMMs in one launch (events[6] then follows events[5] at once)
+    if (moe::launch_gemm_fused_mlp(tm_w13, tm_xg, tm_w2, tm_act, a1, a2, num_sms, cs) != cudaSuccess || !mark(5) ||
+        !mark(6))
+      return MOE_ERR_CUDA;
+  } else {
+    if (moe::launch_gemm_gate_up(tm_w13, tm_xg, a1, plan, num_sms, cs) != cudaSuccess || !mark(5))
+      return MOE_ERR_CUDA;
+    if (moe::launch_gemm_down(tm_w2, tm_act, a2, plan, num_sms, cs) != cudaSuccess || !mark(6))
+      return MOE_ERR_CUDA;
+  }
 
   if (!fused_combine &&
       moe::launch_combine(at<uint16_t>(workspace, L.out), at<int32_t>(workspace, L.slot), at<float>(workspace, L.w),

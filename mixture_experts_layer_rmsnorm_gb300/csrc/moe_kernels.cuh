@@ -112,6 +112,10 @@ struct ExpertGemmArgs {
   int stream_k;             // 1: equal K-block ranges per CTA; 0: whole units round-robin
   int pair;                 // 1: CTA pairs, a unit = weight tiles 2t and 2t+1 (large plan only)
   int tables_from_parent;   // 1: the routing tables come from the previous kernel (wait before reading)
+  int tokens_from_h;        // 1 (one token, gate/up GEMM): tm_x maps h itself; every unit's token rows start
+                            // at h row 0 (rows past T are read as zeros)
+  int32_t* ready;           // fused gate/up -> down kernel: per gate/up unit, the epilogue warps that have
+                            // stored its activation rows (zero on entry)
   const uint8_t* w_scales;  // MXFP8 GEMMs: weight scales (512-byte tiles per 128 rows x 128 of K)
   const uint8_t* x_scales;  // MXFP8 GEMMs: token scales, one 512-byte tile per token chunk and 128 of K
   const float* w_gscale;    // NVFP4 GEMMs: fp32 tensor scale per expert matrix [E]
@@ -140,11 +144,35 @@ inline GemmPlan choose_plan(int64_t T, int64_t top_k, int64_t E) {
   return T * top_k <= 16 * E ? GemmPlan::kSmall : GemmPlan::kLarge;
 }
 
+// Whether a moe_forward call runs both expert GEMMs as one launch
+// (launch_gemm_fused_mlp): the small tile plan, unless the combine runs in
+// the down GEMM's epilogue.
+inline bool fused_mlp(GemmPlan plan, bool fused_combine) { return plan == GemmPlan::kSmall && !fused_combine; }
+
+// Whether the gate/up GEMM of a moe_forward call reads its token tiles from h
+// (one token: no gather kernel), given the entry point's options.
+inline bool tokens_from_h(int T, bool single_launch_front, bool fused_combine) {
+  return T == 1 && !single_launch_front && !fused_combine;
+}
+
 // Encodes nothing itself: the tensor maps are built by the caller.
 cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
                                 GemmPlan plan, int num_sms, cudaStream_t stream);
 cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act, const ExpertGemmArgs& a,
                              GemmPlan plan, int num_sms, cudaStream_t stream);
+// Both GEMMs of the small tile plan in one persistent launch ("4 · La fusion
+// de noyaux", §4.2 "GEMM + GEMM" and §4.6): every CTA runs its stream-K range
+// of the gate/up GEMM (a1), then its range of the down GEMM (a2); a down-GEMM
+// stage's activation rows are loaded once the gate/up unit that writes them
+// (same expert and token chunk, weight tile = the stage's K block) has counted
+// its four epilogue warps in a1.ready.  a1.ready: >= fused_mlp_ready_ints
+// ints, zero on entry.
+cudaError_t launch_gemm_fused_mlp(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const CUtensorMap& tm_w2,
+                                  const CUtensorMap& tm_act, const ExpertGemmArgs& a1, const ExpertGemmArgs& a2,
+                                  int num_sms, cudaStream_t stream);
+// gate/up units of the small plan at most: P_max rows in lists of >= 16 rows,
+// so at most P_max / 16 token chunks per weight tile, I / 64 tiles
+inline int64_t fused_mlp_ready_ints(int64_t P_max, int64_t I) { return (P_max + 15) / 16 * (I / 64); }
 // Whether a GEMM with `tiles` weight tiles per expert runs on CTA pairs, and
 // the tiles per expert its work-unit table counts (pairs of tiles then).
 bool gemm_uses_pairs(GemmPlan plan, int tiles);

@@ -217,7 +217,11 @@ def check_expert_rows(o, li: inputs.LayerInputs, dl: "DeviceLayer", T: int, g: d
     out: the GPU rounds its fp32 sum of act x W2 to bf16; the reference is the
     oracle's fp64 output rounded once to bf16.  Every element within one bf16
     step plus 1e-5 of the row maximum plus the exact effect of the GPU's act
-    differences (sum_i |W2[n,i]| |d act_i|), and at least 99% bit-equal."""
+    differences (sum_i |W2[n,i]| |d act_i|).  At least 99% of the elements
+    bit-equal to that reference, or, where the GPU's act differs from the
+    oracle's, to the down projection of the GPU's own act in exact (fp64)
+    arithmetic rounded once to bf16: at K = 4096 the act differences alone
+    move a few percent of the outputs across a bf16 rounding boundary."""
     k = li.cfg.top_k
     rows = np.asarray(rows, np.int64)
     if rows.size == 0:
@@ -251,8 +255,13 @@ def check_expert_rows(o, li: inputs.LayerInputs, dl: "DeviceLayer", T: int, g: d
             prop = np.abs(widen(li.w2[e][:, nz])) @ da[nz] if nz.size else 0.0
             tol_o = bf16_ulp(np.maximum(np.abs(o16), np.abs(o_g))) + 1e-5 * np.abs(o_ref).max() + prop
             assert (do <= tol_o).all(), f"{label} out row {p} (token {t}, expert {e}): max excess {(do - tol_o).max():.3e}"
+            eq = do == 0
+            miss = np.nonzero(~eq)[0]
+            if miss.size and nz.size:
+                own = round_bf16(widen(li.w2[e][miss]) @ a_g)  # exact down projection of the GPU's act
+                eq[miss] = o_g[miss] == own
             eq_a += int((da == 0).sum()); n_a += da.size
-            eq_o += int((do == 0).sum()); n_o += do.size
+            eq_o += int(eq.sum()); n_o += do.size
     assert eq_a >= 0.99 * n_a, f"{label} act: only {eq_a / n_a:.4f} of elements bit-equal"
     assert eq_o >= 0.99 * n_o, f"{label} out: only {eq_o / n_o:.4f} of elements bit-equal"
     _report({"check": "expert_rows", "label": label, "T": int(T), "rows": int(rows.size),
