@@ -455,7 +455,7 @@ def run_ours(args, wl, world, rank, local):
     kern_ev = {T: [new_events() for _ in range(args.steps)] for T in Ts}
     setup_s = time.time() - t_setup
 
-    ff, fc = args.fused_front, args.fused_combine
+    ff, fc, fm = args.fused_front, args.fused_combine, args.fused_mlp
     mx = ("nvfp4" if args.nvfp4 else "mxfp4a4" if args.mxfp4a4 else "mxfp4" if args.mxfp4
           else args.mx)  # formats for the byte counts
     if args.nvfp4:
@@ -472,14 +472,15 @@ def run_ours(args, wl, world, rank, local):
             return layer.forward_mxfp4(x, y, events=events, fp4_tokens=args.mxfp4a4)
         if mx:
             return layer.forward_mx(x, y, events=events)
-        return layer.forward(x, y, events=events, fused_front=ff, fused_combine=fc)
+        return layer.forward(x, y, events=events, fused_front=ff, fused_combine=fc, fused_mlp=fm)
 
     def kpc(T):  # our kernels per layer call
         call = (binding.MOE_CALL_FORWARD_NVFP4 if args.nvfp4 else
                 binding.MOE_CALL_FORWARD_MXFP4A4 if args.mxfp4a4 else
                 binding.MOE_CALL_FORWARD_MXFP4 if args.mxfp4 else binding.MOE_CALL_FORWARD_MX if mx else
                 binding.MOE_CALL_FORWARD_FUSED_FRONT if ff else
-                binding.MOE_CALL_FORWARD_FUSED_COMBINE if fc else binding.MOE_CALL_FORWARD)
+                binding.MOE_CALL_FORWARD_FUSED_COMBINE if fc else
+                binding.MOE_CALL_FORWARD_FUSED_MLP if fm else binding.MOE_CALL_FORWARD)
         return binding.kernels_per_call(T, H, wl["I"], wl["E"], wl["k"], call)
 
     def one_step(step_idx=None, per_kernel=False):
@@ -597,7 +598,10 @@ def run_ours(args, wl, world, rank, local):
                             ncu_traffic_per_launch(dom, args.workload))
             roof["peak_source"] = f"bf16_tflops ({peak_kind})"
     else:
-        if dom == "gemm_gate_up_swiglu":
+        if dom == "gemm_gate_up_swiglu" and fm:  # both GEMMs in one launch
+            per = [accounting.gemm1_kernel_bytes(T, H, wl["I"], wl["k"], touched[T], mx) +
+                   accounting.gemm2_kernel_bytes(T, H, wl["I"], wl["k"], touched[T], mx) for T in Ts]
+        elif dom == "gemm_gate_up_swiglu":
             per = [accounting.gemm1_kernel_bytes(T, H, wl["I"], wl["k"], touched[T], mx) for T in Ts]
         elif dom == "gemm_down":
             per = [accounting.gemm2_kernel_bytes(T, H, wl["I"], wl["k"], touched[T], mx) for T in Ts]
@@ -606,7 +610,8 @@ def run_ours(args, wl, world, rank, local):
         traffic = None if mx else ncu_traffic_per_launch(dom, args.workload)
         roof = roofline("hbm", sum(per) / len(per), avg_s, peaks["hbm_gbs"], traffic)
         roof["peak_source"] = f"hbm_gbs ({peak_kind}, copy bandwidth)"
-    roof["kernel"] = dom
+    roof["kernel"] = "expert_mlp_fused (gate/up and down GEMMs in one launch)" if (fm and dom == "gemm_gate_up_swiglu") \
+        else dom
     roof["algorithmic_per_launch"] = sum(per) / len(per)
     roof["avg_launch_us"] = round(avg_s * 1e6, 2)
 
@@ -632,7 +637,7 @@ def run_ours(args, wl, world, rank, local):
            "ms_per_step": round(e2e_ms_step, 4)}
 
     prefill = None
-    if args.workload == "decode" and not args.no_prefill and not ff:
+    if args.workload == "decode" and not args.no_prefill and not ff and not fm:
         prefill = prefill_section(args, wl, layer, fwd, flush_l2, stream, gpu_index, world, d16, mx)
 
     out = {
@@ -657,6 +662,7 @@ def run_ours(args, wl, world, rank, local):
                                  else "moe_forward: multi-launch front end"),
                    "combine": ("moe_forward_fused_combine: in the down GEMM's epilogue" if fc
                                else "separate kernel"),
+                   "expert_gemms": ("moe_forward_fused_mlp: both in one launch" if fm else "two launches"),
                    "l2": "flushed before every layer call (256 MB write, then a 256 MB read of another buffer so "
                          "no dirty lines remain); flush outside the timed CUDA-event intervals",
                    "timing": "CUDA events on the launch stream around each plain moe_forward call; kernel times from "
@@ -756,13 +762,16 @@ def prefill_section(args, wl, layer, fwd, flush_l2, stream, gpu_index, world, d1
             "T": T, "experts_touched": touched, "calls_timed": n_calls,
             "us_median": round(med_ms * 1e3, 2), "us_mean": round(sum(calls) / len(calls) * 1e3, 2),
             "us_min": round(min(calls) * 1e3, 2), "tokens_per_s": round(world * T / (ms_max * 1e-3), 1),
+            # the first `steps` calls, before a sustained load meets the power cap
+            "us_median_first_calls": round(statistics.median(calls[: args.steps]) * 1e3, 2),
             "layer_tflops": round(layer_tf, 2), "layer_frac_of_peak": round(layer_tf / peak_b, 4),
             "layer_frac_of_sustained": round(layer_tf / peak_s, 4),
             "flops": {n: int(v) for n, v in fl.items()},
             "kernel_us_median": {n: round(statistics.median(v) * 1e3, 2) for n, v in kern.items()},
             "roofline": roof, "clocks": clocks,
-            "timing": "flushed calls (256 MB write + 256 MB read before each), CUDA events on the launch stream; "
-                      "kernel times from a second pass through moe_forward_events"}
+            "timing": "flushed calls (256 MB write + 256 MB read before each), CUDA events on the launch stream, "
+                      "back to back for >= 2.5 s (us_median over all of them, sustained; us_median_first_calls over "
+                      "the first `steps`); kernel times from a second pass through moe_forward_events"}
 
 
 def main():
@@ -790,10 +799,12 @@ def main():
                     help="time moe_forward_fused_front (norm .. gather in one cluster launch; T <= 64)")
     ap.add_argument("--fused-combine", action="store_true",
                     help="time moe_forward_fused_combine (the combine in the down GEMM's epilogue)")
+    ap.add_argument("--fused-mlp", action="store_true",
+                    help="time moe_forward_fused_mlp (both expert GEMMs in one launch; decode tile plan)")
     args = ap.parse_args()
-    if sum([args.mx, args.mxfp4, args.mxfp4a4, args.nvfp4, args.fused_front, args.fused_combine]) > 1:
-        ap.error("--mx, --mxfp4, --mxfp4a4, --nvfp4, --fused-front and --fused-combine are separate entry points; "
-                 "pick one")
+    if sum([args.mx, args.mxfp4, args.mxfp4a4, args.nvfp4, args.fused_front, args.fused_combine, args.fused_mlp]) > 1:
+        ap.error("--mx, --mxfp4, --mxfp4a4, --nvfp4, --fused-front, --fused-combine and --fused-mlp are separate entry "
+                 "points; pick one")
     if args.warmup < 3:
         print("bench: at least 3 warm-up steps are required; using 3", file=sys.stderr)
         args.warmup = 3

@@ -143,8 +143,9 @@ MOE_API moe_status moe_kernels_per_call(const moe_shape* shape, int32_t* count);
  * (moe_forward_fused_front), MOE_CALL_FORWARD_MX (moe_forward_mx),
  * MOE_CALL_FORWARD_FUSED_COMBINE (moe_forward_fused_combine),
  * MOE_CALL_FORWARD_MXFP4 (moe_forward_mxfp4), MOE_CALL_FORWARD_MXFP4A4
- * (moe_forward_mxfp4a4) or MOE_CALL_FORWARD_NVFP4 (moe_forward_nvfp4).
- * Another value of call: MOE_ERR_INVALID_ARG.  Host-only. */
+ * (moe_forward_mxfp4a4), MOE_CALL_FORWARD_NVFP4 (moe_forward_nvfp4) or
+ * MOE_CALL_FORWARD_FUSED_MLP (moe_forward_fused_mlp; MOE_ERR_UNSUPPORTED for
+ * shapes it refuses).  Another value of call: MOE_ERR_INVALID_ARG.  Host-only. */
 #define MOE_CALL_FORWARD 0
 #define MOE_CALL_FORWARD_FUSED_FRONT 1
 #define MOE_CALL_FORWARD_MX 2
@@ -152,6 +153,7 @@ MOE_API moe_status moe_kernels_per_call(const moe_shape* shape, int32_t* count);
 #define MOE_CALL_FORWARD_MXFP4 4
 #define MOE_CALL_FORWARD_MXFP4A4 5
 #define MOE_CALL_FORWARD_NVFP4 6
+#define MOE_CALL_FORWARD_FUSED_MLP 7
 MOE_API moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t* count);
 
 /* moe_forward, plus CUDA events recorded on `stream` around the kernels:
@@ -209,6 +211,25 @@ MOE_API moe_status moe_forward_fused_combine(const moe_shape* shape, const moe_b
                                              const moe_bf16* w2, moe_bf16* y, void* workspace,
                                              size_t workspace_bytes, moe_stream_t stream, void* const* events,
                                              int32_t n_events);
+
+/* moe_forward with both expert GEMMs in one persistent launch (the GEMM ->
+ * GEMM fusion of "4 · La fusion de noyaux", §4.2 "GEMM + GEMM", grown into
+ * the megakernel of §4.6): every CTA runs its stream-K share of the gate/up
+ * GEMM, then its share of the down GEMM; a down-GEMM unit loads its
+ * activation rows once every gate/up unit of its expert and token chunk has
+ * counted the stores of its four epilogue warps in a per-chunk counter of the
+ * workspace (zeroed by the align kernel; release add, acquire poll, proxy
+ * fence before the TMA reads), while its weight tiles stream in ahead.  Same
+ * K split as moe_forward, so the same output bits.  Decode tile plan only
+ * (T * top_k <= 16 * E), else MOE_ERR_UNSUPPORTED before anything is
+ * enqueued.  `events` as for moe_forward_events (events[6] then follows
+ * events[5] at once).  moe_forward stays the faster choice on GB300: the
+ * launch boundary saved (~4 us) is lost again because the fused kernel's
+ * gate/up phase runs slower than the separate gate/up kernel. */
+MOE_API moe_status moe_forward_fused_mlp(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                                         const float* w_router, const float* router_bias, const moe_bf16* w13,
+                                         const moe_bf16* w2, moe_bf16* y, void* workspace, size_t workspace_bytes,
+                                         moe_stream_t stream, void* const* events, int32_t n_events);
 
 /* Routing front end only (RMSNorm, router, top-k, align with `pad_rows`
  * rows of padding granularity), with the results copied out:
@@ -416,7 +437,9 @@ MOE_API moe_status moe_forward_mxfp4(const moe_shape* shape, const moe_bf16* x, 
  * input rows and its SwiGLU activations quantized to MXFP4 by the same rule
  * as the weights, and both expert GEMMs on packed E2M1 operands (tcgen05.mma
  * kind::mxf4, two E8M0 scales per row per MMA of K = 64, fp32 accumulation).
- * H and I multiples of 256 (else MOE_ERR_UNSUPPORTED); weight codes 32-byte
+ * H and I multiples of 128 like every block-scaled layer (else
+ * MOE_ERR_UNSUPPORTED; a GEMM stage covers 256 elements of K, and an odd
+ * multiple of 128 ends half way into the last one); weight codes 32-byte
  * aligned. */
 MOE_API moe_status moe_forward_mxfp4a4(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
                                        const float* w_router, const float* router_bias, const uint8_t* w13_codes,
@@ -457,7 +480,7 @@ MOE_API moe_status moe_nvfp4_quantize_weights(const moe_shape* shape, const moe_
  * activations (tcgen05.mma kind::mxf4nvf4, scale_vec::4X: four E4M3 scales per
  * row per MMA of K = 64; the fp32 tensor scales of the expert matrix and of the
  * token row multiply each accumulator in the epilogue), one CTA per work unit
- * in every tile plan.  H and I multiples of 256 (else MOE_ERR_UNSUPPORTED). */
+ * in every tile plan.  H and I multiples of 128 (else MOE_ERR_UNSUPPORTED). */
 MOE_API moe_status moe_forward_nvfp4(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
                                      const float* w_router, const float* router_bias, const uint8_t* w13_codes,
                                      const uint8_t* w13_scales, const float* w13_gscale, const uint8_t* w2_codes,

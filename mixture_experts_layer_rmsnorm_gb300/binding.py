@@ -91,6 +91,7 @@ def load(build: bool = True):
             lib.moe_forward_nvfp4.argtypes = [sp, p, p, p, p, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_forward_fused_front.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_forward_fused_combine.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
+            lib.moe_forward_fused_mlp.argtypes = [sp, p, p, p, p, p, p, p, p, sz, p, p, i32]
             lib.moe_status_string.argtypes = [ctypes.c_int]
             lib.moe_status_string.restype = ctypes.c_char_p
             for f in ("moe_workspace_size", "moe_forward", "moe_forward_events", "moe_route_debug",
@@ -102,7 +103,7 @@ def load(build: bool = True):
                       "moe_workspace_views_mx", "moe_forward_mx", "moe_forward_fused_combine",
                       "moe_mxfp4_weight_sizes", "moe_mxfp4_quantize_weights", "moe_forward_mxfp4",
                       "moe_forward_mxfp4a4", "moe_nvfp4_weight_sizes", "moe_nvfp4_quantize_weights",
-                      "moe_forward_nvfp4"):
+                      "moe_forward_nvfp4", "moe_forward_fused_mlp"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -142,7 +143,8 @@ def moe_kernels_per_call(s: MoeShape) -> tuple[int, int]:
 
 
 (MOE_CALL_FORWARD, MOE_CALL_FORWARD_FUSED_FRONT, MOE_CALL_FORWARD_MX, MOE_CALL_FORWARD_FUSED_COMBINE,
- MOE_CALL_FORWARD_MXFP4, MOE_CALL_FORWARD_MXFP4A4, MOE_CALL_FORWARD_NVFP4) = 0, 1, 2, 3, 4, 5, 6
+ MOE_CALL_FORWARD_MXFP4, MOE_CALL_FORWARD_MXFP4A4, MOE_CALL_FORWARD_NVFP4, MOE_CALL_FORWARD_FUSED_MLP) = \
+    0, 1, 2, 3, 4, 5, 6, 7
 
 
 def moe_kernels_per_call_of(s: MoeShape, call: int) -> tuple[int, int]:
@@ -190,6 +192,17 @@ def moe_forward_fused_combine(s: MoeShape, x, g_norm, w_router, router_bias, w13
         arr, n = (ctypes.c_void_p * len(events))(*events), len(events)
     return load().moe_forward_fused_combine(ctypes.byref(s), x, g_norm, w_router, router_bias, w13, w2, y,
                                             workspace, workspace_bytes, stream, arr, n)
+
+
+def moe_forward_fused_mlp(s: MoeShape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes,
+                          stream, events=None) -> int:
+    """moe_forward with both expert GEMMs in one launch (decode tile plan only)."""
+    if events is None:
+        arr, n = None, 0
+    else:
+        arr, n = (ctypes.c_void_p * len(events))(*events), len(events)
+    return load().moe_forward_fused_mlp(ctypes.byref(s), x, g_norm, w_router, router_bias, w13, w2, y, workspace,
+                                        workspace_bytes, stream, arr, n)
 
 
 def moe_static_scratch_bytes() -> tuple[int, int]:
@@ -370,12 +383,13 @@ class MoeLayer:
             raise MoeError(st, "moe_workspace_size")
         return n
 
-    def forward(self, x, y=None, stream=None, events=None, fused_front=False, fused_combine=False):
+    def forward(self, x, y=None, stream=None, events=None, fused_front=False, fused_combine=False, fused_mlp=False):
         """y = layer(x).  events: optional MOE_NUM_KERNELS + 1 cudaEvent_t handles
         recorded around the kernels (moe_forward_events).  fused_front: run the
         norm .. gather steps as one cluster launch (moe_forward_fused_front).
         fused_combine: the combine in the down GEMM's epilogue
-        (moe_forward_fused_combine)."""
+        (moe_forward_fused_combine).  fused_mlp: both expert GEMMs in one
+        launch (moe_forward_fused_mlp; decode tile plan only)."""
         import torch
         T = x.shape[0]
         self.ensure_capacity(T)
@@ -384,9 +398,11 @@ class MoeLayer:
         s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
         args = (self.shape(T), _ptr(x), _ptr(self.g_norm), _ptr(self.w_router), _ptr(self.bias), _ptr(self.w13),
                 _ptr(self.w2), _ptr(y), _ptr(self.workspace), self.workspace_bytes(T), s)
-        if fused_front and fused_combine:
-            raise ValueError("fused_front and fused_combine are separate entry points")
-        if fused_front:
+        if int(fused_front) + int(fused_combine) + int(fused_mlp) > 1:
+            raise ValueError("fused_front, fused_combine and fused_mlp are separate entry points")
+        if fused_mlp:
+            st = moe_forward_fused_mlp(*args, events)
+        elif fused_front:
             st = moe_forward_fused_front(*args, events)
         elif fused_combine:
             st = moe_forward_fused_combine(*args, events)

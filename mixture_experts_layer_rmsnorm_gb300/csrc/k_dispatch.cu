@@ -23,26 +23,26 @@
 namespace moe {
 namespace {
 
-constexpr int kAlignThreads = 1024;
-constexpr int kAlignWarps = kAlignThreads / 32;
-
-// One CTA of 1024 threads.  Dynamic shared memory: cnt[E], cursor[E],
-// wbase[E][32] (ints), and ids_s[N] in the fused form.  With FUSED_TOPK the CTA
-// first selects the top-k experts of all T tokens from the logits (one warp
-// per token; used for small T, where a separate launch costs more than the
-// work), keeps a copy of the ids in shared memory and aligns from it.
-// Otherwise the routing ids are read with L2-coherent loads.
-template <int FUSED_VPL>  // 0: ids given; else top-k first, with FUSED_VPL logits per lane
-__global__ void __launch_bounds__(kAlignThreads)
+// One CTA of NT threads: 1024, or 256 for a handful of tokens (one warp per
+// token still covers them in one round, and the block's barriers are
+// cheaper).  Dynamic shared memory: cnt[E], cursor[E], wbase[E][NT/32]
+// (ints), and ids_s[N] in the fused form.  With FUSED_TOPK the CTA first
+// selects the top-k experts of all T tokens from the logits (one warp per
+// token; used for small T, where a separate launch costs more than the work),
+// keeps a copy of the ids in shared memory and aligns from it.  Otherwise the
+// routing ids are read with L2-coherent loads.
+template <int FUSED_VPL, int NT>  // FUSED_VPL 0: ids given; else top-k first, with FUSED_VPL logits per lane
+__global__ void __launch_bounds__(NT)
     align_kernel(const float* __restrict__ logits, int T, int k, int renorm, float* __restrict__ topk_w,
                  int32_t* ids, int N, int E, int pad, int bn1, int tiles1, int bn2, int tiles2,
                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_ids,
                  int32_t* __restrict__ slot_of, int32_t* __restrict__ unit_off1, int32_t* __restrict__ unit_off2,
                  int32_t* __restrict__ err, int32_t* __restrict__ flags, int n_flags) {
+  constexpr int kAlignThreads = NT, kAlignWarps = NT / 32;
   extern __shared__ int sm[];
   int* cnt = sm;                 // [E]
   int* cursor = sm + E;          // [E]
-  int* wbase = sm + 2 * E;       // [E][32]
+  int* wbase = sm + 2 * E;       // [E][NT / 32]
   int* ids_s = wbase + kAlignWarps * E;  // [N], fused form only
   __shared__ int scan_tmp[3 * 33];
   __shared__ int bad;
@@ -173,20 +173,37 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 
 }  // namespace
 
+template <int VPL, int NT>
+cudaError_t launch_align_nt(const float* logits, int T, int k, int renorm, int32_t* topk_ids, float* topk_w, int N,
+                            int E, int pad, int bn1, int tiles1, int bn2, int tiles2, int32_t* counts,
+                            int32_t* offsets, int32_t* sorted_ids, int32_t* slot_of, int32_t* unit_off1,
+                            int32_t* unit_off2, int32_t* err, int32_t* flags, int n_flags, cudaStream_t stream) {
+  const size_t smem = (static_cast<size_t>(2 + NT / 32) * E + (VPL > 0 ? N : 0)) * sizeof(int);
+  static PerDevice config;
+  const cudaError_t e = config.get([](int&) {
+    return cudaFuncSetAttribute(align_kernel<VPL, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+  });
+  if (e != cudaSuccess) return e;
+  return launch_pdl(align_kernel<VPL, NT>, dim3(1), dim3(NT), smem, stream, logits, T, k, renorm, topk_w, topk_ids, N,
+                    E, pad, bn1, tiles1, bn2, tiles2, counts, offsets, sorted_ids, slot_of, unit_off1, unit_off2, err,
+                    flags, n_flags);
+}
+
+// 256 threads for up to 8 tokens (E <= 256: one thread per expert in the
+// align's scans), else 1024
+constexpr int kAlignSmallT = 8;
 template <int VPL>
 cudaError_t launch_align_t(const float* logits, int T, int k, int renorm, int32_t* topk_ids, float* topk_w, int N,
                            int E, int pad, int bn1, int tiles1, int bn2, int tiles2, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_ids, int32_t* slot_of, int32_t* unit_off1, int32_t* unit_off2,
                            int32_t* err, int32_t* flags, int n_flags, cudaStream_t stream) {
-  const size_t smem = (static_cast<size_t>(2 + kAlignWarps) * E + (VPL > 0 ? N : 0)) * sizeof(int);
-  static PerDevice config;
-  const cudaError_t e = config.get([](int&) {
-    return cudaFuncSetAttribute(align_kernel<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-  });
-  if (e != cudaSuccess) return e;
-  return launch_pdl(align_kernel<VPL>, dim3(1), dim3(kAlignThreads), smem, stream, logits, T, k, renorm, topk_w,
-                    topk_ids, N, E, pad, bn1, tiles1, bn2, tiles2, counts, offsets, sorted_ids, slot_of, unit_off1,
-                    unit_off2, err, flags, n_flags);
+  if (VPL > 0 && T <= kAlignSmallT && E <= 256)
+    return launch_align_nt<VPL, 256>(logits, T, k, renorm, topk_ids, topk_w, N, E, pad, bn1, tiles1, bn2, tiles2,
+                                     counts, offsets, sorted_ids, slot_of, unit_off1, unit_off2, err, flags, n_flags,
+                                     stream);
+  return launch_align_nt<VPL, 1024>(logits, T, k, renorm, topk_ids, topk_w, N, E, pad, bn1, tiles1, bn2, tiles2,
+                                    counts, offsets, sorted_ids, slot_of, unit_off1, unit_off2, err, flags, n_flags,
+                                    stream);
 }
 
 

@@ -144,7 +144,6 @@ struct GemmCfg {
   // offsets and the unit prefix sums (of both GEMMs in the fused kernel)
   static constexpr int kTabBytes = PAIR ? 0 : (FUSED ? 3 : 2) * (kTabMaxE + 1) * 4;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes + kTabBytes;
-  static constexpr int kFeatPerTile = SWIGLU ? kGateUpTileFeat : kDownTileFeat;  // output features per unit
   static_assert(BN % TOKBOX == 0 && TOKBOX % 16 == 0 && BN >= 16 && BN <= 256, "token tile");
   static_assert(!PAIR || (BN / 2) % TOKBOX == 0, "token boxes of a CTA pair");
   static_assert(!MX || (PAIR ? (BN == 256 || BN == 128) : (BN % 32 == 0 && BN <= 128)),
@@ -444,9 +443,16 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
   const uint32_t tmem_base = *tmem_slot;
 
   const int total_units = t_unit[args.E];
-  const int kblocks = args.K / C::kKPerStage;
+  // stages along K; with packed E2M1 operands (256 elements of K per stage)
+  // K may end half way into the last stage: its box reads zero codes past K,
+  // and only its valid scale tiles are loaded and its valid MMAs issued
+  const int kblocks = (args.K + C::kKPerStage - 1) / C::kKPerStage;
   const int total_units2 = FUSED ? t_unit2[args.E] : 0;
   const int kblocks2 = FUSED ? args2.K / C::kKPerStage : 1;
+  // block-scaled GEMMs: scale tiles per 128-row group along K (one per
+  // kKPerStage / kChunks elements), and the valid ones in stage kb
+  const int sf_tiles_k = args.K / (C::kKPerStage / C::kChunks);
+  auto valid_chunks = [&](int kb) { return min(C::kChunks, sf_tiles_k - kb * C::kChunks); };
   const int ctas = workers;
   // per phase: its GEMM's arguments, unit table, kind and output features per unit
   auto gemm_args = [&](int ph) -> const ExpertGemmArgs& { return (FUSED && ph) ? args2 : args; };
@@ -478,13 +484,17 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
       // their rows exist: the gate/up GEMM's token rows until the previous
       // kernel has completed (pdl_wait), so the first ring-full of stages gets
       // its weight tiles at once and its token rows after; in the fused
-      // kernel, a down-GEMM stage's activation rows until the gate/up unit
-      // that writes them (same expert and token chunk, weight tile = the
-      // stage's K block) has counted the stores of its four epilogue warps.
+      // kernel, a down-GEMM stage's activation rows until every gate/up unit
+      // of the same expert and token chunk has counted the stores of its four
+      // epilogue warps (one counter per chunk, checked once per segment: a
+      // poll per stage, an L2 round trip, would hold the producer back).
       bool deps_ready = false;
       int n_pend = 0, pend_head = 0;
-      int pend_stage[STAGES], pend_kb[STAGES], pend_tok0[STAGES], pend_rows[STAGES], pend_chunk[STAGES];
-      int pend_ready[STAGES];  // fused kernel: the awaited gate/up unit of a down-GEMM stage, or -1
+      int pend_stage[STAGES] = {}, pend_kb[STAGES] = {}, pend_tok0[STAGES] = {}, pend_rows[STAGES] = {},
+          pend_chunk[STAGES] = {};
+      int pend_ready[STAGES] = {};  // fused kernel: the token chunk a down-GEMM stage awaits, or -1
+      int chunk_seen_ready = -1;  // the last chunk found complete
+      const int chunk_need = C::kEpiWarps * args.tiles_per_expert;
       // a CTA pair signals every load on the even CTA's full barrier
       const uint32_t full_cl = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;
       auto load_2d = [&](void* dst, const CUtensorMap* map, int st, int c0, int c1, uint64_t pol) {
@@ -511,21 +521,21 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
           // and 128-element K chunk; tile (h, c) at 512 (c G + h)), in each CTA
           // (tensor map tm_sx: one tile = a box of 2 rows x 256 bytes)
           constexpr int G = C::kSfTokTiles;
-          for (int c = 0; c < C::kChunks; ++c)
+          for (int c = 0; c < valid_chunks(kb); ++c)
             for (int h = 0; h < G; ++h)
               load_2d(sb + C::kBBytes + C::kSfWBytes + 512 * (c * G + h), &tm_sx, st, 0,
-                      2 * (((G * chunk + h) * kblocks + kb) * C::kChunks + c), pol_x);
+                      2 * ((G * chunk + h) * sf_tiles_k + kb * C::kChunks + c), pol_x);
         } else if (MX) {  // one tile per K chunk, the chunks of a stage adjacent
           bulk_load(sb + C::kBBytes + C::kSfWBytes,
-                    args.x_scales + (static_cast<size_t>(chunk) * kblocks + kb) * C::kChunks * 512,
-                    512 * C::kChunks, &full[st], pol_x);
+                    args.x_scales + (static_cast<size_t>(chunk) * sf_tiles_k + kb * C::kChunks) * 512,
+                    512 * valid_chunks(kb), &full[st], pol_x);
         }
       };
       // fused kernel: a down-GEMM stage's activation rows (written by this
-      // kernel's gate/up epilogues through the generic proxy, read here by TMA)
+      // kernel's gate/up epilogues through the generic proxy, read here by TMA
+      // after head_ready's acquire and proxy fence)
       auto load_act = [&](int st, int kb, int tok0, int rows) {
         uint8_t* sb = smem + st * C::kStageBytes + kABytes;
-        fence_proxy_async_global();
         for (int r = 0; r < rows; r += TOKBOX) tma_load_2d(sb + r * kTokRowBytes, &tm_sx, &full[st], kb * C::kBoxX,
                                                            tok0 + r, pol_x);
       };
@@ -550,14 +560,19 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
           if (!wait && !(FUSED && r >= 0)) return false;
           resolve_deps();
         }
-        if (!FUSED || r < 0) return true;
-        if (ld_acquire(args.ready + r) >= C::kEpiWarps) return true;
-        if (!wait) return false;
-        const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire(args.ready + r) < C::kEpiWarps) {
-          if (*abort_flag || globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
-          __nanosleep(64);
+        if (!FUSED || r < 0 || r == chunk_seen_ready) return true;
+        if (ld_acquire(args.ready + r) < chunk_need) {
+          if (!wait) return false;
+          const uint64_t t0 = globaltimer_ns();
+          // (up to one producer per SM polls the same few counters: a slow
+          // poll keeps them from crowding the L2 slices the weights stream through)
+          while (ld_acquire(args.ready + r) < chunk_need) {
+            if (*abort_flag || globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+            __nanosleep(1000);
+          }
         }
+        fence_proxy_async_global();  // the TMA reads that follow see what the acquire saw
+        chunk_seen_ready = r;
         return true;
       };
       Work rg(total_units, kblocks, total_units2, kblocks2, worker, ctas, args.stream_k != 0);
@@ -576,15 +591,13 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
         const int tok_rows = (half + TOKBOX - 1) / TOKBOX * TOKBOX;  // whole boxes; rows past n are unused
         const bool reused = t_off[un.e + 1] - t_off[un.e] > BN;
         const uint64_t pol_w = reused ? pol_keep : pol_stream;
-        const uint32_t bytes = C::kWTxBytes + tok_rows * kTokRowBytes + C::kSfBytes;  // per CTA (both of a pair)
+        // per CTA (both of a pair); scale bytes of a full stage: C::kSfBytes
+        const uint32_t bytes_base = C::kWTxBytes + tok_rows * kTokRowBytes;
         const int chunk = MX ? t_unit[un.e] / args.tiles_per_expert + (un.tok0 - t_off[un.e]) / BN : 0;
-        // fused kernel, down GEMM: K block kb of this unit is gate/up unit
-        // (expert, tile kb, the same token chunk) = rd_base + kb * chunks
-        int rd_base = -1, rd_step = 0;
-        if (FUSED && ph == 1) {
-          rd_step = (t_unit[un.e + 1] - t_unit[un.e]) / args.tiles_per_expert;
-          rd_base = t_unit[un.e] + (un.tok0 - t_off[un.e]) / BN;
-        }
+        // fused kernel, down GEMM: the token chunk (expert, rows [tok0, tok0 + BN))
+        // whose activation rows this unit reads, numbered over all experts
+        const int rd_chunk = (FUSED && ph == 1) ? t_unit[un.e] / args.tiles_per_expert + (un.tok0 - t_off[un.e]) / BN
+                                                : -1;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (n_pend == STAGES) {  // the slot about to be refilled still waits for its token rows
             if (!head_ready(true)) {
@@ -592,7 +605,9 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
               where = kWaitActReady;
               break;
             }
-            issue_head();
+            do {  // it, and every later one whose rows now exist too
+              issue_head();
+            } while (n_pend > 0 && head_ready(false));
           }
           if (!mbar_wait(&empty[stage], phase ^ 1u, kWaitTimeoutNs, abort_flag)) {
             ok = false;
@@ -600,6 +615,8 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
             break;
           }
           uint8_t* sa = smem + stage * C::kStageBytes;
+          const uint32_t bytes =
+              bytes_base + (MX ? static_cast<uint32_t>(valid_chunks(kb)) * 512u * (1u + C::kSfTokTiles) : 0u);
           if (!PAIR)
             mbar_arrive_expect_tx(&full[stage], bytes);
           else if (leader)
@@ -611,24 +628,32 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
           }
           if (MX) {  // the weight tile's scales (static: loaded before the parent kernel ends)
             const int wtiles = PAIR ? 2 * args.tiles_per_expert : args.tiles_per_expert;  // 128-row tiles per expert
-            const int64_t wt = (static_cast<int64_t>(un.e * wtiles + tile) * kblocks + kb) * C::kChunks;
+            const int64_t wt = static_cast<int64_t>(un.e * wtiles + tile) * sf_tiles_k + kb * C::kChunks;
             if (PAIR) {
-              for (int c = 0; c < C::kChunks; ++c)
+              for (int c = 0; c < valid_chunks(kb); ++c)
                 load_2d(sa + kABytes + C::kBBytes + 512 * c, &tm_sw, stage, 0, static_cast<int>(2 * (wt + c)), pol_w);
             } else {
-              bulk_load(sa + kABytes + C::kBBytes, args.w_scales + static_cast<size_t>(wt) * 512, 512 * C::kChunks,
-                        &full[stage], pol_w);
+              bulk_load(sa + kABytes + C::kBBytes, args.w_scales + static_cast<size_t>(wt) * 512,
+                        512 * valid_chunks(kb), &full[stage], pol_w);
             }
           }
-          const int slot = (pend_head + n_pend) % STAGES;
-          pend_stage[slot] = stage;
-          pend_kb[slot] = kb;
-          pend_tok0[slot] = tok_first;
-          pend_rows[slot] = tok_rows;
-          pend_chunk[slot] = chunk;
-          pend_ready[slot] = rd_base >= 0 ? rd_base + kb * rd_step : -1;
-          ++n_pend;
-          while (n_pend > 0 && head_ready(false)) issue_head();
+          if (n_pend == 0 && deps_ready && (rd_chunk < 0 || rd_chunk == chunk_seen_ready)) {
+            // the rows exist and nothing waits ahead of them: load them now
+            if (rd_chunk >= 0)
+              load_act(stage, kb, tok_first, tok_rows);
+            else
+              load_tokens(stage, kb, tok_first, tok_rows, chunk);
+          } else {
+            const int slot = pend_head + n_pend < STAGES ? pend_head + n_pend : pend_head + n_pend - STAGES;
+            pend_stage[slot] = stage;
+            pend_kb[slot] = kb;
+            pend_tok0[slot] = tok_first;
+            pend_rows[slot] = tok_rows;
+            pend_chunk[slot] = chunk;
+            pend_ready[slot] = rd_chunk;
+            ++n_pend;
+            while (n_pend > 0 && head_ready(false)) issue_head();
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -725,8 +750,10 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
                   tmem_cp_32x128b_x4(sfb_t + 4 * (c * G + h), src);
               }
             }
+            const int n_k = 4 * valid_chunks(kb) / C::kChunks;  // MMAs over K inside the stage
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
+              if (k >= n_k) break;
               const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
               const uint64_t ad = sdesc_kmajor_sw128(sa + k * 32), bd = sdesc_kmajor_sw128(sb + k * 32);
               if (NV) {  // MMA k: K elements 64k .. 64k+63 = tile k, its 4 scales one word
@@ -984,13 +1011,15 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
             for (int c = blockIdx.x + 1; c <= c_last; ++c) A.flags[c * 4 + q] = 0;
         }
         // fused kernel: the unit's activation rows of this lane quarter are
-        // stored; count this warp in the unit's counter (the down GEMM's
-        // producers wait for all four, then read the rows by TMA)
+        // stored; count this warp in its token chunk's counter (the down
+        // GEMM's producers wait for four per weight tile, then read the rows
+        // by TMA)
         if (FUSED && ph == 0 && ok) {
           fence_proxy_async_global();
           __threadfence();
           __syncwarp();
-          if (lane == 0) red_release_add(args.ready + u, 1);
+          if (lane == 0)
+            red_release_add(args.ready + t_unit[un.e] / args.tiles_per_expert + (un.tok0 - t_off[un.e]) / BN, 1);
         }
       }
       if (!ok) break;

@@ -18,7 +18,7 @@
 //      the routing tables
 //   4. each CTA copies its share of the routed rows h[t] -> xg[slot].  Padding
 //      rows of xg are not written: they only feed MMA columns whose results are
-//      never stored or read.
+//      never stored or read.  (One token: no copy; the gate/up GEMM reads h.)
 // The arithmetic is that of the router kernel and the align kernels (same
 // device functions), so h, the logits, the ids and the permutation are the
 // same bits as on the multi-launch path.
@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kFrontThreads, 1) front_kernel(const __grid_co
   }
 
   // ---- 4. gather: one warp per routed row, 128-bit copies
+  if (a.skip_gather) return;
   const int nch = a.H >> 3;
   for (int i = c * kFrontWarps + warp; i < N; i += C * kFrontWarps) {
     const int p = s_slot[i];

@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
   const float six_g = __fmul_rn(6.0f, g);
   for (int c0 = 0; c0 < nch; c0 += 32) {
     const int c = c0 + lane;
-    const bool on = c < nch;  // whole lane pairs are on or off (nch is a multiple of 32 for K % 256 == 0)
+    const bool on = c < nch;  // whole lane pairs are on or off (nch is even: K is a multiple of 128)
     float x[8];
     unpack8(on && s ? *reinterpret_cast<const uint4*>(s + c * 8) : make_uint4(0, 0, 0, 0), x);
     float amax = 0.0f;

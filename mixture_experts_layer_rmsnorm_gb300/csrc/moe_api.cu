@@ -34,7 +34,7 @@ struct Layout {
       partials, xg, act, out, xs, aq, as, gx, ga, total;
   int64_t n_ccnt;      // combine arrival counters of the down GEMM: [H / 128][T]
   int64_t n_flags;     // ints at `flags` cleared by the align: stream-K flags, then (small tile plan) the
-                       // fused kernel's per-unit completion counters
+                       // fused gate/up -> down kernel's per-chunk completion counters
   int64_t P_max;       // padded rows: 16-row padding (bf16), 32-row padding rounded to 128 (MXFP8)
   int64_t sorted_cap;  // sorted_ids entries (room for debug padding up to 256)
 };
@@ -73,7 +73,7 @@ Layout make_layout(const moe_shape& s, bool mx = false) {
   L.slot = take(static_cast<size_t>(T * k * 4));
   // stream-K flags and partial sums of the expert GEMMs (slot = BN x 128 fp32 per CTA)
   const bool small = moe::choose_plan(T, k, E) == moe::GemmPlan::kSmall;
-  L.n_flags = kGemmFlagInts + (small && !mx ? moe::fused_mlp_ready_ints(L.P_max, I) : 0);
+  L.n_flags = kGemmFlagInts + (small && !mx ? moe::fused_mlp_ready_ints(L.P_max) : 0);
   L.flags = take(static_cast<size_t>(L.n_flags) * 4);
   L.n_ccnt = (H / 128) * T;
   L.ccnt = take(static_cast<size_t>(L.n_ccnt) * 4);
@@ -310,7 +310,7 @@ moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes) {
 moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t* count) {
   const moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
-  if (!count || call < MOE_CALL_FORWARD || call > MOE_CALL_FORWARD_NVFP4) return MOE_ERR_INVALID_ARG;
+  if (!count || call < MOE_CALL_FORWARD || call > MOE_CALL_FORWARD_FUSED_MLP) return MOE_ERR_INVALID_ARG;
   const moe_shape& s = *shape;
   if (s.T == 0) {
     *count = 0;
@@ -318,12 +318,15 @@ moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t
   }
   // router, top-k + align (1 kernel, or 3), gather, the two GEMMs, combine
   const int front = 1 + (moe::align_fuses_topk(s.T, s.E) ? 1 : 3) + 1;
-  const bool one_mlp = moe::fused_mlp(moe::choose_plan(s.T, s.top_k, s.E), false);  // one launch for both GEMMs
+  if (call == MOE_CALL_FORWARD_FUSED_MLP && !moe::fused_mlp_fits(moe::choose_plan(s.T, s.top_k, s.E)))
+    return MOE_ERR_UNSUPPORTED;
+  const int no_gather = moe::tokens_from_h(s.T, false) ? 1 : 0;  // one token: no gather
   if (call == MOE_CALL_FORWARD)
-    *count = front + 3 - (moe::tokens_from_h(s.T, false, false) ? 1 : 0) - (one_mlp ? 1 : 0);  // no gather for
-                                                                                                  // one token
+    *count = front + 3 - no_gather;
+  else if (call == MOE_CALL_FORWARD_FUSED_MLP)
+    *count = front + 2 - no_gather;  // both GEMMs in one launch
   else if (call == MOE_CALL_FORWARD_FUSED_FRONT)
-    *count = 1 + 3 - (one_mlp ? 1 : 0);
+    *count = 1 + 3;
   else if (call == MOE_CALL_FORWARD_MX || call == MOE_CALL_FORWARD_MXFP4 || call == MOE_CALL_FORWARD_MXFP4A4 ||
            call == MOE_CALL_FORWARD_NVFP4)
     *count = front + 4;  // + the activation quantize between the GEMMs
@@ -379,7 +382,7 @@ void set_fused_combine(moe::ExpertGemmArgs& a, const moe_shape& s, const Layout&
 moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
                         const float* router_bias, const moe_bf16* w13, const moe_bf16* w2, moe_bf16* y,
                         void* workspace, size_t workspace_bytes, moe_stream_t stream, void* const* events,
-                        bool single_launch_front, bool fused_combine) {
+                        bool single_launch_front, bool fused_combine, bool fused_mlp) {
   moe_status st = check_shape(shape);
   if (st != MOE_OK) return st;
   const moe_shape& s = *shape;
@@ -387,6 +390,8 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   st = check_inputs(shape, x, g_norm, w_router, router_bias, workspace, workspace_bytes);
   if (st != MOE_OK) return st;
   if (!w13 || !w2 || !y || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+  if (fused_mlp && (fused_combine || !moe::fused_mlp_fits(moe::choose_plan(s.T, s.top_k, s.E))))
+    return MOE_ERR_UNSUPPORTED;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int num_sms = num_sms_of_current_device();
   if (num_sms <= 0) return MOE_ERR_CUDA;
@@ -404,7 +409,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   // One token: every expert's list is that token's row of h (padded to 16
   // rows), so the gate/up GEMM reads its token tiles straight from h, rows
   // past T reading as zeros, and no gather runs.
-  const bool tokens_from_h = moe::tokens_from_h(s.T, single_launch_front, fused_combine);
+  const bool tokens_from_h = moe::tokens_from_h(s.T, fused_combine);
   CUtensorMap tm_w13, tm_xg, tm_w2, tm_act;
   if (!make_map_gate_up(&tm_w13, w13, s.H, s.I, s.E) ||
       !(tokens_from_h ? make_map(&tm_xg, at<void>(workspace, L.h), s.H, s.T, moe::gemm_tok_box_rows(plan))
@@ -451,6 +456,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
     fa.combine_cnt = at<int32_t>(workspace, L.ccnt);
     fa.n_combine_cnt = fused_combine ? static_cast<int>(L.n_ccnt) : 0;
     fa.xg = at<uint16_t>(workspace, L.xg);
+    fa.skip_gather = tokens_from_h;
     if (moe::launch_front(fa, cs) != cudaSuccess || !mark(1) || !mark(2) || !mark(3) || !mark(4))
       return MOE_ERR_CUDA;
   } else {
@@ -526,7 +532,8 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a2.stream_k = plan == GemmPlan::kSmall;
   a2.pair = moe::gemm_uses_pairs(plan, tiles2);
   if (fused_combine) set_fused_combine(a2, s, L, workspace, y);
-  if (moe::fused_mlp(plan, fused_combine)) {
+
+  if (fused_mlp) {
     // both GEMMs in one launch (events[6] then follows events[5] at once)
     if (moe::launch_gemm_fused_mlp(tm_w13, tm_xg, tm_w2, tm_act, a1, a2, num_sms, cs) != cudaSuccess || !mark(5) ||
         !mark(6))
@@ -549,8 +556,8 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
 // The block-scaled layers: the bf16 layer's routing, then quantized token
 // rows and weights in block-scaled tcgen05 GEMMs.  kind: MXFP8 weights and
 // tokens (kW8A8), MXFP4 weights with MXFP8 tokens (kW4A8), or MXFP4 weights
-// and tokens (kW4A4: packed codes, 256 elements of K per GEMM stage, so H and
-// I multiples of 256).
+// and tokens (kW4A4: packed codes, 256 elements of K per GEMM stage; H or I
+// an odd multiple of 128 ends half way into a GEMM's last stage).
 moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
                            const float* router_bias, const uint8_t* w13c, const uint8_t* w13s, const uint8_t* w2c,
                            const uint8_t* w2s, moe_bf16* y, void* workspace, size_t workspace_bytes,
@@ -564,7 +571,6 @@ moe_status forward_mx_impl(const moe_shape* shape, const moe_bf16* x, const moe_
   if (s.E > 256) return MOE_ERR_UNSUPPORTED;
   const bool fp4 = kind != MxKind::kW8A8, nv = kind == MxKind::kNV4;
   const bool a4 = kind == MxKind::kW4A4 || nv;  // packed E2M1 token codes too
-  if (a4 && (s.H % 256 != 0 || s.I % 256 != 0)) return MOE_ERR_UNSUPPORTED;
   if (nv && (!w13g || !w2g || !aligned(w13g, 4) || !aligned(w2g, 4))) return MOE_ERR_INVALID_ARG;
   st = check_inputs(shape, x, g_norm, w_router, router_bias, workspace, workspace_bytes, true);
   if (st != MOE_OK) return st;
@@ -909,6 +915,19 @@ moe_status moe_forward_fused_front(const moe_shape* shape, const moe_bf16* x, co
   }
   return moe::forward_impl(shape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes, stream,
                            events, true);
+}
+
+moe_status moe_forward_fused_mlp(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,
+                                 const float* w_router, const float* router_bias, const moe_bf16* w13,
+                                 const moe_bf16* w2, moe_bf16* y, void* workspace, size_t workspace_bytes,
+                                 moe_stream_t stream, void* const* events, int32_t n_events) {
+  if (events) {
+    if (n_events < MOE_NUM_KERNELS + 1) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i <= MOE_NUM_KERNELS; ++i)
+      if (!events[i]) return MOE_ERR_INVALID_ARG;
+  }
+  return moe::forward_impl(shape, x, g_norm, w_router, router_bias, w13, w2, y, workspace, workspace_bytes, stream,
+                           events, false, false, true);
 }
 
 moe_status moe_forward_fused_combine(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm,

@@ -12,9 +12,11 @@ namespace moe {
 // router, top-k, align and gather run as one cluster launch; shapes that do
 // not fit it return MOE_ERR_UNSUPPORTED before anything is enqueued.  With
 // fused_combine, the top-k weighted combine runs in the down GEMM's epilogue.
+// With fused_mlp, both expert GEMMs run as one launch (small tile plan only,
+// else MOE_ERR_UNSUPPORTED).
 moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf16* g_norm, const float* w_router,
                         const float* router_bias, const moe_bf16* w13, const moe_bf16* w2, moe_bf16* y,
                         void* workspace, size_t workspace_bytes, moe_stream_t stream, void* const* events,
-                        bool single_launch_front = false, bool fused_combine = false);
+                        bool single_launch_front = false, bool fused_combine = false, bool fused_mlp = false);
 
 }  // namespace moe

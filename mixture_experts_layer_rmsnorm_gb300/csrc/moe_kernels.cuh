@@ -79,6 +79,7 @@ struct FrontArgs {
   int32_t* combine_cnt;  // the down GEMM's combine arrival counters: zeroed
   int n_combine_cnt;
   uint16_t* xg;
+  int skip_gather;  // 1: no gather (one token: the gate/up GEMM reads h itself)
   // set by the launcher: router work items = token tiles x expert groups
   int n_items, groups, experts_per_item;
 };
@@ -114,8 +115,8 @@ struct ExpertGemmArgs {
   int tables_from_parent;   // 1: the routing tables come from the previous kernel (wait before reading)
   int tokens_from_h;        // 1 (one token, gate/up GEMM): tm_x maps h itself; every unit's token rows start
                             // at h row 0 (rows past T are read as zeros)
-  int32_t* ready;           // fused gate/up -> down kernel: per gate/up unit, the epilogue warps that have
-                            // stored its activation rows (zero on entry)
+  int32_t* ready;           // fused gate/up -> down kernel: per token chunk, the gate/up epilogue warps that
+                            // have stored their activation rows of it (zero on entry)
   const uint8_t* w_scales;  // MXFP8 GEMMs: weight scales (512-byte tiles per 128 rows x 128 of K)
   const uint8_t* x_scales;  // MXFP8 GEMMs: token scales, one 512-byte tile per token chunk and 128 of K
   const float* w_gscale;    // NVFP4 GEMMs: fp32 tensor scale per expert matrix [E]
@@ -144,16 +145,14 @@ inline GemmPlan choose_plan(int64_t T, int64_t top_k, int64_t E) {
   return T * top_k <= 16 * E ? GemmPlan::kSmall : GemmPlan::kLarge;
 }
 
-// Whether a moe_forward call runs both expert GEMMs as one launch
-// (launch_gemm_fused_mlp): the small tile plan, unless the combine runs in
-// the down GEMM's epilogue.
-inline bool fused_mlp(GemmPlan plan, bool fused_combine) { return plan == GemmPlan::kSmall && !fused_combine; }
+// Whether an entry point that asks for both expert GEMMs in one launch
+// (launch_gemm_fused_mlp) gets it: the small tile plan only.
+inline bool fused_mlp_fits(GemmPlan plan) { return plan == GemmPlan::kSmall; }
 
-// Whether the gate/up GEMM of a moe_forward call reads its token tiles from h
-// (one token: no gather kernel), given the entry point's options.
-inline bool tokens_from_h(int T, bool single_launch_front, bool fused_combine) {
-  return T == 1 && !single_launch_front && !fused_combine;
-}
+// Whether the gate/up GEMM of a bf16 layer call reads its token tiles from h
+// (one token: no gather), given the entry point's options (the fused combine
+// keeps the gather, which zeroes its counters).
+inline bool tokens_from_h(int T, bool fused_combine) { return T == 1 && !fused_combine; }
 
 // Encodes nothing itself: the tensor maps are built by the caller.
 cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,
@@ -163,16 +162,15 @@ cudaError_t launch_gemm_down(const CUtensorMap& tm_w2, const CUtensorMap& tm_act
 // Both GEMMs of the small tile plan in one persistent launch ("4 · La fusion
 // de noyaux", §4.2 "GEMM + GEMM" and §4.6): every CTA runs its stream-K range
 // of the gate/up GEMM (a1), then its range of the down GEMM (a2); a down-GEMM
-// stage's activation rows are loaded once the gate/up unit that writes them
-// (same expert and token chunk, weight tile = the stage's K block) has counted
-// its four epilogue warps in a1.ready.  a1.ready: >= fused_mlp_ready_ints
-// ints, zero on entry.
+// unit's activation rows are loaded once every gate/up unit of its expert and
+// token chunk has counted its four epilogue warps in a1.ready[chunk] (chunks
+// numbered over all experts).  a1.ready: >= fused_mlp_ready_ints ints, zero
+// on entry.
 cudaError_t launch_gemm_fused_mlp(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const CUtensorMap& tm_w2,
                                   const CUtensorMap& tm_act, const ExpertGemmArgs& a1, const ExpertGemmArgs& a2,
                                   int num_sms, cudaStream_t stream);
-// gate/up units of the small plan at most: P_max rows in lists of >= 16 rows,
-// so at most P_max / 16 token chunks per weight tile, I / 64 tiles
-inline int64_t fused_mlp_ready_ints(int64_t P_max, int64_t I) { return (P_max + 15) / 16 * (I / 64); }
+// token chunks of the small plan at most: P_max rows in lists of >= 16 rows
+inline int64_t fused_mlp_ready_ints(int64_t P_max) { return (P_max + 15) / 16; }
 // Whether a GEMM with `tiles` weight tiles per expert runs on CTA pairs, and
 // the tiles per expert its work-unit table counts (pairs of tiles then).
 bool gemm_uses_pairs(GemmPlan plan, int tiles);

@@ -90,29 +90,38 @@ def test_kernels_per_call_host_checks():
     assert st == binding.MOE_OK and n == 0
     st, _ = binding.moe_kernels_per_call(binding.shape(4, 100, 256, 8, 2))
     assert st == binding.MOE_ERR_UNSUPPORTED
-    # small tile plan (<= 16 rows per expert): norm/router, top-k + align,
-    # gather, both GEMMs in one launch, combine; one token: no gather;
-    # large T: the two GEMMs separately, and the top-k and align take three kernels
+    # small T: norm/router, top-k + align, gather, the two GEMMs, combine;
+    # one token: no gather; large T: the top-k and align take three kernels
     st, n = binding.moe_kernels_per_call(binding.shape(4, 128, 256, 8, 2))
-    assert st == binding.MOE_OK and n == 5
+    assert st == binding.MOE_OK and n == 6
     st, n = binding.moe_kernels_per_call(binding.shape(1, 128, 256, 8, 2))
-    assert st == binding.MOE_OK and n == 4
+    assert st == binding.MOE_OK and n == 5
     st, n = binding.moe_kernels_per_call(binding.shape(200, 128, 256, 8, 2))
     assert st == binding.MOE_OK and n == 6
     st, n = binding.moe_kernels_per_call(binding.shape(4096, 128, 256, 8, 2))
     assert st == binding.MOE_OK and n == 8
     s4 = binding.shape(4, 128, 256, 8, 2)
-    assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD) == (binding.MOE_OK, 5)
-    assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_FUSED_FRONT) == (binding.MOE_OK, 3)
+    assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD) == (binding.MOE_OK, 6)
+    assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_FUSED_FRONT) == (binding.MOE_OK, 4)
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_MX) == (binding.MOE_OK, 7)
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_MXFP4) == (binding.MOE_OK, 7)
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_MXFP4A4) == (binding.MOE_OK, 7)
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_NVFP4) == (binding.MOE_OK, 7)
-    assert binding.moe_kernels_per_call_of(s4, 7)[0] == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_kernels_per_call_of(s4, 8)[0] == binding.MOE_ERR_INVALID_ARG
     assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_FUSED_COMBINE) == (binding.MOE_OK, 5)
+    assert binding.moe_kernels_per_call_of(s4, binding.MOE_CALL_FORWARD_FUSED_MLP) == (binding.MOE_OK, 5)
+    s1 = binding.shape(1, 128, 256, 8, 2)
+    assert binding.moe_kernels_per_call_of(s1, binding.MOE_CALL_FORWARD_FUSED_MLP) == (binding.MOE_OK, 4)
     s4096 = binding.shape(4096, 128, 256, 8, 2)
     assert binding.moe_kernels_per_call_of(s4096, binding.MOE_CALL_FORWARD_FUSED_COMBINE) == (binding.MOE_OK, 7)
-    assert binding.moe_kernels_per_call_of(s4, 7)[0] == binding.MOE_ERR_INVALID_ARG
+    assert binding.moe_kernels_per_call_of(s4096, binding.MOE_CALL_FORWARD_FUSED_MLP)[0] == \
+        binding.MOE_ERR_UNSUPPORTED
+    # the fused MLP entry point refuses the prefill tile plan before touching a pointer
+    _, need = binding.moe_workspace_size(s4096)
+    A = 1 << 20
+    assert binding.moe_forward_fused_mlp(s4096, A, A, A, None, A, A, A, A, need, None) == \
+        binding.MOE_ERR_UNSUPPORTED
+    assert binding.moe_kernels_per_call_of(s4, 8)[0] == binding.MOE_ERR_INVALID_ARG
     assert binding.moe_kernels_per_call_of(s4, -1)[0] == binding.MOE_ERR_INVALID_ARG
 
 
@@ -183,8 +192,12 @@ def test_mxfp4_sizes_and_argument_checks_without_a_gpu():
     _, need512 = binding.moe_workspace_size_mx(s512)
     assert binding.moe_forward_mxfp4a4(s512, A, A, A, None, A + 16, A, A, A, A, A, need512, None) == \
         binding.MOE_ERR_INVALID_ARG
-    # the MXFP4 layer: H and I multiples of 256 (this shape has I = 384)
-    assert binding.moe_forward_mxfp4a4(s, A, A, A, None, A, A, A, A, A, A, need, None) == binding.MOE_ERR_UNSUPPORTED
+    # the MXFP4 layer: H and I multiples of 128 (this shape has I = 384; I = 192 is refused)
+    assert binding.moe_forward_mxfp4a4(s, A, A, A, None, A + 16, A, A, A, A, A, need, None) == \
+        binding.MOE_ERR_INVALID_ARG
+    s192 = binding.shape(4, 256, 192, 8, 2)
+    assert binding.moe_forward_mxfp4a4(s192, A, A, A, None, A, A, A, A, A, A, 1 << 40, None) == \
+        binding.MOE_ERR_UNSUPPORTED
     assert fwd(w2c=A + 16) == binding.MOE_ERR_INVALID_ARG
     assert fwd(w13s=None) == binding.MOE_ERR_INVALID_ARG
     assert binding.moe_forward_mxfp4(s, A, A, A, None, A, A, A, A, A, A, need - 1, None) == binding.MOE_ERR_WORKSPACE
@@ -213,7 +226,7 @@ def test_nvfp4_sizes_and_argument_checks_without_a_gpu():
     assert fwd(g13=None) == binding.MOE_ERR_INVALID_ARG
     assert fwd(g2=A + 2) == binding.MOE_ERR_INVALID_ARG
     assert fwd(nbytes=need - 1) == binding.MOE_ERR_WORKSPACE
-    assert fwd(shape=binding.shape(4, 256, 384, 8, 2)) == binding.MOE_ERR_UNSUPPORTED
+    assert fwd(shape=binding.shape(4, 256, 192, 8, 2), nbytes=1 << 40) == binding.MOE_ERR_UNSUPPORTED
     q = binding.moe_nvfp4_quantize_weights
     assert q(s, A, A, A + 16, A, A, A, A, A, None) == binding.MOE_ERR_INVALID_ARG
     assert q(s, A, A, A, A, None, A, A, A, None) == binding.MOE_ERR_INVALID_ARG

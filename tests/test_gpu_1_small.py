@@ -107,6 +107,36 @@ def test_fused_combine_parity(case, o):
     gu.check_output(o, li, li.x, ref["y"])
 
 
+SMALL_PLAN_CASES = [c for c in CASES if c[1] * c[5] <= 16 * c[4]]  # T * top_k <= 16 * E: the decode tile plan
+
+
+@pytest.mark.parametrize("case", SMALL_PLAN_CASES, ids=[c[0] for c in SMALL_PLAN_CASES])
+def test_fused_mlp_parity(case, o):
+    """Both expert GEMMs in one launch: the same K split as the separate GEMMs,
+    so the same output bits as moe_forward on two calls in a row (completion
+    counters are cleared per call), hence within the oracle's tolerance too."""
+    _, T, H, I, E, k, renorm, zipf, seed = case
+    li = _layer_inputs(T, H, I, E, k, renorm, zipf, seed)
+    dl = gu.DeviceLayer(li)
+    ref = dl.run(li.x)
+    xd = gu.dev_bf16(li.x)
+    for _ in range(2):
+        y = dl.layer.forward(xd, fused_mlp=True)
+        torch.cuda.synchronize()
+        st, det = dl.layer.device_status(T)
+        assert st == binding.MOE_OK, (st, det)
+        assert np.array_equal(y.cpu().numpy().view(np.uint16), ref["y"]), "fused MLP differs from the split GEMMs"
+    gu.check_output(o, li, li.x, ref["y"])
+
+
+def test_fused_mlp_rejects_prefill_plan():
+    li = _layer_inputs(200, 128, 128, 4, 2, True, None, 0)  # 100 rows per expert: the prefill tile plan
+    dl = gu.DeviceLayer(li)
+    with pytest.raises(binding.MoeError) as ei:
+        dl.layer.forward(gu.dev_bf16(li.x), fused_mlp=True)
+    assert ei.value.status == binding.MOE_ERR_UNSUPPORTED
+
+
 def test_fused_front_rejects_large_batches():
     li = _layer_inputs(80, 128, 128, 4, 2, True, None, 0)
     dl = gu.DeviceLayer(li)

@@ -30,7 +30,7 @@ CASES = [
     ("mx_prefill_chunks", 1024, 256, 256, 4, 2, True, None, 4),
     ("mx_prefill_ragged_norenorm", 300, 384, 128, 6, 3, False, None, 5),
     ("mx_prefill_skewed", 512, 256, 256, 16, 4, True, 1.2, 11),
-    # shapes for the MXFP4 layer too (H and I multiples of 256)
+    # H and I multiples of 256: no partial last stage in the packed-FP4 layers
     ("a4_ragged_decode", 37, 256, 512, 16, 4, True, None, 21),
     ("a4_bias_norenorm", 3, 512, 256, 20, 5, False, 1.2, 22),
     ("a4_prefill_ragged_norenorm", 300, 512, 256, 6, 3, False, None, 23),
@@ -58,8 +58,6 @@ def test_mx_layer_parity(case, fmt, o):
     _, T, H, I, E, k, renorm, zipf, seed = case
     nv = fmt == "nvfp4"
     a4 = fmt == "mxfp4a4" or nv  # packed E2M1 token codes
-    if a4 and (H % 256 or I % 256):
-        pytest.skip("the MXFP4 and NVFP4 layers take H and I multiples of 256")
     cfg = inputs.LayerConfig(T=T, H=H, I=I, E=E, top_k=k, renormalize=renorm, seed=seed, zipf_bias=zipf)
     li = inputs.make_layer_inputs(cfg)
     dl = gu.DeviceLayer(li)
@@ -211,15 +209,17 @@ def test_mxfp4_rejects_unaligned_codes():
     assert ei.value.status == binding.MOE_ERR_INVALID_ARG
 
 
-def test_mxfp4a4_rejects_h_not_multiple_of_256():
-    cfg = inputs.LayerConfig(T=4, H=384, I=256, E=4, top_k=2, seed=0)
+def test_block_scaled_layers_reject_i_not_multiple_of_128():
+    """The bf16 layer takes I = 192 (a multiple of 64); the block-scaled layers,
+    whose scale tiles cover 128 elements of K, refuse it before anything runs."""
+    cfg = inputs.LayerConfig(T=4, H=256, I=192, E=4, top_k=2, seed=0)
     li = inputs.make_layer_inputs(cfg)
     dl = gu.DeviceLayer(li)
     L = dl.layer
-    L.quantize_mxfp4()
-    with pytest.raises(binding.MoeError) as ei:
-        L.forward_mxfp4(gu.dev_bf16(li.x), fp4_tokens=True)
-    assert ei.value.status == binding.MOE_ERR_UNSUPPORTED
+    for quantize in (L.quantize_mx, L.quantize_mxfp4, L.quantize_nvfp4):
+        with pytest.raises(binding.MoeError) as ei:
+            quantize()
+        assert ei.value.status == binding.MOE_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("span", [(-4, 4), (-120, 120), (-30, -20)])
