@@ -189,15 +189,15 @@ cudaError_t launch_align_nt(const float* logits, int T, int k, int renorm, int32
                     flags, n_flags);
 }
 
-// 256 threads for up to 8 tokens (E <= 256: one thread per expert in the
-// align's scans), else 1024
-constexpr int kAlignSmallT = 8;
+// 256 threads for up to 8 tokens and 256 experts (one warp per token covers
+// the top-k in one round, one thread per expert the align's scans, and the
+// block's barriers are cheaper than with 1024), else 1024
 template <int VPL>
 cudaError_t launch_align_t(const float* logits, int T, int k, int renorm, int32_t* topk_ids, float* topk_w, int N,
                            int E, int pad, int bn1, int tiles1, int bn2, int tiles2, int32_t* counts, int32_t* offsets,
                            int32_t* sorted_ids, int32_t* slot_of, int32_t* unit_off1, int32_t* unit_off2,
                            int32_t* err, int32_t* flags, int n_flags, cudaStream_t stream) {
-  if (VPL > 0 && T <= kAlignSmallT && E <= 256)
+  if (VPL > 0 && T <= 8 && E <= 256)
     return launch_align_nt<VPL, 256>(logits, T, k, renorm, topk_ids, topk_w, N, E, pad, bn1, tiles1, bn2, tiles2,
                                      counts, offsets, sorted_ids, slot_of, unit_off1, unit_off2, err, flags, n_flags,
                                      stream);

@@ -454,10 +454,25 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
   const int sf_tiles_k = args.K / (C::kKPerStage / C::kChunks);
   auto valid_chunks = [&](int kb) { return min(C::kChunks, sf_tiles_k - kb * C::kChunks); };
   const int ctas = workers;
-  // per phase: its GEMM's arguments, unit table, kind and output features per unit
-  auto gemm_args = [&](int ph) -> const ExpertGemmArgs& { return (FUSED && ph) ? args2 : args; };
+  // per phase (the fused kernel: 0 gate/up, 1 down), the arguments read per
+  // segment, stage or output chunk, held in registers: a reference to one of
+  // the two parameter structs chosen at run time would turn each of these
+  // reads into a generic load from the parameter space
+  struct PhaseArgs {
+    uint16_t* out;
+    float* partials;
+    int32_t* flags;
+    int n_out, tiles, w_rows;
+  };
+  const PhaseArgs pa0{args.out, args.partials, args.flags, args.n_out, args.tiles_per_expert, args.w_rows_per_expert};
+  const PhaseArgs pa1 = FUSED ? PhaseArgs{args2.out, args2.partials, args2.flags, args2.n_out, args2.tiles_per_expert,
+                                          args2.w_rows_per_expert}
+                              : pa0;
+  auto phase_args = [&](int ph) { return (FUSED && ph) ? pa1 : pa0; };  // a copy, in registers
   auto unit_tab = [&](int ph) { return (FUSED && ph) ? t_unit2 : t_unit; };
   auto is_swiglu = [&](int ph) { return FUSED ? ph == 0 : SWIGLU; };
+  const bool tok_from_h = args.tokens_from_h != 0;
+  int32_t* const ready = args.ready;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -494,7 +509,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
           pend_chunk[STAGES] = {};
       int pend_ready[STAGES] = {};  // fused kernel: the token chunk a down-GEMM stage awaits, or -1
       int chunk_seen_ready = -1;  // the last chunk found complete
-      const int chunk_need = C::kEpiWarps * args.tiles_per_expert;
+      const int chunk_need = C::kEpiWarps * pa0.tiles;
       // a CTA pair signals every load on the even CTA's full barrier
       const uint32_t full_cl = PAIR ? mapa_shared(smem_u32(full), 0) : 0u;
       auto load_2d = [&](void* dst, const CUtensorMap* map, int st, int c0, int c1, uint64_t pol) {
@@ -513,7 +528,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
       // chunk: the unit's token chunk (MXFP8 token scales are stored per chunk)
       auto load_tokens = [&](int st, int kb, int tok0, int rows, int chunk) {
         uint8_t* sb = smem + st * C::kStageBytes + kABytes;
-        const int row0 = args.tokens_from_h ? 0 : tok0;  // one token: its row of h, then zeros
+        const int row0 = tok_from_h ? 0 : tok0;  // one token: its row of h, then zeros
         for (int r = 0; r < rows; r += TOKBOX)
           load_2d(sb + r * kTokRowBytes, &tm_x, st, kb * C::kBoxX, row0 + r, pol_x);
         if (MX && PAIR) {
@@ -561,12 +576,12 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
           resolve_deps();
         }
         if (!FUSED || r < 0 || r == chunk_seen_ready) return true;
-        if (ld_acquire(args.ready + r) < chunk_need) {
+        if (ld_acquire(ready + r) < chunk_need) {
           if (!wait) return false;
           const uint64_t t0 = globaltimer_ns();
           // (up to one producer per SM polls the same few counters: a slow
           // poll keeps them from crowding the L2 slices the weights stream through)
-          while (ld_acquire(args.ready + r) < chunk_need) {
+          while (ld_acquire(ready + r) < chunk_need) {
             if (*abort_flag || globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
             __nanosleep(1000);
           }
@@ -578,26 +593,48 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
       Work rg(total_units, kblocks, total_units2, kblocks2, worker, ctas, args.stream_k != 0);
       int ph, u, kb0, kb1;
       while (ok && rg.next(ph, u, kb0, kb1)) {
-        const ExpertGemmArgs& A = gemm_args(ph);
+        const PhaseArgs A = phase_args(ph);
         const bool sw = is_swiglu(ph);
-        const Unit un = decode_unit(u, unit_tab(ph), t_off, args.E, A.tiles_per_expert, BN);
+        const Unit un = decode_unit(u, unit_tab(ph), t_off, args.E, A.tiles, BN);
         // a pair's unit: weight tiles 2t (even CTA) and 2t+1; the MMA's N
         // tokens split in halves, the first half in the even CTA
         const int tile = PAIR ? 2 * un.tile + static_cast<int>(rank) : un.tile;
         const int n_mma = PAIR ? (un.n + 31) / 32 * 32 : un.n;
         const int half = PAIR ? n_mma / 2 : n_mma;
         const int tok_first = un.tok0 + static_cast<int>(rank) * half;
-        const int wrow = un.e * A.w_rows_per_expert + tile * (sw ? kGateUpTileFeat : kDownTileFeat);
+        const int wrow = un.e * A.w_rows + tile * (sw ? kGateUpTileFeat : kDownTileFeat);
         const int tok_rows = (half + TOKBOX - 1) / TOKBOX * TOKBOX;  // whole boxes; rows past n are unused
         const bool reused = t_off[un.e + 1] - t_off[un.e] > BN;
         const uint64_t pol_w = reused ? pol_keep : pol_stream;
         // per CTA (both of a pair); scale bytes of a full stage: C::kSfBytes
         const uint32_t bytes_base = C::kWTxBytes + tok_rows * kTokRowBytes;
-        const int chunk = MX ? t_unit[un.e] / args.tiles_per_expert + (un.tok0 - t_off[un.e]) / BN : 0;
+        const int chunk = MX ? t_unit[un.e] / pa0.tiles + (un.tok0 - t_off[un.e]) / BN : 0;
         // fused kernel, down GEMM: the token chunk (expert, rows [tok0, tok0 + BN))
         // whose activation rows this unit reads, numbered over all experts
-        const int rd_chunk = (FUSED && ph == 1) ? t_unit[un.e] / args.tiles_per_expert + (un.tok0 - t_off[un.e]) / BN
+        const int rd_chunk = (FUSED && ph == 1) ? t_unit[un.e] / pa0.tiles + (un.tok0 - t_off[un.e]) / BN
                                                 : -1;
+        if (FUSED && ph == 1 && rd_chunk != chunk_seen_ready) {
+          // a down-GEMM segment starts its weight stream only once its chunk's
+          // activation rows are complete: streamed earlier, the W2 tiles compete
+          // for DRAM with the gate/up phase's last loads, which every CTA's
+          // readiness waits for
+          while (n_pend > 0) {
+            if (!head_ready(true)) {
+              ok = false;
+              where = kWaitActReady;
+              break;
+            }
+            issue_head();
+          }
+          if (ok) {
+            pend_ready[pend_head] = rd_chunk;  // an empty FIFO's head slot: ask for this chunk
+            if (!head_ready(true)) {
+              ok = false;
+              where = kWaitActReady;
+            }
+          }
+          if (!ok) break;
+        }
         for (int kb = kb0; kb < kb1; ++kb) {
           if (n_pend == STAGES) {  // the slot about to be refilled still waits for its token rows
             if (!head_ready(true)) {
@@ -627,7 +664,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
             load_2d(sa, FUSED ? &tm_sw : &tm_w, stage, kb * C::kBoxX, wrow, pol_w);
           }
           if (MX) {  // the weight tile's scales (static: loaded before the parent kernel ends)
-            const int wtiles = PAIR ? 2 * args.tiles_per_expert : args.tiles_per_expert;  // 128-row tiles per expert
+            const int wtiles = PAIR ? 2 * pa0.tiles : pa0.tiles;  // 128-row tiles per expert
             const int64_t wt = static_cast<int64_t>(un.e * wtiles + tile) * sf_tiles_k + kb * C::kChunks;
             if (PAIR) {
               for (int c = 0; c < valid_chunks(kb); ++c)
@@ -696,7 +733,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
       Work rg(total_units, kblocks, total_units2, kblocks2, worker, ctas, args.stream_k != 0);
       int ph, u, kb0, kb1;
       while (ok && rg.next(ph, u, kb0, kb1)) {
-        const Unit un = decode_unit(u, unit_tab(ph), t_off, args.E, gemm_args(ph).tiles_per_expert, BN);
+        const Unit un = decode_unit(u, unit_tab(ph), t_off, args.E, phase_args(ph).tiles, BN);
         const bool free_acc = PAIR ? mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, kWaitTimeoutNs, abort_flag)
                                    : mbar_wait(&tempty[acc], acc_phase ^ 1u, kWaitTimeoutNs, abort_flag);
         if (!free_acc) {
@@ -877,13 +914,13 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
     Work rg(total_units, kblocks, total_units2, kblocks2, worker, ctas, args.stream_k != 0);
     int ph, u, kb0, kb1;
     while (ok && rg.next(ph, u, kb0, kb1)) {
-      const ExpertGemmArgs& A = gemm_args(ph);
+      const PhaseArgs A = phase_args(ph);
       const bool sw = is_swiglu(ph);
       const int kb_total = ph ? kblocks2 : kblocks;
       const int64_t W = rg.range(ph).W;
       // this CTA's partial-sum slot of this GEMM: [BN columns][128 rows] fp32
       float* my_slot = A.partials + static_cast<int64_t>(blockIdx.x) * BN * 128;
-      const Unit un = decode_unit(u, unit_tab(ph), t_off, args.E, A.tiles_per_expert, BN);
+      const Unit un = decode_unit(u, unit_tab(ph), t_off, args.E, A.tiles, BN);
       // warp-uniform outcome: tcgen05.ld below must be executed by all 32 lanes
       const bool got = mbar_wait(&tfull[acc], acc_phase, kWaitTimeoutNs, abort_flag);
       if (!__all_sync(0xFFFFFFFFu, got)) {
@@ -1012,14 +1049,13 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
         }
         // fused kernel: the unit's activation rows of this lane quarter are
         // stored; count this warp in its token chunk's counter (the down
-        // GEMM's producers wait for four per weight tile, then read the rows
-        // by TMA)
+        // GEMM's producers wait for four per weight tile, then order their TMA
+        // reads after that acquire with a proxy fence)
         if (FUSED && ph == 0 && ok) {
-          fence_proxy_async_global();
           __threadfence();
           __syncwarp();
           if (lane == 0)
-            red_release_add(args.ready + t_unit[un.e] / args.tiles_per_expert + (un.tok0 - t_off[un.e]) / BN, 1);
+            red_release_add(ready + t_unit[un.e] / pa0.tiles + (un.tok0 - t_off[un.e]) / BN, 1);
         }
       }
       if (!ok) break;

@@ -533,6 +533,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a2.pair = moe::gemm_uses_pairs(plan, tiles2);
   if (fused_combine) set_fused_combine(a2, s, L, workspace, y);
 
+
   if (fused_mlp) {
     // both GEMMs in one launch (events[6] then follows events[5] at once)
     if (moe::launch_gemm_fused_mlp(tm_w13, tm_xg, tm_w2, tm_act, a1, a2, num_sms, cs) != cudaSuccess || !mark(5) ||
