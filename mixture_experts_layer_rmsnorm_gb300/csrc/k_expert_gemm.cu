@@ -359,9 +359,12 @@ __device__ __noinline__ bool combine_unit(const ExpertGemmArgs& a, const Unit& u
 }
 
 // FUSED: the gate/up GEMM (args, tm_w, tm_x) and then the down GEMM (args2;
-// tm_sw maps W2, tm_sx the activations) in one persistent launch.
+// tm_sw maps W2, tm_sx the activations) in one persistent launch.  KTAIL
+// (packed E2M1 operands, 256 elements of K per stage): K ends half way into
+// the last stage; its own instance, so that whole-stage shapes keep
+// compile-time scale sizes and MMA counts.
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
-          bool A4 = false, bool NV = false, bool FUSED = false>
+          bool A4 = false, bool NV = false, bool FUSED = false, bool KTAIL = false>
 __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED>::kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_sx,
@@ -452,7 +455,9 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
   // block-scaled GEMMs: scale tiles per 128-row group along K (one per
   // kKPerStage / kChunks elements), and the valid ones in stage kb
   const int sf_tiles_k = args.K / (C::kKPerStage / C::kChunks);
-  auto valid_chunks = [&](int kb) { return min(C::kChunks, sf_tiles_k - kb * C::kChunks); };
+  // scale tiles of the last stage when K ends half way into it (KTAIL)
+  const int sf_tail = sf_tiles_k % C::kChunks;
+  auto tail_stage = [&](int kb) { return KTAIL && kb == kblocks - 1; };
   const int ctas = workers;
   // per phase (the fused kernel: 0 gate/up, 1 down), the arguments read per
   // segment, stage or output chunk, held in registers: a reference to one of
@@ -495,14 +500,17 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
       int64_t issued = 0;
       bool ok = true;
       int where = kWaitRingSlotFree;  // the wait that ran out
-      // The token (or activation) loads of the stages wait in a FIFO until
-      // their rows exist: the gate/up GEMM's token rows until the previous
-      // kernel has completed (pdl_wait), so the first ring-full of stages gets
-      // its weight tiles at once and its token rows after; in the fused
-      // kernel, a down-GEMM stage's activation rows until every gate/up unit
-      // of the same expert and token chunk has counted the stores of its four
-      // epilogue warps (one counter per chunk, checked once per segment: a
-      // poll per stage, an L2 round trip, would hold the producer back).
+      // The token (or activation) loads of the stages wait until their rows
+      // exist: the gate/up GEMM's token rows until the previous kernel has
+      // completed (pdl_wait), so the first ring-full of stages gets its weight
+      // tiles at once and its token rows after (then all at once).  In the
+      // fused kernel they wait in a FIFO, a down-GEMM stage's activation rows
+      // until every gate/up unit of the same expert and token chunk has
+      // counted the stores of its four epilogue warps (one counter per chunk,
+      // checked once per segment: a poll per stage, an L2 round trip, would
+      // hold the producer back).  The other instances keep the plain scheme:
+      // the FIFO's code, inlined at every call site, makes these large
+      // kernels measurably slower.
       bool deps_ready = false;
       int n_pend = 0, pend_head = 0;
       int pend_stage[STAGES] = {}, pend_kb[STAGES] = {}, pend_tok0[STAGES] = {}, pend_rows[STAGES] = {},
@@ -536,14 +544,16 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
           // and 128-element K chunk; tile (h, c) at 512 (c G + h)), in each CTA
           // (tensor map tm_sx: one tile = a box of 2 rows x 256 bytes)
           constexpr int G = C::kSfTokTiles;
-          for (int c = 0; c < valid_chunks(kb); ++c)
+          for (int c = 0; c < (tail_stage(kb) ? sf_tail : C::kChunks); ++c)
             for (int h = 0; h < G; ++h)
               load_2d(sb + C::kBBytes + C::kSfWBytes + 512 * (c * G + h), &tm_sx, st, 0,
                       2 * ((G * chunk + h) * sf_tiles_k + kb * C::kChunks + c), pol_x);
         } else if (MX) {  // one tile per K chunk, the chunks of a stage adjacent
-          bulk_load(sb + C::kBBytes + C::kSfWBytes,
-                    args.x_scales + (static_cast<size_t>(chunk) * sf_tiles_k + kb * C::kChunks) * 512,
-                    512 * valid_chunks(kb), &full[st], pol_x);
+          const uint8_t* src = args.x_scales + (static_cast<size_t>(chunk) * sf_tiles_k + kb * C::kChunks) * 512;
+          if (!tail_stage(kb))
+            bulk_load(sb + C::kBBytes + C::kSfWBytes, src, 512 * C::kChunks, &full[st], pol_x);
+          else
+            bulk_load(sb + C::kBBytes + C::kSfWBytes, src, 512 * sf_tail, &full[st], pol_x);
         }
       };
       // fused kernel: a down-GEMM stage's activation rows (written by this
@@ -636,7 +646,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
           if (!ok) break;
         }
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (n_pend == STAGES) {  // the slot about to be refilled still waits for its token rows
+          if (FUSED && n_pend == STAGES) {  // the slot about to be refilled still waits for its token rows
             if (!head_ready(true)) {
               ok = false;
               where = kWaitActReady;
@@ -653,7 +663,8 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
           }
           uint8_t* sa = smem + stage * C::kStageBytes;
           const uint32_t bytes =
-              bytes_base + (MX ? static_cast<uint32_t>(valid_chunks(kb)) * 512u * (1u + C::kSfTokTiles) : 0u);
+              bytes_base + (tail_stage(kb) ? static_cast<uint32_t>(sf_tail) * 512u * (1u + C::kSfTokTiles)
+                                           : static_cast<uint32_t>(C::kSfBytes));
           if (!PAIR)
             mbar_arrive_expect_tx(&full[stage], bytes);
           else if (leader)
@@ -667,14 +678,32 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
             const int wtiles = PAIR ? 2 * pa0.tiles : pa0.tiles;  // 128-row tiles per expert
             const int64_t wt = static_cast<int64_t>(un.e * wtiles + tile) * sf_tiles_k + kb * C::kChunks;
             if (PAIR) {
-              for (int c = 0; c < valid_chunks(kb); ++c)
+              for (int c = 0; c < (tail_stage(kb) ? sf_tail : C::kChunks); ++c)
                 load_2d(sa + kABytes + C::kBBytes + 512 * c, &tm_sw, stage, 0, static_cast<int>(2 * (wt + c)), pol_w);
             } else {
               bulk_load(sa + kABytes + C::kBBytes, args.w_scales + static_cast<size_t>(wt) * 512,
-                        512 * valid_chunks(kb), &full[stage], pol_w);
+                        512 * (tail_stage(kb) ? sf_tail : C::kChunks), &full[stage], pol_w);
             }
           }
-          if (n_pend == 0 && deps_ready && (rd_chunk < 0 || rd_chunk == chunk_seen_ready)) {
+          if constexpr (!FUSED) {
+            // only the first ring-full of stages waits for the parent kernel;
+            // once it has completed, every pending load goes out at once
+            if (deps_ready) {
+              load_tokens(stage, kb, tok_first, tok_rows, chunk);
+            } else {
+              pend_stage[n_pend] = stage;
+              pend_kb[n_pend] = kb;
+              pend_tok0[n_pend] = tok_first;
+              pend_rows[n_pend] = tok_rows;
+              pend_chunk[n_pend] = chunk;
+              if (++n_pend == STAGES) {
+                resolve_deps();
+                for (int i = 0; i < n_pend; ++i)
+                  load_tokens(pend_stage[i], pend_kb[i], pend_tok0[i], pend_rows[i], pend_chunk[i]);
+                n_pend = 0;
+              }
+            }
+          } else if (n_pend == 0 && deps_ready && (rd_chunk < 0 || rd_chunk == chunk_seen_ready)) {
             // the rows exist and nothing waits ahead of them: load them now
             if (rd_chunk >= 0)
               load_act(stage, kb, tok_first, tok_rows);
@@ -701,13 +730,20 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
       // the token loads still waiting (fewer iterations than stages, or the
       // last ones); after a wait that ran out they are issued all the same
       // (the call reports the timeout), so that every stage's loads land
-      while (n_pend > 0) {
-        if (ok && !head_ready(true)) {
-          ok = false;
-          where = kWaitActReady;
-        }
+      if constexpr (!FUSED) {
         if (!deps_ready) resolve_deps();
-        issue_head();
+        for (int i = 0; i < n_pend; ++i)
+          load_tokens(pend_stage[i], pend_kb[i], pend_tok0[i], pend_rows[i], pend_chunk[i]);
+        n_pend = 0;
+      } else {
+        while (n_pend > 0) {
+          if (ok && !head_ready(true)) {
+            ok = false;
+            where = kWaitActReady;
+          }
+          if (!deps_ready) resolve_deps();
+          issue_head();
+        }
       }
       if (!deps_ready) resolve_deps();
       if (!ok) raise_timeout(args.err, abort_flag, kern, where);
@@ -787,7 +823,9 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
                   tmem_cp_32x128b_x4(sfb_t + 4 * (c * G + h), src);
               }
             }
-            const int n_k = 4 * valid_chunks(kb) / C::kChunks;  // MMAs over K inside the stage
+            // MMAs over K in the stage: 4, fewer in a KTAIL instance's last stage
+            // (past K its scales were not loaded)
+            const int n_k = tail_stage(kb) ? 4 * sf_tail / C::kChunks : 4;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               if (k >= n_k) break;
@@ -1092,13 +1130,13 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
 // tsw / tsx: the scale maps of MXFP8 pairs, or the fused kernel's W2 and
 // activation maps; a2: the fused kernel's down GEMM.
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
-          bool A4 = false, bool NV = false, bool FUSED = false>
+          bool A4 = false, bool NV = false, bool FUSED = false, bool KTAIL = false>
 cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, int num_sms,
                                cudaStream_t stream, const CUtensorMap* tsw = nullptr,
                                const CUtensorMap* tsx = nullptr, const ExpertGemmArgs* a2 = nullptr) {
   static const CUtensorMap kNoMap = {};  // unused map arguments
   using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED>;
-  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED>;
+  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED, KTAIL>;
   static PerDevice config;  // the smem attribute, and the CTA pairs that fit on the device at once
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::kThreads);
@@ -1173,37 +1211,54 @@ constexpr int kMxPairTokBox = kMxPairBn / 2;                // each CTA loads ha
 
 // The block-scaled GEMMs of one tile plan; W4: E2M1 weight codes; A4: E2M1
 // token codes too (kind::mxf4).
+// KTAIL: the MXFP4 layer's instances for K an odd multiple of 128 (its
+// stages cover 256 elements of K)
+template <bool SWIGLU, bool W4, bool A4 = false, bool KTAIL = false>
+cudaError_t launch_mx_k(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& tsw,
+                        const CUtensorMap& tsx, const ExpertGemmArgs& a, GemmPlan plan, int num_sms,
+                        cudaStream_t stream) {
+  switch (plan) {
+    case GemmPlan::kSmall:
+      return launch_expert_gemm<SWIGLU, kMxBn[0], kMxStages[0], kTokBox[0], false, true, W4, A4, false, false, KTAIL>(
+          tw, tx, a, num_sms, stream);
+    default:
+      if (a.pair)
+        return launch_expert_gemm<SWIGLU, kMxPairBn, kMxPairStages, kMxPairTokBox, true, true, W4, A4, false, false,
+                                  KTAIL>(tw, tx, a, num_sms, stream, &tsw, &tsx);
+      return launch_expert_gemm<SWIGLU, kMxBn[1], kMxStages[1], kTokBox[1], false, true, W4, A4, false, false, KTAIL>(
+          tw, tx, a, num_sms, stream);
+  }
+}
+
 template <bool SWIGLU, bool W4, bool A4 = false>
 cudaError_t launch_mx(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& tsw, const CUtensorMap& tsx,
                       const ExpertGemmArgs& a, GemmPlan plan, int num_sms, cudaStream_t stream) {
-  switch (plan) {
-    case GemmPlan::kSmall:
-      return launch_expert_gemm<SWIGLU, kMxBn[0], kMxStages[0], kTokBox[0], false, true, W4, A4>(tw, tx, a,
-                                                                                                num_sms, stream);
-    default:
-      if (a.pair)
-        return launch_expert_gemm<SWIGLU, kMxPairBn, kMxPairStages, kMxPairTokBox, true, true, W4, A4>(
-            tw, tx, a, num_sms, stream, &tsw, &tsx);
-      return launch_expert_gemm<SWIGLU, kMxBn[1], kMxStages[1], kTokBox[1], false, true, W4, A4>(tw, tx, a,
-                                                                                                num_sms, stream);
-  }
+  if (A4 && a.K % 256 != 0) return launch_mx_k<SWIGLU, W4, A4, true>(tw, tx, tsw, tsx, a, plan, num_sms, stream);
+  return launch_mx_k<SWIGLU, W4, A4, false>(tw, tx, tsw, tsx, a, plan, num_sms, stream);
 }
 
 // NVFP4 plans: one CTA per unit of 32 / 128 tokens, 9 / 6 stages of 24 / 36 KB
 // (4 KB of scale tiles per stage)
 constexpr int kNvStages[2] = {9, 6};
 
+template <bool SWIGLU, bool KTAIL>
+cudaError_t launch_nv_k(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, GemmPlan plan,
+                        int num_sms, cudaStream_t stream) {
+  switch (plan) {
+    case GemmPlan::kSmall:
+      return launch_expert_gemm<SWIGLU, kMxBn[0], kNvStages[0], kTokBox[0], false, true, true, true, true, false,
+                                KTAIL>(tw, tx, a, num_sms, stream);
+    default:
+      return launch_expert_gemm<SWIGLU, kMxBn[1], kNvStages[1], kTokBox[1], false, true, true, true, true, false,
+                                KTAIL>(tw, tx, a, num_sms, stream);
+  }
+}
+
 template <bool SWIGLU>
 cudaError_t launch_nv(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, GemmPlan plan,
                       int num_sms, cudaStream_t stream) {
-  switch (plan) {
-    case GemmPlan::kSmall:
-      return launch_expert_gemm<SWIGLU, kMxBn[0], kNvStages[0], kTokBox[0], false, true, true, true, true>(
-          tw, tx, a, num_sms, stream);
-    default:
-      return launch_expert_gemm<SWIGLU, kMxBn[1], kNvStages[1], kTokBox[1], false, true, true, true, true>(
-          tw, tx, a, num_sms, stream);
-  }
+  if (a.K % 256 != 0) return launch_nv_k<SWIGLU, true>(tw, tx, a, plan, num_sms, stream);
+  return launch_nv_k<SWIGLU, false>(tw, tx, a, plan, num_sms, stream);
 }
 
 }  // namespace
