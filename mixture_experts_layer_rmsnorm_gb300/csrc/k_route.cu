@@ -28,7 +28,7 @@ namespace moe {
 namespace {
 
 // grid = (ceil(T / TT), ceil(E / experts_per_cta)), block = 256, dyn smem = TT*H*2.
-template <int TT, int TE>
+template <int TT, int TE, bool PAIRED = false>
 __global__ void __launch_bounds__(rt::kRouteWarps * 32, (TT >= 8) ? 2 : 1)
     norm_router_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g,
                        const float* __restrict__ w_router, const float* __restrict__ bias, int T, int H, int E,
@@ -44,17 +44,18 @@ __global__ void __launch_bounds__(rt::kRouteWarps * 32, (TT >= 8) ? 2 : 1)
   pdl_wait();
   pdl_launch_dependents();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 4) err[threadIdx.x] = 0;
-  rt::norm_router_tile<TT, TE>(x, g, w_router, bias, T, H, E, eps, t0, e0, experts_per_cta, blockIdx.y == 0, h_out,
-                               logits, h_s);
+  rt::norm_router_tile<TT, TE, true, PAIRED>(x, g, w_router, bias, T, H, E, eps, t0, e0, experts_per_cta,
+                                             blockIdx.y == 0, h_out, logits, h_s);
 }
 
-template <int TT, int TE>
+template <int TT, int TE, bool PAIRED = false>
 cudaError_t launch_nr(const uint16_t* x, const uint16_t* g, const float* wr, const float* bias, int T, int H, int E,
                       float eps, uint16_t* h, float* logits, int32_t* err, int num_sms, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(TT) * H * 2;
   static PerDevice config;  // the attribute is per device
   const cudaError_t ce = config.get([](int&) {
-    return cudaFuncSetAttribute(norm_router_kernel<TT, TE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    return cudaFuncSetAttribute(norm_router_kernel<TT, TE, PAIRED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                200 * 1024);
   });
   if (ce != cudaSuccess) return ce;
   const int tiles = (T + TT - 1) / TT;
@@ -65,8 +66,8 @@ cudaError_t launch_nr(const uint16_t* x, const uint16_t* g, const float* wr, con
   int epc = group;
   if (tiles >= num_sms) epc = (E + group - 1) / group * group;
   dim3 grid(tiles, (E + epc - 1) / epc);
-  return launch_pdl(norm_router_kernel<TT, TE>, grid, dim3(rt::kRouteWarps * 32), smem, stream, x, g, wr, bias, T, H, E,
-                    eps, epc, h, logits, err);
+  return launch_pdl(norm_router_kernel<TT, TE, PAIRED>, grid, dim3(rt::kRouteWarps * 32), smem, stream, x, g, wr,
+                    bias, T, H, E, eps, epc, h, logits, err);
 }
 
 }  // namespace
@@ -78,6 +79,14 @@ cudaError_t launch_norm_router(const uint16_t* x, const uint16_t* g, const float
   if (T <= 64) return launch_nr<4, 1>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
   if (H > 8192)
     return launch_nr<4, 2>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
+  // Large batches with rows up to 4096: 14-token tiles (two CTAs of 112 KB
+  // per SM) cover T = 4096 in 293 CTAs, one wave over 152 SMs x 2, where
+  // 8-token tiles need 1.7 waves; the tokens go in pairs through the paired
+  // FMA.  Only once the 14-token tiles alone fill the SMs: with fewer tiles
+  // the expert groups are split over CTAs, and the 8-token tiles do that
+  // better.
+  if (H <= 4096 && (T + 13) / 14 >= num_sms)
+    return launch_nr<14, 4, true>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
   return launch_nr<8, 4>(x, g, w_router, bias, T, H, E, eps, h, logits, err, num_sms, stream);
 }
 

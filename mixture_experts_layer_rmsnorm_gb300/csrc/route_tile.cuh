@@ -115,6 +115,50 @@ __device__ __forceinline__ void gemv_round(const float4* const (&wrow)[TE], cons
   }
 }
 
+// The same round for tokens taken two at a time: one paired fp32 FMA
+// (fma.rn.f32x2, each half rounded exactly as a single fused multiply-add)
+// updates the accumulators of tokens 2p and 2p+1 for one expert, so every
+// accumulator still sees its products in the canonical order and the logits
+// are bit for bit those of gemv_round, in half the FMA instructions.
+template <int TT, int TE, int DEPTH, bool MASKED>
+__device__ __forceinline__ void gemv_round_paired(const float4* const (&wrow)[TE], const uint4* h_s, int nch, int c0,
+                                                  float2 (&acc)[TT / 2][TE]) {
+  float4 wv[DEPTH][TE][2];
+#pragma unroll
+  for (int d = 0; d < DEPTH; ++d)
+#pragma unroll
+    for (int b = 0; b < TE; ++b) {
+      if (!MASKED || c0 + 32 * d < nch) {
+        wv[d][b][0] = __ldg(wrow[b] + 2 * (c0 + 32 * d));
+        wv[d][b][1] = __ldg(wrow[b] + 2 * (c0 + 32 * d) + 1);
+      }
+    }
+#pragma unroll
+  for (int d = 0; d < DEPTH; ++d) {
+    const int c = c0 + 32 * d;
+    if (!MASKED || c < nch) {
+#pragma unroll
+      for (int p = 0; p < TT / 2; ++p) {
+        const uint4 ha = h_s[(2 * p) * nch + c], hb = h_s[(2 * p + 1) * nch + c];
+        const uint32_t wa[4] = {ha.x, ha.y, ha.z, ha.w}, wb[4] = {hb.x, hb.y, hb.z, hb.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // elements 2j and 2j+1 of both tokens' chunk (bf16 -> fp32 is exact)
+          const float2 h0 = make_float2(__uint_as_float(wa[j] << 16), __uint_as_float(wb[j] << 16));
+          const float2 h1 = make_float2(__uint_as_float(wa[j] & 0xFFFF0000u), __uint_as_float(wb[j] & 0xFFFF0000u));
+#pragma unroll
+          for (int b = 0; b < TE; ++b) {
+            const float w[8] = {wv[d][b][0].x, wv[d][b][0].y, wv[d][b][0].z, wv[d][b][0].w,
+                                wv[d][b][1].x, wv[d][b][1].y, wv[d][b][1].z, wv[d][b][1].w};
+            acc[p][b] = __ffma2_rn(h0, make_float2(w[2 * j], w[2 * j]), acc[p][b]);
+            acc[p][b] = __ffma2_rn(h1, make_float2(w[2 * j + 1], w[2 * j + 1]), acc[p][b]);
+          }
+        }
+      }
+    }
+  }
+}
+
 // Tokens [t0, t0+TT) x experts [e0, e0+experts_per_cta): RMSNorm of the
 // tokens into h_s (TT*H bf16 of shared memory; also to h_out when write_h),
 // then the fp32 logits.  Each warp computes TE experts x TT tokens at a time.
@@ -122,8 +166,10 @@ __device__ __forceinline__ void gemv_round(const float4* const (&wrow)[TE], cons
 // Both phases are bound by memory latency at small T, so a lane issues the
 // loads of a whole pass (up to kRegChunks chunks of x and g, DEPTH chunks of
 // router weights per expert) before it uses any of them.  DEEP = false halves
-// both depths, for callers that need the registers for other work.
-template <int TT, int TE, bool DEEP = true>
+// both depths, for callers that need the registers for other work.  PAIRED
+// (TT even): the logits loop takes tokens two at a time (gemv_round_paired),
+// one chunk of router weights per round.
+template <int TT, int TE, bool DEEP = true, bool PAIRED = false>
 __device__ __forceinline__ void norm_router_tile(const uint16_t* __restrict__ x, const uint16_t* __restrict__ g,
                                                  const float* __restrict__ w_router, const float* __restrict__ bias,
                                                  int T, int H, int E, float eps, int t0, int e0, int experts_per_cta,
@@ -210,6 +256,38 @@ __device__ __forceinline__ void norm_router_tile(const uint16_t* __restrict__ x,
   // DEPTH chunks of router weights in flight per lane (32 B each per expert),
   // consumed in chunk order, so every accumulator keeps the canonical sequence
   constexpr int DEPTH = ((TE >= 4) ? 2 : (TE == 2 ? 8 : 16)) / (DEEP || TE >= 4 ? 1 : 2);
+  if constexpr (PAIRED) {
+    static_assert(TT % 2 == 0, "tokens are paired");
+    for (int eg = e0 + warp * TE; eg < e_end; eg += kRouteWarps * TE) {
+      float2 acc[TT / 2][TE];
+#pragma unroll
+      for (int p = 0; p < TT / 2; ++p)
+#pragma unroll
+        for (int b = 0; b < TE; ++b) acc[p][b] = make_float2(0.0f, 0.0f);
+      const float4* wrow[TE];
+#pragma unroll
+      for (int b = 0; b < TE; ++b)
+        wrow[b] = reinterpret_cast<const float4*>(w_router + static_cast<size_t>(min(eg + b, E - 1)) * H);
+      for (int c0 = lane; c0 < nch; c0 += 32) gemv_round_paired<TT, TE, 1, false>(wrow, h_s, nch, c0, acc);
+#pragma unroll
+      for (int p = 0; p < TT / 2; ++p)
+#pragma unroll
+        for (int b = 0; b < TE; ++b) {
+          float v0 = warp_butterfly_sum(acc[p][b].x);
+          float v1 = warp_butterfly_sum(acc[p][b].y);
+          const int e = eg + b;
+          if (lane == 0 && e < e_end) {
+            if (bias) {
+              v0 = __fadd_rn(v0, bias[e]);
+              v1 = __fadd_rn(v1, bias[e]);
+            }
+            if (2 * p < ntok) logits[static_cast<size_t>(t0 + 2 * p) * E + e] = v0;
+            if (2 * p + 1 < ntok) logits[static_cast<size_t>(t0 + 2 * p + 1) * E + e] = v1;
+          }
+        }
+    }
+    return;
+  }
   for (int eg = e0 + warp * TE; eg < e_end; eg += kRouteWarps * TE) {
     float acc[TT][TE];
 #pragma unroll
