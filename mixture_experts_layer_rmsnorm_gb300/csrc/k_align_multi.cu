@@ -62,19 +62,30 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// One CTA of 1024 threads, thread e = expert e (E <= 1024).
+// One CTA of 1024 threads, thread e = expert e (E <= 1024).  The per-block
+// counts are read once, by all threads together, into shared memory when they
+// fit (kScanStageInts); each thread then walks its expert's column there
+// instead of making nblk dependent trips to L2.
+constexpr int kScanStageInts = 11264;  // 44 KB: with the static scan buffer, under the 48 KB default
 __global__ void __launch_bounds__(1024)
     align_scan_kernel(const int32_t* __restrict__ blk_counts, int nblk, int E, int pad, int bn1, int tiles1, int bn2,
                       int tiles2, int N, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                       int32_t* __restrict__ unit_off1, int32_t* __restrict__ unit_off2,
                       int32_t* __restrict__ blk_base, int32_t* __restrict__ sorted_ids) {
   __shared__ int scan_tmp[3 * 33];
+  extern __shared__ int staged[];  // [nblk][E] when nblk * E <= kScanStageInts
   pdl_wait();
   pdl_launch_dependents();
+  const int n_counts = nblk * E;
+  const bool stage = n_counts <= kScanStageInts;
+  if (stage)
+    for (int i = threadIdx.x; i < n_counts; i += 1024) staged[i] = __ldcg(blk_counts + i);
+  __syncthreads();
+  const int32_t* bc = stage ? staged : blk_counts;
   const int e = threadIdx.x;
   int c = 0;
   if (e < E)
-    for (int b = 0; b < nblk; ++b) c += blk_counts[static_cast<size_t>(b) * E + e];
+    for (int b = 0; b < nblk; ++b) c += bc[static_cast<size_t>(b) * E + e];
   const int p = (c + pad - 1) / pad * pad;
   const int u1 = (bn1 > 0) ? (p + bn1 - 1) / bn1 * tiles1 : 0;
   const int u2 = (bn2 > 0) ? (p + bn2 - 1) / bn2 * tiles2 : 0;
@@ -91,7 +102,7 @@ __global__ void __launch_bounds__(1024)
     int run = off;
     for (int b = 0; b < nblk; ++b) {
       blk_base[static_cast<size_t>(b) * E + e] = run;
-      run += blk_counts[static_cast<size_t>(b) * E + e];
+      run += bc[static_cast<size_t>(b) * E + e];
     }
     for (int q = off + c; q < off + p; ++q) sorted_ids[q] = N;  // padding rows
   }
@@ -186,8 +197,10 @@ cudaError_t launch_align_multi(const float* logits, int T, int k, int renorm, in
     st = cudaEventRecord(static_cast<cudaEvent_t>(count_done_event), stream);
     if (st != cudaSuccess) return st;
   }
-  st = launch_pdl(align_scan_kernel, dim3(1), dim3(1024), 0, stream, blk_counts, nblk, E, pad, bn1, tiles1, bn2, tiles2,
-                  T * k, counts, offsets, unit_off1, unit_off2, blk_base, sorted_ids);
+  const size_t smem_scan =
+      static_cast<size_t>(nblk) * E <= kScanStageInts ? static_cast<size_t>(nblk) * E * sizeof(int) : 0;
+  st = launch_pdl(align_scan_kernel, dim3(1), dim3(1024), smem_scan, stream, blk_counts, nblk, E, pad, bn1, tiles1,
+                  bn2, tiles2, T * k, counts, offsets, unit_off1, unit_off2, blk_base, sorted_ids);
   if (st != cudaSuccess) return st;
   const size_t smem_scatter = static_cast<size_t>(1 + kWarps) * E * sizeof(int);
   return launch_pdl(align_scatter_kernel, grid, dim3(kThreads), smem_scatter, stream, topk_ids, T, k, E, blk_base,

@@ -43,6 +43,9 @@ CASES = [
     # tiles and of 64-element K blocks in the down GEMM
     ("I192_decode", 40, 256, 192, 8, 2, True, None, 15),
     ("I320_prefill_odd_tiles", 512, 256, 320, 8, 2, True, None, 16),
+    # 64 align blocks x 256 experts: more per-block counts than the scan
+    # stages in shared memory (it reads them from global memory)
+    ("align_counts_unstaged", 2048, 128, 128, 256, 2, True, None, 17),
 ]
 
 
