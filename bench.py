@@ -483,7 +483,9 @@ def run_ours(args, wl, world, rank, local):
                 binding.MOE_CALL_FORWARD_FUSED_MLP if fm else binding.MOE_CALL_FORWARD)
         return binding.kernels_per_call(T, H, wl["I"], wl["E"], wl["k"], call)
 
-    def one_step(step_idx=None, per_kernel=False):
+    graphs = {}  # batch size -> CUDA graph of one layer call (the timed calls replay it)
+
+    def one_step(step_idx=None, per_kernel=False, eager_ev=None):
         for T in Ts:
             flush_l2(step_idx or 0)
             if step_idx is None:
@@ -491,9 +493,12 @@ def run_ours(args, wl, world, rank, local):
             elif per_kernel:
                 fwd(xs[T], ys[T], events=[e.cuda_event for e in kern_ev[T][step_idx]])
             else:
-                a, b = call_ev[T][step_idx]
+                a, b = (eager_ev or call_ev)[T][step_idx]
                 a.record(stream)
-                fwd(xs[T], ys[T])
+                if T in graphs and eager_ev is None:
+                    graphs[T].replay()
+                else:
+                    fwd(xs[T], ys[T])
                 b.record(stream)
 
     for _ in range(args.warmup):
@@ -511,6 +516,22 @@ def run_ours(args, wl, world, rank, local):
         ids = layer.view_tensor(T, "topk_ids", torch.int32, (T, wl["k"])).cpu().numpy()
         touched[T] = accounting.n_touched(ids, wl["E"])
     torch.cuda.synchronize()
+    # A serving loop captures the decode step once and replays it: each
+    # batch's layer call, captured into a CUDA graph (same kernels, launch
+    # attributes and arguments; the inputs are read from xs[T] at replay)
+    if not args.eager:
+        for T in Ts:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fwd(xs[T], ys[T])
+            graphs[T] = g
+        for T in Ts:
+            graphs[T].replay()
+        torch.cuda.synchronize()
+        for T in Ts:
+            st, det = layer.device_status(T)
+            if st != binding.MOE_OK:
+                raise binding.MoeError(st, f"device status after a graph replay (T={T}, detail {det})")
 
     gpu_index = local
     cvd = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -534,6 +555,12 @@ def run_ours(args, wl, world, rank, local):
         one_step(s, per_kernel=True)
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    # the plain calls made directly (no graph), for comparison
+    eager_ev = {T: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(args.steps)] for T in Ts}
+    for s in range(args.steps):
+        one_step(s, eager_ev=eager_ev)
+    torch.cuda.synchronize()
     # extra, not the headline: the same calls with the L2 left warm (no flush),
     # each batch called `reps` times back to back
     warm = {}
@@ -551,6 +578,7 @@ def run_ours(args, wl, world, rank, local):
     per_T = {}
     kern_ms = {n: 0.0 for n in binding.KERNEL_NAMES}
     total_ms = 0.0
+    eager_ms = 0.0
     for T in Ts:
         calls = [a.elapsed_time(b) for a, b in call_ev[T]]
         kt = {n: [] for n in binding.KERNEL_NAMES}
@@ -562,7 +590,10 @@ def run_ours(args, wl, world, rank, local):
         total_ms += sum(calls)
         lb = accounting.layer_bytes(T, H, wl["I"], wl["E"], wl["k"], touched[T], mx)
         us = statistics.median(calls) * 1e3
+        calls_eager = [a.elapsed_time(b) for a, b in eager_ev[T]]
+        eager_ms += sum(calls_eager)
         per_T[str(T)] = {"us_median": round(us, 2), "us_mean": round(sum(calls) / len(calls) * 1e3, 2),
+                         "us_median_eager": round(statistics.median(calls_eager) * 1e3, 2),
                          "tokens_per_s": round(T / (us * 1e-6), 1), "experts_touched": touched[T],
                          "weight_GB": round(lb["weights"] / 1e9, 4),
                          "weight_GBps": round(lb["weights"] / (us * 1e-6) / 1e9, 1),
@@ -574,6 +605,7 @@ def run_ours(args, wl, world, rank, local):
     tokens_per_step = sum(Ts)
     ms_max = reduce_max(ms_per_step, world)
     value = world * tokens_per_step / (ms_max * 1e-3)
+    eager_ms_max = reduce_max(eager_ms / args.steps, world)
 
     # dominant kernel and its roofline
     peaks, peak_kind = load_peaks()
@@ -665,9 +697,17 @@ def run_ours(args, wl, world, rank, local):
                    "expert_gemms": ("moe_forward_fused_mlp: both in one launch" if fm else "two launches"),
                    "l2": "flushed before every layer call (256 MB write, then a 256 MB read of another buffer so "
                          "no dirty lines remain); flush outside the timed CUDA-event intervals",
-                   "timing": "CUDA events on the launch stream around each plain moe_forward call; kernel times from "
-                             "a second pass of the same calls through moe_forward_events (with 4 kernels per call, "
-                             "'norm_router' is the single-launch front end: norm, router, top-k, align and gather)",
+                   "timing": (("CUDA events on the launch stream around the replay of a CUDA graph holding one "
+                               "layer call per batch size (captured once with stream capture: the same kernels, "
+                               "launch attributes and arguments as the plain call, inputs read from the device "
+                               "buffer at replay); " if graphs else
+                               "CUDA events on the launch stream around each plain layer call; ") +
+                              "per_T.us_median_eager and `eager` time the plain calls made directly; kernel times "
+                              "from a pass of the same calls through the events entry point (with 4 kernels per "
+                              "call, 'norm_router' is the single-launch front end: norm, router, top-k, align and "
+                              "gather)"),
+                   "eager": {"value": round(world * tokens_per_step / (eager_ms_max * 1e-3), 1),
+                             "ms_per_step": round(eager_ms_max, 4)},
                    "parallelism": f"replicas x{world} (no cross-GPU data path)", "per_T": per_T,
                    "kernel_ms_per_step": {n: round(v / args.steps, 4) for n, v in kern_ms.items()},
                    "wall_s_timed_region": round(t_wall, 3), "setup_s": round(setup_s, 1)},
@@ -785,6 +825,8 @@ def main():
                     help="CPU oracle sample: at most this many tokens of each batch per step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum timed CPU-oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the plain layer calls made directly, not their replay from a CUDA graph")
     ap.add_argument("--no-prefill", action="store_true",
                     help="decode workload: skip the prefill (T=4096) object of the JSON line")
     ap.add_argument("--nvfp4", action="store_true",

@@ -35,6 +35,14 @@
  *   - Calls are asynchronous on `stream` (NULL = the legacy default
  *     stream).  Outputs are valid once the stream has reached the end of
  *     the call.  Inputs are never modified.
+ *   - A call can be captured into a CUDA graph (stream capture on `stream`)
+ *     and replayed: it makes no host synchronisation and no allocation, and
+ *     it reads the pointed-to data when the kernels run.  The shape, the
+ *     pointers and the tensor maps built from them are fixed at capture;
+ *     new inputs go into the same buffers between replays.  Make one call
+ *     outside capture first on each device (it sets per-device kernel
+ *     attributes, which are not stream work).  A replay gives the same bits
+ *     as the direct call.
  *   - Argument and shape errors are reported synchronously, before anything
  *     is enqueued.  A failed launch returns MOE_ERR_CUDA.  Errors found on
  *     the device (a routing index out of range, a bounded wait that ran out)
