@@ -315,7 +315,10 @@ typedef struct {
   void* offsets;      /* [E + 1] int32 padded row offsets (16-row padding) */
   void* sorted_ids;   /* [P_max] int32 */
   void* slot_of;      /* [T * top_k] int32 row of each routed token */
-  void* xg;           /* [P_max, H] bf16 gathered, padded expert inputs */
+  void* xg;           /* [P_max, H] bf16 gathered, padded expert inputs; written
+                       * only where a gather kernel runs: moe_forward's decode
+                       * tile plan (T * top_k <= 16 E) reads the rows of h in
+                       * the gate/up GEMM instead (unless the combine is fused) */
   void* act;          /* [P_max, I] bf16 SwiGLU activations */
   void* out_rows;     /* [P_max, H] bf16 per-row expert outputs */
   int64_t P_max;      /* T*top_k + E*15: the most padded rows any routing can need */

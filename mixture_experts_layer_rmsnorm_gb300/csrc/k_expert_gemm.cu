@@ -87,7 +87,7 @@ constexpr int kABytes = kWeightBoxRows * kBlockK * 2;  // 16 KB weight tile per 
 constexpr int kTokRowBytes = kBlockK * 2;              // 128 B per token row per stage
 
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
-          bool A4 = false, bool NV = false, bool FUSED = false>
+          bool A4 = false, bool NV = false, bool FUSED = false, bool GATHER = false>
 struct GemmCfg {
   // a CTA pair splits the unit's tokens: each CTA holds half of the B tile
   static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * kTokRowBytes;
@@ -131,7 +131,11 @@ struct GemmCfg {
   // pair keeps tcgen05.cp: its 8 epilogue warps and 168 registers leave no
   // room for 4 more warps)
   static constexpr int kScaleWarps = (MX && !PAIR && kChunks > 1) ? 4 : 0;
-  static constexpr int kThreads = 64 + 32 * (kEpiWarps + kScaleWarps);
+  // GATHER (bf16 gate/up GEMM, decode tile plan): two row warps copy the
+  // stages' token rows from h (rows picked by sorted_ids) into the B tile
+  // with cp.async, in place of a gather kernel and the token TMA
+  static constexpr int kGatherWarps = GATHER ? 2 : 0;
+  static constexpr int kThreads = 64 + 32 * (kEpiWarps + kScaleWarps + kGatherWarps);
   // TMEM columns of one stage's scales: weight scales at +0 (4 columns), token
   // scales at +16 (4 columns per 128 tokens); slots of 32 keep both addresses
   // 16-column aligned
@@ -154,6 +158,8 @@ struct GemmCfg {
   static_assert(!NV || (A4 && !PAIR), "NVFP4: both operands E2M1, one-CTA units (TMEM columns of the scales)");
   static_assert(!FUSED || (SWIGLU && !PAIR && !MX && kEpiWarps == 4),
                 "the fused gate/up -> down kernel: bf16, one-CTA units, four epilogue warps");
+  static_assert(!GATHER || (SWIGLU && !PAIR && !MX && !FUSED && BN % 4 == 0),
+                "row warps: the bf16 gate/up GEMM on one-CTA units");
   static_assert(!MX || (4 * kChunks <= 16 && 16 + 4 * kChunks * kSfTokTiles <= kSfCols),
                 "scale columns of a stage: weight tiles from +0, token tiles from +16");
   static_assert(kStageBytes % 1024 == 0, "stage tiles must stay 1024-byte aligned");
@@ -364,12 +370,12 @@ __device__ __noinline__ bool combine_unit(const ExpertGemmArgs& a, const Unit& u
 // the last stage; its own instance, so that whole-stage shapes keep
 // compile-time scale sizes and MMA counts.
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
-          bool A4 = false, bool NV = false, bool FUSED = false, bool KTAIL = false>
-__global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED>::kThreads, 1)
+          bool A4 = false, bool NV = false, bool FUSED = false, bool KTAIL = false, bool GATHER = false>
+__global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED, GATHER>::kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_sw, const __grid_constant__ CUtensorMap tm_sx,
                        const __grid_constant__ ExpertGemmArgs args, const __grid_constant__ ExpertGemmArgs args2) {
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED, GATHER>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
@@ -414,7 +420,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], GATHER ? 2 : 1);  // the producer's arrival (with the TMA bytes) [+ the row warp's]
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -535,6 +541,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
       };
       // chunk: the unit's token chunk (MXFP8 token scales are stored per chunk)
       auto load_tokens = [&](int st, int kb, int tok0, int rows, int chunk) {
+        if (GATHER) return;  // the row warps copy them
         uint8_t* sb = smem + st * C::kStageBytes + kABytes;
         const int row0 = tok_from_h ? 0 : tok0;  // one token: its row of h, then zeros
         for (int r = 0; r < rows; r += TOKBOX)
@@ -617,7 +624,7 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
         const bool reused = t_off[un.e + 1] - t_off[un.e] > BN;
         const uint64_t pol_w = reused ? pol_keep : pol_stream;
         // per CTA (both of a pair); scale bytes of a full stage: C::kSfBytes
-        const uint32_t bytes_base = C::kWTxBytes + tok_rows * kTokRowBytes;
+        const uint32_t bytes_base = C::kWTxBytes + (GATHER ? 0 : tok_rows * kTokRowBytes);
         const int chunk = MX ? t_unit[un.e] / pa0.tiles + (un.tok0 - t_off[un.e]) / BN : 0;
         // fused kernel, down GEMM: the token chunk (expert, rows [tok0, tok0 + BN))
         // whose activation rows this unit reads, numbered over all experts
@@ -889,6 +896,94 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
       int dummy = 0;
       mbar_wait(done, 0, kWaitTimeoutNs, &dummy);
     }
+  } else if (GATHER && warp >= 2 + C::kEpiWarps) {
+    if constexpr (GATHER) {
+      // ---------------- row warps: a stage's token rows of the unit, copied
+      // from h into the B tile in the layout a 128-byte swizzled TMA box gives
+      // (row r at r * 128, its 16-byte piece p at p ^ (r mod 8)).  The stages
+      // go round-robin to the row warps (stage iteration i to warp i mod 2);
+      // in a warp, lane takes piece (lane mod 8) of rows lane / 8 + 4 j.
+      // Padding rows (sorted_ids past the routed rows) are left as they are:
+      // they feed MMA columns whose outputs are dropped.  A warp signals a
+      // stage once it has issued its next one: cp.async.wait_group, a proxy
+      // fence (generic writes -> the MMAs' async-proxy reads), then one
+      // arrival on the stage's full barrier.
+      constexpr int kPasses = BN / 4;
+      const int gw = warp - (2 + C::kEpiWarps);
+      const int rsub = lane >> 3, piece = lane & 7;
+      pdl_wait();  // sorted_ids come from the previous kernel
+      const uint64_t pol_rows = policy_evict_last();  // each row is read by every weight tile of its expert
+      const int32_t* sorted = args.sorted_ids;
+      const char* hsrc = reinterpret_cast<const char*>(args.h_rows) + piece * 16;
+      const size_t row_bytes = static_cast<size_t>(args.K) * 2;
+      auto signal = [&](int st) {
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[st]);
+      };
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int pending = -1;  // this warp's last stage copied, not yet signalled
+      int64_t iter = 0;  // stage iterations of the CTA so far
+      Range rg(total_units, kblocks, worker, ctas, args.stream_k != 0);
+      int u, kb0, kb1;
+      while (ok && rg.next(u, kb0, kb1)) {
+        const int first_mine = static_cast<int>((C::kGatherWarps - iter % C::kGatherWarps + gw) % C::kGatherWarps);
+        iter += kb1 - kb0;
+        if (kb0 + first_mine >= kb1) {  // none of this segment's stages is this warp's
+          for (int kb = kb0; kb < kb1; ++kb)
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          continue;
+        }
+        const Unit un = decode_unit(u, t_unit, t_off, args.E, pa0.tiles, BN);
+        int src[kPasses];  // h row of each of this lane's rows, or -1
+#pragma unroll
+        for (int j = 0; j < kPasses; ++j) {
+          const int r = rsub + 4 * j;
+          int t = -1;
+          if (r < un.n) {
+            const int id = __ldg(sorted + un.tok0 + r);
+            if (id >= 0 && id < args.n_routed) t = id / args.top_k;
+          }
+          src[j] = t;
+        }
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if ((kb - kb0) % C::kGatherWarps == first_mine) {
+            const bool got = mbar_wait(&empty[stage], phase ^ 1u, kWaitTimeoutNs, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, got)) {
+              ok = false;
+              break;
+            }
+            const uint32_t sb = smem_u32(smem + stage * C::kStageBytes + kABytes);
+            const char* col = hsrc + static_cast<size_t>(kb) * (C::kBoxX * 2);
+#pragma unroll
+            for (int j = 0; j < kPasses; ++j) {
+              const int r = rsub + 4 * j;
+              if (src[j] >= 0)
+                cp_async_16(sb + static_cast<uint32_t>(r * kTokRowBytes + ((piece ^ (r & 7)) << 4)),
+                            col + static_cast<size_t>(src[j]) * row_bytes, pol_rows);
+            }
+            cp_async_commit();
+            if (pending >= 0) {
+              cp_async_wait<1>();
+              signal(pending);
+            }
+            pending = stage;
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      cp_async_wait<0>();
+      if (pending >= 0) signal(pending);
+      if (!ok && lane == 0) raise_timeout(args.err, abort_flag, kern, kWaitRingSlotFree);
+    }
   } else if (warp >= 2 + C::kEpiWarps) {
     // ---------------- scale warps (block-scaled one-CTA units): per stage, the
     // 16 bytes of each scale tile's row (lane & 31) into this warp's TMEM lane
@@ -1130,13 +1225,13 @@ __global__ void __launch_bounds__(GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, 
 // tsw / tsx: the scale maps of MXFP8 pairs, or the fused kernel's W2 and
 // activation maps; a2: the fused kernel's down GEMM.
 template <bool SWIGLU, int BN, int STAGES, int TOKBOX, bool PAIR, bool MX = false, bool W4 = false,
-          bool A4 = false, bool NV = false, bool FUSED = false, bool KTAIL = false>
+          bool A4 = false, bool NV = false, bool FUSED = false, bool KTAIL = false, bool GATHER = false>
 cudaError_t launch_expert_gemm(const CUtensorMap& tw, const CUtensorMap& tx, const ExpertGemmArgs& a, int num_sms,
                                cudaStream_t stream, const CUtensorMap* tsw = nullptr,
                                const CUtensorMap* tsx = nullptr, const ExpertGemmArgs* a2 = nullptr) {
   static const CUtensorMap kNoMap = {};  // unused map arguments
-  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED>;
-  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED, KTAIL>;
+  using C = GemmCfg<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED, GATHER>;
+  auto kernel = expert_gemm_kernel<SWIGLU, BN, STAGES, TOKBOX, PAIR, MX, W4, A4, NV, FUSED, KTAIL, GATHER>;
   static PerDevice config;  // the smem attribute, and the CTA pairs that fit on the device at once
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::kThreads);
@@ -1313,6 +1408,9 @@ cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm
                                 GemmPlan plan, int num_sms, cudaStream_t stream) {
   switch (plan) {
     case GemmPlan::kSmall:
+      if (a.h_rows)  // token rows fetched from h by the row warps
+        return launch_expert_gemm<true, kGateUpBn[0], kGateUpStages[0], kTokBox[0], false, false, false, false, false,
+                                  false, false, true>(tm_w13, tm_x, a, num_sms, stream);
       return launch_expert_gemm<true, kGateUpBn[0], kGateUpStages[0], kTokBox[0], false>(tm_w13, tm_x, a, num_sms,
                                                                                           stream);
     default:

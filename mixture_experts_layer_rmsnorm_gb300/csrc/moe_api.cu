@@ -320,11 +320,14 @@ moe_status moe_kernels_per_call_of(const moe_shape* shape, int32_t call, int32_t
   const int front = 1 + (moe::align_fuses_topk(s.T, s.E) ? 1 : 3) + 1;
   if (call == MOE_CALL_FORWARD_FUSED_MLP && !moe::fused_mlp_fits(moe::choose_plan(s.T, s.top_k, s.E)))
     return MOE_ERR_UNSUPPORTED;
-  const int no_gather = moe::tokens_from_h(s.T, false) ? 1 : 0;  // one token: no gather
+  // no gather for one token, nor (moe_forward) when the decode-plan gate/up
+  // GEMM reads the rows of h itself
+  const int one_token = moe::tokens_from_h(s.T, false) ? 1 : 0;
+  const int rows_from_h = moe::gate_up_gathers_rows(s.T, moe::choose_plan(s.T, s.top_k, s.E), false) ? 1 : 0;
   if (call == MOE_CALL_FORWARD)
-    *count = front + 3 - no_gather;
+    *count = front + 3 - one_token - rows_from_h;
   else if (call == MOE_CALL_FORWARD_FUSED_MLP)
-    *count = front + 2 - no_gather;  // both GEMMs in one launch
+    *count = front + 2 - one_token;  // both GEMMs in one launch
   else if (call == MOE_CALL_FORWARD_FUSED_FRONT)
     *count = 1 + 3;
   else if (call == MOE_CALL_FORWARD_MX || call == MOE_CALL_FORWARD_MXFP4 || call == MOE_CALL_FORWARD_MXFP4A4 ||
@@ -410,6 +413,9 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   // rows), so the gate/up GEMM reads its token tiles straight from h, rows
   // past T reading as zeros, and no gather runs.
   const bool tokens_from_h = moe::tokens_from_h(s.T, fused_combine);
+  // More tokens on the decode tile plan: the gate/up GEMM copies each unit's
+  // token rows from h itself (its row warps read sorted_ids); no gather runs.
+  const bool rows_from_h = !single_launch_front && !fused_mlp && moe::gate_up_gathers_rows(s.T, plan, fused_combine);
   CUtensorMap tm_w13, tm_xg, tm_w2, tm_act;
   if (!make_map_gate_up(&tm_w13, w13, s.H, s.I, s.E) ||
       !(tokens_from_h ? make_map(&tm_xg, at<void>(workspace, L.h), s.H, s.T, moe::gemm_tok_box_rows(plan))
@@ -490,7 +496,7 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
                                    static_cast<int>(L.n_flags), cs, events ? events[2] : nullptr);
     }
     if (ce != cudaSuccess || !mark(3)) return MOE_ERR_CUDA;
-    if (!tokens_from_h &&
+    if (!tokens_from_h && !rows_from_h &&
         moe::launch_gather(at<uint16_t>(workspace, L.h), at<int32_t>(workspace, L.sorted),
                            at<int32_t>(workspace, L.offsets), s.E, N, s.top_k, s.H, L.P_max,
                            at<uint16_t>(workspace, L.xg), at<int32_t>(workspace, L.ccnt),
@@ -513,8 +519,14 @@ moe_status forward_impl(const moe_shape* shape, const moe_bf16* x, const moe_bf1
   a1.flags = at<int32_t>(workspace, L.flags);
   a1.stream_k = plan == GemmPlan::kSmall;
   a1.pair = moe::gemm_uses_pairs(plan, tiles1);
-  a1.tables_from_parent = front || tokens_from_h;  // the align is then the GEMM's parent
+  a1.tables_from_parent = front || tokens_from_h || rows_from_h;  // the align is then the GEMM's parent
   a1.tokens_from_h = tokens_from_h;
+  if (rows_from_h) {
+    a1.h_rows = at<uint16_t>(workspace, L.h);
+    a1.sorted_ids = at<int32_t>(workspace, L.sorted);
+    a1.top_k = s.top_k;
+    a1.n_routed = N;
+  }
   a1.ready = at<int32_t>(workspace, L.flags) + kGemmFlagInts;
 
   moe::ExpertGemmArgs a2{};

@@ -117,6 +117,9 @@ struct ExpertGemmArgs {
                             // at h row 0 (rows past T are read as zeros)
   int32_t* ready;           // fused gate/up -> down kernel: per token chunk, the gate/up epilogue warps that
                             // have stored their activation rows of it (zero on entry)
+  const uint16_t* h_rows;   // gate/up GEMM of the decode tile plan: non-null = no gathered copy; the kernel's
+                            // row warps fetch each unit's token rows from h [T, K] through sorted_ids (then
+                            // also set: sorted_ids, top_k, n_routed)
   const uint8_t* w_scales;  // MXFP8 GEMMs: weight scales (512-byte tiles per 128 rows x 128 of K)
   const uint8_t* x_scales;  // MXFP8 GEMMs: token scales, one 512-byte tile per token chunk and 128 of K
   const float* w_gscale;    // NVFP4 GEMMs: fp32 tensor scale per expert matrix [E]
@@ -153,6 +156,12 @@ inline bool fused_mlp_fits(GemmPlan plan) { return plan == GemmPlan::kSmall; }
 // (one token: no gather), given the entry point's options (the fused combine
 // keeps the gather, which zeroes its counters).
 inline bool tokens_from_h(int T, bool fused_combine) { return T == 1 && !fused_combine; }
+// Above one token on the decode tile plan, the gate/up GEMM copies its token
+// rows from h itself (no gather kernel) unless a fused combine needs the
+// gather's counter reset.
+inline bool gate_up_gathers_rows(int T, GemmPlan plan, bool fused_combine) {
+  return T > 1 && plan == GemmPlan::kSmall && !fused_combine;
+}
 
 // Encodes nothing itself: the tensor maps are built by the caller.
 cudaError_t launch_gemm_gate_up(const CUtensorMap& tm_w13, const CUtensorMap& tm_x, const ExpertGemmArgs& a,

@@ -132,6 +132,28 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy writes of its CTA's shared memory (e.g.
+// by cp.async, once complete) with later async-proxy reads of them (tcgen05
+// MMAs, TMA), here or, through a release/acquire, in another thread.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16 bytes global -> shared, asynchronous, cached in L2 only (cp.async.cg);
+// both addresses 16-byte aligned; `policy` an L2 cache policy (createpolicy).
+// Completion: cp_async_commit groups the copies this thread has issued,
+// cp_async_wait<N> waits until at most the N most recent groups are still in
+// flight.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // atomic add with release semantics at GPU scope (no return value)
 __device__ __forceinline__ void red_release_add(int32_t* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
