@@ -55,7 +55,10 @@ WORKLOADS = {
                  label="tiny T=4, H=128, I=256, E=8, top_k=2, bf16"),
     # small cases of the same per-unit shapes, for ncu captures (inputs > L2, < 2 GB on the device)
     "decode_ncu": dict(H=4096, I=4096, E=16, k=8, Ts=[64], seed=0, zipf=None,
-                       label="ncu case: T=64, H=I=4096, E=16, top_k=8 (decode tiles, 32 tokens/expert)"),
+                       label="ncu case: T=64, H=I=4096, E=16, top_k=8 (32 tokens/expert)"),
+    "decode_rows_ncu": dict(H=4096, I=4096, E=8, k=8, Ts=[16], seed=0, zipf=None,
+                            label="ncu case: T=16, H=I=4096, E=8, top_k=8 (decode tile plan, 16 rows per expert: "
+                                  "the gate/up GEMM with row warps)"),
     "router_ncu": dict(H=4096, I=256, E=64, k=8, Ts=[1, 64], seed=0, zipf=None,
                        label="ncu case: router of the decode layer (H=4096, E=64) with small experts (I=256)"),
     "router_prefill_ncu": dict(H=4096, I=256, E=64, k=8, Ts=[4096], seed=0, zipf=None,
