@@ -43,6 +43,10 @@ CASES = [
     # tiles and of 64-element K blocks in the down GEMM
     ("I192_decode", 40, 256, 192, 8, 2, True, None, 15),
     ("I320_prefill_odd_tiles", 512, 256, 320, 8, 2, True, None, 16),
+    # the decode tile plan (T * k <= 16 E) under skewed routing: hot experts
+    # with 45-64 rows take two or three 32-row chunks (the row warps' chunk
+    # offsets and padded tails)
+    ("decode_plan_hot_experts", 64, 256, 256, 16, 4, True, 1.2, 20),
     # 64 align blocks x 256 experts: more per-block counts than the scan
     # stages in shared memory (it reads them from global memory)
     ("align_counts_unstaged", 2048, 128, 128, 256, 2, True, None, 17),
